@@ -1,0 +1,102 @@
+// Internal host-side launch interface between the C ABI (api.cu) and the
+// kernel translation units.  Not installed; the public contract is gdr.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdr {
+
+struct RecurrentArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g;
+    const void* beta;
+    void* pool;
+    const int32_t* state_indices;
+    const int32_t* cu_seqlens;
+    void* o;
+    void* ibuf;
+    int N, Hk, Hv, K, V, steps, num_slots;
+    int64_t T;
+    int dtype, pool_dtype, flags;
+    float scale;
+};
+
+// Enqueue the recurrent decode / verify kernel.  Returns a cudaError_t.
+cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t stream);
+
+struct ChunkArgs {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g;
+    const float* gk;
+    const void* beta;
+    const float* initial_state;
+    const int32_t* cu_seqlens;
+    void* o;
+    float* final_state;
+    int N;
+    int64_t T;
+    int Hk, Hv, K, V, dtype, flags;
+    float scale;
+    void* workspace;
+    size_t ws_bytes;
+};
+
+// Workspace layout of the chunked prefill (byte offsets, 256-aligned).
+struct ChunkWorkspace {
+    int64_t max_chunks;
+    size_t off_meta;      // int: [0] = chunk count
+    size_t off_offsets;   // int [N+1]: first global chunk of each sequence
+    size_t off_table;     // int4 [max_chunks]: (seq, start token, length, -)
+    size_t off_qn, off_kn;  // normalised q / k (GDR_QK_L2NORM), input dtype
+    size_t off_w, off_u, off_kd, off_qd;   // fp32 [T, Hv, K|V]
+    size_t off_p;         // fp32 [max_chunks, Hv, 64, 64]
+    size_t off_dl;        // fp32 [max_chunks, Hv, K]
+    size_t off_h;         // fp32 [max_chunks, Hv, V, K]
+    size_t off_vn;        // fp32 [T, Hv, V]
+    size_t total;
+};
+
+ChunkWorkspace chunk_workspace_layout(int N, int64_t T, int Hk, int Hv, int K, int V, int dtype,
+                                      int flags);
+
+cudaError_t launch_chunk(const ChunkArgs& a, cudaStream_t stream);
+
+struct GatingArgs {
+    const void* a;
+    const float* dt_bias;
+    const float* A_log;
+    const void* b;
+    float* g;
+    void* beta;
+    int64_t T;
+    int Hv, dtype, flags;
+};
+
+cudaError_t launch_gating(const GatingArgs& a, cudaStream_t stream);
+
+// Device error word (set by bounded device waits that give up).
+unsigned int* device_error_word();
+
+// Scoped per-kernel timing (active only after gdr_profile_enable(1)): records
+// an event on `s` at construction and at destruction, so declare it right
+// before a launch inside its own block.
+class KernelTimer {
+  public:
+    KernelTimer(const char* name, cudaStream_t s);
+    ~KernelTimer();
+    KernelTimer(const KernelTimer&) = delete;
+    KernelTimer& operator=(const KernelTimer&) = delete;
+
+  private:
+    const char* name_;
+    cudaStream_t stream_;
+    void* a_;
+};
+
+}  // namespace gdr

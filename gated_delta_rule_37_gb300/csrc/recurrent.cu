@@ -1,0 +1,171 @@
+// Recurrent decode / multi-step verify over a slot-indexed state pool.
+//
+// Design (FlashQLA PR #1, core decode-kernel and paged-verify commits, read
+// for what they compute; the H100 tiling is not reused):
+//   * one CTA per (sequence b, value-head h, block of BV value rows);
+//   * the fp32 state rows live in registers for the whole sequence: a warp
+//     owns 16 consecutive rows, lane l holds K/32 consecutive key channels of
+//     each row, so a row is one coalesced 512-byte (fp32) read;
+//   * per token the two state-vector products S k and S q are reduced for all
+//     16 rows at once with a halving butterfly (31 shuffles instead of 160);
+//   * o_t = scale * S_t q_t is formed as scale * (a S_{t-1} q + n_t (k . q)),
+//     which is S_t q_t with the rank-1 term expanded;
+//   * the state stays V-major end to end (pool, intermediate states), so every
+//     store is a coalesced row write (the same page measured a K-major
+//     transpose store of the final state at ~0.4 TB/s).
+// No tensor cores: every step is a matrix-vector product (M = 1).
+#include "common.cuh"
+#include "launch.h"
+
+namespace gdr {
+namespace {
+
+constexpr int kRowsPerWarp = 16;
+
+struct RecParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g;
+    const void* beta;
+    void* pool;
+    const int32_t* idx;
+    const int32_t* cu;
+    void* o;
+    void* ibuf;
+    int Hk, Hv, steps, flags, num_slots;
+    int64_t T;
+    float scale;
+};
+
+template <typename InT, typename PoolT, int K, int BV>
+__global__ void __launch_bounds__(BV / kRowsPerWarp * 32)
+recurrent_kernel(RecParams p) {
+    constexpr int KPT = K / 32;  // key channels per lane
+    const int b = blockIdx.x;
+    const int h = blockIdx.y;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int slot = p.idx[b];
+    if (slot < 0 || slot >= p.num_slots) return;  // padding (or out of range): untouched
+    // token range clamped to [0, T) so a malformed cu_seqlens cannot index out of bounds
+    const int bos = max(p.cu[b], 0), eos = (int)min((int64_t)p.cu[b + 1], p.T);
+    const int kh = h / (p.Hv / p.Hk);
+    const int V = gridDim.z * BV;
+    const int v0 = blockIdx.z * BV + warp * kRowsPerWarp;
+
+    const InT* __restrict__ qp = static_cast<const InT*>(p.q);
+    const InT* __restrict__ kp = static_cast<const InT*>(p.k);
+    const InT* __restrict__ vp = static_cast<const InT*>(p.v);
+    const InT* __restrict__ bp = static_cast<const InT*>(p.beta);
+    InT* __restrict__ op = static_cast<InT*>(p.o);
+    PoolT* pool = static_cast<PoolT*>(p.pool);
+
+    PoolT* srow = pool + (((size_t)slot * p.Hv + h) * V + v0) * K + lane * KPT;
+    float s[kRowsPerWarp][KPT];
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) Vec<PoolT, KPT>::load(srow + (size_t)r * K, s[r]);
+
+    for (int t = bos; t < eos; ++t) {
+        float kk[KPT], qq[KPT];
+        Vec<InT, KPT>::load(kp + ((size_t)t * p.Hk + kh) * K + lane * KPT, kk);
+        Vec<InT, KPT>::load(qp + ((size_t)t * p.Hk + kh) * K + lane * KPT, qq);
+        if (p.flags & 1) {  // GDR_QK_L2NORM
+            float sk = 0.f, sq = 0.f;
+#pragma unroll
+            for (int c = 0; c < KPT; ++c) { sk += kk[c] * kk[c]; sq += qq[c] * qq[c]; }
+            const float ik = rsqrtf(warp_sum(sk) + 1e-6f), iq = rsqrtf(warp_sum(sq) + 1e-6f);
+#pragma unroll
+            for (int c = 0; c < KPT; ++c) { kk[c] *= ik; qq[c] *= iq; }
+        }
+        const float a = __expf(p.g[(size_t)t * p.Hv + h]);
+        const float bt = to_f(bp[(size_t)t * p.Hv + h]);
+        const float vv = to_f(vp[((size_t)t * p.Hv + h) * V + v0 + (lane & 15)]);
+
+        float x[32];
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+            float dk = 0.f, dq = 0.f;
+#pragma unroll
+            for (int c = 0; c < KPT; ++c) { dk += s[r][c] * kk[c]; dq += s[r][c] * qq[c]; }
+            x[r] = dk;
+            x[r + kRowsPerWarp] = dq;
+        }
+        float kq = 0.f;
+#pragma unroll
+        for (int c = 0; c < KPT; ++c) kq += kk[c] * qq[c];
+        kq = warp_sum(kq);
+        // lane r < 16 now holds (S k)_r, lane 16 + r holds (S q)_r (pre-decay)
+        const float red = reduce32_to_lane(x, lane);
+        const float n_mine = bt * (vv - a * red);  // valid on lanes < 16
+        const float n_row = __shfl_sync(0xffffffffu, n_mine, lane & 15);
+        if (lane >= kRowsPerWarp) {
+            const float o = p.scale * (a * red + n_row * kq);
+            op[((size_t)t * p.Hv + h) * V + v0 + (lane - kRowsPerWarp)] = from_f<InT>(o);
+        }
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+            const float nr = __shfl_sync(0xffffffffu, n_mine, r);
+#pragma unroll
+            for (int c = 0; c < KPT; ++c) s[r][c] = fmaf(a, s[r][c], nr * kk[c]);
+        }
+        if (p.ibuf && t - bos < p.steps) {
+            PoolT* irow = static_cast<PoolT*>(p.ibuf) +
+                          ((((size_t)b * p.steps + (t - bos)) * p.Hv + h) * V + v0) * K + lane * KPT;
+#pragma unroll
+            for (int r = 0; r < kRowsPerWarp; ++r) Vec<PoolT, KPT>::store(irow + (size_t)r * K, s[r]);
+        }
+    }
+    if (p.flags & 4) {  // GDR_COMMIT
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) Vec<PoolT, KPT>::store(srow + (size_t)r * K, s[r]);
+    }
+}
+
+template <typename InT, typename PoolT, int K>
+cudaError_t launch_k(const RecParams& p, int N, int V, cudaStream_t stream) {
+    // V-column split for occupancy: enough CTAs to fill 152 SMs several times.
+    const long units = (long)N * p.Hv;
+    int bv = 128;
+    if (V < 128 || units < 1024) bv = 64;
+    if (V < 64 || units < 256) bv = 32;
+    dim3 grid(N, p.Hv, V / bv);
+    KernelTimer kt("recurrent", stream);
+    switch (bv) {
+        case 128:
+            recurrent_kernel<InT, PoolT, K, 128><<<grid, 256, 0, stream>>>(p);
+            break;
+        case 64:
+            recurrent_kernel<InT, PoolT, K, 64><<<grid, 128, 0, stream>>>(p);
+            break;
+        default:
+            recurrent_kernel<InT, PoolT, K, 32><<<grid, 64, 0, stream>>>(p);
+            break;
+    }
+    return cudaGetLastError();
+}
+
+template <typename InT, typename PoolT>
+cudaError_t launch_kt(const RecParams& p, int N, int K, int V, cudaStream_t stream) {
+    if (K == 128) return launch_k<InT, PoolT, 128>(p, N, V, stream);
+    return launch_k<InT, PoolT, 64>(p, N, V, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t stream) {
+    RecParams p;
+    p.q = a.q; p.k = a.k; p.v = a.v; p.g = a.g; p.beta = a.beta;
+    p.pool = a.pool; p.idx = a.state_indices; p.cu = a.cu_seqlens;
+    p.o = a.o; p.ibuf = a.ibuf;
+    p.Hk = a.Hk; p.Hv = a.Hv; p.steps = a.steps; p.flags = a.flags; p.scale = a.scale;
+    p.num_slots = a.num_slots;
+    p.T = a.T;
+    const bool in_bf16 = a.dtype == 0, pool_bf16 = a.pool_dtype == 0;
+    if (in_bf16 && pool_bf16) return launch_kt<__nv_bfloat16, __nv_bfloat16>(p, a.N, a.K, a.V, stream);
+    if (in_bf16) return launch_kt<__nv_bfloat16, float>(p, a.N, a.K, a.V, stream);
+    if (pool_bf16) return launch_kt<float, __nv_bfloat16>(p, a.N, a.K, a.V, stream);
+    return launch_kt<float, float>(p, a.N, a.K, a.V, stream);
+}
+
+}  // namespace gdr

@@ -1,0 +1,134 @@
+"""Host-side checks of the C ABI: the library builds, loads, exports every
+symbol include/gdr.h declares, sizes its workspace, and rejects bad
+arguments before touching the device (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import gated_delta_rule_37_gb300 as gdr
+from gated_delta_rule_37_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gdr.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "gdr.h")).read()
+    return sorted(set(re.findall(r"GDR_API\s+[\w\s\*]*?\b(gdr_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_exports():
+    assert _declared() == sorted(gdr.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", gdr.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (gdr_\w+)", out))
+    assert set(_declared()) == exported
+
+
+def test_version_and_clean_error(lib):
+    assert lib.gdr_version() == 100
+
+
+def test_workspace_size(lib):
+    n1 = gdr.chunk_workspace_size(4, 6113, 16, 16, 128, 128, gate_kind=0, dtype=0)
+    n2 = gdr.chunk_workspace_size(4, 6113, 16, 16, 128, 128, gate_kind=0, dtype=0, flags=gdr.GDR_QK_L2NORM)
+    assert n1 > 0 and n2 > n1
+    assert n1 % 256 == 0
+    # capacity bound: ceil(T/64) + N chunks, so more sequences never shrink it
+    assert gdr.chunk_workspace_size(8, 6113, 16, 16, 128, 128, gate_kind=0, dtype=0) >= n1
+
+
+@pytest.mark.parametrize("args,code", [
+    (dict(Hk=3, Hv=4), 1),               # Hv not a multiple of Hk
+    (dict(K=96, V=96), 2),               # unsupported head dim
+    (dict(K=128, V=64), 2),              # K != V
+    (dict(dtype=7), 2),                  # bad dtype
+    (dict(gate_kind=5), 1),
+])
+def test_workspace_size_rejects(lib, args, code):
+    base = dict(N=1, T=64, Hk=2, Hv=4, K=128, V=128, gate_kind=0, dtype=0)
+    base.update(args)
+    out = ctypes.c_size_t(0)
+    rc = lib.gdr_chunk_workspace_size(base["N"], base["T"], base["Hk"], base["Hv"], base["K"], base["V"],
+                                      base["gate_kind"], base["dtype"], 0, ctypes.byref(out))
+    assert rc == code
+    assert lib.gdr_last_error().decode()
+
+
+def _chunk_call(lib, **kw):
+    P = ctypes.c_void_p
+    a = dict(q=P(16), k=P(32), v=P(48), g=P(64), gk=None, beta=P(80), h0=None, cu=P(96), N=1, T=64,
+             Hk=2, Hv=4, K=128, V=128, scale=0.1, dtype=0, flags=0, o=P(112), hT=None,
+             ws=P(256), ws_bytes=1 << 40, stream=None)
+    a.update(kw)
+    return lib.gdr_chunk_fwd(a["q"], a["k"], a["v"], a["g"], a["gk"], a["beta"], a["h0"], a["cu"], a["N"],
+                             a["T"], a["Hk"], a["Hv"], a["K"], a["V"], a["scale"], a["dtype"], a["flags"],
+                             a["o"], a["hT"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(g=None), 1),                                  # neither g nor gk
+    (dict(gk=ctypes.c_void_p(128)), 1),                 # both g and gk
+    (dict(q=None), 1),                                  # null input
+    (dict(q=ctypes.c_void_p(17)), 1),                   # misaligned
+    (dict(ws=ctypes.c_void_p(272)), 1),                 # workspace not 256-aligned
+    (dict(ws_bytes=1024), 3),                           # workspace too small
+    (dict(flags=0x4), 1),                               # commit is not a prefill flag
+    (dict(K=64, V=128), 2),
+    (dict(N=0, T=64), 1),                               # tokens without sequences
+])
+def test_chunk_fwd_rejects_before_launch(lib, kw, code):
+    assert _chunk_call(lib, **kw) == code
+    assert lib.gdr_last_error().decode()
+
+
+def test_chunk_fwd_empty_is_ok_without_device(lib):
+    assert _chunk_call(lib, N=0, T=0) == 0
+
+
+def _rec_call(lib, **kw):
+    P = ctypes.c_void_p
+    a = dict(q=P(16), k=P(32), v=P(48), g=P(64), beta=P(80), pool=P(96), pool_dtype=1, num_slots=8,
+             idx=P(112), cu=P(128), N=4, T=4, Hk=2, Hv=4, K=128, V=128, scale=0.1, dtype=0, flags=4,
+             o=P(144), ibuf=None, steps=0, stream=None)
+    a.update(kw)
+    return lib.gdr_recurrent_fwd(a["q"], a["k"], a["v"], a["g"], a["beta"], a["pool"], a["pool_dtype"],
+                                 a["num_slots"], a["idx"], a["cu"], a["N"], a["T"], a["Hk"], a["Hv"], a["K"],
+                                 a["V"], a["scale"], a["dtype"], a["flags"], a["o"], a["ibuf"], a["steps"],
+                                 a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(pool_dtype=3), 2),
+    (dict(num_slots=0), 1),
+    (dict(ibuf=ctypes.c_void_p(160), steps=0), 1),
+    (dict(idx=None), 1),
+    (dict(pool=ctypes.c_void_p(100)), 1),               # misaligned pool
+    (dict(flags=0x2), 1),                               # neg-eigval is a gating flag
+    (dict(Hk=3), 1),
+])
+def test_recurrent_fwd_rejects_before_launch(lib, kw, code):
+    assert _rec_call(lib, **kw) == code
+
+
+def test_recurrent_fwd_empty_is_ok(lib):
+    assert _rec_call(lib, N=0, T=0) == 0
+
+
+def test_gating_rejects(lib):
+    P = ctypes.c_void_p
+    assert lib.gdr_gating_fwd(P(16), P(32), P(48), P(64), 4, 0, 0, 0, P(80), P(96), None) == 1
+    assert lib.gdr_gating_fwd(P(16), P(32), P(48), P(64), 4, 2, 9, 0, P(80), P(96), None) == 2
+    assert lib.gdr_gating_fwd(P(16), P(32), P(48), P(64), 0, 2, 0, 0, P(80), P(96), None) == 0

@@ -1,0 +1,235 @@
+"""GPU parity of the chunked prefill against the CPU oracle, through the C ABI:
+the three prefill workloads at full size (the long KDA one on sampled heads),
+small ragged / GVA / tail / adversarial-decay cases, contract checks."""
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_37_gb300 as gdr
+import oracle
+from gated_delta_rule_37_gb300 import workloads
+from tests.gpu_util import Guarded, bits_equal, check_out, check_state
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gdr.load()
+
+
+def run_gpu(case, flags=0, guarded=True):
+    dev = DEV
+    T, Hv, V, K, N = case.T, case.v.shape[1], case.v.shape[2], case.q.shape[2], case.N
+    o = Guarded((T, Hv, V), case.q.dtype, dev)
+    sf = Guarded((N, Hv, V, K), torch.float32, dev)
+    ins = dict(g=case.g.to(dev) if case.g is not None else None,
+               gk=case.gk.to(dev) if case.gk is not None else None,
+               initial_state=case.initial_state.to(dev) if case.initial_state is not None else None)
+    q, k, v, beta = case.q.to(dev), case.k.to(dev), case.v.to(dev), case.beta.to(dev)
+    snap = [t.clone() for t in (q, k, v, beta)]
+    gdr.chunk_fwd(q, k, v, beta, case.cu_seqlens.to(dev), scale=case.scale, flags=flags, o=o.view,
+                  final_state=sf.view, **ins)
+    torch.cuda.synchronize()
+    assert o.guards_intact() and sf.guards_intact(), "write outside the output buffers"
+    for a, b in zip((q, k, v, beta), snap):
+        assert bits_equal(a, b), "an input was modified"
+    return o.view, sf.view
+
+
+def oracle_ref(case, heads=None):
+    if heads is None:
+        return oracle.tokenwise(case.q, case.k, case.v, case.beta, case.cu_seqlens, g=case.g, gk=case.gk,
+                                initial_state=case.initial_state, scale=case.scale)
+    Hk, Hv = case.q.shape[1], case.v.shape[1]
+    kh = [h // (Hv // Hk) for h in heads]
+    sl = lambda t: None if t is None else t[:, heads]
+    return oracle.tokenwise(case.q[:, kh], case.k[:, kh], case.v[:, heads], case.beta[:, heads],
+                            case.cu_seqlens, g=sl(case.g), gk=sl(case.gk),
+                            initial_state=None if case.initial_state is None else case.initial_state[:, heads],
+                            scale=case.scale)
+
+
+def test_tiny_fp32_prefill_full_size():
+    """1 sequence T=128 (2 chunks), 2 heads, K=V=64, fp32, scale 1/8."""
+    case = workloads.tiny_fp32_prefill()
+    o, sf = run_gpu(case)
+    ro, rs = oracle_ref(case)
+    check_out(o.cpu(), ro, "o")
+    check_state(sf.cpu(), rs, "final state")
+
+
+def test_varlen_bf16_prefill_full_size():
+    """4 sequences {65,1000,2048,3000}, H=16, K=V=128, bf16, g ~ U[-2,0], h0."""
+    case = workloads.varlen_bf16_prefill()
+    o, sf = run_gpu(case)
+    ro, rs = oracle_ref(case)
+    check_out(o.cpu(), ro, "o")
+    check_state(sf.cpu(), rs, "final state")
+
+
+def test_kda_long_prefill_full_size_sampled_heads():
+    """T=32768, Hk 16 / Hv 32, per-channel gk ~ U[-0.1,0]; the oracle runs the
+    whole sequence for 4 sampled value-heads (both heads of one key head, and
+    two others), every token of those heads is compared."""
+    case = workloads.kda_long_prefill()
+    o, sf = run_gpu(case, guarded=True)
+    heads = [0, 1, 17, 30]
+    ro, rs = oracle_ref(case, heads)
+    check_out(o[:, heads].cpu(), ro, "o (sampled heads)")
+    check_state(sf[:, heads].cpu(), rs, "final state (sampled heads)")
+
+
+CASES = [
+    # (lens, Hk, Hv, gate, g_range, h0, dtype, K)
+    ([1], 2, 2, "g", (-0.05, 0.0), False, torch.bfloat16, 128),
+    ([65, 1], 2, 2, "g", (-1.0, 0.0), True, torch.bfloat16, 128),
+    ([65, 63], 2, 2, "g", (-2.0, 0.0), True, torch.bfloat16, 128),
+    ([1024], 1, 1, "g", (-0.5, 0.0), False, torch.bfloat16, 128),
+    ([1] * 32, 2, 2, "g", (-1.0, 0.0), True, torch.bfloat16, 128),
+    ([1, 63, 65, 2], 2, 4, "g", (-2.0, 0.0), True, torch.bfloat16, 128),     # GVA 2
+    ([4], 1, 4, "g", (-1.0, 0.0), True, torch.bfloat16, 128),                # GVA 4 with init
+    ([65, 1, 129, 63], 1, 4, "gk", (-0.3, 0.0), True, torch.bfloat16, 128),  # KDA GVA 4
+    ([200, 7], 2, 4, "gk", (-2.0, 0.0), False, torch.bfloat16, 128),         # KDA adversarial
+    ([100, 28], 2, 2, "g", (-1.0, 0.0), True, torch.float32, 64),
+    ([130, 3], 1, 2, "gk", (-0.5, 0.0), True, torch.float32, 128),
+]
+
+
+@pytest.mark.parametrize("lens,Hk,Hv,gate,g_range,h0,dtype,K", CASES)
+def test_small_cases(lens, Hk, Hv, gate, g_range, h0, dtype, K):
+    case = workloads.chunk_case(51 + sum(lens) % 97, lens, Hk, Hv, K, K, dtype=dtype, gate=gate,
+                                g_range=g_range, h0_std=0.1 if h0 else None)
+    o, sf = run_gpu(case)
+    ro, rs = oracle_ref(case)
+    check_out(o.cpu(), ro, "o")
+    check_state(sf.cpu(), rs, "final state")
+
+
+@pytest.mark.parametrize("gate", ["g", "gk"])
+def test_gate_minus_two_everywhere(gate):
+    """g = -2 on every token: a prefix of -128 per 64-token chunk; every
+    exponential must stay an in-chunk difference (finite results)."""
+    case = workloads.chunk_case(61, [128, 64, 33], 2, 2, 128, 128, gate=gate, h0_std=0.1)
+    if gate == "g":
+        case.g[:] = -2.0
+    else:
+        case.gk[:] = -2.0
+    o, sf = run_gpu(case)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(sf).all()
+    ro, rs = oracle_ref(case)
+    check_out(o.cpu(), ro, "o")
+    check_state(sf.cpu(), rs, "final state")
+
+
+def test_gate_zero_and_beta_endpoints():
+    case = workloads.chunk_case(62, [70, 64], 2, 2, 128, 128, h0_std=0.1)
+    case.g[:40] = 0.0
+    case.beta[:20] = 0.0
+    case.beta[20:60] = 1.0
+    o, sf = run_gpu(case)
+    ro, rs = oracle_ref(case)
+    check_out(o.cpu(), ro, "o")
+    check_state(sf.cpu(), rs, "final state")
+
+
+def test_qk_l2norm_flag():
+    case = workloads.chunk_case(63, [90, 40], 2, 4, 128, 128, dtype=torch.float32, h0_std=0.1)
+    gen = torch.Generator().manual_seed(3)
+    case.q = torch.randn(case.q.shape, generator=gen) * 2.0
+    case.k = torch.randn(case.k.shape, generator=gen) * 0.7
+    o, sf = run_gpu(case, flags=gdr.GDR_QK_L2NORM)
+    qn = torch.from_numpy(oracle.l2norm(case.q, 1e-6))
+    kn = torch.from_numpy(oracle.l2norm(case.k, 1e-6))
+    ro, rs = oracle.tokenwise(qn, kn, case.v, case.beta, case.cu_seqlens, g=case.g,
+                              initial_state=case.initial_state, scale=case.scale)
+    check_out(o.cpu(), ro, "o")
+    check_state(sf.cpu(), rs, "final state")
+
+
+def test_position_independence():
+    """A sequence's result does not depend on where it sits in the packed batch."""
+    a = workloads.chunk_case(64, [100, 37, 70], 1, 2, 128, 128, h0_std=0.1)
+    o1, s1 = run_gpu(a)
+    perm = [2, 0, 1]
+    cu = a.cu_seqlens.tolist()
+    segs = [slice(cu[i], cu[i + 1]) for i in range(3)]
+    b = workloads.ChunkCase(name="perm", q=torch.cat([a.q[segs[i]] for i in perm]),
+                            k=torch.cat([a.k[segs[i]] for i in perm]), v=torch.cat([a.v[segs[i]] for i in perm]),
+                            beta=torch.cat([a.beta[segs[i]] for i in perm]),
+                            g=torch.cat([a.g[segs[i]] for i in perm]),
+                            cu_seqlens=torch.tensor([0, 70, 170, 207], dtype=torch.int32),
+                            scale=a.scale, initial_state=a.initial_state[perm])
+    o2, s2 = run_gpu(b)
+    for j, i in enumerate(perm):
+        assert bits_equal(s2[j], s1[i])
+        cb = b.cu_seqlens.tolist()
+        assert bits_equal(o2[cb[j]:cb[j + 1]], o1[segs[i]])
+
+
+def test_deterministic_repeat():
+    case = workloads.varlen_bf16_prefill()
+    o1, s1 = run_gpu(case)
+    o1, s1 = o1.clone(), s1.clone()
+    for _ in range(2):
+        o2, s2 = run_gpu(case)
+        assert bits_equal(o2, o1) and bits_equal(s2, s1)
+
+
+def test_validate_flag():
+    case = workloads.chunk_case(65, [10, 20], 1, 1, 128, 128)
+    dev = DEV
+    g = case.g.clone()
+    g[3, 0] = float("inf")
+    with pytest.raises(gdr.GdrError) as e:
+        gdr.chunk_fwd(case.q.to(dev), case.k.to(dev), case.v.to(dev), case.beta.to(dev),
+                      case.cu_seqlens.to(dev), g=g.to(dev), flags=gdr.GDR_VALIDATE)
+    assert e.value.code == 6
+    bad_cu = torch.tensor([0, 20, 10], dtype=torch.int32, device=dev)
+    with pytest.raises(gdr.GdrError):
+        gdr.chunk_fwd(case.q.to(dev), case.k.to(dev), case.v.to(dev), case.beta.to(dev), bad_cu,
+                      g=case.g.to(dev), flags=gdr.GDR_VALIDATE)
+
+
+def test_cuda_graph_replay_equals_eager():
+    case = workloads.varlen_bf16_prefill()
+    dev = DEV
+    q, k, v, beta = (t.to(dev) for t in (case.q, case.k, case.v, case.beta))
+    g, h0, cu = case.g.to(dev), case.initial_state.to(dev), case.cu_seqlens.to(dev)
+    o = torch.empty_like(v)
+    sf = torch.empty_like(h0)
+    ws = torch.empty(gdr.chunk_workspace_size(case.N, case.T, 16, 16, 128, 128, gate_kind=0, dtype=0),
+                     dtype=torch.uint8, device=dev)
+    gdr.chunk_fwd(q, k, v, beta, cu, g=g, initial_state=h0, scale=case.scale, o=o, final_state=sf, workspace=ws)
+    torch.cuda.synchronize()
+    o_e, s_e = o.clone(), sf.clone()
+    o.zero_()
+    sf.zero_()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            gdr.chunk_fwd(q, k, v, beta, cu, g=g, initial_state=h0, scale=case.scale, o=o, final_state=sf,
+                          workspace=ws, stream=s)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert bits_equal(o, o_e) and bits_equal(sf, s_e)
+
+
+def test_gating_kernel():
+    T, Hv = 300, 8
+    gen = torch.Generator().manual_seed(66)
+    a = torch.randn(T, Hv, generator=gen) * 8
+    a[0, 0] = 30.0                       # threshold branch
+    b = torch.randn(T, Hv, generator=gen) * 3
+    dt = torch.randn(Hv, generator=gen)
+    A_log = torch.randn(Hv, generator=gen) * 0.5
+    for flags, neg in ((0, False), (gdr.GDR_NEG_EIGVAL, True)):
+        g, beta = gdr.gating_fwd(a.to(DEV), dt.to(DEV), A_log.to(DEV), b.to(DEV), flags=flags)
+        torch.cuda.synchronize()
+        rg, rb = oracle.gating(a, dt, A_log, b, neg_eigval=neg)
+        np.testing.assert_allclose(g.cpu().double().numpy(), rg, rtol=1e-5, atol=1e-6)
+        np.testing.assert_allclose(beta.cpu().double().numpy(), rb, rtol=1e-5, atol=1e-6)

@@ -1,0 +1,206 @@
+"""GPU parity of the recurrent decode / verify kernel against the CPU oracle,
+through the C ABI.  Slot indexing, padding skips, ragged boundaries and every
+region the call must not write are checked bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_37_gb300 as gdr
+import oracle
+from gated_delta_rule_37_gb300 import workloads
+from tests.gpu_util import Guarded, bits_equal, check_out, check_state, sentinel_like
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    gdr.load()
+
+
+def run_case(case, *, flags, with_ibuf):
+    dev = DEV
+    pool = Guarded(case.pool.shape, case.pool.dtype, dev, fill_bytes=case.pool)
+    o_init = sentinel_like((case.T, case.v.shape[1], case.v.shape[2]), case.q.dtype)
+    o = Guarded(o_init.shape, case.q.dtype, dev, fill_bytes=o_init)
+    ib = None
+    if with_ibuf:
+        ib_shape = (case.ibuf_rows, case.steps) + tuple(case.pool.shape[1:])
+        ib_init = sentinel_like(ib_shape, case.pool.dtype)
+        ib = Guarded(ib_shape, case.pool.dtype, dev, fill_bytes=ib_init)
+    gdr.recurrent_fwd(case.q.to(dev), case.k.to(dev), case.v.to(dev), case.g.to(dev), case.beta.to(dev),
+                      pool.view, case.state_indices.to(dev), case.cu_seqlens.to(dev), scale=case.scale,
+                      flags=flags, o=o.view, intermediate_states=ib.view if ib else None)
+    torch.cuda.synchronize()
+    assert pool.guards_intact() and o.guards_intact() and (ib is None or ib.guards_intact())
+    return pool, o, ib, o_init
+
+
+def check_case(case, pool, o, ib, o_init, *, commit):
+    ro, rpool, rib = oracle.pool(case.q, case.k, case.v, case.g, case.beta, case.pool, case.state_indices,
+                                 case.cu_seqlens, scale=case.scale, commit=commit, steps=case.steps,
+                                 ibuf_rows=case.ibuf_rows)
+    cu = case.cu_seqlens.tolist()
+    idx = case.state_indices.tolist()
+    valid_rows = [b for b in range(case.N) if idx[b] >= 0]
+    ov = o.view.cpu()
+    tok_valid = np.zeros(case.T, dtype=bool)
+    for b in valid_rows:
+        tok_valid[cu[b]:cu[b + 1]] = True
+    # outputs of valid tokens vs the oracle; padding rows keep the sentinel bits
+    if tok_valid.any():
+        check_out(ov[torch.from_numpy(tok_valid)], ro[tok_valid], "o")
+    assert bits_equal(ov[torch.from_numpy(~tok_valid)], o_init[torch.from_numpy(~tok_valid)])
+    pv = pool.view.cpu()
+    used = sorted(idx[b] for b in valid_rows)
+    if commit and used:
+        check_state(pv[used], rpool[used], "pool (committed slots)")
+    untouched = [s for s in range(case.pool.shape[0]) if not (commit and s in set(used))]
+    assert bits_equal(pv[untouched], case.pool[untouched]), "pool slots that must stay untouched changed"
+    if ib is not None:
+        ibv = ib.view.cpu()
+        sentinel = sentinel_like(ibv.shape[2:], ibv.dtype)
+        for b in range(case.ibuf_rows):
+            L = cu[b + 1] - cu[b] if b < case.N else 0
+            if b < case.N and idx[b] >= 0 and L > 0:
+                check_state(ibv[b, :L], rib[b, :L], f"ibuf row {b}")
+                rest = range(L, case.steps)
+            else:
+                rest = range(case.steps)
+            for t in rest:
+                assert bits_equal(ibv[b, t], sentinel), f"ibuf row {b} step {t} written"
+
+
+def test_decode_fp32_pool_full_size():
+    """256 single-token sequences, Hk 16 / Hv 32, K = V = 128, fp32 pool of 513
+    slots, 26 padding rows, committed in place."""
+    case = workloads.decode_fp32_pool()
+    pool, o, ib, o_init = run_case(case, flags=gdr.GDR_COMMIT, with_ibuf=False)
+    check_case(case, pool, o, ib, o_init, commit=True)
+
+
+def test_verify_bf16_pool_full_size():
+    """64 sequences of 1..12 accepted tokens, bf16 pool, per-token states into
+    [65, 12, 32, 128, 128], pool not committed."""
+    case = workloads.verify_bf16_pool()
+    pool, o, ib, o_init = run_case(case, flags=0, with_ibuf=True)
+    check_case(case, pool, o, ib, o_init, commit=False)
+
+
+def test_verify_with_padding_rows():
+    case = workloads.verify_bf16_pool(pad_count=7)
+    pool, o, ib, o_init = run_case(case, flags=0, with_ibuf=True)
+    check_case(case, pool, o, ib, o_init, commit=False)
+
+
+@pytest.mark.parametrize("Hk,Hv", [(4, 4), (2, 8), (1, 4)])       # MHA, GVA 4, MQA
+@pytest.mark.parametrize("K", [64, 128])
+@pytest.mark.parametrize("dtype,pool_dtype", [(torch.bfloat16, torch.float32), (torch.float32, torch.float32),
+                                              (torch.bfloat16, torch.bfloat16)])
+def test_small_cases(Hk, Hv, K, dtype, pool_dtype):
+    lens = [1, 8, 3, 0, 12, 5]
+    case = workloads.pool_case(31 + K + Hk, lens, Hk, Hv, K, K, 9, dtype=dtype, pool_dtype=pool_dtype,
+                               pad_count=1, commit=True, steps=12, ibuf_rows=7, g_range=(-1.0, 0.0))
+    pool, o, ib, o_init = run_case(case, flags=gdr.GDR_COMMIT, with_ibuf=True)
+    check_case(case, pool, o, ib, o_init, commit=True)
+
+
+def test_gate_endpoints_and_slot_zero():
+    """g = 0 and g = -2 (adversarial decay), beta at 0 and 1; slot 0 valid."""
+    case = workloads.pool_case(41, [4, 4, 4], 2, 4, 128, 128, 3, pool_dtype=torch.float32,
+                               commit=True, steps=4, ibuf_rows=3)
+    case.g[:4] = 0.0
+    case.g[4:8] = -2.0
+    case.beta[8:10] = 0.0
+    case.beta[10:12] = 1.0
+    case.state_indices = torch.tensor([0, 2, 1], dtype=torch.int32)
+    pool, o, ib, o_init = run_case(case, flags=gdr.GDR_COMMIT, with_ibuf=True)
+    check_case(case, pool, o, ib, o_init, commit=True)
+
+
+def test_qk_l2norm_flag():
+    """GDR_QK_L2NORM normalises q and k rows in the kernel (x rsqrt(sum x^2 + 1e-6))."""
+    case = workloads.pool_case(42, [2, 5, 1], 2, 4, 128, 128, 4, dtype=torch.float32,
+                               pool_dtype=torch.float32, commit=True)
+    gen = torch.Generator().manual_seed(5)
+    case.q = torch.randn(case.q.shape, generator=gen) * 3.0
+    case.k = torch.randn(case.k.shape, generator=gen) * 0.5
+    pool, o, _, _ = run_case(case, flags=gdr.GDR_COMMIT | gdr.GDR_QK_L2NORM, with_ibuf=False)
+    qn = torch.from_numpy(oracle.l2norm(case.q, 1e-6))
+    kn = torch.from_numpy(oracle.l2norm(case.k, 1e-6))
+    ro, rpool, _ = oracle.pool(qn, kn, case.v, case.g, case.beta, case.pool, case.state_indices,
+                               case.cu_seqlens, scale=case.scale, commit=True)
+    check_out(o.view.cpu(), ro, "o")
+    used = sorted(int(s) for s in case.state_indices if s >= 0)
+    check_state(pool.view.cpu()[used], rpool[used], "pool")
+
+
+def test_decode_equals_chunk_path_at_one_token():
+    """Decode at T = 1 and the chunked prefill at T = 1 give the same state."""
+    case = workloads.pool_case(43, [1, 1, 1, 1], 2, 4, 128, 128, 4, pool_dtype=torch.float32, commit=True)
+    case.state_indices = torch.arange(4, dtype=torch.int32)
+    pool, o, _, _ = run_case(case, flags=gdr.GDR_COMMIT, with_ibuf=False)
+    oc, sc = gdr.chunk_fwd(case.q.to(DEV), case.k.to(DEV), case.v.to(DEV), case.beta.to(DEV),
+                           case.cu_seqlens.to(DEV), g=case.g.to(DEV), initial_state=case.pool.to(DEV),
+                           scale=case.scale)
+    torch.cuda.synchronize()
+    check_state(pool.view.cpu(), sc.cpu().double().numpy(), "decode vs chunk state")
+    check_out(o.view.cpu(), oc.float().cpu().double().numpy(), "decode vs chunk o")
+
+
+def test_deterministic_repeat():
+    case = workloads.verify_bf16_pool()
+    outs = []
+    for _ in range(3):
+        pool, o, ib, _ = run_case(case, flags=0, with_ibuf=True)
+        outs.append((o.view.cpu(), ib.view.cpu()))
+    for o2, ib2 in outs[1:]:
+        assert bits_equal(o2, outs[0][0]) and bits_equal(ib2, outs[0][1])
+
+
+def test_validate_flag_rejects_bad_content():
+    case = workloads.pool_case(44, [2, 3], 2, 4, 128, 128, 4, pool_dtype=torch.float32, commit=True,
+                               steps=3, ibuf_rows=2)
+    dev = DEV
+    args = [case.q.to(dev), case.k.to(dev), case.v.to(dev), case.g.to(dev), case.beta.to(dev)]
+    pool = case.pool.to(dev)
+    ib = torch.zeros((2, 3) + tuple(case.pool.shape[1:]), device=dev)
+    bad_idx = torch.tensor([1, 1], dtype=torch.int32, device=dev)          # duplicate slot
+    with pytest.raises(gdr.GdrError) as e:
+        gdr.recurrent_fwd(*args, pool, bad_idx, case.cu_seqlens.to(dev), flags=gdr.GDR_COMMIT | gdr.GDR_VALIDATE,
+                          intermediate_states=ib)
+    assert e.value.code == 6 and "duplicate" in str(e.value)
+    g_bad = case.g.clone()
+    g_bad[0, 0] = 0.5                                                   # gate > 0
+    args[3] = g_bad.to(dev)
+    with pytest.raises(gdr.GdrError):
+        gdr.recurrent_fwd(*args, pool, case.state_indices.to(dev), case.cu_seqlens.to(dev),
+                          flags=gdr.GDR_VALIDATE, intermediate_states=ib)
+    assert torch.equal(pool.cpu(), case.pool)                            # nothing launched
+
+
+def test_cuda_graph_replay_equals_eager():
+    case = workloads.verify_bf16_pool()
+    dev = DEV
+    ins = [t.to(dev) for t in (case.q, case.k, case.v, case.g, case.beta)]
+    pool = case.pool.to(dev)
+    idx, cu = case.state_indices.to(dev), case.cu_seqlens.to(dev)
+    o = torch.empty(case.T, 32, 128, dtype=torch.bfloat16, device=dev)
+    ib = torch.zeros((65, 12, 32, 128, 128), dtype=torch.bfloat16, device=dev)
+    gdr.recurrent_fwd(*ins, pool, idx, cu, scale=case.scale, flags=0, o=o, intermediate_states=ib)
+    torch.cuda.synchronize()
+    o_e, ib_e = o.clone(), ib.clone()
+    o.zero_()
+    ib.zero_()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            gdr.recurrent_fwd(*ins, pool, idx, cu, scale=case.scale, flags=0, o=o, intermediate_states=ib,
+                              stream=s)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert bits_equal(o, o_e) and bits_equal(ib, ib_e)
