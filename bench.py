@@ -1,0 +1,475 @@
+"""Benchmark of the GB300 gated delta rule forward library.
+
+One step = one chunked-prefill call (gdr_chunk_fwd: chunk metadata, intra-chunk
+cumsum / A / solve / WY, inter-chunk state recurrence, output) over the varlen
+bf16 workload: 4 sequences {65, 1000, 2048, 3000} (6113 tokens), 16 heads,
+K = V = 128, g ~ U[-2, 0], fp32 initial state.  `value` is prefill tokens/s with
+inputs resident in HBM; the L2 (129 MB) is flushed before every timed step by
+writing a 256 MB buffer outside the step's events.  The same line carries the
+recurrent decode (256 sequences, fp32 pool, commit), the multi-step verify
+(64 sequences, 1..12 tokens, bf16 pool + per-token states) and the long KDA
+prefill (T = 32768, Hv = 32, per-channel gate) as extra objects, each with its
+own roofline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun every rank runs the same workload on its own GPU (replicas, no
+collective on the data path) and rank 0 prints one JSON line with the
+whole-job throughput over the slowest rank.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import gated_delta_rule_37_gb300 as gdr  # noqa: E402
+from gated_delta_rule_37_gb300 import workloads  # noqa: E402
+
+METRIC = "prefill tokens/s (% bf16 TC peak); decode tokens/s (% HBM GB/s) on 1 GB300"
+L2_FLUSH_BYTES = 256 << 20
+
+# Algorithmic work (per token and value-head unless stated), K = V = D, C = 64.
+#   chunk_intra : K K^T, Q K^T, Tm K (each C*K, triangular) + Tm V (C*V)
+#   chunk_state : W S^T and the state update (2*K*V each)
+#   chunk_out   : Q S^T (2*K*V) + P Nn (C*V, triangular)
+# The three sum to 6KV + 3CK + 2CV = 139,264 flop at K = V = 128.
+
+
+def kernel_flops_per_token_head(name, K, V, C=64):
+    return {"chunk_intra": 3 * C * K + C * V, "chunk_state": 4 * K * V, "chunk_out": 2 * K * V + C * V}.get(name)
+
+
+def prefill_flops(T, Hv, K, V, C=64):
+    return T * Hv * (6 * K * V + 3 * C * K + 2 * C * V)
+
+
+def prefill_bytes(case):
+    """Algorithmic HBM bytes of one prefill call: inputs read once, outputs
+    written once (q, k, v, gate, beta, o, initial and final state)."""
+    n = sum(t.numel() * t.element_size() for t in (case.q, case.k, case.v, case.beta))
+    n += (case.g if case.g is not None else case.gk).numel() * 4
+    n += case.v.numel() * case.v.element_size()  # o
+    if case.initial_state is not None:
+        n += case.initial_state.numel() * 4
+    n += case.N * case.v.shape[1] * case.v.shape[2] * case.q.shape[2] * 4  # final state
+    return n
+
+
+def pool_bytes(case):
+    """Algorithmic HBM bytes of one decode / verify call over valid rows:
+    slab read, slab write back (commit) or per-token states (verify), and the
+    per-token q, k, v, g, beta, o."""
+    Hv, V, K = case.pool.shape[1:]
+    esz = case.pool.element_size()
+    slab = Hv * V * K * esz
+    cu = case.cu_seqlens.tolist()
+    valid = [b for b in range(case.N) if int(case.state_indices[b]) >= 0]
+    toks = sum(cu[b + 1] - cu[b] for b in valid)
+    n = len(valid) * slab
+    if case.commit:
+        n += len(valid) * slab
+    if case.steps:
+        n += toks * slab
+    per_tok = 2 * case.q.shape[1] * K * case.q.element_size() + 2 * Hv * V * case.v.element_size() \
+        + Hv * 4 + Hv * case.beta.element_size()
+    return n + toks * per_tok, toks
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sustained=d.get("bf16_tflops_sustained"),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        self.proc.wait()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def timed_steps(step, K, flush, stream, profile=True):
+    """Run K steps, each bracketed by CUDA events on `stream`, with the L2
+    flushed (outside the events) before each.  Returns per-step ms and the
+    per-kernel profile of the timed steps."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if profile:
+        gdr.profile_read()
+        gdr.profile_enable(True)
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush()
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    prof = {}
+    if profile:
+        gdr.profile_enable(False)
+        prof = gdr.profile_read()
+    return [a.elapsed_time(b) for a, b in evs], prof
+
+
+def roofline(prof, steps, work_per_kernel, peaks, bound_of):
+    """Dominant kernel (largest device time) -> roofline object."""
+    name = max(prof, key=lambda k: prof[k][0])
+    total_ms, launches = prof[name]
+    avg_s = total_ms / launches / 1e3
+    work = work_per_kernel(name)
+    bound = bound_of(name)
+    if bound == "hbm":
+        ach = work / avg_s / 1e9
+        peak, unit = peaks["hbm"], "GB/s"
+    else:
+        ach = work / avg_s / 1e12
+        peak, unit = peaks["bf16"], "TFLOP/s"
+    share = {k: round(v[0] / sum(x[0] for x in prof.values()), 4) for k, v in prof.items()}
+    return {"kernel": name, "bound": bound, "achieved": round(ach, 3), "peak": peak, "unit": unit,
+            "frac": round(ach / peak, 5), "peak_source": peaks["source"], "traffic": None,
+            "avg_launch_us": round(avg_s * 1e6, 3), "launches": launches, "time_share": share}
+
+
+# ---------------------------------------------------------------------------
+# prefill
+# ---------------------------------------------------------------------------
+class Prefill:
+    def __init__(self, case, dev):
+        self.case = case
+        c = case
+        self.dev = dev
+        self.q, self.k, self.v, self.beta = (t.to(dev) for t in (c.q, c.k, c.v, c.beta))
+        self.g = c.g.to(dev) if c.g is not None else None
+        self.gk = c.gk.to(dev) if c.gk is not None else None
+        self.h0 = c.initial_state.to(dev) if c.initial_state is not None else None
+        self.cu = c.cu_seqlens.to(dev)
+        d = c.dims
+        self.o = torch.empty(c.T, d["Hv"], d["V"], dtype=c.q.dtype, device=dev)
+        self.hT = torch.empty(c.N, d["Hv"], d["V"], d["K"], dtype=torch.float32, device=dev)
+        gk_kind = gdr.GDR_GATE_SCALAR if c.g is not None else gdr.GDR_GATE_CHANNEL
+        dt = gdr.GDR_BF16 if c.q.dtype == torch.bfloat16 else gdr.GDR_F32
+        self.ws = torch.empty(gdr.chunk_workspace_size(c.N, c.T, d["Hk"], d["Hv"], d["K"], d["V"],
+                                                       gate_kind=gk_kind, dtype=dt), dtype=torch.uint8, device=dev)
+
+    def step(self, stream=None):
+        gdr.chunk_fwd(self.q, self.k, self.v, self.beta, self.cu, g=self.g, gk=self.gk, initial_state=self.h0,
+                      scale=self.case.scale, o=self.o, final_state=self.hT, workspace=self.ws, stream=stream)
+
+    def e2e(self, K, stream):
+        """Same call through the public API from pinned host buffers: H2D of
+        the step's inputs and D2H of its outputs inside the timed region."""
+        c = self.case
+        host_in = [t.pin_memory() for t in (c.q, c.k, c.v, c.beta, c.cu_seqlens)]
+        gate = (c.g if c.g is not None else c.gk).pin_memory()
+        h0 = c.initial_state.pin_memory() if c.initial_state is not None else None
+        dev_in = [self.q, self.k, self.v, self.beta, self.cu]
+        dgate = self.g if self.g is not None else self.gk
+        o_host = torch.empty(self.o.shape, dtype=self.o.dtype).pin_memory()
+        hT_host = torch.empty(self.hT.shape, dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host_in + [gate] + ([h0] if h0 is not None else []))
+        d2h = o_host.numel() * o_host.element_size() + hT_host.numel() * 4
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(K):
+                for d, h in zip(dev_in, host_in):
+                    d.copy_(h, non_blocking=True)
+                dgate.copy_(gate, non_blocking=True)
+                if h0 is not None:
+                    self.h0.copy_(h0, non_blocking=True)
+                self.step(stream)
+                o_host.copy_(self.o, non_blocking=True)
+                hT_host.copy_(self.hT, non_blocking=True)
+            end.record(stream)
+        torch.cuda.synchronize()
+        ms = start.elapsed_time(end) / K
+        return ms, h2d, d2h
+
+
+def prefill_work_fn(case):
+    d = case.dims
+    tok_heads = case.T * d["Hv"]
+
+    def work(name):
+        f = kernel_flops_per_token_head(name, d["K"], d["V"])
+        return 0.0 if f is None else f * tok_heads
+    return work
+
+
+# ---------------------------------------------------------------------------
+# decode / verify
+# ---------------------------------------------------------------------------
+class PoolRun:
+    def __init__(self, case, dev):
+        self.case = case
+        c = case
+        self.q, self.k, self.v, self.g, self.beta = (t.to(dev) for t in (c.q, c.k, c.v, c.g, c.beta))
+        self.pool = c.pool.to(dev)
+        self.idx, self.cu = c.state_indices.to(dev), c.cu_seqlens.to(dev)
+        self.o = torch.empty(c.T, c.v.shape[1], c.v.shape[2], dtype=c.q.dtype, device=dev)
+        self.ib = None
+        if c.steps:
+            self.ib = torch.empty((c.ibuf_rows, c.steps) + tuple(c.pool.shape[1:]), dtype=c.pool.dtype, device=dev)
+        self.flags = gdr.GDR_COMMIT if c.commit else 0
+
+    def step(self, stream=None):
+        gdr.recurrent_fwd(self.q, self.k, self.v, self.g, self.beta, self.pool, self.idx, self.cu,
+                          scale=self.case.scale, flags=self.flags, o=self.o, intermediate_states=self.ib,
+                          stream=stream)
+
+
+def measure(runner, K, W, flush, stream, work_fn, bound_of, peaks, units_per_step):
+    for _ in range(W):
+        runner.step(stream)
+    torch.cuda.synchronize()
+    times, prof = timed_steps(lambda: runner.step(stream), K, flush, stream)
+    ms = float(np.mean(times))
+    return ms, prof, roofline(prof, K, work_fn, peaks, bound_of), units_per_step / (ms / 1e3)
+
+
+def cpu_baseline_prefill(case, budget_s=12.0):
+    """The oracle as it stands (fp64 tokenwise, OpenMP over sequence x head) on a
+    bounded sample of the varlen workload: the 1000-token sequence, all heads,
+    repeated until about `budget_s` seconds of wall time have passed."""
+    import oracle
+    cu = case.cu_seqlens.tolist()
+    b = 1
+    sl = slice(cu[b], cu[b + 1])
+    ntok = cu[b + 1] - cu[b]
+    h0 = case.initial_state[b:b + 1] if case.initial_state is not None else None
+    args = dict(q=case.q[sl], k=case.k[sl], v=case.v[sl], beta=case.beta[sl],
+                g=case.g[sl] if case.g is not None else None, gk=case.gk[sl] if case.gk is not None else None,
+                initial_state=h0, cu_seqlens=[0, ntok], scale=case.scale)
+    cores = len(os.sched_getaffinity(0))
+    oracle.tokenwise(**args, nthreads=cores)      # load + warm
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.tokenwise(**args, nthreads=cores)
+        reps += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": round(ntok / dt, 2), "unit": "tokens/s", "cores": min(cores, oracle.num_threads()),
+            "kind": "oracle",
+            "sample": f"1 sequence of {ntok} tokens x all {case.v.shape[1]} heads of the varlen workload, "
+                      f"{reps} repetitions ({dt * reps:.1f} s)"}
+
+
+def config_of(case):
+    d = case.dims
+    return {"workload": case.name, "global_batch": case.N, "seq_len": case.T, "heads_k": d["Hk"],
+            "heads_v": d["Hv"], "head_dim": d["K"], "chunk": 64, "parallelism": "replicas",
+            "l2": "flushed (256 MB write) before every timed step"}
+
+
+def reference_arm(args):
+    """--impl reference: the oracle, as it stands, timed on the host cores on a
+    bounded sample of the same workload (rank 0 only)."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    case = workloads.varlen_bf16_prefill()
+    cu = case.cu_seqlens.tolist()
+    b = 1
+    sl = slice(cu[b], cu[b + 1])
+    ntok = cu[b + 1] - cu[b]
+    kw = dict(q=case.q[sl], k=case.k[sl], v=case.v[sl], beta=case.beta[sl], g=case.g[sl],
+              initial_state=case.initial_state[b:b + 1], cu_seqlens=[0, ntok], scale=case.scale)
+    cores = len(os.sched_getaffinity(0))
+    for _ in range(args.warmup):
+        oracle.tokenwise(**kw, nthreads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.tokenwise(**kw, nthreads=cores)
+    dt = (time.perf_counter() - t0) / args.steps
+    val = ntok / dt
+    line = {"impl": "reference", "metric": METRIC, "value": round(val, 2), "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(case),
+            "cpu_baseline": {"value": round(val, 2), "unit": "tokens/s", "cores": min(cores, oracle.num_threads()),
+                             "kind": "oracle",
+                             "sample": f"1 sequence of {ntok} tokens x all 16 heads of the varlen workload per step"},
+            "e2e": {"value": round(val, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", default="", help="comma list of sections: prefill,decode,verify,kda")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        reference_arm(args)
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    gdr.load()
+    peaks = load_peaks()
+    stream = torch.cuda.Stream()
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_buf.fill_(1)
+    only = set(filter(None, args.only.split(","))) or {"prefill", "decode", "verify", "kda"}
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    pre_case = workloads.varlen_bf16_prefill()
+    pre = Prefill(pre_case, dev)
+    extra = {}
+    dec = ver = kda = None
+    if "decode" in only:
+        dec = PoolRun(workloads.decode_fp32_pool(), dev)
+    if "verify" in only:
+        ver = PoolRun(workloads.verify_bf16_pool(), dev)
+    if "kda" in only:
+        kda = Prefill(workloads.kda_long_prefill(), dev)
+    for _ in range(args.warmup):
+        pre.step(stream)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier()
+    times, prof = timed_steps(lambda: pre.step(stream), args.steps, flush, stream)
+    barrier()
+    ms = max_over_ranks(float(np.mean(times)))
+    launches = sum(v[1] for v in prof.values())
+    roof = roofline(prof, args.steps, prefill_work_fn(pre_case), peaks, lambda n: "tensor")
+    tokens = pre_case.T
+    value = world * tokens / (ms / 1e3)
+    whole_flops = prefill_flops(pre_case.T, 16, 128, 128)
+    whole_bytes = prefill_bytes(pre_case)
+    whole = {"tflops": round(whole_flops / (ms / 1e3) / 1e12, 3),
+             "frac_bf16": round(whole_flops / (ms / 1e3) / 1e12 / peaks["bf16"], 5),
+             "gbs": round(whole_bytes / (ms / 1e3) / 1e9, 2),
+             "frac_hbm": round(whole_bytes / (ms / 1e3) / 1e9 / peaks["hbm"], 5),
+             "algorithmic_flop_per_step": whole_flops, "algorithmic_bytes_per_step": whole_bytes}
+
+    if dec is not None:
+        nbytes, toks = pool_bytes(dec.case)
+        d_ms, d_prof, d_roof, _ = measure(dec, max(args.steps, 20), args.warmup, flush, stream,
+                                          lambda n: nbytes, lambda n: "hbm", peaks, toks)
+        launches += sum(v[1] for v in d_prof.values())
+        d_ms = max_over_ranks(d_ms)
+        extra["decode"] = {"workload": dec.case.name, "tokens_per_s": round(world * toks / (d_ms / 1e3), 1),
+                           "ms_per_step": round(d_ms, 4), "valid_tokens": toks, "roofline": d_roof}
+    if ver is not None:
+        nbytes, toks = pool_bytes(ver.case)
+        v_ms, v_prof, v_roof, _ = measure(ver, max(args.steps, 20), args.warmup, flush, stream,
+                                          lambda n: nbytes, lambda n: "hbm", peaks, toks)
+        launches += sum(v[1] for v in v_prof.values())
+        v_ms = max_over_ranks(v_ms)
+        extra["verify"] = {"workload": ver.case.name, "tokens_per_s": round(world * toks / (v_ms / 1e3), 1),
+                           "ms_per_step": round(v_ms, 4), "valid_tokens": toks, "roofline": v_roof}
+    if kda is not None:
+        k_ms, k_prof, k_roof, _ = measure(kda, max(3, args.steps // 10), args.warmup, flush, stream,
+                                          prefill_work_fn(kda.case), lambda n: "tensor", peaks, kda.case.T)
+        launches += sum(v[1] for v in k_prof.values())
+        k_ms = max_over_ranks(k_ms)
+        kf = prefill_flops(kda.case.T, 32, 128, 128)
+        kb = prefill_bytes(kda.case)
+        extra["kda_long"] = {"workload": kda.case.name, "tokens_per_s": round(world * kda.case.T / (k_ms / 1e3), 1),
+                             "ms_per_step": round(k_ms, 4), "roofline": k_roof,
+                             "whole_call": {"tflops": round(kf / (k_ms / 1e3) / 1e12, 3),
+                                            "gbs": round(kb / (k_ms / 1e3) / 1e9, 2),
+                                            "frac_hbm": round(kb / (k_ms / 1e3) / 1e9 / peaks["hbm"], 5)}}
+    clocks = sampler.stop()
+
+    # end to end through the public API from pinned host buffers
+    e2e_ms, h2d, d2h = pre.e2e(max(5, args.steps // 5), stream)
+    e2e_ms = max_over_ranks(e2e_ms)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_prefill(pre_case)
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic", "config": config_of(pre_case),
+                "roofline": roof, "whole_call": whole,
+                "e2e": {"value": round(world * tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+                "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu, **extra}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
