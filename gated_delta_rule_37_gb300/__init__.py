@@ -30,7 +30,8 @@ STATUS = {0: "GDR_OK", 1: "GDR_ERR_INVALID_ARG", 2: "GDR_ERR_UNSUPPORTED", 3: "G
           4: "GDR_ERR_LAUNCH", 5: "GDR_ERR_DEVICE_TIMEOUT", 6: "GDR_ERR_VALIDATION"}
 
 # every symbol include/gdr.h declares
-EXPORTED = ("gdr_chunk_workspace_size", "gdr_chunk_fwd", "gdr_recurrent_fwd", "gdr_gating_fwd",
+EXPORTED = ("gdr_chunk_workspace_size", "gdr_chunk_fwd", "gdr_chunk_fwd_noalloc", "gdr_recurrent_fwd",
+            "gdr_gating_fwd",
             "gdr_last_error", "gdr_get_device_status", "gdr_profile_enable", "gdr_profile_read",
             "gdr_version")
 
@@ -57,6 +58,8 @@ def load(path: str | None = None):
     lib.gdr_chunk_workspace_size.restype = I
     lib.gdr_chunk_fwd.argtypes = [P, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, I, I, P, P, P, SZ, P]
     lib.gdr_chunk_fwd.restype = I
+    lib.gdr_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, I, I64, I, I, I, I, F, I, I, P, P, P]
+    lib.gdr_chunk_fwd_noalloc.restype = I
     lib.gdr_recurrent_fwd.argtypes = [P, P, P, P, P, P, I, I, P, P, I, I64, I, I, I, I, F, I, I, P, P, I, P]
     lib.gdr_recurrent_fwd.restype = I
     lib.gdr_gating_fwd.argtypes = [P, P, P, P, I64, I, I, I, P, P, P]
@@ -136,6 +139,28 @@ def chunk_fwd(q, k, v, beta, cu_seqlens, *, g=None, gk=None, initial_state=None,
                                 _ptr(initial_state), _ptr(cu_seqlens), N, T, Hk, Hv, K, V,
                                 float(scale), dt, flags, _ptr(o), _ptr(final_state),
                                 _ptr(workspace), workspace.numel(), _stream(stream)))
+    return o, final_state
+
+
+NOALLOC_WORKSPACE_BYTES = 64 << 20
+
+
+def chunk_fwd_noalloc(q, k, v, beta, cu_seqlens, *, g=None, gk=None, initial_state=None, scale=None,
+                      flags: int = 0, o, final_state=None, stream=None):
+    """Chunked prefill through gdr_chunk_fwd_noalloc: no workspace argument and
+    no device allocation inside the call (the library's fixed scratch array of
+    NOALLOC_WORKSPACE_BYTES is used).  For callers that cannot allocate device
+    memory; they pass preallocated outputs ``o`` (and ``final_state``).  Calls
+    that overlap on the GPU share the scratch and must be serialised."""
+    T, Hk, K = q.shape
+    Hv, V = v.shape[1], v.shape[2]
+    N = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = K ** -0.5
+    _check(load().gdr_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(gk), _ptr(beta),
+                                        _ptr(initial_state), _ptr(cu_seqlens), N, T, Hk, Hv, K, V,
+                                        float(scale), _dtype_code(q), flags, _ptr(o), _ptr(final_state),
+                                        _stream(stream)))
     return o, final_state
 
 

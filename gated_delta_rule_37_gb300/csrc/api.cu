@@ -130,6 +130,15 @@ int check_common(int N, int64_t T, int Hk, int Hv, int K, int V, int dtype) {
 }
 
 }  // namespace
+
+int set_last_error(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
 }  // namespace gdr
 
 using namespace gdr;

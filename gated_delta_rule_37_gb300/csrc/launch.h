@@ -80,6 +80,9 @@ struct GatingArgs {
 
 cudaError_t launch_gating(const GatingArgs& a, cudaStream_t stream);
 
+// Record a formatted message for gdr_last_error() on this thread; returns code.
+int set_last_error(int code, const char* fmt, ...);
+
 // Device error word (set by bounded device waits that give up).
 unsigned int* device_error_word();
 

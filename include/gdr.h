@@ -120,6 +120,33 @@ GDR_API int gdr_chunk_fwd(const void* q, const void* k, const void* v, const flo
                   gdr_stream_t stream);
 
 /*
+ * gdr_chunk_fwd_noalloc -- gdr_chunk_fwd without a caller workspace.  There is
+ * no counterpart on the reference pages; it exists for callers that cannot
+ * allocate device memory (a serving engine whose arena already owns all device
+ * memory, a plugin host that exposes no allocator, a decode loop that cannot
+ * afford cudaMalloc's implicit synchronisation).
+ *   Same arguments and results as gdr_chunk_fwd, minus workspace / ws_bytes.
+ *   Scratch comes from an array of GDR_NOALLOC_WORKSPACE_BYTES compiled into
+ *   the library; every GPU that loads the library holds it until exit.  A
+ *   problem whose gdr_chunk_workspace_size exceeds it is rejected with
+ *   GDR_ERR_WORKSPACE before anything runs.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current) and caches it: make that first call before any
+ *   stream capture.
+ *   Nothing is allocated or freed, by the library or any routine it calls.
+ *   All calls share the one array and it keeps the previous call's contents
+ *   (nothing in it has to start at zero): calls whose work overlaps on the
+ *   GPU -- on different streams, or from different host threads -- race on it
+ *   and must be serialised by the caller.
+ */
+#define GDR_NOALLOC_WORKSPACE_BYTES (64ull << 20)
+GDR_API int gdr_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,
+                                  const float* gk, const void* beta, const float* initial_state,
+                                  const int32_t* cu_seqlens, int N, int64_t T_total, int Hk, int Hv,
+                                  int K, int V, float scale, int dtype, int flags, void* o,
+                                  float* final_state, gdr_stream_t stream);
+
+/*
  * gdr_recurrent_fwd -- slot-indexed recurrent decode / multi-step verify
  * (FlashQLA PR #1, paged verify commit and deployment-facts commit).
  *

@@ -132,3 +132,12 @@ def test_gating_rejects(lib):
     assert lib.gdr_gating_fwd(P(16), P(32), P(48), P(64), 4, 0, 0, 0, P(80), P(96), None) == 1
     assert lib.gdr_gating_fwd(P(16), P(32), P(48), P(64), 4, 2, 9, 0, P(80), P(96), None) == 2
     assert lib.gdr_gating_fwd(P(16), P(32), P(48), P(64), 0, 2, 0, 0, P(80), P(96), None) == 0
+
+
+def test_noalloc_rejects_oversized_problem_before_touching_the_device(lib):
+    P = ctypes.c_void_p
+    # 1M tokens x 32 heads needs far more scratch than the library's static array
+    rc = lib.gdr_chunk_fwd_noalloc(P(16), P(32), P(48), P(64), None, P(80), None, P(96), 1, 1 << 20,
+                                   16, 32, 128, 128, 0.1, 0, 0, P(112), None, None)
+    assert rc == 3
+    assert "static scratch" in lib.gdr_last_error().decode()
