@@ -155,7 +155,7 @@ int gdr_chunk_workspace_size(int N, int64_t T_total, int Hk, int Hv, int K, int 
     if (int rc = check_common(N, T_total, Hk, Hv, K, V, dtype)) return rc;
     if (gate_kind != GDR_GATE_SCALAR && gate_kind != GDR_GATE_CHANNEL)
         return fail(GDR_ERR_INVALID_ARG, "gate_kind %d", gate_kind);
-    *bytes = chunk_workspace_layout(N, T_total, Hk, Hv, K, V, dtype, flags).total;
+    *bytes = chunk_workspace_layout(N, T_total, Hk, Hv, K, V, gate_kind, dtype, flags).total;
     return ok();
 }
 
@@ -189,7 +189,8 @@ int gdr_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
         if (p && !aligned16(p)) return fail(GDR_ERR_INVALID_ARG, "pointer %p not 16-byte aligned", p);
     if (reinterpret_cast<uintptr_t>(workspace) & 255u)
         return fail(GDR_ERR_INVALID_ARG, "workspace not 256-byte aligned");
-    const ChunkWorkspace w = chunk_workspace_layout(N, T_total, Hk, Hv, K, V, dtype, flags);
+    const ChunkWorkspace w = chunk_workspace_layout(N, T_total, Hk, Hv, K, V, g ? 0 : 1, dtype, flags);
+    if (w.tc && N > 65535) return fail(GDR_ERR_UNSUPPORTED, "N (%d) above 65535 sequences per call", N);
     if (ws_bytes < w.total)
         return fail(GDR_ERR_WORKSPACE, "workspace %zu bytes < required %zu", ws_bytes, w.total);
     if (w.max_chunks > 0x7fffffffLL) return fail(GDR_ERR_UNSUPPORTED, "too many chunks");

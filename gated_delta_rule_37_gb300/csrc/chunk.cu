@@ -27,8 +27,8 @@ namespace gdr {
 
 static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-ChunkWorkspace chunk_workspace_layout(int N, int64_t T, int Hk, int Hv, int K, int V, int dtype,
-                                      int flags) {
+ChunkWorkspace chunk_workspace_layout(int N, int64_t T, int Hk, int Hv, int K, int V, int gate_kind,
+                                      int dtype, int flags) {
     ChunkWorkspace w{};
     w.max_chunks = (T + kChunk - 1) / kChunk + N;
     const size_t esz = dtype == 0 ? 2 : 4;
@@ -40,6 +40,14 @@ ChunkWorkspace chunk_workspace_layout(int N, int64_t T, int Hk, int Hv, int K, i
     const bool l2 = flags & 1;
     w.off_qn = take(l2 ? esz * (size_t)T * Hk * K : 0);
     w.off_kn = take(l2 ? esz * (size_t)T * Hk * K : 0);
+    w.off_order = take(sizeof(int) * (size_t)(N + 1));
+    w.tc = dtype == 0 && K == 128 && V == 128;
+    if (w.tc) {
+        // tensor-core path: pre-swizzled per-chunk operand images only
+        w.off_blobs = take(chunk_tc_blob_bytes(w.max_chunks, Hk, Hv, gate_kind == 1));
+        w.total = off;
+        return w;
+    }
     w.off_w = take(4 * (size_t)T * Hv * K);
     w.off_u = take(4 * (size_t)T * Hv * V);
     w.off_kd = take(4 * (size_t)T * Hv * K);
@@ -362,7 +370,7 @@ template <typename InT, int K>
 cudaError_t launch_chunk_t(const ChunkArgs& a, cudaStream_t stream) {
     constexpr int C = kChunk;
     constexpr int LD = K + 1;
-    const ChunkWorkspace w = chunk_workspace_layout(a.N, a.T, a.Hk, a.Hv, a.K, a.V, a.dtype, a.flags);
+    const ChunkWorkspace w = chunk_workspace_layout(a.N, a.T, a.Hk, a.Hv, a.K, a.V, a.gk ? 1 : 0, a.dtype, a.flags);
     char* ws = static_cast<char*>(a.workspace);
     ChunkParams p{};
     p.q = a.q; p.k = a.k; p.v = a.v; p.g = a.g; p.gk = a.gk; p.beta = a.beta;
@@ -397,6 +405,7 @@ cudaError_t launch_chunk_t(const ChunkArgs& a, cudaStream_t stream) {
         p.q = qn;
         p.k = kn;
     }
+    if (w.tc) return launch_chunk_tc(a, w, ws, p.q, p.k, stream);
     const size_t sm_intra = sizeof(float) * (4 * C * LD + 2 * C * (C + 1) + C);
     cudaFuncSetAttribute(chunk_intra_kernel<InT, K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_intra);
     {

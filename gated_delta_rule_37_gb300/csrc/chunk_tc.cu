@@ -1,0 +1,833 @@
+// Chunked prefill on the Blackwell tensor cores (bf16 inputs, K = V = 128).
+//
+// Two kernels after the chunk metadata:
+//
+//  prep  (one CTA per chunk x value-head, fully parallel)
+//        gam = in-chunk cumsum of the gate; G = K K^T and Q K^T on tcgen05
+//        (exact bf16 products, fp32 accumulation); A_ij = beta_i e^{gam_i-gam_j}
+//        G_ij (j < i); Tm = (I + A)^{-1} by a blocked forward substitution in
+//        fp32; W = Tm diag(beta e^{gam}) K and U = Tm diag(beta) V on tcgen05
+//        with Tm split into bf16 hi + lo (K, V exact); the masked attention
+//        P_ij = e^{gam_i-gam_j} (q_i . k_j) (j <= i), the decayed queries
+//        e^{gam_i} q_i and the decay factors.  Results are written as
+//        pre-swizzled operand images ("blobs") so the chain kernel stages them
+//        with single 1-D bulk copies.
+//        Per-key-channel gates (KDA) take the same route with A and P formed
+//        per channel on the CUDA cores, W = Tm diag(beta) (K o e^{Gam}) with a
+//        3-term split, and the decayed keys Kd = K o e^{gam_L - Gam} as hi/lo.
+//
+//  chain (one CTA per value-head x 32-column block of V x sequence, serial
+//        over the sequence's chunks; attention-gym PR #344's inter-chunk state
+//        recurrence with the output fused in):
+//          N  = U - W S0^T            M=64, 3-term split (W hi/lo x S hi/lo)
+//          O  = Qd S0^T + P N         M=64 (output, 2 + 1 MMA groups)
+//          S  = e^{gam_L} S0 + K^T (f o N)     M=128, 2-term split
+//        Warp roles: warp 0 stages chunk blobs with cp.async.bulk into a
+//        two-deep ring; warp 1 issues every tcgen05.mma from one thread;
+//        warps 4-7 hold the fp32 state S^T (thread k owns row k, 32 values)
+//        and turn the N accumulator into the split operands; warps 8-11 drain
+//        the output accumulator (double-buffered in TMEM) to bf16 rows of o.
+//
+// Every exponential is of gam_i - gam_j with i >= j or of gam_i, all <= 0:
+// any finite gate <= 0 keeps every operand finite (cuLA PR #113 review).
+#include "common.cuh"
+#include "launch.h"
+#include "tc.cuh"
+
+namespace gdr {
+namespace {
+
+constexpr int C = kChunk;  // 64
+constexpr int D = 128;     // K = V
+constexpr int BV = 32;     // value columns per chain CTA
+constexpr int NVB = D / BV;
+constexpr int LDA = C + 1;  // padded fp32 row stride for the 64 x 64 solve
+
+// Blob sizes (bytes)
+constexpr uint32_t kTile64x128 = C * D * 2;       // 16 KB bf16 [64][128]
+constexpr uint32_t kTile64x64 = C * C * 2;        // 8 KB bf16 [64][64]
+constexpr uint32_t kUBlock = C * BV * 4;          // 8 KB fp32 [64][32]
+constexpr uint32_t kRec = 1024;                   // rowf[64], colf[128], L
+
+struct TcParams {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g;
+    const float* gk;
+    const void* beta;
+    const float* h0;
+    void* o;
+    float* hT;
+    const int32_t* cu;
+    const int* meta;
+    const int* offsets;
+    const int4* table;
+    const int* order;
+    unsigned char* Wb;   // [chunk][Hv][2][16 KB]
+    unsigned char* Ub;   // [chunk][Hv][NVB][8 KB]
+    unsigned char* Qb;   // [chunk][Hv][16 KB]
+    unsigned char* Pb;   // [chunk][Hv][8 KB]
+    unsigned char* Kb;   // scalar gate: [chunk][Hk][16 KB]; channel gate: [chunk][Hv][2][16 KB]
+    unsigned char* Rb;   // [chunk][Hv][1 KB]
+    unsigned int* err;
+    int N, Hk, Hv;
+    float scale;
+};
+
+__device__ __forceinline__ void raise_error(const TcParams& p, unsigned code) {
+    atomicOr(p.err, code);
+}
+
+// ---------------------------------------------------------------------------
+// Blocked inverse of a 64 x 64 unit-lower-triangular matrix (I + A), A strictly
+// lower, fp32, 128 threads.  Diagonal 16 x 16 blocks by forward substitution,
+// then block diagonals d = 1..3:  T_ij = -D_i * sum_{m in blocks j..i-1} A_im T_mj.
+// ---------------------------------------------------------------------------
+__device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict__ Tm, float* __restrict__ Z,
+                                 int tid) {
+    for (int e = tid; e < C * LDA; e += 128) Tm[e] = 0.f;
+    __syncthreads();
+    if (tid < 64) {
+        const int b = tid >> 4, c = tid & 15, r0 = 16 * b;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float s = (r == c) ? 1.f : 0.f;
+#pragma unroll
+            for (int m = 0; m < r; ++m) s = fmaf(-A[(r0 + r) * LDA + r0 + m], x[m], s);
+            x[r] = (r >= c) ? s : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Tm[(r0 + r) * LDA + r0 + c] = x[r];
+    }
+    __syncthreads();
+    for (int d = 1; d < 4; ++d) {
+        const int nblk = 4 - d;
+        for (int e = tid; e < nblk * 256; e += 128) {
+            const int j = e >> 8, i = j + d, r = (e >> 4) & 15, c = e & 15;
+            float s = 0.f;
+            for (int m = 16 * j; m < 16 * i; ++m) s = fmaf(A[(16 * i + r) * LDA + m], Tm[m * LDA + 16 * j + c], s);
+            Z[e] = s;
+        }
+        __syncthreads();
+        for (int e = tid; e < nblk * 256; e += 128) {
+            const int j = e >> 8, i = j + d, r = (e >> 4) & 15, c = e & 15;
+            float s = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m) s = fmaf(Tm[(16 * i + r) * LDA + 16 * i + m], Z[(j << 8) + m * 16 + c], s);
+            Tm[(16 * i + r) * LDA + 16 * j + c] = -s;
+        }
+        __syncthreads();
+    }
+}
+
+// Stage a [64][128] bf16 token tile (rows >= L zero) into a k128 smem tile.
+__device__ __forceinline__ void stage_rows(unsigned char* tile, const __nv_bfloat16* src, size_t row_stride,
+                                           int L, int tid) {
+    for (int e = tid; e < C * 16; e += 128) {
+        const int row = e >> 4, ch = e & 15;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (row < L) val = *reinterpret_cast<const uint4*>(src + (size_t)row * row_stride + ch * 8);
+        *reinterpret_cast<uint4*>(tile + tc::chunk_k128(row, ch, C)) = val;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// prep kernel
+// ---------------------------------------------------------------------------
+template <bool kKDA>
+struct PrepSmem {
+    static constexpr uint32_t kK = 0;                        // K tile 16 KB
+    static constexpr uint32_t kQ = kK + kTile64x128;         // Q tile
+    static constexpr uint32_t kV = kQ + kTile64x128;         // V tile
+    static constexpr uint32_t kT1h = kV + kTile64x128;       // T' hi  [64][64]
+    static constexpr uint32_t kT1l = kT1h + kTile64x64;      // T' lo
+    static constexpr uint32_t kT2h = kT1l + kTile64x64;      // T'' hi
+    static constexpr uint32_t kT2l = kT2h + kTile64x64;      // T'' lo
+    static constexpr uint32_t kKgh = kT2l + kTile64x64;      // K o e^Gam hi (channel gate)
+    static constexpr uint32_t kKgl = kKgh + (kKDA ? kTile64x128 : 0);
+    static constexpr uint32_t kA = kKgl + (kKDA ? kTile64x128 : 0);   // fp32 [64][65]
+    static constexpr uint32_t kTm = kA + C * LDA * 4;                   // fp32 [64][65]
+    static constexpr uint32_t kZ = kTm + C * LDA * 4;                   // fp32 [3][256]
+    static constexpr uint32_t kGam = kZ + 3 * 256 * 4;                  // fp32 [64][128] or [64]
+    static constexpr uint32_t kBeta = kGam + (kKDA ? C * D * 4 : C * 4);
+    static constexpr uint32_t kBar = kBeta + C * 4;
+    static constexpr uint32_t kTotal = kBar + 64 + 1024;  // + alignment slack
+};
+
+template <bool kKDA>
+__global__ void __launch_bounds__(128, 1) chunk_prep_kernel(TcParams p) {
+    using S = PrepSmem<kKDA>;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int chunk = blockIdx.x;
+    if (chunk >= p.meta[0]) return;
+    const int h = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int4 info = p.table[chunk];
+    const int start = info.y, L = info.z;
+    const int grp = p.Hv / p.Hk, kh = h / grp;
+    const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(p.q);
+    const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(p.k);
+    const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(p.v);
+    const __nv_bfloat16* bp = static_cast<const __nv_bfloat16*>(p.beta);
+
+    float* As = reinterpret_cast<float*>(sm + S::kA);
+    float* Tm = reinterpret_cast<float*>(sm + S::kTm);
+    float* Z = reinterpret_cast<float*>(sm + S::kZ);
+    float* gam = reinterpret_cast<float*>(sm + S::kGam);
+    float* bet = reinterpret_cast<float*>(sm + S::kBeta);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::kBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::kBar + 16);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::kBar + 24);
+    const uint32_t bar0 = tc::smem_u32(&bars[0]);
+
+    if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), 256);
+    if (tid == 0) {
+        tc::mbar_init(bar0, 1);
+        *abort_flag = 0;
+        tc::mbar_fence_init();
+    }
+    // stage K, Q, V rows of this chunk (token-major rows, head kh / h)
+    stage_rows(sm + S::kK, kp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
+    stage_rows(sm + S::kQ, qp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
+    stage_rows(sm + S::kV, vp + ((size_t)start * p.Hv + h) * D, (size_t)p.Hv * D, L, tid);
+    if (tid < C) bet[tid] = tid < L ? to_f(bp[((size_t)start + tid) * p.Hv + h]) : 0.f;
+    if (kKDA) {
+        // per-channel inclusive cumsum in token order (thread = channel)
+        float acc = 0.f;
+        for (int i = 0; i < C; ++i) {
+            if (i < L) acc += p.gk[(((size_t)start + i) * p.Hv + h) * D + tid];
+            gam[i * D + tid] = acc;
+        }
+    } else if (tid == 0) {
+        float acc = 0.f;
+        for (int i = 0; i < C; ++i) {
+            if (i < L) acc += p.g[((size_t)start + i) * p.Hv + h];
+            gam[i] = acc;
+        }
+    }
+    tc::fence_proxy_async();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t sK = tc::smem_u32(sm + S::kK), sQ = tc::smem_u32(sm + S::kQ), sV = tc::smem_u32(sm + S::kV);
+    auto gm = [&](int i, int c) -> float { return kKDA ? gam[i * D + c] : gam[i]; };
+    const float* gl = kKDA ? gam + (L - 1) * D : gam + (L - 1);
+
+    // --- A (strictly lower) and P (lower incl. diagonal) ---------------------
+    unsigned char* Pdst = p.Pb + ((size_t)chunk * p.Hv + h) * kTile64x64;
+    if (!kKDA) {
+        if (tid == 0) {
+            constexpr uint32_t id = tc::idesc_bf16(64, 64, false, false);
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t off = (ks >> 2) * (C * 128) + (ks & 3) * 32;
+                tc::mma_bf16(tmem, tc::smem_desc(sK + off, 16, 1024, tc::kSwizzle128),
+                             tc::smem_desc(sK + off, 16, 1024, tc::kSwizzle128), id, ks > 0);
+            }
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t off = (ks >> 2) * (C * 128) + (ks & 3) * 32;
+                tc::mma_bf16(tmem + 64, tc::smem_desc(sQ + off, 16, 1024, tc::kSwizzle128),
+                             tc::smem_desc(sK + off, 16, 1024, tc::kSwizzle128), id, ks > 0);
+            }
+            tc::mma_commit(bar0);
+        }
+        __syncwarp();
+        if (!tc::mbar_wait(bar0, 0, abort_flag)) raise_error(p, 1u);
+        tc::fence_after();
+        const int i = 16 * (warp & 3) + (lane & 15);
+        const uint32_t lrow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        for (int half = 0; half < 2; ++half) {
+            float gv[32], qv[32];
+            tc::tmem_ld32(lrow + 32 * half, gv);
+            tc::tmem_ld32(lrow + 64 + 32 * half, qv);
+            if (lane < 16) {
+                const float gi = gam[i], bi = bet[i];
+                uint32_t pk[16];
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = 32 * half + jj;
+                    const bool inl = i < L && j <= i;
+                    const float e = inl ? __expf(gi - gam[j]) : 0.f;
+                    As[i * LDA + j] = (j < i && i < L) ? bi * e * gv[jj] : 0.f;
+                    const float pv = e * qv[jj];
+                    if (jj & 1) pk[jj >> 1] |= (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(pv)) << 16;
+                    else pk[jj >> 1] = __bfloat16_as_ushort(__float2bfloat16_rn(pv));
+                }
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(i, 4 * half + cc, C)) =
+                        make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+            }
+        }
+    } else {
+        // per-channel decays: A_ij = beta_i sum_c k_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}
+        const __nv_bfloat16* Kt = reinterpret_cast<const __nv_bfloat16*>(sm + S::kK);
+        const __nv_bfloat16* Qt = reinterpret_cast<const __nv_bfloat16*>(sm + S::kQ);
+        for (int e = tid; e < C * C; e += 128) {
+            const int i = e >> 6, j = e & 63;
+            float a = 0.f, pv = 0.f;
+            if (j <= i && i < L) {
+                for (int c = 0; c < D; ++c) {
+                    const float ex = __expf(gam[i * D + c] - gam[j * D + c]);
+                    const float kj = __bfloat162float(Kt[tc::off_k128(j, c, C) >> 1]) * ex;
+                    a = fmaf(__bfloat162float(Kt[tc::off_k128(i, c, C) >> 1]), kj, a);
+                    pv = fmaf(__bfloat162float(Qt[tc::off_k128(i, c, C) >> 1]), kj, pv);
+                }
+            }
+            As[i * LDA + j] = (j < i) ? bet[i] * a : 0.f;
+            reinterpret_cast<__nv_bfloat16*>(Pdst)[tc::off_k128(i, j, C) >> 1] = __float2bfloat16_rn(pv);
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+
+    // --- Tm = (I + A)^{-1} ------------------------------------------------------
+    solve_unit_lower(As, Tm, Z, tid);
+
+    // --- split operands: T' = Tm diag(beta e^{gam}) (scalar gate) / Tm diag(beta);
+    //     T'' = Tm diag(beta); channel gate also K o e^{Gam}.
+    for (int e = tid; e < C * 8; e += 128) {
+        const int i = e >> 3, ch = e & 7;
+        uint32_t h1[4], l1[4], h2[4], l2[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            float a1[2], a2[2];
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+                const int j = ch * 8 + 2 * u + w;
+                const float t = Tm[i * LDA + j] * bet[j];
+                a2[w] = t;
+                a1[w] = kKDA ? t : t * __expf(gam[j]);
+            }
+            float hh[2], ll[2], hh2[2], ll2[2];
+            tc::split_bf16(a1[0], hh[0], ll[0]);
+            tc::split_bf16(a1[1], hh[1], ll[1]);
+            tc::split_bf16(a2[0], hh2[0], ll2[0]);
+            tc::split_bf16(a2[1], hh2[1], ll2[1]);
+            h1[u] = tc::pack_bf16(hh[0], hh[1]);
+            l1[u] = tc::pack_bf16(ll[0], ll[1]);
+            h2[u] = tc::pack_bf16(hh2[0], hh2[1]);
+            l2[u] = tc::pack_bf16(ll2[0], ll2[1]);
+        }
+        const uint32_t off = tc::chunk_k128(i, ch, C);
+        *reinterpret_cast<uint4*>(sm + S::kT1h + off) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
+        *reinterpret_cast<uint4*>(sm + S::kT1l + off) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
+        *reinterpret_cast<uint4*>(sm + S::kT2h + off) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+        *reinterpret_cast<uint4*>(sm + S::kT2l + off) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
+    }
+    if (kKDA) {
+        const __nv_bfloat16* Kt = reinterpret_cast<const __nv_bfloat16*>(sm + S::kK);
+        for (int e = tid; e < C * 16; e += 128) {
+            const int i = e >> 4, ch = e & 15;
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                float hh[2], ll[2];
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    const int c = ch * 8 + 2 * u + w;
+                    const float x = __bfloat162float(Kt[tc::off_k128(i, c, C) >> 1]) * __expf(gam[i * D + c]);
+                    tc::split_bf16(x, hh[w], ll[w]);
+                }
+                hw[u] = tc::pack_bf16(hh[0], hh[1]);
+                lw[u] = tc::pack_bf16(ll[0], ll[1]);
+            }
+            const uint32_t off = tc::chunk_k128(i, ch, C);
+            *reinterpret_cast<uint4*>(sm + S::kKgh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(sm + S::kKgl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+    }
+    tc::fence_proxy_async();
+    __syncthreads();
+
+    // --- W = T' K (or T'' (K o e^Gam)), U = T'' V  --------------------------------
+    if (tid == 0) {
+        tc::fence_after();
+        constexpr uint32_t id = tc::idesc_bf16(64, 128, false, true);
+        const uint32_t t1h = tc::smem_u32(sm + S::kT1h), t1l = tc::smem_u32(sm + S::kT1l);
+        const uint32_t t2h = tc::smem_u32(sm + S::kT2h), t2l = tc::smem_u32(sm + S::kT2l);
+        auto mm = [&](uint32_t dcol, uint32_t a, uint32_t b, bool first) {
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_bf16(tmem + dcol, tc::smem_desc(a + ks * 32, 16, 1024, tc::kSwizzle128),
+                             tc::smem_desc(b + ks * 2048, C * 128, 1024, tc::kSwizzle128), id, (first && ks == 0) ? 0u : 1u);
+        };
+        if (!kKDA) {
+            mm(0, t1h, sK, true);
+            mm(0, t1l, sK, false);
+        } else {
+            const uint32_t kgh = tc::smem_u32(sm + S::kKgh), kgl = tc::smem_u32(sm + S::kKgl);
+            mm(0, t2h, kgh, true);
+            mm(0, t2h, kgl, false);
+            mm(0, t2l, kgh, false);
+        }
+        mm(128, t2h, sV, true);
+        mm(128, t2l, sV, false);
+        tc::mma_commit(bar0);
+    }
+    __syncwarp();
+
+    // --- while the MMAs run: Qd blob, K / Kd blobs, decay record ----------------
+    {
+        const __nv_bfloat16* Qt = reinterpret_cast<const __nv_bfloat16*>(sm + S::kQ);
+        unsigned char* Qdst = p.Qb + ((size_t)chunk * p.Hv + h) * kTile64x128;
+        for (int e = tid; e < C * 16; e += 128) {
+            const int i = e >> 4, ch = e & 15;
+            const uint32_t off = tc::chunk_k128(i, ch, C);
+            uint32_t w4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                float x[2];
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    const int c = ch * 8 + 2 * u + w;
+                    x[w] = __bfloat162float(Qt[(off >> 1) + 2 * u + w]) * __expf(gm(i, c));
+                }
+                w4[u] = tc::pack_bf16(x[0], x[1]);
+            }
+            *reinterpret_cast<uint4*>(Qdst + off) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+        if (!kKDA) {
+            if (h % grp == 0) {
+                unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hk + kh) * kTile64x128;
+                for (int e = tid; e < (int)(kTile64x128 / 16); e += 128)
+                    reinterpret_cast<uint4*>(Kdst)[e] = reinterpret_cast<const uint4*>(sm + S::kK)[e];
+            }
+        } else {
+            const __nv_bfloat16* Kt = reinterpret_cast<const __nv_bfloat16*>(sm + S::kK);
+            unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hv + h) * 2 * kTile64x128;
+            for (int e = tid; e < C * 16; e += 128) {
+                const int i = e >> 4, ch = e & 15;
+                const uint32_t off = tc::chunk_k128(i, ch, C);
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float hh[2], ll[2];
+#pragma unroll
+                    for (int w = 0; w < 2; ++w) {
+                        const int c = ch * 8 + 2 * u + w;
+                        const float x = i < L ? __bfloat162float(Kt[(off >> 1) + 2 * u + w]) *
+                                                    __expf(gl[c] - gam[i * D + c])
+                                              : 0.f;
+                        tc::split_bf16(x, hh[w], ll[w]);
+                    }
+                    hw[u] = tc::pack_bf16(hh[0], hh[1]);
+                    lw[u] = tc::pack_bf16(ll[0], ll[1]);
+                }
+                *reinterpret_cast<uint4*>(Kdst + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(Kdst + kTile64x128 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+        }
+        float* rec = reinterpret_cast<float*>(p.Rb + ((size_t)chunk * p.Hv + h) * kRec);
+        if (tid < C) rec[tid] = tid < L ? (kKDA ? 1.f : __expf(gl[0] - gam[tid])) : 0.f;
+        rec[64 + tid] = __expf(kKDA ? gl[tid] : gl[0]);
+        if (tid == 0) reinterpret_cast<int*>(rec)[192] = L;
+    }
+
+    // --- W, U out of TMEM into their blobs -------------------------------------------
+    // second use of bar0 (the first, K K^T / Q K^T, exists only for the scalar gate)
+    if (!tc::mbar_wait(bar0, kKDA ? 0 : 1, abort_flag)) raise_error(p, 1u);
+    tc::fence_after();
+    {
+        const int i = 16 * (warp & 3) + (lane & 15);
+        const uint32_t lrow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        unsigned char* Wdst = p.Wb + ((size_t)chunk * p.Hv + h) * 2 * kTile64x128;
+        float* Udst = reinterpret_cast<float*>(p.Ub + ((size_t)chunk * p.Hv + h) * NVB * kUBlock);
+        for (int q4 = 0; q4 < 4; ++q4) {
+            float wv[32], uv[32];
+            tc::tmem_ld32(lrow + 32 * q4, wv);
+            tc::tmem_ld32(lrow + 128 + 32 * q4, uv);
+            if (lane < 16) {
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        float hh[2], ll[2];
+                        tc::split_bf16(wv[8 * cc + 2 * u], hh[0], ll[0]);
+                        tc::split_bf16(wv[8 * cc + 2 * u + 1], hh[1], ll[1]);
+                        hw[u] = tc::pack_bf16(hh[0], hh[1]);
+                        lw[u] = tc::pack_bf16(ll[0], ll[1]);
+                    }
+                    const uint32_t off = tc::chunk_k128(i, 4 * q4 + cc, C);
+                    *reinterpret_cast<uint4*>(Wdst + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4*>(Wdst + kTile64x128 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
+                float* urow = Udst + (size_t)q4 * (C * BV) + (size_t)i * BV;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    reinterpret_cast<float4*>(urow)[u] =
+                        make_float4(uv[4 * u], uv[4 * u + 1], uv[4 * u + 2], uv[4 * u + 3]);
+            }
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+// ---------------------------------------------------------------------------
+// chain kernel
+// ---------------------------------------------------------------------------
+template <bool kKDA>
+struct ChainSmem {
+    static constexpr uint32_t kKtBytes = kKDA ? 2 * kTile64x128 : kTile64x128;
+    // one pipeline stage
+    static constexpr uint32_t kW = 0;
+    static constexpr uint32_t kKt = kW + 2 * kTile64x128;
+    static constexpr uint32_t kQd = kKt + kKtBytes;
+    static constexpr uint32_t kP = kQd + kTile64x128;
+    static constexpr uint32_t kU = kP + kTile64x64;
+    static constexpr uint32_t kRec_ = kU + kUBlock;
+    static constexpr uint32_t kStage = kRec_ + kRec;
+    static constexpr uint32_t kStageTx = kStage;  // bytes landed per stage
+    // resident tiles
+    static constexpr uint32_t kSh = 2 * kStage;              // S^T hi [128][32] mn64
+    static constexpr uint32_t kSl = kSh + D * BV * 2;        // S^T lo
+    static constexpr uint32_t kNh = kSl + D * BV * 2;        // N' hi [64][32] mn64
+    static constexpr uint32_t kNl = kNh + C * BV * 2;        // N' lo
+    static constexpr uint32_t kN = kNl + C * BV * 2;         // N (bf16) for the output
+    static constexpr uint32_t kBar = kN + C * BV * 2;
+    static constexpr uint32_t kTotal = kBar + 256 + 1024;
+};
+
+enum ChainBar {
+    kFull0 = 0, kFull1, kEmpty0, kEmpty1, kSReady, kD1Full, kNReady, kD2Full, kOFull0, kOFull1, kOFree0, kOFree1,
+    kDrain, kNumBars
+};
+
+template <bool kKDA>
+__global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
+    using S = ChainSmem<kKDA>;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    if (!p.meta[1]) return;  // malformed cu_seqlens
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.x / NVB, vb = blockIdx.x % NVB, v0 = vb * BV;
+    const int b = p.order[blockIdx.y];
+    const int bos = p.cu[b], eos = p.cu[b + 1];
+    const int nc = (eos - bos + C - 1) / C;
+    const int c0 = p.offsets[b];
+    const int kh = h / (p.Hv / p.Hk);
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::kBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::kBar + 8 * kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::kBar + 8 * kNumBars + 8);
+    auto bar = [&](int i) { return tc::smem_u32(&bars[i]); };
+
+    if (warp == 2) tc::tmem_alloc(tc::smem_u32(tmem_slot), 128);
+    if (tid == 0) {
+        for (int i = 0; i < kNumBars; ++i) tc::mbar_init(bar(i), 1);
+        *abort_flag = 0;
+        tc::mbar_fence_init();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tD1 = tmem, tD2 = tmem + 32, tO = tmem + 64;  // O double-buffered: +0 / +32
+    const uint32_t base = tc::smem_u32(sm);
+    auto fail = [&]() {
+        *abort_flag = 1;
+        raise_error(p, 2u);
+    };
+
+    if (warp == 0) {
+        // ------------------------------ producer ------------------------------
+        if (lane == 0) {
+            for (int c = 0; c < nc && !*abort_flag; ++c) {
+                const int s = c & 1;
+                if (c >= 2 && !tc::mbar_wait(bar(kEmpty0 + s), ((c >> 1) - 1) & 1, abort_flag)) { fail(); break; }
+                const size_t gc = (size_t)c0 + c;
+                const uint32_t st = base + s * S::kStage;
+                const uint32_t fb = bar(kFull0 + s);
+                tc::mbar_arrive_tx(fb, S::kStageTx);
+                tc::bulk_g2s(st + S::kW, p.Wb + (gc * p.Hv + h) * 2 * kTile64x128, 2 * kTile64x128, fb);
+                if (kKDA) tc::bulk_g2s(st + S::kKt, p.Kb + (gc * p.Hv + h) * 2 * kTile64x128, 2 * kTile64x128, fb);
+                else tc::bulk_g2s(st + S::kKt, p.Kb + (gc * p.Hk + kh) * kTile64x128, kTile64x128, fb);
+                tc::bulk_g2s(st + S::kQd, p.Qb + (gc * p.Hv + h) * kTile64x128, kTile64x128, fb);
+                tc::bulk_g2s(st + S::kP, p.Pb + (gc * p.Hv + h) * kTile64x64, kTile64x64, fb);
+                tc::bulk_g2s(st + S::kU, p.Ub + ((gc * p.Hv + h) * NVB + vb) * kUBlock, kUBlock, fb);
+                tc::bulk_g2s(st + S::kRec_, p.Rb + (gc * p.Hv + h) * kRec, kRec, fb);
+            }
+            // drain: wait for the copies of the last (up to) two stages to land
+            for (int c = (nc > 2 ? nc - 2 : 0); c < nc; ++c)
+                tc::mbar_wait_copies(bar(kFull0 + (c & 1)), (c >> 1) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer ------------------------------
+        if (lane == 0) {
+            const uint32_t id1 = tc::idesc_bf16(64, BV, false, true);   // N = W S^T, O = Qd S^T
+            const uint32_t id2 = tc::idesc_bf16(128, BV, true, true);   // dS = K^T N'
+            const uint32_t idO2 = tc::idesc_bf16(64, BV, false, true);  // O += P N
+            const uint32_t sSh = base + S::kSh, sSl = base + S::kSl;
+            const uint32_t sNh = base + S::kNh, sNl = base + S::kNl, sN = base + S::kN;
+            bool issued = false;
+            for (int c = 0; c < nc; ++c) {
+                const int s = c & 1, ob = c & 1;
+                const uint32_t st = base + s * S::kStage;
+                if (!tc::mbar_wait(bar(kFull0 + s), (c >> 1) & 1, abort_flag)) { fail(); break; }
+                if (!tc::mbar_wait(bar(kSReady), c & 1, abort_flag)) { fail(); break; }
+                tc::fence_after();
+                // N-accumulator: W S^T with W = W_hi + W_lo, S = S_hi + S_lo (drop lo x lo)
+                const uint32_t wh = st + S::kW, wl = st + S::kW + kTile64x128;
+                int n = 0;
+                auto mma1 = [&](uint32_t a, uint32_t bsm, uint32_t d) {
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_bf16(d, tc::smem_desc(a + (ks >> 2) * (C * 128) + (ks & 3) * 32, 16, 1024, tc::kSwizzle128),
+                                     tc::smem_desc(bsm + ks * 1024, 512, 512, tc::kSwizzle64), id1, n++ > 0);
+                };
+                mma1(wh, sSh, tD1);
+                mma1(wh, sSl, tD1);
+                mma1(wl, sSh, tD1);
+                tc::mma_commit(bar(kD1Full));
+                issued = true;
+                // output, inter-chunk part: O = Qd S^T (S hi + lo)
+                if (c >= 2 && !tc::mbar_wait(bar(kOFree0 + ob), ((c >> 1) - 1) & 1, abort_flag)) { fail(); break; }
+                tc::fence_after();
+                n = 0;
+                mma1(st + S::kQd, sSh, tO + 32 * ob);
+                mma1(st + S::kQd, sSl, tO + 32 * ob);
+                // state update: dS^T = K^T (f o N)   (A = K tile read MN-major)
+                if (!tc::mbar_wait(bar(kNReady), c & 1, abort_flag)) { fail(); break; }
+                tc::fence_after();
+                n = 0;
+                auto mma2 = [&](uint32_t a, uint32_t bsm) {
+                    for (int ks = 0; ks < 4; ++ks)
+                        tc::mma_bf16(tD2, tc::smem_desc(a + ks * 2048, C * 128, 1024, tc::kSwizzle128),
+                                     tc::smem_desc(bsm + ks * 1024, 512, 512, tc::kSwizzle64), id2, n++ > 0);
+                };
+                const uint32_t kt = st + S::kKt;
+                mma2(kt, sNh);
+                mma2(kt, sNl);
+                if (kKDA) mma2(kt + kTile64x128, sNh);
+                tc::mma_commit(bar(kD2Full));
+                // output, intra-chunk part: O += P N
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16(tO + 32 * ob, tc::smem_desc(st + S::kP + ks * 32, 16, 1024, tc::kSwizzle128),
+                                 tc::smem_desc(sN + ks * 1024, 512, 512, tc::kSwizzle64), idO2, 1u);
+                tc::mma_commit(bar(kOFull0 + ob));
+                tc::mma_commit(bar(kEmpty0 + s));
+            }
+            if (issued) {  // every MMA finished before the CTA leaves
+                tc::mma_commit(bar(kDrain));
+                tc::mbar_wait(bar(kDrain), 0, abort_flag);
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4 && warp < 8) {
+        // ------------------------------ state warpgroup ------------------------------
+        const int t = tid - 128;                 // = TMEM lane = row k of S^T
+        const int q = warp & 3;
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const bool nrow = lane < 16;            // owns row i of the M=64 N accumulator
+        const int i = 16 * q + lane;
+        float Sreg[BV];
+        if (p.h0) {
+#pragma unroll
+            for (int v = 0; v < BV; ++v) Sreg[v] = p.h0[(((size_t)b * p.Hv + h) * D + v0 + v) * D + t];
+        } else {
+#pragma unroll
+            for (int v = 0; v < BV; ++v) Sreg[v] = 0.f;
+        }
+        unsigned char* sSh = sm + S::kSh;
+        unsigned char* sSl = sm + S::kSl;
+        for (int c = 0; c < nc; ++c) {
+            const int s = c & 1;
+            const unsigned char* stg = sm + s * S::kStage;
+            if (!tc::mbar_wait(bar(kFull0 + s), (c >> 1) & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
+            // S^T rows (hi, lo) into the MMA operand tiles
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float hh[2], ll[2];
+                    tc::split_bf16(Sreg[8 * ch + 2 * u], hh[0], ll[0]);
+                    tc::split_bf16(Sreg[8 * ch + 2 * u + 1], hh[1], ll[1]);
+                    hw[u] = tc::pack_bf16(hh[0], hh[1]);
+                    lw[u] = tc::pack_bf16(ll[0], ll[1]);
+                }
+                const uint32_t off = tc::chunk_mn64(t, ch);
+                *reinterpret_cast<uint4*>(sSh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(sSl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+            const float* rec = reinterpret_cast<const float*>(stg + S::kRec_);
+            const float colf = rec[64 + t];
+            const float rowf = nrow ? rec[i] : 0.f;
+            const int Lc = reinterpret_cast<const int*>(rec)[192];
+            float uv[BV];
+            if (nrow) {
+                const float4* ur = reinterpret_cast<const float4*>(stg + S::kU + (size_t)i * BV * 4);
+#pragma unroll
+                for (int u = 0; u < BV / 4; ++u) {
+                    const float4 x = ur[u];
+                    uv[4 * u] = x.x; uv[4 * u + 1] = x.y; uv[4 * u + 2] = x.z; uv[4 * u + 3] = x.w;
+                }
+            }
+            tc::fence_proxy_async();
+            tc::fence_before();
+            tc::bar_sync(1, 128);
+            if (t == 0) tc::mbar_arrive(bar(kSReady));
+            // N = U - W S^T  ->  N' = rowf * N (hi, lo), N (bf16, masked)
+            if (!tc::mbar_wait(bar(kD1Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
+            tc::fence_after();
+            float dv[BV];
+            tc::tmem_ld32(tD1 + lane_base, dv);
+            if (nrow) {
+                const float keep = i < Lc ? 1.f : 0.f;  // rows past the chunk end
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t hw[4], lw[4], nw[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        float hh[2], ll[2], nn[2];
+#pragma unroll
+                        for (int w = 0; w < 2; ++w) {
+                            const int v = 8 * ch + 2 * u + w;
+                            const float nval = (uv[v] - dv[v]) * keep;
+                            nn[w] = nval;
+                            tc::split_bf16(nval * rowf, hh[w], ll[w]);
+                        }
+                        hw[u] = tc::pack_bf16(hh[0], hh[1]);
+                        lw[u] = tc::pack_bf16(ll[0], ll[1]);
+                        nw[u] = tc::pack_bf16(nn[0], nn[1]);
+                    }
+                    const uint32_t off = tc::chunk_mn64(i, ch);
+                    *reinterpret_cast<uint4*>(sm + S::kNh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4*>(sm + S::kNl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    *reinterpret_cast<uint4*>(sm + S::kN + off) = make_uint4(nw[0], nw[1], nw[2], nw[3]);
+                }
+            }
+            tc::fence_proxy_async();
+            tc::fence_before();
+            tc::bar_sync(1, 128);
+            if (t == 0) tc::mbar_arrive(bar(kNReady));
+            // S^T <- colf * S^T + dS^T
+            if (!tc::mbar_wait(bar(kD2Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
+            tc::fence_after();
+            tc::tmem_ld32(tD2 + lane_base, dv);
+#pragma unroll
+            for (int v = 0; v < BV; ++v) Sreg[v] = fmaf(colf, Sreg[v], dv[v]);
+            tc::fence_before();
+        }
+        if (p.hT && !*abort_flag) {
+#pragma unroll
+            for (int v = 0; v < BV; ++v) p.hT[(((size_t)b * p.Hv + h) * D + v0 + v) * D + t] = Sreg[v];
+        }
+    } else if (warp >= 8) {
+        // ------------------------------ output warpgroup ------------------------------
+        const int q = warp & 3;
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        const int i = 16 * q + lane;
+        __nv_bfloat16* op = static_cast<__nv_bfloat16*>(p.o);
+        for (int c = 0; c < nc; ++c) {
+            const int ob = c & 1;
+            if (!tc::mbar_wait(bar(kOFull0 + ob), (c >> 1) & 1, abort_flag)) fail();
+            tc::fence_after();
+            float ov[BV];
+            tc::tmem_ld32(tO + 32 * ob + lane_base, ov);
+            const int cs = bos + c * C;
+            if (lane < 16 && cs + i < eos) {
+                uint4* dst = reinterpret_cast<uint4*>(op + ((size_t)(cs + i) * p.Hv + h) * D + v0);
+#pragma unroll
+                for (int u = 0; u < BV / 8; ++u)
+                    dst[u] = make_uint4(tc::pack_bf16(p.scale * ov[8 * u], p.scale * ov[8 * u + 1]),
+                                        tc::pack_bf16(p.scale * ov[8 * u + 2], p.scale * ov[8 * u + 3]),
+                                        tc::pack_bf16(p.scale * ov[8 * u + 4], p.scale * ov[8 * u + 5]),
+                                        tc::pack_bf16(p.scale * ov[8 * u + 6], p.scale * ov[8 * u + 7]));
+            }
+            tc::fence_before();
+            tc::bar_sync(2, 128);
+            if (tid == 256) tc::mbar_arrive(bar(kOFree0 + ob));
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 2) tc::tmem_dealloc(tmem, 128);
+}
+
+// LPT order: sequence indices by decreasing length (ties by index).
+__global__ void __launch_bounds__(1024) lpt_order_kernel(const int32_t* __restrict__ cu, int N,
+                                                         int* __restrict__ order) {
+    for (int b = threadIdx.x; b < N; b += blockDim.x) {
+        const int lb = cu[b + 1] - cu[b];
+        int rank = 0;
+        if (N <= 4096) {
+            for (int j = 0; j < N; ++j) {
+                const int lj = cu[j + 1] - cu[j];
+                rank += (lj > lb) || (lj == lb && j < b);
+            }
+        } else {
+            rank = b;
+        }
+        order[rank] = b;
+    }
+}
+
+}  // namespace
+
+size_t chunk_tc_blob_bytes(int64_t max_chunks, int Hk, int Hv, bool kda) {
+    const size_t mc = (size_t)max_chunks;
+    size_t n = mc * Hv * 2 * kTile64x128;       // W
+    n += mc * Hv * NVB * kUBlock;               // U
+    n += mc * Hv * kTile64x128;                 // Qd
+    n += mc * Hv * kTile64x64;                  // P
+    n += kda ? mc * Hv * 2 * kTile64x128 : mc * Hk * kTile64x128;  // K / Kd
+    n += mc * Hv * kRec;                        // records
+    return n;
+}
+
+cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* ws, const void* q, const void* k,
+                            cudaStream_t stream) {
+    const bool kda = a.gk != nullptr;
+    TcParams p{};
+    p.q = q; p.k = k; p.v = a.v; p.g = a.g; p.gk = a.gk; p.beta = a.beta;
+    p.h0 = a.initial_state; p.o = a.o; p.hT = a.final_state; p.cu = a.cu_seqlens;
+    p.meta = reinterpret_cast<const int*>(ws + w.off_meta);
+    p.offsets = reinterpret_cast<const int*>(ws + w.off_offsets);
+    p.table = reinterpret_cast<const int4*>(ws + w.off_table);
+    p.order = reinterpret_cast<const int*>(ws + w.off_order);
+    const size_t mc = (size_t)w.max_chunks;
+    unsigned char* blob = reinterpret_cast<unsigned char*>(ws + w.off_blobs);
+    p.Wb = blob; blob += mc * a.Hv * 2 * kTile64x128;
+    p.Ub = blob; blob += mc * a.Hv * NVB * kUBlock;
+    p.Qb = blob; blob += mc * a.Hv * kTile64x128;
+    p.Pb = blob; blob += mc * a.Hv * kTile64x64;
+    p.Kb = blob; blob += kda ? mc * a.Hv * 2 * kTile64x128 : mc * a.Hk * kTile64x128;
+    p.Rb = blob;
+    p.err = device_error_word();
+    p.N = a.N; p.Hk = a.Hk; p.Hv = a.Hv; p.scale = a.scale;
+
+    {
+        KernelTimer kt("lpt_order", stream);
+        lpt_order_kernel<<<1, 1024, 0, stream>>>(a.cu_seqlens, a.N, reinterpret_cast<int*>(ws + w.off_order));
+    }
+    if (kda) {
+        const int smp = PrepSmem<true>::kTotal, smc = ChainSmem<true>::kTotal;
+        cudaFuncSetAttribute(chunk_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smp);
+        cudaFuncSetAttribute(chunk_chain_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smc);
+        {
+            KernelTimer kt("chunk_prep", stream);
+            chunk_prep_kernel<true><<<dim3((unsigned)mc, a.Hv), 128, smp, stream>>>(p);
+        }
+        KernelTimer kt("chunk_chain", stream);
+        chunk_chain_kernel<true><<<dim3(a.Hv * NVB, a.N), 384, smc, stream>>>(p);
+    } else {
+        const int smp = PrepSmem<false>::kTotal, smc = ChainSmem<false>::kTotal;
+        cudaFuncSetAttribute(chunk_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smp);
+        cudaFuncSetAttribute(chunk_chain_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smc);
+        {
+            KernelTimer kt("chunk_prep", stream);
+            chunk_prep_kernel<false><<<dim3((unsigned)mc, a.Hv), 128, smp, stream>>>(p);
+        }
+        KernelTimer kt("chunk_chain", stream);
+        chunk_chain_kernel<false><<<dim3(a.Hv * NVB, a.N), 384, smc, stream>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace gdr

@@ -59,13 +59,21 @@ struct ChunkWorkspace {
     size_t off_dl;        // fp32 [max_chunks, Hv, K]
     size_t off_h;         // fp32 [max_chunks, Hv, V, K]
     size_t off_vn;        // fp32 [T, Hv, V]
+    size_t off_order;     // int [N]: sequences by decreasing length
+    size_t off_blobs;     // tensor-core path operand images
+    bool tc;              // tensor-core path (bf16, K = V = 128)
     size_t total;
 };
 
-ChunkWorkspace chunk_workspace_layout(int N, int64_t T, int Hk, int Hv, int K, int V, int dtype,
-                                      int flags);
+ChunkWorkspace chunk_workspace_layout(int N, int64_t T, int Hk, int Hv, int K, int V, int gate_kind,
+                                      int dtype, int flags);
 
 cudaError_t launch_chunk(const ChunkArgs& a, cudaStream_t stream);
+
+// Tensor-core chunked prefill (bf16, K = V = 128): blob bytes and launcher.
+size_t chunk_tc_blob_bytes(int64_t max_chunks, int Hk, int Hv, bool channel_gate);
+cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* ws, const void* q, const void* k,
+                            cudaStream_t stream);
 
 struct GatingArgs {
     const void* a;

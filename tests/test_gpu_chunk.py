@@ -34,6 +34,7 @@ def run_gpu(case, flags=0, guarded=True):
     gdr.chunk_fwd(q, k, v, beta, case.cu_seqlens.to(dev), scale=case.scale, flags=flags, o=o.view,
                   final_state=sf.view, **ins)
     torch.cuda.synchronize()
+    assert gdr.device_status() == 0, "a bounded device wait gave up"
     assert o.guards_intact() and sf.guards_intact(), "write outside the output buffers"
     for a, b in zip((q, k, v, beta), snap):
         assert bits_equal(a, b), "an input was modified"
