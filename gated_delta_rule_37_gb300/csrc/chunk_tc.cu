@@ -34,6 +34,23 @@
 #include "launch.h"
 #include "tc.cuh"
 
+// Optional timeline trace of one chain CTA (built only with -DGDR_TRACE):
+// %globaltimer stamps per role and chunk, read back with gdr_trace_dump.
+#ifdef GDR_TRACE
+__device__ unsigned long long g_trace[16][64];
+#define GDR_TRACE_POINT(slot, c)                                                      \
+    do {                                                                              \
+        if (blockIdx.x == 0 && blockIdx.y == 0 && (c) < 64) g_trace[slot][c] = gdr::tc::globaltimer_ns(); \
+    } while (0)
+extern "C" __attribute__((visibility("default"))) int gdr_trace_dump(unsigned long long* host) {
+    return (int)cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace));
+}
+#else
+#define GDR_TRACE_POINT(slot, c) \
+    do {                         \
+    } while (0)
+#endif
+
 namespace gdr {
 namespace {
 
@@ -106,58 +123,73 @@ __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict_
         const int nblk = 4 - d;
         for (int e = tid; e < nblk * 256; e += 128) {
             const int j = e >> 8, i = j + d, r = (e >> 4) & 15, c = e & 15;
-            float s = 0.f;
-            for (int m = 16 * j; m < 16 * i; ++m) s = fmaf(A[(16 * i + r) * LDA + m], Tm[m * LDA + 16 * j + c], s);
-            Z[e] = s;
+            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+            const float* arow = A + (16 * i + r) * LDA;
+            const float* tcol = Tm + 16 * j + c;
+            for (int m = 16 * j; m < 16 * i; m += 4) {
+                s0 = fmaf(arow[m], tcol[m * LDA], s0);
+                s1 = fmaf(arow[m + 1], tcol[(m + 1) * LDA], s1);
+                s2 = fmaf(arow[m + 2], tcol[(m + 2) * LDA], s2);
+                s3 = fmaf(arow[m + 3], tcol[(m + 3) * LDA], s3);
+            }
+            Z[e] = (s0 + s1) + (s2 + s3);
         }
         __syncthreads();
         for (int e = tid; e < nblk * 256; e += 128) {
             const int j = e >> 8, i = j + d, r = (e >> 4) & 15, c = e & 15;
-            float s = 0.f;
+            float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-            for (int m = 0; m < 16; ++m) s = fmaf(Tm[(16 * i + r) * LDA + 16 * i + m], Z[(j << 8) + m * 16 + c], s);
-            Tm[(16 * i + r) * LDA + 16 * j + c] = -s;
+            for (int m = 0; m < 16; m += 2) {
+                s0 = fmaf(Tm[(16 * i + r) * LDA + 16 * i + m], Z[(j << 8) + m * 16 + c], s0);
+                s1 = fmaf(Tm[(16 * i + r) * LDA + 16 * i + m + 1], Z[(j << 8) + (m + 1) * 16 + c], s1);
+            }
+            Tm[(16 * i + r) * LDA + 16 * j + c] = -(s0 + s1);
         }
         __syncthreads();
     }
 }
 
-// Stage a [64][128] bf16 token tile (rows >= L zero) into a k128 smem tile.
-__device__ __forceinline__ void stage_rows(unsigned char* tile, const __nv_bfloat16* src, size_t row_stride,
-                                           int L, int tid) {
+// Stage a [64][128] bf16 token tile (rows >= L zero-filled) into a k128 smem
+// tile with cp.async: all 16-byte pieces are in flight at once.
+__device__ __forceinline__ void stage_rows_async(unsigned char* tile, const __nv_bfloat16* src, size_t row_stride,
+                                                 int L, int tid) {
     for (int e = tid; e < C * 16; e += 128) {
         const int row = e >> 4, ch = e & 15;
-        uint4 val = make_uint4(0, 0, 0, 0);
-        if (row < L) val = *reinterpret_cast<const uint4*>(src + (size_t)row * row_stride + ch * 8);
-        *reinterpret_cast<uint4*>(tile + tc::chunk_k128(row, ch, C)) = val;
+        const __nv_bfloat16* g = src + (size_t)(row < L ? row : 0) * row_stride + ch * 8;
+        const uint32_t dst = tc::smem_u32(tile + tc::chunk_k128(row, ch, C));
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(g), "r"(row < L ? 16 : 0)
+                     : "memory");
     }
 }
 
 // ---------------------------------------------------------------------------
 // prep kernel
 // ---------------------------------------------------------------------------
+// Shared memory: the Q tile and the fp32 A matrix are dead once the solve has
+// started, and the four split T tiles (32 KB) reuse their space.
 template <bool kKDA>
 struct PrepSmem {
     static constexpr uint32_t kK = 0;                        // K tile 16 KB
-    static constexpr uint32_t kQ = kK + kTile64x128;         // Q tile
-    static constexpr uint32_t kV = kQ + kTile64x128;         // V tile
-    static constexpr uint32_t kT1h = kV + kTile64x128;       // T' hi  [64][64]
-    static constexpr uint32_t kT1l = kT1h + kTile64x64;      // T' lo
-    static constexpr uint32_t kT2h = kT1l + kTile64x64;      // T'' hi
-    static constexpr uint32_t kT2l = kT2h + kTile64x64;      // T'' lo
-    static constexpr uint32_t kKgh = kT2l + kTile64x64;      // K o e^Gam hi (channel gate)
-    static constexpr uint32_t kKgl = kKgh + (kKDA ? kTile64x128 : 0);
-    static constexpr uint32_t kA = kKgl + (kKDA ? kTile64x128 : 0);   // fp32 [64][65]
-    static constexpr uint32_t kTm = kA + C * LDA * 4;                   // fp32 [64][65]
+    static constexpr uint32_t kV = kK + kTile64x128;         // V tile
+    static constexpr uint32_t kQ = kV + kTile64x128;         // Q tile (later T' hi / lo)
+    static constexpr uint32_t kA = kQ + kTile64x128;         // fp32 [64][65] (later T'' hi / lo)
+    static constexpr uint32_t kT1h = kQ;
+    static constexpr uint32_t kT1l = kQ + kTile64x64;
+    static constexpr uint32_t kT2h = kQ + 2 * kTile64x64;
+    static constexpr uint32_t kT2l = kQ + 3 * kTile64x64;
+    static constexpr uint32_t kTm = (kA + C * LDA * 4 + 1023) & ~1023u;  // fp32 [64][65]
     static constexpr uint32_t kZ = kTm + C * LDA * 4;                   // fp32 [3][256]
-    static constexpr uint32_t kGam = kZ + 3 * 256 * 4;                  // fp32 [64][128] or [64]
+    static constexpr uint32_t kKgh = (kZ + 3 * 256 * 4 + 1023) & ~1023u;  // K o e^Gam hi (channel gate)
+    static constexpr uint32_t kKgl = kKgh + (kKDA ? kTile64x128 : 0);
+    static constexpr uint32_t kGam = kKgl + (kKDA ? kTile64x128 : 0);    // fp32 [64][128] or [64]
     static constexpr uint32_t kBeta = kGam + (kKDA ? C * D * 4 : C * 4);
     static constexpr uint32_t kBar = kBeta + C * 4;
     static constexpr uint32_t kTotal = kBar + 64 + 1024;  // + alignment slack
+    static_assert(kT2l + kTile64x64 <= kTm, "T tiles overlap Tm");
 };
 
 template <bool kKDA>
-__global__ void __launch_bounds__(128, 1) chunk_prep_kernel(TcParams p) {
+__global__ void __launch_bounds__(128, kKDA ? 1 : 2) chunk_prep_kernel(TcParams p) {
     using S = PrepSmem<kKDA>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -183,31 +215,44 @@ __global__ void __launch_bounds__(128, 1) chunk_prep_kernel(TcParams p) {
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::kBar + 24);
     const uint32_t bar0 = tc::smem_u32(&bars[0]);
 
+    // ---- stage K, Q, V rows (cp.async), gates, beta ----------------------------
+    stage_rows_async(sm + S::kK, kp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
+    stage_rows_async(sm + S::kQ, qp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
+    stage_rows_async(sm + S::kV, vp + ((size_t)start * p.Hv + h) * D, (size_t)p.Hv * D, L, tid);
+    asm volatile("cp.async.commit_group;" ::: "memory");
     if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), 256);
     if (tid == 0) {
         tc::mbar_init(bar0, 1);
         *abort_flag = 0;
         tc::mbar_fence_init();
     }
-    // stage K, Q, V rows of this chunk (token-major rows, head kh / h)
-    stage_rows(sm + S::kK, kp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
-    stage_rows(sm + S::kQ, qp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
-    stage_rows(sm + S::kV, vp + ((size_t)start * p.Hv + h) * D, (size_t)p.Hv * D, L, tid);
     if (tid < C) bet[tid] = tid < L ? to_f(bp[((size_t)start + tid) * p.Hv + h]) : 0.f;
     if (kKDA) {
-        // per-channel inclusive cumsum in token order (thread = channel)
+        // per-channel inclusive cumsum in token order (thread = channel); all
+        // 64 loads are issued before the dependent adds
+        const float* __restrict__ gk = p.gk + ((size_t)start * p.Hv + h) * D + tid;
+        float x[C];
+#pragma unroll
+        for (int i = 0; i < C; ++i) x[i] = i < L ? __ldg(gk + (size_t)i * p.Hv * D) : 0.f;
         float acc = 0.f;
+#pragma unroll
         for (int i = 0; i < C; ++i) {
-            if (i < L) acc += p.gk[(((size_t)start + i) * p.Hv + h) * D + tid];
+            acc += x[i];
             gam[i * D + tid] = acc;
         }
-    } else if (tid == 0) {
-        float acc = 0.f;
-        for (int i = 0; i < C; ++i) {
-            if (i < L) acc += p.g[((size_t)start + i) * p.Hv + h];
-            gam[i] = acc;
+    } else if (warp < 2) {
+        // scalar gate: inclusive scan over 64 tokens with two warps
+        float x = tid < L ? __ldg(p.g + ((size_t)start + tid) * p.Hv + h) : 0.f;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, off);
+            if (lane >= off) x += y;
         }
+        gam[tid] = x;
     }
+    __syncthreads();
+    if (!kKDA && warp == 1) gam[tid] += gam[31];
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
     tc::fence_proxy_async();
     tc::fence_before();
     __syncthreads();
@@ -217,24 +262,81 @@ __global__ void __launch_bounds__(128, 1) chunk_prep_kernel(TcParams p) {
     auto gm = [&](int i, int c) -> float { return kKDA ? gam[i * D + c] : gam[i]; };
     const float* gl = kKDA ? gam + (L - 1) * D : gam + (L - 1);
 
-    // --- A (strictly lower) and P (lower incl. diagonal) ---------------------
+    // ---- G = K K^T and Q K^T on the tensor cores (scalar gate) -------------------
+    if (!kKDA && tid == 0) {
+        constexpr uint32_t id = tc::idesc_bf16(64, 64, false, false);
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * (C * 128) + (ks & 3) * 32;
+            tc::mma_bf16(tmem, tc::smem_desc(sK + off, 16, 1024, tc::kSwizzle128),
+                         tc::smem_desc(sK + off, 16, 1024, tc::kSwizzle128), id, ks > 0);
+        }
+        for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * (C * 128) + (ks & 3) * 32;
+            tc::mma_bf16(tmem + 64, tc::smem_desc(sQ + off, 16, 1024, tc::kSwizzle128),
+                         tc::smem_desc(sK + off, 16, 1024, tc::kSwizzle128), id, ks > 0);
+        }
+        tc::mma_commit(bar0);
+    }
+    __syncwarp();
+
+    // ---- while those run: Qd blob, K / Kd blob, decay record -----------------------
+    {
+        const __nv_bfloat16* Qt = reinterpret_cast<const __nv_bfloat16*>(sm + S::kQ);
+        unsigned char* Qdst = p.Qb + ((size_t)chunk * p.Hv + h) * kTile64x128;
+        for (int e = tid; e < C * 16; e += 128) {
+            const int i = e >> 4, ch = e & 15;
+            const uint32_t off = tc::chunk_k128(i, ch, C);
+            const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kQ + off);
+            const __nv_bfloat16* qv = reinterpret_cast<const __nv_bfloat16*>(&raw);
+            uint32_t w4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = ch * 8 + 2 * u;
+                w4[u] = tc::pack_bf16(__bfloat162float(qv[2 * u]) * __expf(gm(i, c)),
+                                      __bfloat162float(qv[2 * u + 1]) * __expf(gm(i, c + 1)));
+            }
+            *reinterpret_cast<uint4*>(Qdst + off) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+        }
+        (void)Qt;
+        if (!kKDA) {
+            if (h % grp == 0) {
+                unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hk + kh) * kTile64x128;
+                for (int e = tid; e < (int)(kTile64x128 / 16); e += 128)
+                    reinterpret_cast<uint4*>(Kdst)[e] = reinterpret_cast<const uint4*>(sm + S::kK)[e];
+            }
+        } else {
+            unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hv + h) * 2 * kTile64x128;
+            for (int e = tid; e < C * 16; e += 128) {
+                const int i = e >> 4, ch = e & 15;
+                const uint32_t off = tc::chunk_k128(i, ch, C);
+                const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kK + off);
+                const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&raw);
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    float hh[2], ll[2];
+#pragma unroll
+                    for (int w = 0; w < 2; ++w) {
+                        const int c = ch * 8 + 2 * u + w;
+                        const float x = i < L ? __bfloat162float(kv[2 * u + w]) * __expf(gl[c] - gam[i * D + c]) : 0.f;
+                        tc::split_bf16(x, hh[w], ll[w]);
+                    }
+                    hw[u] = tc::pack_bf16(hh[0], hh[1]);
+                    lw[u] = tc::pack_bf16(ll[0], ll[1]);
+                }
+                *reinterpret_cast<uint4*>(Kdst + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(Kdst + kTile64x128 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+        }
+        float* rec = reinterpret_cast<float*>(p.Rb + ((size_t)chunk * p.Hv + h) * kRec);
+        if (tid < C) rec[tid] = tid < L ? (kKDA ? 1.f : __expf(gl[0] - gam[tid])) : 0.f;
+        rec[64 + tid] = __expf(kKDA ? gl[tid] : gl[0]);
+        if (tid == 0) reinterpret_cast<int*>(rec)[192] = L;
+    }
+
+    // ---- A (strictly lower) and P (lower incl. diagonal) -------------------------
     unsigned char* Pdst = p.Pb + ((size_t)chunk * p.Hv + h) * kTile64x64;
     if (!kKDA) {
-        if (tid == 0) {
-            constexpr uint32_t id = tc::idesc_bf16(64, 64, false, false);
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t off = (ks >> 2) * (C * 128) + (ks & 3) * 32;
-                tc::mma_bf16(tmem, tc::smem_desc(sK + off, 16, 1024, tc::kSwizzle128),
-                             tc::smem_desc(sK + off, 16, 1024, tc::kSwizzle128), id, ks > 0);
-            }
-            for (int ks = 0; ks < 8; ++ks) {
-                const uint32_t off = (ks >> 2) * (C * 128) + (ks & 3) * 32;
-                tc::mma_bf16(tmem + 64, tc::smem_desc(sQ + off, 16, 1024, tc::kSwizzle128),
-                             tc::smem_desc(sK + off, 16, 1024, tc::kSwizzle128), id, ks > 0);
-            }
-            tc::mma_commit(bar0);
-        }
-        __syncwarp();
         if (!tc::mbar_wait(bar0, 0, abort_flag)) raise_error(p, 1u);
         tc::fence_after();
         const int i = 16 * (warp & 3) + (lane & 15);
@@ -280,15 +382,36 @@ __global__ void __launch_bounds__(128, 1) chunk_prep_kernel(TcParams p) {
             As[i * LDA + j] = (j < i) ? bet[i] * a : 0.f;
             reinterpret_cast<__nv_bfloat16*>(Pdst)[tc::off_k128(i, j, C) >> 1] = __float2bfloat16_rn(pv);
         }
+        // K o e^{Gam} as hi / lo for W
+        for (int e = tid; e < C * 16; e += 128) {
+            const int i = e >> 4, ch = e & 15;
+            const uint32_t off = tc::chunk_k128(i, ch, C);
+            const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kK + off);
+            const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&raw);
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                float hh[2], ll[2];
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    const int c = ch * 8 + 2 * u + w;
+                    tc::split_bf16(__bfloat162float(kv[2 * u + w]) * __expf(gam[i * D + c]), hh[w], ll[w]);
+                }
+                hw[u] = tc::pack_bf16(hh[0], hh[1]);
+                lw[u] = tc::pack_bf16(ll[0], ll[1]);
+            }
+            *reinterpret_cast<uint4*>(sm + S::kKgh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(sm + S::kKgl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
     }
     tc::fence_before();
     __syncthreads();
 
-    // --- Tm = (I + A)^{-1} ------------------------------------------------------
+    // ---- Tm = (I + A)^{-1} -----------------------------------------------------------
     solve_unit_lower(As, Tm, Z, tid);
 
-    // --- split operands: T' = Tm diag(beta e^{gam}) (scalar gate) / Tm diag(beta);
-    //     T'' = Tm diag(beta); channel gate also K o e^{Gam}.
+    // ---- split operands: T' = Tm diag(beta e^{gam}) (scalar gate) or Tm diag(beta);
+    //      T'' = Tm diag(beta).  Written over the (dead) Q tile and A matrix.
     for (int e = tid; e < C * 8; e += 128) {
         const int i = e >> 3, ch = e & 7;
         uint32_t h1[4], l1[4], h2[4], l2[4];
@@ -318,32 +441,10 @@ __global__ void __launch_bounds__(128, 1) chunk_prep_kernel(TcParams p) {
         *reinterpret_cast<uint4*>(sm + S::kT2h + off) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
         *reinterpret_cast<uint4*>(sm + S::kT2l + off) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
     }
-    if (kKDA) {
-        const __nv_bfloat16* Kt = reinterpret_cast<const __nv_bfloat16*>(sm + S::kK);
-        for (int e = tid; e < C * 16; e += 128) {
-            const int i = e >> 4, ch = e & 15;
-            uint32_t hw[4], lw[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                float hh[2], ll[2];
-#pragma unroll
-                for (int w = 0; w < 2; ++w) {
-                    const int c = ch * 8 + 2 * u + w;
-                    const float x = __bfloat162float(Kt[tc::off_k128(i, c, C) >> 1]) * __expf(gam[i * D + c]);
-                    tc::split_bf16(x, hh[w], ll[w]);
-                }
-                hw[u] = tc::pack_bf16(hh[0], hh[1]);
-                lw[u] = tc::pack_bf16(ll[0], ll[1]);
-            }
-            const uint32_t off = tc::chunk_k128(i, ch, C);
-            *reinterpret_cast<uint4*>(sm + S::kKgh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(sm + S::kKgl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        }
-    }
     tc::fence_proxy_async();
     __syncthreads();
 
-    // --- W = T' K (or T'' (K o e^Gam)), U = T'' V  --------------------------------
+    // ---- W = T' K (or T'' (K o e^Gam)), U = T'' V ----------------------------------------
     if (tid == 0) {
         tc::fence_after();
         constexpr uint32_t id = tc::idesc_bf16(64, 128, false, true);
@@ -369,64 +470,7 @@ __global__ void __launch_bounds__(128, 1) chunk_prep_kernel(TcParams p) {
     }
     __syncwarp();
 
-    // --- while the MMAs run: Qd blob, K / Kd blobs, decay record ----------------
-    {
-        const __nv_bfloat16* Qt = reinterpret_cast<const __nv_bfloat16*>(sm + S::kQ);
-        unsigned char* Qdst = p.Qb + ((size_t)chunk * p.Hv + h) * kTile64x128;
-        for (int e = tid; e < C * 16; e += 128) {
-            const int i = e >> 4, ch = e & 15;
-            const uint32_t off = tc::chunk_k128(i, ch, C);
-            uint32_t w4[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                float x[2];
-#pragma unroll
-                for (int w = 0; w < 2; ++w) {
-                    const int c = ch * 8 + 2 * u + w;
-                    x[w] = __bfloat162float(Qt[(off >> 1) + 2 * u + w]) * __expf(gm(i, c));
-                }
-                w4[u] = tc::pack_bf16(x[0], x[1]);
-            }
-            *reinterpret_cast<uint4*>(Qdst + off) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-        }
-        if (!kKDA) {
-            if (h % grp == 0) {
-                unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hk + kh) * kTile64x128;
-                for (int e = tid; e < (int)(kTile64x128 / 16); e += 128)
-                    reinterpret_cast<uint4*>(Kdst)[e] = reinterpret_cast<const uint4*>(sm + S::kK)[e];
-            }
-        } else {
-            const __nv_bfloat16* Kt = reinterpret_cast<const __nv_bfloat16*>(sm + S::kK);
-            unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hv + h) * 2 * kTile64x128;
-            for (int e = tid; e < C * 16; e += 128) {
-                const int i = e >> 4, ch = e & 15;
-                const uint32_t off = tc::chunk_k128(i, ch, C);
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    float hh[2], ll[2];
-#pragma unroll
-                    for (int w = 0; w < 2; ++w) {
-                        const int c = ch * 8 + 2 * u + w;
-                        const float x = i < L ? __bfloat162float(Kt[(off >> 1) + 2 * u + w]) *
-                                                    __expf(gl[c] - gam[i * D + c])
-                                              : 0.f;
-                        tc::split_bf16(x, hh[w], ll[w]);
-                    }
-                    hw[u] = tc::pack_bf16(hh[0], hh[1]);
-                    lw[u] = tc::pack_bf16(ll[0], ll[1]);
-                }
-                *reinterpret_cast<uint4*>(Kdst + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4*>(Kdst + kTile64x128 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            }
-        }
-        float* rec = reinterpret_cast<float*>(p.Rb + ((size_t)chunk * p.Hv + h) * kRec);
-        if (tid < C) rec[tid] = tid < L ? (kKDA ? 1.f : __expf(gl[0] - gam[tid])) : 0.f;
-        rec[64 + tid] = __expf(kKDA ? gl[tid] : gl[0]);
-        if (tid == 0) reinterpret_cast<int*>(rec)[192] = L;
-    }
-
-    // --- W, U out of TMEM into their blobs -------------------------------------------
+    // ---- W, U out of TMEM into their blobs ------------------------------------------------
     // second use of bar0 (the first, K K^T / Q K^T, exists only for the scalar gate)
     if (!tc::mbar_wait(bar0, kKDA ? 0 : 1, abort_flag)) raise_error(p, 1u);
     tc::fence_after();
@@ -540,6 +584,7 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
             for (int c = 0; c < nc && !*abort_flag; ++c) {
                 const int s = c & 1;
                 if (c >= 2 && !tc::mbar_wait(bar(kEmpty0 + s), ((c >> 1) - 1) & 1, abort_flag)) { fail(); break; }
+                GDR_TRACE_POINT(0, c);
                 const size_t gc = (size_t)c0 + c;
                 const uint32_t st = base + s * S::kStage;
                 const uint32_t fb = bar(kFull0 + s);
@@ -551,6 +596,7 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
                 tc::bulk_g2s(st + S::kP, p.Pb + (gc * p.Hv + h) * kTile64x64, kTile64x64, fb);
                 tc::bulk_g2s(st + S::kU, p.Ub + ((gc * p.Hv + h) * NVB + vb) * kUBlock, kUBlock, fb);
                 tc::bulk_g2s(st + S::kRec_, p.Rb + (gc * p.Hv + h) * kRec, kRec, fb);
+                GDR_TRACE_POINT(1, c);
             }
             // drain: wait for the copies of the last (up to) two stages to land
             for (int c = (nc > 2 ? nc - 2 : 0); c < nc; ++c)
@@ -570,7 +616,9 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
                 const int s = c & 1, ob = c & 1;
                 const uint32_t st = base + s * S::kStage;
                 if (!tc::mbar_wait(bar(kFull0 + s), (c >> 1) & 1, abort_flag)) { fail(); break; }
+                GDR_TRACE_POINT(2, c);
                 if (!tc::mbar_wait(bar(kSReady), c & 1, abort_flag)) { fail(); break; }
+                GDR_TRACE_POINT(3, c);
                 tc::fence_after();
                 // N-accumulator: W S^T with W = W_hi + W_lo, S = S_hi + S_lo (drop lo x lo)
                 const uint32_t wh = st + S::kW, wl = st + S::kW + kTile64x128;
@@ -584,6 +632,7 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
                 mma1(wh, sSl, tD1);
                 mma1(wl, sSh, tD1);
                 tc::mma_commit(bar(kD1Full));
+                GDR_TRACE_POINT(4, c);
                 issued = true;
                 // output, inter-chunk part: O = Qd S^T (S hi + lo)
                 if (c >= 2 && !tc::mbar_wait(bar(kOFree0 + ob), ((c >> 1) - 1) & 1, abort_flag)) { fail(); break; }
@@ -593,6 +642,7 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
                 mma1(st + S::kQd, sSl, tO + 32 * ob);
                 // state update: dS^T = K^T (f o N)   (A = K tile read MN-major)
                 if (!tc::mbar_wait(bar(kNReady), c & 1, abort_flag)) { fail(); break; }
+                GDR_TRACE_POINT(5, c);
                 tc::fence_after();
                 n = 0;
                 auto mma2 = [&](uint32_t a, uint32_t bsm) {
@@ -611,6 +661,7 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
                                  tc::smem_desc(sN + ks * 1024, 512, 512, tc::kSwizzle64), idO2, 1u);
                 tc::mma_commit(bar(kOFull0 + ob));
                 tc::mma_commit(bar(kEmpty0 + s));
+                GDR_TRACE_POINT(6, c);
             }
             if (issued) {  // every MMA finished before the CTA leaves
                 tc::mma_commit(bar(kDrain));
@@ -639,6 +690,7 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
             const int s = c & 1;
             const unsigned char* stg = sm + s * S::kStage;
             if (!tc::mbar_wait(bar(kFull0 + s), (c >> 1) & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
+            if (t == 0) GDR_TRACE_POINT(7, c);
             // S^T rows (hi, lo) into the MMA operand tiles
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
@@ -671,9 +723,13 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
             tc::fence_proxy_async();
             tc::fence_before();
             tc::bar_sync(1, 128);
-            if (t == 0) tc::mbar_arrive(bar(kSReady));
+            if (t == 0) {
+                GDR_TRACE_POINT(8, c);
+                tc::mbar_arrive(bar(kSReady));
+            }
             // N = U - W S^T  ->  N' = rowf * N (hi, lo), N (bf16, masked)
             if (!tc::mbar_wait(bar(kD1Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
+            if (t == 0) GDR_TRACE_POINT(9, c);
             tc::fence_after();
             float dv[BV];
             tc::tmem_ld32(tD1 + lane_base, dv);
@@ -705,13 +761,18 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
             tc::fence_proxy_async();
             tc::fence_before();
             tc::bar_sync(1, 128);
-            if (t == 0) tc::mbar_arrive(bar(kNReady));
+            if (t == 0) {
+                GDR_TRACE_POINT(10, c);
+                tc::mbar_arrive(bar(kNReady));
+            }
             // S^T <- colf * S^T + dS^T
             if (!tc::mbar_wait(bar(kD2Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
+            if (t == 0) GDR_TRACE_POINT(11, c);
             tc::fence_after();
             tc::tmem_ld32(tD2 + lane_base, dv);
 #pragma unroll
             for (int v = 0; v < BV; ++v) Sreg[v] = fmaf(colf, Sreg[v], dv[v]);
+            if (t == 0) GDR_TRACE_POINT(12, c);
             tc::fence_before();
         }
         if (p.hT && !*abort_flag) {
@@ -727,6 +788,7 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
         for (int c = 0; c < nc; ++c) {
             const int ob = c & 1;
             if (!tc::mbar_wait(bar(kOFull0 + ob), (c >> 1) & 1, abort_flag)) fail();
+            if (tid == 256) GDR_TRACE_POINT(13, c);
             tc::fence_after();
             float ov[BV];
             tc::tmem_ld32(tO + 32 * ob + lane_base, ov);
@@ -742,7 +804,10 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
             }
             tc::fence_before();
             tc::bar_sync(2, 128);
-            if (tid == 256) tc::mbar_arrive(bar(kOFree0 + ob));
+            if (tid == 256) {
+                GDR_TRACE_POINT(14, c);
+                tc::mbar_arrive(bar(kOFree0 + ob));
+            }
         }
     }
     tc::fence_before();
