@@ -37,10 +37,14 @@
 // Optional timeline trace of one chain CTA (built only with -DGDR_TRACE):
 // %globaltimer stamps per role and chunk, read back with gdr_trace_dump.
 #ifdef GDR_TRACE
-__device__ unsigned long long g_trace[16][64];
+__device__ unsigned long long g_trace[24][64];
 #define GDR_TRACE_POINT(slot, c)                                                      \
     do {                                                                              \
-        if (blockIdx.x == 0 && blockIdx.y == 0 && (c) < 64) g_trace[slot][c] = gdr::tc::globaltimer_ns(); \
+        if (blockIdx.x == 0 && blockIdx.y == 0 && (c) < 64) g_trace[slot][c] = clock64(); \
+    } while (0)
+#define GDR_TRACE_PREP(phase)                                                                      \
+    do {                                                                                           \
+        if (blockIdx.x == 7 && blockIdx.y == 0 && threadIdx.x == 0) g_trace[23][phase] = clock64(); \
     } while (0)
 extern "C" __attribute__((visibility("default"))) int gdr_trace_dump(unsigned long long* host) {
     return (int)cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace));
@@ -48,6 +52,9 @@ extern "C" __attribute__((visibility("default"))) int gdr_trace_dump(unsigned lo
 #else
 #define GDR_TRACE_POINT(slot, c) \
     do {                         \
+    } while (0)
+#define GDR_TRACE_PREP(phase) \
+    do {                      \
     } while (0)
 #endif
 
@@ -215,6 +222,7 @@ __global__ void __launch_bounds__(128, kKDA ? 1 : 2) chunk_prep_kernel(TcParams 
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::kBar + 24);
     const uint32_t bar0 = tc::smem_u32(&bars[0]);
 
+    GDR_TRACE_PREP(0);
     // ---- stage K, Q, V rows (cp.async), gates, beta ----------------------------
     stage_rows_async(sm + S::kK, kp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
     stage_rows_async(sm + S::kQ, qp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
@@ -259,6 +267,7 @@ __global__ void __launch_bounds__(128, kKDA ? 1 : 2) chunk_prep_kernel(TcParams 
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
     const uint32_t sK = tc::smem_u32(sm + S::kK), sQ = tc::smem_u32(sm + S::kQ), sV = tc::smem_u32(sm + S::kV);
+    GDR_TRACE_PREP(1);
     auto gm = [&](int i, int c) -> float { return kKDA ? gam[i * D + c] : gam[i]; };
     const float* gl = kKDA ? gam + (L - 1) * D : gam + (L - 1);
 
@@ -334,6 +343,7 @@ __global__ void __launch_bounds__(128, kKDA ? 1 : 2) chunk_prep_kernel(TcParams 
         if (tid == 0) reinterpret_cast<int*>(rec)[192] = L;
     }
 
+    GDR_TRACE_PREP(2);
     // ---- A (strictly lower) and P (lower incl. diagonal) -------------------------
     unsigned char* Pdst = p.Pb + ((size_t)chunk * p.Hv + h) * kTile64x64;
     if (!kKDA) {
@@ -407,9 +417,11 @@ __global__ void __launch_bounds__(128, kKDA ? 1 : 2) chunk_prep_kernel(TcParams 
     tc::fence_before();
     __syncthreads();
 
+    GDR_TRACE_PREP(3);
     // ---- Tm = (I + A)^{-1} -----------------------------------------------------------
     solve_unit_lower(As, Tm, Z, tid);
 
+    GDR_TRACE_PREP(4);
     // ---- split operands: T' = Tm diag(beta e^{gam}) (scalar gate) or Tm diag(beta);
     //      T'' = Tm diag(beta).  Written over the (dead) Q tile and A matrix.
     for (int e = tid; e < C * 8; e += 128) {
@@ -444,6 +456,7 @@ __global__ void __launch_bounds__(128, kKDA ? 1 : 2) chunk_prep_kernel(TcParams 
     tc::fence_proxy_async();
     __syncthreads();
 
+    GDR_TRACE_PREP(5);
     // ---- W = T' K (or T'' (K o e^Gam)), U = T'' V ----------------------------------------
     if (tid == 0) {
         tc::fence_after();
@@ -470,6 +483,7 @@ __global__ void __launch_bounds__(128, kKDA ? 1 : 2) chunk_prep_kernel(TcParams 
     }
     __syncwarp();
 
+    GDR_TRACE_PREP(6);
     // ---- W, U out of TMEM into their blobs ------------------------------------------------
     // second use of bar0 (the first, K K^T / Q K^T, exists only for the scalar gate)
     if (!tc::mbar_wait(bar0, kKDA ? 0 : 1, abort_flag)) raise_error(p, 1u);
@@ -507,9 +521,11 @@ __global__ void __launch_bounds__(128, kKDA ? 1 : 2) chunk_prep_kernel(TcParams 
             }
         }
     }
+    GDR_TRACE_PREP(7);
     tc::fence_before();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
+    GDR_TRACE_PREP(8);
 }
 
 // ---------------------------------------------------------------------------
@@ -527,10 +543,14 @@ struct ChainSmem {
     static constexpr uint32_t kRec_ = kU + kUBlock;
     static constexpr uint32_t kStage = kRec_ + kRec;
     static constexpr uint32_t kStageTx = kStage;  // bytes landed per stage
-    // resident tiles
-    static constexpr uint32_t kSh = 2 * kStage;              // S^T hi [128][32] mn64
+    // resident tiles.  The scalar gate double-buffers the state operand so the
+    // output MMAs of chunk c can run after the state update of chunk c; the
+    // channel gate (larger stages) keeps one buffer and issues them earlier.
+    static constexpr int kSBufs = kKDA ? 1 : 2;
+    static constexpr uint32_t kSh = 2 * kStage;              // S^T hi [128][32] mn64 (x kSBufs)
     static constexpr uint32_t kSl = kSh + D * BV * 2;        // S^T lo
-    static constexpr uint32_t kNh = kSl + D * BV * 2;        // N' hi [64][32] mn64
+    static constexpr uint32_t kSBuf = 2 * D * BV * 2;        // bytes per state buffer (hi + lo)
+    static constexpr uint32_t kNh = kSh + kSBufs * kSBuf;    // N' hi [64][32] mn64
     static constexpr uint32_t kNl = kNh + C * BV * 2;        // N' lo
     static constexpr uint32_t kN = kNl + C * BV * 2;         // N (bf16) for the output
     static constexpr uint32_t kBar = kN + C * BV * 2;
@@ -539,8 +559,13 @@ struct ChainSmem {
 
 enum ChainBar {
     kFull0 = 0, kFull1, kEmpty0, kEmpty1, kSReady, kD1Full, kNReady, kD2Full, kOFull0, kOFull1, kOFree0, kOFree1,
-    kDrain, kNumBars
+    kDrainA, kDrainB, kDrainC, kNumBars
 };
+// Arrival counts: the N accumulator is committed by issuers A and B, a stage is
+// released by all three issuers, everything else by one arrival.
+__device__ __forceinline__ uint32_t chain_bar_count(int i) {
+    return i == kD1Full ? 2u : (i == kEmpty0 || i == kEmpty1) ? 3u : 1u;
+}
 
 template <bool kKDA>
 __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
@@ -561,9 +586,9 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::kBar + 8 * kNumBars + 8);
     auto bar = [&](int i) { return tc::smem_u32(&bars[i]); };
 
-    if (warp == 2) tc::tmem_alloc(tc::smem_u32(tmem_slot), 128);
+    if (warp == 2) tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
     if (tid == 0) {
-        for (int i = 0; i < kNumBars; ++i) tc::mbar_init(bar(i), 1);
+        for (int i = 0; i < kNumBars; ++i) tc::mbar_init(bar(i), chain_bar_count(i));
         *abort_flag = 0;
         tc::mbar_fence_init();
     }
@@ -571,7 +596,11 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t tD1 = tmem, tD2 = tmem + 32, tO = tmem + 64;  // O double-buffered: +0 / +32
+    // Accumulators: the hi and lo split terms of the state (or of N') sit side
+    // by side along N, so one N = 64 MMA forms two split products; columns v
+    // and 32 + v are summed when read.  D1a / D1b are the two halves of the N
+    // accumulator written by different issuing threads.
+    const uint32_t tD1 = tmem, tD1b = tmem + 64, tD2 = tmem + 128, tO = tmem + 256;  // O: +0 / +64
     const uint32_t base = tc::smem_u32(sm);
     auto fail = [&]() {
         *abort_flag = 1;
@@ -603,69 +632,73 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
                 tc::mbar_wait_copies(bar(kFull0 + (c & 1)), (c >> 1) & 1);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------ MMA issuer ------------------------------
+    } else if (warp >= 1 && warp <= 3) {
+        // ------------------------------ MMA issuers ------------------------------
+        // A single thread issues a tcgen05.mma about every 60 cycles, well
+        // below what the tensor pipe sustains for these shapes, so the work is
+        // spread over three issuing threads, each committing its own MMAs:
+        //   A (warp 1): N partial W_hi [S_hi | S_lo], then dS = K^T [N'_hi | N'_lo]
+        //   B (warp 2): N partial W_lo S_hi            (in parallel with A)
+        //   C (warp 3): output O = Qd [S_hi | S_lo] + P N (off the state chain)
+        // Descriptors are built once per tile; a k-step adds its byte offset / 16
+        // to the start-address field (tiles sit below 256 KB, so no carry).
         if (lane == 0) {
-            const uint32_t id1 = tc::idesc_bf16(64, BV, false, true);   // N = W S^T, O = Qd S^T
-            const uint32_t id2 = tc::idesc_bf16(128, BV, true, true);   // dS = K^T N'
-            const uint32_t idO2 = tc::idesc_bf16(64, BV, false, true);  // O += P N
-            const uint32_t sSh = base + S::kSh, sSl = base + S::kSl;
-            const uint32_t sNh = base + S::kNh, sNl = base + S::kNl, sN = base + S::kN;
+            const int role = warp;  // 1 = A, 2 = B, 3 = C
+            const uint32_t id64 = tc::idesc_bf16(64, 2 * BV, false, true);   // W_hi [S_hi|S_lo], Qd [S_hi|S_lo]
+            const uint32_t id32 = tc::idesc_bf16(64, BV, false, true);       // W_lo S_hi, P N
+            const uint32_t id2w = tc::idesc_bf16(128, 2 * BV, true, true);   // K^T [N'_hi|N'_lo]
+            const uint32_t id2n = tc::idesc_bf16(128, BV, true, true);       // Kd_lo^T N'_hi
+            auto dk128 = [](uint32_t a) { return tc::smem_desc(a, 16, 1024, tc::kSwizzle128); };
+            auto dmn128 = [](uint32_t a) { return tc::smem_desc(a, C * 128, 1024, tc::kSwizzle128); };
+            auto dmn64 = [](uint32_t a, uint32_t atom) { return tc::smem_desc(a, atom, 512, tc::kSwizzle64); };
+            const uint64_t dNpair = dmn64(base + S::kNh, C * BV * 2), dNh = dmn64(base + S::kNh, 512);
+            const uint64_t dN = dmn64(base + S::kN, 512);
+            constexpr uint32_t a128[8] = {0, 2, 4, 6, (C * 128) >> 4, ((C * 128) >> 4) + 2, ((C * 128) >> 4) + 4,
+                                          ((C * 128) >> 4) + 6};       // [64][128] k128: 32 B steps, 2 column blocks
+            constexpr uint32_t a64[4] = {0, 2, 4, 6};                  // [64][64] k128
+            constexpr uint32_t amn[4] = {0, 128, 256, 384};            // MN-major A: 2 x 8-row groups per step
             bool issued = false;
             for (int c = 0; c < nc; ++c) {
-                const int s = c & 1, ob = c & 1;
+                const int s = c & 1, ob = c & 1, sb = S::kSBufs == 2 ? (c & 1) : 0;
                 const uint32_t st = base + s * S::kStage;
+                const uint32_t sS = base + S::kSh + sb * S::kSBuf;
+                const uint64_t dSpair = dmn64(sS, D * BV * 2), dSh = dmn64(sS, 512);
                 if (!tc::mbar_wait(bar(kFull0 + s), (c >> 1) & 1, abort_flag)) { fail(); break; }
-                GDR_TRACE_POINT(2, c);
+                if (role == 1) GDR_TRACE_POINT(2, c);
+                if (role == 3 && c >= 2 && !tc::mbar_wait(bar(kOFree0 + ob), ((c >> 1) - 1) & 1, abort_flag)) { fail(); break; }
                 if (!tc::mbar_wait(bar(kSReady), c & 1, abort_flag)) { fail(); break; }
-                GDR_TRACE_POINT(3, c);
+                if (role == 1) GDR_TRACE_POINT(3, c);
                 tc::fence_after();
-                // N-accumulator: W S^T with W = W_hi + W_lo, S = S_hi + S_lo (drop lo x lo)
-                const uint32_t wh = st + S::kW, wl = st + S::kW + kTile64x128;
-                int n = 0;
-                auto mma1 = [&](uint32_t a, uint32_t bsm, uint32_t d) {
-                    for (int ks = 0; ks < 8; ++ks)
-                        tc::mma_bf16(d, tc::smem_desc(a + (ks >> 2) * (C * 128) + (ks & 3) * 32, 16, 1024, tc::kSwizzle128),
-                                     tc::smem_desc(bsm + ks * 1024, 512, 512, tc::kSwizzle64), id1, n++ > 0);
-                };
-                mma1(wh, sSh, tD1);
-                mma1(wh, sSl, tD1);
-                mma1(wl, sSh, tD1);
-                tc::mma_commit(bar(kD1Full));
-                GDR_TRACE_POINT(4, c);
                 issued = true;
-                // output, inter-chunk part: O = Qd S^T (S hi + lo)
-                if (c >= 2 && !tc::mbar_wait(bar(kOFree0 + ob), ((c >> 1) - 1) & 1, abort_flag)) { fail(); break; }
-                tc::fence_after();
-                n = 0;
-                mma1(st + S::kQd, sSh, tO + 32 * ob);
-                mma1(st + S::kQd, sSl, tO + 32 * ob);
-                // state update: dS^T = K^T (f o N)   (A = K tile read MN-major)
-                if (!tc::mbar_wait(bar(kNReady), c & 1, abort_flag)) { fail(); break; }
-                GDR_TRACE_POINT(5, c);
-                tc::fence_after();
-                n = 0;
-                auto mma2 = [&](uint32_t a, uint32_t bsm) {
-                    for (int ks = 0; ks < 4; ++ks)
-                        tc::mma_bf16(tD2, tc::smem_desc(a + ks * 2048, C * 128, 1024, tc::kSwizzle128),
-                                     tc::smem_desc(bsm + ks * 1024, 512, 512, tc::kSwizzle64), id2, n++ > 0);
-                };
-                const uint32_t kt = st + S::kKt;
-                mma2(kt, sNh);
-                mma2(kt, sNl);
-                if (kKDA) mma2(kt + kTile64x128, sNh);
-                tc::mma_commit(bar(kD2Full));
-                // output, intra-chunk part: O += P N
-                for (int ks = 0; ks < 4; ++ks)
-                    tc::mma_bf16(tO + 32 * ob, tc::smem_desc(st + S::kP + ks * 32, 16, 1024, tc::kSwizzle128),
-                                 tc::smem_desc(sN + ks * 1024, 512, 512, tc::kSwizzle64), idO2, 1u);
-                tc::mma_commit(bar(kOFull0 + ob));
-                tc::mma_commit(bar(kEmpty0 + s));
-                GDR_TRACE_POINT(6, c);
+                if (role == 1) {
+                    tc::mma_ksteps<8>(tD1, dk128(st + S::kW), a128, dSpair, 64, id64, true);
+                    tc::mma_commit(bar(kD1Full));
+                    GDR_TRACE_POINT(4, c);
+                    if (!tc::mbar_wait(bar(kNReady), c & 1, abort_flag)) { fail(); break; }
+                    GDR_TRACE_POINT(5, c);
+                    tc::fence_after();
+                    tc::mma_ksteps<4>(tD2, dmn128(st + S::kKt), amn, dNpair, 64, id2w, true);
+                    if (kKDA) tc::mma_ksteps<4>(tD2, dmn128(st + S::kKt + kTile64x128), amn, dNh, 64, id2n, false);
+                    tc::mma_commit(bar(kD2Full));
+                    tc::mma_commit(bar(kEmpty0 + s));
+                    GDR_TRACE_POINT(6, c);
+                } else if (role == 2) {
+                    tc::mma_ksteps<8>(tD1b, dk128(st + S::kW + kTile64x128), a128, dSh, 64, id32, true);
+                    tc::mma_commit(bar(kD1Full));
+                    tc::mma_commit(bar(kEmpty0 + s));
+                } else {
+                    tc::mma_ksteps<8>(tO + 64 * ob, dk128(st + S::kQd), a128, dSpair, 64, id64, true);
+                    if (!tc::mbar_wait(bar(kNReady), c & 1, abort_flag)) { fail(); break; }
+                    tc::fence_after();
+                    tc::mma_ksteps<4>(tO + 64 * ob, dk128(st + S::kP), a64, dN, 64, id32, false);
+                    tc::mma_commit(bar(kOFull0 + ob));
+                    tc::mma_commit(bar(kEmpty0 + s));
+                }
             }
-            if (issued) {  // every MMA finished before the CTA leaves
-                tc::mma_commit(bar(kDrain));
-                tc::mbar_wait(bar(kDrain), 0, abort_flag);
+            if (issued) {  // every MMA this thread issued finished before the CTA leaves
+                const int dr = role == 1 ? kDrainA : role == 2 ? kDrainB : kDrainC;
+                tc::mma_commit(bar(dr));
+                tc::mbar_wait(bar(dr), 0, abort_flag);
             }
         }
         __syncwarp();
@@ -684,14 +717,19 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
 #pragma unroll
             for (int v = 0; v < BV; ++v) Sreg[v] = 0.f;
         }
-        unsigned char* sSh = sm + S::kSh;
-        unsigned char* sSl = sm + S::kSl;
         for (int c = 0; c < nc; ++c) {
-            const int s = c & 1;
+            const int s = c & 1, sb = S::kSBufs == 2 ? (c & 1) : 0;
             const unsigned char* stg = sm + s * S::kStage;
-            if (!tc::mbar_wait(bar(kFull0 + s), (c >> 1) & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
-            if (t == 0) GDR_TRACE_POINT(7, c);
-            // S^T rows (hi, lo) into the MMA operand tiles
+            unsigned char* sSh = sm + S::kSh + sb * S::kSBuf;
+            unsigned char* sSl = sm + S::kSl + sb * S::kSBuf;
+            // S^T rows (hi, lo) into the MMA operand tiles.  The buffer was last
+            // read by chunk c - kSBufs: its N products finished before the last
+            // state update, its output product is covered by that chunk's o_full.
+            if (c >= S::kSBufs) {
+                const int j = c - S::kSBufs;
+                if (!tc::mbar_wait(bar(kOFull0 + (j & 1)), (j >> 1) & 1, abort_flag)) fail();
+            }
+            if (t == 0) GDR_TRACE_POINT(21, c);
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
                 uint32_t hw[4], lw[4];
@@ -707,6 +745,17 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
                 *reinterpret_cast<uint4*>(sSh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                 *reinterpret_cast<uint4*>(sSl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
+            if (t == 0) GDR_TRACE_POINT(19, c);
+            tc::fence_proxy_async();
+            if (t == 0) GDR_TRACE_POINT(20, c);
+            tc::fence_before();
+            tc::bar_sync(1, 128);
+            if (t == 0) {
+                GDR_TRACE_POINT(8, c);
+                tc::mbar_arrive(bar(kSReady));
+            }
+            if (!tc::mbar_wait(bar(kFull0 + s), (c >> 1) & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
+            if (t == 0) GDR_TRACE_POINT(7, c);
             const float* rec = reinterpret_cast<const float*>(stg + S::kRec_);
             const float colf = rec[64 + t];
             const float rowf = nrow ? rec[i] : 0.f;
@@ -720,19 +769,21 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
                     uv[4 * u] = x.x; uv[4 * u + 1] = x.y; uv[4 * u + 2] = x.z; uv[4 * u + 3] = x.w;
                 }
             }
-            tc::fence_proxy_async();
-            tc::fence_before();
-            tc::bar_sync(1, 128);
-            if (t == 0) {
-                GDR_TRACE_POINT(8, c);
-                tc::mbar_arrive(bar(kSReady));
-            }
             // N = U - W S^T  ->  N' = rowf * N (hi, lo), N (bf16, masked)
             if (!tc::mbar_wait(bar(kD1Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
             if (t == 0) GDR_TRACE_POINT(9, c);
             tc::fence_after();
-            float dv[BV];
-            tc::tmem_ld32(tD1 + lane_base, dv);
+            float dv[2 * BV];
+            tc::tmem_ld64(tD1 + lane_base, dv);
+#pragma unroll
+            for (int v = 0; v < BV; ++v) dv[v] += dv[BV + v];
+            tc::tmem_ld32(tD1b + lane_base, dv + BV);  // reuse the upper half for the W_lo part
+#pragma unroll
+            for (int v = 0; v < BV; ++v) dv[v] += dv[BV + v];
+            if (t == 0) GDR_TRACE_POINT(15, c);
+            // the N tiles were last read by the output product of chunk c - 1
+            if (c >= 1 && !tc::mbar_wait(bar(kOFull0 + ((c - 1) & 1)), ((c - 1) >> 1) & 1, abort_flag)) fail();
+            if (t == 0) GDR_TRACE_POINT(16, c);
             if (nrow) {
                 const float keep = i < Lc ? 1.f : 0.f;  // rows past the chunk end
 #pragma unroll
@@ -758,7 +809,9 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
                     *reinterpret_cast<uint4*>(sm + S::kN + off) = make_uint4(nw[0], nw[1], nw[2], nw[3]);
                 }
             }
+            if (t == 0) GDR_TRACE_POINT(17, c);
             tc::fence_proxy_async();
+            if (t == 0) GDR_TRACE_POINT(18, c);
             tc::fence_before();
             tc::bar_sync(1, 128);
             if (t == 0) {
@@ -769,9 +822,9 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
             if (!tc::mbar_wait(bar(kD2Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
             if (t == 0) GDR_TRACE_POINT(11, c);
             tc::fence_after();
-            tc::tmem_ld32(tD2 + lane_base, dv);
+            tc::tmem_ld64(tD2 + lane_base, dv);
 #pragma unroll
-            for (int v = 0; v < BV; ++v) Sreg[v] = fmaf(colf, Sreg[v], dv[v]);
+            for (int v = 0; v < BV; ++v) Sreg[v] = fmaf(colf, Sreg[v], dv[v] + dv[BV + v]);
             if (t == 0) GDR_TRACE_POINT(12, c);
             tc::fence_before();
         }
@@ -790,8 +843,10 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
             if (!tc::mbar_wait(bar(kOFull0 + ob), (c >> 1) & 1, abort_flag)) fail();
             if (tid == 256) GDR_TRACE_POINT(13, c);
             tc::fence_after();
-            float ov[BV];
-            tc::tmem_ld32(tO + 32 * ob + lane_base, ov);
+            float ov[2 * BV];
+            tc::tmem_ld64(tO + 64 * ob + lane_base, ov);
+#pragma unroll
+            for (int v = 0; v < BV; ++v) ov[v] += ov[BV + v];
             const int cs = bos + c * C;
             if (lane < 16 && cs + i < eos) {
                 uint4* dst = reinterpret_cast<uint4*>(op + ((size_t)(cs + i) * p.Hv + h) * D + v0);
@@ -812,7 +867,7 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
     }
     tc::fence_before();
     __syncthreads();
-    if (warp == 2) tc::tmem_dealloc(tmem, 128);
+    if (warp == 2) tc::tmem_dealloc(tmem, 512);
 }
 
 // LPT order: sequence indices by decreasing length (ties by index).

@@ -67,6 +67,17 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
                  :: "r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(acc));
 }
 
+// n_steps (4 or 8) k-steps into one accumulator: descriptors advance by
+// a_step[ks] / b_step per k-step (16-byte units); the first step overwrites D
+// when `first`, every later one accumulates.
+template <int kSteps>
+__device__ __forceinline__ void mma_ksteps(uint32_t d_tmem, uint64_t a, const uint32_t (&a_step)[kSteps], uint64_t b,
+                                           uint32_t b_step, uint32_t idesc, bool first) {
+#pragma unroll
+    for (int ks = 0; ks < kSteps; ++ks)
+        mma_bf16(d_tmem, a + a_step[ks], b + (uint64_t)b_step * ks, idesc, (first && ks == 0) ? 0u : 1u);
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t mbar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(mbar) : "memory");
 }
@@ -97,6 +108,29 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
+// 64 consecutive fp32 columns (two 32-column loads, one wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
+    uint32_t r[64];
+#define GDR_LD32(base, off)                                                                                       \
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15," \
+                 "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"                       \
+                 : "=r"(r[base + 0]), "=r"(r[base + 1]), "=r"(r[base + 2]), "=r"(r[base + 3]), "=r"(r[base + 4]),  \
+                   "=r"(r[base + 5]), "=r"(r[base + 6]), "=r"(r[base + 7]), "=r"(r[base + 8]), "=r"(r[base + 9]),  \
+                   "=r"(r[base + 10]), "=r"(r[base + 11]), "=r"(r[base + 12]), "=r"(r[base + 13]),                 \
+                   "=r"(r[base + 14]), "=r"(r[base + 15]), "=r"(r[base + 16]), "=r"(r[base + 17]),                 \
+                   "=r"(r[base + 18]), "=r"(r[base + 19]), "=r"(r[base + 20]), "=r"(r[base + 21]),                 \
+                   "=r"(r[base + 22]), "=r"(r[base + 23]), "=r"(r[base + 24]), "=r"(r[base + 25]),                 \
+                   "=r"(r[base + 26]), "=r"(r[base + 27]), "=r"(r[base + 28]), "=r"(r[base + 29]),                 \
+                   "=r"(r[base + 30]), "=r"(r[base + 31])                                                           \
+                 : "r"(taddr + (off)))
+    GDR_LD32(0, 0);
+    GDR_LD32(32, 32);
+#undef GDR_LD32
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 64; ++j) v[j] = __uint_as_float(r[j]);
 }
 
 // ---- mbarriers ----------------------------------------------------------------
