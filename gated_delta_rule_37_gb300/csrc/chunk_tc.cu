@@ -22,11 +22,13 @@
 //          N  = U - W S0^T            M=64, 3-term split (W hi/lo x S hi/lo)
 //          O  = Qd S0^T + P N         M=64 (output, 2 + 1 MMA groups)
 //          S  = e^{gam_L} S0 + K^T (f o N)     M=128, 2-term split
-//        Warp roles: warp 0 stages chunk blobs with cp.async.bulk into a
-//        two-deep ring; warp 1 issues every tcgen05.mma from one thread;
-//        warps 4-7 hold the fp32 state S^T (thread k owns row k, 32 values)
-//        and turn the N accumulator into the split operands; warps 8-11 drain
-//        the output accumulator (double-buffered in TMEM) to bf16 rows of o.
+//        Warp roles (512 threads): warp 0 stages chunk blobs with
+//        cp.async.bulk into a two-deep ring; warps 1-3 each issue part of the
+//        tcgen05.mma work from one thread (a single thread issues about one MMA
+//        per 60 cycles); warps 4-11 hold the fp32 state S^T (row k in TMEM lane
+//        k, 16 of the 32 columns per thread) and turn the N accumulator into the
+//        split operands; warps 12-15 drain the output accumulator
+//        (double-buffered in TMEM) to bf16 rows of o.
 //
 // Every exponential is of gam_i - gam_j with i >= j or of gam_i, all <= 0:
 // any finite gate <= 0 keeps every operand finite (cuLA PR #113 review).
@@ -108,9 +110,10 @@ __device__ __forceinline__ void raise_error(const TcParams& p, unsigned code) {
 // lower, fp32, 128 threads.  Diagonal 16 x 16 blocks by forward substitution,
 // then block diagonals d = 1..3:  T_ij = -D_i * sum_{m in blocks j..i-1} A_im T_mj.
 // ---------------------------------------------------------------------------
+template <int NT>
 __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict__ Tm, float* __restrict__ Z,
                                  int tid) {
-    for (int e = tid; e < C * LDA; e += 128) Tm[e] = 0.f;
+    for (int e = tid; e < C * LDA; e += NT) Tm[e] = 0.f;
     __syncthreads();
     if (tid < 64) {
         const int b = tid >> 4, c = tid & 15, r0 = 16 * b;
@@ -128,7 +131,7 @@ __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict_
     __syncthreads();
     for (int d = 1; d < 4; ++d) {
         const int nblk = 4 - d;
-        for (int e = tid; e < nblk * 256; e += 128) {
+        for (int e = tid; e < nblk * 256; e += NT) {
             const int j = e >> 8, i = j + d, r = (e >> 4) & 15, c = e & 15;
             float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
             const float* arow = A + (16 * i + r) * LDA;
@@ -142,7 +145,7 @@ __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict_
             Z[e] = (s0 + s1) + (s2 + s3);
         }
         __syncthreads();
-        for (int e = tid; e < nblk * 256; e += 128) {
+        for (int e = tid; e < nblk * 256; e += NT) {
             const int j = e >> 8, i = j + d, r = (e >> 4) & 15, c = e & 15;
             float s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -156,34 +159,40 @@ __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict_
     }
 }
 
-// Stage a [64][128] bf16 token tile (rows >= L zero-filled) into a k128 smem
-// tile with cp.async: all 16-byte pieces are in flight at once.
-__device__ __forceinline__ void stage_rows_async(unsigned char* tile, const __nv_bfloat16* src, size_t row_stride,
-                                                 int L, int tid) {
-    for (int e = tid; e < C * 16; e += 128) {
+// Stage 64 token rows [64][128] bf16 (rows >= L zero-filled) into rows
+// [row0, row0 + 64) of a k128 smem tile of `rows` rows, with cp.async (all
+// 16-byte pieces in flight at once).
+template <int NT>
+__device__ __forceinline__ void stage_rows_async(unsigned char* tile, int rows, int row0, const __nv_bfloat16* src,
+                                                 size_t row_stride, int L, int tid) {
+    for (int e = tid; e < C * 16; e += NT) {
         const int row = e >> 4, ch = e & 15;
         const __nv_bfloat16* g = src + (size_t)(row < L ? row : 0) * row_stride + ch * 8;
-        const uint32_t dst = tc::smem_u32(tile + tc::chunk_k128(row, ch, C));
+        const uint32_t dst = tc::smem_u32(tile + tc::chunk_k128(row0 + row, ch, rows));
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(g), "r"(row < L ? 16 : 0)
                      : "memory");
     }
 }
 
 // ---------------------------------------------------------------------------
-// prep kernel
+// prep kernel (256 threads)
 // ---------------------------------------------------------------------------
-// Shared memory: the Q tile and the fp32 A matrix are dead once the solve has
-// started, and the four split T tiles (32 KB) reuse their space.
+// Shared memory.  X stacks K (rows 0..63) and Q (rows 64..127) as one M = 128
+// operand, so K K^T and Q K^T come from one group of MMAs.  Dead regions are
+// reused: the Q rows of X hold T' hi / lo and the fp32 A matrix holds T'' hi /
+// lo once the solve has finished.
+constexpr int kPrepThreads = 256;
+constexpr uint32_t kXcb = 2 * C * 128;  // column-block stride of X (128 rows x 128 B)
+
 template <bool kKDA>
 struct PrepSmem {
-    static constexpr uint32_t kK = 0;                        // K tile 16 KB
-    static constexpr uint32_t kV = kK + kTile64x128;         // V tile
-    static constexpr uint32_t kQ = kV + kTile64x128;         // Q tile (later T' hi / lo)
-    static constexpr uint32_t kA = kQ + kTile64x128;         // fp32 [64][65] (later T'' hi / lo)
-    static constexpr uint32_t kT1h = kQ;
-    static constexpr uint32_t kT1l = kQ + kTile64x64;
-    static constexpr uint32_t kT2h = kQ + 2 * kTile64x64;
-    static constexpr uint32_t kT2l = kQ + 3 * kTile64x64;
+    static constexpr uint32_t kX = 0;                         // [K; Q] 128 x 128 bf16 (32 KB)
+    static constexpr uint32_t kV = kX + 2 * kTile64x128;      // V tile 64 x 128 (16 KB)
+    static constexpr uint32_t kA = kV + kTile64x128;          // fp32 [64][65]
+    static constexpr uint32_t kT1h = kX + C * 128;            // Q rows, column block 0
+    static constexpr uint32_t kT1l = kX + kXcb + C * 128;     // Q rows, column block 1
+    static constexpr uint32_t kT2h = kA;
+    static constexpr uint32_t kT2l = kA + kTile64x64;
     static constexpr uint32_t kTm = (kA + C * LDA * 4 + 1023) & ~1023u;  // fp32 [64][65]
     static constexpr uint32_t kZ = kTm + C * LDA * 4;                   // fp32 [3][256]
     static constexpr uint32_t kKgh = (kZ + 3 * 256 * 4 + 1023) & ~1023u;  // K o e^Gam hi (channel gate)
@@ -192,18 +201,20 @@ struct PrepSmem {
     static constexpr uint32_t kBeta = kGam + (kKDA ? C * D * 4 : C * 4);
     static constexpr uint32_t kBar = kBeta + C * 4;
     static constexpr uint32_t kTotal = kBar + 64 + 1024;  // + alignment slack
-    static_assert(kT2l + kTile64x64 <= kTm, "T tiles overlap Tm");
+    static_assert(kT2l + kTile64x64 <= kTm, "T'' tiles overlap Tm");
 };
 
 template <bool kKDA>
-__global__ void __launch_bounds__(128, kKDA ? 1 : 2) chunk_prep_kernel(TcParams p) {
+__global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(TcParams p) {
     using S = PrepSmem<kKDA>;
+    constexpr int NT = kPrepThreads;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int chunk = blockIdx.x;
     if (chunk >= p.meta[0]) return;
     const int h = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int q = warp & 3, hf = warp >> 2;  // TMEM lane quadrant, column half
     const int4 info = p.table[chunk];
     const int start = info.y, L = info.z;
     const int grp = p.Hv / p.Hk, kh = h / grp;
@@ -223,10 +234,10 @@ __global__ void __launch_bounds__(128, kKDA ? 1 : 2) chunk_prep_kernel(TcParams 
     const uint32_t bar0 = tc::smem_u32(&bars[0]);
 
     GDR_TRACE_PREP(0);
-    // ---- stage K, Q, V rows (cp.async), gates, beta ----------------------------
-    stage_rows_async(sm + S::kK, kp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
-    stage_rows_async(sm + S::kQ, qp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
-    stage_rows_async(sm + S::kV, vp + ((size_t)start * p.Hv + h) * D, (size_t)p.Hv * D, L, tid);
+    // ---- stage K, Q (as X) and V rows (cp.async), gates, beta -------------------
+    stage_rows_async<NT>(sm + S::kX, 2 * C, 0, kp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
+    stage_rows_async<NT>(sm + S::kX, 2 * C, C, qp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
+    stage_rows_async<NT>(sm + S::kV, C, 0, vp + ((size_t)start * p.Hv + h) * D, (size_t)p.Hv * D, L, tid);
     asm volatile("cp.async.commit_group;" ::: "memory");
     if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), 256);
     if (tid == 0) {
@@ -236,17 +247,19 @@ __global__ void __launch_bounds__(128, kKDA ? 1 : 2) chunk_prep_kernel(TcParams 
     }
     if (tid < C) bet[tid] = tid < L ? to_f(bp[((size_t)start + tid) * p.Hv + h]) : 0.f;
     if (kKDA) {
-        // per-channel inclusive cumsum in token order (thread = channel); all
-        // 64 loads are issued before the dependent adds
-        const float* __restrict__ gk = p.gk + ((size_t)start * p.Hv + h) * D + tid;
-        float x[C];
+        if (tid < D) {
+            // per-channel inclusive cumsum in token order (thread = channel); all
+            // 64 loads are issued before the dependent adds
+            const float* __restrict__ gk = p.gk + ((size_t)start * p.Hv + h) * D + tid;
+            float x[C];
 #pragma unroll
-        for (int i = 0; i < C; ++i) x[i] = i < L ? __ldg(gk + (size_t)i * p.Hv * D) : 0.f;
-        float acc = 0.f;
+            for (int i = 0; i < C; ++i) x[i] = i < L ? __ldg(gk + (size_t)i * p.Hv * D) : 0.f;
+            float acc = 0.f;
 #pragma unroll
-        for (int i = 0; i < C; ++i) {
-            acc += x[i];
-            gam[i * D + tid] = acc;
+            for (int i = 0; i < C; ++i) {
+                acc += x[i];
+                gam[i * D + tid] = acc;
+            }
         }
     } else if (warp < 2) {
         // scalar gate: inclusive scan over 64 tokens with two warps
@@ -266,36 +279,29 @@ __global__ void __launch_bounds__(128, kKDA ? 1 : 2) chunk_prep_kernel(TcParams 
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t sK = tc::smem_u32(sm + S::kK), sQ = tc::smem_u32(sm + S::kQ), sV = tc::smem_u32(sm + S::kV);
     GDR_TRACE_PREP(1);
+    const uint32_t sX = tc::smem_u32(sm + S::kX), sV = tc::smem_u32(sm + S::kV);
     auto gm = [&](int i, int c) -> float { return kKDA ? gam[i * D + c] : gam[i]; };
     const float* gl = kKDA ? gam + (L - 1) * D : gam + (L - 1);
 
-    // ---- G = K K^T and Q K^T on the tensor cores (scalar gate) -------------------
+    // ---- [K K^T ; Q K^T] on the tensor cores (scalar gate), one M = 128 group ------
     if (!kKDA && tid == 0) {
-        constexpr uint32_t id = tc::idesc_bf16(64, 64, false, false);
+        constexpr uint32_t id = tc::idesc_bf16(128, 64, false, false);
         for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = (ks >> 2) * (C * 128) + (ks & 3) * 32;
-            tc::mma_bf16(tmem, tc::smem_desc(sK + off, 16, 1024, tc::kSwizzle128),
-                         tc::smem_desc(sK + off, 16, 1024, tc::kSwizzle128), id, ks > 0);
-        }
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = (ks >> 2) * (C * 128) + (ks & 3) * 32;
-            tc::mma_bf16(tmem + 64, tc::smem_desc(sQ + off, 16, 1024, tc::kSwizzle128),
-                         tc::smem_desc(sK + off, 16, 1024, tc::kSwizzle128), id, ks > 0);
+            const uint32_t off = (ks >> 2) * kXcb + (ks & 3) * 32;
+            tc::mma_bf16(tmem, tc::smem_desc(sX + off, 16, 1024, tc::kSwizzle128),
+                         tc::smem_desc(sX + off, 16, 1024, tc::kSwizzle128), id, ks > 0);
         }
         tc::mma_commit(bar0);
     }
     __syncwarp();
 
-    // ---- while those run: Qd blob, K / Kd blob, decay record -----------------------
+    // ---- while that runs: Qd blob, K / Kd blob, decay record ------------------------
     {
-        const __nv_bfloat16* Qt = reinterpret_cast<const __nv_bfloat16*>(sm + S::kQ);
         unsigned char* Qdst = p.Qb + ((size_t)chunk * p.Hv + h) * kTile64x128;
-        for (int e = tid; e < C * 16; e += 128) {
+        for (int e = tid; e < C * 16; e += NT) {
             const int i = e >> 4, ch = e & 15;
-            const uint32_t off = tc::chunk_k128(i, ch, C);
-            const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kQ + off);
+            const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(C + i, ch, 2 * C));
             const __nv_bfloat16* qv = reinterpret_cast<const __nv_bfloat16*>(&raw);
             uint32_t w4[4];
 #pragma unroll
@@ -304,148 +310,126 @@ __global__ void __launch_bounds__(128, kKDA ? 1 : 2) chunk_prep_kernel(TcParams 
                 w4[u] = tc::pack_bf16(__bfloat162float(qv[2 * u]) * __expf(gm(i, c)),
                                       __bfloat162float(qv[2 * u + 1]) * __expf(gm(i, c + 1)));
             }
-            *reinterpret_cast<uint4*>(Qdst + off) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            *reinterpret_cast<uint4*>(Qdst + tc::chunk_k128(i, ch, C)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
-        (void)Qt;
         if (!kKDA) {
-            if (h % grp == 0) {
+            if (h % grp == 0) {  // K rows of X, both column blocks -> a [64][128] k128 image
                 unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hk + kh) * kTile64x128;
-                for (int e = tid; e < (int)(kTile64x128 / 16); e += 128)
-                    reinterpret_cast<uint4*>(Kdst)[e] = reinterpret_cast<const uint4*>(sm + S::kK)[e];
+                for (int e = tid; e < (int)(kTile64x128 / 16); e += NT) {
+                    const int cb = e >> 9, r = e & 511;
+                    reinterpret_cast<uint4*>(Kdst)[e] = reinterpret_cast<const uint4*>(sm + S::kX + cb * kXcb)[r];
+                }
             }
         } else {
             unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hv + h) * 2 * kTile64x128;
-            for (int e = tid; e < C * 16; e += 128) {
+            for (int e = tid; e < C * 16; e += NT) {
                 const int i = e >> 4, ch = e & 15;
-                const uint32_t off = tc::chunk_k128(i, ch, C);
-                const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kK + off);
+                const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(i, ch, 2 * C));
                 const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&raw);
                 uint32_t hw[4], lw[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    float hh[2], ll[2];
-#pragma unroll
-                    for (int w = 0; w < 2; ++w) {
-                        const int c = ch * 8 + 2 * u + w;
-                        const float x = i < L ? __bfloat162float(kv[2 * u + w]) * __expf(gl[c] - gam[i * D + c]) : 0.f;
-                        tc::split_bf16(x, hh[w], ll[w]);
-                    }
-                    hw[u] = tc::pack_bf16(hh[0], hh[1]);
-                    lw[u] = tc::pack_bf16(ll[0], ll[1]);
+                    const int c = ch * 8 + 2 * u;
+                    const float x0 = i < L ? __bfloat162float(kv[2 * u]) * __expf(gl[c] - gam[i * D + c]) : 0.f;
+                    const float x1 = i < L ? __bfloat162float(kv[2 * u + 1]) * __expf(gl[c + 1] - gam[i * D + c + 1]) : 0.f;
+                    tc::split2(x0, x1, hw[u], lw[u]);
                 }
+                const uint32_t off = tc::chunk_k128(i, ch, C);
                 *reinterpret_cast<uint4*>(Kdst + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                 *reinterpret_cast<uint4*>(Kdst + kTile64x128 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
         }
         float* rec = reinterpret_cast<float*>(p.Rb + ((size_t)chunk * p.Hv + h) * kRec);
         if (tid < C) rec[tid] = tid < L ? (kKDA ? 1.f : __expf(gl[0] - gam[tid])) : 0.f;
-        rec[64 + tid] = __expf(kKDA ? gl[tid] : gl[0]);
+        if (tid < D) rec[64 + tid] = __expf(kKDA ? gl[tid] : gl[0]);
         if (tid == 0) reinterpret_cast<int*>(rec)[192] = L;
     }
-
     GDR_TRACE_PREP(2);
+
     // ---- A (strictly lower) and P (lower incl. diagonal) -------------------------
     unsigned char* Pdst = p.Pb + ((size_t)chunk * p.Hv + h) * kTile64x64;
     if (!kKDA) {
         if (!tc::mbar_wait(bar0, 0, abort_flag)) raise_error(p, 1u);
         tc::fence_after();
-        const int i = 16 * (warp & 3) + (lane & 15);
-        const uint32_t lrow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-        for (int half = 0; half < 2; ++half) {
-            float gv[32], qv[32];
-            tc::tmem_ld32(lrow + 32 * half, gv);
-            tc::tmem_ld32(lrow + 64 + 32 * half, qv);
-            if (lane < 16) {
-                const float gi = gam[i], bi = bet[i];
-                uint32_t pk[16];
+        // thread: accumulator row r = 32 q + lane (rows < 64: K K^T, >= 64: Q K^T),
+        // columns [32 hf, 32 hf + 32)
+        const int r = 32 * q + lane, i = r & 63;
+        float gv[32];
+        tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * hf, gv);
+        const float gi = gam[i], bi = bet[i];
+        if (r < C) {
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const int j = 32 * half + jj;
-                    const bool inl = i < L && j <= i;
-                    const float e = inl ? __expf(gi - gam[j]) : 0.f;
-                    As[i * LDA + j] = (j < i && i < L) ? bi * e * gv[jj] : 0.f;
-                    const float pv = e * qv[jj];
-                    if (jj & 1) pk[jj >> 1] |= (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(pv)) << 16;
-                    else pk[jj >> 1] = __bfloat16_as_ushort(__float2bfloat16_rn(pv));
-                }
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc)
-                    *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(i, 4 * half + cc, C)) =
-                        make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+            for (int jj = 0; jj < 32; ++jj) {
+                const int j = 32 * hf + jj;
+                As[i * LDA + j] = (j < i && i < L) ? bi * __expf(gi - gam[j]) * gv[jj] : 0.f;
             }
+        } else {
+            uint32_t pk[16];
+#pragma unroll
+            for (int jj = 0; jj < 32; jj += 2) {
+                const int j = 32 * hf + jj;
+                const float p0 = (j <= i && i < L) ? __expf(gi - gam[j]) * gv[jj] : 0.f;
+                const float p1 = (j + 1 <= i && i < L) ? __expf(gi - gam[j + 1]) * gv[jj + 1] : 0.f;
+                pk[jj >> 1] = tc::pack_bf16(p0, p1);
+            }
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+                *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(i, 4 * hf + cc, C)) =
+                    make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
         }
     } else {
         // per-channel decays: A_ij = beta_i sum_c k_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}
-        const __nv_bfloat16* Kt = reinterpret_cast<const __nv_bfloat16*>(sm + S::kK);
-        const __nv_bfloat16* Qt = reinterpret_cast<const __nv_bfloat16*>(sm + S::kQ);
-        for (int e = tid; e < C * C; e += 128) {
+        const __nv_bfloat16* Xt = reinterpret_cast<const __nv_bfloat16*>(sm + S::kX);
+        for (int e = tid; e < C * C; e += NT) {
             const int i = e >> 6, j = e & 63;
             float a = 0.f, pv = 0.f;
             if (j <= i && i < L) {
                 for (int c = 0; c < D; ++c) {
                     const float ex = __expf(gam[i * D + c] - gam[j * D + c]);
-                    const float kj = __bfloat162float(Kt[tc::off_k128(j, c, C) >> 1]) * ex;
-                    a = fmaf(__bfloat162float(Kt[tc::off_k128(i, c, C) >> 1]), kj, a);
-                    pv = fmaf(__bfloat162float(Qt[tc::off_k128(i, c, C) >> 1]), kj, pv);
+                    const float kj = __bfloat162float(Xt[tc::off_k128(j, c, 2 * C) >> 1]) * ex;
+                    a = fmaf(__bfloat162float(Xt[tc::off_k128(i, c, 2 * C) >> 1]), kj, a);
+                    pv = fmaf(__bfloat162float(Xt[tc::off_k128(C + i, c, 2 * C) >> 1]), kj, pv);
                 }
             }
             As[i * LDA + j] = (j < i) ? bet[i] * a : 0.f;
             reinterpret_cast<__nv_bfloat16*>(Pdst)[tc::off_k128(i, j, C) >> 1] = __float2bfloat16_rn(pv);
         }
         // K o e^{Gam} as hi / lo for W
-        for (int e = tid; e < C * 16; e += 128) {
+        for (int e = tid; e < C * 16; e += NT) {
             const int i = e >> 4, ch = e & 15;
-            const uint32_t off = tc::chunk_k128(i, ch, C);
-            const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kK + off);
+            const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(i, ch, 2 * C));
             const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&raw);
             uint32_t hw[4], lw[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                float hh[2], ll[2];
-#pragma unroll
-                for (int w = 0; w < 2; ++w) {
-                    const int c = ch * 8 + 2 * u + w;
-                    tc::split_bf16(__bfloat162float(kv[2 * u + w]) * __expf(gam[i * D + c]), hh[w], ll[w]);
-                }
-                hw[u] = tc::pack_bf16(hh[0], hh[1]);
-                lw[u] = tc::pack_bf16(ll[0], ll[1]);
+                const int c = ch * 8 + 2 * u;
+                tc::split2(__bfloat162float(kv[2 * u]) * __expf(gam[i * D + c]),
+                           __bfloat162float(kv[2 * u + 1]) * __expf(gam[i * D + c + 1]), hw[u], lw[u]);
             }
+            const uint32_t off = tc::chunk_k128(i, ch, C);
             *reinterpret_cast<uint4*>(sm + S::kKgh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
             *reinterpret_cast<uint4*>(sm + S::kKgl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
     }
     tc::fence_before();
     __syncthreads();
-
     GDR_TRACE_PREP(3);
-    // ---- Tm = (I + A)^{-1} -----------------------------------------------------------
-    solve_unit_lower(As, Tm, Z, tid);
 
+    // ---- Tm = (I + A)^{-1} -----------------------------------------------------------
+    solve_unit_lower<NT>(As, Tm, Z, tid);
     GDR_TRACE_PREP(4);
+
     // ---- split operands: T' = Tm diag(beta e^{gam}) (scalar gate) or Tm diag(beta);
-    //      T'' = Tm diag(beta).  Written over the (dead) Q tile and A matrix.
-    for (int e = tid; e < C * 8; e += 128) {
+    //      T'' = Tm diag(beta).  Written over the dead Q rows of X and the A matrix.
+    for (int e = tid; e < C * 8; e += NT) {
         const int i = e >> 3, ch = e & 7;
         uint32_t h1[4], l1[4], h2[4], l2[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            float a1[2], a2[2];
-#pragma unroll
-            for (int w = 0; w < 2; ++w) {
-                const int j = ch * 8 + 2 * u + w;
-                const float t = Tm[i * LDA + j] * bet[j];
-                a2[w] = t;
-                a1[w] = kKDA ? t : t * __expf(gam[j]);
-            }
-            float hh[2], ll[2], hh2[2], ll2[2];
-            tc::split_bf16(a1[0], hh[0], ll[0]);
-            tc::split_bf16(a1[1], hh[1], ll[1]);
-            tc::split_bf16(a2[0], hh2[0], ll2[0]);
-            tc::split_bf16(a2[1], hh2[1], ll2[1]);
-            h1[u] = tc::pack_bf16(hh[0], hh[1]);
-            l1[u] = tc::pack_bf16(ll[0], ll[1]);
-            h2[u] = tc::pack_bf16(hh2[0], hh2[1]);
-            l2[u] = tc::pack_bf16(ll2[0], ll2[1]);
+            const int j = ch * 8 + 2 * u;
+            const float t0 = Tm[i * LDA + j] * bet[j], t1 = Tm[i * LDA + j + 1] * bet[j + 1];
+            tc::split2(kKDA ? t0 : t0 * __expf(gam[j]), kKDA ? t1 : t1 * __expf(gam[j + 1]), h1[u], l1[u]);
+            tc::split2(t0, t1, h2[u], l2[u]);
         }
         const uint32_t off = tc::chunk_k128(i, ch, C);
         *reinterpret_cast<uint4*>(sm + S::kT1h + off) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
@@ -455,65 +439,62 @@ __global__ void __launch_bounds__(128, kKDA ? 1 : 2) chunk_prep_kernel(TcParams 
     }
     tc::fence_proxy_async();
     __syncthreads();
-
     GDR_TRACE_PREP(5);
+
     // ---- W = T' K (or T'' (K o e^Gam)), U = T'' V ----------------------------------------
     if (tid == 0) {
         tc::fence_after();
         constexpr uint32_t id = tc::idesc_bf16(64, 128, false, true);
         const uint32_t t1h = tc::smem_u32(sm + S::kT1h), t1l = tc::smem_u32(sm + S::kT1l);
         const uint32_t t2h = tc::smem_u32(sm + S::kT2h), t2l = tc::smem_u32(sm + S::kT2l);
-        auto mm = [&](uint32_t dcol, uint32_t a, uint32_t b, bool first) {
+        // B operands read MN-major: K rows of X (atom stride kXcb), V / Kg (atom stride 8 KB)
+        auto mm = [&](uint32_t dcol, uint32_t a, uint32_t b, uint32_t atom, bool first) {
             for (int ks = 0; ks < 4; ++ks)
                 tc::mma_bf16(tmem + dcol, tc::smem_desc(a + ks * 32, 16, 1024, tc::kSwizzle128),
-                             tc::smem_desc(b + ks * 2048, C * 128, 1024, tc::kSwizzle128), id, (first && ks == 0) ? 0u : 1u);
+                             tc::smem_desc(b + ks * 2048, atom, 1024, tc::kSwizzle128), id, (first && ks == 0) ? 0u : 1u);
         };
         if (!kKDA) {
-            mm(0, t1h, sK, true);
-            mm(0, t1l, sK, false);
+            mm(0, t1h, sX, kXcb, true);
+            mm(0, t1l, sX, kXcb, false);
         } else {
             const uint32_t kgh = tc::smem_u32(sm + S::kKgh), kgl = tc::smem_u32(sm + S::kKgl);
-            mm(0, t2h, kgh, true);
-            mm(0, t2h, kgl, false);
-            mm(0, t2l, kgh, false);
+            mm(0, t2h, kgh, C * 128, true);
+            mm(0, t2h, kgl, C * 128, false);
+            mm(0, t2l, kgh, C * 128, false);
         }
-        mm(128, t2h, sV, true);
-        mm(128, t2l, sV, false);
+        mm(128, t2h, sV, C * 128, true);
+        mm(128, t2l, sV, C * 128, false);
         tc::mma_commit(bar0);
     }
     __syncwarp();
-
     GDR_TRACE_PREP(6);
-    // ---- W, U out of TMEM into their blobs ------------------------------------------------
+
+    // ---- W, U out of TMEM into their blobs: 8 warps, row i = 16 q + lane (lane <
+    //      16), columns [64 hf, 64 hf + 64) of W and of U -------------------------------
     // second use of bar0 (the first, K K^T / Q K^T, exists only for the scalar gate)
     if (!tc::mbar_wait(bar0, kKDA ? 0 : 1, abort_flag)) raise_error(p, 1u);
     tc::fence_after();
     {
-        const int i = 16 * (warp & 3) + (lane & 15);
-        const uint32_t lrow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+        const int i = 16 * q + (lane & 15);
+        const uint32_t lrow = tmem + ((uint32_t)(32 * q) << 16);
         unsigned char* Wdst = p.Wb + ((size_t)chunk * p.Hv + h) * 2 * kTile64x128;
         float* Udst = reinterpret_cast<float*>(p.Ub + ((size_t)chunk * p.Hv + h) * NVB * kUBlock);
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q2 = 0; q2 < 2; ++q2) {
+            const int cb = 2 * hf + q2;  // 32-column block of W and of U
             float wv[32], uv[32];
-            tc::tmem_ld32(lrow + 32 * q4, wv);
-            tc::tmem_ld32(lrow + 128 + 32 * q4, uv);
+            tc::tmem_ld32(lrow + 32 * cb, wv);
+            tc::tmem_ld32(lrow + 128 + 32 * cb, uv);
             if (lane < 16) {
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
                     uint32_t hw[4], lw[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        float hh[2], ll[2];
-                        tc::split_bf16(wv[8 * cc + 2 * u], hh[0], ll[0]);
-                        tc::split_bf16(wv[8 * cc + 2 * u + 1], hh[1], ll[1]);
-                        hw[u] = tc::pack_bf16(hh[0], hh[1]);
-                        lw[u] = tc::pack_bf16(ll[0], ll[1]);
-                    }
-                    const uint32_t off = tc::chunk_k128(i, 4 * q4 + cc, C);
+                    for (int u = 0; u < 4; ++u) tc::split2(wv[8 * cc + 2 * u], wv[8 * cc + 2 * u + 1], hw[u], lw[u]);
+                    const uint32_t off = tc::chunk_k128(i, 4 * cb + cc, C);
                     *reinterpret_cast<uint4*>(Wdst + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                     *reinterpret_cast<uint4*>(Wdst + kTile64x128 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 }
-                float* urow = Udst + (size_t)q4 * (C * BV) + (size_t)i * BV;
+                float* urow = Udst + (size_t)cb * (C * BV) + (size_t)i * BV;
 #pragma unroll
                 for (int u = 0; u < 8; ++u)
                     reinterpret_cast<float4*>(urow)[u] =
@@ -568,7 +549,7 @@ __device__ __forceinline__ uint32_t chain_bar_count(int i) {
 }
 
 template <bool kKDA>
-__global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
+__global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
     using S = ChainSmem<kKDA>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -663,10 +644,10 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
                 const uint32_t st = base + s * S::kStage;
                 const uint32_t sS = base + S::kSh + sb * S::kSBuf;
                 const uint64_t dSpair = dmn64(sS, D * BV * 2), dSh = dmn64(sS, 512);
-                if (!tc::mbar_wait(bar(kFull0 + s), (c >> 1) & 1, abort_flag)) { fail(); break; }
+                if (!tc::mbar_spin(bar(kFull0 + s), (c >> 1) & 1, abort_flag)) { fail(); break; }
                 if (role == 1) GDR_TRACE_POINT(2, c);
-                if (role == 3 && c >= 2 && !tc::mbar_wait(bar(kOFree0 + ob), ((c >> 1) - 1) & 1, abort_flag)) { fail(); break; }
-                if (!tc::mbar_wait(bar(kSReady), c & 1, abort_flag)) { fail(); break; }
+                if (role == 3 && c >= 2 && !tc::mbar_spin(bar(kOFree0 + ob), ((c >> 1) - 1) & 1, abort_flag)) { fail(); break; }
+                if (!tc::mbar_spin(bar(kSReady), c & 1, abort_flag)) { fail(); break; }
                 if (role == 1) GDR_TRACE_POINT(3, c);
                 tc::fence_after();
                 issued = true;
@@ -674,7 +655,7 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
                     tc::mma_ksteps<8>(tD1, dk128(st + S::kW), a128, dSpair, 64, id64, true);
                     tc::mma_commit(bar(kD1Full));
                     GDR_TRACE_POINT(4, c);
-                    if (!tc::mbar_wait(bar(kNReady), c & 1, abort_flag)) { fail(); break; }
+                    if (!tc::mbar_spin(bar(kNReady), c & 1, abort_flag)) { fail(); break; }
                     GDR_TRACE_POINT(5, c);
                     tc::fence_after();
                     tc::mma_ksteps<4>(tD2, dmn128(st + S::kKt), amn, dNpair, 64, id2w, true);
@@ -687,9 +668,19 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
                     tc::mma_commit(bar(kD1Full));
                     tc::mma_commit(bar(kEmpty0 + s));
                 } else {
+                    // With a double-buffered state operand the output MMAs wait for the
+                    // state-update MMA so they never compete with the chain in the
+                    // tensor pipe; with one buffer they must finish before the
+                    // buffer is rewritten, so they go first.
+                    if (S::kSBufs == 2) {
+                        if (!tc::mbar_spin(bar(kD2Full), c & 1, abort_flag)) { fail(); break; }
+                        tc::fence_after();
+                    }
                     tc::mma_ksteps<8>(tO + 64 * ob, dk128(st + S::kQd), a128, dSpair, 64, id64, true);
-                    if (!tc::mbar_wait(bar(kNReady), c & 1, abort_flag)) { fail(); break; }
-                    tc::fence_after();
+                    if (S::kSBufs == 1) {
+                        if (!tc::mbar_spin(bar(kNReady), c & 1, abort_flag)) { fail(); break; }
+                        tc::fence_after();
+                    }
                     tc::mma_ksteps<4>(tO + 64 * ob, dk128(st + S::kP), a64, dN, 64, id32, false);
                     tc::mma_commit(bar(kOFull0 + ob));
                     tc::mma_commit(bar(kEmpty0 + s));
@@ -698,24 +689,29 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
             if (issued) {  // every MMA this thread issued finished before the CTA leaves
                 const int dr = role == 1 ? kDrainA : role == 2 ? kDrainB : kDrainC;
                 tc::mma_commit(bar(dr));
-                tc::mbar_wait(bar(dr), 0, abort_flag);
+                tc::mbar_spin(bar(dr), 0, abort_flag);
             }
         }
         __syncwarp();
-    } else if (warp >= 4 && warp < 8) {
-        // ------------------------------ state warpgroup ------------------------------
-        const int t = tid - 128;                 // = TMEM lane = row k of S^T
-        const int q = warp & 3;
+    } else if (warp >= 4 && warp < 12) {
+        // ------------------------------ state group ------------------------------
+        // Eight warps: warp w owns TMEM lane quadrant w % 4 (rows k of S^T, or
+        // rows i of the M = 64 N accumulator in lanes 0..15 of the quadrant) and
+        // the 16-column half hf of the block's 32 value columns.
+        const int q = warp & 3, hf = (warp - 4) >> 2;
+        const int t = 32 * q + lane;            // TMEM lane = row k of S^T
+        const bool lead = warp == 4 && lane == 0;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const bool nrow = lane < 16;            // owns row i of the M=64 N accumulator
         const int i = 16 * q + lane;
-        float Sreg[BV];
+        const int vh = 16 * hf;                 // first column of this thread's half
+        float Sreg[16];
         if (p.h0) {
 #pragma unroll
-            for (int v = 0; v < BV; ++v) Sreg[v] = p.h0[(((size_t)b * p.Hv + h) * D + v0 + v) * D + t];
+            for (int v = 0; v < 16; ++v) Sreg[v] = p.h0[(((size_t)b * p.Hv + h) * D + v0 + vh + v) * D + t];
         } else {
 #pragma unroll
-            for (int v = 0; v < BV; ++v) Sreg[v] = 0.f;
+            for (int v = 0; v < 16; ++v) Sreg[v] = 0.f;
         }
         for (int c = 0; c < nc; ++c) {
             const int s = c & 1, sb = S::kSBufs == 2 ? (c & 1) : 0;
@@ -729,110 +725,93 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
                 const int j = c - S::kSBufs;
                 if (!tc::mbar_wait(bar(kOFull0 + (j & 1)), (j >> 1) & 1, abort_flag)) fail();
             }
-            if (t == 0) GDR_TRACE_POINT(21, c);
+            if (lead) GDR_TRACE_POINT(21, c);
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
+            for (int cc = 0; cc < 2; ++cc) {
                 uint32_t hw[4], lw[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    float hh[2], ll[2];
-                    tc::split_bf16(Sreg[8 * ch + 2 * u], hh[0], ll[0]);
-                    tc::split_bf16(Sreg[8 * ch + 2 * u + 1], hh[1], ll[1]);
-                    hw[u] = tc::pack_bf16(hh[0], hh[1]);
-                    lw[u] = tc::pack_bf16(ll[0], ll[1]);
-                }
-                const uint32_t off = tc::chunk_mn64(t, ch);
+                for (int u = 0; u < 4; ++u) tc::split2(Sreg[8 * cc + 2 * u], Sreg[8 * cc + 2 * u + 1], hw[u], lw[u]);
+                const uint32_t off = tc::chunk_mn64(t, 2 * hf + cc);
                 *reinterpret_cast<uint4*>(sSh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                 *reinterpret_cast<uint4*>(sSl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
-            if (t == 0) GDR_TRACE_POINT(19, c);
+            if (lead) GDR_TRACE_POINT(19, c);
             tc::fence_proxy_async();
-            if (t == 0) GDR_TRACE_POINT(20, c);
+            if (lead) GDR_TRACE_POINT(20, c);
             tc::fence_before();
-            tc::bar_sync(1, 128);
-            if (t == 0) {
+            tc::bar_sync(1, 256);
+            if (lead) {
                 GDR_TRACE_POINT(8, c);
                 tc::mbar_arrive(bar(kSReady));
             }
             if (!tc::mbar_wait(bar(kFull0 + s), (c >> 1) & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
-            if (t == 0) GDR_TRACE_POINT(7, c);
+            if (lead) GDR_TRACE_POINT(7, c);
             const float* rec = reinterpret_cast<const float*>(stg + S::kRec_);
             const float colf = rec[64 + t];
             const float rowf = nrow ? rec[i] : 0.f;
             const int Lc = reinterpret_cast<const int*>(rec)[192];
-            float uv[BV];
+            float uv[16];
             if (nrow) {
-                const float4* ur = reinterpret_cast<const float4*>(stg + S::kU + (size_t)i * BV * 4);
+                const float4* ur = reinterpret_cast<const float4*>(stg + S::kU + ((size_t)i * BV + vh) * 4);
 #pragma unroll
-                for (int u = 0; u < BV / 4; ++u) {
+                for (int u = 0; u < 4; ++u) {
                     const float4 x = ur[u];
                     uv[4 * u] = x.x; uv[4 * u + 1] = x.y; uv[4 * u + 2] = x.z; uv[4 * u + 3] = x.w;
                 }
             }
             // N = U - W S^T  ->  N' = rowf * N (hi, lo), N (bf16, masked)
             if (!tc::mbar_wait(bar(kD1Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
-            if (t == 0) GDR_TRACE_POINT(9, c);
+            if (lead) GDR_TRACE_POINT(9, c);
             tc::fence_after();
-            float dv[2 * BV];
-            tc::tmem_ld64(tD1 + lane_base, dv);
-#pragma unroll
-            for (int v = 0; v < BV; ++v) dv[v] += dv[BV + v];
-            tc::tmem_ld32(tD1b + lane_base, dv + BV);  // reuse the upper half for the W_lo part
-#pragma unroll
-            for (int v = 0; v < BV; ++v) dv[v] += dv[BV + v];
-            if (t == 0) GDR_TRACE_POINT(15, c);
+            float dv[48];
+            tc::tmem_ld16x3(tD1 + lane_base + vh, tD1 + lane_base + BV + vh, tD1b + lane_base + vh, dv);
+            if (lead) GDR_TRACE_POINT(15, c);
             // the N tiles were last read by the output product of chunk c - 1
             if (c >= 1 && !tc::mbar_wait(bar(kOFull0 + ((c - 1) & 1)), ((c - 1) >> 1) & 1, abort_flag)) fail();
-            if (t == 0) GDR_TRACE_POINT(16, c);
+            if (lead) GDR_TRACE_POINT(16, c);
             if (nrow) {
                 const float keep = i < Lc ? 1.f : 0.f;  // rows past the chunk end
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
+                for (int cc = 0; cc < 2; ++cc) {
                     uint32_t hw[4], lw[4], nw[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        float hh[2], ll[2], nn[2];
-#pragma unroll
-                        for (int w = 0; w < 2; ++w) {
-                            const int v = 8 * ch + 2 * u + w;
-                            const float nval = (uv[v] - dv[v]) * keep;
-                            nn[w] = nval;
-                            tc::split_bf16(nval * rowf, hh[w], ll[w]);
-                        }
-                        hw[u] = tc::pack_bf16(hh[0], hh[1]);
-                        lw[u] = tc::pack_bf16(ll[0], ll[1]);
-                        nw[u] = tc::pack_bf16(nn[0], nn[1]);
+                        const int v = 8 * cc + 2 * u;
+                        const float n0 = (uv[v] - (dv[v] + dv[16 + v] + dv[32 + v])) * keep;
+                        const float n1 = (uv[v + 1] - (dv[v + 1] + dv[17 + v] + dv[33 + v])) * keep;
+                        tc::split2(n0 * rowf, n1 * rowf, hw[u], lw[u]);
+                        nw[u] = tc::pack_bf16(n0, n1);
                     }
-                    const uint32_t off = tc::chunk_mn64(i, ch);
+                    const uint32_t off = tc::chunk_mn64(i, 2 * hf + cc);
                     *reinterpret_cast<uint4*>(sm + S::kNh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                     *reinterpret_cast<uint4*>(sm + S::kNl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                     *reinterpret_cast<uint4*>(sm + S::kN + off) = make_uint4(nw[0], nw[1], nw[2], nw[3]);
                 }
             }
-            if (t == 0) GDR_TRACE_POINT(17, c);
+            if (lead) GDR_TRACE_POINT(17, c);
             tc::fence_proxy_async();
-            if (t == 0) GDR_TRACE_POINT(18, c);
+            if (lead) GDR_TRACE_POINT(18, c);
             tc::fence_before();
-            tc::bar_sync(1, 128);
-            if (t == 0) {
+            tc::bar_sync(1, 256);
+            if (lead) {
                 GDR_TRACE_POINT(10, c);
                 tc::mbar_arrive(bar(kNReady));
             }
-            // S^T <- colf * S^T + dS^T
+            // S^T <- colf * S^T + dS^T  (hi and lo halves of the accumulator summed)
             if (!tc::mbar_wait(bar(kD2Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
-            if (t == 0) GDR_TRACE_POINT(11, c);
+            if (lead) GDR_TRACE_POINT(11, c);
             tc::fence_after();
-            tc::tmem_ld64(tD2 + lane_base, dv);
+            tc::tmem_ld16x3(tD2 + lane_base + vh, tD2 + lane_base + BV + vh, tD2 + lane_base + vh, dv);
 #pragma unroll
-            for (int v = 0; v < BV; ++v) Sreg[v] = fmaf(colf, Sreg[v], dv[v] + dv[BV + v]);
-            if (t == 0) GDR_TRACE_POINT(12, c);
+            for (int v = 0; v < 16; ++v) Sreg[v] = fmaf(colf, Sreg[v], dv[v] + dv[16 + v]);
+            if (lead) GDR_TRACE_POINT(12, c);
             tc::fence_before();
         }
         if (p.hT && !*abort_flag) {
 #pragma unroll
-            for (int v = 0; v < BV; ++v) p.hT[(((size_t)b * p.Hv + h) * D + v0 + v) * D + t] = Sreg[v];
+            for (int v = 0; v < 16; ++v) p.hT[(((size_t)b * p.Hv + h) * D + v0 + vh + v) * D + t] = Sreg[v];
         }
-    } else if (warp >= 8) {
+    } else if (warp >= 12) {
         // ------------------------------ output warpgroup ------------------------------
         const int q = warp & 3;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
@@ -841,7 +820,7 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
         for (int c = 0; c < nc; ++c) {
             const int ob = c & 1;
             if (!tc::mbar_wait(bar(kOFull0 + ob), (c >> 1) & 1, abort_flag)) fail();
-            if (tid == 256) GDR_TRACE_POINT(13, c);
+            if (tid == 384) GDR_TRACE_POINT(13, c);
             tc::fence_after();
             float ov[2 * BV];
             tc::tmem_ld64(tO + 64 * ob + lane_base, ov);
@@ -859,7 +838,7 @@ __global__ void __launch_bounds__(384, 1) chunk_chain_kernel(TcParams p) {
             }
             tc::fence_before();
             tc::bar_sync(2, 128);
-            if (tid == 256) {
+            if (tid == 384) {
                 GDR_TRACE_POINT(14, c);
                 tc::mbar_arrive(bar(kOFree0 + ob));
             }
@@ -932,20 +911,20 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* w
         cudaFuncSetAttribute(chunk_chain_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smc);
         {
             KernelTimer kt("chunk_prep", stream);
-            chunk_prep_kernel<true><<<dim3((unsigned)mc, a.Hv), 128, smp, stream>>>(p);
+            chunk_prep_kernel<true><<<dim3((unsigned)mc, a.Hv), kPrepThreads, smp, stream>>>(p);
         }
         KernelTimer kt("chunk_chain", stream);
-        chunk_chain_kernel<true><<<dim3(a.Hv * NVB, a.N), 384, smc, stream>>>(p);
+        chunk_chain_kernel<true><<<dim3(a.Hv * NVB, a.N), 512, smc, stream>>>(p);
     } else {
         const int smp = PrepSmem<false>::kTotal, smc = ChainSmem<false>::kTotal;
         cudaFuncSetAttribute(chunk_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smp);
         cudaFuncSetAttribute(chunk_chain_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smc);
         {
             KernelTimer kt("chunk_prep", stream);
-            chunk_prep_kernel<false><<<dim3((unsigned)mc, a.Hv), 128, smp, stream>>>(p);
+            chunk_prep_kernel<false><<<dim3((unsigned)mc, a.Hv), kPrepThreads, smp, stream>>>(p);
         }
         KernelTimer kt("chunk_chain", stream);
-        chunk_chain_kernel<false><<<dim3(a.Hv * NVB, a.N), 384, smc, stream>>>(p);
+        chunk_chain_kernel<false><<<dim3(a.Hv * NVB, a.N), 512, smc, stream>>>(p);
     }
     return cudaGetLastError();
 }

@@ -162,9 +162,12 @@ __device__ __forceinline__ bool mbar_try(uint32_t mbar, uint32_t parity) {
                  "selp.b32 %0, 1, 0, P1;\n\t}\n" : "=r"(done) : "r"(mbar), "r"(parity) : "memory");
     return done != 0;
 }
-// Returns false if the wait gave up or `abort` (shared flag) was raised.
+__device__ __forceinline__ bool mbar_test(uint32_t mbar, uint32_t parity);
+
+// Returns false if the wait gave up or `abort` (shared flag) was raised.  A
+// phase that has already completed is detected with a non-suspending test.
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, volatile int* abort) {
-    if (mbar_try(mbar, parity)) return true;
+    if (mbar_test(mbar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try(mbar, parity)) return true;
@@ -197,11 +200,58 @@ __device__ __forceinline__ void bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
 }
 
+// Non-suspending variant for a single polling thread (the MMA issuers).
+__device__ __forceinline__ bool mbar_test(uint32_t mbar, uint32_t parity) {
+    uint32_t done;
+    asm volatile("{\n\t.reg .pred P1;\n\tmbarrier.test_wait.parity.shared::cta.b64 P1, [%1], %2;\n\t"
+                 "selp.b32 %0, 1, 0, P1;\n\t}\n" : "=r"(done) : "r"(mbar), "r"(parity) : "memory");
+    return done != 0;
+}
+__device__ __forceinline__ bool mbar_spin(uint32_t mbar, uint32_t parity, volatile int* abort) {
+    if (mbar_test(mbar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test(mbar, parity)) return true;
+        if ((i & 255) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        }
+    }
+}
+
+// 16 consecutive fp32 columns of this thread's lane from each of three
+// addresses, one wait.
+__device__ __forceinline__ void tmem_ld16x3(uint32_t a0, uint32_t a1, uint32_t a2, float* v) {
+    uint32_t r[48];
+#define GDR_LD16(base, addr)                                                                                \
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];" \
+                 : "=r"(r[base + 0]), "=r"(r[base + 1]), "=r"(r[base + 2]), "=r"(r[base + 3]), "=r"(r[base + 4]), \
+                   "=r"(r[base + 5]), "=r"(r[base + 6]), "=r"(r[base + 7]), "=r"(r[base + 8]), "=r"(r[base + 9]), \
+                   "=r"(r[base + 10]), "=r"(r[base + 11]), "=r"(r[base + 12]), "=r"(r[base + 13]),              \
+                   "=r"(r[base + 14]), "=r"(r[base + 15])                                                       \
+                 : "r"(addr))
+    GDR_LD16(0, a0);
+    GDR_LD16(16, a1);
+    GDR_LD16(32, a2);
+#undef GDR_LD16
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 48; ++j) v[j] = __uint_as_float(r[j]);
+}
+
 // ---- bf16 packing -------------------------------------------------------------
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t*>(&t);
 }
+// Two values x0, x1 -> packed bf16 pairs hi = (bf16(x0), bf16(x1)) and
+// lo = (bf16(x0 - hi0), bf16(x1 - hi1)).
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16(x0, x1);
+    const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
+    lo = pack_bf16(x0 - h0, x1 - h1);
+}
+
 // x = hi + lo with hi = bf16(x), lo = bf16(x - hi)
 __device__ __forceinline__ void split_bf16(float x, float& hi, float& lo) {
     hi = __bfloat162float(__float2bfloat16_rn(x));
