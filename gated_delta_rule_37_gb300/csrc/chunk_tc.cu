@@ -198,7 +198,8 @@ struct PrepSmem {
     static constexpr uint32_t kKgh = (kZ + 3 * 256 * 4 + 1023) & ~1023u;  // K o e^Gam hi (channel gate)
     static constexpr uint32_t kKgl = kKgh + (kKDA ? kTile64x128 : 0);
     static constexpr uint32_t kGam = kKgl + (kKDA ? kTile64x128 : 0);    // fp32 [64][128] or [64]
-    static constexpr uint32_t kBeta = kGam + (kKDA ? C * D * 4 : C * 4);
+    static constexpr uint32_t kDec = kGam + (kKDA ? C * D * 4 : C * 4);  // fp32 [64][128] e^{gk} (channel gate)
+    static constexpr uint32_t kBeta = kDec + (kKDA ? C * D * 4 : 0);
     static constexpr uint32_t kBar = kBeta + C * 4;
     static constexpr uint32_t kTotal = kBar + 64 + 1024;  // + alignment slack
     static_assert(kT2l + kTile64x64 <= kTm, "T'' tiles overlap Tm");
@@ -254,11 +255,13 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
             float x[C];
 #pragma unroll
             for (int i = 0; i < C; ++i) x[i] = i < L ? __ldg(gk + (size_t)i * p.Hv * D) : 0.f;
+            float* dec = reinterpret_cast<float*>(sm + S::kDec);
             float acc = 0.f;
 #pragma unroll
             for (int i = 0; i < C; ++i) {
                 acc += x[i];
                 gam[i * D + tid] = acc;
+                dec[i * D + tid] = __expf(x[i]);  // per-token decay, <= 1
             }
         }
     } else if (warp < 2) {
@@ -378,21 +381,63 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
                     make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
         }
     } else {
-        // per-channel decays: A_ij = beta_i sum_c k_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}
-        const __nv_bfloat16* Xt = reinterpret_cast<const __nv_bfloat16*>(sm + S::kX);
-        for (int e = tid; e < C * C; e += NT) {
-            const int i = e >> 6, j = e & 63;
-            float a = 0.f, pv = 0.f;
-            if (j <= i && i < L) {
-                for (int c = 0; c < D; ++c) {
-                    const float ex = __expf(gam[i * D + c] - gam[j * D + c]);
-                    const float kj = __bfloat162float(Xt[tc::off_k128(j, c, 2 * C) >> 1]) * ex;
-                    a = fmaf(__bfloat162float(Xt[tc::off_k128(i, c, 2 * C) >> 1]), kj, a);
-                    pv = fmaf(__bfloat162float(Xt[tc::off_k128(C + i, c, 2 * C) >> 1]), kj, pv);
+        // Per-channel decays: A_ij = beta_i sum_c k_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}
+        // and P_ij = sum_c q_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}.  The factor is the
+        // running product of the per-token decays e^{gk_t} (t = j+1..i), all <= 1,
+        // so every intermediate is bounded for any finite gate.  Warp w handles
+        // columns j = w, w+8, ...; lane l holds key channels 4l..4l+3; 32 rows
+        // are reduced over the channels at once with the halving butterfly.
+        const float* dec = reinterpret_cast<const float*>(sm + S::kDec);
+        float* Pf = Tm;  // fp32 [64][65] staging for P (Tm is rebuilt by the solve)
+        for (int j = warp; j < C; j += NT / 32) {
+            const uint2 kjr = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(j, 4 * lane, 2 * C));
+            const __nv_bfloat16* kjb = reinterpret_cast<const __nv_bfloat16*>(&kjr);
+            float kj[4], d[4] = {1.f, 1.f, 1.f, 1.f};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) kj[u] = __bfloat162float(kjb[u]);
+            for (int base = j; base < C; base += 32) {
+                float xa[32], xp[32];
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int i = base + u;
+                    float pa = 0.f, pq = 0.f;
+                    if (i < C) {
+                        const float4 dv4 = *reinterpret_cast<const float4*>(dec + i * D + 4 * lane);
+                        if (i > j) { d[0] *= dv4.x; d[1] *= dv4.y; d[2] *= dv4.z; d[3] *= dv4.w; }
+                        const uint2 kir = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(i, 4 * lane, 2 * C));
+                        const uint2 qir = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(C + i, 4 * lane, 2 * C));
+                        const __nv_bfloat16* kib = reinterpret_cast<const __nv_bfloat16*>(&kir);
+                        const __nv_bfloat16* qib = reinterpret_cast<const __nv_bfloat16*>(&qir);
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const float kd = kj[w] * d[w];
+                            pa = fmaf(__bfloat162float(kib[w]), kd, pa);
+                            pq = fmaf(__bfloat162float(qib[w]), kd, pq);
+                        }
+                    }
+                    xa[u] = pa;
+                    xp[u] = pq;
+                }
+                const float ra = reduce32_to_lane(xa, lane);
+                const float rp = reduce32_to_lane(xp, lane);
+                const int i = base + lane;
+                if (i < C) {
+                    As[i * LDA + j] = (j < i && i < L) ? bet[i] * ra : 0.f;
+                    Pf[i * LDA + j] = (j <= i && i < L) ? rp : 0.f;
                 }
             }
-            As[i * LDA + j] = (j < i) ? bet[i] * a : 0.f;
-            reinterpret_cast<__nv_bfloat16*>(Pdst)[tc::off_k128(i, j, C) >> 1] = __float2bfloat16_rn(pv);
+        }
+        for (int e = tid; e < C * C; e += NT) {  // entries j > i never written above
+            const int i = e >> 6, j = e & 63;
+            if (j > i) { As[i * LDA + j] = 0.f; Pf[i * LDA + j] = 0.f; }
+        }
+        __syncthreads();
+        for (int e = tid; e < C * 8; e += NT) {
+            const int i = e >> 3, ch = e & 7;
+            uint32_t w4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) w4[u] = tc::pack_bf16(Pf[i * LDA + ch * 8 + 2 * u], Pf[i * LDA + ch * 8 + 2 * u + 1]);
+            *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(i, ch, C)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
         // K o e^{Gam} as hi / lo for W
         for (int e = tid; e < C * 16; e += NT) {
