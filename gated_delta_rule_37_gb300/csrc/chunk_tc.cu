@@ -74,6 +74,8 @@ constexpr uint32_t kTile64x128 = C * D * 2;       // 16 KB bf16 [64][128]
 constexpr uint32_t kTile64x64 = C * C * 2;        // 8 KB bf16 [64][64]
 constexpr uint32_t kUBlock = C * BV * 4;          // 8 KB fp32 [64][32]
 constexpr uint32_t kRec = 1024;                   // rowf[64], colf[128], L
+constexpr uint32_t kXwBytes = 2 * kTile64x128;    // 32 KB stacked [W_hi ; Qd]
+constexpr uint32_t kYwBytes = 3 * C * 128;        // 24 KB stacked [W_lo ; P] without its last 8 KB
 
 struct TcParams {
     const void* q;
@@ -90,10 +92,9 @@ struct TcParams {
     const int* offsets;
     const int4* table;
     const int* order;
-    unsigned char* Wb;   // [chunk][Hv][2][16 KB]
+    unsigned char* Xw;   // [chunk][Hv][32 KB]: k128 128 rows = [W_hi ; Qd]
     unsigned char* Ub;   // [chunk][Hv][NVB][8 KB]
-    unsigned char* Qb;   // [chunk][Hv][16 KB]
-    unsigned char* Pb;   // [chunk][Hv][8 KB]
+    unsigned char* Yw;   // [chunk][Hv][24 KB]: k128 128 rows = [W_lo ; P] (column block 1: W_lo only)
     unsigned char* Kb;   // scalar gate: [chunk][Hk][16 KB]; channel gate: [chunk][Hv][2][16 KB]
     unsigned char* Rb;   // [chunk][Hv][1 KB]
     unsigned int* err;
@@ -301,7 +302,7 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
 
     // ---- while that runs: Qd blob, K / Kd blob, decay record ------------------------
     {
-        unsigned char* Qdst = p.Qb + ((size_t)chunk * p.Hv + h) * kTile64x128;
+        unsigned char* Qdst = p.Xw + ((size_t)chunk * p.Hv + h) * kXwBytes;  // rows 64..127
         for (int e = tid; e < C * 16; e += NT) {
             const int i = e >> 4, ch = e & 15;
             const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(C + i, ch, 2 * C));
@@ -313,7 +314,7 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
                 w4[u] = tc::pack_bf16(__bfloat162float(qv[2 * u]) * __expf(gm(i, c)),
                                       __bfloat162float(qv[2 * u + 1]) * __expf(gm(i, c + 1)));
             }
-            *reinterpret_cast<uint4*>(Qdst + tc::chunk_k128(i, ch, C)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            *reinterpret_cast<uint4*>(Qdst + tc::chunk_k128(C + i, ch, 2 * C)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
         if (!kKDA) {
             if (h % grp == 0) {  // K rows of X, both column blocks -> a [64][128] k128 image
@@ -350,7 +351,7 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
     GDR_TRACE_PREP(2);
 
     // ---- A (strictly lower) and P (lower incl. diagonal) -------------------------
-    unsigned char* Pdst = p.Pb + ((size_t)chunk * p.Hv + h) * kTile64x64;
+    unsigned char* Pdst = p.Yw + ((size_t)chunk * p.Hv + h) * kYwBytes;  // rows 64..127 of column block 0
     if (!kKDA) {
         if (!tc::mbar_wait(bar0, 0, abort_flag)) raise_error(p, 1u);
         tc::fence_after();
@@ -377,7 +378,7 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
             }
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc)
-                *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(i, 4 * hf + cc, C)) =
+                *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(C + i, 4 * hf + cc, 2 * C)) =
                     make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
         }
     } else {
@@ -437,7 +438,7 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
             uint32_t w4[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) w4[u] = tc::pack_bf16(Pf[i * LDA + ch * 8 + 2 * u], Pf[i * LDA + ch * 8 + 2 * u + 1]);
-            *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(i, ch, C)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(C + i, ch, 2 * C)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
         // K o e^{Gam} as hi / lo for W
         for (int e = tid; e < C * 16; e += NT) {
@@ -522,7 +523,8 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
     {
         const int i = 16 * q + (lane & 15);
         const uint32_t lrow = tmem + ((uint32_t)(32 * q) << 16);
-        unsigned char* Wdst = p.Wb + ((size_t)chunk * p.Hv + h) * 2 * kTile64x128;
+        unsigned char* Whi = p.Xw + ((size_t)chunk * p.Hv + h) * kXwBytes;  // rows 0..63
+        unsigned char* Wlo = p.Yw + ((size_t)chunk * p.Hv + h) * kYwBytes;  // rows 0..63
         float* Udst = reinterpret_cast<float*>(p.Ub + ((size_t)chunk * p.Hv + h) * NVB * kUBlock);
         for (int q2 = 0; q2 < 2; ++q2) {
             const int cb = 2 * hf + q2;  // 32-column block of W and of U
@@ -535,9 +537,9 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
                     uint32_t hw[4], lw[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) tc::split2(wv[8 * cc + 2 * u], wv[8 * cc + 2 * u + 1], hw[u], lw[u]);
-                    const uint32_t off = tc::chunk_k128(i, 4 * cb + cc, C);
-                    *reinterpret_cast<uint4*>(Wdst + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4*>(Wdst + kTile64x128 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    const uint32_t off = tc::chunk_k128(i, 4 * cb + cc, 2 * C);
+                    *reinterpret_cast<uint4*>(Whi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4*>(Wlo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 }
                 float* urow = Udst + (size_t)cb * (C * BV) + (size_t)i * BV;
 #pragma unroll
@@ -561,22 +563,17 @@ template <bool kKDA>
 struct ChainSmem {
     static constexpr uint32_t kKtBytes = kKDA ? 2 * kTile64x128 : kTile64x128;
     // one pipeline stage
-    static constexpr uint32_t kW = 0;
-    static constexpr uint32_t kKt = kW + 2 * kTile64x128;
-    static constexpr uint32_t kQd = kKt + kKtBytes;
-    static constexpr uint32_t kP = kQd + kTile64x128;
-    static constexpr uint32_t kU = kP + kTile64x64;
-    static constexpr uint32_t kRec_ = kU + kUBlock;
+    static constexpr uint32_t kXW = 0;                     // [W_hi ; Qd]   k128, 128 rows (32 KB)
+    static constexpr uint32_t kYW = kXW + kXwBytes;        // [W_lo ; P | U] k128, 128 rows (32 KB)
+    static constexpr uint32_t kU = kYW + kYwBytes;         // U fp32 [64][32] in the last 8 KB of YW
+    static constexpr uint32_t kKt = kYW + 2 * kTile64x128;
+    static constexpr uint32_t kRec_ = kKt + kKtBytes;
     static constexpr uint32_t kStage = kRec_ + kRec;
     static constexpr uint32_t kStageTx = kStage;  // bytes landed per stage
-    // resident tiles.  The scalar gate double-buffers the state operand so the
-    // output MMAs of chunk c can run after the state update of chunk c; the
-    // channel gate (larger stages) keeps one buffer and issues them earlier.
-    static constexpr int kSBufs = kKDA ? 1 : 2;
-    static constexpr uint32_t kSh = 2 * kStage;              // S^T hi [128][32] mn64 (x kSBufs)
-    static constexpr uint32_t kSl = kSh + D * BV * 2;        // S^T lo
-    static constexpr uint32_t kSBuf = 2 * D * BV * 2;        // bytes per state buffer (hi + lo)
-    static constexpr uint32_t kNh = kSh + kSBufs * kSBuf;    // N' hi [64][32] mn64
+    // resident tiles
+    static constexpr uint32_t kSh = 2 * kStage;              // S^T hi [128][32] mn64
+    static constexpr uint32_t kSl = kSh + D * BV * 2;        // S^T lo (the next atom: [S_hi | S_lo])
+    static constexpr uint32_t kNh = kSl + D * BV * 2;        // N' hi [64][32] mn64
     static constexpr uint32_t kNl = kNh + C * BV * 2;        // N' lo
     static constexpr uint32_t kN = kNl + C * BV * 2;         // N (bf16) for the output
     static constexpr uint32_t kBar = kN + C * BV * 2;
@@ -588,8 +585,10 @@ enum ChainBar {
     kDrainA, kDrainB, kDrainC, kNumBars
 };
 // Arrival counts: the N accumulator is committed by issuers A and B, a stage is
-// released by all three issuers, everything else by one arrival.
+// released by all three issuers, the state operands are published by each of
+// the eight state-group warps, everything else by one arrival.
 __device__ __forceinline__ uint32_t chain_bar_count(int i) {
+    if (i == kSReady || i == kNReady) return 8u;  // one arrival per state-group warp
     return i == kD1Full ? 2u : (i == kEmpty0 || i == kEmpty1) ? 3u : 1u;
 }
 
@@ -612,7 +611,7 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::kBar + 8 * kNumBars + 8);
     auto bar = [&](int i) { return tc::smem_u32(&bars[i]); };
 
-    if (warp == 2) tc::tmem_alloc(tc::smem_u32(tmem_slot), 512);
+    if (warp == 2) tc::tmem_alloc(tc::smem_u32(tmem_slot), 256);
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) tc::mbar_init(bar(i), chain_bar_count(i));
         *abort_flag = 0;
@@ -622,11 +621,14 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
-    // Accumulators: the hi and lo split terms of the state (or of N') sit side
-    // by side along N, so one N = 64 MMA forms two split products; columns v
-    // and 32 + v are summed when read.  D1a / D1b are the two halves of the N
-    // accumulator written by different issuing threads.
-    const uint32_t tD1 = tmem, tD1b = tmem + 64, tD2 = tmem + 128, tO = tmem + 256;  // O: +0 / +64
+    // Accumulators (fp32 TMEM columns).  The hi and lo split terms of the state
+    // (or of N') sit side by side along N, so one N = 64 MMA forms two split
+    // products; columns v and 32 + v are summed when read.
+    //   D1[2] (M=128, 64 columns, double-buffered): rows 0..63 = W_hi S^T (part
+    //         of the N accumulator), rows 64..127 = Qd S^T + P N (the output)
+    //   D1b   (M=128, 32 columns): rows 0..63 = W_lo S_hi^T
+    //   D2    (M=128, 64 columns): K^T [N'_hi | N'_lo]
+    const uint32_t tD1 = tmem, tD1b = tmem + 128, tD2 = tmem + 192;
     const uint32_t base = tc::smem_u32(sm);
     auto fail = [&]() {
         *abort_flag = 1;
@@ -644,12 +646,11 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                 const uint32_t st = base + s * S::kStage;
                 const uint32_t fb = bar(kFull0 + s);
                 tc::mbar_arrive_tx(fb, S::kStageTx);
-                tc::bulk_g2s(st + S::kW, p.Wb + (gc * p.Hv + h) * 2 * kTile64x128, 2 * kTile64x128, fb);
+                tc::bulk_g2s(st + S::kXW, p.Xw + (gc * p.Hv + h) * kXwBytes, kXwBytes, fb);
+                tc::bulk_g2s(st + S::kYW, p.Yw + (gc * p.Hv + h) * kYwBytes, kYwBytes, fb);
+                tc::bulk_g2s(st + S::kU, p.Ub + ((gc * p.Hv + h) * NVB + vb) * kUBlock, kUBlock, fb);
                 if (kKDA) tc::bulk_g2s(st + S::kKt, p.Kb + (gc * p.Hv + h) * 2 * kTile64x128, 2 * kTile64x128, fb);
                 else tc::bulk_g2s(st + S::kKt, p.Kb + (gc * p.Hk + kh) * kTile64x128, kTile64x128, fb);
-                tc::bulk_g2s(st + S::kQd, p.Qb + (gc * p.Hv + h) * kTile64x128, kTile64x128, fb);
-                tc::bulk_g2s(st + S::kP, p.Pb + (gc * p.Hv + h) * kTile64x64, kTile64x64, fb);
-                tc::bulk_g2s(st + S::kU, p.Ub + ((gc * p.Hv + h) * NVB + vb) * kUBlock, kUBlock, fb);
                 tc::bulk_g2s(st + S::kRec_, p.Rb + (gc * p.Hv + h) * kRec, kRec, fb);
                 GDR_TRACE_POINT(1, c);
             }
@@ -663,15 +664,17 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
         // A single thread issues a tcgen05.mma about every 60 cycles, well
         // below what the tensor pipe sustains for these shapes, so the work is
         // spread over three issuing threads, each committing its own MMAs:
-        //   A (warp 1): N partial W_hi [S_hi | S_lo], then dS = K^T [N'_hi | N'_lo]
-        //   B (warp 2): N partial W_lo S_hi            (in parallel with A)
-        //   C (warp 3): output O = Qd [S_hi | S_lo] + P N (off the state chain)
+        //   A (warp 1): D1 = [W_hi ; Qd] [S_hi | S_lo], then D2 = K^T [N'_hi | N'_lo]
+        //   B (warp 2): D1b = [W_lo ; P] S_hi            (in parallel with A)
+        //   C (warp 3): D1 rows 64..127 += P N           (after N is ready)
+        // Rows of a stacked operand that a product does not need land in
+        // accumulator rows nobody reads (or that are dead at that time).
         // Descriptors are built once per tile; a k-step adds its byte offset / 16
         // to the start-address field (tiles sit below 256 KB, so no carry).
         if (lane == 0) {
             const int role = warp;  // 1 = A, 2 = B, 3 = C
-            const uint32_t id64 = tc::idesc_bf16(64, 2 * BV, false, true);   // W_hi [S_hi|S_lo], Qd [S_hi|S_lo]
-            const uint32_t id32 = tc::idesc_bf16(64, BV, false, true);       // W_lo S_hi, P N
+            const uint32_t idA = tc::idesc_bf16(128, 2 * BV, false, true);   // [W_hi;Qd] [S_hi|S_lo]
+            const uint32_t idB = tc::idesc_bf16(128, BV, false, true);       // [W_lo;P] S_hi, [.;P] N
             const uint32_t id2w = tc::idesc_bf16(128, 2 * BV, true, true);   // K^T [N'_hi|N'_lo]
             const uint32_t id2n = tc::idesc_bf16(128, BV, true, true);       // Kd_lo^T N'_hi
             auto dk128 = [](uint32_t a) { return tc::smem_desc(a, 16, 1024, tc::kSwizzle128); };
@@ -679,25 +682,34 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             auto dmn64 = [](uint32_t a, uint32_t atom) { return tc::smem_desc(a, atom, 512, tc::kSwizzle64); };
             const uint64_t dNpair = dmn64(base + S::kNh, C * BV * 2), dNh = dmn64(base + S::kNh, 512);
             const uint64_t dN = dmn64(base + S::kN, 512);
-            constexpr uint32_t a128[8] = {0, 2, 4, 6, (C * 128) >> 4, ((C * 128) >> 4) + 2, ((C * 128) >> 4) + 4,
-                                          ((C * 128) >> 4) + 6};       // [64][128] k128: 32 B steps, 2 column blocks
-            constexpr uint32_t a64[4] = {0, 2, 4, 6};                  // [64][64] k128
+            const uint64_t dSpair = dmn64(base + S::kSh, D * BV * 2), dSh = dmn64(base + S::kSh, 512);
+            constexpr uint32_t a128[8] = {0, 2, 4, 6, (2 * C * 128) >> 4, ((2 * C * 128) >> 4) + 2,
+                                          ((2 * C * 128) >> 4) + 4, ((2 * C * 128) >> 4) + 6};  // 128-row k128, K = 128
+            constexpr uint32_t a64[4] = {0, 2, 4, 6};                  // 128-row k128, K = 64 (column block 0)
             constexpr uint32_t amn[4] = {0, 128, 256, 384};            // MN-major A: 2 x 8-row groups per step
             bool issued = false;
             for (int c = 0; c < nc; ++c) {
-                const int s = c & 1, ob = c & 1, sb = S::kSBufs == 2 ? (c & 1) : 0;
+                const int s = c & 1, ob = c & 1;
                 const uint32_t st = base + s * S::kStage;
-                const uint32_t sS = base + S::kSh + sb * S::kSBuf;
-                const uint64_t dSpair = dmn64(sS, D * BV * 2), dSh = dmn64(sS, 512);
                 if (!tc::mbar_spin(bar(kFull0 + s), (c >> 1) & 1, abort_flag)) { fail(); break; }
                 if (role == 1) GDR_TRACE_POINT(2, c);
-                if (role == 3 && c >= 2 && !tc::mbar_spin(bar(kOFree0 + ob), ((c >> 1) - 1) & 1, abort_flag)) { fail(); break; }
+                if (role == 3) {
+                    // output intra part once N is ready (implies D1 of this chunk complete)
+                    if (!tc::mbar_spin(bar(kNReady), c & 1, abort_flag)) { fail(); break; }
+                    tc::fence_after();
+                    issued = true;
+                    tc::mma_ksteps<4>(tD1 + 64 * ob, dk128(st + S::kYW), a64, dN, 64, idB, false);
+                    tc::mma_commit(bar(kOFull0 + ob));
+                    tc::mma_commit(bar(kEmpty0 + s));
+                    continue;
+                }
+                if (role == 1 && c >= 2 && !tc::mbar_spin(bar(kOFree0 + ob), ((c >> 1) - 1) & 1, abort_flag)) { fail(); break; }
                 if (!tc::mbar_spin(bar(kSReady), c & 1, abort_flag)) { fail(); break; }
                 if (role == 1) GDR_TRACE_POINT(3, c);
                 tc::fence_after();
                 issued = true;
                 if (role == 1) {
-                    tc::mma_ksteps<8>(tD1, dk128(st + S::kW), a128, dSpair, 64, id64, true);
+                    tc::mma_ksteps<8>(tD1 + 64 * ob, dk128(st + S::kXW), a128, dSpair, 64, idA, true);
                     tc::mma_commit(bar(kD1Full));
                     GDR_TRACE_POINT(4, c);
                     if (!tc::mbar_spin(bar(kNReady), c & 1, abort_flag)) { fail(); break; }
@@ -708,47 +720,30 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                     tc::mma_commit(bar(kD2Full));
                     tc::mma_commit(bar(kEmpty0 + s));
                     GDR_TRACE_POINT(6, c);
-                } else if (role == 2) {
-                    tc::mma_ksteps<8>(tD1b, dk128(st + S::kW + kTile64x128), a128, dSh, 64, id32, true);
-                    tc::mma_commit(bar(kD1Full));
-                    tc::mma_commit(bar(kEmpty0 + s));
                 } else {
-                    // With a double-buffered state operand the output MMAs wait for the
-                    // state-update MMA so they never compete with the chain in the
-                    // tensor pipe; with one buffer they must finish before the
-                    // buffer is rewritten, so they go first.
-                    if (S::kSBufs == 2) {
-                        if (!tc::mbar_spin(bar(kD2Full), c & 1, abort_flag)) { fail(); break; }
-                        tc::fence_after();
-                    }
-                    tc::mma_ksteps<8>(tO + 64 * ob, dk128(st + S::kQd), a128, dSpair, 64, id64, true);
-                    if (S::kSBufs == 1) {
-                        if (!tc::mbar_spin(bar(kNReady), c & 1, abort_flag)) { fail(); break; }
-                        tc::fence_after();
-                    }
-                    tc::mma_ksteps<4>(tO + 64 * ob, dk128(st + S::kP), a64, dN, 64, id32, false);
-                    tc::mma_commit(bar(kOFull0 + ob));
+                    tc::mma_ksteps<8>(tD1b, dk128(st + S::kYW), a128, dSh, 64, idB, true);
+                    tc::mma_commit(bar(kD1Full));
                     tc::mma_commit(bar(kEmpty0 + s));
                 }
             }
             if (issued) {  // every MMA this thread issued finished before the CTA leaves
                 const int dr = role == 1 ? kDrainA : role == 2 ? kDrainB : kDrainC;
                 tc::mma_commit(bar(dr));
-                tc::mbar_spin(bar(dr), 0, abort_flag);
+                tc::mbar_wait(bar(dr), 0, abort_flag);
             }
         }
         __syncwarp();
     } else if (warp >= 4 && warp < 12) {
         // ------------------------------ state group ------------------------------
-        // Eight warps: warp w owns TMEM lane quadrant w % 4 (rows k of S^T, or
-        // rows i of the M = 64 N accumulator in lanes 0..15 of the quadrant) and
-        // the 16-column half hf of the block's 32 value columns.
+        // Eight warps: warp w owns TMEM lane quadrant w % 4 (rows k of S^T) and
+        // the 16-column half hf of the block's 32 value columns; the N
+        // accumulator rows 0..63 sit in quadrants 0 and 1.
         const int q = warp & 3, hf = (warp - 4) >> 2;
         const int t = 32 * q + lane;            // TMEM lane = row k of S^T
         const bool lead = warp == 4 && lane == 0;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        const bool nrow = lane < 16;            // owns row i of the M=64 N accumulator
-        const int i = 16 * q + lane;
+        const bool nrow = q < 2;                // owns row i = t of the N accumulator
+        const int i = t;
         const int vh = 16 * hf;                 // first column of this thread's half
         float Sreg[16];
         if (p.h0) {
@@ -758,18 +753,13 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
 #pragma unroll
             for (int v = 0; v < 16; ++v) Sreg[v] = 0.f;
         }
+        unsigned char* sSh = sm + S::kSh;
+        unsigned char* sSl = sm + S::kSl;
         for (int c = 0; c < nc; ++c) {
-            const int s = c & 1, sb = S::kSBufs == 2 ? (c & 1) : 0;
+            const int s = c & 1, ob = c & 1;
             const unsigned char* stg = sm + s * S::kStage;
-            unsigned char* sSh = sm + S::kSh + sb * S::kSBuf;
-            unsigned char* sSl = sm + S::kSl + sb * S::kSBuf;
-            // S^T rows (hi, lo) into the MMA operand tiles.  The buffer was last
-            // read by chunk c - kSBufs: its N products finished before the last
-            // state update, its output product is covered by that chunk's o_full.
-            if (c >= S::kSBufs) {
-                const int j = c - S::kSBufs;
-                if (!tc::mbar_wait(bar(kOFull0 + (j & 1)), (j >> 1) & 1, abort_flag)) fail();
-            }
+            // S^T rows (hi, lo) into the MMA operand tiles.  Their readers (the N
+            // products of chunk c - 1) finished before the last state update.
             if (lead) GDR_TRACE_POINT(21, c);
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
@@ -781,14 +771,13 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                 *reinterpret_cast<uint4*>(sSl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
             if (lead) GDR_TRACE_POINT(19, c);
+            // publish: each warp fences its own stores and arrives once
             tc::fence_proxy_async();
             if (lead) GDR_TRACE_POINT(20, c);
             tc::fence_before();
-            tc::bar_sync(1, 256);
-            if (lead) {
-                GDR_TRACE_POINT(8, c);
-                tc::mbar_arrive(bar(kSReady));
-            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bar(kSReady));
+            if (lead) GDR_TRACE_POINT(8, c);
             if (!tc::mbar_wait(bar(kFull0 + s), (c >> 1) & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
             if (lead) GDR_TRACE_POINT(7, c);
             const float* rec = reinterpret_cast<const float*>(stg + S::kRec_);
@@ -809,7 +798,10 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             if (lead) GDR_TRACE_POINT(9, c);
             tc::fence_after();
             float dv[48];
-            tc::tmem_ld16x3(tD1 + lane_base + vh, tD1 + lane_base + BV + vh, tD1b + lane_base + vh, dv);
+            if (nrow) {  // quadrants 0 and 1 (warp-uniform)
+                tc::tmem_ld16x3(tD1 + 64 * ob + lane_base + vh, tD1 + 64 * ob + lane_base + BV + vh,
+                                tD1b + lane_base + vh, dv);
+            }
             if (lead) GDR_TRACE_POINT(15, c);
             // the N tiles were last read by the output product of chunk c - 1
             if (c >= 1 && !tc::mbar_wait(bar(kOFull0 + ((c - 1) & 1)), ((c - 1) >> 1) & 1, abort_flag)) fail();
@@ -837,11 +829,9 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             tc::fence_proxy_async();
             if (lead) GDR_TRACE_POINT(18, c);
             tc::fence_before();
-            tc::bar_sync(1, 256);
-            if (lead) {
-                GDR_TRACE_POINT(10, c);
-                tc::mbar_arrive(bar(kNReady));
-            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(bar(kNReady));
+            if (lead) GDR_TRACE_POINT(10, c);
             // S^T <- colf * S^T + dS^T  (hi and lo halves of the accumulator summed)
             if (!tc::mbar_wait(bar(kD2Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
             if (lead) GDR_TRACE_POINT(11, c);
@@ -857,29 +847,34 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             for (int v = 0; v < 16; ++v) p.hT[(((size_t)b * p.Hv + h) * D + v0 + vh + v) * D + t] = Sreg[v];
         }
     } else if (warp >= 12) {
-        // ------------------------------ output warpgroup ------------------------------
+        // ------------------------------ output warps ------------------------------
+        // The output rows 64..127 of D1 sit in lane quadrants 2 and 3: warps 14
+        // and 15 drain them; warps 12 and 13 only take part in the barriers.
         const int q = warp & 3;
+        const bool drain = q >= 2;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
-        const int i = 16 * q + lane;
+        const int i = 32 * (q - 2) + lane;
         __nv_bfloat16* op = static_cast<__nv_bfloat16*>(p.o);
         for (int c = 0; c < nc; ++c) {
             const int ob = c & 1;
             if (!tc::mbar_wait(bar(kOFull0 + ob), (c >> 1) & 1, abort_flag)) fail();
             if (tid == 384) GDR_TRACE_POINT(13, c);
             tc::fence_after();
-            float ov[2 * BV];
-            tc::tmem_ld64(tO + 64 * ob + lane_base, ov);
+            if (drain) {
+                float ov[2 * BV];
+                tc::tmem_ld64(tD1 + 64 * ob + lane_base, ov);
 #pragma unroll
-            for (int v = 0; v < BV; ++v) ov[v] += ov[BV + v];
-            const int cs = bos + c * C;
-            if (lane < 16 && cs + i < eos) {
-                uint4* dst = reinterpret_cast<uint4*>(op + ((size_t)(cs + i) * p.Hv + h) * D + v0);
+                for (int v = 0; v < BV; ++v) ov[v] += ov[BV + v];
+                const int cs = bos + c * C;
+                if (cs + i < eos) {
+                    uint4* dst = reinterpret_cast<uint4*>(op + ((size_t)(cs + i) * p.Hv + h) * D + v0);
 #pragma unroll
-                for (int u = 0; u < BV / 8; ++u)
-                    dst[u] = make_uint4(tc::pack_bf16(p.scale * ov[8 * u], p.scale * ov[8 * u + 1]),
-                                        tc::pack_bf16(p.scale * ov[8 * u + 2], p.scale * ov[8 * u + 3]),
-                                        tc::pack_bf16(p.scale * ov[8 * u + 4], p.scale * ov[8 * u + 5]),
-                                        tc::pack_bf16(p.scale * ov[8 * u + 6], p.scale * ov[8 * u + 7]));
+                    for (int u = 0; u < BV / 8; ++u)
+                        dst[u] = make_uint4(tc::pack_bf16(p.scale * ov[8 * u], p.scale * ov[8 * u + 1]),
+                                            tc::pack_bf16(p.scale * ov[8 * u + 2], p.scale * ov[8 * u + 3]),
+                                            tc::pack_bf16(p.scale * ov[8 * u + 4], p.scale * ov[8 * u + 5]),
+                                            tc::pack_bf16(p.scale * ov[8 * u + 6], p.scale * ov[8 * u + 7]));
+                }
             }
             tc::fence_before();
             tc::bar_sync(2, 128);
@@ -891,7 +886,7 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
     }
     tc::fence_before();
     __syncthreads();
-    if (warp == 2) tc::tmem_dealloc(tmem, 512);
+    if (warp == 2) tc::tmem_dealloc(tmem, 256);
 }
 
 // LPT order: sequence indices by decreasing length (ties by index).
@@ -916,10 +911,9 @@ __global__ void __launch_bounds__(1024) lpt_order_kernel(const int32_t* __restri
 
 size_t chunk_tc_blob_bytes(int64_t max_chunks, int Hk, int Hv, bool kda) {
     const size_t mc = (size_t)max_chunks;
-    size_t n = mc * Hv * 2 * kTile64x128;       // W
+    size_t n = mc * Hv * kXwBytes;              // [W_hi ; Qd]
     n += mc * Hv * NVB * kUBlock;               // U
-    n += mc * Hv * kTile64x128;                 // Qd
-    n += mc * Hv * kTile64x64;                  // P
+    n += mc * Hv * kYwBytes;                    // [W_lo ; P]
     n += kda ? mc * Hv * 2 * kTile64x128 : mc * Hk * kTile64x128;  // K / Kd
     n += mc * Hv * kRec;                        // records
     return n;
@@ -937,10 +931,9 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* w
     p.order = reinterpret_cast<const int*>(ws + w.off_order);
     const size_t mc = (size_t)w.max_chunks;
     unsigned char* blob = reinterpret_cast<unsigned char*>(ws + w.off_blobs);
-    p.Wb = blob; blob += mc * a.Hv * 2 * kTile64x128;
+    p.Xw = blob; blob += mc * a.Hv * kXwBytes;
     p.Ub = blob; blob += mc * a.Hv * NVB * kUBlock;
-    p.Qb = blob; blob += mc * a.Hv * kTile64x128;
-    p.Pb = blob; blob += mc * a.Hv * kTile64x64;
+    p.Yw = blob; blob += mc * a.Hv * kYwBytes;
     p.Kb = blob; blob += kda ? mc * a.Hv * 2 * kTile64x128 : mc * a.Hk * kTile64x128;
     p.Rb = blob;
     p.err = device_error_word();
