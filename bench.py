@@ -38,15 +38,17 @@ from gated_delta_rule_37_gb300 import workloads  # noqa: E402
 METRIC = "prefill tokens/s (% bf16 TC peak); decode tokens/s (% HBM GB/s) on 1 GB300"
 L2_FLUSH_BYTES = 256 << 20
 
-# Algorithmic work (per token and value-head unless stated), K = V = D, C = 64.
-#   chunk_intra : K K^T, Q K^T, Tm K (each C*K, triangular) + Tm V (C*V)
-#   chunk_state : W S^T and the state update (2*K*V each)
-#   chunk_out   : Q S^T (2*K*V) + P Nn (C*V, triangular)
-# The three sum to 6KV + 3CK + 2CV = 139,264 flop at K = V = 128.
+# Algorithmic work per token and value-head (K = V = D, chunk C = 64), split by
+# the kernel that performs it.  Tensor-core path (bf16, D = 128):
+#   chunk_prep  : K K^T, Q K^T, Tm K (each C*K, triangular) + Tm V (C*V)
+#   chunk_chain : W S^T, state update, Q S^T (2*K*V each) + P N (C*V)
+# fp32 / D = 64 path: chunk_intra as chunk_prep; chunk_state 4KV; chunk_out 2KV + CV.
+# Each split sums to 6KV + 3CK + 2CV = 139,264 flop at K = V = 128.
 
 
 def kernel_flops_per_token_head(name, K, V, C=64):
-    return {"chunk_intra": 3 * C * K + C * V, "chunk_state": 4 * K * V, "chunk_out": 2 * K * V + C * V}.get(name)
+    return {"chunk_prep": 3 * C * K + C * V, "chunk_chain": 6 * K * V + C * V,
+            "chunk_intra": 3 * C * K + C * V, "chunk_state": 4 * K * V, "chunk_out": 2 * K * V + C * V}.get(name)
 
 
 def prefill_flops(T, Hv, K, V, C=64):
@@ -83,6 +85,55 @@ def pool_bytes(case):
     per_tok = 2 * case.q.shape[1] * K * case.q.element_size() + 2 * Hv * V * case.v.element_size() \
         + Hv * 4 + Hv * case.beta.element_size()
     return n + toks * per_tok, toks
+
+
+class Dist:
+    """Process-group plumbing for N > 1 (one process per GPU, replicas): a
+    barrier and a max over ranks.  Works with NCCL (GPU tensors) and gloo (CPU
+    tensors, used by the tests)."""
+
+    def __init__(self, world: int, device):
+        self.world = world
+        self.device = device
+
+    def barrier(self):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max(self, x: float) -> float:
+        if self.world == 1:
+            return float(x)
+        import torch.distributed as dist
+        t = torch.tensor([float(x)], dtype=torch.float64, device=self.device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+
+def whole_job_throughput(units_per_rank: float, ms_per_step_max: float, world: int) -> float:
+    """Units all ranks processed in one step / the slowest rank's step time."""
+    return world * units_per_rank / (ms_per_step_max / 1e3)
+
+
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu record, or None
+    when there is no record for this workload or the kernel's source changed
+    since the counters were taken."""
+    import hashlib
+    try:
+        rec = json.load(open(TRAFFIC_FILE))[kernel]
+    except (OSError, KeyError, ValueError):
+        return None
+    if rec.get("workload") != workload:
+        return None
+    try:
+        sha = hashlib.sha256(open(os.path.join(ROOT, rec["source"]), "rb").read()).hexdigest()
+    except OSError:
+        return None
+    return rec["dram_bytes_per_launch"] if sha == rec.get("source_sha256") else None
 
 
 def load_peaks():
@@ -161,7 +212,7 @@ def timed_steps(step, K, flush, stream, profile=True):
     return [a.elapsed_time(b) for a, b in evs], prof
 
 
-def roofline(prof, steps, work_per_kernel, peaks, bound_of):
+def roofline(prof, steps, work_per_kernel, peaks, bound_of, workload=""):
     """Dominant kernel (largest device time) -> roofline object."""
     name = max(prof, key=lambda k: prof[k][0])
     total_ms, launches = prof[name]
@@ -176,7 +227,7 @@ def roofline(prof, steps, work_per_kernel, peaks, bound_of):
         peak, unit = peaks["bf16"], "TFLOP/s"
     share = {k: round(v[0] / sum(x[0] for x in prof.values()), 4) for k, v in prof.items()}
     return {"kernel": name, "bound": bound, "achieved": round(ach, 3), "peak": peak, "unit": unit,
-            "frac": round(ach / peak, 5), "peak_source": peaks["source"], "traffic": None,
+            "frac": round(ach / peak, 5), "peak_source": peaks["source"], "traffic": ncu_traffic(name, workload),
             "avg_launch_us": round(avg_s * 1e6, 3), "launches": launches, "time_share": share}
 
 
@@ -274,7 +325,7 @@ def measure(runner, K, W, flush, stream, work_fn, bound_of, peaks, units_per_ste
     torch.cuda.synchronize()
     times, prof = timed_steps(lambda: runner.step(stream), K, flush, stream)
     ms = float(np.mean(times))
-    return ms, prof, roofline(prof, K, work_fn, peaks, bound_of), units_per_step / (ms / 1e3)
+    return ms, prof, roofline(prof, K, work_fn, peaks, bound_of, runner.case.name), units_per_step / (ms / 1e3)
 
 
 def cpu_baseline_prefill(case, budget_s=12.0):
@@ -376,17 +427,13 @@ def main():
     flush = lambda: flush_buf.fill_(1)
     only = set(filter(None, args.only.split(","))) or {"prefill", "decode", "verify", "kda"}
 
+    dist_ = Dist(world, dev)
+
     def barrier():
-        if world > 1:
-            torch.distributed.barrier()
+        dist_.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+    max_over_ranks = dist_.max
 
     pre_case = workloads.varlen_bf16_prefill()
     pre = Prefill(pre_case, dev)
@@ -410,9 +457,9 @@ def main():
     barrier()
     ms = max_over_ranks(float(np.mean(times)))
     launches = sum(v[1] for v in prof.values())
-    roof = roofline(prof, args.steps, prefill_work_fn(pre_case), peaks, lambda n: "tensor")
+    roof = roofline(prof, args.steps, prefill_work_fn(pre_case), peaks, lambda n: "tensor", pre_case.name)
     tokens = pre_case.T
-    value = world * tokens / (ms / 1e3)
+    value = whole_job_throughput(tokens, ms, world)
     whole_flops = prefill_flops(pre_case.T, 16, 128, 128)
     whole_bytes = prefill_bytes(pre_case)
     whole = {"tflops": round(whole_flops / (ms / 1e3) / 1e12, 3),
