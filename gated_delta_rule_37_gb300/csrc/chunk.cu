@@ -67,13 +67,16 @@ namespace {
 // ---------------------------------------------------------------------------
 // A malformed cu_seqlens (cu[0] != 0, a decreasing entry, cu[N] != T) makes
 // the chunk count 0 and meta[1] = 0, so the later kernels touch no memory.
+// Also writes order[]: sequence indices by decreasing length (ties by index),
+// the longest-first launch order of the per-sequence kernels (N <= 4096;
+// identity beyond).
 __global__ void __launch_bounds__(1024) chunk_meta_kernel(const int32_t* __restrict__ cu, int N,
                                                           int64_t T, int* __restrict__ meta,
                                                           int* __restrict__ offsets,
-                                                          int4* __restrict__ table) {
-    __shared__ int part[1024];
+                                                          int4* __restrict__ table, int* __restrict__ order) {
+    __shared__ int warp_sum[32];
     __shared__ int bad;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     if (tid == 0) bad = (cu[0] != 0 || (int64_t)cu[N] != T);
     __syncthreads();
     const int per = (N + blockDim.x - 1) / blockDim.x;
@@ -83,26 +86,52 @@ __global__ void __launch_bounds__(1024) chunk_meta_kernel(const int32_t* __restr
         if (cu[b + 1] < cu[b]) bad = 1;
         cnt += (cu[b + 1] - cu[b] + kChunk - 1) / kChunk;
     }
-    part[tid] = cnt;
+    // block-wide exclusive scan of the per-thread chunk counts
+    int incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_sum[wid] = incl;
     __syncthreads();
     if (bad) {
         if (tid == 0) { meta[0] = 0; meta[1] = 0; }
         return;
     }
-    if (tid == 0) {  // small serial exclusive scan over 1024 partial counts
-        int run = 0;
-        for (int i = 0; i < (int)blockDim.x; ++i) { int c = part[i]; part[i] = run; run += c; }
-        meta[0] = run;
-        meta[1] = 1;
-        offsets[N] = run;
+    if (wid == 0) {
+        int v = warp_sum[lane];
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += y;
+        }
+        warp_sum[lane] = v;
     }
     __syncthreads();
-    int c = part[tid];
+    int c = incl - cnt + (wid > 0 ? warp_sum[wid - 1] : 0);
+    if (tid == 0) {
+        meta[0] = warp_sum[31];
+        meta[1] = 1;
+        offsets[N] = warp_sum[31];
+    }
     for (int b = b0; b < b1; ++b) {
         offsets[b] = c;
         const int bos = cu[b], len = cu[b + 1] - bos;
         for (int s = 0; s < len; s += kChunk, ++c)
             table[c] = make_int4(b, bos + s, min(kChunk, len - s), 0);
+    }
+    for (int b = tid; b < N; b += blockDim.x) {
+        const int lb = cu[b + 1] - cu[b];
+        int rank = b;
+        if (N <= 4096) {
+            rank = 0;
+            for (int j = 0; j < N; ++j) {
+                const int lj = cu[j + 1] - cu[j];
+                rank += (lj > lb) || (lj == lb && j < b);
+            }
+        }
+        order[rank] = b;
     }
 }
 
@@ -392,7 +421,8 @@ cudaError_t launch_chunk_t(const ChunkArgs& a, cudaStream_t stream) {
         KernelTimer kt("chunk_meta", stream);
         chunk_meta_kernel<<<1, 1024, 0, stream>>>(a.cu_seqlens, a.N, a.T, reinterpret_cast<int*>(ws + w.off_meta),
                                                   reinterpret_cast<int*>(ws + w.off_offsets),
-                                                  reinterpret_cast<int4*>(ws + w.off_table));
+                                                  reinterpret_cast<int4*>(ws + w.off_table),
+                                                  reinterpret_cast<int*>(ws + w.off_order));
     }
     if (a.flags & 1) {
         const int64_t rows = a.T * a.Hk;

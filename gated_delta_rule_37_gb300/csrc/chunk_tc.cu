@@ -541,11 +541,11 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
                     *reinterpret_cast<uint4*>(Whi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                     *reinterpret_cast<uint4*>(Wlo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 }
-                float* urow = Udst + (size_t)cb * (C * BV) + (size_t)i * BV;
+                // U block cb stored value-major [32 v][64 i]: the chain's thread for
+                // row i then reads a conflict-free column of shared memory
+                float* ublk = Udst + (size_t)cb * (C * BV) + i;
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    reinterpret_cast<float4*>(urow)[u] =
-                        make_float4(uv[4 * u], uv[4 * u + 1], uv[4 * u + 2], uv[4 * u + 3]);
+                for (int v = 0; v < BV; ++v) ublk[(size_t)v * C] = uv[v];
             }
         }
     }
@@ -585,10 +585,8 @@ enum ChainBar {
     kDrainA, kDrainB, kDrainC, kNumBars
 };
 // Arrival counts: the N accumulator is committed by issuers A and B, a stage is
-// released by all three issuers, the state operands are published by each of
-// the eight state-group warps, everything else by one arrival.
+// released by all three issuers, everything else by one arrival.
 __device__ __forceinline__ uint32_t chain_bar_count(int i) {
-    if (i == kSReady || i == kNReady) return 8u;  // one arrival per state-group warp
     return i == kD1Full ? 2u : (i == kEmpty0 || i == kEmpty1) ? 3u : 1u;
 }
 
@@ -659,92 +657,40 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                 tc::mbar_wait_copies(bar(kFull0 + (c & 1)), (c >> 1) & 1);
         }
         __syncwarp();
-    } else if (warp >= 1 && warp <= 3) {
-        // ------------------------------ MMA issuers ------------------------------
-        // A single thread issues a tcgen05.mma about every 60 cycles, well
-        // below what the tensor pipe sustains for these shapes, so the work is
-        // spread over three issuing threads, each committing its own MMAs:
-        //   A (warp 1): D1 = [W_hi ; Qd] [S_hi | S_lo], then D2 = K^T [N'_hi | N'_lo]
-        //   B (warp 2): D1b = [W_lo ; P] S_hi            (in parallel with A)
-        //   C (warp 3): D1 rows 64..127 += P N           (after N is ready)
-        // Rows of a stacked operand that a product does not need land in
-        // accumulator rows nobody reads (or that are dead at that time).
-        // Descriptors are built once per tile; a k-step adds its byte offset / 16
-        // to the start-address field (tiles sit below 256 KB, so no carry).
-        if (lane == 0) {
-            const int role = warp;  // 1 = A, 2 = B, 3 = C
-            const uint32_t idA = tc::idesc_bf16(128, 2 * BV, false, true);   // [W_hi;Qd] [S_hi|S_lo]
-            const uint32_t idB = tc::idesc_bf16(128, BV, false, true);       // [W_lo;P] S_hi, [.;P] N
-            const uint32_t id2w = tc::idesc_bf16(128, 2 * BV, true, true);   // K^T [N'_hi|N'_lo]
-            const uint32_t id2n = tc::idesc_bf16(128, BV, true, true);       // Kd_lo^T N'_hi
-            auto dk128 = [](uint32_t a) { return tc::smem_desc(a, 16, 1024, tc::kSwizzle128); };
-            auto dmn128 = [](uint32_t a) { return tc::smem_desc(a, C * 128, 1024, tc::kSwizzle128); };
-            auto dmn64 = [](uint32_t a, uint32_t atom) { return tc::smem_desc(a, atom, 512, tc::kSwizzle64); };
-            const uint64_t dNpair = dmn64(base + S::kNh, C * BV * 2), dNh = dmn64(base + S::kNh, 512);
-            const uint64_t dN = dmn64(base + S::kN, 512);
-            const uint64_t dSpair = dmn64(base + S::kSh, D * BV * 2), dSh = dmn64(base + S::kSh, 512);
-            constexpr uint32_t a128[8] = {0, 2, 4, 6, (2 * C * 128) >> 4, ((2 * C * 128) >> 4) + 2,
-                                          ((2 * C * 128) >> 4) + 4, ((2 * C * 128) >> 4) + 6};  // 128-row k128, K = 128
-            constexpr uint32_t a64[4] = {0, 2, 4, 6};                  // 128-row k128, K = 64 (column block 0)
-            constexpr uint32_t amn[4] = {0, 128, 256, 384};            // MN-major A: 2 x 8-row groups per step
-            bool issued = false;
-            for (int c = 0; c < nc; ++c) {
-                const int s = c & 1, ob = c & 1;
-                const uint32_t st = base + s * S::kStage;
-                if (!tc::mbar_spin(bar(kFull0 + s), (c >> 1) & 1, abort_flag)) { fail(); break; }
-                if (role == 1) GDR_TRACE_POINT(2, c);
-                if (role == 3) {
-                    // output intra part once N is ready (implies D1 of this chunk complete)
-                    if (!tc::mbar_spin(bar(kNReady), c & 1, abort_flag)) { fail(); break; }
-                    tc::fence_after();
-                    issued = true;
-                    tc::mma_ksteps<4>(tD1 + 64 * ob, dk128(st + S::kYW), a64, dN, 64, idB, false);
-                    tc::mma_commit(bar(kOFull0 + ob));
-                    tc::mma_commit(bar(kEmpty0 + s));
-                    continue;
-                }
-                if (role == 1 && c >= 2 && !tc::mbar_spin(bar(kOFree0 + ob), ((c >> 1) - 1) & 1, abort_flag)) { fail(); break; }
-                if (!tc::mbar_spin(bar(kSReady), c & 1, abort_flag)) { fail(); break; }
-                if (role == 1) GDR_TRACE_POINT(3, c);
-                tc::fence_after();
-                issued = true;
-                if (role == 1) {
-                    tc::mma_ksteps<8>(tD1 + 64 * ob, dk128(st + S::kXW), a128, dSpair, 64, idA, true);
-                    tc::mma_commit(bar(kD1Full));
-                    GDR_TRACE_POINT(4, c);
-                    if (!tc::mbar_spin(bar(kNReady), c & 1, abort_flag)) { fail(); break; }
-                    GDR_TRACE_POINT(5, c);
-                    tc::fence_after();
-                    tc::mma_ksteps<4>(tD2, dmn128(st + S::kKt), amn, dNpair, 64, id2w, true);
-                    if (kKDA) tc::mma_ksteps<4>(tD2, dmn128(st + S::kKt + kTile64x128), amn, dNh, 64, id2n, false);
-                    tc::mma_commit(bar(kD2Full));
-                    tc::mma_commit(bar(kEmpty0 + s));
-                    GDR_TRACE_POINT(6, c);
-                } else {
-                    tc::mma_ksteps<8>(tD1b, dk128(st + S::kYW), a128, dSh, 64, idB, true);
-                    tc::mma_commit(bar(kD1Full));
-                    tc::mma_commit(bar(kEmpty0 + s));
-                }
-            }
-            if (issued) {  // every MMA this thread issued finished before the CTA leaves
-                const int dr = role == 1 ? kDrainA : role == 2 ? kDrainB : kDrainC;
-                tc::mma_commit(bar(dr));
-                tc::mbar_wait(bar(dr), 0, abort_flag);
-            }
-        }
-        __syncwarp();
     } else if (warp >= 4 && warp < 12) {
         // ------------------------------ state group ------------------------------
         // Eight warps: warp w owns TMEM lane quadrant w % 4 (rows k of S^T) and
         // the 16-column half hf of the block's 32 value columns; the N
-        // accumulator rows 0..63 sit in quadrants 0 and 1.
+        // accumulator rows 0..63 sit in quadrants 0 and 1.  After each named
+        // barrier that publishes operand tiles, one lane of warps 4, 5 and 6
+        // issues the MMAs that read them (a single thread issues about one
+        // tcgen05.mma per 60 cycles, so the work is split):
+        //   A (warp 4): D1 = [W_hi ; Qd] [S_hi | S_lo], later D2 = K^T [N'_hi | N'_lo]
+        //   B (warp 5): D1b = [W_lo ; P] S_hi
+        //   C (warp 6): D1 rows 64..127 += P N (after N is published)
+        // Rows of a stacked operand that a product does not need land in
+        // accumulator rows nobody reads (or that are dead at that time).
+        // Descriptors are built once per tile; a k-step adds its byte offset / 16
+        // to the start-address field (tiles sit below 256 KB, so no carry).
         const int q = warp & 3, hf = (warp - 4) >> 2;
         const int t = 32 * q + lane;            // TMEM lane = row k of S^T
         const bool lead = warp == 4 && lane == 0;
+        const bool isA = warp == 4 && lane == 0, isB = warp == 5 && lane == 0, isC = warp == 6 && lane == 0;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const bool nrow = q < 2;                // owns row i = t of the N accumulator
         const int i = t;
         const int vh = 16 * hf;                 // first column of this thread's half
+        const uint32_t idA = tc::idesc_bf16(128, 2 * BV, false, true);   // [W_hi;Qd] [S_hi|S_lo]
+        const uint32_t idB = tc::idesc_bf16(128, BV, false, true);       // [W_lo;P] S_hi, [.;P] N
+        const uint32_t id2w = tc::idesc_bf16(128, 2 * BV, true, true);   // K^T [N'_hi|N'_lo]
+        const uint32_t id2n = tc::idesc_bf16(128, BV, true, true);       // Kd_lo^T N'_hi
+        auto dk128 = [](uint32_t a) { return tc::smem_desc(a, 16, 1024, tc::kSwizzle128); };
+        auto dmn128 = [](uint32_t a) { return tc::smem_desc(a, C * 128, 1024, tc::kSwizzle128); };
+        auto dmn64 = [](uint32_t a, uint32_t atom) { return tc::smem_desc(a, atom, 512, tc::kSwizzle64); };
+        constexpr uint32_t a128[8] = {0, 2, 4, 6, (2 * C * 128) >> 4, ((2 * C * 128) >> 4) + 2,
+                                      ((2 * C * 128) >> 4) + 4, ((2 * C * 128) >> 4) + 6};  // 128-row k128, K = 128
+        constexpr uint32_t a64[4] = {0, 2, 4, 6};                  // 128-row k128, K = 64 (column block 0)
+        constexpr uint32_t amn[4] = {0, 128, 256, 384};            // MN-major A: 2 x 8-row groups per step
         float Sreg[16];
         if (p.h0) {
 #pragma unroll
@@ -755,12 +701,15 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
         }
         unsigned char* sSh = sm + S::kSh;
         unsigned char* sSl = sm + S::kSl;
+        bool issued = false;
         for (int c = 0; c < nc; ++c) {
             const int s = c & 1, ob = c & 1;
             const unsigned char* stg = sm + s * S::kStage;
+            const uint32_t st = base + s * S::kStage;
+            if (!tc::mbar_wait(bar(kFull0 + s), (c >> 1) & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
+            if (lead) GDR_TRACE_POINT(21, c);
             // S^T rows (hi, lo) into the MMA operand tiles.  Their readers (the N
             // products of chunk c - 1) finished before the last state update.
-            if (lead) GDR_TRACE_POINT(21, c);
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 uint32_t hw[4], lw[4];
@@ -771,27 +720,34 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                 *reinterpret_cast<uint4*>(sSl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
             if (lead) GDR_TRACE_POINT(19, c);
-            // publish: each warp fences its own stores and arrives once
             tc::fence_proxy_async();
-            if (lead) GDR_TRACE_POINT(20, c);
             tc::fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(bar(kSReady));
+            tc::bar_sync(1, 256);
             if (lead) GDR_TRACE_POINT(8, c);
-            if (!tc::mbar_wait(bar(kFull0 + s), (c >> 1) & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
-            if (lead) GDR_TRACE_POINT(7, c);
+            if (isA) {
+                // the output rows of D1[ob] were drained (chunk c - 2) before reuse
+                if (c >= 2 && !tc::mbar_wait(bar(kOFree0 + ob), ((c >> 1) - 1) & 1, abort_flag)) fail();
+                tc::fence_after();
+                tc::mma_ksteps<8>(tD1 + 64 * ob, dk128(st + S::kXW), a128, dmn64(base + S::kSh, D * BV * 2), 64, idA, true);
+                tc::mma_commit(bar(kD1Full));
+                issued = true;
+                GDR_TRACE_POINT(4, c);
+            } else if (isB) {
+                tc::fence_after();
+                tc::mma_ksteps<8>(tD1b, dk128(st + S::kYW), a128, dmn64(base + S::kSh, 512), 64, idB, true);
+                tc::mma_commit(bar(kD1Full));
+                tc::mma_commit(bar(kEmpty0 + s));
+                issued = true;
+            }
             const float* rec = reinterpret_cast<const float*>(stg + S::kRec_);
             const float colf = rec[64 + t];
             const float rowf = nrow ? rec[i] : 0.f;
             const int Lc = reinterpret_cast<const int*>(rec)[192];
             float uv[16];
             if (nrow) {
-                const float4* ur = reinterpret_cast<const float4*>(stg + S::kU + ((size_t)i * BV + vh) * 4);
+                const float* ucol = reinterpret_cast<const float*>(stg + S::kU) + (size_t)vh * C + i;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float4 x = ur[u];
-                    uv[4 * u] = x.x; uv[4 * u + 1] = x.y; uv[4 * u + 2] = x.z; uv[4 * u + 3] = x.w;
-                }
+                for (int v = 0; v < 16; ++v) uv[v] = ucol[(size_t)v * C];
             }
             // N = U - W S^T  ->  N' = rowf * N (hi, lo), N (bf16, masked)
             if (!tc::mbar_wait(bar(kD1Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
@@ -827,11 +783,24 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             }
             if (lead) GDR_TRACE_POINT(17, c);
             tc::fence_proxy_async();
-            if (lead) GDR_TRACE_POINT(18, c);
             tc::fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(bar(kNReady));
+            tc::bar_sync(1, 256);
             if (lead) GDR_TRACE_POINT(10, c);
+            if (isA) {
+                tc::fence_after();
+                tc::mma_ksteps<4>(tD2, dmn128(st + S::kKt), amn, dmn64(base + S::kNh, C * BV * 2), 64, id2w, true);
+                if (kKDA)
+                    tc::mma_ksteps<4>(tD2, dmn128(st + S::kKt + kTile64x128), amn, dmn64(base + S::kNh, 512), 64, id2n, false);
+                tc::mma_commit(bar(kD2Full));
+                tc::mma_commit(bar(kEmpty0 + s));
+                GDR_TRACE_POINT(6, c);
+            } else if (isC) {
+                tc::fence_after();
+                tc::mma_ksteps<4>(tD1 + 64 * ob, dk128(st + S::kYW), a64, dmn64(base + S::kN, 512), 64, idB, false);
+                tc::mma_commit(bar(kOFull0 + ob));
+                tc::mma_commit(bar(kEmpty0 + s));
+                issued = true;
+            }
             // S^T <- colf * S^T + dS^T  (hi and lo halves of the accumulator summed)
             if (!tc::mbar_wait(bar(kD2Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
             if (lead) GDR_TRACE_POINT(11, c);
@@ -841,6 +810,11 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             for (int v = 0; v < 16; ++v) Sreg[v] = fmaf(colf, Sreg[v], dv[v] + dv[16 + v]);
             if (lead) GDR_TRACE_POINT(12, c);
             tc::fence_before();
+        }
+        if (issued) {  // every MMA this thread issued finished before the CTA leaves
+            const int dr = isA ? kDrainA : isB ? kDrainB : kDrainC;
+            tc::mma_commit(bar(dr));
+            tc::mbar_wait(bar(dr), 0, abort_flag);
         }
         if (p.hT && !*abort_flag) {
 #pragma unroll
@@ -889,24 +863,6 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
     if (warp == 2) tc::tmem_dealloc(tmem, 256);
 }
 
-// LPT order: sequence indices by decreasing length (ties by index).
-__global__ void __launch_bounds__(1024) lpt_order_kernel(const int32_t* __restrict__ cu, int N,
-                                                         int* __restrict__ order) {
-    for (int b = threadIdx.x; b < N; b += blockDim.x) {
-        const int lb = cu[b + 1] - cu[b];
-        int rank = 0;
-        if (N <= 4096) {
-            for (int j = 0; j < N; ++j) {
-                const int lj = cu[j + 1] - cu[j];
-                rank += (lj > lb) || (lj == lb && j < b);
-            }
-        } else {
-            rank = b;
-        }
-        order[rank] = b;
-    }
-}
-
 }  // namespace
 
 size_t chunk_tc_blob_bytes(int64_t max_chunks, int Hk, int Hv, bool kda) {
@@ -939,10 +895,6 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* w
     p.err = device_error_word();
     p.N = a.N; p.Hk = a.Hk; p.Hv = a.Hv; p.scale = a.scale;
 
-    {
-        KernelTimer kt("lpt_order", stream);
-        lpt_order_kernel<<<1, 1024, 0, stream>>>(a.cu_seqlens, a.N, reinterpret_cast<int*>(ws + w.off_order));
-    }
     if (kda) {
         const int smp = PrepSmem<true>::kTotal, smc = ChainSmem<true>::kTotal;
         cudaFuncSetAttribute(chunk_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smp);
