@@ -23,12 +23,14 @@
 //          O  = Qd S0^T + P N         M=64 (output, 2 + 1 MMA groups)
 //          S  = e^{gam_L} S0 + K^T (f o N)     M=128, 2-term split
 //        Warp roles (512 threads): warp 0 stages chunk blobs with
-//        cp.async.bulk into a two-deep ring; warps 1-3 each issue part of the
-//        tcgen05.mma work from one thread (a single thread issues about one MMA
-//        per 60 cycles); warps 4-11 hold the fp32 state S^T (row k in TMEM lane
-//        k, 16 of the 32 columns per thread) and turn the N accumulator into the
-//        split operands; warps 12-15 drain the output accumulator
-//        (double-buffered in TMEM) to bf16 rows of o.
+//        cp.async.bulk into a two-deep ring; warp 2 owns the TMEM allocation;
+//        warps 4-11 hold the fp32 state S^T (row k in TMEM lane k, 16 of the 32
+//        columns per thread), turn the N accumulator into the split operands,
+//        and one lane each of warps 4, 5 and 6 issues the tcgen05.mma groups as
+//        soon as their operands are published (a single thread issues about
+//        one MMA per 60 cycles, so the work is split three ways); warps 14 and
+//        15 drain the output accumulator (double-buffered in TMEM) to bf16
+//        rows of o.
 //
 // Every exponential is of gam_i - gam_j with i >= j or of gam_i, all <= 0:
 // any finite gate <= 0 keeps every operand finite (cuLA PR #113 review).
