@@ -109,56 +109,99 @@ __device__ __forceinline__ void raise_error(const TcParams& p, unsigned code) {
 }
 
 // ---------------------------------------------------------------------------
-// Blocked inverse of a 64 x 64 unit-lower-triangular matrix (I + A), A strictly
-// lower, fp32, 128 threads.  Diagonal 16 x 16 blocks by forward substitution,
-// then block diagonals d = 1..3:  T_ij = -D_i * sum_{m in blocks j..i-1} A_im T_mj.
+// Inverse of a 64 x 64 unit-lower-triangular matrix (I + A), A strictly lower,
+// fp32, 256 threads, by recursive doubling over 16 x 16 blocks:
+//   1. the four diagonal blocks X_b = (I + A_bb)^{-1}, one column per thread,
+//      right-looking (after x_m is final it is subtracted from every later
+//      row, so the dependent chain is 16 steps long, not 120);
+//   2. the 32 x 32 halves: T_{2p+1,2p} = -X_{2p+1} (A_{2p+1,2p} X_{2p});
+//   3. the lower-left 32 x 32 block: T_10 = -B_1 (A_10 B_0) with B_0, B_1 the
+//      two 32 x 32 inverses from step 2.
+// Each product is one pass over shared memory with a small register tile per
+// thread.  Every entry of Tm is written (zeros above the diagonal).  Z holds
+// 1024 floats of scratch.
 // ---------------------------------------------------------------------------
-template <int NT>
 __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict__ Tm, float* __restrict__ Z,
                                  int tid) {
-    for (int e = tid; e < C * LDA; e += NT) Tm[e] = 0.f;
-    __syncthreads();
     if (tid < 64) {
-        const int b = tid >> 4, c = tid & 15, r0 = 16 * b;
+        const int r0 = 16 * (tid >> 4), c = tid & 15;
         float x[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float s = (r == c) ? 1.f : 0.f;
+        for (int r = 0; r < 16; ++r) x[r] = (r == c) ? 1.f : 0.f;
 #pragma unroll
-            for (int m = 0; m < r; ++m) s = fmaf(-A[(r0 + r) * LDA + r0 + m], x[m], s);
-            x[r] = (r >= c) ? s : 0.f;
+        for (int m = 0; m < 15; ++m) {
+#pragma unroll
+            for (int r = m + 1; r < 16; ++r) x[r] = fmaf(-A[(r0 + r) * LDA + r0 + m], x[m], x[r]);
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) Tm[(r0 + r) * LDA + r0 + c] = x[r];
+    } else {
+        // zeros in the six blocks above the block diagonal
+        for (int e = tid - 64; e < 6 * 256; e += 192) {
+            const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
+            const int bi = blk < 3 ? 0 : blk < 5 ? 1 : 2;
+            const int bj = blk < 3 ? blk + 1 : blk < 5 ? blk - 1 : 3;
+            Tm[(16 * bi + r) * LDA + 16 * bj + c] = 0.f;
+        }
     }
     __syncthreads();
-    for (int d = 1; d < 4; ++d) {
-        const int nblk = 4 - d;
-        for (int e = tid; e < nblk * 256; e += NT) {
-            const int j = e >> 8, i = j + d, r = (e >> 4) & 15, c = e & 15;
-            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-            const float* arow = A + (16 * i + r) * LDA;
-            const float* tcol = Tm + 16 * j + c;
-            for (int m = 16 * j; m < 16 * i; m += 4) {
-                s0 = fmaf(arow[m], tcol[m * LDA], s0);
-                s1 = fmaf(arow[m + 1], tcol[(m + 1) * LDA], s1);
-                s2 = fmaf(arow[m + 2], tcol[(m + 2) * LDA], s2);
-                s3 = fmaf(arow[m + 3], tcol[(m + 3) * LDA], s3);
-            }
-            Z[e] = (s0 + s1) + (s2 + s3);
-        }
-        __syncthreads();
-        for (int e = tid; e < nblk * 256; e += NT) {
-            const int j = e >> 8, i = j + d, r = (e >> 4) & 15, c = e & 15;
-            float s0 = 0.f, s1 = 0.f;
+    // step 2: pair p = tid / 128; thread: row i, columns j0, j0 + 1 of a 16 x 16 block
+    {
+        const int p = tid >> 7, e = tid & 127, i = e >> 3, j0 = 2 * (e & 7);
+        const int r0 = 32 * p, r1 = r0 + 16;
+        float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-            for (int m = 0; m < 16; m += 2) {
-                s0 = fmaf(Tm[(16 * i + r) * LDA + 16 * i + m], Z[(j << 8) + m * 16 + c], s0);
-                s1 = fmaf(Tm[(16 * i + r) * LDA + 16 * i + m + 1], Z[(j << 8) + (m + 1) * 16 + c], s1);
-            }
-            Tm[(16 * i + r) * LDA + 16 * j + c] = -(s0 + s1);
+        for (int m = 0; m < 16; ++m) {
+            const float a = A[(r1 + i) * LDA + r0 + m];
+            y0 = fmaf(a, Tm[(r0 + m) * LDA + r0 + j0], y0);
+            y1 = fmaf(a, Tm[(r0 + m) * LDA + r0 + j0 + 1], y1);
         }
+        Z[p * 256 + i * 16 + j0] = y0;
+        Z[p * 256 + i * 16 + j0 + 1] = y1;
         __syncthreads();
+        float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const float x = Tm[(r1 + i) * LDA + r1 + m];
+            t0 = fmaf(x, Z[p * 256 + m * 16 + j0], t0);
+            t1 = fmaf(x, Z[p * 256 + m * 16 + j0 + 1], t1);
+        }
+        Tm[(r1 + i) * LDA + r0 + j0] = -t0;
+        Tm[(r1 + i) * LDA + r0 + j0 + 1] = -t1;
+    }
+    __syncthreads();
+    // step 3: 2 x 2 tile per thread, rows 2 ti, 2 ti + 1 and columns 2 tj, 2 tj + 1
+    {
+        const int ti = tid >> 4, tj = tid & 15, i0 = 2 * ti, j0 = 2 * tj;
+        float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
+#pragma unroll 8
+        for (int m = 0; m < 32; ++m) {
+            const float a0 = A[(32 + i0) * LDA + m], a1 = A[(33 + i0) * LDA + m];
+            const float b0 = Tm[m * LDA + j0], b1 = Tm[m * LDA + j0 + 1];
+            y00 = fmaf(a0, b0, y00);
+            y01 = fmaf(a0, b1, y01);
+            y10 = fmaf(a1, b0, y10);
+            y11 = fmaf(a1, b1, y11);
+        }
+        Z[i0 * 32 + j0] = y00;
+        Z[i0 * 32 + j0 + 1] = y01;
+        Z[(i0 + 1) * 32 + j0] = y10;
+        Z[(i0 + 1) * 32 + j0 + 1] = y11;
+        __syncthreads();
+        float t00 = 0.f, t01 = 0.f, t10 = 0.f, t11 = 0.f;
+#pragma unroll 8
+        for (int m = 0; m < 32; ++m) {
+            const float x0 = Tm[(32 + i0) * LDA + 32 + m], x1 = Tm[(33 + i0) * LDA + 32 + m];
+            const float z0 = Z[m * 32 + j0], z1 = Z[m * 32 + j0 + 1];
+            t00 = fmaf(x0, z0, t00);
+            t01 = fmaf(x0, z1, t01);
+            t10 = fmaf(x1, z0, t10);
+            t11 = fmaf(x1, z1, t11);
+        }
+        Tm[(32 + i0) * LDA + j0] = -t00;
+        Tm[(32 + i0) * LDA + j0 + 1] = -t01;
+        Tm[(33 + i0) * LDA + j0] = -t10;
+        Tm[(33 + i0) * LDA + j0 + 1] = -t11;
     }
 }
 
@@ -184,7 +227,7 @@ __device__ __forceinline__ void stage_rows_async(unsigned char* tile, int rows, 
 // operand, so K K^T and Q K^T come from one group of MMAs.  Dead regions are
 // reused: the Q rows of X hold T' hi / lo and the fp32 A matrix holds T'' hi /
 // lo once the solve has finished.
-constexpr int kPrepThreads = 256;
+constexpr int kPrepThreads = 256;  // solve_unit_lower assumes exactly 256 threads
 constexpr uint32_t kXcb = 2 * C * 128;  // column-block stride of X (128 rows x 128 B)
 
 template <bool kKDA>
@@ -197,8 +240,8 @@ struct PrepSmem {
     static constexpr uint32_t kT2h = kA;
     static constexpr uint32_t kT2l = kA + kTile64x64;
     static constexpr uint32_t kTm = (kA + C * LDA * 4 + 1023) & ~1023u;  // fp32 [64][65]
-    static constexpr uint32_t kZ = kTm + C * LDA * 4;                   // fp32 [3][256]
-    static constexpr uint32_t kKgh = (kZ + 3 * 256 * 4 + 1023) & ~1023u;  // K o e^Gam hi (channel gate)
+    static constexpr uint32_t kZ = kTm + C * LDA * 4;                   // fp32 [1024]
+    static constexpr uint32_t kKgh = (kZ + 4 * 256 * 4 + 1023) & ~1023u;  // K o e^Gam hi (channel gate)
     static constexpr uint32_t kKgl = kKgh + (kKDA ? kTile64x128 : 0);
     static constexpr uint32_t kGam = kKgl + (kKDA ? kTile64x128 : 0);    // fp32 [64][128] or [64]
     static constexpr uint32_t kDec = kGam + (kKDA ? C * D * 4 : C * 4);  // fp32 [64][128] e^{gk} (channel gate)
@@ -464,7 +507,7 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
     GDR_TRACE_PREP(3);
 
     // ---- Tm = (I + A)^{-1} -----------------------------------------------------------
-    solve_unit_lower<NT>(As, Tm, Z, tid);
+    solve_unit_lower(As, Tm, Z, tid);
     GDR_TRACE_PREP(4);
 
     // ---- split operands: T' = Tm diag(beta e^{gam}) (scalar gate) or Tm diag(beta);
