@@ -50,15 +50,31 @@ __device__ unsigned long long g_trace[24][64];
     do {                                                                                           \
         if (blockIdx.x == 7 && blockIdx.y == 0 && threadIdx.x == 0) g_trace[23][phase] = clock64(); \
     } while (0)
+__device__ unsigned long long g_items[4096][3];  // prep item: start, end (%globaltimer), SM id
 extern "C" __attribute__((visibility("default"))) int gdr_trace_dump(unsigned long long* host) {
     return (int)cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace));
 }
+extern "C" __attribute__((visibility("default"))) int gdr_trace_items(unsigned long long* host) {
+    return (int)cudaMemcpyFromSymbol(host, g_items, sizeof(g_items));
+}
+#define GDR_TRACE_ITEM(item, which)                                                                  \
+    do {                                                                                             \
+        if (threadIdx.x == 0 && (item) < 4096) {                                                     \
+            unsigned long long t;                                                                    \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));                                    \
+            g_items[item][which] = t;                                                                \
+            if (which == 0) { unsigned sm; asm("mov.u32 %0, %%smid;" : "=r"(sm)); g_items[item][2] = sm; } \
+        }                                                                                            \
+    } while (0)
 #else
 #define GDR_TRACE_POINT(slot, c) \
     do {                         \
     } while (0)
 #define GDR_TRACE_PREP(phase) \
     do {                      \
+    } while (0)
+#define GDR_TRACE_ITEM(item, which) \
+    do {                            \
     } while (0)
 #endif
 
@@ -257,14 +273,13 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
     constexpr int NT = kPrepThreads;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int chunk = blockIdx.x;
-    if (chunk >= p.meta[0]) return;
-    const int h = blockIdx.y;
+    // Persistent: CTA x takes items x, x + gridDim.x, ... (item = chunk * Hv + h)
+    // and warms L2 with the next item's rows while it computes the current one.
+    const int nitems = p.meta[0] * p.Hv;
+    if ((int)blockIdx.x >= nitems) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q = warp & 3, hf = warp >> 2;  // TMEM lane quadrant, column half
-    const int4 info = p.table[chunk];
-    const int start = info.y, L = info.z;
-    const int grp = p.Hv / p.Hk, kh = h / grp;
+    const int grp = p.Hv / p.Hk;
     const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(p.q);
     const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(p.k);
     const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(p.v);
@@ -280,97 +295,242 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::kBar + 24);
     const uint32_t bar0 = tc::smem_u32(&bars[0]);
 
-    GDR_TRACE_PREP(0);
-    // ---- stage K, Q (as X) and V rows (cp.async), gates, beta -------------------
-    stage_rows_async<NT>(sm + S::kX, 2 * C, 0, kp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
-    stage_rows_async<NT>(sm + S::kX, 2 * C, C, qp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
-    stage_rows_async<NT>(sm + S::kV, C, 0, vp + ((size_t)start * p.Hv + h) * D, (size_t)p.Hv * D, L, tid);
-    asm volatile("cp.async.commit_group;" ::: "memory");
     if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), 256);
     if (tid == 0) {
         tc::mbar_init(bar0, 1);
         *abort_flag = 0;
         tc::mbar_fence_init();
     }
-    if (tid < C) bet[tid] = tid < L ? to_f(bp[((size_t)start + tid) * p.Hv + h]) : 0.f;
-    if (kKDA) {
-        if (tid < D) {
-            // per-channel inclusive cumsum in token order (thread = channel); all
-            // 64 loads are issued before the dependent adds
-            const float* __restrict__ gk = p.gk + ((size_t)start * p.Hv + h) * D + tid;
-            float x[C];
-#pragma unroll
-            for (int i = 0; i < C; ++i) x[i] = i < L ? __ldg(gk + (size_t)i * p.Hv * D) : 0.f;
-            float* dec = reinterpret_cast<float*>(sm + S::kDec);
-            float acc = 0.f;
-#pragma unroll
-            for (int i = 0; i < C; ++i) {
-                acc += x[i];
-                gam[i * D + tid] = acc;
-                dec[i * D + tid] = __expf(x[i]);  // per-token decay, <= 1
-            }
-        }
-    } else if (warp < 2) {
-        // scalar gate: inclusive scan over 64 tokens with two warps
-        float x = tid < L ? __ldg(p.g + ((size_t)start + tid) * p.Hv + h) : 0.f;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, x, off);
-            if (lane >= off) x += y;
-        }
-        gam[tid] = x;
-    }
-    __syncthreads();
-    if (!kKDA && warp == 1) gam[tid] += gam[31];
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    tc::fence_proxy_async();
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
-    GDR_TRACE_PREP(1);
-    const uint32_t sX = tc::smem_u32(sm + S::kX), sV = tc::smem_u32(sm + S::kV);
-    auto gm = [&](int i, int c) -> float { return kKDA ? gam[i * D + c] : gam[i]; };
-    const float* gl = kKDA ? gam + (L - 1) * D : gam + (L - 1);
+    uint32_t ph0 = 0;  // parity of the next completion of bar0
 
-    // ---- [K K^T ; Q K^T] on the tensor cores (scalar gate), one M = 128 group ------
-    if (!kKDA && tid == 0) {
-        constexpr uint32_t id = tc::idesc_bf16(128, 64, false, false);
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = (ks >> 2) * kXcb + (ks & 3) * 32;
-            tc::mma_bf16(tmem, tc::smem_desc(sX + off, 16, 1024, tc::kSwizzle128),
-                         tc::smem_desc(sX + off, 16, 1024, tc::kSwizzle128), id, ks > 0);
-        }
-        tc::mma_commit(bar0);
-    }
-    __syncwarp();
+    for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+        const int chunk = item / p.Hv, h = item - chunk * p.Hv;
+        const int4 info = p.table[chunk];
+        const int start = info.y, L = info.z;
+        const int kh = h / grp;
 
-    // ---- while that runs: Qd blob, K / Kd blob, decay record ------------------------
-    {
-        unsigned char* Qdst = p.Xw + ((size_t)chunk * p.Hv + h) * kXwBytes;  // rows 64..127
-        for (int e = tid; e < C * 16; e += NT) {
-            const int i = e >> 4, ch = e & 15;
-            const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(C + i, ch, 2 * C));
-            const __nv_bfloat16* qv = reinterpret_cast<const __nv_bfloat16*>(&raw);
-            uint32_t w4[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int c = ch * 8 + 2 * u;
-                w4[u] = tc::pack_bf16(__bfloat162float(qv[2 * u]) * __expf(gm(i, c)),
-                                      __bfloat162float(qv[2 * u + 1]) * __expf(gm(i, c + 1)));
+        GDR_TRACE_PREP(0);
+        GDR_TRACE_ITEM(item, 0);
+        // ---- stage K, Q (as X) and V rows (cp.async), gates, beta -------------------
+        stage_rows_async<NT>(sm + S::kX, 2 * C, 0, kp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
+        stage_rows_async<NT>(sm + S::kX, 2 * C, C, qp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
+        stage_rows_async<NT>(sm + S::kV, C, 0, vp + ((size_t)start * p.Hv + h) * D, (size_t)p.Hv * D, L, tid);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        {
+            const int nxt = item + (int)gridDim.x;
+            if (nxt < nitems) {
+                const int nc = nxt / p.Hv, nh = nxt - nc * p.Hv;
+                const int4 ni = p.table[nc];
+                const int r = tid & 63, which = tid >> 6;
+                const size_t tok = (size_t)ni.y + r;
+                if (r < ni.z) {
+                    if (which == 0) tc::prefetch_l2(kp + (tok * p.Hk + nh / grp) * D, D * 2);
+                    else if (which == 1) tc::prefetch_l2(qp + (tok * p.Hk + nh / grp) * D, D * 2);
+                    else if (which == 2) tc::prefetch_l2(vp + (tok * p.Hv + nh) * D, D * 2);
+                    else if (kKDA) tc::prefetch_l2(p.gk + (tok * p.Hv + nh) * D, D * 4);
+                }
+                if (!kKDA && tid == 255) tc::prefetch_l2_span(p.g + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 4);
+                if (tid == 254) tc::prefetch_l2_span(bp + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 2);
             }
-            *reinterpret_cast<uint4*>(Qdst + tc::chunk_k128(C + i, ch, 2 * C)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
-        if (!kKDA) {
-            if (h % grp == 0) {  // K rows of X, both column blocks -> a [64][128] k128 image
-                unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hk + kh) * kTile64x128;
-                for (int e = tid; e < (int)(kTile64x128 / 16); e += NT) {
-                    const int cb = e >> 9, r = e & 511;
-                    reinterpret_cast<uint4*>(Kdst)[e] = reinterpret_cast<const uint4*>(sm + S::kX + cb * kXcb)[r];
+        if (tid < C) bet[tid] = tid < L ? to_f(bp[((size_t)start + tid) * p.Hv + h]) : 0.f;
+        if (kKDA) {
+            if (tid < D) {
+                // per-channel inclusive cumsum in token order (thread = channel); all
+                // 64 loads are issued before the dependent adds
+                const float* __restrict__ gk = p.gk + ((size_t)start * p.Hv + h) * D + tid;
+                float x[C];
+#pragma unroll
+                for (int i = 0; i < C; ++i) x[i] = i < L ? __ldg(gk + (size_t)i * p.Hv * D) : 0.f;
+                float* dec = reinterpret_cast<float*>(sm + S::kDec);
+                float acc = 0.f;
+#pragma unroll
+                for (int i = 0; i < C; ++i) {
+                    acc += x[i];
+                    gam[i * D + tid] = acc;
+                    dec[i * D + tid] = __expf(x[i]);  // per-token decay, <= 1
                 }
             }
+        } else if (warp < 2) {
+            // scalar gate: inclusive scan over 64 tokens with two warps
+            float x = tid < L ? __ldg(p.g + ((size_t)start + tid) * p.Hv + h) : 0.f;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off) x += y;
+            }
+            gam[tid] = x;
+        }
+        __syncthreads();
+        if (!kKDA && warp == 1) gam[tid] += gam[31];
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        tc::fence_proxy_async();
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+        GDR_TRACE_PREP(1);
+        const uint32_t sX = tc::smem_u32(sm + S::kX), sV = tc::smem_u32(sm + S::kV);
+        auto gm = [&](int i, int c) -> float { return kKDA ? gam[i * D + c] : gam[i]; };
+        const float* gl = kKDA ? gam + (L - 1) * D : gam + (L - 1);
+
+        // ---- [K K^T ; Q K^T] on the tensor cores (scalar gate), one M = 128 group ------
+        if (!kKDA && tid == 0) {
+            constexpr uint32_t id = tc::idesc_bf16(128, 64, false, false);
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t off = (ks >> 2) * kXcb + (ks & 3) * 32;
+                tc::mma_bf16(tmem, tc::smem_desc(sX + off, 16, 1024, tc::kSwizzle128),
+                             tc::smem_desc(sX + off, 16, 1024, tc::kSwizzle128), id, ks > 0);
+            }
+            tc::mma_commit(bar0);
+        }
+        __syncwarp();
+
+        // ---- while that runs: Qd blob, K / Kd blob, decay record ------------------------
+        {
+            unsigned char* Qdst = p.Xw + ((size_t)chunk * p.Hv + h) * kXwBytes;  // rows 64..127
+            for (int e = tid; e < C * 16; e += NT) {
+                const int i = e >> 4, ch = e & 15;
+                const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(C + i, ch, 2 * C));
+                const __nv_bfloat16* qv = reinterpret_cast<const __nv_bfloat16*>(&raw);
+                uint32_t w4[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c = ch * 8 + 2 * u;
+                    w4[u] = tc::pack_bf16(__bfloat162float(qv[2 * u]) * __expf(gm(i, c)),
+                                          __bfloat162float(qv[2 * u + 1]) * __expf(gm(i, c + 1)));
+                }
+                *reinterpret_cast<uint4*>(Qdst + tc::chunk_k128(C + i, ch, 2 * C)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+            if (!kKDA) {
+                if (h % grp == 0) {  // K rows of X, both column blocks -> a [64][128] k128 image
+                    unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hk + kh) * kTile64x128;
+                    for (int e = tid; e < (int)(kTile64x128 / 16); e += NT) {
+                        const int cb = e >> 9, r = e & 511;
+                        reinterpret_cast<uint4*>(Kdst)[e] = reinterpret_cast<const uint4*>(sm + S::kX + cb * kXcb)[r];
+                    }
+                }
+            } else {
+                unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hv + h) * 2 * kTile64x128;
+                for (int e = tid; e < C * 16; e += NT) {
+                    const int i = e >> 4, ch = e & 15;
+                    const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(i, ch, 2 * C));
+                    const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&raw);
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int c = ch * 8 + 2 * u;
+                        const float x0 = i < L ? __bfloat162float(kv[2 * u]) * __expf(gl[c] - gam[i * D + c]) : 0.f;
+                        const float x1 = i < L ? __bfloat162float(kv[2 * u + 1]) * __expf(gl[c + 1] - gam[i * D + c + 1]) : 0.f;
+                        tc::split2(x0, x1, hw[u], lw[u]);
+                    }
+                    const uint32_t off = tc::chunk_k128(i, ch, C);
+                    *reinterpret_cast<uint4*>(Kdst + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4*>(Kdst + kTile64x128 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
+            }
+            float* rec = reinterpret_cast<float*>(p.Rb + ((size_t)chunk * p.Hv + h) * kRec);
+            if (tid < C) rec[tid] = tid < L ? (kKDA ? 1.f : __expf(gl[0] - gam[tid])) : 0.f;
+            if (tid < D) rec[64 + tid] = __expf(kKDA ? gl[tid] : gl[0]);
+            if (tid == 0) reinterpret_cast<int*>(rec)[192] = L;
+        }
+        GDR_TRACE_PREP(2);
+
+        // ---- A (strictly lower) and P (lower incl. diagonal) -------------------------
+        unsigned char* Pdst = p.Yw + ((size_t)chunk * p.Hv + h) * kYwBytes;  // rows 64..127 of column block 0
+        if (!kKDA) {
+            if (!tc::mbar_wait(bar0, ph0, abort_flag)) raise_error(p, 1u);
+            ph0 ^= 1u;
+            tc::fence_after();
+            // thread: accumulator row r = 32 q + lane (rows < 64: K K^T, >= 64: Q K^T),
+            // columns [32 hf, 32 hf + 32)
+            const int r = 32 * q + lane, i = r & 63;
+            float gv[32];
+            tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * hf, gv);
+            const float gi = gam[i], bi = bet[i];
+            if (r < C) {
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = 32 * hf + jj;
+                    As[i * LDA + j] = (j < i && i < L) ? bi * __expf(gi - gam[j]) * gv[jj] : 0.f;
+                }
+            } else {
+                uint32_t pk[16];
+#pragma unroll
+                for (int jj = 0; jj < 32; jj += 2) {
+                    const int j = 32 * hf + jj;
+                    const float p0 = (j <= i && i < L) ? __expf(gi - gam[j]) * gv[jj] : 0.f;
+                    const float p1 = (j + 1 <= i && i < L) ? __expf(gi - gam[j + 1]) * gv[jj + 1] : 0.f;
+                    pk[jj >> 1] = tc::pack_bf16(p0, p1);
+                }
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(C + i, 4 * hf + cc, 2 * C)) =
+                        make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+            }
         } else {
-            unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hv + h) * 2 * kTile64x128;
+            // Per-channel decays: A_ij = beta_i sum_c k_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}
+            // and P_ij = sum_c q_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}.  The factor is the
+            // running product of the per-token decays e^{gk_t} (t = j+1..i), all <= 1,
+            // so every intermediate is bounded for any finite gate.  Warp w handles
+            // columns j = w, w+8, ...; lane l holds key channels 4l..4l+3; 32 rows
+            // are reduced over the channels at once with the halving butterfly.
+            const float* dec = reinterpret_cast<const float*>(sm + S::kDec);
+            float* Pf = Tm;  // fp32 [64][65] staging for P (Tm is rebuilt by the solve)
+            for (int j = warp; j < C; j += NT / 32) {
+                const uint2 kjr = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(j, 4 * lane, 2 * C));
+                const __nv_bfloat16* kjb = reinterpret_cast<const __nv_bfloat16*>(&kjr);
+                float kj[4], d[4] = {1.f, 1.f, 1.f, 1.f};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) kj[u] = __bfloat162float(kjb[u]);
+                for (int base = j; base < C; base += 32) {
+                    float xa[32], xp[32];
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) {
+                        const int i = base + u;
+                        float pa = 0.f, pq = 0.f;
+                        if (i < C) {
+                            const float4 dv4 = *reinterpret_cast<const float4*>(dec + i * D + 4 * lane);
+                            if (i > j) { d[0] *= dv4.x; d[1] *= dv4.y; d[2] *= dv4.z; d[3] *= dv4.w; }
+                            const uint2 kir = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(i, 4 * lane, 2 * C));
+                            const uint2 qir = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(C + i, 4 * lane, 2 * C));
+                            const __nv_bfloat16* kib = reinterpret_cast<const __nv_bfloat16*>(&kir);
+                            const __nv_bfloat16* qib = reinterpret_cast<const __nv_bfloat16*>(&qir);
+#pragma unroll
+                            for (int w = 0; w < 4; ++w) {
+                                const float kd = kj[w] * d[w];
+                                pa = fmaf(__bfloat162float(kib[w]), kd, pa);
+                                pq = fmaf(__bfloat162float(qib[w]), kd, pq);
+                            }
+                        }
+                        xa[u] = pa;
+                        xp[u] = pq;
+                    }
+                    const float ra = reduce32_to_lane(xa, lane);
+                    const float rp = reduce32_to_lane(xp, lane);
+                    const int i = base + lane;
+                    if (i < C) {
+                        As[i * LDA + j] = (j < i && i < L) ? bet[i] * ra : 0.f;
+                        Pf[i * LDA + j] = (j <= i && i < L) ? rp : 0.f;
+                    }
+                }
+            }
+            for (int e = tid; e < C * C; e += NT) {  // entries j > i never written above
+                const int i = e >> 6, j = e & 63;
+                if (j > i) { As[i * LDA + j] = 0.f; Pf[i * LDA + j] = 0.f; }
+            }
+            __syncthreads();
+            for (int e = tid; e < C * 8; e += NT) {
+                const int i = e >> 3, ch = e & 7;
+                uint32_t w4[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) w4[u] = tc::pack_bf16(Pf[i * LDA + ch * 8 + 2 * u], Pf[i * LDA + ch * 8 + 2 * u + 1]);
+                *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(C + i, ch, 2 * C)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+            // K o e^{Gam} as hi / lo for W
             for (int e = tid; e < C * 16; e += NT) {
                 const int i = e >> 4, ch = e & 15;
                 const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(i, ch, 2 * C));
@@ -379,226 +539,115 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int c = ch * 8 + 2 * u;
-                    const float x0 = i < L ? __bfloat162float(kv[2 * u]) * __expf(gl[c] - gam[i * D + c]) : 0.f;
-                    const float x1 = i < L ? __bfloat162float(kv[2 * u + 1]) * __expf(gl[c + 1] - gam[i * D + c + 1]) : 0.f;
-                    tc::split2(x0, x1, hw[u], lw[u]);
+                    tc::split2(__bfloat162float(kv[2 * u]) * __expf(gam[i * D + c]),
+                               __bfloat162float(kv[2 * u + 1]) * __expf(gam[i * D + c + 1]), hw[u], lw[u]);
                 }
                 const uint32_t off = tc::chunk_k128(i, ch, C);
-                *reinterpret_cast<uint4*>(Kdst + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4*>(Kdst + kTile64x128 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                *reinterpret_cast<uint4*>(sm + S::kKgh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(sm + S::kKgl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
         }
-        float* rec = reinterpret_cast<float*>(p.Rb + ((size_t)chunk * p.Hv + h) * kRec);
-        if (tid < C) rec[tid] = tid < L ? (kKDA ? 1.f : __expf(gl[0] - gam[tid])) : 0.f;
-        if (tid < D) rec[64 + tid] = __expf(kKDA ? gl[tid] : gl[0]);
-        if (tid == 0) reinterpret_cast<int*>(rec)[192] = L;
-    }
-    GDR_TRACE_PREP(2);
-
-    // ---- A (strictly lower) and P (lower incl. diagonal) -------------------------
-    unsigned char* Pdst = p.Yw + ((size_t)chunk * p.Hv + h) * kYwBytes;  // rows 64..127 of column block 0
-    if (!kKDA) {
-        if (!tc::mbar_wait(bar0, 0, abort_flag)) raise_error(p, 1u);
-        tc::fence_after();
-        // thread: accumulator row r = 32 q + lane (rows < 64: K K^T, >= 64: Q K^T),
-        // columns [32 hf, 32 hf + 32)
-        const int r = 32 * q + lane, i = r & 63;
-        float gv[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * hf, gv);
-        const float gi = gam[i], bi = bet[i];
-        if (r < C) {
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int j = 32 * hf + jj;
-                As[i * LDA + j] = (j < i && i < L) ? bi * __expf(gi - gam[j]) * gv[jj] : 0.f;
-            }
-        } else {
-            uint32_t pk[16];
-#pragma unroll
-            for (int jj = 0; jj < 32; jj += 2) {
-                const int j = 32 * hf + jj;
-                const float p0 = (j <= i && i < L) ? __expf(gi - gam[j]) * gv[jj] : 0.f;
-                const float p1 = (j + 1 <= i && i < L) ? __expf(gi - gam[j + 1]) * gv[jj + 1] : 0.f;
-                pk[jj >> 1] = tc::pack_bf16(p0, p1);
-            }
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-                *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(C + i, 4 * hf + cc, 2 * C)) =
-                    make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-        }
-    } else {
-        // Per-channel decays: A_ij = beta_i sum_c k_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}
-        // and P_ij = sum_c q_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}.  The factor is the
-        // running product of the per-token decays e^{gk_t} (t = j+1..i), all <= 1,
-        // so every intermediate is bounded for any finite gate.  Warp w handles
-        // columns j = w, w+8, ...; lane l holds key channels 4l..4l+3; 32 rows
-        // are reduced over the channels at once with the halving butterfly.
-        const float* dec = reinterpret_cast<const float*>(sm + S::kDec);
-        float* Pf = Tm;  // fp32 [64][65] staging for P (Tm is rebuilt by the solve)
-        for (int j = warp; j < C; j += NT / 32) {
-            const uint2 kjr = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(j, 4 * lane, 2 * C));
-            const __nv_bfloat16* kjb = reinterpret_cast<const __nv_bfloat16*>(&kjr);
-            float kj[4], d[4] = {1.f, 1.f, 1.f, 1.f};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) kj[u] = __bfloat162float(kjb[u]);
-            for (int base = j; base < C; base += 32) {
-                float xa[32], xp[32];
-#pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int i = base + u;
-                    float pa = 0.f, pq = 0.f;
-                    if (i < C) {
-                        const float4 dv4 = *reinterpret_cast<const float4*>(dec + i * D + 4 * lane);
-                        if (i > j) { d[0] *= dv4.x; d[1] *= dv4.y; d[2] *= dv4.z; d[3] *= dv4.w; }
-                        const uint2 kir = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(i, 4 * lane, 2 * C));
-                        const uint2 qir = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(C + i, 4 * lane, 2 * C));
-                        const __nv_bfloat16* kib = reinterpret_cast<const __nv_bfloat16*>(&kir);
-                        const __nv_bfloat16* qib = reinterpret_cast<const __nv_bfloat16*>(&qir);
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            const float kd = kj[w] * d[w];
-                            pa = fmaf(__bfloat162float(kib[w]), kd, pa);
-                            pq = fmaf(__bfloat162float(qib[w]), kd, pq);
-                        }
-                    }
-                    xa[u] = pa;
-                    xp[u] = pq;
-                }
-                const float ra = reduce32_to_lane(xa, lane);
-                const float rp = reduce32_to_lane(xp, lane);
-                const int i = base + lane;
-                if (i < C) {
-                    As[i * LDA + j] = (j < i && i < L) ? bet[i] * ra : 0.f;
-                    Pf[i * LDA + j] = (j <= i && i < L) ? rp : 0.f;
-                }
-            }
-        }
-        for (int e = tid; e < C * C; e += NT) {  // entries j > i never written above
-            const int i = e >> 6, j = e & 63;
-            if (j > i) { As[i * LDA + j] = 0.f; Pf[i * LDA + j] = 0.f; }
-        }
+        tc::fence_before();
         __syncthreads();
+        GDR_TRACE_PREP(3);
+
+        // ---- Tm = (I + A)^{-1} -----------------------------------------------------------
+        solve_unit_lower(As, Tm, Z, tid);
+        GDR_TRACE_PREP(4);
+
+        // ---- split operands: T' = Tm diag(beta e^{gam}) (scalar gate) or Tm diag(beta);
+        //      T'' = Tm diag(beta).  Written over the dead Q rows of X and the A matrix.
         for (int e = tid; e < C * 8; e += NT) {
             const int i = e >> 3, ch = e & 7;
-            uint32_t w4[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) w4[u] = tc::pack_bf16(Pf[i * LDA + ch * 8 + 2 * u], Pf[i * LDA + ch * 8 + 2 * u + 1]);
-            *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(C + i, ch, 2 * C)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-        }
-        // K o e^{Gam} as hi / lo for W
-        for (int e = tid; e < C * 16; e += NT) {
-            const int i = e >> 4, ch = e & 15;
-            const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(i, ch, 2 * C));
-            const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&raw);
-            uint32_t hw[4], lw[4];
+            uint32_t h1[4], l1[4], h2[4], l2[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const int c = ch * 8 + 2 * u;
-                tc::split2(__bfloat162float(kv[2 * u]) * __expf(gam[i * D + c]),
-                           __bfloat162float(kv[2 * u + 1]) * __expf(gam[i * D + c + 1]), hw[u], lw[u]);
+                const int j = ch * 8 + 2 * u;
+                const float t0 = Tm[i * LDA + j] * bet[j], t1 = Tm[i * LDA + j + 1] * bet[j + 1];
+                tc::split2(kKDA ? t0 : t0 * __expf(gam[j]), kKDA ? t1 : t1 * __expf(gam[j + 1]), h1[u], l1[u]);
+                tc::split2(t0, t1, h2[u], l2[u]);
             }
             const uint32_t off = tc::chunk_k128(i, ch, C);
-            *reinterpret_cast<uint4*>(sm + S::kKgh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(sm + S::kKgl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            *reinterpret_cast<uint4*>(sm + S::kT1h + off) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
+            *reinterpret_cast<uint4*>(sm + S::kT1l + off) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
+            *reinterpret_cast<uint4*>(sm + S::kT2h + off) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+            *reinterpret_cast<uint4*>(sm + S::kT2l + off) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
         }
-    }
-    tc::fence_before();
-    __syncthreads();
-    GDR_TRACE_PREP(3);
+        tc::fence_proxy_async();
+        __syncthreads();
+        GDR_TRACE_PREP(5);
 
-    // ---- Tm = (I + A)^{-1} -----------------------------------------------------------
-    solve_unit_lower(As, Tm, Z, tid);
-    GDR_TRACE_PREP(4);
-
-    // ---- split operands: T' = Tm diag(beta e^{gam}) (scalar gate) or Tm diag(beta);
-    //      T'' = Tm diag(beta).  Written over the dead Q rows of X and the A matrix.
-    for (int e = tid; e < C * 8; e += NT) {
-        const int i = e >> 3, ch = e & 7;
-        uint32_t h1[4], l1[4], h2[4], l2[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int j = ch * 8 + 2 * u;
-            const float t0 = Tm[i * LDA + j] * bet[j], t1 = Tm[i * LDA + j + 1] * bet[j + 1];
-            tc::split2(kKDA ? t0 : t0 * __expf(gam[j]), kKDA ? t1 : t1 * __expf(gam[j + 1]), h1[u], l1[u]);
-            tc::split2(t0, t1, h2[u], l2[u]);
+        // ---- W = T' K (or T'' (K o e^Gam)), U = T'' V ----------------------------------------
+        if (tid == 0) {
+            tc::fence_after();
+            constexpr uint32_t id = tc::idesc_bf16(64, 128, false, true);
+            const uint32_t t1h = tc::smem_u32(sm + S::kT1h), t1l = tc::smem_u32(sm + S::kT1l);
+            const uint32_t t2h = tc::smem_u32(sm + S::kT2h), t2l = tc::smem_u32(sm + S::kT2l);
+            // B operands read MN-major: K rows of X (atom stride kXcb), V / Kg (atom stride 8 KB)
+            auto mm = [&](uint32_t dcol, uint32_t a, uint32_t b, uint32_t atom, bool first) {
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16(tmem + dcol, tc::smem_desc(a + ks * 32, 16, 1024, tc::kSwizzle128),
+                                 tc::smem_desc(b + ks * 2048, atom, 1024, tc::kSwizzle128), id, (first && ks == 0) ? 0u : 1u);
+            };
+            if (!kKDA) {
+                mm(0, t1h, sX, kXcb, true);
+                mm(0, t1l, sX, kXcb, false);
+            } else {
+                const uint32_t kgh = tc::smem_u32(sm + S::kKgh), kgl = tc::smem_u32(sm + S::kKgl);
+                mm(0, t2h, kgh, C * 128, true);
+                mm(0, t2h, kgl, C * 128, false);
+                mm(0, t2l, kgh, C * 128, false);
+            }
+            mm(128, t2h, sV, C * 128, true);
+            mm(128, t2l, sV, C * 128, false);
+            tc::mma_commit(bar0);
         }
-        const uint32_t off = tc::chunk_k128(i, ch, C);
-        *reinterpret_cast<uint4*>(sm + S::kT1h + off) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
-        *reinterpret_cast<uint4*>(sm + S::kT1l + off) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
-        *reinterpret_cast<uint4*>(sm + S::kT2h + off) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
-        *reinterpret_cast<uint4*>(sm + S::kT2l + off) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
-    }
-    tc::fence_proxy_async();
-    __syncthreads();
-    GDR_TRACE_PREP(5);
+        __syncwarp();
+        GDR_TRACE_PREP(6);
 
-    // ---- W = T' K (or T'' (K o e^Gam)), U = T'' V ----------------------------------------
-    if (tid == 0) {
+        // ---- W, U out of TMEM into their blobs: 8 warps, row i = 16 q + lane (lane <
+        //      16), columns [64 hf, 64 hf + 64) of W and of U -------------------------------
+        // the item's last completion of bar0 (the scalar gate's K K^T / Q K^T group was the first)
+        if (!tc::mbar_wait(bar0, ph0, abort_flag)) raise_error(p, 1u);
+        ph0 ^= 1u;
         tc::fence_after();
-        constexpr uint32_t id = tc::idesc_bf16(64, 128, false, true);
-        const uint32_t t1h = tc::smem_u32(sm + S::kT1h), t1l = tc::smem_u32(sm + S::kT1l);
-        const uint32_t t2h = tc::smem_u32(sm + S::kT2h), t2l = tc::smem_u32(sm + S::kT2l);
-        // B operands read MN-major: K rows of X (atom stride kXcb), V / Kg (atom stride 8 KB)
-        auto mm = [&](uint32_t dcol, uint32_t a, uint32_t b, uint32_t atom, bool first) {
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tmem + dcol, tc::smem_desc(a + ks * 32, 16, 1024, tc::kSwizzle128),
-                             tc::smem_desc(b + ks * 2048, atom, 1024, tc::kSwizzle128), id, (first && ks == 0) ? 0u : 1u);
-        };
-        if (!kKDA) {
-            mm(0, t1h, sX, kXcb, true);
-            mm(0, t1l, sX, kXcb, false);
-        } else {
-            const uint32_t kgh = tc::smem_u32(sm + S::kKgh), kgl = tc::smem_u32(sm + S::kKgl);
-            mm(0, t2h, kgh, C * 128, true);
-            mm(0, t2h, kgl, C * 128, false);
-            mm(0, t2l, kgh, C * 128, false);
-        }
-        mm(128, t2h, sV, C * 128, true);
-        mm(128, t2l, sV, C * 128, false);
-        tc::mma_commit(bar0);
-    }
-    __syncwarp();
-    GDR_TRACE_PREP(6);
-
-    // ---- W, U out of TMEM into their blobs: 8 warps, row i = 16 q + lane (lane <
-    //      16), columns [64 hf, 64 hf + 64) of W and of U -------------------------------
-    // second use of bar0 (the first, K K^T / Q K^T, exists only for the scalar gate)
-    if (!tc::mbar_wait(bar0, kKDA ? 0 : 1, abort_flag)) raise_error(p, 1u);
-    tc::fence_after();
-    {
-        const int i = 16 * q + (lane & 15);
-        const uint32_t lrow = tmem + ((uint32_t)(32 * q) << 16);
-        unsigned char* Whi = p.Xw + ((size_t)chunk * p.Hv + h) * kXwBytes;  // rows 0..63
-        unsigned char* Wlo = p.Yw + ((size_t)chunk * p.Hv + h) * kYwBytes;  // rows 0..63
-        float* Udst = reinterpret_cast<float*>(p.Ub + ((size_t)chunk * p.Hv + h) * NVB * kUBlock);
-        for (int q2 = 0; q2 < 2; ++q2) {
-            const int cb = 2 * hf + q2;  // 32-column block of W and of U
-            float wv[32], uv[32];
-            tc::tmem_ld32(lrow + 32 * cb, wv);
-            tc::tmem_ld32(lrow + 128 + 32 * cb, uv);
-            if (lane < 16) {
+        {
+            const int i = 16 * q + (lane & 15);
+            const uint32_t lrow = tmem + ((uint32_t)(32 * q) << 16);
+            unsigned char* Whi = p.Xw + ((size_t)chunk * p.Hv + h) * kXwBytes;  // rows 0..63
+            unsigned char* Wlo = p.Yw + ((size_t)chunk * p.Hv + h) * kYwBytes;  // rows 0..63
+            float* Udst = reinterpret_cast<float*>(p.Ub + ((size_t)chunk * p.Hv + h) * NVB * kUBlock);
+            for (int q2 = 0; q2 < 2; ++q2) {
+                const int cb = 2 * hf + q2;  // 32-column block of W and of U
+                float wv[32], uv[32];
+                tc::tmem_ld32(lrow + 32 * cb, wv);
+                tc::tmem_ld32(lrow + 128 + 32 * cb, uv);
+                if (lane < 16) {
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t hw[4], lw[4];
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t hw[4], lw[4];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) tc::split2(wv[8 * cc + 2 * u], wv[8 * cc + 2 * u + 1], hw[u], lw[u]);
-                    const uint32_t off = tc::chunk_k128(i, 4 * cb + cc, 2 * C);
-                    *reinterpret_cast<uint4*>(Whi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4*>(Wlo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                        for (int u = 0; u < 4; ++u) tc::split2(wv[8 * cc + 2 * u], wv[8 * cc + 2 * u + 1], hw[u], lw[u]);
+                        const uint32_t off = tc::chunk_k128(i, 4 * cb + cc, 2 * C);
+                        *reinterpret_cast<uint4*>(Whi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4*>(Wlo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    }
+                    // U block cb stored value-major [32 v][64 i]: the chain's thread for
+                    // row i then reads a conflict-free column of shared memory
+                    float* ublk = Udst + (size_t)cb * (C * BV) + i;
+#pragma unroll
+                    for (int v = 0; v < BV; ++v) ublk[(size_t)v * C] = uv[v];
                 }
-                // U block cb stored value-major [32 v][64 i]: the chain's thread for
-                // row i then reads a conflict-free column of shared memory
-                float* ublk = Udst + (size_t)cb * (C * BV) + i;
-#pragma unroll
-                for (int v = 0; v < BV; ++v) ublk[(size_t)v * C] = uv[v];
             }
         }
-    }
-    GDR_TRACE_PREP(7);
-    tc::fence_before();
-    __syncthreads();
+        GDR_TRACE_PREP(7);
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+        GDR_TRACE_PREP(8);
+        GDR_TRACE_ITEM(item, 1);
+    }  // item loop
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
-    GDR_TRACE_PREP(8);
 }
 
 // ---------------------------------------------------------------------------
@@ -920,6 +969,17 @@ size_t chunk_tc_blob_bytes(int64_t max_chunks, int Hk, int Hv, bool kda) {
     return n;
 }
 
+// Persistent prep grid: one CTA per resident slot (SMs x CTAs per SM), never
+// more than the item capacity (chunk capacity x value heads).
+static unsigned prep_grid(size_t items, int per_sm) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+        sms = 148;
+    const size_t slots = (size_t)sms * per_sm;
+    return (unsigned)(items < slots ? items : slots);
+}
+
 cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* ws, const void* q, const void* k,
                             cudaStream_t stream) {
     const bool kda = a.gk != nullptr;
@@ -946,7 +1006,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* w
         cudaFuncSetAttribute(chunk_chain_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smc);
         {
             KernelTimer kt("chunk_prep", stream);
-            chunk_prep_kernel<true><<<dim3((unsigned)mc, a.Hv), kPrepThreads, smp, stream>>>(p);
+            chunk_prep_kernel<true><<<prep_grid(mc * a.Hv, 1), kPrepThreads, smp, stream>>>(p);
         }
         KernelTimer kt("chunk_chain", stream);
         chunk_chain_kernel<true><<<dim3(a.Hv * NVB, a.N), 512, smc, stream>>>(p);
@@ -956,7 +1016,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* w
         cudaFuncSetAttribute(chunk_chain_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smc);
         {
             KernelTimer kt("chunk_prep", stream);
-            chunk_prep_kernel<false><<<dim3((unsigned)mc, a.Hv), kPrepThreads, smp, stream>>>(p);
+            chunk_prep_kernel<false><<<prep_grid(mc * a.Hv, 2), kPrepThreads, smp, stream>>>(p);
         }
         KernelTimer kt("chunk_chain", stream);
         chunk_chain_kernel<false><<<dim3(a.Hv * NVB, a.N), 512, smc, stream>>>(p);

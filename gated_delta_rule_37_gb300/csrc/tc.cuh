@@ -195,6 +195,17 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uin
                  :: "r"(dst_smem), "l"(src), "r"(bytes), "r"(mbar) : "memory");
 }
 
+// L2 prefetch of `bytes` (multiple of 16) at a 16-byte aligned global address.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
+}
+// L2 prefetch of the 16-byte aligned interior of [src, src + bytes).
+__device__ __forceinline__ void prefetch_l2_span(const void* src, size_t bytes) {
+    const uintptr_t a = (reinterpret_cast<uintptr_t>(src) + 15) & ~uintptr_t(15);
+    const uintptr_t b = (reinterpret_cast<uintptr_t>(src) + bytes) & ~uintptr_t(15);
+    if (b > a) prefetch_l2(reinterpret_cast<const void*>(a), (uint32_t)(b - a));
+}
+
 // ---- named barriers -------------------------------------------------------------
 __device__ __forceinline__ void bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
