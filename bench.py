@@ -257,31 +257,61 @@ class Prefill:
                       scale=self.case.scale, o=self.o, final_state=self.hT, workspace=self.ws, stream=stream)
 
     def e2e(self, K, stream):
-        """Same call through the public API from pinned host buffers: H2D of
-        the step's inputs and D2H of its outputs inside the timed region."""
+        """The same call through the public API from pinned host buffers: every
+        step copies its inputs host -> device, runs the call and copies o and
+        the final state back, all inside the timed region.  Steps are
+        pipelined the way a serving loop would run them: inputs and outputs
+        are double-buffered on the device, the copies run on their own streams
+        and overlap the neighbouring steps' compute."""
         c = self.case
         host_in = [t.pin_memory() for t in (c.q, c.k, c.v, c.beta, c.cu_seqlens)]
-        gate = (c.g if c.g is not None else c.gk).pin_memory()
-        h0 = c.initial_state.pin_memory() if c.initial_state is not None else None
-        dev_in = [self.q, self.k, self.v, self.beta, self.cu]
-        dgate = self.g if self.g is not None else self.gk
+        host_in.append((c.g if c.g is not None else c.gk).pin_memory())
+        if c.initial_state is not None:
+            host_in.append(c.initial_state.pin_memory())
+        dev_in = [[torch.empty_like(h, device=self.dev) for h in host_in] for _ in range(2)]
+        dev_out = [(torch.empty_like(self.o), torch.empty_like(self.hT)) for _ in range(2)]
         o_host = torch.empty(self.o.shape, dtype=self.o.dtype).pin_memory()
         hT_host = torch.empty(self.hT.shape, dtype=torch.float32).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host_in + [gate] + ([h0] if h0 is not None else []))
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
         d2h = o_host.numel() * o_host.element_size() + hT_host.numel() * 4
+        s_in, s_out = torch.cuda.Stream(self.dev), torch.cuda.Stream(self.dev)
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        in_ready = [ev() for _ in range(2)]
+        in_free = [ev() for _ in range(2)]
+        out_ready = [ev() for _ in range(2)]
+        out_free = [ev() for _ in range(2)]
         start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            start.record(stream)
-            for _ in range(K):
-                for d, h in zip(dev_in, host_in):
+        torch.cuda.synchronize()
+        start.record(stream)
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        for i in range(K):
+            b = i & 1
+            if i >= 2:
+                s_in.wait_event(in_free[b])
+            with torch.cuda.stream(s_in):
+                for d, h in zip(dev_in[b], host_in):
                     d.copy_(h, non_blocking=True)
-                dgate.copy_(gate, non_blocking=True)
-                if h0 is not None:
-                    self.h0.copy_(h0, non_blocking=True)
-                self.step(stream)
-                o_host.copy_(self.o, non_blocking=True)
-                hT_host.copy_(self.hT, non_blocking=True)
-            end.record(stream)
+                in_ready[b].record(s_in)
+            stream.wait_event(in_ready[b])
+            if i >= 2:
+                stream.wait_event(out_free[b])
+            q, k, v, beta, cu, gate = dev_in[b][:6]
+            h0 = dev_in[b][6] if c.initial_state is not None else None
+            o, hT = dev_out[b]
+            gdr.chunk_fwd(q, k, v, beta, cu, g=gate if c.g is not None else None,
+                          gk=gate if c.gk is not None else None, initial_state=h0, scale=c.scale,
+                          o=o, final_state=hT, workspace=self.ws, stream=stream)
+            in_free[b].record(stream)
+            out_ready[b].record(stream)
+            s_out.wait_event(out_ready[b])
+            with torch.cuda.stream(s_out):
+                o_host.copy_(o, non_blocking=True)
+                hT_host.copy_(hT, non_blocking=True)
+                out_free[b].record(s_out)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+        end.record(stream)
         torch.cuda.synchronize()
         ms = start.elapsed_time(end) / K
         return ms, h2d, d2h
