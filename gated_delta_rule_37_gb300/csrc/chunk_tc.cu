@@ -260,11 +260,15 @@ struct PrepSmem {
     static constexpr uint32_t kKgh = (kZ + 4 * 256 * 4 + 1023) & ~1023u;  // K o e^Gam hi (channel gate)
     static constexpr uint32_t kKgl = kKgh + (kKDA ? kTile64x128 : 0);
     static constexpr uint32_t kGam = kKgl + (kKDA ? kTile64x128 : 0);    // fp32 [64][128] or [64]
-    static constexpr uint32_t kDec = kGam + (kKDA ? C * D * 4 : C * 4);  // fp32 [64][128] e^{gk} (channel gate)
-    static constexpr uint32_t kBeta = kDec + (kKDA ? C * D * 4 : 0);
+    static constexpr uint32_t kPf = kGam + (kKDA ? C * D * 4 : C * 4);   // fp32 [64][65] P staging (channel gate)
+    static constexpr uint32_t kBeta = kPf + (kKDA ? C * LDA * 4 : 0);
+    // channel gate, while A and P are formed: pivoted operands over the dead
+    // Tm / Z / Kg region (64-row left and 32-row right tiles, hi and lo)
+    static constexpr uint32_t kLh = kTm, kLl = kLh + C * 256, kRh = kLl + C * 256, kRl = kRh + 32 * 256;
     static constexpr uint32_t kBar = kBeta + C * 4;
     static constexpr uint32_t kTotal = kBar + 64 + 1024;  // + alignment slack
     static_assert(kT2l + kTile64x64 <= kTm, "T'' tiles overlap Tm");
+    static_assert(!kKDA || kRl + 32 * 256 <= kGam, "pivot operands overlap the gate cumsum");
 };
 
 template <bool kKDA>
@@ -293,11 +297,12 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::kBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::kBar + 16);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::kBar + 24);
-    const uint32_t bar0 = tc::smem_u32(&bars[0]);
+    const uint32_t bar0 = tc::smem_u32(&bars[0]), bar1 = tc::smem_u32(&bars[1]);
 
     if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), 256);
     if (tid == 0) {
         tc::mbar_init(bar0, 1);
+        tc::mbar_init(bar1, 3);
         *abort_flag = 0;
         tc::mbar_fence_init();
     }
@@ -305,7 +310,7 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
-    uint32_t ph0 = 0;  // parity of the next completion of bar0
+    uint32_t ph0 = 0, ph1 = 0;  // parity of the next completion of bar0 / bar1
 
     for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
         const int chunk = item / p.Hv, h = item - chunk * p.Hv;
@@ -346,13 +351,11 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
                 float x[C];
 #pragma unroll
                 for (int i = 0; i < C; ++i) x[i] = i < L ? __ldg(gk + (size_t)i * p.Hv * D) : 0.f;
-                float* dec = reinterpret_cast<float*>(sm + S::kDec);
                 float acc = 0.f;
 #pragma unroll
                 for (int i = 0; i < C; ++i) {
                     acc += x[i];
                     gam[i * D + tid] = acc;
-                    dec[i * D + tid] = __expf(x[i]);  // per-token decay, <= 1
                 }
             }
         } else if (warp < 2) {
@@ -473,54 +476,157 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
             }
         } else {
             // Per-channel decays: A_ij = beta_i sum_c k_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}
-            // and P_ij = sum_c q_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}.  The factor is the
-            // running product of the per-token decays e^{gk_t} (t = j+1..i), all <= 1,
-            // so every intermediate is bounded for any finite gate.  Warp w handles
-            // columns j = w, w+8, ...; lane l holds key channels 4l..4l+3; 32 rows
-            // are reduced over the channels at once with the halving butterfly.
-            const float* dec = reinterpret_cast<const float*>(sm + S::kDec);
-            float* Pf = Tm;  // fp32 [64][65] staging for P (Tm is rebuilt by the solve)
-            for (int j = warp; j < C; j += NT / 32) {
-                const uint2 kjr = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(j, 4 * lane, 2 * C));
-                const __nv_bfloat16* kjb = reinterpret_cast<const __nv_bfloat16*>(&kjr);
-                float kj[4], d[4] = {1.f, 1.f, 1.f, 1.f};
+            // and P_ij = sum_c q_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}.  Pairs in different
+            // halves of a block of 2h tokens (h = 32, 16, 8, 4) go through the tensor
+            // cores with the pivot p = first token of the upper half (j < p <= i):
+            // e^{gam_i - gam_j} = e^{gam_i - gam_p} e^{gam_p - gam_j}, both factors
+            // <= 1, folded into the left (k_i, q_i) and right (k_j) operands, each
+            // split into bf16 hi + lo (3 products).  Pairs inside a 4-token block are
+            // formed directly.  Every exponent is <= 0 for any finite gate.
+            float* Pf = reinterpret_cast<float*>(sm + S::kPf);
+            for (int e = tid; e < C * LDA; e += NT) {
+                As[e] = 0.f;
+                Pf[e] = 0.f;
+            }
+            constexpr uint32_t idL = tc::idesc_bf16(64, 32, false, false);
+            for (int lev = 0; lev < 4; ++lev) {
+                const int sh = 5 - lev, hh = 1 << sh;  // half-block size 32, 16, 8, 4
+                // operand rows: 32 left tokens (K rows 0..31 and Q rows 32..63 of the
+                // 64-row tile) and 32 right tokens, each in 16 chunks of 8 channels
+                for (int e = tid; e < 64 * 16; e += NT) {
+                    const int tr = e >> 4, ch = e & 15;
+                    const bool left = tr < 32;
+                    const int idx = tr & 31, B = idx >> sh, t = idx & (hh - 1);
+                    const int piv = 2 * hh * B + hh;
+                    const int tok = left ? piv + t : piv - hh + t;
+                    const float4* gt = reinterpret_cast<const float4*>(gam + tok * D + ch * 8);
+                    const float4* gp = reinterpret_cast<const float4*>(gam + piv * D + ch * 8);
+                    float f[8];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) kj[u] = __bfloat162float(kjb[u]);
-                for (int base = j; base < C; base += 32) {
-                    float xa[32], xp[32];
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) {
-                        const int i = base + u;
-                        float pa = 0.f, pq = 0.f;
-                        if (i < C) {
-                            const float4 dv4 = *reinterpret_cast<const float4*>(dec + i * D + 4 * lane);
-                            if (i > j) { d[0] *= dv4.x; d[1] *= dv4.y; d[2] *= dv4.z; d[3] *= dv4.w; }
-                            const uint2 kir = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(i, 4 * lane, 2 * C));
-                            const uint2 qir = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(C + i, 4 * lane, 2 * C));
-                            const __nv_bfloat16* kib = reinterpret_cast<const __nv_bfloat16*>(&kir);
-                            const __nv_bfloat16* qib = reinterpret_cast<const __nv_bfloat16*>(&qir);
-#pragma unroll
-                            for (int w = 0; w < 4; ++w) {
-                                const float kd = kj[w] * d[w];
-                                pa = fmaf(__bfloat162float(kib[w]), kd, pa);
-                                pq = fmaf(__bfloat162float(qib[w]), kd, pq);
-                            }
-                        }
-                        xa[u] = pa;
-                        xp[u] = pq;
+                    for (int u = 0; u < 2; ++u) {
+                        const float4 a4 = gt[u], b4 = gp[u];
+                        const float d0 = a4.x - b4.x, d1 = a4.y - b4.y, d2 = a4.z - b4.z, d3 = a4.w - b4.w;
+                        f[4 * u + 0] = __expf(left ? d0 : -d0);
+                        f[4 * u + 1] = __expf(left ? d1 : -d1);
+                        f[4 * u + 2] = __expf(left ? d2 : -d2);
+                        f[4 * u + 3] = __expf(left ? d3 : -d3);
                     }
-                    const float ra = reduce32_to_lane(xa, lane);
-                    const float rp = reduce32_to_lane(xp, lane);
-                    const int i = base + lane;
-                    if (i < C) {
-                        As[i * LDA + j] = (j < i && i < L) ? bet[i] * ra : 0.f;
-                        Pf[i * LDA + j] = (j <= i && i < L) ? rp : 0.f;
+                    const uint4 kr = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(tok, ch, 2 * C));
+                    const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&kr);
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        tc::split2(__bfloat162float(kv[2 * u]) * f[2 * u], __bfloat162float(kv[2 * u + 1]) * f[2 * u + 1],
+                                   hw[u], lw[u]);
+                    if (left) {
+                        const uint32_t off = tc::chunk_k128(idx, ch, C);
+                        *reinterpret_cast<uint4*>(sm + S::kLh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4*>(sm + S::kLl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                        const uint4 qr = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(C + tok, ch, 2 * C));
+                        const __nv_bfloat16* qv = reinterpret_cast<const __nv_bfloat16*>(&qr);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            tc::split2(__bfloat162float(qv[2 * u]) * f[2 * u], __bfloat162float(qv[2 * u + 1]) * f[2 * u + 1],
+                                       hw[u], lw[u]);
+                        const uint32_t offq = tc::chunk_k128(32 + idx, ch, C);
+                        *reinterpret_cast<uint4*>(sm + S::kLh + offq) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4*>(sm + S::kLl + offq) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    } else {
+                        const uint32_t off = tc::chunk_k128(idx, ch, 32);
+                        *reinterpret_cast<uint4*>(sm + S::kRh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4*>(sm + S::kRl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                     }
                 }
+                tc::fence_proxy_async();
+                tc::fence_before();
+                __syncthreads();
+                tc::fence_after();
+                // three issuers, one split product each, into accumulator columns 32 w
+                if (warp < 3 && lane == 0) {
+                    const uint32_t la = tc::smem_u32(sm + (warp == 2 ? S::kLl : S::kLh));
+                    const uint32_t rb = tc::smem_u32(sm + (warp == 1 ? S::kRl : S::kRh));
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_bf16(tmem + 32 * warp,
+                                     tc::smem_desc(la + (ks >> 2) * (C * 128) + (ks & 3) * 32, 16, 1024, tc::kSwizzle128),
+                                     tc::smem_desc(rb + (ks >> 2) * (32 * 128) + (ks & 3) * 32, 16, 1024, tc::kSwizzle128),
+                                     idL, ks > 0);
+                    tc::mma_commit(bar1);
+                }
+                __syncwarp();
+                if (!tc::mbar_wait(bar1, ph1, abort_flag)) raise_error(p, 1u);
+                ph1 ^= 1u;
+                tc::fence_after();
+                if (warp < 4) {
+                    // M = 64 accumulator: row r = 16 warp + lane (lane < 16); rows 0..31
+                    // are A rows, 32..63 P rows; column n pairs with row r when both
+                    // fall in the same block of 2h tokens
+                    float d[32], e2[32];
+                    const uint32_t lrow = tmem + ((uint32_t)(32 * warp) << 16);
+                    tc::tmem_ld32(lrow, d);
+                    tc::tmem_ld32(lrow + 32, e2);
+#pragma unroll
+                    for (int n = 0; n < 32; ++n) d[n] += e2[n];
+                    tc::tmem_ld32(lrow + 64, e2);
+#pragma unroll
+                    for (int n = 0; n < 32; ++n) d[n] += e2[n];
+                    const int r = 16 * warp + lane, idx = r & 31, B = idx >> sh;
+                    const int i = 2 * hh * B + hh + (idx & (hh - 1));
+                    if (lane < 16 && i < L) {
+                        float* dst = (warp < 2 ? As : Pf) + i * LDA;
+                        const float sc = warp < 2 ? bet[i] : 1.f;
+#pragma unroll
+                        for (int n = 0; n < 32; ++n)
+                            if ((n >> sh) == B) dst[2 * hh * B + (n & (hh - 1))] = sc * d[n];
+                    }
+                }
+                tc::fence_before();
             }
-            for (int e = tid; e < C * C; e += NT) {  // entries j > i never written above
-                const int i = e >> 6, j = e & 63;
-                if (j > i) { As[i * LDA + j] = 0.f; Pf[i * LDA + j] = 0.f; }
+            {
+                // pairs inside a 4-token block: warp w takes tokens 8w..8w+7 (two
+                // blocks, 10 pairs j <= i each), lane l channels 4l..4l+3
+                float gv[8][4], kf[8][4], qf[8][4];
+#pragma unroll
+                for (int tk = 0; tk < 8; ++tk) {
+                    const int tok = 8 * warp + tk;
+                    const float4 g4 = *reinterpret_cast<const float4*>(gam + tok * D + 4 * lane);
+                    gv[tk][0] = g4.x; gv[tk][1] = g4.y; gv[tk][2] = g4.z; gv[tk][3] = g4.w;
+                    const uint2 kr = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(tok, 4 * lane, 2 * C));
+                    const uint2 qr = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(C + tok, 4 * lane, 2 * C));
+                    const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&kr);
+                    const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(&qr);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        kf[tk][c] = __bfloat162float(kb[c]);
+                        qf[tk][c] = __bfloat162float(qb[c]);
+                    }
+                }
+                float xa[32], xp[32];
+#pragma unroll
+                for (int pp = 0; pp < 32; ++pp) {
+                    xa[pp] = 0.f;
+                    xp[pp] = 0.f;
+                    if (pp < 20) {
+                        const int pr = pp % 10, di = (pr >= 1) + (pr >= 3) + (pr >= 6), dj = pr - di * (di + 1) / 2;
+                        const int a = 4 * (pp / 10) + di, bb = 4 * (pp / 10) + dj;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const float ex = __expf(gv[a][c] - gv[bb][c]);
+                            const float kd = kf[bb][c] * ex;
+                            xa[pp] = fmaf(kf[a][c], kd, xa[pp]);
+                            xp[pp] = fmaf(qf[a][c], kd, xp[pp]);
+                        }
+                    }
+                }
+                const float ra = reduce32_to_lane(xa, lane);
+                const float rp = reduce32_to_lane(xp, lane);
+                if (lane < 20) {
+                    const int pr = lane % 10, di = (pr >= 1) + (pr >= 3) + (pr >= 6), dj = pr - di * (di + 1) / 2;
+                    const int i = 8 * warp + 4 * (lane / 10) + di, j = 8 * warp + 4 * (lane / 10) + dj;
+                    if (i < L) {
+                        if (j < i) As[i * LDA + j] = bet[i] * ra;
+                        Pf[i * LDA + j] = rp;
+                    }
+                }
             }
             __syncthreads();
             for (int e = tid; e < C * 8; e += NT) {
