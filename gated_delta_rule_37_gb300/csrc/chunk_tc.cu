@@ -541,6 +541,7 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
                 tc::fence_before();
                 __syncthreads();
                 tc::fence_after();
+                GDR_TRACE_PREP(9 + 3 * lev);
                 // three issuers, one split product each, into accumulator columns 32 w
                 if (warp < 3 && lane == 0) {
                     const uint32_t la = tc::smem_u32(sm + (warp == 2 ? S::kLl : S::kLh));
@@ -556,6 +557,7 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
                 if (!tc::mbar_wait(bar1, ph1, abort_flag)) raise_error(p, 1u);
                 ph1 ^= 1u;
                 tc::fence_after();
+                GDR_TRACE_PREP(10 + 3 * lev);
                 if (warp < 4) {
                     // M = 64 accumulator: row r = 16 warp + lane (lane < 16); rows 0..31
                     // are A rows, 32..63 P rows; column n pairs with row r when both
@@ -580,6 +582,7 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
                     }
                 }
                 tc::fence_before();
+                GDR_TRACE_PREP(11 + 3 * lev);
             }
             {
                 // pairs inside a 4-token block: warp w takes tokens 8w..8w+7 (two
@@ -775,9 +778,13 @@ struct ChainSmem {
     static constexpr uint32_t kSl = kSh + D * BV * 2;        // S^T lo (the next atom: [S_hi | S_lo])
     static constexpr uint32_t kNh = kSl + D * BV * 2;        // N' hi [64][32] mn64
     static constexpr uint32_t kNl = kNh + C * BV * 2;        // N' lo
-    static constexpr uint32_t kN = kNl + C * BV * 2;         // N (bf16) for the output
-    static constexpr uint32_t kBar = kN + C * BV * 2;
+    // N (bf16) for the output: two buffers by chunk parity (one with per-channel
+    // gates, whose stages carry the second K tile and leave no room)
+    static constexpr int kNBuf = kKDA ? 1 : 2;
+    static constexpr uint32_t kN = kNl + C * BV * 2;
+    static constexpr uint32_t kBar = kN + kNBuf * C * BV * 2;
     static constexpr uint32_t kTotal = kBar + 256 + 1024;
+    static_assert(kTotal <= 232448, "chain shared memory above the 227 KB opt-in limit");
 };
 
 enum ChainBar {
@@ -850,6 +857,15 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                 if (kKDA) tc::bulk_g2s(st + S::kKt, p.Kb + (gc * p.Hv + h) * 2 * kTile64x128, 2 * kTile64x128, fb);
                 else tc::bulk_g2s(st + S::kKt, p.Kb + (gc * p.Hk + kh) * kTile64x128, kTile64x128, fb);
                 tc::bulk_g2s(st + S::kRec_, p.Rb + (gc * p.Hv + h) * kRec, kRec, fb);
+                if (c + 2 < nc) {  // warm L2 with the blobs of chunk c + 2
+                    const size_t g2 = gc + 2;
+                    tc::prefetch_l2(p.Xw + (g2 * p.Hv + h) * kXwBytes, kXwBytes);
+                    tc::prefetch_l2(p.Yw + (g2 * p.Hv + h) * kYwBytes, kYwBytes);
+                    tc::prefetch_l2(p.Ub + ((g2 * p.Hv + h) * NVB + vb) * kUBlock, kUBlock);
+                    if (kKDA) tc::prefetch_l2(p.Kb + (g2 * p.Hv + h) * 2 * kTile64x128, 2 * kTile64x128);
+                    else tc::prefetch_l2(p.Kb + (g2 * p.Hk + kh) * kTile64x128, kTile64x128);
+                    tc::prefetch_l2(p.Rb + (g2 * p.Hv + h) * kRec, kRec);
+                }
                 GDR_TRACE_POINT(1, c);
             }
             // drain: wait for the copies of the last (up to) two stages to land
@@ -933,6 +949,8 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                 issued = true;
                 GDR_TRACE_POINT(4, c);
             } else if (isB) {
+                // rows 64..127 of the second column block are not part of the blob;
+                // the accumulator rows they reach are not read
                 tc::fence_after();
                 tc::mma_ksteps<8>(tD1b, dk128(st + S::kYW), a128, dmn64(base + S::kSh, 512), 64, idB, true);
                 tc::mma_commit(bar(kD1Full));
@@ -953,14 +971,22 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             if (!tc::mbar_wait(bar(kD1Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
             if (lead) GDR_TRACE_POINT(9, c);
             tc::fence_after();
-            float dv[48];
+            float ws[16];  // (W S^T) for this thread's row and 16 columns
             if (nrow) {  // quadrants 0 and 1 (warp-uniform)
+                float dv[48];
                 tc::tmem_ld16x3(tD1 + 64 * ob + lane_base + vh, tD1 + 64 * ob + lane_base + BV + vh,
                                 tD1b + lane_base + vh, dv);
+#pragma unroll
+                for (int v = 0; v < 16; ++v) ws[v] = dv[v] + dv[16 + v] + dv[32 + v];
             }
             if (lead) GDR_TRACE_POINT(15, c);
-            // the N tiles were last read by the output product of chunk c - 1
-            if (c >= 1 && !tc::mbar_wait(bar(kOFull0 + ((c - 1) & 1)), ((c - 1) >> 1) & 1, abort_flag)) fail();
+            // the N tile was last read by the output product of chunk c - kNBuf
+            if (S::kNBuf == 2) {
+                if (c >= 2 && !tc::mbar_wait(bar(kOFull0 + ob), ((c - 2) >> 1) & 1, abort_flag)) fail();
+            } else {
+                if (c >= 1 && !tc::mbar_wait(bar(kOFull0 + ((c - 1) & 1)), ((c - 1) >> 1) & 1, abort_flag)) fail();
+            }
+            const uint32_t nbuf = (uint32_t)(ob % S::kNBuf) * (C * BV * 2);
             if (lead) GDR_TRACE_POINT(16, c);
             if (nrow) {
                 const float keep = i < Lc ? 1.f : 0.f;  // rows past the chunk end
@@ -970,15 +996,15 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int v = 8 * cc + 2 * u;
-                        const float n0 = (uv[v] - (dv[v] + dv[16 + v] + dv[32 + v])) * keep;
-                        const float n1 = (uv[v + 1] - (dv[v + 1] + dv[17 + v] + dv[33 + v])) * keep;
+                        const float n0 = (uv[v] - ws[v]) * keep;
+                        const float n1 = (uv[v + 1] - ws[v + 1]) * keep;
                         tc::split2(n0 * rowf, n1 * rowf, hw[u], lw[u]);
                         nw[u] = tc::pack_bf16(n0, n1);
                     }
                     const uint32_t off = tc::chunk_mn64(i, 2 * hf + cc);
                     *reinterpret_cast<uint4*>(sm + S::kNh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                     *reinterpret_cast<uint4*>(sm + S::kNl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                    *reinterpret_cast<uint4*>(sm + S::kN + off) = make_uint4(nw[0], nw[1], nw[2], nw[3]);
+                    *reinterpret_cast<uint4*>(sm + S::kN + nbuf + off) = make_uint4(nw[0], nw[1], nw[2], nw[3]);
                 }
             }
             if (lead) GDR_TRACE_POINT(17, c);
@@ -996,7 +1022,8 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                 GDR_TRACE_POINT(6, c);
             } else if (isC) {
                 tc::fence_after();
-                tc::mma_ksteps<4>(tD1 + 64 * ob, dk128(st + S::kYW), a64, dmn64(base + S::kN, 512), 64, idB, false);
+                tc::mma_ksteps<4>(tD1 + 64 * ob, dk128(st + S::kYW), a64, dmn64(base + S::kN + nbuf, 512), 64,
+                                  idB, false);
                 tc::mma_commit(bar(kOFull0 + ob));
                 tc::mma_commit(bar(kEmpty0 + s));
                 issued = true;
@@ -1005,9 +1032,12 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             if (!tc::mbar_wait(bar(kD2Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
             if (lead) GDR_TRACE_POINT(11, c);
             tc::fence_after();
-            tc::tmem_ld16x3(tD2 + lane_base + vh, tD2 + lane_base + BV + vh, tD2 + lane_base + vh, dv);
+            {
+                float dv[48];
+                tc::tmem_ld16x3(tD2 + lane_base + vh, tD2 + lane_base + BV + vh, tD2 + lane_base + vh, dv);
 #pragma unroll
-            for (int v = 0; v < 16; ++v) Sreg[v] = fmaf(colf, Sreg[v], dv[v] + dv[16 + v]);
+                for (int v = 0; v < 16; ++v) Sreg[v] = fmaf(colf, Sreg[v], dv[v] + dv[16 + v]);
+            }
             if (lead) GDR_TRACE_POINT(12, c);
             tc::fence_before();
         }
@@ -1035,10 +1065,10 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             if (tid == 384) GDR_TRACE_POINT(13, c);
             tc::fence_after();
             if (drain) {
-                float ov[2 * BV];
-                tc::tmem_ld64(tD1 + 64 * ob + lane_base, ov);
+                float ov[BV], ld[2 * BV];
+                tc::tmem_ld64(tD1 + 64 * ob + lane_base, ld);
 #pragma unroll
-                for (int v = 0; v < BV; ++v) ov[v] += ov[BV + v];
+                for (int v = 0; v < BV; ++v) ov[v] = ld[v] + ld[BV + v];
                 const int cs = bos + c * C;
                 if (cs + i < eos) {
                     uint4* dst = reinterpret_cast<uint4*>(op + ((size_t)(cs + i) * p.Hv + h) * D + v0);

@@ -66,10 +66,26 @@ recurrent_kernel(RecParams p) {
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r) Vec<PoolT, KPT>::load(srow + (size_t)r * K, s[r]);
 
+    // Per-token inputs of token t + 1 are loaded while token t is processed, so
+    // their global-load latency is hidden behind the reductions of the current token.
+    float kn[KPT], qn[KPT], gn = 0.f, bn = 0.f, vn = 0.f;
+    auto load_token = [&](int t) {
+        Vec<InT, KPT>::load(kp + ((size_t)t * p.Hk + kh) * K + lane * KPT, kn);
+        Vec<InT, KPT>::load(qp + ((size_t)t * p.Hk + kh) * K + lane * KPT, qn);
+        gn = p.g[(size_t)t * p.Hv + h];
+        bn = to_f(bp[(size_t)t * p.Hv + h]);
+        vn = to_f(vp[((size_t)t * p.Hv + h) * V + v0 + (lane & 15)]);
+    };
+    if (bos < eos) load_token(bos);
+#pragma unroll 1
     for (int t = bos; t < eos; ++t) {
         float kk[KPT], qq[KPT];
-        Vec<InT, KPT>::load(kp + ((size_t)t * p.Hk + kh) * K + lane * KPT, kk);
-        Vec<InT, KPT>::load(qp + ((size_t)t * p.Hk + kh) * K + lane * KPT, qq);
+#pragma unroll
+        for (int c = 0; c < KPT; ++c) { kk[c] = kn[c]; qq[c] = qn[c]; }
+        const float a = __expf(gn);
+        const float bt = bn;
+        const float vv = vn;
+        if (t + 1 < eos) load_token(t + 1);
         if (p.flags & 1) {  // GDR_QK_L2NORM
             float sk = 0.f, sq = 0.f;
 #pragma unroll
@@ -78,9 +94,6 @@ recurrent_kernel(RecParams p) {
 #pragma unroll
             for (int c = 0; c < KPT; ++c) { kk[c] *= ik; qq[c] *= iq; }
         }
-        const float a = __expf(p.g[(size_t)t * p.Hv + h]);
-        const float bt = to_f(bp[(size_t)t * p.Hv + h]);
-        const float vv = to_f(vp[((size_t)t * p.Hv + h) * V + v0 + (lane & 15)]);
 
         float x[32];
 #pragma unroll
