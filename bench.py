@@ -193,11 +193,11 @@ class ClockSampler:
 def timed_steps(step, K, flush, stream, profile=True):
     """Run K steps, each bracketed by CUDA events on `stream`, with the L2
     flushed (outside the events) before each.  Returns per-step ms and the
-    per-kernel profile of the timed steps."""
+    per-kernel profile of an identical pass of K steps run right after: the
+    library's per-launch profiling events sit between its launches and would
+    keep the kernels of one call from overlapping, so the timed pass runs
+    without them."""
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    if profile:
-        gdr.profile_read()
-        gdr.profile_enable(True)
     with torch.cuda.stream(stream):
         for i in range(K):
             flush()
@@ -207,6 +207,13 @@ def timed_steps(step, K, flush, stream, profile=True):
     torch.cuda.synchronize()
     prof = {}
     if profile:
+        gdr.profile_read()
+        gdr.profile_enable(True)
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                flush()
+                step()
+        torch.cuda.synchronize()
         gdr.profile_enable(False)
         prof = gdr.profile_read()
     return [a.elapsed_time(b) for a, b in evs], prof

@@ -76,6 +76,8 @@ __global__ void __launch_bounds__(1024) chunk_meta_kernel(const int32_t* __restr
                                                           int4* __restrict__ table, int* __restrict__ order) {
     __shared__ int warp_sum[32];
     __shared__ int bad;
+    // the next kernel, if launched as a dependent, may start its prologue now
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     if (tid == 0) bad = (cu[0] != 0 || (int64_t)cu[N] != T);
     __syncthreads();

@@ -279,8 +279,6 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     // Persistent: CTA x takes items x, x + gridDim.x, ... (item = chunk * Hv + h)
     // and warms L2 with the next item's rows while it computes the current one.
-    const int nitems = p.meta[0] * p.Hv;
-    if ((int)blockIdx.x >= nitems) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q = warp & 3, hf = warp >> 2;  // TMEM lane quadrant, column half
     const int grp = p.Hv / p.Hk;
@@ -311,6 +309,9 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
     uint32_t ph0 = 0, ph1 = 0;  // parity of the next completion of bar0 / bar1
+    tc::grid_dep_wait();    // the chunk table comes from the metadata kernel
+    tc::grid_dep_launch();  // the chain kernel may start its prologue on free SMs
+    const int nitems = p.meta[0] * p.Hv;
 
     for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
         const int chunk = item / p.Hv, h = item - chunk * p.Hv;
@@ -802,20 +803,13 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
     using S = ChainSmem<kKDA>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    if (!p.meta[1]) return;  // malformed cu_seqlens
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x / NVB, vb = blockIdx.x % NVB, v0 = vb * BV;
-    const int b = p.order[blockIdx.y];
-    const int bos = p.cu[b], eos = p.cu[b + 1];
-    const int nc = (eos - bos + C - 1) / C;
-    const int c0 = p.offsets[b];
-    const int kh = h / (p.Hv / p.Hk);
-
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::kBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::kBar + 8 * kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::kBar + 8 * kNumBars + 8);
     auto bar = [&](int i) { return tc::smem_u32(&bars[i]); };
 
+    // prologue (touches no memory the earlier kernels write), then wait for them
     if (warp == 2) tc::tmem_alloc(tc::smem_u32(tmem_slot), 256);
     if (tid == 0) {
         for (int i = 0; i < kNumBars; ++i) tc::mbar_init(bar(i), chain_bar_count(i));
@@ -826,6 +820,19 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
+    tc::grid_dep_wait();
+    if (!p.meta[1]) {  // malformed cu_seqlens
+        tc::fence_before();
+        __syncthreads();
+        if (warp == 2) tc::tmem_dealloc(tmem, 256);
+        return;
+    }
+    const int h = blockIdx.x / NVB, vb = blockIdx.x % NVB, v0 = vb * BV;
+    const int b = p.order[blockIdx.y];
+    const int bos = p.cu[b], eos = p.cu[b + 1];
+    const int nc = (eos - bos + C - 1) / C;
+    const int c0 = p.offsets[b];
+    const int kh = h / (p.Hv / p.Hk);
     // Accumulators (fp32 TMEM columns).  The hi and lo split terms of the state
     // (or of N') sit side by side along N, so one N = 64 MMA forms two split
     // products; columns v and 32 + v are summed when read.
@@ -1142,20 +1149,28 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* w
         cudaFuncSetAttribute(chunk_chain_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smc);
         {
             KernelTimer kt("chunk_prep", stream);
-            chunk_prep_kernel<true><<<prep_grid(mc * a.Hv, 1), kPrepThreads, smp, stream>>>(p);
+            const cudaError_t e = launch_dependent(chunk_prep_kernel<true>, dim3(prep_grid(mc * a.Hv, 1)), dim3(kPrepThreads),
+                                                   (size_t)smp, stream, p);
+            if (e != cudaSuccess) return e;
         }
         KernelTimer kt("chunk_chain", stream);
-        chunk_chain_kernel<true><<<dim3(a.Hv * NVB, a.N), 512, smc, stream>>>(p);
+        const cudaError_t e = launch_dependent(chunk_chain_kernel<true>, dim3(a.Hv * NVB, a.N), dim3(512), (size_t)smc,
+                                               stream, p);
+        if (e != cudaSuccess) return e;
     } else {
         const int smp = PrepSmem<false>::kTotal, smc = ChainSmem<false>::kTotal;
         cudaFuncSetAttribute(chunk_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smp);
         cudaFuncSetAttribute(chunk_chain_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smc);
         {
             KernelTimer kt("chunk_prep", stream);
-            chunk_prep_kernel<false><<<prep_grid(mc * a.Hv, 2), kPrepThreads, smp, stream>>>(p);
+            const cudaError_t e = launch_dependent(chunk_prep_kernel<false>, dim3(prep_grid(mc * a.Hv, 2)),
+                                                   dim3(kPrepThreads), (size_t)smp, stream, p);
+            if (e != cudaSuccess) return e;
         }
         KernelTimer kt("chunk_chain", stream);
-        chunk_chain_kernel<false><<<dim3(a.Hv * NVB, a.N), 512, smc, stream>>>(p);
+        const cudaError_t e = launch_dependent(chunk_chain_kernel<false>, dim3(a.Hv * NVB, a.N), dim3(512), (size_t)smc,
+                                               stream, p);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

@@ -94,6 +94,25 @@ int set_last_error(int code, const char* fmt, ...);
 // Device error word (set by bounded device waits that give up).
 unsigned int* device_error_word();
 
+// Launch `kernel` so that it may start while the previous kernel in `stream`
+// is still running (programmatic dependent launch): the kernel must execute
+// griddepcontrol.wait before it reads anything that kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                             Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Scoped per-kernel timing (active only after gdr_profile_enable(1)): records
 // an event on `s` at construction and at destruction, so declare it right
 // before a launch inside its own block.

@@ -206,6 +206,13 @@ __device__ __forceinline__ void prefetch_l2_span(const void* src, size_t bytes) 
     if (b > a) prefetch_l2(reinterpret_cast<const void*>(a), (uint32_t)(b - a));
 }
 
+// ---- programmatic dependent launch ---------------------------------------------
+// Block until the grids this one depends on have completed and their writes are
+// visible (a no-op for a normally launched kernel).
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next kernel in the stream, if launched as a dependent, to start.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- named barriers -------------------------------------------------------------
 __device__ __forceinline__ void bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
