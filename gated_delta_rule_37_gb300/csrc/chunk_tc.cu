@@ -50,6 +50,10 @@ __device__ unsigned long long g_trace[24][64];
     do {                                                                                           \
         if (blockIdx.x == 7 && blockIdx.y == 0 && threadIdx.x == 0) g_trace[23][phase] = clock64(); \
     } while (0)
+#define GDR_TRACE_WARP(slot)                                                                                   \
+    do {                                                                                                       \
+        if (blockIdx.x == 7 && blockIdx.y == 0 && (threadIdx.x & 31) == 0) g_trace[22][(slot) * 8 + (threadIdx.x >> 5)] = clock64(); \
+    } while (0)
 __device__ unsigned long long g_items[4096][3];  // prep item: start, end (%globaltimer), SM id
 extern "C" __attribute__((visibility("default"))) int gdr_trace_dump(unsigned long long* host) {
     return (int)cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace));
@@ -75,6 +79,9 @@ extern "C" __attribute__((visibility("default"))) int gdr_trace_items(unsigned l
     } while (0)
 #define GDR_TRACE_ITEM(item, which) \
     do {                            \
+    } while (0)
+#define GDR_TRACE_WARP(slot) \
+    do {                     \
     } while (0)
 #endif
 
@@ -161,6 +168,7 @@ __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict_
         }
     }
     __syncthreads();
+    GDR_TRACE_PREP(21);
     // step 2: pair p = tid / 128; thread: row i, columns j0, j0 + 1 of a 16 x 16 block
     {
         const int p = tid >> 7, e = tid & 127, i = e >> 3, j0 = 2 * (e & 7);
@@ -186,6 +194,7 @@ __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict_
         Tm[(r1 + i) * LDA + r0 + j0 + 1] = -t1;
     }
     __syncthreads();
+    GDR_TRACE_PREP(22);
     // step 3: 2 x 2 tile per thread, rows 2 ti, 2 ti + 1 and columns 2 tj, 2 tj + 1
     {
         const int ti = tid >> 4, tj = tid & 15, i0 = 2 * ti, j0 = 2 * tj;
@@ -204,6 +213,7 @@ __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict_
         Z[(i0 + 1) * 32 + j0] = y10;
         Z[(i0 + 1) * 32 + j0 + 1] = y11;
         __syncthreads();
+        GDR_TRACE_PREP(23);
         float t00 = 0.f, t01 = 0.f, t10 = 0.f, t11 = 0.f;
 #pragma unroll 8
         for (int m = 0; m < 32; ++m) {
@@ -449,25 +459,42 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
             if (!tc::mbar_wait(bar0, ph0, abort_flag)) raise_error(p, 1u);
             ph0 ^= 1u;
             tc::fence_after();
+            GDR_TRACE_PREP(24);
+            GDR_TRACE_WARP(0);
             // thread: accumulator row r = 32 q + lane (rows < 64: K K^T, >= 64: Q K^T),
             // columns [32 hf, 32 hf + 32)
             const int r = 32 * q + lane, i = r & 63;
-            float gv[32];
-            tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * hf, gv);
+            // all shared-memory reads first (gam, beta), then the arithmetic, then
+            // the stores: As may alias gam as far as the compiler knows, and an
+            // interleaved load / store order would serialise the 32 elements
+            float gj[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; jj += 4) {
+                const float4 g4 = *reinterpret_cast<const float4*>(gam + 32 * hf + jj);
+                gj[jj] = g4.x; gj[jj + 1] = g4.y; gj[jj + 2] = g4.z; gj[jj + 3] = g4.w;
+            }
             const float gi = gam[i], bi = bet[i];
+            float gv[32];
+            GDR_TRACE_WARP(3);
+            tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * hf, gv);
+            GDR_TRACE_WARP(4);
             if (r < C) {
+                const float sc = i < L ? bi : 0.f;
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) {
                     const int j = 32 * hf + jj;
-                    As[i * LDA + j] = (j < i && i < L) ? bi * __expf(gi - gam[j]) * gv[jj] : 0.f;
+                    gv[jj] = j < i ? sc * __expf(gi - gj[jj]) * gv[jj] : 0.f;
                 }
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) As[i * LDA + 32 * hf + jj] = gv[jj];
             } else {
                 uint32_t pk[16];
+                const float sc = i < L ? 1.f : 0.f;
 #pragma unroll
                 for (int jj = 0; jj < 32; jj += 2) {
                     const int j = 32 * hf + jj;
-                    const float p0 = (j <= i && i < L) ? __expf(gi - gam[j]) * gv[jj] : 0.f;
-                    const float p1 = (j + 1 <= i && i < L) ? __expf(gi - gam[j + 1]) * gv[jj + 1] : 0.f;
+                    const float p0 = j <= i ? sc * __expf(gi - gj[jj]) * gv[jj] : 0.f;
+                    const float p1 = j + 1 <= i ? sc * __expf(gi - gj[jj + 1]) * gv[jj + 1] : 0.f;
                     pk[jj >> 1] = tc::pack_bf16(p0, p1);
                 }
 #pragma unroll
@@ -475,6 +502,7 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
                     *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(C + i, 4 * hf + cc, 2 * C)) =
                         make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
             }
+            GDR_TRACE_WARP(1);
         } else {
             // Per-channel decays: A_ij = beta_i sum_c k_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}
             // and P_ij = sum_c q_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}.  Pairs in different
@@ -660,6 +688,7 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
         tc::fence_before();
         __syncthreads();
         GDR_TRACE_PREP(3);
+        GDR_TRACE_WARP(2);
 
         // ---- Tm = (I + A)^{-1} -----------------------------------------------------------
         solve_unit_lower(As, Tm, Z, tid);
@@ -716,7 +745,10 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
         GDR_TRACE_PREP(6);
 
         // ---- W, U out of TMEM into their blobs: 8 warps, row i = 16 q + lane (lane <
-        //      16), columns [64 hf, 64 hf + 64) of W and of U -------------------------------
+        //      16), columns [64 hf, 64 hf + 64) of W and of U.  The images are staged in
+        //      shared memory left dead by the finished MMAs (W hi / lo as 64-row k128
+        //      tiles over X, U value-major over V and A) and written with bulk copies,
+        //      so every global write is a contiguous run. ---------------------------------
         // the item's last completion of bar0 (the scalar gate's K K^T / Q K^T group was the first)
         if (!tc::mbar_wait(bar0, ph0, abort_flag)) raise_error(p, 1u);
         ph0 ^= 1u;
@@ -724,9 +756,9 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
         {
             const int i = 16 * q + (lane & 15);
             const uint32_t lrow = tmem + ((uint32_t)(32 * q) << 16);
-            unsigned char* Whi = p.Xw + ((size_t)chunk * p.Hv + h) * kXwBytes;  // rows 0..63
-            unsigned char* Wlo = p.Yw + ((size_t)chunk * p.Hv + h) * kYwBytes;  // rows 0..63
-            float* Udst = reinterpret_cast<float*>(p.Ub + ((size_t)chunk * p.Hv + h) * NVB * kUBlock);
+            unsigned char* sWh = sm + S::kX;            // [64][128] k128, column-block stride 8 KB
+            unsigned char* sWl = sm + S::kX + kTile64x128;
+            float* sU = reinterpret_cast<float*>(sm + S::kV);  // 4 x [32 v][64 i]
             for (int q2 = 0; q2 < 2; ++q2) {
                 const int cb = 2 * hf + q2;  // 32-column block of W and of U
                 float wv[32], uv[32];
@@ -738,16 +770,30 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
                         uint32_t hw[4], lw[4];
 #pragma unroll
                         for (int u = 0; u < 4; ++u) tc::split2(wv[8 * cc + 2 * u], wv[8 * cc + 2 * u + 1], hw[u], lw[u]);
-                        const uint32_t off = tc::chunk_k128(i, 4 * cb + cc, 2 * C);
-                        *reinterpret_cast<uint4*>(Whi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                        *reinterpret_cast<uint4*>(Wlo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                        const uint32_t off = tc::chunk_k128(i, 4 * cb + cc, C);
+                        *reinterpret_cast<uint4*>(sWh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4*>(sWl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                     }
-                    // U block cb stored value-major [32 v][64 i]: the chain's thread for
-                    // row i then reads a conflict-free column of shared memory
-                    float* ublk = Udst + (size_t)cb * (C * BV) + i;
+                    // U block cb value-major [32 v][64 i]: the chain's thread for row i
+                    // then reads a conflict-free column of shared memory
+                    float* ublk = sU + cb * (C * BV) + i;
 #pragma unroll
-                    for (int v = 0; v < BV; ++v) ublk[(size_t)v * C] = uv[v];
+                    for (int v = 0; v < BV; ++v) ublk[v * C] = uv[v];
                 }
+            }
+            tc::fence_proxy_async();
+            __syncthreads();
+            if (tid == 0) {
+                unsigned char* Xd = p.Xw + ((size_t)chunk * p.Hv + h) * kXwBytes;  // rows 0..63 of each column block
+                unsigned char* Yd = p.Yw + ((size_t)chunk * p.Hv + h) * kYwBytes;
+                const uint32_t half = kTile64x128 / 2;  // one 64-row column block
+                tc::bulk_s2g(Xd, tc::smem_u32(sWh), half);
+                tc::bulk_s2g(Xd + 2 * half, tc::smem_u32(sWh) + half, half);
+                tc::bulk_s2g(Yd, tc::smem_u32(sWl), half);
+                tc::bulk_s2g(Yd + 2 * half, tc::smem_u32(sWl) + half, half);
+                tc::bulk_s2g(p.Ub + ((size_t)chunk * p.Hv + h) * NVB * kUBlock, tc::smem_u32(sU), NVB * kUBlock);
+                tc::bulk_commit();
+                tc::bulk_wait_read();  // the staging area is reused by the next item
             }
         }
         GDR_TRACE_PREP(7);
@@ -757,6 +803,7 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
         GDR_TRACE_PREP(8);
         GDR_TRACE_ITEM(item, 1);
     }  // item loop
+    if (tid == 0) tc::bulk_wait_all();
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
 
