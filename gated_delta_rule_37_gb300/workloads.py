@@ -124,7 +124,10 @@ class PoolCase:
 def pool_case(seed: int, lens, Hk: int, Hv: int, K: int, V: int, num_slots: int, *,
               dtype=torch.bfloat16, pool_dtype=torch.float32, g_range=(-1.0, 0.0),
               pad_count: int = 0, commit: bool = True, steps: int = 0, ibuf_rows: int = 0,
-              pool_std: float = 0.1, scale: float | None = None, name: str = "pool") -> PoolCase:
+              pool_std: float = 0.1, scale: float | None = None, channel_gate: bool = False,
+              name: str = "pool") -> PoolCase:
+    """``channel_gate``: g is a per-key-channel log-decay [T, Hv, K] instead of
+    the scalar [T, Hv]."""
     gen = _gen(seed)
     lens = [int(x) for x in lens]
     N = len(lens)
@@ -135,7 +138,7 @@ def pool_case(seed: int, lens, Hk: int, Hv: int, K: int, V: int, num_slots: int,
     k = _unit_rows(torch.randn(T, Hk, K, generator=gen)).to(dtype)
     v = torch.randn(T, Hv, V, generator=gen).to(dtype)
     beta = torch.sigmoid(torch.randn(T, Hv, generator=gen)).to(dtype)
-    g = _uniform(gen, (T, Hv), *g_range)
+    g = _uniform(gen, (T, Hv, K) if channel_gate else (T, Hv), *g_range)
     pool = (torch.randn(num_slots, Hv, V, K, generator=gen) * pool_std).to(pool_dtype)
     idx = torch.randperm(num_slots, generator=gen)[:N].to(torch.int32)
     if pad_count:

@@ -61,7 +61,7 @@ def _load():
         lib.oracle_tokenwise.restype = I
         lib.oracle_chunked.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, D, I, P, P, I]
         lib.oracle_chunked.restype = I
-        lib.oracle_pool.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, D, I, P, P, I, I]
+        lib.oracle_pool.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, D, I, P, P, I, I]
         lib.oracle_pool.restype = I
         lib.oracle_gating.argtypes = [P, P, P, P, ctypes.c_int64, I, I, P, P]
         lib.oracle_gating.restype = None
@@ -139,10 +139,14 @@ def chunked(q, k, v, beta, cu_seqlens, *, g=None, gk=None, initial_state=None, s
 
 def pool(q, k, v, g, beta, pool_state, state_indices, cu_seqlens, *, scale, commit: bool,
          steps: int = 0, ibuf_rows: int = 0, o_init=None, ibuf_init=None, nthreads: int = 0):
-    """Slot-indexed decode / verify.  Returns (o, pool_out, ibuf) in fp64, where
-    rows that the method leaves untouched keep ``o_init`` / ``ibuf_init`` (NaN
-    when not given) and the input pool content."""
+    """Slot-indexed decode / verify.  ``g`` is the scalar log-decay [T, Hv] or
+    the per-key-channel one [T, Hv, K].  Returns (o, pool_out, ibuf) in fp64,
+    where rows that the method leaves untouched keep ``o_init`` / ``ibuf_init``
+    (NaN when not given) and the input pool content."""
     q, k, v, g, beta = _f64(q), _f64(k), _f64(v), _f64(g), _f64(beta)
+    gk = g if g.ndim == 3 else None
+    if gk is not None:
+        g = np.zeros(g.shape[:2])
     pin = _f64(pool_state)
     pout = pin.copy()
     idx = state_indices
@@ -159,7 +163,7 @@ def pool(q, k, v, g, beta, pool_state, state_indices, cu_seqlens, *, scale, comm
     if steps > 0:
         ib = (np.full((ibuf_rows, steps, Hv, V, K), np.nan) if ibuf_init is None
               else _f64(ibuf_init).copy())
-    rc = _load().oracle_pool(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(pin), _ptr(pout),
+    rc = _load().oracle_pool(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(gk), _ptr(beta), _ptr(pin), _ptr(pout),
                              _ptr(idx), _ptr(cu), N, num_slots, Hk, Hv, K, V, float(scale),
                              int(bool(commit)), _ptr(o), _ptr(ib), int(steps), int(nthreads))
     if rc != 0:

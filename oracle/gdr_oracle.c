@@ -270,7 +270,12 @@ int oracle_chunked(const double* q, const double* k, const double* v, const doub
 }
 
 /*
- * Slot-indexed decode / multi-step verify over a state pool (scalar gate).
+ * Slot-indexed decode / multi-step verify over a state pool.
+ *   g        [T, Hv] scalar log-decay, used when gk is NULL
+ *   gk       [T, Hv, K] per-key-channel log-decay, or NULL (the per-channel
+ *            decode of tokenspeed PR #834: column c of the state is scaled
+ *            by e^{gk[c]} before the delta-rule update, as in the tokenwise
+ *            definition above)
  *   pool_in  [num_slots, Hv, V, K]   fp64 copy of the pool as the GPU sees it
  *   pool_out same shape; on entry a copy of pool_in; slot state_idx[b] is
  *            overwritten with the final state when commit != 0
@@ -282,7 +287,7 @@ int oracle_chunked(const double* q, const double* k, const double* v, const doub
  * Returns 0, or -1 on a malformed argument (e.g. L_b > steps with ibuf).
  */
 int oracle_pool(const double* q, const double* k, const double* v, const double* g,
-                const double* beta, const double* pool_in, double* pool_out,
+                const double* gk, const double* beta, const double* pool_in, double* pool_out,
                 const int32_t* state_idx, const int64_t* cu, int N, int num_slots, int Hk,
                 int Hv, int K, int V, double scale, int commit, double* o, double* ibuf,
                 int steps, int nthreads) {
@@ -303,8 +308,12 @@ int oracle_pool(const double* q, const double* k, const double* v, const double*
         double* dec = (double*)malloc(sizeof(double) * (size_t)K);
         load_state(S, pool_in + ((size_t)slot * Hv + h) * V * K, K, V, 0);
         for (int64_t t = cu[b]; t < cu[b + 1]; ++t) {
-            const double a = exp(g[(size_t)t * Hv + h]);
-            for (int c = 0; c < K; ++c) dec[c] = a;
+            if (gk) {  /* per-key-channel decay: column c of S scaled by e^{gk[c]} */
+                for (int c = 0; c < K; ++c) dec[c] = exp(gk[((size_t)t * Hv + h) * K + c]);
+            } else {
+                const double a = exp(g[(size_t)t * Hv + h]);
+                for (int c = 0; c < K; ++c) dec[c] = a;
+            }
             token_step(S, dec, q + ((size_t)t * Hk + kh) * K, k + ((size_t)t * Hk + kh) * K,
                        v + ((size_t)t * Hv + h) * V, beta[(size_t)t * Hv + h], scale, K, V, 0,
                        o + ((size_t)t * Hv + h) * V);

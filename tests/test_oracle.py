@@ -277,6 +277,50 @@ def test_pool_decode_and_verify_match_tokenwise():
         assert np.array_equal(pout[s], pin[s])
 
 
+def test_pool_channel_gate_matches_tokenwise():
+    """Per-key-channel gates in decode / verify: each per-token state and the
+    committed state are the tokenwise recurrence (with gk) from the gathered
+    slot; the padding row stays untouched."""
+    case = workloads.pool_case(23, [2, 3, 1], 1, 2, 6, 5, num_slots=5, pool_dtype=torch.float32,
+                               pad_count=1, commit=True, steps=3, ibuf_rows=3, channel_gate=True,
+                               g_range=(-1.5, 0.0))
+    assert case.g.shape == (case.T, 2, 6)
+    o, pout, ib = oracle.pool(case.q, case.k, case.v, case.g, case.beta, case.pool, case.state_indices,
+                              case.cu_seqlens, scale=case.scale, commit=True, steps=3, ibuf_rows=3)
+    pin = case.pool.double().numpy()
+    cu = case.cu_seqlens.numpy()
+    for b in range(case.N):
+        slot = int(case.state_indices[b])
+        sl = slice(cu[b], cu[b + 1])
+        if slot < 0:
+            assert np.isnan(o[sl]).all() and np.isnan(ib[b]).all()
+            continue
+        L = cu[b + 1] - cu[b]
+        for t in range(1, L + 1):
+            ot, st = oracle.tokenwise(q=case.q[cu[b]:cu[b] + t], k=case.k[cu[b]:cu[b] + t],
+                                      v=case.v[cu[b]:cu[b] + t], gk=case.g[cu[b]:cu[b] + t],
+                                      beta=case.beta[cu[b]:cu[b] + t], initial_state=pin[slot:slot + 1],
+                                      cu_seqlens=[0, t], scale=case.scale)
+            np.testing.assert_allclose(ib[b, t - 1], st[0], rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(o[sl], ot, rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(pout[slot], st[0], rtol=1e-13, atol=1e-15)
+
+
+def test_pool_channel_constant_gate_equals_scalar_gate():
+    """A per-channel gate that is the same on every key channel is the scalar gate."""
+    case = workloads.pool_case(24, [3, 2], 2, 4, 8, 4, num_slots=4, pool_dtype=torch.float32,
+                               commit=True, steps=3, ibuf_rows=2)
+    gk = case.g[:, :, None].expand(-1, -1, 8).contiguous()
+    kw = dict(scale=case.scale, commit=True, steps=3, ibuf_rows=2)
+    o1, p1, i1 = oracle.pool(case.q, case.k, case.v, case.g, case.beta, case.pool, case.state_indices,
+                             case.cu_seqlens, **kw)
+    o2, p2, i2 = oracle.pool(case.q, case.k, case.v, gk, case.beta, case.pool, case.state_indices,
+                             case.cu_seqlens, **kw)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(p1, p2)
+    np.testing.assert_array_equal(i1, i2)
+
+
 def test_pool_no_commit_leaves_pool():
     case = workloads.pool_case(22, [2, 2], 1, 2, 4, 4, num_slots=3, pool_dtype=torch.float32,
                                commit=False, steps=2, ibuf_rows=2)
