@@ -7,9 +7,9 @@ K = V = 128, g ~ U[-2, 0], fp32 initial state.  `value` is prefill tokens/s with
 inputs resident in HBM; the L2 (129 MB) is flushed before every timed step by
 writing a 256 MB buffer outside the step's events.  The same line carries the
 recurrent decode (256 sequences, fp32 pool, commit), the multi-step verify
-(64 sequences, 1..12 tokens, bf16 pool + per-token states) and the long KDA
-prefill (T = 32768, Hv = 32, per-channel gate) as extra objects, each with its
-own roofline.
+(64 sequences, 1..12 tokens, bf16 pool + per-token states), the decode with
+per-key-channel gates and the long KDA prefill (T = 32768, Hv = 32,
+per-channel gate) as extra objects, each with its own roofline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -82,8 +82,9 @@ def pool_bytes(case):
         n += len(valid) * slab
     if case.steps:
         n += toks * slab
+    gate_per_tok = case.g[0].numel() * 4  # [Hv] or, per key channel, [Hv, K] fp32
     per_tok = 2 * case.q.shape[1] * K * case.q.element_size() + 2 * Hv * V * case.v.element_size() \
-        + Hv * 4 + Hv * case.beta.element_size()
+        + gate_per_tok + Hv * case.beta.element_size()
     return n + toks * per_tok, toks
 
 
@@ -441,7 +442,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default="", help="comma list of sections: prefill,decode,verify,kda")
+    ap.add_argument("--only", default="", help="comma list of sections: prefill,decode,verify,kda,kda_decode")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -462,7 +463,7 @@ def main():
     stream = torch.cuda.Stream()
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush = lambda: flush_buf.fill_(1)
-    only = set(filter(None, args.only.split(","))) or {"prefill", "decode", "verify", "kda"}
+    only = set(filter(None, args.only.split(","))) or {"prefill", "decode", "verify", "kda", "kda_decode"}
 
     dist_ = Dist(world, dev)
 
@@ -475,9 +476,11 @@ def main():
     pre_case = workloads.varlen_bf16_prefill()
     pre = Prefill(pre_case, dev)
     extra = {}
-    dec = ver = kda = None
+    dec = ver = kda = kdec = None
     if "decode" in only:
         dec = PoolRun(workloads.decode_fp32_pool(), dev)
+    if "kda_decode" in only:
+        kdec = PoolRun(workloads.decode_kda_fp32_pool(), dev)
     if "verify" in only:
         ver = PoolRun(workloads.verify_bf16_pool(), dev)
     if "kda" in only:
@@ -521,6 +524,14 @@ def main():
         v_ms = max_over_ranks(v_ms)
         extra["verify"] = {"workload": ver.case.name, "tokens_per_s": round(world * toks / (v_ms / 1e3), 1),
                            "ms_per_step": round(v_ms, 4), "valid_tokens": toks, "roofline": v_roof}
+    if kdec is not None:
+        nbytes, toks = pool_bytes(kdec.case)
+        kd_ms, kd_prof, kd_roof, _ = measure(kdec, max(args.steps, 20), args.warmup, flush, stream,
+                                             lambda n: nbytes, lambda n: "hbm", peaks, toks)
+        launches += sum(v[1] for v in kd_prof.values())
+        kd_ms = max_over_ranks(kd_ms)
+        extra["kda_decode"] = {"workload": kdec.case.name, "tokens_per_s": round(world * toks / (kd_ms / 1e3), 1),
+                               "ms_per_step": round(kd_ms, 4), "valid_tokens": toks, "roofline": kd_roof}
     if kda is not None:
         k_ms, k_prof, k_roof, _ = measure(kda, max(3, args.steps // 10), args.warmup, flush, stream,
                                           prefill_work_fn(kda.case), lambda n: "tensor", peaks, kda.case.T)

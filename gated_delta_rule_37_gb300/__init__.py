@@ -23,7 +23,7 @@ LIB_PATH = os.path.join(_PKG, "libgdr.so")
 
 GDR_BF16, GDR_F32 = 0, 1
 GDR_GATE_SCALAR, GDR_GATE_CHANNEL = 0, 1
-GDR_QK_L2NORM, GDR_NEG_EIGVAL, GDR_COMMIT, GDR_VALIDATE = 0x1, 0x2, 0x4, 0x8
+GDR_QK_L2NORM, GDR_NEG_EIGVAL, GDR_COMMIT, GDR_VALIDATE, GDR_CHANNEL_GATE = 0x1, 0x2, 0x4, 0x8, 0x10
 CHUNK = 64
 
 STATUS = {0: "GDR_OK", 1: "GDR_ERR_INVALID_ARG", 2: "GDR_ERR_UNSUPPORTED", 3: "GDR_ERR_WORKSPACE",
@@ -166,12 +166,17 @@ def chunk_fwd_noalloc(q, k, v, beta, cu_seqlens, *, g=None, gk=None, initial_sta
 
 def recurrent_fwd(q, k, v, g, beta, state_pool, state_indices, cu_seqlens, *, scale=None,
                   flags: int = GDR_COMMIT, o=None, intermediate_states=None, stream=None):
-    """Slot-indexed decode / verify.  The pool is updated in place only with
-    GDR_COMMIT; ``intermediate_states`` [rows, steps, Hv, V, K] (pool dtype)
-    receives per-token states.  Returns o."""
+    """Slot-indexed decode / verify.  ``g`` is the scalar log-decay [T, Hv] or
+    the per-key-channel one [T, Hv, K] (sets GDR_CHANNEL_GATE).  The pool is
+    updated in place only with GDR_COMMIT; ``intermediate_states`` [rows, steps,
+    Hv, V, K] (pool dtype) receives per-token states.  Returns o."""
     T, Hk, K = q.shape
     Hv, V = v.shape[1], v.shape[2]
     N = cu_seqlens.numel() - 1
+    if g.dim() == 3:
+        if tuple(g.shape) != (T, Hv, K):
+            raise ValueError("a per-channel gate must be [T, Hv, K]")
+        flags |= GDR_CHANNEL_GATE
     if scale is None:
         scale = K ** -0.5
     if o is None:

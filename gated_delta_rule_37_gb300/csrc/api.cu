@@ -218,7 +218,7 @@ int gdr_recurrent_fwd(const void* q, const void* k, const void* v, const float* 
     if (int rc = check_common(N, T_total, Hk, Hv, K, V, dtype)) return rc;
     if (pool_dtype != GDR_BF16 && pool_dtype != GDR_F32)
         return fail(GDR_ERR_UNSUPPORTED, "pool_dtype %d", pool_dtype);
-    if (flags & ~(GDR_QK_L2NORM | GDR_COMMIT | GDR_VALIDATE))
+    if (flags & ~(GDR_QK_L2NORM | GDR_COMMIT | GDR_VALIDATE | GDR_CHANNEL_GATE))
         return fail(GDR_ERR_INVALID_ARG, "unsupported flags 0x%x for gdr_recurrent_fwd", flags);
     if (N == 0) return ok();
     if (num_slots <= 0) return fail(GDR_ERR_INVALID_ARG, "num_slots must be positive");
@@ -235,7 +235,8 @@ int gdr_recurrent_fwd(const void* q, const void* k, const void* v, const float* 
     if (int rc = check_device()) return rc;
     cudaStream_t s = (cudaStream_t)stream;
     if (flags & GDR_VALIDATE) {
-        if (int rc = run_validation(s, cu_seqlens, N, T_total, true, g, T_total * Hv, state_indices,
+        const int64_t gate_n = T_total * Hv * ((flags & GDR_CHANNEL_GATE) ? K : 1);
+        if (int rc = run_validation(s, cu_seqlens, N, T_total, true, g, gate_n, state_indices,
                                     num_slots, intermediate_states ? steps : 0))
             return rc;
     }

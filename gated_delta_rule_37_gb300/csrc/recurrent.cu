@@ -38,7 +38,7 @@ struct RecParams {
     float scale;
 };
 
-template <typename InT, typename PoolT, int K, int BV>
+template <typename InT, typename PoolT, int K, int BV, bool kChan>
 __global__ void __launch_bounds__(BV / kRowsPerWarp * 32)
 recurrent_kernel(RecParams p) {
     constexpr int KPT = K / 32;  // key channels per lane
@@ -68,21 +68,23 @@ recurrent_kernel(RecParams p) {
 
     // Per-token inputs of token t + 1 are loaded while token t is processed, so
     // their global-load latency is hidden behind the reductions of the current token.
-    float kn[KPT], qn[KPT], gn = 0.f, bn = 0.f, vn = 0.f;
+    constexpr bool chan = kChan;  // GDR_CHANNEL_GATE: g is [T, Hv, K]
+    float kn[KPT], qn[KPT], gcn[KPT], gn = 0.f, bn = 0.f, vn = 0.f;
     auto load_token = [&](int t) {
         Vec<InT, KPT>::load(kp + ((size_t)t * p.Hk + kh) * K + lane * KPT, kn);
         Vec<InT, KPT>::load(qp + ((size_t)t * p.Hk + kh) * K + lane * KPT, qn);
-        gn = p.g[(size_t)t * p.Hv + h];
+        if (chan) Vec<float, KPT>::load(p.g + ((size_t)t * p.Hv + h) * K + lane * KPT, gcn);
+        else gn = p.g[(size_t)t * p.Hv + h];
         bn = to_f(bp[(size_t)t * p.Hv + h]);
         vn = to_f(vp[((size_t)t * p.Hv + h) * V + v0 + (lane & 15)]);
     };
     if (bos < eos) load_token(bos);
 #pragma unroll 1
     for (int t = bos; t < eos; ++t) {
-        float kk[KPT], qq[KPT];
+        float kk[KPT], qq[KPT], ac[KPT];
 #pragma unroll
-        for (int c = 0; c < KPT; ++c) { kk[c] = kn[c]; qq[c] = qn[c]; }
-        const float a = __expf(gn);
+        for (int c = 0; c < KPT; ++c) { kk[c] = kn[c]; qq[c] = qn[c]; ac[c] = chan ? __expf(gcn[c]) : 1.f; }
+        const float a = chan ? 1.f : __expf(gn);
         const float bt = bn;
         const float vv = vn;
         if (t + 1 < eos) load_token(t + 1);
@@ -95,12 +97,21 @@ recurrent_kernel(RecParams p) {
             for (int c = 0; c < KPT; ++c) { kk[c] *= ik; qq[c] *= iq; }
         }
 
+        // decayed products: scalar gate S~ = a S (a applied after the reduction);
+        // channel gate S~ = S diag(ac), i.e. S~ k = S (ac o k), S~ q = S (ac o q)
+        float ka[KPT], qa[KPT], da[KPT];
+#pragma unroll
+        for (int c = 0; c < KPT; ++c) {
+            ka[c] = chan ? kk[c] * ac[c] : kk[c];
+            qa[c] = chan ? qq[c] * ac[c] : qq[c];
+            da[c] = chan ? ac[c] : a;
+        }
         float x[32];
 #pragma unroll
         for (int r = 0; r < kRowsPerWarp; ++r) {
             float dk = 0.f, dq = 0.f;
 #pragma unroll
-            for (int c = 0; c < KPT; ++c) { dk += s[r][c] * kk[c]; dq += s[r][c] * qq[c]; }
+            for (int c = 0; c < KPT; ++c) { dk += s[r][c] * ka[c]; dq += s[r][c] * qa[c]; }
             x[r] = dk;
             x[r + kRowsPerWarp] = dq;
         }
@@ -108,7 +119,8 @@ recurrent_kernel(RecParams p) {
 #pragma unroll
         for (int c = 0; c < KPT; ++c) kq += kk[c] * qq[c];
         kq = warp_sum(kq);
-        // lane r < 16 now holds (S k)_r, lane 16 + r holds (S q)_r (pre-decay)
+        // lane r < 16 now holds (S k)_r, lane 16 + r holds (S q)_r (before the
+        // scalar decay a; channel decays are already inside)
         const float red = reduce32_to_lane(x, lane);
         const float n_mine = bt * (vv - a * red);  // valid on lanes < 16
         const float n_row = __shfl_sync(0xffffffffu, n_mine, lane & 15);
@@ -120,7 +132,7 @@ recurrent_kernel(RecParams p) {
         for (int r = 0; r < kRowsPerWarp; ++r) {
             const float nr = __shfl_sync(0xffffffffu, n_mine, r);
 #pragma unroll
-            for (int c = 0; c < KPT; ++c) s[r][c] = fmaf(a, s[r][c], nr * kk[c]);
+            for (int c = 0; c < KPT; ++c) s[r][c] = fmaf(da[c], s[r][c], nr * kk[c]);
         }
         if (p.ibuf && t - bos < p.steps) {
             PoolT* irow = static_cast<PoolT*>(p.ibuf) +
@@ -135,7 +147,7 @@ recurrent_kernel(RecParams p) {
     }
 }
 
-template <typename InT, typename PoolT, int K>
+template <typename InT, typename PoolT, int K, bool kChan>
 cudaError_t launch_k(const RecParams& p, int N, int V, cudaStream_t stream) {
     // V-column split: 64-row blocks (128 threads) measured best on GB300 for
     // both single-token decode (6.50 vs 6.42 TB/s at 128 rows) and 12-token
@@ -150,13 +162,13 @@ cudaError_t launch_k(const RecParams& p, int N, int V, cudaStream_t stream) {
     KernelTimer kt("recurrent", stream);
     switch (bv) {
         case 128:
-            recurrent_kernel<InT, PoolT, K, 128><<<grid, 256, 0, stream>>>(p);
+            recurrent_kernel<InT, PoolT, K, 128, kChan><<<grid, 256, 0, stream>>>(p);
             break;
         case 64:
-            recurrent_kernel<InT, PoolT, K, 64><<<grid, 128, 0, stream>>>(p);
+            recurrent_kernel<InT, PoolT, K, 64, kChan><<<grid, 128, 0, stream>>>(p);
             break;
         default:
-            recurrent_kernel<InT, PoolT, K, 32><<<grid, 64, 0, stream>>>(p);
+            recurrent_kernel<InT, PoolT, K, 32, kChan><<<grid, 64, 0, stream>>>(p);
             break;
     }
     return cudaGetLastError();
@@ -164,8 +176,9 @@ cudaError_t launch_k(const RecParams& p, int N, int V, cudaStream_t stream) {
 
 template <typename InT, typename PoolT>
 cudaError_t launch_kt(const RecParams& p, int N, int K, int V, cudaStream_t stream) {
-    if (K == 128) return launch_k<InT, PoolT, 128>(p, N, V, stream);
-    return launch_k<InT, PoolT, 64>(p, N, V, stream);
+    const bool chan = p.flags & 0x10;  // GDR_CHANNEL_GATE
+    if (K == 128) return chan ? launch_k<InT, PoolT, 128, true>(p, N, V, stream) : launch_k<InT, PoolT, 128, false>(p, N, V, stream);
+    return chan ? launch_k<InT, PoolT, 64, true>(p, N, V, stream) : launch_k<InT, PoolT, 64, false>(p, N, V, stream);
 }
 
 }  // namespace

@@ -183,6 +183,15 @@ def decode_fp32_pool() -> PoolCase:
                      name="decode_B256_Hk16_Hv32_D128_fp32pool")
 
 
+def decode_kda_fp32_pool() -> PoolCase:
+    """The decode workload with per-key-channel gates: 256 single-token
+    sequences, Hk=16, Hv=32, K=V=128, gk ~ U[-1,0] [T, Hv, K], fp32 pool of 513
+    slots, 26 padding indices, committed in place."""
+    return pool_case(5, [1] * 256, 16, 32, 128, 128, 513, pool_dtype=torch.float32,
+                     g_range=(-1.0, 0.0), pad_count=26, commit=True, channel_gate=True,
+                     name="decode_kda_B256_Hk16_Hv32_D128_fp32pool")
+
+
 def verify_bf16_pool(pad_count: int = 0) -> PoolCase:
     """64 sequences with accepted lengths U{1..12}, bf16 pool of 65 slots,
     per-token states into a [65, 12, Hv, V, K] bf16 buffer, no commit."""

@@ -74,6 +74,7 @@ typedef enum gdr_gate_kind {
 #define GDR_NEG_EIGVAL 0x2 /* gdr_gating_fwd: beta = 2 * sigmoid(b)                         */
 #define GDR_COMMIT     0x4 /* gdr_recurrent_fwd: write the final state back to the pool     */
 #define GDR_VALIDATE   0x8 /* check input contents on the device first (synchronises)       */
+#define GDR_CHANNEL_GATE 0x10 /* gdr_recurrent_fwd: g is per key channel, [T_total, Hv, K]  */
 
 /* Chunk length of the chunked prefill (tokens).  The pages' kernels use 64. */
 #define GDR_CHUNK 64
@@ -151,7 +152,10 @@ GDR_API int gdr_chunk_fwd_noalloc(const void* q, const void* k, const void* v, c
  * (FlashQLA PR #1, paged verify commit and deployment-facts commit).
  *
  *   q, k           [T_total, Hk, K] dtype;   v [T_total, Hv, V] dtype
- *   g              [T_total, Hv] fp32 raw log-decay;  beta [T_total, Hv] dtype
+ *   g              [T_total, Hv] fp32 raw log-decay, or with GDR_CHANNEL_GATE
+ *                  [T_total, Hv, K] fp32 per-key-channel log-decay (column c
+ *                  of the state scaled by e^{g[t,h,c]}: the per-channel decode
+ *                  of tokenspeed PR #834);  beta [T_total, Hv] dtype
  *   state_pool     [num_slots, Hv, V, K] (V-major), pool_dtype GDR_F32 or
  *                  GDR_BF16; read, and written in place only with GDR_COMMIT
  *   state_indices  [N] int32 device: pool slot of sequence b; -1 (any value

@@ -96,6 +96,44 @@ def test_verify_with_padding_rows():
     check_case(case, pool, o, ib, o_init, commit=False)
 
 
+def test_channel_gate_decode_full_size():
+    """Per-key-channel gates (tokenspeed PR #834's KDA decode): the decode
+    workload with gk [T, Hv, K], fp32 pool committed in place."""
+    case = workloads.decode_kda_fp32_pool()
+    pool, o, ib, o_init = run_case(case, flags=gdr.GDR_COMMIT, with_ibuf=False)
+    check_case(case, pool, o, ib, o_init, commit=True)
+
+
+@pytest.mark.parametrize("K", [64, 128])
+@pytest.mark.parametrize("dtype,pool_dtype", [(torch.bfloat16, torch.float32), (torch.float32, torch.float32),
+                                              (torch.bfloat16, torch.bfloat16)])
+def test_channel_gate_small_cases(K, dtype, pool_dtype):
+    """Ragged verify with per-channel gates, GVA 2, padding row, per-token
+    states and commit."""
+    lens = [1, 7, 0, 12, 4]
+    case = workloads.pool_case(41 + K, lens, 2, 4, K, K, 7, dtype=dtype, pool_dtype=pool_dtype, pad_count=1,
+                               commit=True, steps=12, ibuf_rows=6, g_range=(-2.0, 0.0), channel_gate=True)
+    pool, o, ib, o_init = run_case(case, flags=gdr.GDR_COMMIT, with_ibuf=True)
+    check_case(case, pool, o, ib, o_init, commit=True)
+
+
+def test_channel_gate_constant_matches_scalar_gate():
+    """A per-channel gate equal on every key channel gives the scalar-gate
+    result (up to rounding order)."""
+    case = workloads.pool_case(45, [3, 5, 1], 2, 4, 128, 128, 5, pool_dtype=torch.float32, commit=True,
+                               steps=5, ibuf_rows=3)
+    pool_a, o_a, ib_a, _ = run_case(case, flags=gdr.GDR_COMMIT, with_ibuf=True)
+    import dataclasses
+    chan = dataclasses.replace(case, g=case.g[:, :, None].expand(-1, -1, 128).contiguous())
+    pool_b, o_b, ib_b, _ = run_case(chan, flags=gdr.GDR_COMMIT, with_ibuf=True)
+    check_out(o_b.view.cpu(), o_a.view.cpu().double().numpy(), "o")
+    check_state(pool_b.view.cpu(), pool_a.view.cpu().double().numpy(), "pool")
+    cu = case.cu_seqlens.tolist()
+    for b in range(case.N):
+        L = cu[b + 1] - cu[b]
+        check_state(ib_b.view[b, :L].cpu(), ib_a.view[b, :L].cpu().double().numpy(), f"ibuf row {b}")
+
+
 @pytest.mark.parametrize("Hk,Hv", [(4, 4), (2, 8), (1, 4)])       # MHA, GVA 4, MQA
 @pytest.mark.parametrize("K", [64, 128])
 @pytest.mark.parametrize("dtype,pool_dtype", [(torch.bfloat16, torch.float32), (torch.float32, torch.float32),
