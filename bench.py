@@ -7,7 +7,8 @@ K = V = 128, g ~ U[-2, 0], fp32 initial state.  `value` is prefill tokens/s with
 inputs resident in HBM; the L2 (129 MB) is flushed before every timed step by
 writing a 256 MB buffer outside the step's events.  The same line carries the
 recurrent decode (256 sequences, fp32 pool, commit), the multi-step verify
-(64 sequences, 1..12 tokens, bf16 pool + per-token states), the decode with
+(64 sequences, 1..12 tokens, bf16 pool + per-token states), the same verify
+with the gates formed in the kernel from raw projections, the decode with
 per-key-channel gates and the long KDA prefill (T = 32768, Hv = 32,
 per-channel gate) as extra objects, each with its own roofline.
 
@@ -82,9 +83,11 @@ def pool_bytes(case):
         n += len(valid) * slab
     if case.steps:
         n += toks * slab
-    gate_per_tok = case.g[0].numel() * 4  # [Hv] or, per key channel, [Hv, K] fp32
-    per_tok = 2 * case.q.shape[1] * K * case.q.element_size() + 2 * Hv * V * case.v.element_size() \
-        + gate_per_tok + Hv * case.beta.element_size()
+    if case.raw is not None:  # raw projections a, b [Hv] per token (A_log, dt_bias are per head)
+        gate_per_tok = 2 * Hv * case.raw["a"].element_size()
+    else:  # g [Hv] or, per key channel, [Hv, K] fp32, and beta [Hv]
+        gate_per_tok = case.g[0].numel() * 4 + Hv * case.beta.element_size()
+    per_tok = 2 * case.q.shape[1] * K * case.q.element_size() + 2 * Hv * V * case.v.element_size() + gate_per_tok
     return n + toks * per_tok, toks
 
 
@@ -350,8 +353,15 @@ class PoolRun:
         if c.steps:
             self.ib = torch.empty((c.ibuf_rows, c.steps) + tuple(c.pool.shape[1:]), dtype=c.pool.dtype, device=dev)
         self.flags = gdr.GDR_COMMIT if c.commit else 0
+        self.raw = None if c.raw is None else {n: t.to(dev) for n, t in c.raw.items()}
 
     def step(self, stream=None):
+        if self.raw is not None:
+            r = self.raw
+            gdr.recurrent_fwd_gated(self.q, self.k, self.v, r["a"], r["b"], r["A_log"], r["dt_bias"], self.pool,
+                                    self.idx, self.cu, scale=self.case.scale, flags=self.flags, o=self.o,
+                                    intermediate_states=self.ib, stream=stream)
+            return
         gdr.recurrent_fwd(self.q, self.k, self.v, self.g, self.beta, self.pool, self.idx, self.cu,
                           scale=self.case.scale, flags=self.flags, o=self.o, intermediate_states=self.ib,
                           stream=stream)
@@ -442,7 +452,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default="", help="comma list of sections: prefill,decode,verify,kda,kda_decode")
+    ap.add_argument("--only", default="", help="comma list of sections: prefill,decode,verify,kda,kda_decode,"
+                                               "verify_gated")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -463,7 +474,8 @@ def main():
     stream = torch.cuda.Stream()
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush = lambda: flush_buf.fill_(1)
-    only = set(filter(None, args.only.split(","))) or {"prefill", "decode", "verify", "kda", "kda_decode"}
+    only = set(filter(None, args.only.split(","))) or {"prefill", "decode", "verify", "kda", "kda_decode",
+                                                        "verify_gated"}
 
     dist_ = Dist(world, dev)
 
@@ -476,11 +488,13 @@ def main():
     pre_case = workloads.varlen_bf16_prefill()
     pre = Prefill(pre_case, dev)
     extra = {}
-    dec = ver = kda = kdec = None
+    dec = ver = kda = kdec = vg = None
     if "decode" in only:
         dec = PoolRun(workloads.decode_fp32_pool(), dev)
     if "kda_decode" in only:
         kdec = PoolRun(workloads.decode_kda_fp32_pool(), dev)
+    if "verify_gated" in only:
+        vg = PoolRun(workloads.verify_bf16_pool_raw_gates(), dev)
     if "verify" in only:
         ver = PoolRun(workloads.verify_bf16_pool(), dev)
     if "kda" in only:
@@ -532,6 +546,14 @@ def main():
         kd_ms = max_over_ranks(kd_ms)
         extra["kda_decode"] = {"workload": kdec.case.name, "tokens_per_s": round(world * toks / (kd_ms / 1e3), 1),
                                "ms_per_step": round(kd_ms, 4), "valid_tokens": toks, "roofline": kd_roof}
+    if vg is not None:
+        nbytes, toks = pool_bytes(vg.case)
+        vg_ms, vg_prof, vg_roof, _ = measure(vg, max(args.steps, 20), args.warmup, flush, stream,
+                                             lambda n: nbytes, lambda n: "hbm", peaks, toks)
+        launches += sum(v[1] for v in vg_prof.values())
+        vg_ms = max_over_ranks(vg_ms)
+        extra["verify_gated"] = {"workload": vg.case.name, "tokens_per_s": round(world * toks / (vg_ms / 1e3), 1),
+                                 "ms_per_step": round(vg_ms, 4), "valid_tokens": toks, "roofline": vg_roof}
     if kda is not None:
         k_ms, k_prof, k_roof, _ = measure(kda, max(3, args.steps // 10), args.warmup, flush, stream,
                                           prefill_work_fn(kda.case), lambda n: "tensor", peaks, kda.case.T)

@@ -31,7 +31,7 @@ STATUS = {0: "GDR_OK", 1: "GDR_ERR_INVALID_ARG", 2: "GDR_ERR_UNSUPPORTED", 3: "G
 
 # every symbol include/gdr.h declares
 EXPORTED = ("gdr_chunk_workspace_size", "gdr_chunk_fwd", "gdr_chunk_fwd_noalloc", "gdr_recurrent_fwd",
-            "gdr_gating_fwd",
+            "gdr_recurrent_fwd_gated", "gdr_gating_fwd",
             "gdr_last_error", "gdr_get_device_status", "gdr_profile_enable", "gdr_profile_read",
             "gdr_version")
 
@@ -62,6 +62,8 @@ def load(path: str | None = None):
     lib.gdr_chunk_fwd_noalloc.restype = I
     lib.gdr_recurrent_fwd.argtypes = [P, P, P, P, P, P, I, I, P, P, I, I64, I, I, I, I, F, I, I, P, P, I, P]
     lib.gdr_recurrent_fwd.restype = I
+    lib.gdr_recurrent_fwd_gated.argtypes = [P, P, P, P, P, P, P, P, I, I, P, P, I, I64, I, I, I, I, F, I, I, P, P, I, P]
+    lib.gdr_recurrent_fwd_gated.restype = I
     lib.gdr_gating_fwd.argtypes = [P, P, P, P, I64, I, I, I, P, P, P]
     lib.gdr_gating_fwd.restype = I
     lib.gdr_last_error.argtypes = []
@@ -192,6 +194,36 @@ def recurrent_fwd(q, k, v, g, beta, state_pool, state_indices, cu_seqlens, *, sc
                                     _dtype_code(state_pool), state_pool.shape[0], _ptr(state_indices),
                                     _ptr(cu_seqlens), N, T, Hk, Hv, K, V, float(scale), _dtype_code(q),
                                     flags, _ptr(o), _ptr(intermediate_states), steps, _stream(stream)))
+    return o
+
+
+def recurrent_fwd_gated(q, k, v, a, b, A_log, dt_bias, state_pool, state_indices, cu_seqlens, *, scale=None,
+                        flags: int = GDR_COMMIT, o=None, intermediate_states=None, stream=None):
+    """recurrent_fwd with the gates formed in the kernel from the raw
+    projections: g = -exp(A_log) softplus(a + dt_bias), beta = sigmoid(b) (x2
+    with GDR_NEG_EIGVAL).  a, b [T, Hv] (q's dtype); A_log, dt_bias [Hv] fp32.
+    Returns o."""
+    T, Hk, K = q.shape
+    Hv, V = v.shape[1], v.shape[2]
+    N = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = K ** -0.5
+    if o is None:
+        o = torch.empty(T, Hv, V, dtype=q.dtype, device=q.device)
+    steps = 0
+    if intermediate_states is not None:
+        if intermediate_states.dim() != 5 or intermediate_states.shape[0] < N:
+            raise ValueError("intermediate_states must be [rows >= N, steps, Hv, V, K]")
+        if intermediate_states.dtype != state_pool.dtype:
+            raise TypeError("intermediate_states must have the pool dtype")
+        steps = intermediate_states.shape[1]
+    if a.dtype != q.dtype or b.dtype != q.dtype:
+        raise TypeError("a and b must have q's dtype")
+    _check(load().gdr_recurrent_fwd_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias),
+                                          _ptr(state_pool), _dtype_code(state_pool), state_pool.shape[0],
+                                          _ptr(state_indices), _ptr(cu_seqlens), N, T, Hk, Hv, K, V, float(scale),
+                                          _dtype_code(q), flags, _ptr(o), _ptr(intermediate_states), steps,
+                                          _stream(stream)))
     return o
 
 

@@ -210,23 +210,35 @@ int gdr_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
     return launch_status(launch_chunk(a, s), "gdr_chunk_fwd launch");
 }
 
-int gdr_recurrent_fwd(const void* q, const void* k, const void* v, const float* g, const void* beta,
-                      void* state_pool, int pool_dtype, int num_slots, const int32_t* state_indices,
-                      const int32_t* cu_seqlens, int N, int64_t T_total, int Hk, int Hv, int K, int V,
-                      float scale, int dtype, int flags, void* o, void* intermediate_states, int steps,
-                      gdr_stream_t stream) {
+// Shared by gdr_recurrent_fwd and gdr_recurrent_fwd_gated: `rg` carries the
+// raw gate projections of the fused variant (g and beta are then null).
+struct RawGates {
+    const void* a;
+    const void* b;
+    const float* A_log;
+    const float* dt_bias;
+};
+
+static int recurrent_impl(const void* q, const void* k, const void* v, const float* g, const void* beta,
+                          const RawGates* rg, void* state_pool, int pool_dtype, int num_slots,
+                          const int32_t* state_indices, const int32_t* cu_seqlens, int N, int64_t T_total, int Hk,
+                          int Hv, int K, int V, float scale, int dtype, int flags, void* o, void* intermediate_states,
+                          int steps, gdr_stream_t stream, const char* who) {
     if (int rc = check_common(N, T_total, Hk, Hv, K, V, dtype)) return rc;
     if (pool_dtype != GDR_BF16 && pool_dtype != GDR_F32)
         return fail(GDR_ERR_UNSUPPORTED, "pool_dtype %d", pool_dtype);
-    if (flags & ~(GDR_QK_L2NORM | GDR_COMMIT | GDR_VALIDATE | GDR_CHANNEL_GATE))
-        return fail(GDR_ERR_INVALID_ARG, "unsupported flags 0x%x for gdr_recurrent_fwd", flags);
+    const int allowed = rg ? (GDR_QK_L2NORM | GDR_COMMIT | GDR_VALIDATE | GDR_NEG_EIGVAL)
+                           : (GDR_QK_L2NORM | GDR_COMMIT | GDR_VALIDATE | GDR_CHANNEL_GATE);
+    if (flags & ~allowed) return fail(GDR_ERR_INVALID_ARG, "unsupported flags 0x%x for %s", flags, who);
     if (N == 0) return ok();
     if (num_slots <= 0) return fail(GDR_ERR_INVALID_ARG, "num_slots must be positive");
     if (intermediate_states && steps <= 0)
         return fail(GDR_ERR_INVALID_ARG, "steps must be positive with intermediate_states");
     if (!state_pool || !state_indices || !cu_seqlens)
         return fail(GDR_ERR_INVALID_ARG, "null pointer argument");
-    if (T_total > 0 && (!q || !k || !v || !g || !beta || !o))
+    if (T_total > 0 && (!q || !k || !v || !o)) return fail(GDR_ERR_INVALID_ARG, "null pointer argument");
+    if (T_total > 0 && !rg && (!g || !beta)) return fail(GDR_ERR_INVALID_ARG, "null pointer argument");
+    if (rg && (!rg->A_log || !rg->dt_bias || (T_total > 0 && (!rg->a || !rg->b))))
         return fail(GDR_ERR_INVALID_ARG, "null pointer argument");
     const void* ptrs[] = {q, k, v, g, beta, state_pool, o, intermediate_states};
     for (const void* p : ptrs)
@@ -235,7 +247,8 @@ int gdr_recurrent_fwd(const void* q, const void* k, const void* v, const float* 
     if (int rc = check_device()) return rc;
     cudaStream_t s = (cudaStream_t)stream;
     if (flags & GDR_VALIDATE) {
-        const int64_t gate_n = T_total * Hv * ((flags & GDR_CHANNEL_GATE) ? K : 1);
+        // formed gates are <= 0 and finite for finite projections: only the given ones are checked
+        const int64_t gate_n = rg ? 0 : T_total * Hv * ((flags & GDR_CHANNEL_GATE) ? K : 1);
         if (int rc = run_validation(s, cu_seqlens, N, T_total, true, g, gate_n, state_indices,
                                     num_slots, intermediate_states ? steps : 0))
             return rc;
@@ -247,8 +260,33 @@ int gdr_recurrent_fwd(const void* q, const void* k, const void* v, const float* 
     a.N = N; a.Hk = Hk; a.Hv = Hv; a.K = K; a.V = V; a.steps = intermediate_states ? steps : 0;
     a.num_slots = num_slots;
     a.T = T_total;
-    a.dtype = dtype; a.pool_dtype = pool_dtype; a.flags = flags & ~GDR_VALIDATE; a.scale = scale;
-    return launch_status(launch_recurrent(a, s), "gdr_recurrent_fwd launch");
+    a.dtype = dtype; a.pool_dtype = pool_dtype; a.flags = flags & ~(GDR_VALIDATE | GDR_NEG_EIGVAL); a.scale = scale;
+    if (rg) {
+        a.ga = rg->a; a.gb = rg->b; a.A_log = rg->A_log; a.dt_bias = rg->dt_bias;
+        a.beta_mul = (flags & GDR_NEG_EIGVAL) ? 2.f : 1.f;
+    }
+    return launch_status(launch_recurrent(a, s), who);
+}
+
+int gdr_recurrent_fwd(const void* q, const void* k, const void* v, const float* g, const void* beta,
+                      void* state_pool, int pool_dtype, int num_slots, const int32_t* state_indices,
+                      const int32_t* cu_seqlens, int N, int64_t T_total, int Hk, int Hv, int K, int V,
+                      float scale, int dtype, int flags, void* o, void* intermediate_states, int steps,
+                      gdr_stream_t stream) {
+    return recurrent_impl(q, k, v, g, beta, nullptr, state_pool, pool_dtype, num_slots, state_indices, cu_seqlens,
+                          N, T_total, Hk, Hv, K, V, scale, dtype, flags, o, intermediate_states, steps, stream,
+                          "gdr_recurrent_fwd");
+}
+
+int gdr_recurrent_fwd_gated(const void* q, const void* k, const void* v, const void* a, const void* b,
+                            const float* A_log, const float* dt_bias, void* state_pool, int pool_dtype,
+                            int num_slots, const int32_t* state_indices, const int32_t* cu_seqlens, int N,
+                            int64_t T_total, int Hk, int Hv, int K, int V, float scale, int dtype, int flags,
+                            void* o, void* intermediate_states, int steps, gdr_stream_t stream) {
+    const RawGates rg{a, b, A_log, dt_bias};
+    return recurrent_impl(q, k, v, nullptr, nullptr, &rg, state_pool, pool_dtype, num_slots, state_indices,
+                          cu_seqlens, N, T_total, Hk, Hv, K, V, scale, dtype, flags, o, intermediate_states, steps,
+                          stream, "gdr_recurrent_fwd_gated");
 }
 
 int gdr_gating_fwd(const void* a, const float* dt_bias, const float* A_log, const void* b, int64_t T,

@@ -23,6 +23,14 @@ struct RecurrentArgs {
     int64_t T;
     int dtype, pool_dtype, flags;
     float scale;
+    // gates formed in the kernel from raw projections (gdr_recurrent_fwd_gated):
+    // g = -exp(A_log) softplus(ga + dt_bias), beta = beta_mul sigmoid(gb);
+    // ga == nullptr means g / beta are given
+    const void* ga = nullptr;
+    const void* gb = nullptr;
+    const float* A_log = nullptr;
+    const float* dt_bias = nullptr;
+    float beta_mul = 1.f;
 };
 
 // Enqueue the recurrent decode / verify kernel.  Returns a cudaError_t.

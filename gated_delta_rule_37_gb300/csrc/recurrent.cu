@@ -36,10 +36,20 @@ struct RecParams {
     int Hk, Hv, steps, flags, num_slots;
     int64_t T;
     float scale;
+    const void* ga;  // raw gate projections (kGate == 2)
+    const void* gb;
+    const float* A_log;
+    const float* dt_bias;
+    float beta_mul;
 };
 
-template <typename InT, typename PoolT, int K, int BV, bool kChan>
-__global__ void __launch_bounds__(BV / kRowsPerWarp * 32)
+// kGate: 0 scalar log-decay g [T, Hv]; 1 per-key-channel g [T, Hv, K];
+// 2 gates formed from raw projections (FlashQLA in-kernel gating commit).
+
+// At most 128 registers per thread: four 128-thread CTAs per SM keep enough
+// rows in flight (the per-token loop is latency-bound).
+template <typename InT, typename PoolT, int K, int BV, int kGate>
+__global__ void __launch_bounds__(BV / kRowsPerWarp * 32, BV == 64 ? 4 : 1)
 recurrent_kernel(RecParams p) {
     constexpr int KPT = K / 32;  // key channels per lane
     const int b = blockIdx.x;
@@ -68,24 +78,48 @@ recurrent_kernel(RecParams p) {
 
     // Per-token inputs of token t + 1 are loaded while token t is processed, so
     // their global-load latency is hidden behind the reductions of the current token.
-    constexpr bool chan = kChan;  // GDR_CHANNEL_GATE: g is [T, Hv, K]
+    constexpr bool chan = kGate == 1;  // GDR_CHANNEL_GATE: g is [T, Hv, K]
+    constexpr bool raw = kGate == 2;   // g and beta from raw projections
+    const InT* __restrict__ gap = static_cast<const InT*>(p.ga);
+    const InT* __restrict__ gbp = static_cast<const InT*>(p.gb);
+    const float negA = raw ? -expf(p.A_log[h]) : 0.f, dtb = raw ? p.dt_bias[h] : 0.f;
     float kn[KPT], qn[KPT], gcn[KPT], gn = 0.f, bn = 0.f, vn = 0.f;
     auto load_token = [&](int t) {
         Vec<InT, KPT>::load(kp + ((size_t)t * p.Hk + kh) * K + lane * KPT, kn);
         Vec<InT, KPT>::load(qp + ((size_t)t * p.Hk + kh) * K + lane * KPT, qn);
         if (chan) Vec<float, KPT>::load(p.g + ((size_t)t * p.Hv + h) * K + lane * KPT, gcn);
-        else gn = p.g[(size_t)t * p.Hv + h];
-        bn = to_f(bp[(size_t)t * p.Hv + h]);
+        else if (!raw) gn = p.g[(size_t)t * p.Hv + h];
+        if (!raw) bn = to_f(bp[(size_t)t * p.Hv + h]);
         vn = to_f(vp[((size_t)t * p.Hv + h) * V + v0 + (lane & 15)]);
     };
-    if (bos < eos) load_token(bos);
+    // raw projections: lane j forms the decay and beta of token base + j for the
+    // next 32 tokens at once, off the per-token dependency chain; each token
+    // then takes its pair with one shuffle
+    float ra = 1.f, rb = 0.f;
+    auto form_gates = [&](int base) {
+        const int t = base + lane;
+        if (t < eos) {
+            const float x = to_f(gap[(size_t)t * p.Hv + h]) + dtb;  // softplus, threshold 20, as gdr_gating_fwd
+            ra = __expf(negA * (x > 20.f ? x : log1pf(expf(x))));
+            rb = p.beta_mul / (1.f + expf(-to_f(gbp[(size_t)t * p.Hv + h])));
+        }
+    };
+    if (bos < eos) load_token(bos);  // first, so its loads overlap those of the gates
+    if (raw && bos < eos) form_gates(bos);
 #pragma unroll 1
     for (int t = bos; t < eos; ++t) {
         float kk[KPT], qq[KPT], ac[KPT];
 #pragma unroll
         for (int c = 0; c < KPT; ++c) { kk[c] = kn[c]; qq[c] = qn[c]; ac[c] = chan ? __expf(gcn[c]) : 1.f; }
-        const float a = chan ? 1.f : __expf(gn);
-        const float bt = bn;
+        float a, bt;
+        if (raw) {
+            if (t > bos && ((t - bos) & 31) == 0) form_gates(t);
+            a = __shfl_sync(0xffffffffu, ra, (t - bos) & 31);
+            bt = __shfl_sync(0xffffffffu, rb, (t - bos) & 31);
+        } else {
+            a = chan ? 1.f : __expf(gn);
+            bt = bn;
+        }
         const float vv = vn;
         if (t + 1 < eos) load_token(t + 1);
         if (p.flags & 1) {  // GDR_QK_L2NORM
@@ -147,7 +181,7 @@ recurrent_kernel(RecParams p) {
     }
 }
 
-template <typename InT, typename PoolT, int K, bool kChan>
+template <typename InT, typename PoolT, int K, int kGate>
 cudaError_t launch_k(const RecParams& p, int N, int V, cudaStream_t stream) {
     // V-column split: 64-row blocks (128 threads) measured best on GB300 for
     // both single-token decode (6.50 vs 6.42 TB/s at 128 rows) and 12-token
@@ -162,13 +196,13 @@ cudaError_t launch_k(const RecParams& p, int N, int V, cudaStream_t stream) {
     KernelTimer kt("recurrent", stream);
     switch (bv) {
         case 128:
-            recurrent_kernel<InT, PoolT, K, 128, kChan><<<grid, 256, 0, stream>>>(p);
+            recurrent_kernel<InT, PoolT, K, 128, kGate><<<grid, 256, 0, stream>>>(p);
             break;
         case 64:
-            recurrent_kernel<InT, PoolT, K, 64, kChan><<<grid, 128, 0, stream>>>(p);
+            recurrent_kernel<InT, PoolT, K, 64, kGate><<<grid, 128, 0, stream>>>(p);
             break;
         default:
-            recurrent_kernel<InT, PoolT, K, 32, kChan><<<grid, 64, 0, stream>>>(p);
+            recurrent_kernel<InT, PoolT, K, 32, kGate><<<grid, 64, 0, stream>>>(p);
             break;
     }
     return cudaGetLastError();
@@ -176,9 +210,13 @@ cudaError_t launch_k(const RecParams& p, int N, int V, cudaStream_t stream) {
 
 template <typename InT, typename PoolT>
 cudaError_t launch_kt(const RecParams& p, int N, int K, int V, cudaStream_t stream) {
-    const bool chan = p.flags & 0x10;  // GDR_CHANNEL_GATE
-    if (K == 128) return chan ? launch_k<InT, PoolT, 128, true>(p, N, V, stream) : launch_k<InT, PoolT, 128, false>(p, N, V, stream);
-    return chan ? launch_k<InT, PoolT, 64, true>(p, N, V, stream) : launch_k<InT, PoolT, 64, false>(p, N, V, stream);
+    const int mode = p.ga ? 2 : (p.flags & 0x10) ? 1 : 0;  // raw gates / GDR_CHANNEL_GATE / scalar
+    if (K == 128) {
+        if (mode == 2) return launch_k<InT, PoolT, 128, 2>(p, N, V, stream);
+        return mode ? launch_k<InT, PoolT, 128, 1>(p, N, V, stream) : launch_k<InT, PoolT, 128, 0>(p, N, V, stream);
+    }
+    if (mode == 2) return launch_k<InT, PoolT, 64, 2>(p, N, V, stream);
+    return mode ? launch_k<InT, PoolT, 64, 1>(p, N, V, stream) : launch_k<InT, PoolT, 64, 0>(p, N, V, stream);
 }
 
 }  // namespace
@@ -191,6 +229,7 @@ cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t stream) {
     p.Hk = a.Hk; p.Hv = a.Hv; p.steps = a.steps; p.flags = a.flags; p.scale = a.scale;
     p.num_slots = a.num_slots;
     p.T = a.T;
+    p.ga = a.ga; p.gb = a.gb; p.A_log = a.A_log; p.dt_bias = a.dt_bias; p.beta_mul = a.beta_mul;
     const bool in_bf16 = a.dtype == 0, pool_bf16 = a.pool_dtype == 0;
     if (in_bf16 && pool_bf16) return launch_kt<__nv_bfloat16, __nv_bfloat16>(p, a.N, a.K, a.V, stream);
     if (in_bf16) return launch_kt<__nv_bfloat16, float>(p, a.N, a.K, a.V, stream);

@@ -20,6 +20,8 @@ from __future__ import annotations
 
 from dataclasses import dataclass, field
 
+import math
+
 import torch
 
 
@@ -111,6 +113,7 @@ class PoolCase:
     steps: int = 0
     ibuf_rows: int = 0
     meta: dict = field(default_factory=dict)
+    raw: dict | None = None  # raw gate projections a, b [T, Hv], A_log, dt_bias [Hv]
 
     @property
     def N(self):
@@ -200,3 +203,27 @@ def verify_bf16_pool(pad_count: int = 0) -> PoolCase:
     return pool_case(4, lens, 16, 32, 128, 128, 65, pool_dtype=torch.bfloat16,
                      g_range=(-1.0, 0.0), pad_count=pad_count, commit=False, steps=12,
                      ibuf_rows=65, name="verify_B64_T1to12_Hk16_Hv32_D128_bf16pool")
+
+
+def raw_gates(seed: int, T: int, Hv: int, dtype=torch.bfloat16) -> dict:
+    """Raw gate projections for the in-kernel gating path: a, b ~ N(0, 1) in
+    the input dtype; A_log = log U[1, 16]; dt_bias = log(expm1(dt)) with
+    log dt ~ U[log 1e-3, log 1e-1] (a Mamba-style initialisation; the pages do
+    not state one), both fp32 [Hv]."""
+    gen = _gen(seed)
+    a = torch.randn(T, Hv, generator=gen).to(dtype)
+    b = torch.randn(T, Hv, generator=gen).to(dtype)
+    A_log = torch.log(_uniform(gen, (Hv,), 1.0, 16.0))
+    dt = torch.exp(_uniform(gen, (Hv,), math.log(1e-3), math.log(1e-1)))
+    dt_bias = torch.log(torch.expm1(dt))
+    return dict(a=a, b=b, A_log=A_log.float(), dt_bias=dt_bias.float())
+
+
+def verify_bf16_pool_raw_gates() -> PoolCase:
+    """The verify workload with its gates given as raw projections (the
+    in-kernel gating path) in ``raw``; the case's own g and beta are not used
+    by that path."""
+    case = verify_bf16_pool()
+    case.raw = raw_gates(6, case.T, case.v.shape[1])
+    case.name = "verify_gated_B64_T1to12_Hk16_Hv32_D128_bf16pool"
+    return case

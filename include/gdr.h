@@ -179,6 +179,24 @@ GDR_API int gdr_recurrent_fwd(const void* q, const void* k, const void* v, const
                       gdr_stream_t stream);
 
 /*
+ * gdr_recurrent_fwd_gated -- gdr_recurrent_fwd with the gates formed inside the
+ * kernel from the raw projections (FlashQLA PR #1, in-kernel gating commit):
+ *   g[t,h]    = -exp(A_log[h]) * softplus(a[t,h] + dt_bias[h])
+ *               (softplus beta 1, threshold 20, as gdr_gating_fwd)
+ *   beta[t,h] = sigmoid(b[t,h]), times 2 with GDR_NEG_EIGVAL
+ *   a, b [T_total, Hv] dtype; A_log, dt_bias [Hv] fp32 device.
+ * beta is kept in fp32 (it is not rounded to dtype as gdr_gating_fwd's output
+ * is).  Every other argument, flag (GDR_QK_L2NORM, GDR_COMMIT, GDR_VALIDATE)
+ * and guarantee is gdr_recurrent_fwd's; GDR_CHANNEL_GATE is not accepted.
+ */
+GDR_API int gdr_recurrent_fwd_gated(const void* q, const void* k, const void* v, const void* a,
+                      const void* b, const float* A_log, const float* dt_bias, void* state_pool,
+                      int pool_dtype, int num_slots, const int32_t* state_indices,
+                      const int32_t* cu_seqlens, int N, int64_t T_total, int Hk, int Hv, int K,
+                      int V, float scale, int dtype, int flags, void* o, void* intermediate_states,
+                      int steps, gdr_stream_t stream);
+
+/*
  * gdr_gating_fwd -- gate preparation from raw projections (FlashQLA PR #1,
  * host-gating and in-kernel-gating commits):
  *   g[t,h]    = -exp(A_log[h]) * softplus(a[t,h] + dt_bias[h])

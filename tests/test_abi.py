@@ -127,6 +127,33 @@ def test_recurrent_fwd_empty_is_ok(lib):
     assert _rec_call(lib, N=0, T=0) == 0
 
 
+def _gated_call(lib, **kw):
+    P = ctypes.c_void_p
+    a = dict(q=P(16), k=P(32), v=P(48), a=P(64), b=P(80), A_log=P(96), dt_bias=P(112), pool=P(128), pool_dtype=1,
+             num_slots=8, idx=P(144), cu=P(160), N=4, T=4, Hk=2, Hv=4, K=128, V=128, scale=0.1, dtype=0, flags=4,
+             o=P(176), ibuf=None, steps=0, stream=None)
+    a.update(kw)
+    return lib.gdr_recurrent_fwd_gated(a["q"], a["k"], a["v"], a["a"], a["b"], a["A_log"], a["dt_bias"], a["pool"],
+                                       a["pool_dtype"], a["num_slots"], a["idx"], a["cu"], a["N"], a["T"], a["Hk"],
+                                       a["Hv"], a["K"], a["V"], a["scale"], a["dtype"], a["flags"], a["o"], a["ibuf"],
+                                       a["steps"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(flags=0x10), 1),                              # per-channel gates are not formed from raw projections
+    (dict(A_log=None), 1),
+    (dict(b=None), 1),
+    (dict(pool_dtype=3), 2),
+    (dict(K=96, V=96), 2),
+])
+def test_recurrent_fwd_gated_rejects_before_launch(lib, kw, code):
+    assert _gated_call(lib, **kw) == code
+
+
+def test_recurrent_fwd_gated_empty_is_ok(lib):
+    assert _gated_call(lib, N=0, T=0) == 0
+
+
 def test_gating_rejects(lib):
     P = ctypes.c_void_p
     assert lib.gdr_gating_fwd(P(16), P(32), P(48), P(64), 4, 0, 0, 0, P(80), P(96), None) == 1

@@ -21,7 +21,7 @@ def _lib():
     gdr.load()
 
 
-def run_case(case, *, flags, with_ibuf):
+def run_case(case, *, flags, with_ibuf, gated=False):
     dev = DEV
     pool = Guarded(case.pool.shape, case.pool.dtype, dev, fill_bytes=case.pool)
     o_init = sentinel_like((case.T, case.v.shape[1], case.v.shape[2]), case.q.dtype)
@@ -31,9 +31,15 @@ def run_case(case, *, flags, with_ibuf):
         ib_shape = (case.ibuf_rows, case.steps) + tuple(case.pool.shape[1:])
         ib_init = sentinel_like(ib_shape, case.pool.dtype)
         ib = Guarded(ib_shape, case.pool.dtype, dev, fill_bytes=ib_init)
-    gdr.recurrent_fwd(case.q.to(dev), case.k.to(dev), case.v.to(dev), case.g.to(dev), case.beta.to(dev),
-                      pool.view, case.state_indices.to(dev), case.cu_seqlens.to(dev), scale=case.scale,
-                      flags=flags, o=o.view, intermediate_states=ib.view if ib else None)
+    if gated:
+        r = {n: t.to(dev) for n, t in case.raw.items()}
+        gdr.recurrent_fwd_gated(case.q.to(dev), case.k.to(dev), case.v.to(dev), r["a"], r["b"], r["A_log"],
+                                r["dt_bias"], pool.view, case.state_indices.to(dev), case.cu_seqlens.to(dev),
+                                scale=case.scale, flags=flags, o=o.view, intermediate_states=ib.view if ib else None)
+    else:
+        gdr.recurrent_fwd(case.q.to(dev), case.k.to(dev), case.v.to(dev), case.g.to(dev), case.beta.to(dev),
+                          pool.view, case.state_indices.to(dev), case.cu_seqlens.to(dev), scale=case.scale,
+                          flags=flags, o=o.view, intermediate_states=ib.view if ib else None)
     torch.cuda.synchronize()
     assert pool.guards_intact() and o.guards_intact() and (ib is None or ib.guards_intact())
     return pool, o, ib, o_init
@@ -132,6 +138,34 @@ def test_channel_gate_constant_matches_scalar_gate():
     for b in range(case.N):
         L = cu[b + 1] - cu[b]
         check_state(ib_b.view[b, :L].cpu(), ib_a.view[b, :L].cpu().double().numpy(), f"ibuf row {b}")
+
+
+def _with_oracle_gates(case, neg_eigval=False):
+    """The case with g and beta formed from its raw projections by the oracle (fp64)."""
+    import dataclasses
+    r = case.raw
+    g, beta = oracle.gating(r["a"], r["dt_bias"], r["A_log"], r["b"], neg_eigval=neg_eigval)
+    return dataclasses.replace(case, g=torch.from_numpy(g), beta=torch.from_numpy(beta))
+
+
+def test_gated_verify_full_size():
+    """In-kernel gating (FlashQLA's in-kernel gating commit) on the verify
+    workload: gates formed from raw a, b, A_log, dt_bias inside the kernel."""
+    case = workloads.verify_bf16_pool_raw_gates()
+    pool, o, ib, o_init = run_case(case, flags=0, with_ibuf=True, gated=True)
+    check_case(_with_oracle_gates(case), pool, o, ib, o_init, commit=False)
+
+
+@pytest.mark.parametrize("neg_eigval", [False, True])
+@pytest.mark.parametrize("dtype,pool_dtype", [(torch.bfloat16, torch.float32), (torch.float32, torch.bfloat16)])
+def test_gated_small_cases(neg_eigval, dtype, pool_dtype):
+    lens = [1, 6, 0, 3, 12]
+    case = workloads.pool_case(51, lens, 2, 4, 128, 128, 7, dtype=dtype, pool_dtype=pool_dtype, pad_count=1,
+                               commit=True, steps=12, ibuf_rows=5)
+    case.raw = workloads.raw_gates(52, case.T, 4, dtype=dtype)
+    flags = gdr.GDR_COMMIT | (gdr.GDR_NEG_EIGVAL if neg_eigval else 0)
+    pool, o, ib, o_init = run_case(case, flags=flags, with_ibuf=True, gated=True)
+    check_case(_with_oracle_gates(case, neg_eigval), pool, o, ib, o_init, commit=True)
 
 
 @pytest.mark.parametrize("Hk,Hv", [(4, 4), (2, 8), (1, 4)])       # MHA, GVA 4, MQA
