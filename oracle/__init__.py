@@ -12,6 +12,9 @@ Contents
   * ``pool``        -- slot-indexed decode / multi-step verify (C, fp64).
   * ``bruteforce``  -- explicit K x K transition matrices (numpy, tiny sizes).
   * ``gating``, ``l2norm`` -- the optional input preparation (C, fp64).
+  * ``gated_rmsnorm`` -- the optional output epilogue of decode (numpy, fp64):
+                       rmsnorm(o) * w * sigmoid(gate) over each value row
+                       (tokenspeed PR #834, fused gated-norm epilogue commit).
 
 Recurrence per value-head (state S in R^{V x K}, V-major):
   S~ = exp(g_t) S_{t-1};  n_t = beta_t (v_t - S~ k_t);  S_t = S~ + n_t k_t^T;
@@ -189,6 +192,17 @@ def l2norm(x, eps: float = 1e-6):
     y = np.zeros_like(x)
     _load().oracle_l2norm(_ptr(x), x.size // D, D, float(eps), _ptr(y))
     return y
+
+
+def gated_rmsnorm(o, weight, gate, eps: float):
+    """The decode output epilogue: each value row x = o[t, h, :] becomes
+    x / sqrt(mean(x^2) + eps) * weight * sigmoid(gate[t, h, :]).  o, gate
+    [T, Hv, V]; weight [V]."""
+    x = _f64(o)
+    w = _f64(weight)
+    z = _f64(gate)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * w * (1.0 / (1.0 + np.exp(-z)))
 
 
 def bruteforce(q, k, v, beta, *, g=None, gk=None, initial_state=None, scale):

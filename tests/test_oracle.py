@@ -330,6 +330,24 @@ def test_pool_no_commit_leaves_pool():
     assert np.array_equal(pout, case.pool.double().numpy())
 
 
+def test_gated_rmsnorm_hand_example_and_invariants():
+    """Decode output epilogue rmsnorm(o) * w * sigmoid(gate): a hand-worked row,
+    unit RMS with w = 1 and an open gate, scale invariance at eps = 0, and the
+    gate at 0 halving the output."""
+    # row (3, 4): mean square 12.5; eps 0.5 -> divisor sqrt(13) ; w (2, 1); gate 0 -> 1/2
+    y = oracle.gated_rmsnorm(np.array([[[3.0, 4.0]]]), np.array([2.0, 1.0]), np.zeros((1, 1, 2)), 0.5)
+    np.testing.assert_allclose(y[0, 0], [3.0 / math.sqrt(13.0), 2.0 / math.sqrt(13.0)], rtol=1e-15)
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((3, 2, 16))
+    open_gate = np.full_like(x, 50.0)
+    y1 = oracle.gated_rmsnorm(x, np.ones(16), open_gate, 0.0)
+    np.testing.assert_allclose(np.mean(y1 * y1, axis=-1), 1.0, rtol=1e-12)
+    y2 = oracle.gated_rmsnorm(7.5 * x, np.ones(16), open_gate, 0.0)
+    np.testing.assert_allclose(y2, y1, rtol=1e-12)
+    y3 = oracle.gated_rmsnorm(x, np.ones(16), np.zeros_like(x), 0.0)
+    np.testing.assert_allclose(y3, 0.5 * y1, rtol=1e-12)
+
+
 def test_gating_closed_forms():
     # a + dt_bias = 0 -> softplus = ln 2; b = 0 -> sigmoid = 1/2
     a = np.array([[0.0, 25.0, -3.0]])
