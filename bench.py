@@ -9,7 +9,8 @@ writing a 256 MB buffer outside the step's events.  The same line carries the
 recurrent decode (256 sequences, fp32 pool, commit), the multi-step verify
 (64 sequences, 1..12 tokens, bf16 pool + per-token states), the same verify
 with the gates formed in the kernel from raw projections, the decode with
-per-key-channel gates and the long KDA prefill (T = 32768, Hv = 32,
+per-key-channel gates, the decode with the gated RMSNorm output epilogue and
+the long KDA prefill (T = 32768, Hv = 32,
 per-channel gate) as extra objects, each with its own roofline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
@@ -88,6 +89,8 @@ def pool_bytes(case):
     else:  # g [Hv] or, per key channel, [Hv, K] fp32, and beta [Hv]
         gate_per_tok = case.g[0].numel() * 4 + Hv * case.beta.element_size()
     per_tok = 2 * case.q.shape[1] * K * case.q.element_size() + 2 * Hv * V * case.v.element_size() + gate_per_tok
+    if case.norm is not None:  # the epilogue's gate [Hv, V] per token
+        per_tok += Hv * V * case.norm["gate"].element_size()
     return n + toks * per_tok, toks
 
 
@@ -354,8 +357,14 @@ class PoolRun:
             self.ib = torch.empty((c.ibuf_rows, c.steps) + tuple(c.pool.shape[1:]), dtype=c.pool.dtype, device=dev)
         self.flags = gdr.GDR_COMMIT if c.commit else 0
         self.raw = None if c.raw is None else {n: t.to(dev) for n, t in c.raw.items()}
+        self.norm = None if c.norm is None else {n: (t.to(dev) if torch.is_tensor(t) else t) for n, t in c.norm.items()}
 
     def step(self, stream=None):
+        if self.norm is not None:
+            gdr.recurrent_fwd_norm(self.q, self.k, self.v, self.g, self.beta, self.pool, self.idx, self.cu,
+                                   self.norm["weight"], self.norm["gate"], eps=self.norm["eps"], scale=self.case.scale,
+                                   flags=self.flags, o=self.o, intermediate_states=self.ib, stream=stream)
+            return
         if self.raw is not None:
             r = self.raw
             gdr.recurrent_fwd_gated(self.q, self.k, self.v, r["a"], r["b"], r["A_log"], r["dt_bias"], self.pool,
@@ -453,7 +462,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", help="comma list of sections: prefill,decode,verify,kda,kda_decode,"
-                                               "verify_gated")
+                                               "verify_gated,decode_norm")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -475,7 +484,7 @@ def main():
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush = lambda: flush_buf.fill_(1)
     only = set(filter(None, args.only.split(","))) or {"prefill", "decode", "verify", "kda", "kda_decode",
-                                                        "verify_gated"}
+                                                        "verify_gated", "decode_norm"}
 
     dist_ = Dist(world, dev)
 
@@ -488,13 +497,15 @@ def main():
     pre_case = workloads.varlen_bf16_prefill()
     pre = Prefill(pre_case, dev)
     extra = {}
-    dec = ver = kda = kdec = vg = None
+    dec = ver = kda = kdec = vg = dn = None
     if "decode" in only:
         dec = PoolRun(workloads.decode_fp32_pool(), dev)
     if "kda_decode" in only:
         kdec = PoolRun(workloads.decode_kda_fp32_pool(), dev)
     if "verify_gated" in only:
         vg = PoolRun(workloads.verify_bf16_pool_raw_gates(), dev)
+    if "decode_norm" in only:
+        dn = PoolRun(workloads.decode_fp32_pool_norm(), dev)
     if "verify" in only:
         ver = PoolRun(workloads.verify_bf16_pool(), dev)
     if "kda" in only:
@@ -554,6 +565,14 @@ def main():
         vg_ms = max_over_ranks(vg_ms)
         extra["verify_gated"] = {"workload": vg.case.name, "tokens_per_s": round(world * toks / (vg_ms / 1e3), 1),
                                  "ms_per_step": round(vg_ms, 4), "valid_tokens": toks, "roofline": vg_roof}
+    if dn is not None:
+        nbytes, toks = pool_bytes(dn.case)
+        dn_ms, dn_prof, dn_roof, _ = measure(dn, max(args.steps, 20), args.warmup, flush, stream,
+                                             lambda n: nbytes, lambda n: "hbm", peaks, toks)
+        launches += sum(v[1] for v in dn_prof.values())
+        dn_ms = max_over_ranks(dn_ms)
+        extra["decode_norm"] = {"workload": dn.case.name, "tokens_per_s": round(world * toks / (dn_ms / 1e3), 1),
+                                "ms_per_step": round(dn_ms, 4), "valid_tokens": toks, "roofline": dn_roof}
     if kda is not None:
         k_ms, k_prof, k_roof, _ = measure(kda, max(3, args.steps // 10), args.warmup, flush, stream,
                                           prefill_work_fn(kda.case), lambda n: "tensor", peaks, kda.case.T)

@@ -31,7 +31,7 @@ STATUS = {0: "GDR_OK", 1: "GDR_ERR_INVALID_ARG", 2: "GDR_ERR_UNSUPPORTED", 3: "G
 
 # every symbol include/gdr.h declares
 EXPORTED = ("gdr_chunk_workspace_size", "gdr_chunk_fwd", "gdr_chunk_fwd_noalloc", "gdr_recurrent_fwd",
-            "gdr_recurrent_fwd_gated", "gdr_gating_fwd",
+            "gdr_recurrent_fwd_gated", "gdr_recurrent_fwd_norm", "gdr_gating_fwd",
             "gdr_last_error", "gdr_get_device_status", "gdr_profile_enable", "gdr_profile_read",
             "gdr_version")
 
@@ -64,6 +64,9 @@ def load(path: str | None = None):
     lib.gdr_recurrent_fwd.restype = I
     lib.gdr_recurrent_fwd_gated.argtypes = [P, P, P, P, P, P, P, P, I, I, P, P, I, I64, I, I, I, I, F, I, I, P, P, I, P]
     lib.gdr_recurrent_fwd_gated.restype = I
+    lib.gdr_recurrent_fwd_norm.argtypes = [P, P, P, P, P, P, I, I, P, P, I, I64, I, I, I, I, F, I, I, P, P, F, P, P, I,
+                                           P]
+    lib.gdr_recurrent_fwd_norm.restype = I
     lib.gdr_gating_fwd.argtypes = [P, P, P, P, I64, I, I, I, P, P, P]
     lib.gdr_gating_fwd.restype = I
     lib.gdr_last_error.argtypes = []
@@ -194,6 +197,34 @@ def recurrent_fwd(q, k, v, g, beta, state_pool, state_indices, cu_seqlens, *, sc
                                     _dtype_code(state_pool), state_pool.shape[0], _ptr(state_indices),
                                     _ptr(cu_seqlens), N, T, Hk, Hv, K, V, float(scale), _dtype_code(q),
                                     flags, _ptr(o), _ptr(intermediate_states), steps, _stream(stream)))
+    return o
+
+
+def recurrent_fwd_norm(q, k, v, g, beta, state_pool, state_indices, cu_seqlens, norm_weight, norm_gate, *,
+                       eps: float = 1e-6, scale=None, flags: int = GDR_COMMIT, o=None, intermediate_states=None,
+                       stream=None):
+    """recurrent_fwd with the gated RMSNorm output epilogue: each value row x of
+    o becomes x / sqrt(mean(x^2) + eps) * norm_weight * sigmoid(norm_gate).
+    norm_weight [V] fp32; norm_gate [T, Hv, V] (q's dtype).  Returns o."""
+    T, Hk, K = q.shape
+    Hv, V = v.shape[1], v.shape[2]
+    N = cu_seqlens.numel() - 1
+    if scale is None:
+        scale = K ** -0.5
+    if g.dim() == 3:
+        flags |= GDR_CHANNEL_GATE
+    if o is None:
+        o = torch.empty(T, Hv, V, dtype=q.dtype, device=q.device)
+    steps = 0
+    if intermediate_states is not None:
+        steps = intermediate_states.shape[1]
+    if norm_gate.dtype != q.dtype or tuple(norm_gate.shape) != (T, Hv, V):
+        raise ValueError("norm_gate must be [T, Hv, V] in q's dtype")
+    _check(load().gdr_recurrent_fwd_norm(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_pool),
+                                         _dtype_code(state_pool), state_pool.shape[0], _ptr(state_indices),
+                                         _ptr(cu_seqlens), N, T, Hk, Hv, K, V, float(scale), _dtype_code(q), flags,
+                                         _ptr(norm_weight), _ptr(norm_gate), float(eps), _ptr(o),
+                                         _ptr(intermediate_states), steps, _stream(stream)))
     return o
 
 

@@ -219,8 +219,14 @@ struct RawGates {
     const float* dt_bias;
 };
 
+struct OutNorm {
+    const float* weight;
+    const void* gate;
+    float eps;
+};
+
 static int recurrent_impl(const void* q, const void* k, const void* v, const float* g, const void* beta,
-                          const RawGates* rg, void* state_pool, int pool_dtype, int num_slots,
+                          const RawGates* rg, const OutNorm* on, void* state_pool, int pool_dtype, int num_slots,
                           const int32_t* state_indices, const int32_t* cu_seqlens, int N, int64_t T_total, int Hk,
                           int Hv, int K, int V, float scale, int dtype, int flags, void* o, void* intermediate_states,
                           int steps, gdr_stream_t stream, const char* who) {
@@ -240,6 +246,8 @@ static int recurrent_impl(const void* q, const void* k, const void* v, const flo
     if (T_total > 0 && !rg && (!g || !beta)) return fail(GDR_ERR_INVALID_ARG, "null pointer argument");
     if (rg && (!rg->A_log || !rg->dt_bias || (T_total > 0 && (!rg->a || !rg->b))))
         return fail(GDR_ERR_INVALID_ARG, "null pointer argument");
+    if (on && (!on->weight || (T_total > 0 && !on->gate))) return fail(GDR_ERR_INVALID_ARG, "null pointer argument");
+    if (on && !(on->eps >= 0.f)) return fail(GDR_ERR_INVALID_ARG, "eps must be >= 0");
     const void* ptrs[] = {q, k, v, g, beta, state_pool, o, intermediate_states};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return fail(GDR_ERR_INVALID_ARG, "pointer %p not 16-byte aligned", p);
@@ -265,6 +273,9 @@ static int recurrent_impl(const void* q, const void* k, const void* v, const flo
         a.ga = rg->a; a.gb = rg->b; a.A_log = rg->A_log; a.dt_bias = rg->dt_bias;
         a.beta_mul = (flags & GDR_NEG_EIGVAL) ? 2.f : 1.f;
     }
+    if (on) {
+        a.norm_weight = on->weight; a.norm_gate = on->gate; a.norm_eps = on->eps;
+    }
     return launch_status(launch_recurrent(a, s), who);
 }
 
@@ -273,9 +284,20 @@ int gdr_recurrent_fwd(const void* q, const void* k, const void* v, const float* 
                       const int32_t* cu_seqlens, int N, int64_t T_total, int Hk, int Hv, int K, int V,
                       float scale, int dtype, int flags, void* o, void* intermediate_states, int steps,
                       gdr_stream_t stream) {
-    return recurrent_impl(q, k, v, g, beta, nullptr, state_pool, pool_dtype, num_slots, state_indices, cu_seqlens,
-                          N, T_total, Hk, Hv, K, V, scale, dtype, flags, o, intermediate_states, steps, stream,
-                          "gdr_recurrent_fwd");
+    return recurrent_impl(q, k, v, g, beta, nullptr, nullptr, state_pool, pool_dtype, num_slots, state_indices,
+                          cu_seqlens, N, T_total, Hk, Hv, K, V, scale, dtype, flags, o, intermediate_states, steps,
+                          stream, "gdr_recurrent_fwd");
+}
+
+int gdr_recurrent_fwd_norm(const void* q, const void* k, const void* v, const float* g, const void* beta,
+                           void* state_pool, int pool_dtype, int num_slots, const int32_t* state_indices,
+                           const int32_t* cu_seqlens, int N, int64_t T_total, int Hk, int Hv, int K, int V,
+                           float scale, int dtype, int flags, const float* norm_weight, const void* norm_gate,
+                           float eps, void* o, void* intermediate_states, int steps, gdr_stream_t stream) {
+    const OutNorm on{norm_weight, norm_gate, eps};
+    return recurrent_impl(q, k, v, g, beta, nullptr, &on, state_pool, pool_dtype, num_slots, state_indices,
+                          cu_seqlens, N, T_total, Hk, Hv, K, V, scale, dtype, flags, o, intermediate_states, steps,
+                          stream, "gdr_recurrent_fwd_norm");
 }
 
 int gdr_recurrent_fwd_gated(const void* q, const void* k, const void* v, const void* a, const void* b,
@@ -284,7 +306,7 @@ int gdr_recurrent_fwd_gated(const void* q, const void* k, const void* v, const v
                             int64_t T_total, int Hk, int Hv, int K, int V, float scale, int dtype, int flags,
                             void* o, void* intermediate_states, int steps, gdr_stream_t stream) {
     const RawGates rg{a, b, A_log, dt_bias};
-    return recurrent_impl(q, k, v, nullptr, nullptr, &rg, state_pool, pool_dtype, num_slots, state_indices,
+    return recurrent_impl(q, k, v, nullptr, nullptr, &rg, nullptr, state_pool, pool_dtype, num_slots, state_indices,
                           cu_seqlens, N, T_total, Hk, Hv, K, V, scale, dtype, flags, o, intermediate_states, steps,
                           stream, "gdr_recurrent_fwd_gated");
 }

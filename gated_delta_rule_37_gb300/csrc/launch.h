@@ -31,6 +31,11 @@ struct RecurrentArgs {
     const float* A_log = nullptr;
     const float* dt_bias = nullptr;
     float beta_mul = 1.f;
+    // gated RMSNorm epilogue (gdr_recurrent_fwd_norm): o <- rmsnorm(o) * weight
+    // * sigmoid(gate) per value row; norm_weight == nullptr means none
+    const float* norm_weight = nullptr;
+    const void* norm_gate = nullptr;
+    float norm_eps = 0.f;
 };
 
 // Enqueue the recurrent decode / verify kernel.  Returns a cudaError_t.

@@ -41,16 +41,26 @@ struct RecParams {
     const float* A_log;
     const float* dt_bias;
     float beta_mul;
+    const float* nw;  // gated RMSNorm epilogue: weight [V], gate [T, Hv, V], eps
+    const void* nz;
+    float neps;
 };
 
-// kGate: 0 scalar log-decay g [T, Hv]; 1 per-key-channel g [T, Hv, K];
+// kMode & 3: 0 scalar log-decay g [T, Hv]; 1 per-key-channel g [T, Hv, K];
 // 2 gates formed from raw projections (FlashQLA in-kernel gating commit).
+// kMode & 4: gated RMSNorm output epilogue, o <- rmsnorm(o) * w * sigmoid(z)
+// over each value row (tokenspeed PR #834, fused gated-norm commit); the CTA
+// then owns the whole row (BV = V) and sums the squares across its warps.
 
-// At most 128 registers per thread: four 128-thread CTAs per SM keep enough
-// rows in flight (the per-token loop is latency-bound).
-template <typename InT, typename PoolT, int K, int BV, int kGate>
-__global__ void __launch_bounds__(BV / kRowsPerWarp * 32, BV == 64 ? 4 : 1)
+// At most 128 registers per thread: four 128-thread (two 256-thread) CTAs per
+// SM keep enough rows in flight (the per-token loop is latency-bound).
+template <typename InT, typename PoolT, int K, int BV, int kMode>
+__global__ void __launch_bounds__(BV / kRowsPerWarp * 32, BV == 64 ? 4 : BV == 128 ? 2 : 1)
 recurrent_kernel(RecParams p) {
+    constexpr int kGate = kMode & 3;
+    constexpr bool kNorm = (kMode & 4) != 0;
+    constexpr int kWarps = BV / kRowsPerWarp;
+    __shared__ float ssq[2][kWarps];  // per-warp sums of squares, by token parity
     constexpr int KPT = K / 32;  // key channels per lane
     const int b = blockIdx.x;
     const int h = blockIdx.y;
@@ -83,7 +93,10 @@ recurrent_kernel(RecParams p) {
     const InT* __restrict__ gap = static_cast<const InT*>(p.ga);
     const InT* __restrict__ gbp = static_cast<const InT*>(p.gb);
     const float negA = raw ? -expf(p.A_log[h]) : 0.f, dtb = raw ? p.dt_bias[h] : 0.f;
-    float kn[KPT], qn[KPT], gcn[KPT], gn = 0.f, bn = 0.f, vn = 0.f;
+    float kn[KPT], qn[KPT], gcn[KPT], gn = 0.f, bn = 0.f, vn = 0.f, zn = 0.f;
+    const InT* __restrict__ nzp = static_cast<const InT*>(p.nz);
+    const float nwv = kNorm ? p.nw[v0 + (lane & 15)] : 0.f;
+    int par = 0;
     auto load_token = [&](int t) {
         Vec<InT, KPT>::load(kp + ((size_t)t * p.Hk + kh) * K + lane * KPT, kn);
         Vec<InT, KPT>::load(qp + ((size_t)t * p.Hk + kh) * K + lane * KPT, qn);
@@ -91,6 +104,7 @@ recurrent_kernel(RecParams p) {
         else if (!raw) gn = p.g[(size_t)t * p.Hv + h];
         if (!raw) bn = to_f(bp[(size_t)t * p.Hv + h]);
         vn = to_f(vp[((size_t)t * p.Hv + h) * V + v0 + (lane & 15)]);
+        if (kNorm) zn = to_f(nzp[((size_t)t * p.Hv + h) * V + v0 + (lane & 15)]);
     };
     // raw projections: lane j forms the decay and beta of token base + j for the
     // next 32 tokens at once, off the per-token dependency chain; each token
@@ -120,7 +134,7 @@ recurrent_kernel(RecParams p) {
             a = chan ? 1.f : __expf(gn);
             bt = bn;
         }
-        const float vv = vn;
+        const float vv = vn, zz = zn;
         if (t + 1 < eos) load_token(t + 1);
         if (p.flags & 1) {  // GDR_QK_L2NORM
             float sk = 0.f, sq = 0.f;
@@ -158,7 +172,20 @@ recurrent_kernel(RecParams p) {
         const float red = reduce32_to_lane(x, lane);
         const float n_mine = bt * (vv - a * red);  // valid on lanes < 16
         const float n_row = __shfl_sync(0xffffffffu, n_mine, lane & 15);
-        if (lane >= kRowsPerWarp) {
+        if (kNorm) {
+            const float o = lane >= kRowsPerWarp ? p.scale * (a * red + n_row * kq) : 0.f;
+            const float ss = warp_sum(o * o);
+            if (lane == 0) ssq[par][warp] = ss;
+            __syncthreads();
+            float tot = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) tot += ssq[par][w];
+            par ^= 1;
+            const float rinv = rsqrtf(tot / (float)V + p.neps);
+            if (lane >= kRowsPerWarp)
+                op[((size_t)t * p.Hv + h) * V + v0 + (lane - kRowsPerWarp)] =
+                    from_f<InT>(o * rinv * nwv / (1.f + __expf(-zz)));
+        } else if (lane >= kRowsPerWarp) {
             const float o = p.scale * (a * red + n_row * kq);
             op[((size_t)t * p.Hv + h) * V + v0 + (lane - kRowsPerWarp)] = from_f<InT>(o);
         }
@@ -183,6 +210,11 @@ recurrent_kernel(RecParams p) {
 
 template <typename InT, typename PoolT, int K, int kGate>
 cudaError_t launch_k(const RecParams& p, int N, int V, cudaStream_t stream) {
+    if (kGate != 2 && p.nw) {  // gated-norm epilogue: one CTA per (sequence, head), BV = V = K
+        KernelTimer kt("recurrent", stream);
+        recurrent_kernel<InT, PoolT, K, K, kGate | 4><<<dim3(N, p.Hv, 1), K / kRowsPerWarp * 32, 0, stream>>>(p);
+        return cudaGetLastError();
+    }
     // V-column split: 64-row blocks (128 threads) measured best on GB300 for
     // both single-token decode (6.50 vs 6.42 TB/s at 128 rows) and 12-token
     // verify (4.42 vs 4.10 TB/s); 32-row blocks when there are few sequences.
@@ -230,6 +262,7 @@ cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t stream) {
     p.num_slots = a.num_slots;
     p.T = a.T;
     p.ga = a.ga; p.gb = a.gb; p.A_log = a.A_log; p.dt_bias = a.dt_bias; p.beta_mul = a.beta_mul;
+    p.nw = a.norm_weight; p.nz = a.norm_gate; p.neps = a.norm_eps;
     const bool in_bf16 = a.dtype == 0, pool_bf16 = a.pool_dtype == 0;
     if (in_bf16 && pool_bf16) return launch_kt<__nv_bfloat16, __nv_bfloat16>(p, a.N, a.K, a.V, stream);
     if (in_bf16) return launch_kt<__nv_bfloat16, float>(p, a.N, a.K, a.V, stream);

@@ -114,6 +114,7 @@ class PoolCase:
     ibuf_rows: int = 0
     meta: dict = field(default_factory=dict)
     raw: dict | None = None  # raw gate projections a, b [T, Hv], A_log, dt_bias [Hv]
+    norm: dict | None = None  # output epilogue: weight [V] fp32, gate [T, Hv, V], eps
 
     @property
     def N(self):
@@ -226,4 +227,21 @@ def verify_bf16_pool_raw_gates() -> PoolCase:
     case = verify_bf16_pool()
     case.raw = raw_gates(6, case.T, case.v.shape[1])
     case.name = "verify_gated_B64_T1to12_Hk16_Hv32_D128_bf16pool"
+    return case
+
+
+def output_norm(seed: int, T: int, Hv: int, V: int, dtype=torch.bfloat16, eps: float = 1e-6) -> dict:
+    """Inputs of the gated RMSNorm output epilogue: weight ~ U[0.5, 1.5] fp32
+    [V], gate ~ N(0, 1) [T, Hv, V] in the input dtype, eps 1e-6 (our choice;
+    the pages do not state the model's value)."""
+    gen = _gen(seed)
+    return dict(weight=_uniform(gen, (V,), 0.5, 1.5).float(), gate=torch.randn(T, Hv, V, generator=gen).to(dtype),
+                eps=eps)
+
+
+def decode_fp32_pool_norm() -> PoolCase:
+    """The decode workload with the gated RMSNorm output epilogue fused."""
+    case = decode_fp32_pool()
+    case.norm = output_norm(7, case.T, case.v.shape[1], case.v.shape[2])
+    case.name = "decode_norm_B256_Hk16_Hv32_D128_fp32pool"
     return case

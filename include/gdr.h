@@ -179,6 +179,23 @@ GDR_API int gdr_recurrent_fwd(const void* q, const void* k, const void* v, const
                       gdr_stream_t stream);
 
 /*
+ * gdr_recurrent_fwd_norm -- gdr_recurrent_fwd with the gated RMSNorm output
+ * epilogue fused (tokenspeed PR #834, fused gated-norm epilogue commit): every
+ * value row x = o[t,h,:] of the recurrence output is written as
+ *   x / sqrt(mean_v(x^2) + eps) * norm_weight[v] * sigmoid(norm_gate[t,h,v])
+ * norm_weight [V] fp32 device; norm_gate [T_total, Hv, V] dtype device;
+ * eps >= 0.  The normalisation uses the fp32 output before any rounding (one
+ * bf16 round trip fewer than a separate norm kernel).  Every other argument,
+ * flag and guarantee is gdr_recurrent_fwd's.
+ */
+GDR_API int gdr_recurrent_fwd_norm(const void* q, const void* k, const void* v, const float* g,
+                      const void* beta, void* state_pool, int pool_dtype, int num_slots,
+                      const int32_t* state_indices, const int32_t* cu_seqlens, int N,
+                      int64_t T_total, int Hk, int Hv, int K, int V, float scale, int dtype,
+                      int flags, const float* norm_weight, const void* norm_gate, float eps,
+                      void* o, void* intermediate_states, int steps, gdr_stream_t stream);
+
+/*
  * gdr_recurrent_fwd_gated -- gdr_recurrent_fwd with the gates formed inside the
  * kernel from the raw projections (FlashQLA PR #1, in-kernel gating commit):
  *   g[t,h]    = -exp(A_log[h]) * softplus(a[t,h] + dt_bias[h])

@@ -154,6 +154,16 @@ def test_recurrent_fwd_gated_empty_is_ok(lib):
     assert _gated_call(lib, N=0, T=0) == 0
 
 
+def test_recurrent_fwd_norm_rejects_before_launch(lib):
+    P = ctypes.c_void_p
+    base = [P(16), P(32), P(48), P(64), P(80), P(96), 1, 8, P(112), P(128), 4, 4, 2, 4, 128, 128, 0.1, 0, 4]
+    tail = [P(176), None, 0, None]
+    assert lib.gdr_recurrent_fwd_norm(*base, None, P(144), 1e-6, *tail) == 1        # no weight
+    assert lib.gdr_recurrent_fwd_norm(*base, P(160), None, 1e-6, *tail) == 1        # no gate
+    assert lib.gdr_recurrent_fwd_norm(*base, P(160), P(144), -1.0, *tail) == 1      # negative eps
+    assert lib.gdr_recurrent_fwd_norm(*base[:10], 0, 0, *base[12:], P(160), P(144), 1e-6, *tail) == 0  # empty
+
+
 def test_gating_rejects(lib):
     P = ctypes.c_void_p
     assert lib.gdr_gating_fwd(P(16), P(32), P(48), P(64), 4, 0, 0, 0, P(80), P(96), None) == 1

@@ -31,7 +31,13 @@ def run_case(case, *, flags, with_ibuf, gated=False):
         ib_shape = (case.ibuf_rows, case.steps) + tuple(case.pool.shape[1:])
         ib_init = sentinel_like(ib_shape, case.pool.dtype)
         ib = Guarded(ib_shape, case.pool.dtype, dev, fill_bytes=ib_init)
-    if gated:
+    if case.norm is not None:
+        nw, nz = case.norm["weight"].to(dev), case.norm["gate"].to(dev)
+        gdr.recurrent_fwd_norm(case.q.to(dev), case.k.to(dev), case.v.to(dev), case.g.to(dev), case.beta.to(dev),
+                               pool.view, case.state_indices.to(dev), case.cu_seqlens.to(dev), nw, nz,
+                               eps=case.norm["eps"], scale=case.scale, flags=flags, o=o.view,
+                               intermediate_states=ib.view if ib else None)
+    elif gated:
         r = {n: t.to(dev) for n, t in case.raw.items()}
         gdr.recurrent_fwd_gated(case.q.to(dev), case.k.to(dev), case.v.to(dev), r["a"], r["b"], r["A_log"],
                                 r["dt_bias"], pool.view, case.state_indices.to(dev), case.cu_seqlens.to(dev),
@@ -49,6 +55,8 @@ def check_case(case, pool, o, ib, o_init, *, commit):
     ro, rpool, rib = oracle.pool(case.q, case.k, case.v, case.g, case.beta, case.pool, case.state_indices,
                                  case.cu_seqlens, scale=case.scale, commit=commit, steps=case.steps,
                                  ibuf_rows=case.ibuf_rows)
+    if case.norm is not None:  # padding rows of ro stay NaN
+        ro = oracle.gated_rmsnorm(ro, case.norm["weight"], case.norm["gate"], case.norm["eps"])
     cu = case.cu_seqlens.tolist()
     idx = case.state_indices.tolist()
     valid_rows = [b for b in range(case.N) if idx[b] >= 0]
@@ -138,6 +146,28 @@ def test_channel_gate_constant_matches_scalar_gate():
     for b in range(case.N):
         L = cu[b + 1] - cu[b]
         check_state(ib_b.view[b, :L].cpu(), ib_a.view[b, :L].cpu().double().numpy(), f"ibuf row {b}")
+
+
+def test_output_norm_decode_full_size():
+    """Gated RMSNorm output epilogue (tokenspeed PR #834) fused into decode:
+    the decode workload, rows normalised over V, scaled by the weight and the
+    sigmoid of the gate; padding rows untouched."""
+    case = workloads.decode_fp32_pool_norm()
+    pool, o, ib, o_init = run_case(case, flags=gdr.GDR_COMMIT, with_ibuf=False)
+    check_case(case, pool, o, ib, o_init, commit=True)
+
+
+@pytest.mark.parametrize("K", [64, 128])
+@pytest.mark.parametrize("channel", [False, True])
+def test_output_norm_small_cases(K, channel):
+    """Ragged verify with the epilogue: per-token states, commit, padding,
+    scalar or per-channel gates."""
+    lens = [1, 5, 0, 9]
+    case = workloads.pool_case(61 + K, lens, 2, 4, K, K, 6, pool_dtype=torch.bfloat16, pad_count=1, commit=True,
+                               steps=9, ibuf_rows=4, channel_gate=channel)
+    case.norm = workloads.output_norm(62, case.T, 4, K, eps=1e-4)
+    pool, o, ib, o_init = run_case(case, flags=gdr.GDR_COMMIT, with_ibuf=True)
+    check_case(case, pool, o, ib, o_init, commit=True)
 
 
 def _with_oracle_gates(case, neg_eigval=False):
