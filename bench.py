@@ -126,21 +126,24 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 
 
 def ncu_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu record, or None
-    when there is no record for this workload or the kernel's source changed
-    since the counters were taken."""
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    record (one record or a list of records per kernel), or None when there is
+    no record for this workload or the kernel's source changed since the
+    counters were taken."""
     import hashlib
     try:
-        rec = json.load(open(TRAFFIC_FILE))[kernel]
+        recs = json.load(open(TRAFFIC_FILE))[kernel]
     except (OSError, KeyError, ValueError):
         return None
-    if rec.get("workload") != workload:
-        return None
-    try:
-        sha = hashlib.sha256(open(os.path.join(ROOT, rec["source"]), "rb").read()).hexdigest()
-    except OSError:
-        return None
-    return rec["dram_bytes_per_launch"] if sha == rec.get("source_sha256") else None
+    for rec in recs if isinstance(recs, list) else [recs]:
+        if rec.get("workload") != workload:
+            continue
+        try:
+            sha = hashlib.sha256(open(os.path.join(ROOT, rec["source"]), "rb").read()).hexdigest()
+        except OSError:
+            return None
+        return rec["dram_bytes_per_launch"] if sha == rec.get("source_sha256") else None
+    return None
 
 
 def load_peaks():

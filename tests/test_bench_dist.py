@@ -60,3 +60,21 @@ def test_traffic_record_is_ignored_when_source_changes(tmp_path, monkeypatch):
     assert bench.ncu_traffic("chunk_chain", "other") is None
     src.write_text("kernel v2")
     assert bench.ncu_traffic("chunk_chain", "w") is None
+
+
+def test_traffic_record_list_per_kernel(tmp_path, monkeypatch):
+    import hashlib
+    import json
+    import bench
+    src = tmp_path / "r.cu"
+    src.write_text("recurrent v1")
+    sha = hashlib.sha256(b"recurrent v1").hexdigest()
+    rec = {"recurrent": [{"workload": "decode", "source": str(src), "dram_bytes_per_launch": 9, "source_sha256": sha},
+                         {"workload": "verify", "source": str(src), "dram_bytes_per_launch": 5, "source_sha256": sha}]}
+    f = tmp_path / "t.json"
+    f.write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    monkeypatch.setattr(bench, "ROOT", "/")
+    assert bench.ncu_traffic("recurrent", "decode") == 9
+    assert bench.ncu_traffic("recurrent", "verify") == 5
+    assert bench.ncu_traffic("recurrent", "kda") is None
