@@ -32,7 +32,8 @@ STATUS = {0: "GDR_OK", 1: "GDR_ERR_INVALID_ARG", 2: "GDR_ERR_UNSUPPORTED", 3: "G
 # every symbol include/gdr.h declares
 EXPORTED = ("gdr_chunk_workspace_size", "gdr_chunk_fwd", "gdr_chunk_fwd_noalloc", "gdr_recurrent_fwd",
             "gdr_recurrent_fwd_gated", "gdr_recurrent_fwd_norm", "gdr_gating_fwd",
-            "gdr_last_error", "gdr_get_device_status", "gdr_profile_enable", "gdr_profile_read",
+            "gdr_last_error", "gdr_get_device_status", "gdr_selftest_bounded_wait", "gdr_profile_enable",
+            "gdr_profile_read",
             "gdr_version")
 
 _lib = None
@@ -73,6 +74,8 @@ def load(path: str | None = None):
     lib.gdr_last_error.restype = ctypes.c_char_p
     lib.gdr_get_device_status.argtypes = [P, ctypes.POINTER(I)]
     lib.gdr_get_device_status.restype = I
+    lib.gdr_selftest_bounded_wait.argtypes = [P]
+    lib.gdr_selftest_bounded_wait.restype = I
     lib.gdr_profile_enable.argtypes = [I]
     lib.gdr_profile_enable.restype = I
     lib.gdr_profile_read.argtypes = [I, ctypes.c_char_p, SZ, ctypes.POINTER(ctypes.c_double),

@@ -238,6 +238,17 @@ GDR_API const char* gdr_last_error(void);
 GDR_API int gdr_get_device_status(gdr_stream_t stream, int* word);
 
 /*
+ * gdr_selftest_bounded_wait -- diagnostic for the failure path (no counterpart
+ * on the pages): enqueues on `stream` one small kernel that waits on an
+ * mbarrier nothing ever completes, using the same bounded wait as the
+ * tensor-core kernels (about one second of %globaltimer); it then sets bit
+ * 0x100 of the device error word and returns.  A following
+ * gdr_get_device_status reports GDR_ERR_DEVICE_TIMEOUT, and the context stays
+ * usable.  Nothing faults, traps or spins without a limit.
+ */
+GDR_API int gdr_selftest_bounded_wait(gdr_stream_t stream);
+
+/*
  * Kernel timing for diagnostics (no counterpart on the pages; measurement
  * support).  gdr_profile_enable(1): from then on every kernel the library
  * launches is bracketed by two CUDA events on its stream (not capturable:
