@@ -45,11 +45,15 @@ L2_FLUSH_BYTES = 256 << 20
 #   chunk_prep  : K K^T, Q K^T, Tm K (each C*K, triangular) + Tm V (C*V)
 #   chunk_chain : W S^T, state update, Q S^T (2*K*V each) + P N (C*V)
 # fp32 / D = 64 path: chunk_intra as chunk_prep; chunk_state 4KV; chunk_out 2KV + CV.
+# Chunk-parallel scan (GDR_CHUNK_SCAN): chunk_chain_summary forms each
+# segment's transition (K columns) and offset (V columns), W S^T and the state
+# update for each: 4K(K + V); chunk_seg_scan is fp32 CUDA-core work (not counted).
 # Each split sums to 6KV + 3CK + 2CV = 139,264 flop at K = V = 128.
 
 
 def kernel_flops_per_token_head(name, K, V, C=64):
     return {"chunk_prep": 3 * C * K + C * V, "chunk_chain": 6 * K * V + C * V,
+            "chunk_chain_summary": 4 * K * (K + V), "chunk_seg_scan": 0,
             "chunk_intra": 3 * C * K + C * V, "chunk_state": 4 * K * V, "chunk_out": 2 * K * V + C * V}.get(name)
 
 
@@ -252,8 +256,9 @@ def roofline(prof, steps, work_per_kernel, peaks, bound_of, workload=""):
 # prefill
 # ---------------------------------------------------------------------------
 class Prefill:
-    def __init__(self, case, dev):
+    def __init__(self, case, dev, flags=0):
         self.case = case
+        self.flags = flags
         c = case
         self.dev = dev
         self.q, self.k, self.v, self.beta = (t.to(dev) for t in (c.q, c.k, c.v, c.beta))
@@ -267,11 +272,13 @@ class Prefill:
         gk_kind = gdr.GDR_GATE_SCALAR if c.g is not None else gdr.GDR_GATE_CHANNEL
         dt = gdr.GDR_BF16 if c.q.dtype == torch.bfloat16 else gdr.GDR_F32
         self.ws = torch.empty(gdr.chunk_workspace_size(c.N, c.T, d["Hk"], d["Hv"], d["K"], d["V"],
-                                                       gate_kind=gk_kind, dtype=dt), dtype=torch.uint8, device=dev)
+                                                       gate_kind=gk_kind, dtype=dt, flags=flags),
+                              dtype=torch.uint8, device=dev)
 
     def step(self, stream=None):
         gdr.chunk_fwd(self.q, self.k, self.v, self.beta, self.cu, g=self.g, gk=self.gk, initial_state=self.h0,
-                      scale=self.case.scale, o=self.o, final_state=self.hT, workspace=self.ws, stream=stream)
+                      scale=self.case.scale, flags=self.flags, o=self.o, final_state=self.hT, workspace=self.ws,
+                      stream=stream)
 
     def e2e(self, K, stream):
         """The same call through the public API from pinned host buffers: every
@@ -465,7 +472,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", help="comma list of sections: prefill,decode,verify,kda,kda_decode,"
-                                               "verify_gated,decode_norm")
+                                               "verify_gated,decode_norm,long_scan")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -487,7 +494,7 @@ def main():
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush = lambda: flush_buf.fill_(1)
     only = set(filter(None, args.only.split(","))) or {"prefill", "decode", "verify", "kda", "kda_decode",
-                                                        "verify_gated", "decode_norm"}
+                                                        "verify_gated", "decode_norm", "long_scan"}
 
     dist_ = Dist(world, dev)
 
@@ -513,6 +520,11 @@ def main():
         ver = PoolRun(workloads.verify_bf16_pool(), dev)
     if "kda" in only:
         kda = Prefill(workloads.kda_long_prefill(), dev)
+    lsc = lpl = None
+    if "long_scan" in only:
+        long_case = workloads.long_few_heads_prefill()
+        lsc = Prefill(long_case, dev, flags=gdr.GDR_CHUNK_SCAN)
+        lpl = Prefill(long_case, dev)
     for _ in range(args.warmup):
         pre.step(stream)
     torch.cuda.synchronize()
@@ -588,6 +600,30 @@ def main():
                              "whole_call": {"tflops": round(kf / (k_ms / 1e3) / 1e12, 3),
                                             "gbs": round(kb / (k_ms / 1e3) / 1e9, 2),
                                             "frac_hbm": round(kb / (k_ms / 1e3) / 1e9 / peaks["hbm"], 5)}}
+    if lsc is not None:
+        # the long few-head sequence with the chunk-parallel scan, and the
+        # one-pass chain on the same inputs for comparison
+        nst = max(5, args.steps // 5)
+        ls_ms, ls_prof, ls_roof, _ = measure(lsc, nst, args.warmup, flush, stream, prefill_work_fn(lsc.case),
+                                             lambda n: "tensor", peaks, lsc.case.T)
+        lp_ms, lp_prof, _, _ = measure(lpl, nst, args.warmup, flush, stream, prefill_work_fn(lpl.case),
+                                       lambda n: "tensor", peaks, lpl.case.T)
+        launches += sum(v[1] for v in ls_prof.values()) + sum(v[1] for v in lp_prof.values())
+        ls_ms, lp_ms = max_over_ranks(ls_ms), max_over_ranks(lp_ms)
+        d = lsc.case.dims
+        lf = prefill_flops(lsc.case.T, d["Hv"], d["K"], d["V"])
+        extra["long_scan"] = {
+            "workload": lsc.case.name, "flags": "GDR_CHUNK_SCAN",
+            "tokens_per_s": round(world * lsc.case.T / (ls_ms / 1e3), 1), "ms_per_step": round(ls_ms, 4),
+            "one_pass_chain": {"tokens_per_s": round(world * lpl.case.T / (lp_ms / 1e3), 1),
+                               "ms_per_step": round(lp_ms, 4),
+                               "time_share": {k: round(v[0] / sum(x[0] for x in lp_prof.values()), 4)
+                                              for k, v in lp_prof.items()}},
+            "speedup_vs_one_pass": round(lp_ms / ls_ms, 3),
+            "kernel_ms": {k: round(v[0] / v[1], 4) for k, v in ls_prof.items()},
+            "whole_call": {"tflops": round(lf / (ls_ms / 1e3) / 1e12, 3),
+                           "frac_bf16": round(lf / (ls_ms / 1e3) / 1e12 / peaks["bf16"], 5)},
+            "roofline": ls_roof}
     clocks = sampler.stop()
 
     # end to end through the public API from pinned host buffers

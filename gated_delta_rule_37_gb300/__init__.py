@@ -24,6 +24,7 @@ LIB_PATH = os.path.join(_PKG, "libgdr.so")
 GDR_BF16, GDR_F32 = 0, 1
 GDR_GATE_SCALAR, GDR_GATE_CHANNEL = 0, 1
 GDR_QK_L2NORM, GDR_NEG_EIGVAL, GDR_COMMIT, GDR_VALIDATE, GDR_CHANNEL_GATE = 0x1, 0x2, 0x4, 0x8, 0x10
+GDR_CHUNK_SCAN = 0x20
 CHUNK = 64
 
 STATUS = {0: "GDR_OK", 1: "GDR_ERR_INVALID_ARG", 2: "GDR_ERR_UNSUPPORTED", 3: "GDR_ERR_WORKSPACE",

@@ -165,7 +165,7 @@ int gdr_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
                   void* o, float* final_state, void* workspace, size_t ws_bytes,
                   gdr_stream_t stream) {
     if (int rc = check_common(N, T_total, Hk, Hv, K, V, dtype)) return rc;
-    if (flags & ~(GDR_QK_L2NORM | GDR_VALIDATE))
+    if (flags & ~(GDR_QK_L2NORM | GDR_VALIDATE | GDR_CHUNK_SCAN))
         return fail(GDR_ERR_INVALID_ARG, "unsupported flags 0x%x for gdr_chunk_fwd", flags);
     if ((g == nullptr) == (gk == nullptr))
         return fail(GDR_ERR_INVALID_ARG, "exactly one of g / gk must be given");
@@ -191,6 +191,8 @@ int gdr_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
         return fail(GDR_ERR_INVALID_ARG, "workspace not 256-byte aligned");
     const ChunkWorkspace w = chunk_workspace_layout(N, T_total, Hk, Hv, K, V, g ? 0 : 1, dtype, flags);
     if (w.tc && N > 65535) return fail(GDR_ERR_UNSUPPORTED, "N (%d) above 65535 sequences per call", N);
+    if (w.seg_chunks > 0 && w.max_segs > 65535)
+        return fail(GDR_ERR_UNSUPPORTED, "GDR_CHUNK_SCAN: segment capacity %lld above 65535", (long long)w.max_segs);
     if (ws_bytes < w.total)
         return fail(GDR_ERR_WORKSPACE, "workspace %zu bytes < required %zu", ws_bytes, w.total);
     if (w.max_chunks > 0x7fffffffLL) return fail(GDR_ERR_UNSUPPORTED, "too many chunks");

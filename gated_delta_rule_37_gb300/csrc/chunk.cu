@@ -27,6 +27,13 @@ namespace gdr {
 
 static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
+int chunk_scan_segment(int64_t T, int Hv) {
+    const int64_t nc = (T + kChunk - 1) / kChunk;
+    const int64_t segs = Hv >= 38 ? 1 : 38 / Hv;
+    const int64_t g = (nc + segs - 1) / segs;
+    return (int)(g < 8 ? 8 : g > (1 << 30) ? (1 << 30) : g);
+}
+
 ChunkWorkspace chunk_workspace_layout(int N, int64_t T, int Hk, int Hv, int K, int V, int gate_kind,
                                       int dtype, int flags) {
     ChunkWorkspace w{};
@@ -45,6 +52,14 @@ ChunkWorkspace chunk_workspace_layout(int N, int64_t T, int Hk, int Hv, int K, i
     if (w.tc) {
         // tensor-core path: pre-swizzled per-chunk operand images only
         w.off_blobs = take(chunk_tc_blob_bytes(w.max_chunks, Hk, Hv, gate_kind == 1));
+        if (flags & 0x20) {  // GDR_CHUNK_SCAN
+            w.seg_chunks = chunk_scan_segment(T, Hv);
+            w.max_segs = (w.max_chunks + w.seg_chunks - 1) / w.seg_chunks + N;
+            w.off_segs = take(16 * (size_t)w.max_segs);
+            w.off_segoff = take(sizeof(int) * (size_t)(N + 1));
+            w.off_mt = take(4 * (size_t)w.max_segs * Hv * K * K);
+            w.off_bs = take(4 * (size_t)w.max_segs * Hv * V * K);
+        }
         w.total = off;
         return w;
     }
@@ -70,11 +85,18 @@ namespace {
 // Also writes order[]: sequence indices by decreasing length (ties by index),
 // the longest-first launch order of the per-sequence kernels (N <= 4096;
 // identity beyond).
+// With G > 0 (chunk-parallel scan) it also cuts every sequence into segments
+// of G chunks (the last one shorter): segs[] = (sequence, first chunk within
+// the sequence, chunk count, 1 if it is the sequence's last segment),
+// segoff[b] = first segment of sequence b, meta[2] = the segment count.
 __global__ void __launch_bounds__(1024) chunk_meta_kernel(const int32_t* __restrict__ cu, int N,
                                                           int64_t T, int* __restrict__ meta,
                                                           int* __restrict__ offsets,
-                                                          int4* __restrict__ table, int* __restrict__ order) {
+                                                          int4* __restrict__ table, int* __restrict__ order,
+                                                          int G, int4* __restrict__ segs,
+                                                          int* __restrict__ segoff) {
     __shared__ int warp_sum[32];
+    __shared__ int seg_sum[32];
     __shared__ int bad;
     // the next kernel, if launched as a dependent, may start its prologue now
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -98,7 +120,7 @@ __global__ void __launch_bounds__(1024) chunk_meta_kernel(const int32_t* __restr
     if (lane == 31) warp_sum[wid] = incl;
     __syncthreads();
     if (bad) {
-        if (tid == 0) { meta[0] = 0; meta[1] = 0; }
+        if (tid == 0) { meta[0] = 0; meta[1] = 0; meta[2] = 0; }
         return;
     }
     if (wid == 0) {
@@ -122,6 +144,42 @@ __global__ void __launch_bounds__(1024) chunk_meta_kernel(const int32_t* __restr
         const int bos = cu[b], len = cu[b + 1] - bos;
         for (int s = 0; s < len; s += kChunk, ++c)
             table[c] = make_int4(b, bos + s, min(kChunk, len - s), 0);
+    }
+    if (G > 0) {
+        // the same block-wide exclusive scan over the per-thread segment counts
+        int scnt = 0;
+        for (int b = b0; b < b1; ++b) {
+            const int nc = (cu[b + 1] - cu[b] + kChunk - 1) / kChunk;
+            scnt += (nc + G - 1) / G;
+        }
+        int sincl = scnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, sincl, off);
+            if (lane >= off) sincl += y;
+        }
+        if (lane == 31) seg_sum[wid] = sincl;
+        __syncthreads();
+        if (wid == 0) {
+            int v = seg_sum[lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, v, off);
+                if (lane >= off) v += y;
+            }
+            seg_sum[lane] = v;
+        }
+        __syncthreads();
+        int sg = sincl - scnt + (wid > 0 ? seg_sum[wid - 1] : 0);
+        if (tid == 0) {
+            meta[2] = seg_sum[31];
+            segoff[N] = seg_sum[31];
+        }
+        for (int b = b0; b < b1; ++b) {
+            segoff[b] = sg;
+            const int nc = (cu[b + 1] - cu[b] + kChunk - 1) / kChunk;
+            for (int s = 0; s < nc; s += G, ++sg) segs[sg] = make_int4(b, s, min(G, nc - s), s + G >= nc);
+        }
     }
     for (int b = tid; b < N; b += blockDim.x) {
         const int lb = cu[b + 1] - cu[b];
@@ -424,7 +482,9 @@ cudaError_t launch_chunk_t(const ChunkArgs& a, cudaStream_t stream) {
         chunk_meta_kernel<<<1, 1024, 0, stream>>>(a.cu_seqlens, a.N, a.T, reinterpret_cast<int*>(ws + w.off_meta),
                                                   reinterpret_cast<int*>(ws + w.off_offsets),
                                                   reinterpret_cast<int4*>(ws + w.off_table),
-                                                  reinterpret_cast<int*>(ws + w.off_order));
+                                                  reinterpret_cast<int*>(ws + w.off_order), w.seg_chunks,
+                                                  reinterpret_cast<int4*>(ws + w.off_segs),
+                                                  reinterpret_cast<int*>(ws + w.off_segoff));
     }
     if (a.flags & 1) {
         const int64_t rows = a.T * a.Hk;

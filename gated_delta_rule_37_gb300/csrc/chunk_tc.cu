@@ -125,6 +125,15 @@ struct TcParams {
     unsigned int* err;
     int N, Hk, Hv;
     float scale;
+    // chunk-parallel scan: mode 0 = one chain CTA runs a whole sequence;
+    // 1 = segment summaries (transition Mt from the identity with U = 0, offset
+    // Bs from zero), no output; 2 = segments from the scanned start states in Bs,
+    // with output
+    int mode;
+    const int4* segs;    // (sequence, first chunk in sequence, chunks, last?)
+    const int* segoff;   // [N + 1] first segment of each sequence
+    float* Mt;           // [segment][Hv][128][128]: Mt[m][k] = P[m][k]
+    float* Bs;           // [segment][Hv][128 (v)][128 (k)]
 };
 
 __device__ __forceinline__ void raise_error(const TcParams& p, unsigned code) {
@@ -874,11 +883,31 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
         if (warp == 2) tc::tmem_dealloc(tmem, 256);
         return;
     }
-    const int h = blockIdx.x / NVB, vb = blockIdx.x % NVB, v0 = vb * BV;
-    const int b = p.order[blockIdx.y];
-    const int bos = p.cu[b], eos = p.cu[b + 1];
-    const int nc = (eos - bos + C - 1) / C;
-    const int c0 = p.offsets[b];
+    // Work unit: a whole sequence (mode 0) or one segment of G chunks of it
+    // (modes 1 and 2; the summary pass runs two CTA sets, the transition from
+    // the identity with U = 0 and the offset from zero).
+    const int hx = blockIdx.x % (p.Hv * NVB);
+    const bool transition = p.mode == 1 && blockIdx.x >= p.Hv * NVB;
+    const int h = hx / NVB, vb = hx % NVB, v0 = vb * BV;
+    int b, nc, c0, cs0 = 0, sg = 0;
+    bool last = true;
+    if (p.mode == 0) {
+        b = p.order[blockIdx.y];
+        nc = (p.cu[b + 1] - p.cu[b] + C - 1) / C;
+        c0 = p.offsets[b];
+    } else {
+        sg = blockIdx.y;
+        if (sg >= p.meta[2]) {  // beyond this call's segment count
+            tc::fence_before();
+            __syncthreads();
+            if (warp == 2) tc::tmem_dealloc(tmem, 256);
+            return;
+        }
+        const int4 e = p.segs[sg];
+        b = e.x; cs0 = e.y; nc = e.z; last = e.w != 0;
+        c0 = p.offsets[b] + cs0;
+    }
+    const int bos = p.cu[b] + cs0 * C, eos = p.cu[b + 1];
     const int kh = h / (p.Hv / p.Hk);
     // Accumulators (fp32 TMEM columns).  The hi and lo split terms of the state
     // (or of N') sit side by side along N, so one N = 64 MMA forms two split
@@ -962,7 +991,13 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
         constexpr uint32_t a64[4] = {0, 2, 4, 6};                  // 128-row k128, K = 64 (column block 0)
         constexpr uint32_t amn[4] = {0, 128, 256, 384};            // MN-major A: 2 x 8-row groups per step
         float Sreg[16];
-        if (p.h0) {
+        if (p.mode == 2) {  // scanned start state of the segment
+#pragma unroll
+            for (int v = 0; v < 16; ++v) Sreg[v] = p.Bs[(((size_t)sg * p.Hv + h) * D + v0 + vh + v) * D + t];
+        } else if (transition) {  // identity: column v0 + vh + v of I
+#pragma unroll
+            for (int v = 0; v < 16; ++v) Sreg[v] = (v0 + vh + v == t) ? 1.f : 0.f;
+        } else if (p.h0 && p.mode == 0) {
 #pragma unroll
             for (int v = 0; v < 16; ++v) Sreg[v] = p.h0[(((size_t)b * p.Hv + h) * D + v0 + vh + v) * D + t];
         } else {
@@ -1019,7 +1054,7 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             if (nrow) {
                 const float* ucol = reinterpret_cast<const float*>(stg + S::kU) + (size_t)vh * C + i;
 #pragma unroll
-                for (int v = 0; v < 16; ++v) uv[v] = ucol[(size_t)v * C];
+                for (int v = 0; v < 16; ++v) uv[v] = transition ? 0.f : ucol[(size_t)v * C];  // transition: U = 0
             }
             // N = U - W S^T  ->  N' = rowf * N (hi, lo), N (bf16, masked)
             if (!tc::mbar_wait(bar(kD1Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
@@ -1100,7 +1135,11 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             tc::mma_commit(bar(dr));
             tc::mbar_wait(bar(dr), 0, abort_flag);
         }
-        if (p.hT && !*abort_flag) {
+        if (p.mode == 1 && !*abort_flag) {  // segment summary
+            float* dst = (transition ? p.Mt : p.Bs) + (((size_t)sg * p.Hv + h) * D + v0 + vh) * D + t;
+#pragma unroll
+            for (int v = 0; v < 16; ++v) dst[(size_t)v * D] = Sreg[v];
+        } else if (p.hT && last && !*abort_flag) {
 #pragma unroll
             for (int v = 0; v < 16; ++v) p.hT[(((size_t)b * p.Hv + h) * D + v0 + vh + v) * D + t] = Sreg[v];
         }
@@ -1118,7 +1157,7 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             if (!tc::mbar_wait(bar(kOFull0 + ob), (c >> 1) & 1, abort_flag)) fail();
             if (tid == 384) GDR_TRACE_POINT(13, c);
             tc::fence_after();
-            if (drain) {
+            if (drain && p.mode != 1) {
                 float ov[BV], ld[2 * BV];
                 tc::tmem_ld64(tD1 + 64 * ob + lane_base, ld);
 #pragma unroll
@@ -1145,6 +1184,86 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
     tc::fence_before();
     __syncthreads();
     if (warp == 2) tc::tmem_dealloc(tmem, 256);
+}
+
+// ---------------------------------------------------------------------------
+// segment scan (chunk-parallel mode)
+// ---------------------------------------------------------------------------
+// The state map of a run of chunks is affine in its start state: with S in
+// the [V][K] layout, S_end = S_start P + B, P the run from the identity with
+// U = 0 and B the run from zero (the summary chain pass writes both).  This
+// kernel composes them in order, in fp32:
+//   S_start(0) = h0 (or 0),   S_start(j + 1) = S_start(j) P_j + B_j,
+// writing S_start(j) over B_j (each thread reads its own elements of B_j
+// before it writes them).  One CTA per (value head, 8 value rows, sequence);
+// thread (k, hf) keeps rows 4 hf .. 4 hf + 3 of column k in registers and the
+// CTA's rows transposed in shared memory; P_j is staged whole in shared memory
+// with cp.async, the next one in flight while the current one is used.
+constexpr int kScanRows = 8;
+constexpr int kScanThreads = 256;
+constexpr uint32_t kScanSmem = 2 * D * D * 4;  // two P buffers
+
+__global__ void __launch_bounds__(kScanThreads) chunk_seg_scan_kernel(TcParams p) {
+    extern __shared__ float4 scan_smem[];
+    float* Ps = reinterpret_cast<float*>(scan_smem);
+    __shared__ float4 Xs[D][kScanRows / 4];  // [k][rows 0..3 | rows 4..7]
+    const int tid = threadIdx.x, k = tid & (D - 1), hf = tid >> 7;
+    const int h = blockIdx.x / (D / kScanRows), r0 = (blockIdx.x % (D / kScanRows)) * kScanRows + 4 * hf;
+    const int b = blockIdx.y;
+    tc::grid_dep_wait();    // the segment summaries come from the chain kernel
+    tc::grid_dep_launch();  // the output pass may start its prologue
+    if (!p.meta[1]) return;
+    const int sg0 = p.segoff[b], ns = p.segoff[b + 1] - sg0;
+    float x[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) x[r] = p.h0 ? p.h0[(((size_t)b * p.Hv + h) * D + r0 + r) * D + k] : 0.f;
+    if (ns == 0) {  // no chunks: the final state is the start state
+        if (p.hT) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) p.hT[(((size_t)b * p.Hv + h) * D + r0 + r) * D + k] = x[r];
+        }
+        return;
+    }
+    Xs[k][hf] = make_float4(x[0], x[1], x[2], x[3]);
+    auto stage = [&](int j) {
+        const char* src = reinterpret_cast<const char*>(p.Mt + ((size_t)(sg0 + j) * p.Hv + h) * D * D);
+        const uint32_t dst = tc::smem_u32(Ps + (j & 1) * D * D);
+        for (int e = tid; e < D * D / 4; e += kScanThreads)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst + 16 * e), "l"(src + 16 * e) : "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    if (ns > 1) stage(0);
+    for (int j = 0; j < ns; ++j) {
+        float* bj = p.Bs + ((size_t)(sg0 + j) * p.Hv + h) * D * D + (size_t)r0 * D + k;
+        float acc[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            acc[r] = bj[(size_t)r * D];
+            bj[(size_t)r * D] = x[r];  // the start state of segment j
+        }
+        if (j == ns - 1) break;
+        if (j + 2 < ns) {
+            stage(j + 1);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();  // P_j and the start state of segment j are visible
+        const float* P = Ps + (j & 1) * D * D + k;
+#pragma unroll 8
+        for (int m = 0; m < D; ++m) {
+            const float pm = P[m * D];
+            const float4 xm = Xs[m][hf];
+            acc[0] = fmaf(xm.x, pm, acc[0]);
+            acc[1] = fmaf(xm.y, pm, acc[1]);
+            acc[2] = fmaf(xm.z, pm, acc[2]);
+            acc[3] = fmaf(xm.w, pm, acc[3]);
+        }
+        __syncthreads();  // every read of the old start state (and of P_j) is done
+        Xs[k][hf] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) x[r] = acc[r];
+    }
 }
 
 }  // namespace
@@ -1190,35 +1309,50 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* w
     p.err = device_error_word();
     p.N = a.N; p.Hk = a.Hk; p.Hv = a.Hv; p.scale = a.scale;
 
-    if (kda) {
-        const int smp = PrepSmem<true>::kTotal, smc = ChainSmem<true>::kTotal;
-        cudaFuncSetAttribute(chunk_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smp);
-        cudaFuncSetAttribute(chunk_chain_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smc);
+    if (w.seg_chunks > 0) {
+        p.segs = reinterpret_cast<const int4*>(ws + w.off_segs);
+        p.segoff = reinterpret_cast<const int*>(ws + w.off_segoff);
+        p.Mt = reinterpret_cast<float*>(ws + w.off_mt);
+        p.Bs = reinterpret_cast<float*>(ws + w.off_bs);
+    }
+    auto run = [&](auto prep_kernel, auto chain_kernel, int smp, int smc, int prep_per_sm) -> cudaError_t {
+        cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smp);
+        cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smc);
         {
             KernelTimer kt("chunk_prep", stream);
-            const cudaError_t e = launch_dependent(chunk_prep_kernel<true>, dim3(prep_grid(mc * a.Hv, 1)), dim3(kPrepThreads),
-                                                   (size_t)smp, stream, p);
-            if (e != cudaSuccess) return e;
-        }
-        KernelTimer kt("chunk_chain", stream);
-        const cudaError_t e = launch_dependent(chunk_chain_kernel<true>, dim3(a.Hv * NVB, a.N), dim3(512), (size_t)smc,
-                                               stream, p);
-        if (e != cudaSuccess) return e;
-    } else {
-        const int smp = PrepSmem<false>::kTotal, smc = ChainSmem<false>::kTotal;
-        cudaFuncSetAttribute(chunk_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smp);
-        cudaFuncSetAttribute(chunk_chain_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smc);
-        {
-            KernelTimer kt("chunk_prep", stream);
-            const cudaError_t e = launch_dependent(chunk_prep_kernel<false>, dim3(prep_grid(mc * a.Hv, 2)),
+            const cudaError_t e = launch_dependent(prep_kernel, dim3(prep_grid(mc * a.Hv, prep_per_sm)),
                                                    dim3(kPrepThreads), (size_t)smp, stream, p);
             if (e != cudaSuccess) return e;
         }
+        if (w.seg_chunks == 0) {
+            p.mode = 0;
+            KernelTimer kt("chunk_chain", stream);
+            return launch_dependent(chain_kernel, dim3(a.Hv * NVB, a.N), dim3(512), (size_t)smc, stream, p);
+        }
+        const unsigned segs = (unsigned)w.max_segs;
+        {
+            p.mode = 1;  // segment transitions and offsets
+            KernelTimer kt("chunk_chain_summary", stream);
+            const cudaError_t e = launch_dependent(chain_kernel, dim3(2 * a.Hv * NVB, segs), dim3(512), (size_t)smc,
+                                                   stream, p);
+            if (e != cudaSuccess) return e;
+        }
+        {
+            cudaFuncSetAttribute(chunk_seg_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem);
+            KernelTimer kt("chunk_seg_scan", stream);
+            const cudaError_t e = launch_dependent(chunk_seg_scan_kernel, dim3(a.Hv * (D / kScanRows), a.N),
+                                                   dim3(kScanThreads), (size_t)kScanSmem, stream, p);
+            if (e != cudaSuccess) return e;
+        }
+        p.mode = 2;  // segments from their start states, with the output
         KernelTimer kt("chunk_chain", stream);
-        const cudaError_t e = launch_dependent(chunk_chain_kernel<false>, dim3(a.Hv * NVB, a.N), dim3(512), (size_t)smc,
-                                               stream, p);
-        if (e != cudaSuccess) return e;
-    }
+        return launch_dependent(chain_kernel, dim3(a.Hv * NVB, segs), dim3(512), (size_t)smc, stream, p);
+    };
+    const cudaError_t e = kda ? run(chunk_prep_kernel<true>, chunk_chain_kernel<true>, PrepSmem<true>::kTotal,
+                                    ChainSmem<true>::kTotal, 1)
+                              : run(chunk_prep_kernel<false>, chunk_chain_kernel<false>, PrepSmem<false>::kTotal,
+                                    ChainSmem<false>::kTotal, 2);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -75,8 +75,20 @@ struct ChunkWorkspace {
     size_t off_order;     // int [N]: sequences by decreasing length
     size_t off_blobs;     // tensor-core path operand images
     bool tc;              // tensor-core path (bf16, K = V = 128)
+    // chunk-parallel scan (GDR_CHUNK_SCAN on the tensor-core path)
+    int seg_chunks;       // segment length G in chunks; 0 = scan off
+    int64_t max_segs;     // segment capacity: ceil(max_chunks / G) + N
+    size_t off_segs;      // int4 [max_segs]: (seq, first chunk in seq, chunks, last?)
+    size_t off_segoff;    // int [N+1]: first segment of each sequence
+    size_t off_mt;        // fp32 [max_segs, Hv, K, K]: segment transition P
+    size_t off_bs;        // fp32 [max_segs, Hv, V, K]: segment offset B, then start state
     size_t total;
 };
+
+// Segment length (chunks) of the chunk-parallel scan: about 38 / Hv segments
+// per sequence of ceil(T / 64) chunks, so that the summary pass (8 Hv CTAs
+// per segment) is near two waves of a 152-SM GPU; never below 8 chunks.
+int chunk_scan_segment(int64_t T, int Hv);
 
 ChunkWorkspace chunk_workspace_layout(int N, int64_t T, int Hk, int Hv, int K, int V, int gate_kind,
                                       int dtype, int flags);

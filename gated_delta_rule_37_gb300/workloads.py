@@ -179,6 +179,14 @@ def kda_long_prefill(T: int = 32768) -> ChunkCase:
                       g_range=(-0.1, 0.0), name=f"kda_bf16_T{T}_Hk16_Hv32_D128")
 
 
+def long_few_heads_prefill(T: int = 32768, Hv: int = 4) -> ChunkCase:
+    """1 sequence T=32768 with few heads (Hk = Hv = 4, one tensor-parallel
+    eighth of a 32-head layer), K=V=128, bf16, g ~ U[-0.1,0] (the long-context
+    decay range), h0 ~ N(0,0.1): the shape the chunk-parallel scan is for."""
+    return chunk_case(8, [T], Hv, Hv, 128, 128, dtype=torch.bfloat16, gate="g",
+                      g_range=(-0.1, 0.0), h0_std=0.1, name=f"long_gdn_bf16_T{T}_H{Hv}_D128")
+
+
 def decode_fp32_pool() -> PoolCase:
     """256 single-token sequences, Hk=16, Hv=32, K=V=128, fp32 pool of 513 slots,
     26 of 256 indices padding, committed in place."""

@@ -75,6 +75,7 @@ typedef enum gdr_gate_kind {
 #define GDR_COMMIT     0x4 /* gdr_recurrent_fwd: write the final state back to the pool     */
 #define GDR_VALIDATE   0x8 /* check input contents on the device first (synchronises)       */
 #define GDR_CHANNEL_GATE 0x10 /* gdr_recurrent_fwd: g is per key channel, [T_total, Hv, K]  */
+#define GDR_CHUNK_SCAN 0x20   /* gdr_chunk_fwd: chunk-parallel state scan (long sequences)     */
 
 /* Chunk length of the chunked prefill (tokens).  The pages' kernels use 64. */
 #define GDR_CHUNK 64
@@ -112,6 +113,19 @@ GDR_API int gdr_chunk_workspace_size(int N, int64_t T_total, int Hk, int Hv, int
  * Supported: Hv % Hk == 0, K == V, K in {64, 128}.  Any finite g <= 0 is
  * accepted: every exponential formed is of an in-chunk difference
  * exp(gam_i - gam_j), i >= j (cuLA PR #113 review on exp(-prefix) overflow).
+ *
+ * GDR_CHUNK_SCAN (bf16, K = V = 128; ignored otherwise, with the same
+ * results): the serial chain over a sequence's chunks is cut into segments.
+ * The state map of a segment is affine in its start state,
+ * S_end = S_start P + B, with P [K, K] and B [V, K]; the segments' P and B
+ * are formed in parallel, a scan composes them into every segment's start
+ * state, and the segments then run in parallel again to write o.  It pays
+ * for long sequences with few value heads (the plain chain runs
+ * Hv * K / 32 CTAs per sequence, each 64 tokens per step), and costs three
+ * chain passes of work instead of one, so it loses where the plain chain
+ * already fills the GPU.  The workspace grows by
+ * 2 * (ceil(T_total / 64 / G) + N + 1) * Hv * K * K * 4 bytes, G the segment
+ * length in chunks that the library derives from T_total and Hv.
  */
 GDR_API int gdr_chunk_fwd(const void* q, const void* k, const void* v, const float* g,
                   const float* gk, const void* beta, const float* initial_state,

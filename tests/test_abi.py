@@ -50,6 +50,25 @@ def test_workspace_size(lib):
     assert gdr.chunk_workspace_size(8, 6113, 16, 16, 128, 128, gate_kind=0, dtype=0) >= n1
 
 
+def test_workspace_size_chunk_scan(lib):
+    """GDR_CHUNK_SCAN adds, per segment and value head, a K x K transition and
+    a V x K offset (fp32) on the tensor-core path, at least one segment per
+    sequence; other shapes ignore the flag."""
+    S = gdr.GDR_CHUNK_SCAN
+    for N, T, Hv in [(1, 32768, 4), (4, 6113, 16), (3, 100, 1)]:
+        n0 = gdr.chunk_workspace_size(N, T, Hv, Hv, 128, 128, gate_kind=0, dtype=0)
+        n1 = gdr.chunk_workspace_size(N, T, Hv, Hv, 128, 128, gate_kind=0, dtype=0, flags=S)
+        assert n1 % 256 == 0
+        assert n1 - n0 >= 2 * (N + 1) * Hv * 128 * 128 * 4
+        # segments of at least 8 chunks: no more than ceil(T / 512) + N + 1 of them
+        segs_max = -(-T // 512) + N + 1
+        assert n1 - n0 <= 2 * segs_max * Hv * 128 * 128 * 4 + 16 * segs_max + 4 * (N + 1) + 3 * 256
+    assert gdr.chunk_workspace_size(1, 4096, 1, 1, 64, 64, gate_kind=0, dtype=0, flags=S) == \
+        gdr.chunk_workspace_size(1, 4096, 1, 1, 64, 64, gate_kind=0, dtype=0)
+    assert gdr.chunk_workspace_size(1, 4096, 1, 1, 128, 128, gate_kind=0, dtype=1, flags=S) == \
+        gdr.chunk_workspace_size(1, 4096, 1, 1, 128, 128, gate_kind=0, dtype=1)
+
+
 @pytest.mark.parametrize("args,code", [
     (dict(Hk=3, Hv=4), 1),               # Hv not a multiple of Hk
     (dict(K=96, V=96), 2),               # unsupported head dim
@@ -86,6 +105,7 @@ def _chunk_call(lib, **kw):
     (dict(ws=ctypes.c_void_p(272)), 1),                 # workspace not 256-aligned
     (dict(ws_bytes=1024), 3),                           # workspace too small
     (dict(flags=0x4), 1),                               # commit is not a prefill flag
+    (dict(flags=0x40), 1),                              # unknown flag
     (dict(K=64, V=128), 2),
     (dict(N=0, T=64), 1),                               # tokens without sequences
 ])

@@ -184,6 +184,49 @@ def test_varlen_equals_separate_calls():
         np.testing.assert_allclose(sf[b], sb[0], rtol=1e-14, atol=0)
 
 
+@pytest.mark.parametrize("gate", ["g", "gk"])
+def test_segment_state_map_is_affine(gate):
+    """The reading the chunk-parallel scan rests on: over any run of tokens the
+    state map is affine in the start state, S_end = S_start P + B ([V][K]
+    layout), with P the run from the identity with v = 0 and B the run from
+    zero; composing two segments that way gives the one-pass final state."""
+    rng = np.random.default_rng(21)
+    K = V = 6
+    T1, T2 = 9, 13
+    d = _rand_case(rng, T1 + T2, 1, 2, K, V, gate=gate, g_lo=-0.7, h0=False)
+    h0 = rng.standard_normal((1, 2, V, K))
+    full = {k_: v_ for k_, v_ in d.items() if k_ != "initial_state"}
+    _, s_full = oracle.tokenwise(cu_seqlens=[0, T1 + T2], scale=0.5, initial_state=h0, **full)
+
+    def run(sl, start, zero_v=False):
+        seg = {k_: v_[sl] for k_, v_ in full.items()}
+        if zero_v:
+            seg["v"] = np.zeros_like(seg["v"])
+        n = sl.stop - sl.start
+        return oracle.tokenwise(cu_seqlens=[0, n], scale=0.5, initial_state=start, **seg)[1]
+
+    eye = np.broadcast_to(np.eye(K), (1, 2, K, K)).copy()
+    s_mid = h0
+    for sl in (slice(0, T1), slice(T1, T1 + T2)):
+        P = run(sl, eye, zero_v=True)
+        B = run(sl, None)
+        direct = run(sl, s_mid)
+        composed = np.einsum("nhvm,nhmk->nhvk", s_mid, P) + B
+        np.testing.assert_allclose(composed, direct, rtol=1e-12, atol=1e-12)
+        s_mid = composed
+    np.testing.assert_allclose(s_mid, s_full, rtol=1e-12, atol=1e-12)
+    # P depends on the keys, gates and betas but not on v
+    P1 = run(slice(0, T1), eye, zero_v=True)
+    d2 = dict(full, v=rng.standard_normal(full["v"].shape))
+    seg = {k_: v_[:T1] for k_, v_ in d2.items()}
+    seg["v"] = np.zeros_like(seg["v"])
+    P2 = oracle.tokenwise(cu_seqlens=[0, T1], scale=0.5, initial_state=eye, **seg)[1]
+    np.testing.assert_array_equal(P1, P2)
+    # a wrong composition order (P S instead of S P) is caught
+    wrong = np.einsum("nhvm,nhmk->nhvk", P1, h0)
+    assert rel_l2(wrong + run(slice(0, T1), None), run(slice(0, T1), h0)) > 1e-3
+
+
 @pytest.mark.parametrize("gate,g_lo", [("g", -0.05), ("g", -2.0), ("gk", -0.1), ("gk", -2.0)])
 @pytest.mark.parametrize("chunk", [1, 7, 16, 64])
 def test_chunked_equals_tokenwise(gate, g_lo, chunk):
