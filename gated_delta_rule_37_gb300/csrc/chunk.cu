@@ -20,6 +20,9 @@
 //   out    per (chunk, value-head): O = scale (Qd S0^T + P Nn).
 // Every exponential is of gam_i - gam_j with i >= j or of gam_i itself, all
 // <= 0, so any finite gate <= 0 stays finite (cuLA PR #113 review).
+#include <algorithm>
+#include <cmath>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -27,11 +30,31 @@ namespace gdr {
 
 static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-int chunk_scan_segment(int64_t T, int Hv) {
-    const int64_t nc = (T + kChunk - 1) / kChunk;
-    const int64_t segs = Hv >= 38 ? 1 : 38 / Hv;
-    const int64_t g = (nc + segs - 1) / segs;
-    return (int)(g < 8 ? 8 : g > (1 << 30) ? (1 << 30) : g);
+// Segment length of the chunk-parallel scan, from a cost model fitted to
+// GB300 measurements (microseconds; N sequences of the mean length, 152 SMs,
+// one chain or scan CTA per SM):
+//   G * (1.51 waves(8 Hv N S) + 1.75 waves(4 Hv N S)) + 1.45 S waves(32 Hv N) + 10
+// for S segments of G = ceil(nc / S) chunks: the summary pass, the output
+// pass, the scan (a step streams one 64 KB transition per CTA) and a fixed
+// cost.  Returns the G of the cheapest S in 2..64 with G >= 4 (ceil(nc / 2)
+// for sequences under 8 chunks).  The one pass costs about 1.6 us * nc *
+// waves(4 Hv N): the scan pays only while 12 Hv N is well under the SM count.
+int chunk_scan_segment(int N, int64_t T, int Hv) {
+    constexpr double kSMs = 152.0;
+    if (N <= 0 || T <= 0) return 1;
+    const double nc = std::ceil((double)T / kChunk / N);
+    auto waves = [&](double ctas) { return std::ceil(ctas / kSMs); };
+    double best = 1e300;
+    int best_g = (int)std::max(1.0, std::ceil(nc / 2));
+    for (int S = 2; S <= 64; ++S) {
+        const double G = std::ceil(nc / S);
+        if (G < 4) break;
+        const double segs = std::ceil(nc / G);
+        const double t = G * (1.51 * waves(8.0 * Hv * N * segs) + 1.75 * waves(4.0 * Hv * N * segs)) +
+                         1.45 * segs * waves(32.0 * Hv * N) + 10.0;
+        if (t < best) { best = t; best_g = (int)G; }
+    }
+    return best_g;
 }
 
 ChunkWorkspace chunk_workspace_layout(int N, int64_t T, int Hk, int Hv, int K, int V, int gate_kind,
@@ -52,8 +75,8 @@ ChunkWorkspace chunk_workspace_layout(int N, int64_t T, int Hk, int Hv, int K, i
     if (w.tc) {
         // tensor-core path: pre-swizzled per-chunk operand images only
         w.off_blobs = take(chunk_tc_blob_bytes(w.max_chunks, Hk, Hv, gate_kind == 1));
-        if (flags & 0x20) {  // GDR_CHUNK_SCAN
-            w.seg_chunks = chunk_scan_segment(T, Hv);
+        w.seg_chunks = (flags & 0x20) ? chunk_scan_segment(N, T, Hv) : 0;  // GDR_CHUNK_SCAN (>= 1)
+        if (w.seg_chunks > 0) {
             w.max_segs = (w.max_chunks + w.seg_chunks - 1) / w.seg_chunks + N;
             w.off_segs = take(16 * (size_t)w.max_segs);
             w.off_segoff = take(sizeof(int) * (size_t)(N + 1));

@@ -1110,12 +1110,17 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                 tc::mma_commit(bar(kEmpty0 + s));
                 GDR_TRACE_POINT(6, c);
             } else if (isC) {
-                tc::fence_after();
-                tc::mma_ksteps<4>(tD1 + 64 * ob, dk128(st + S::kYW), a64, dmn64(base + S::kN + nbuf, 512), 64,
-                                  idB, false);
-                tc::mma_commit(bar(kOFull0 + ob));
-                tc::mma_commit(bar(kEmpty0 + s));
-                issued = true;
+                if (p.mode == 1) {  // segment summary: no output, so no P N product
+                    tc::mbar_arrive(bar(kOFull0 + ob));
+                    tc::mbar_arrive(bar(kEmpty0 + s));
+                } else {
+                    tc::fence_after();
+                    tc::mma_ksteps<4>(tD1 + 64 * ob, dk128(st + S::kYW), a64, dmn64(base + S::kN + nbuf, 512), 64,
+                                      idB, false);
+                    tc::mma_commit(bar(kOFull0 + ob));
+                    tc::mma_commit(bar(kEmpty0 + s));
+                    issued = true;
+                }
             }
             // S^T <- colf * S^T + dS^T  (hi and lo halves of the accumulator summed)
             if (!tc::mbar_wait(bar(kD2Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
@@ -1195,21 +1200,39 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
 // kernel composes them in order, in fp32:
 //   S_start(0) = h0 (or 0),   S_start(j + 1) = S_start(j) P_j + B_j,
 // writing S_start(j) over B_j (each thread reads its own elements of B_j
-// before it writes them).  One CTA per (value head, 8 value rows, sequence);
-// thread (k, hf) keeps rows 4 hf .. 4 hf + 3 of column k in registers and the
-// CTA's rows transposed in shared memory; P_j is staged whole in shared memory
-// with cp.async, the next one in flight while the current one is used.
-constexpr int kScanRows = 8;
-constexpr int kScanThreads = 256;
-constexpr uint32_t kScanSmem = 2 * D * D * 4;  // two P buffers
+// before it writes them).  One CTA per (value head, 4 value rows, sequence)
+// of 512 threads: thread (k, mg) forms the partial product over
+// m in [32 mg, 32 mg + 32) for the 4 rows of column k (four warps per
+// scheduler hide the shared-memory latency), group 0 adds the partials and
+// keeps the rows in registers; the rows sit transposed in shared memory for
+// the next product.  P_j and the CTA's rows of B_j stream through a
+// three-deep ring of shared-memory buffers, each filled by two 1-D bulk
+// copies on its mbarrier two steps ahead.
+constexpr int kScanRows = 4;
+constexpr int kScanGroups = 4;
+constexpr int kScanThreads = D * kScanGroups;
+constexpr int kScanRing = 3;
+constexpr uint32_t kScanP = D * D * 4;            // one P buffer
+constexpr uint32_t kScanB = kScanRows * D * 4;    // one B buffer (the CTA's rows)
+constexpr uint32_t kScanSmem = kScanRing * (kScanP + kScanB);
 
 __global__ void __launch_bounds__(kScanThreads) chunk_seg_scan_kernel(TcParams p) {
     extern __shared__ float4 scan_smem[];
     float* Ps = reinterpret_cast<float*>(scan_smem);
-    __shared__ float4 Xs[D][kScanRows / 4];  // [k][rows 0..3 | rows 4..7]
-    const int tid = threadIdx.x, k = tid & (D - 1), hf = tid >> 7;
-    const int h = blockIdx.x / (D / kScanRows), r0 = (blockIdx.x % (D / kScanRows)) * kScanRows + 4 * hf;
+    float* Bsm = Ps + kScanRing * D * D;
+    __shared__ float4 Xs[D];                    // [k] -> rows 0..3
+    __shared__ float4 red[kScanGroups - 1][D];  // partials of groups 1..3
+    __shared__ __align__(8) uint64_t full[kScanRing];
+    __shared__ int abort_flag;
+    const int tid = threadIdx.x, k = tid & (D - 1), mg = tid >> 7;
+    const int h = blockIdx.x / (D / kScanRows), r0 = (blockIdx.x % (D / kScanRows)) * kScanRows;
     const int b = blockIdx.y;
+    if (tid == 0) {
+        for (int i = 0; i < kScanRing; ++i) tc::mbar_init(tc::smem_u32(&full[i]), 1);
+        abort_flag = 0;
+        tc::mbar_fence_init();
+    }
+    __syncthreads();
     tc::grid_dep_wait();    // the segment summaries come from the chain kernel
     tc::grid_dep_launch();  // the output pass may start its prologue
     if (!p.meta[1]) return;
@@ -1218,51 +1241,84 @@ __global__ void __launch_bounds__(kScanThreads) chunk_seg_scan_kernel(TcParams p
 #pragma unroll
     for (int r = 0; r < 4; ++r) x[r] = p.h0 ? p.h0[(((size_t)b * p.Hv + h) * D + r0 + r) * D + k] : 0.f;
     if (ns == 0) {  // no chunks: the final state is the start state
-        if (p.hT) {
+        if (p.hT && mg == 0) {
 #pragma unroll
             for (int r = 0; r < 4; ++r) p.hT[(((size_t)b * p.Hv + h) * D + r0 + r) * D + k] = x[r];
         }
         return;
     }
-    Xs[k][hf] = make_float4(x[0], x[1], x[2], x[3]);
+    if (mg == 0) Xs[k] = make_float4(x[0], x[1], x[2], x[3]);
+    auto bptr = [&](int j) { return p.Bs + ((size_t)(sg0 + j) * p.Hv + h) * D * D + (size_t)r0 * D; };
+    // P_j and B_j are needed by steps 0 .. ns - 2
     auto stage = [&](int j) {
-        const char* src = reinterpret_cast<const char*>(p.Mt + ((size_t)(sg0 + j) * p.Hv + h) * D * D);
-        const uint32_t dst = tc::smem_u32(Ps + (j & 1) * D * D);
-        for (int e = tid; e < D * D / 4; e += kScanThreads)
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(dst + 16 * e), "l"(src + 16 * e) : "memory");
-        asm volatile("cp.async.commit_group;" ::: "memory");
+        if (tid == 0 && j < ns - 1) {
+            const uint32_t fb = tc::smem_u32(&full[j % kScanRing]);
+            tc::mbar_arrive_tx(fb, kScanP + kScanB);
+            tc::bulk_g2s(tc::smem_u32(Ps + (j % kScanRing) * D * D), p.Mt + ((size_t)(sg0 + j) * p.Hv + h) * D * D,
+                         kScanP, fb);
+            tc::bulk_g2s(tc::smem_u32(Bsm + (j % kScanRing) * kScanRows * D), bptr(j), kScanB, fb);
+        }
     };
-    if (ns > 1) stage(0);
+    stage(0);
+    stage(1);
     for (int j = 0; j < ns; ++j) {
-        float* bj = p.Bs + ((size_t)(sg0 + j) * p.Hv + h) * D * D + (size_t)r0 * D + k;
-        float acc[4];
+        stage(j + 2);  // into the buffers read two steps ago (released by the barrier that ended that step)
+        if (j < ns - 1 && !tc::mbar_wait(tc::smem_u32(&full[j % kScanRing]), (j / kScanRing) & 1, &abort_flag)) {
+            abort_flag = 1;
+            atomicOr(p.err, 2u);
+        }
+        __syncthreads();  // P_j, B_j and the start state of segment j are visible
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        if (mg == 0) {
+            // the start state of segment j, over B_j (B_j has been copied in)
+            float* bj = bptr(j) + k;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-            acc[r] = bj[(size_t)r * D];
-            bj[(size_t)r * D] = x[r];  // the start state of segment j
+            for (int r = 0; r < 4; ++r) bj[(size_t)r * D] = x[r];
+            if (j < ns - 1) {
+                const float* bs = Bsm + (j % kScanRing) * kScanRows * D + k;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) acc[r] = bs[r * D];
+            }
         }
         if (j == ns - 1) break;
-        if (j + 2 < ns) {
-            stage(j + 1);
-            asm volatile("cp.async.wait_group 1;" ::: "memory");
-        } else {
-            asm volatile("cp.async.wait_group 0;" ::: "memory");
-        }
-        __syncthreads();  // P_j and the start state of segment j are visible
-        const float* P = Ps + (j & 1) * D * D + k;
+        const float* P = Ps + (j % kScanRing) * D * D + k;
+        float acc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
-        for (int m = 0; m < D; ++m) {
-            const float pm = P[m * D];
-            const float4 xm = Xs[m][hf];
-            acc[0] = fmaf(xm.x, pm, acc[0]);
-            acc[1] = fmaf(xm.y, pm, acc[1]);
-            acc[2] = fmaf(xm.z, pm, acc[2]);
-            acc[3] = fmaf(xm.w, pm, acc[3]);
+        for (int m = 32 * mg; m < 32 * mg + 32; m += 2) {
+            const float p0 = P[m * D], p1 = P[(m + 1) * D];
+            const float4 x0 = Xs[m], x1 = Xs[m + 1];
+            acc[0] = fmaf(x0.x, p0, acc[0]);
+            acc[1] = fmaf(x0.y, p0, acc[1]);
+            acc[2] = fmaf(x0.z, p0, acc[2]);
+            acc[3] = fmaf(x0.w, p0, acc[3]);
+            acc2[0] = fmaf(x1.x, p1, acc2[0]);
+            acc2[1] = fmaf(x1.y, p1, acc2[1]);
+            acc2[2] = fmaf(x1.z, p1, acc2[2]);
+            acc2[3] = fmaf(x1.w, p1, acc2[3]);
         }
-        __syncthreads();  // every read of the old start state (and of P_j) is done
-        Xs[k][hf] = make_float4(acc[0], acc[1], acc[2], acc[3]);
 #pragma unroll
-        for (int r = 0; r < 4; ++r) x[r] = acc[r];
+        for (int r = 0; r < 4; ++r) acc[r] += acc2[r];
+        if (mg > 0) red[mg - 1][k] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        __syncthreads();  // partials written; every read of the old start state, P_j and B_j is done
+        if (mg == 0) {
+#pragma unroll
+            for (int g2 = 0; g2 < kScanGroups - 1; ++g2) {
+                const float4 t = red[g2][k];
+                acc[0] += t.x;
+                acc[1] += t.y;
+                acc[2] += t.z;
+                acc[3] += t.w;
+            }
+            Xs[k] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) x[r] = acc[r];
+        }
+    }
+    // no copy may still be writing shared memory when the CTA exits (they are
+    // all waited for above unless a wait gave up): the last use of each slot
+    if (tid == 0) {
+        for (int j = (ns - 1 > kScanRing ? ns - 1 - kScanRing : 0); j < ns - 1; ++j)
+            tc::mbar_wait_copies(tc::smem_u32(&full[j % kScanRing]), (j / kScanRing) & 1);
     }
 }
 

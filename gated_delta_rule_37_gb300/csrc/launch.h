@@ -85,10 +85,9 @@ struct ChunkWorkspace {
     size_t total;
 };
 
-// Segment length (chunks) of the chunk-parallel scan: about 38 / Hv segments
-// per sequence of ceil(T / 64) chunks, so that the summary pass (8 Hv CTAs
-// per segment) is near two waves of a 152-SM GPU; never below 8 chunks.
-int chunk_scan_segment(int64_t T, int Hv);
+// Segment length (chunks, >= 1) of the chunk-parallel scan for N sequences
+// of T tokens in all and Hv value heads.
+int chunk_scan_segment(int N, int64_t T, int Hv);
 
 ChunkWorkspace chunk_workspace_layout(int N, int64_t T, int Hk, int Hv, int K, int V, int gate_kind,
                                       int dtype, int flags);

@@ -60,8 +60,8 @@ def test_workspace_size_chunk_scan(lib):
         n1 = gdr.chunk_workspace_size(N, T, Hv, Hv, 128, 128, gate_kind=0, dtype=0, flags=S)
         assert n1 % 256 == 0
         assert n1 - n0 >= 2 * (N + 1) * Hv * 128 * 128 * 4
-        # segments of at least 8 chunks: no more than ceil(T / 512) + N + 1 of them
-        segs_max = -(-T // 512) + N + 1
+        # at most one segment per chunk of the capacity ceil(T / 64) + N, plus N
+        segs_max = -(-T // 64) + 2 * N
         assert n1 - n0 <= 2 * segs_max * Hv * 128 * 128 * 4 + 16 * segs_max + 4 * (N + 1) + 3 * 256
     assert gdr.chunk_workspace_size(1, 4096, 1, 1, 64, 64, gate_kind=0, dtype=0, flags=S) == \
         gdr.chunk_workspace_size(1, 4096, 1, 1, 64, 64, gate_kind=0, dtype=0)
