@@ -150,11 +150,15 @@ __device__ __forceinline__ void raise_error(const TcParams& p, unsigned code) {
 //   3. the lower-left 32 x 32 block: T_10 = -B_1 (A_10 B_0) with B_0, B_1 the
 //      two 32 x 32 inverses from step 2.
 // Each product is one pass over shared memory with a small register tile per
-// thread.  Every entry of Tm is written (zeros above the diagonal).  Z holds
-// 1024 floats of scratch.
+// thread.  Every entry of Tm is written (zeros above the diagonal) and visible
+// to every thread on return.  Z holds 1024 floats of scratch.  Threads from 256
+// on only take part in the barriers.
 // ---------------------------------------------------------------------------
+template <int NT>
 __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict__ Tm, float* __restrict__ Z,
                                  int tid) {
+    static_assert(NT == 256 || NT == 512, "solve_unit_lower runs on 256 of 256 or 512 threads");
+    const bool act = NT == 256 || tid < 256;
     if (tid < 64) {
         const int r0 = 16 * (tid >> 4), c = tid & 15;
         float x[16];
@@ -167,7 +171,7 @@ __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict_
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) Tm[(r0 + r) * LDA + r0 + c] = x[r];
-    } else {
+    } else if (act) {
         // zeros in the six blocks above the block diagonal
         for (int e = tid - 64; e < 6 * 256; e += 192) {
             const int blk = e >> 8, r = (e >> 4) & 15, c = e & 15;
@@ -180,64 +184,73 @@ __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict_
     GDR_TRACE_PREP(21);
     // step 2: pair p = tid / 128; thread: row i, columns j0, j0 + 1 of a 16 x 16 block
     {
-        const int p = tid >> 7, e = tid & 127, i = e >> 3, j0 = 2 * (e & 7);
+        const int p = (tid >> 7) & 1, e = tid & 127, i = e >> 3, j0 = 2 * (e & 7);
         const int r0 = 32 * p, r1 = r0 + 16;
-        float y0 = 0.f, y1 = 0.f;
+        if (act) {
+            float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float a = A[(r1 + i) * LDA + r0 + m];
-            y0 = fmaf(a, Tm[(r0 + m) * LDA + r0 + j0], y0);
-            y1 = fmaf(a, Tm[(r0 + m) * LDA + r0 + j0 + 1], y1);
+            for (int m = 0; m < 16; ++m) {
+                const float a = A[(r1 + i) * LDA + r0 + m];
+                y0 = fmaf(a, Tm[(r0 + m) * LDA + r0 + j0], y0);
+                y1 = fmaf(a, Tm[(r0 + m) * LDA + r0 + j0 + 1], y1);
+            }
+            Z[p * 256 + i * 16 + j0] = y0;
+            Z[p * 256 + i * 16 + j0 + 1] = y1;
         }
-        Z[p * 256 + i * 16 + j0] = y0;
-        Z[p * 256 + i * 16 + j0 + 1] = y1;
         __syncthreads();
-        float t0 = 0.f, t1 = 0.f;
+        if (act) {
+            float t0 = 0.f, t1 = 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const float x = Tm[(r1 + i) * LDA + r1 + m];
-            t0 = fmaf(x, Z[p * 256 + m * 16 + j0], t0);
-            t1 = fmaf(x, Z[p * 256 + m * 16 + j0 + 1], t1);
+            for (int m = 0; m < 16; ++m) {
+                const float x = Tm[(r1 + i) * LDA + r1 + m];
+                t0 = fmaf(x, Z[p * 256 + m * 16 + j0], t0);
+                t1 = fmaf(x, Z[p * 256 + m * 16 + j0 + 1], t1);
+            }
+            Tm[(r1 + i) * LDA + r0 + j0] = -t0;
+            Tm[(r1 + i) * LDA + r0 + j0 + 1] = -t1;
         }
-        Tm[(r1 + i) * LDA + r0 + j0] = -t0;
-        Tm[(r1 + i) * LDA + r0 + j0 + 1] = -t1;
     }
     __syncthreads();
     GDR_TRACE_PREP(22);
     // step 3: 2 x 2 tile per thread, rows 2 ti, 2 ti + 1 and columns 2 tj, 2 tj + 1
     {
-        const int ti = tid >> 4, tj = tid & 15, i0 = 2 * ti, j0 = 2 * tj;
-        float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
+        const int ti = (tid >> 4) & 15, tj = tid & 15, i0 = 2 * ti, j0 = 2 * tj;
+        if (act) {
+            float y00 = 0.f, y01 = 0.f, y10 = 0.f, y11 = 0.f;
 #pragma unroll 8
-        for (int m = 0; m < 32; ++m) {
-            const float a0 = A[(32 + i0) * LDA + m], a1 = A[(33 + i0) * LDA + m];
-            const float b0 = Tm[m * LDA + j0], b1 = Tm[m * LDA + j0 + 1];
-            y00 = fmaf(a0, b0, y00);
-            y01 = fmaf(a0, b1, y01);
-            y10 = fmaf(a1, b0, y10);
-            y11 = fmaf(a1, b1, y11);
+            for (int m = 0; m < 32; ++m) {
+                const float a0 = A[(32 + i0) * LDA + m], a1 = A[(33 + i0) * LDA + m];
+                const float b0 = Tm[m * LDA + j0], b1 = Tm[m * LDA + j0 + 1];
+                y00 = fmaf(a0, b0, y00);
+                y01 = fmaf(a0, b1, y01);
+                y10 = fmaf(a1, b0, y10);
+                y11 = fmaf(a1, b1, y11);
+            }
+            Z[i0 * 32 + j0] = y00;
+            Z[i0 * 32 + j0 + 1] = y01;
+            Z[(i0 + 1) * 32 + j0] = y10;
+            Z[(i0 + 1) * 32 + j0 + 1] = y11;
         }
-        Z[i0 * 32 + j0] = y00;
-        Z[i0 * 32 + j0 + 1] = y01;
-        Z[(i0 + 1) * 32 + j0] = y10;
-        Z[(i0 + 1) * 32 + j0 + 1] = y11;
         __syncthreads();
         GDR_TRACE_PREP(23);
-        float t00 = 0.f, t01 = 0.f, t10 = 0.f, t11 = 0.f;
+        if (act) {
+            float t00 = 0.f, t01 = 0.f, t10 = 0.f, t11 = 0.f;
 #pragma unroll 8
-        for (int m = 0; m < 32; ++m) {
-            const float x0 = Tm[(32 + i0) * LDA + 32 + m], x1 = Tm[(33 + i0) * LDA + 32 + m];
-            const float z0 = Z[m * 32 + j0], z1 = Z[m * 32 + j0 + 1];
-            t00 = fmaf(x0, z0, t00);
-            t01 = fmaf(x0, z1, t01);
-            t10 = fmaf(x1, z0, t10);
-            t11 = fmaf(x1, z1, t11);
+            for (int m = 0; m < 32; ++m) {
+                const float x0 = Tm[(32 + i0) * LDA + 32 + m], x1 = Tm[(33 + i0) * LDA + 32 + m];
+                const float z0 = Z[m * 32 + j0], z1 = Z[m * 32 + j0 + 1];
+                t00 = fmaf(x0, z0, t00);
+                t01 = fmaf(x0, z1, t01);
+                t10 = fmaf(x1, z0, t10);
+                t11 = fmaf(x1, z1, t11);
+            }
+            Tm[(32 + i0) * LDA + j0] = -t00;
+            Tm[(32 + i0) * LDA + j0 + 1] = -t01;
+            Tm[(33 + i0) * LDA + j0] = -t10;
+            Tm[(33 + i0) * LDA + j0 + 1] = -t11;
         }
-        Tm[(32 + i0) * LDA + j0] = -t00;
-        Tm[(32 + i0) * LDA + j0 + 1] = -t01;
-        Tm[(33 + i0) * LDA + j0] = -t10;
-        Tm[(33 + i0) * LDA + j0 + 1] = -t11;
     }
+    __syncthreads();  // Tm complete before any thread reads it
 }
 
 // Stage 64 token rows [64][128] bf16 (rows >= L zero-filled) into rows
@@ -262,7 +275,12 @@ __device__ __forceinline__ void stage_rows_async(unsigned char* tile, int rows, 
 // operand, so K K^T and Q K^T come from one group of MMAs.  Dead regions are
 // reused: the Q rows of X hold T' hi / lo and the fp32 A matrix holds T'' hi /
 // lo once the solve has finished.
-constexpr int kPrepThreads = 256;  // solve_unit_lower assumes exactly 256 threads
+// 256 threads (two CTAs per SM) with a scalar gate; 512 threads (one CTA per
+// SM, its shared memory does not fit twice) with per-channel gates, so that
+// the long elementwise phases of that path run on 16 warps.  The 64 x 64
+// solve always runs on the first 256.
+template <bool kKDA>
+constexpr int prep_threads() { return kKDA ? 512 : 256; }
 constexpr uint32_t kXcb = 2 * C * 128;  // column-block stride of X (128 rows x 128 B)
 
 template <bool kKDA>
@@ -291,9 +309,9 @@ struct PrepSmem {
 };
 
 template <bool kKDA>
-__global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(TcParams p) {
+__global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep_kernel(TcParams p) {
     using S = PrepSmem<kKDA>;
-    constexpr int NT = kPrepThreads;
+    constexpr int NT = prep_threads<kKDA>();
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     // Persistent: CTA x takes items x, x + gridDim.x, ... (item = chunk * Hv + h)
@@ -356,7 +374,7 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
                     if (which == 0) tc::prefetch_l2(kp + (tok * p.Hk + nh / grp) * D, D * 2);
                     else if (which == 1) tc::prefetch_l2(qp + (tok * p.Hk + nh / grp) * D, D * 2);
                     else if (which == 2) tc::prefetch_l2(vp + (tok * p.Hv + nh) * D, D * 2);
-                    else if (kKDA) tc::prefetch_l2(p.gk + (tok * p.Hv + nh) * D, D * 4);
+                    else if (kKDA && which == 3) tc::prefetch_l2(p.gk + (tok * p.Hv + nh) * D, D * 4);
                 }
                 if (!kKDA && tid == 255) tc::prefetch_l2_span(p.g + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 4);
                 if (tid == 254) tc::prefetch_l2_span(bp + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 2);
@@ -364,20 +382,26 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
         }
         if (tid < C) bet[tid] = tid < L ? to_f(bp[((size_t)start + tid) * p.Hv + h]) : 0.f;
         if (kKDA) {
-            if (tid < D) {
-                // per-channel inclusive cumsum in token order (thread = channel); all
-                // 64 loads are issued before the dependent adds
-                const float* __restrict__ gk = p.gk + ((size_t)start * p.Hv + h) * D + tid;
-                float x[C];
+            // per-channel inclusive cumsum in token order: thread (channel c, quarter
+            // qt) scans tokens 16 qt .. 16 qt + 15 (all 16 loads issued before the
+            // dependent adds), then adds the totals of the earlier quarters
+            static_assert(!kKDA || NT == 4 * D, "one thread per channel and quarter of the chunk");
+            const int c = tid & (D - 1), qt = tid >> 7;
+            const float* __restrict__ gk = p.gk + ((size_t)start * p.Hv + h) * D + c;
+            float x[16];
 #pragma unroll
-                for (int i = 0; i < C; ++i) x[i] = i < L ? __ldg(gk + (size_t)i * p.Hv * D) : 0.f;
-                float acc = 0.f;
-#pragma unroll
-                for (int i = 0; i < C; ++i) {
-                    acc += x[i];
-                    gam[i * D + tid] = acc;
-                }
+            for (int u = 0; u < 16; ++u) {
+                const int i = 16 * qt + u;
+                x[u] = i < L ? __ldg(gk + (size_t)i * p.Hv * D) : 0.f;
             }
+#pragma unroll
+            for (int u = 1; u < 16; ++u) x[u] += x[u - 1];
+            Z[qt * D + c] = x[15];  // Z is free until the solve
+            __syncthreads();
+            float off = 0.f;
+            for (int u = 0; u < qt; ++u) off += Z[u * D + c];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) gam[(16 * qt + u) * D + c] = x[u] + off;
         } else if (warp < 2) {
             // scalar gate: inclusive scan over 64 tokens with two warps
             float x = tid < L ? __ldg(p.g + ((size_t)start + tid) * p.Hv + h) : 0.f;
@@ -623,12 +647,15 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
                 GDR_TRACE_PREP(11 + 3 * lev);
             }
             {
-                // pairs inside a 4-token block: warp w takes tokens 8w..8w+7 (two
-                // blocks, 10 pairs j <= i each), lane l channels 4l..4l+3
-                float gv[8][4], kf[8][4], qf[8][4];
+                // pairs inside a 4-token block: warp w takes the block of tokens
+                // 4w..4w+3 (its 10 pairs j <= i), lane l channels 4l..4l+3; the 10
+                // A sums and the 10 P sums are reduced across the warp together
+                static_assert(!kKDA || NT / 32 == C / 4, "one warp per 4-token block");
+                const int t0 = 4 * warp;
+                float gv[4][4], kf[4][4], qf[4][4];
 #pragma unroll
-                for (int tk = 0; tk < 8; ++tk) {
-                    const int tok = 8 * warp + tk;
+                for (int tk = 0; tk < 4; ++tk) {
+                    const int tok = t0 + tk;
                     const float4 g4 = *reinterpret_cast<const float4*>(gam + tok * D + 4 * lane);
                     gv[tk][0] = g4.x; gv[tk][1] = g4.y; gv[tk][2] = g4.z; gv[tk][3] = g4.w;
                     const uint2 kr = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(tok, 4 * lane, 2 * C));
@@ -641,31 +668,29 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
                         qf[tk][c] = __bfloat162float(qb[c]);
                     }
                 }
-                float xa[32], xp[32];
+                float xs[32];  // [0, 10): A pairs, [10, 20): P pairs
 #pragma unroll
-                for (int pp = 0; pp < 32; ++pp) {
-                    xa[pp] = 0.f;
-                    xp[pp] = 0.f;
-                    if (pp < 20) {
-                        const int pr = pp % 10, di = (pr >= 1) + (pr >= 3) + (pr >= 6), dj = pr - di * (di + 1) / 2;
-                        const int a = 4 * (pp / 10) + di, bb = 4 * (pp / 10) + dj;
+                for (int pp = 0; pp < 32; ++pp) xs[pp] = 0.f;
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
-                            const float ex = __expf(gv[a][c] - gv[bb][c]);
-                            const float kd = kf[bb][c] * ex;
-                            xa[pp] = fmaf(kf[a][c], kd, xa[pp]);
-                            xp[pp] = fmaf(qf[a][c], kd, xp[pp]);
-                        }
+                for (int pr = 0; pr < 10; ++pr) {
+                    const int di = (pr >= 1) + (pr >= 3) + (pr >= 6), dj = pr - di * (di + 1) / 2;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float kd = kf[dj][c] * __expf(gv[di][c] - gv[dj][c]);
+                        xs[pr] = fmaf(kf[di][c], kd, xs[pr]);
+                        xs[10 + pr] = fmaf(qf[di][c], kd, xs[10 + pr]);
                     }
                 }
-                const float ra = reduce32_to_lane(xa, lane);
-                const float rp = reduce32_to_lane(xp, lane);
+                const float rs = reduce32_to_lane(xs, lane);
                 if (lane < 20) {
                     const int pr = lane % 10, di = (pr >= 1) + (pr >= 3) + (pr >= 6), dj = pr - di * (di + 1) / 2;
-                    const int i = 8 * warp + 4 * (lane / 10) + di, j = 8 * warp + 4 * (lane / 10) + dj;
+                    const int i = t0 + di, j = t0 + dj;
                     if (i < L) {
-                        if (j < i) As[i * LDA + j] = bet[i] * ra;
-                        Pf[i * LDA + j] = rp;
+                        if (lane < 10) {
+                            if (j < i) As[i * LDA + j] = bet[i] * rs;
+                        } else {
+                            Pf[i * LDA + j] = rs;
+                        }
                     }
                 }
             }
@@ -700,7 +725,7 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
         GDR_TRACE_WARP(2);
 
         // ---- Tm = (I + A)^{-1} -----------------------------------------------------------
-        solve_unit_lower(As, Tm, Z, tid);
+        solve_unit_lower<NT>(As, Tm, Z, tid);
         GDR_TRACE_PREP(4);
 
         // ---- split operands: T' = Tm diag(beta e^{gam}) (scalar gate) or Tm diag(beta);
@@ -753,8 +778,9 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
         __syncwarp();
         GDR_TRACE_PREP(6);
 
-        // ---- W, U out of TMEM into their blobs: 8 warps, row i = 16 q + lane (lane <
-        //      16), columns [64 hf, 64 hf + 64) of W and of U.  The images are staged in
+        // ---- W, U out of TMEM into their blobs: row i = 16 q + lane (lane < 16);
+        //      8 warps: columns [64 hf, 64 hf + 64) of W and of U, 16 warps: columns
+        //      [32 hf, 32 hf + 32).  The images are staged in
         //      shared memory left dead by the finished MMAs (W hi / lo as 64-row k128
         //      tiles over X, U value-major over V and A) and written with bulk copies,
         //      so every global write is a contiguous run. ---------------------------------
@@ -768,8 +794,9 @@ __global__ void __launch_bounds__(kPrepThreads, kKDA ? 1 : 2) chunk_prep_kernel(
             unsigned char* sWh = sm + S::kX;            // [64][128] k128, column-block stride 8 KB
             unsigned char* sWl = sm + S::kX + kTile64x128;
             float* sU = reinterpret_cast<float*>(sm + S::kV);  // 4 x [32 v][64 i]
-            for (int q2 = 0; q2 < 2; ++q2) {
-                const int cb = 2 * hf + q2;  // 32-column block of W and of U
+            constexpr int kBlocks = 512 / NT;  // 32-column blocks per warp: 2 (8 warps) or 1 (16 warps)
+            for (int q2 = 0; q2 < kBlocks; ++q2) {
+                const int cb = kBlocks * hf + q2;  // 32-column block of W and of U
                 float wv[32], uv[32];
                 tc::tmem_ld32(lrow + 32 * cb, wv);
                 tc::tmem_ld32(lrow + 128 + 32 * cb, uv);
@@ -1371,13 +1398,13 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* w
         p.Mt = reinterpret_cast<float*>(ws + w.off_mt);
         p.Bs = reinterpret_cast<float*>(ws + w.off_bs);
     }
-    auto run = [&](auto prep_kernel, auto chain_kernel, int smp, int smc, int prep_per_sm) -> cudaError_t {
+    auto run = [&](auto prep_kernel, auto chain_kernel, int smp, int smc, int prep_per_sm, int prep_nt) -> cudaError_t {
         cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smp);
         cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smc);
         {
             KernelTimer kt("chunk_prep", stream);
             const cudaError_t e = launch_dependent(prep_kernel, dim3(prep_grid(mc * a.Hv, prep_per_sm)),
-                                                   dim3(kPrepThreads), (size_t)smp, stream, p);
+                                                   dim3(prep_nt), (size_t)smp, stream, p);
             if (e != cudaSuccess) return e;
         }
         if (w.seg_chunks == 0) {
@@ -1405,9 +1432,9 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* w
         return launch_dependent(chain_kernel, dim3(a.Hv * NVB, segs), dim3(512), (size_t)smc, stream, p);
     };
     const cudaError_t e = kda ? run(chunk_prep_kernel<true>, chunk_chain_kernel<true>, PrepSmem<true>::kTotal,
-                                    ChainSmem<true>::kTotal, 1)
+                                    ChainSmem<true>::kTotal, 1, prep_threads<true>())
                               : run(chunk_prep_kernel<false>, chunk_chain_kernel<false>, PrepSmem<false>::kTotal,
-                                    ChainSmem<false>::kTotal, 2);
+                                    ChainSmem<false>::kTotal, 2, prep_threads<false>());
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
