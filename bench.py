@@ -473,6 +473,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--only", default="", help="comma list of sections: prefill,decode,verify,kda,kda_decode,"
                                                "verify_gated,decode_norm,long_scan")
+    ap.add_argument("--kda-T", type=int, default=32768,
+                    help="tokens of the long KDA prefill section (32768 is the workload; smaller for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -519,7 +521,7 @@ def main():
     if "verify" in only:
         ver = PoolRun(workloads.verify_bf16_pool(), dev)
     if "kda" in only:
-        kda = Prefill(workloads.kda_long_prefill(), dev)
+        kda = Prefill(workloads.kda_long_prefill(args.kda_T), dev)
     lsc = lpl = None
     if "long_scan" in only:
         long_case = workloads.long_few_heads_prefill()
