@@ -98,3 +98,49 @@ def test_scan_deterministic_and_graph_safe():
     graph.replay()
     torch.cuda.synchronize()
     assert bits_equal(og, outs[0][0]) and bits_equal(sg, outs[0][1])
+
+
+def test_scan_gate_minus_two_everywhere():
+    """g = -2 on every token: every segment transition decays to (nearly) zero
+    and every exponential stays an in-chunk difference."""
+    case = workloads.chunk_case(81, [1300, 700], 1, 2, 128, 128, gate="g", h0_std=0.1)
+    case.g[:] = -2.0
+    o, sf = run_gpu(case, flags=SCAN)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(sf).all()
+    ro, rs = oracle_ref(case)
+    check_out(o.cpu(), ro, "o")
+    check_state(sf.cpu(), rs, "final state")
+
+
+def test_scan_many_ragged_sequences():
+    """40 sequences of 1..700 tokens: one to several segments each, the
+    segment table spanning many sequences."""
+    gen = torch.Generator().manual_seed(82)
+    lens = torch.randint(1, 701, (40,), generator=gen).tolist()
+    case = workloads.chunk_case(82, lens, 1, 2, 128, 128, gate="g", g_range=(-0.3, 0.0), h0_std=0.1)
+    o, sf = run_gpu(case, flags=SCAN)
+    ro, rs = oracle_ref(case)
+    check_out(o.cpu(), ro, "o")
+    check_state(sf.cpu(), rs, "final state")
+
+
+def test_scan_with_qk_l2norm():
+    """GDR_CHUNK_SCAN together with in-library q / k normalisation (bf16): the
+    oracle runs on the normalised rows rounded to bf16 as the library stores them."""
+    case = workloads.chunk_case(83, [2100, 300], 1, 2, 128, 128, gate="g", g_range=(-0.2, 0.0), h0_std=0.1)
+    gen = torch.Generator().manual_seed(84)
+    q = (torch.randn(case.q.shape, generator=gen) * 2.0).to(torch.bfloat16)
+    k = (torch.randn(case.k.shape, generator=gen) * 0.7).to(torch.bfloat16)
+    case.q, case.k = q, k
+    o, sf = run_gpu(case, flags=SCAN | gdr.GDR_QK_L2NORM)
+
+    def norm_bf16(x):
+        xf = x.float()
+        return (xf * torch.rsqrt((xf * xf).sum(-1, keepdim=True) + 1e-6)).to(torch.bfloat16)
+
+    ref = workloads.ChunkCase(name="normed", q=norm_bf16(q), k=norm_bf16(k), v=case.v, beta=case.beta, g=case.g,
+                              cu_seqlens=case.cu_seqlens, scale=case.scale, initial_state=case.initial_state)
+    ro, rs = oracle_ref(ref)
+    check_out(o.cpu(), ro, "o")
+    check_state(sf.cpu(), rs, "final state")
+

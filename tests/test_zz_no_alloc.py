@@ -17,7 +17,7 @@ import torch
 
 import gated_delta_rule_37_gb300 as gdr
 from gated_delta_rule_37_gb300 import workloads
-from tests.gpu_util import check_out, check_state
+from tests.gpu_util import bits_equal, check_out, check_state
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -67,3 +67,19 @@ def test_noalloc_rejects_problem_larger_than_its_scratch():
     with pytest.raises(gdr.GdrError) as e:
         gdr.chunk_fwd_noalloc(*pos, scale=c.scale, o=o, **kw)
     assert e.value.code == 3 and "static scratch" in str(e.value)
+
+
+def test_scan_no_alloc_entry():
+    """The scan through the no-allocation entry point equals the workspace entry bit for bit."""
+    case = workloads.chunk_case(85, [3000, 200], 1, 2, 128, 128, gate="g", g_range=(-0.2, 0.0), h0_std=0.1)
+    need = gdr.chunk_workspace_size(case.N, case.T, 1, 2, 128, 128, gate_kind=0, dtype=0, flags=gdr.GDR_CHUNK_SCAN)
+    assert need <= 64 << 20
+    q, k, v, beta = (t.to(DEV) for t in (case.q, case.k, case.v, case.beta))
+    g, h0, cu = case.g.to(DEV), case.initial_state.to(DEV), case.cu_seqlens.to(DEV)
+    o1, s1 = gdr.chunk_fwd(q, k, v, beta, cu, g=g, initial_state=h0, scale=case.scale, flags=gdr.GDR_CHUNK_SCAN)
+    o2 = torch.empty_like(o1)
+    s2 = torch.empty_like(s1)
+    gdr.chunk_fwd_noalloc(q, k, v, beta, cu, g=g, initial_state=h0, scale=case.scale, flags=gdr.GDR_CHUNK_SCAN, o=o2,
+                          final_state=s2)
+    torch.cuda.synchronize()
+    assert bits_equal(o1, o2) and bits_equal(s1, s2)
