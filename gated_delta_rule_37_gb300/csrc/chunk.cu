@@ -32,26 +32,29 @@ static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Segment length of the chunk-parallel scan, from a cost model fitted to
 // GB300 measurements (microseconds; N sequences of the mean length, 152 SMs,
-// one chain or scan CTA per SM):
-//   G * (1.51 waves(8 Hv N S) + 1.75 waves(4 Hv N S)) + 1.45 S waves(32 Hv N) + 10
-// for S segments of G = ceil(nc / S) chunks: the summary pass, the output
-// pass, the scan (a step streams one 64 KB transition per CTA) and a fixed
-// cost.  Returns the G of the cheapest S in 2..64 with G >= 4 (ceil(nc / 2)
-// for sequences under 8 chunks).  The one pass costs about 1.6 us * nc *
+// one chain or scan CTA per SM).  For S segments of G = ceil(nc / S) chunks:
+// the summary pass runs S offsets (the first one from h0, with its output) and
+// S - 2 transitions of 4 Hv N CTAs each, the output pass S - 1 segments, the
+// scan S - 2 products of a 64 KB transition per CTA:
+//   G * (1.51 waves(4 Hv N (2 S - 2)) + 1.75 waves(4 Hv N (S - 1)))
+//     + 1.45 (S - 2) waves(32 Hv N) + 10.
+// Returns the G of the cheapest S in 2..64 with G >= 4 (ceil(nc / 2) for
+// sequences under 8 chunks).  The one pass costs about 1.6 us * nc *
 // waves(4 Hv N): the scan pays only while 12 Hv N is well under the SM count.
 int chunk_scan_segment(int N, int64_t T, int Hv) {
     constexpr double kSMs = 152.0;
     if (N <= 0 || T <= 0) return 1;
     const double nc = std::ceil((double)T / kChunk / N);
     auto waves = [&](double ctas) { return std::ceil(ctas / kSMs); };
+    const double u = 4.0 * Hv * N;
     double best = 1e300;
     int best_g = (int)std::max(1.0, std::ceil(nc / 2));
     for (int S = 2; S <= 64; ++S) {
         const double G = std::ceil(nc / S);
         if (G < 4) break;
         const double segs = std::ceil(nc / G);
-        const double t = G * (1.51 * waves(8.0 * Hv * N * segs) + 1.75 * waves(4.0 * Hv * N * segs)) +
-                         1.45 * segs * waves(32.0 * Hv * N) + 10.0;
+        const double t = G * (1.51 * waves(u * (2 * segs - 2)) + 1.75 * waves(u * (segs - 1))) +
+                         1.45 * (segs - 2) * waves(32.0 * Hv * N) + 10.0;
         if (t < best) { best = t; best_g = (int)G; }
     }
     return best_g;

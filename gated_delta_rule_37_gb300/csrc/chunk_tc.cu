@@ -924,16 +924,25 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
         c0 = p.offsets[b];
     } else {
         sg = blockIdx.y;
-        if (sg >= p.meta[2]) {  // beyond this call's segment count
+        bool idle = sg >= p.meta[2];  // beyond this call's segment count
+        if (!idle) {
+            const int4 e = p.segs[sg];
+            b = e.x; cs0 = e.y; nc = e.z; last = e.w != 0;
+            c0 = p.offsets[b] + cs0;
+            // the first segment of a sequence runs from h0 in the summary pass
+            // (the true chain: output and end state); no transition is formed for
+            // it or for the last one, and the output pass skips it
+            idle = p.mode == 1 ? (transition && (cs0 == 0 || last)) : cs0 == 0;
+        }
+        if (idle) {
             tc::fence_before();
             __syncthreads();
             if (warp == 2) tc::tmem_dealloc(tmem, 256);
             return;
         }
-        const int4 e = p.segs[sg];
-        b = e.x; cs0 = e.y; nc = e.z; last = e.w != 0;
-        c0 = p.offsets[b] + cs0;
     }
+    const bool first = cs0 == 0;
+    const bool outputs = p.mode != 1 || first;  // transitions are never first
     const int bos = p.cu[b] + cs0 * C, eos = p.cu[b + 1];
     const int kh = h / (p.Hv / p.Hk);
     // Accumulators (fp32 TMEM columns).  The hi and lo split terms of the state
@@ -1024,7 +1033,7 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
         } else if (transition) {  // identity: column v0 + vh + v of I
 #pragma unroll
             for (int v = 0; v < 16; ++v) Sreg[v] = (v0 + vh + v == t) ? 1.f : 0.f;
-        } else if (p.h0 && p.mode == 0) {
+        } else if (p.h0 && first) {
 #pragma unroll
             for (int v = 0; v < 16; ++v) Sreg[v] = p.h0[(((size_t)b * p.Hv + h) * D + v0 + vh + v) * D + t];
         } else {
@@ -1137,7 +1146,7 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                 tc::mma_commit(bar(kEmpty0 + s));
                 GDR_TRACE_POINT(6, c);
             } else if (isC) {
-                if (p.mode == 1) {  // segment summary: no output, so no P N product
+                if (!outputs) {  // segment summary: no output, so no P N product
                     tc::mbar_arrive(bar(kOFull0 + ob));
                     tc::mbar_arrive(bar(kEmpty0 + s));
                 } else {
@@ -1167,7 +1176,7 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             tc::mma_commit(bar(dr));
             tc::mbar_wait(bar(dr), 0, abort_flag);
         }
-        if (p.mode == 1 && !*abort_flag) {  // segment summary
+        if (p.mode == 1 && !(first && last) && !*abort_flag) {  // segment summary (or the true end of a first segment)
             float* dst = (transition ? p.Mt : p.Bs) + (((size_t)sg * p.Hv + h) * D + v0 + vh) * D + t;
 #pragma unroll
             for (int v = 0; v < 16; ++v) dst[(size_t)v * D] = Sreg[v];
@@ -1189,7 +1198,7 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             if (!tc::mbar_wait(bar(kOFull0 + ob), (c >> 1) & 1, abort_flag)) fail();
             if (tid == 384) GDR_TRACE_POINT(13, c);
             tc::fence_after();
-            if (drain && p.mode != 1) {
+            if (drain && outputs) {
                 float ov[BV], ld[2 * BV];
                 tc::tmem_ld64(tD1 + 64 * ob + lane_base, ld);
 #pragma unroll
@@ -1223,18 +1232,18 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
 // ---------------------------------------------------------------------------
 // The state map of a run of chunks is affine in its start state: with S in
 // the [V][K] layout, S_end = S_start P + B, P the run from the identity with
-// U = 0 and B the run from zero (the summary chain pass writes both).  This
-// kernel composes them in order, in fp32:
-//   S_start(0) = h0 (or 0),   S_start(j + 1) = S_start(j) P_j + B_j,
-// writing S_start(j) over B_j (each thread reads its own elements of B_j
-// before it writes them).  One CTA per (value head, 4 value rows, sequence)
-// of 512 threads: thread (k, mg) forms the partial product over
-// m in [32 mg, 32 mg + 32) for the 4 rows of column k (four warps per
-// scheduler hide the shared-memory latency), group 0 adds the partials and
-// keeps the rows in registers; the rows sit transposed in shared memory for
-// the next product.  P_j and the CTA's rows of B_j stream through a
-// three-deep ring of shared-memory buffers, each filled by two 1-D bulk
-// copies on its mbarrier two steps ahead.
+// U = 0 and B the run from zero.  The summary pass ran the first segment of
+// every sequence from h0 (its true end state E_0 is in B_0) and wrote P_j, B_j
+// for the others (no P for the last one).  This kernel composes, in fp32,
+//   S_start(1) = E_0,   S_start(j + 1) = S_start(j) P_j + B_j,
+// writing S_start(j) over B_j (B_j has been copied in first).  One CTA per
+// (value head, 4 value rows, sequence) of 512 threads: thread (k, mg) forms
+// the partial product over m in [32 mg, 32 mg + 32) for the 4 rows of column
+// k (four warps per scheduler hide the shared-memory latency), group 0 adds
+// the partials and keeps the rows in registers; the rows sit transposed in
+// shared memory for the next product.  P_j and the CTA's rows of B_j stream
+// through a three-deep ring of shared-memory buffers, each filled by two 1-D
+// bulk copies on its mbarrier two steps ahead.
 constexpr int kScanRows = 4;
 constexpr int kScanGroups = 4;
 constexpr int kScanThreads = D * kScanGroups;
@@ -1264,51 +1273,58 @@ __global__ void __launch_bounds__(kScanThreads) chunk_seg_scan_kernel(TcParams p
     tc::grid_dep_launch();  // the output pass may start its prologue
     if (!p.meta[1]) return;
     const int sg0 = p.segoff[b], ns = p.segoff[b + 1] - sg0;
-    float x[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) x[r] = p.h0 ? p.h0[(((size_t)b * p.Hv + h) * D + r0 + r) * D + k] : 0.f;
+    auto bptr = [&](int j) { return p.Bs + ((size_t)(sg0 + j) * p.Hv + h) * D * D + (size_t)r0 * D; };
     if (ns == 0) {  // no chunks: the final state is the start state
         if (p.hT && mg == 0) {
 #pragma unroll
-            for (int r = 0; r < 4; ++r) p.hT[(((size_t)b * p.Hv + h) * D + r0 + r) * D + k] = x[r];
+            for (int r = 0; r < 4; ++r)
+                p.hT[(((size_t)b * p.Hv + h) * D + r0 + r) * D + k] =
+                    p.h0 ? p.h0[(((size_t)b * p.Hv + h) * D + r0 + r) * D + k] : 0.f;
         }
         return;
     }
-    if (mg == 0) Xs[k] = make_float4(x[0], x[1], x[2], x[3]);
-    auto bptr = [&](int j) { return p.Bs + ((size_t)(sg0 + j) * p.Hv + h) * D * D + (size_t)r0 * D; };
-    // P_j and B_j are needed by steps 0 .. ns - 2
-    auto stage = [&](int j) {
-        if (tid == 0 && j < ns - 1) {
-            const uint32_t fb = tc::smem_u32(&full[j % kScanRing]);
+    if (ns == 1) return;  // the summary pass ran the whole sequence
+    // step t = 0 .. ns - 2 writes the start state of segment t + 1 and, for
+    // t <= ns - 3, forms the next one from P_{t+1} and B_{t+1}
+    float x[4];
+    if (mg == 0) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) x[r] = bptr(0)[(size_t)r * D + k];  // E_0
+        Xs[k] = make_float4(x[0], x[1], x[2], x[3]);
+    }
+    auto stage = [&](int t) {
+        if (tid == 0 && t <= ns - 3) {
+            const uint32_t fb = tc::smem_u32(&full[t % kScanRing]);
             tc::mbar_arrive_tx(fb, kScanP + kScanB);
-            tc::bulk_g2s(tc::smem_u32(Ps + (j % kScanRing) * D * D), p.Mt + ((size_t)(sg0 + j) * p.Hv + h) * D * D,
-                         kScanP, fb);
-            tc::bulk_g2s(tc::smem_u32(Bsm + (j % kScanRing) * kScanRows * D), bptr(j), kScanB, fb);
+            tc::bulk_g2s(tc::smem_u32(Ps + (t % kScanRing) * D * D),
+                         p.Mt + ((size_t)(sg0 + t + 1) * p.Hv + h) * D * D, kScanP, fb);
+            tc::bulk_g2s(tc::smem_u32(Bsm + (t % kScanRing) * kScanRows * D), bptr(t + 1), kScanB, fb);
         }
     };
     stage(0);
     stage(1);
-    for (int j = 0; j < ns; ++j) {
-        stage(j + 2);  // into the buffers read two steps ago (released by the barrier that ended that step)
-        if (j < ns - 1 && !tc::mbar_wait(tc::smem_u32(&full[j % kScanRing]), (j / kScanRing) & 1, &abort_flag)) {
+    for (int t = 0; t <= ns - 2; ++t) {
+        stage(t + 2);  // into the buffers read two steps ago (released by the barrier that ended that step)
+        const bool more = t <= ns - 3;
+        if (more && !tc::mbar_wait(tc::smem_u32(&full[t % kScanRing]), (t / kScanRing) & 1, &abort_flag)) {
             abort_flag = 1;
             atomicOr(p.err, 2u);
         }
-        __syncthreads();  // P_j, B_j and the start state of segment j are visible
+        __syncthreads();  // P, B of segment t + 1 and its start state are visible
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         if (mg == 0) {
-            // the start state of segment j, over B_j (B_j has been copied in)
-            float* bj = bptr(j) + k;
+            // the start state of segment t + 1, over its B (copied in above)
+            float* bj = bptr(t + 1) + k;
 #pragma unroll
             for (int r = 0; r < 4; ++r) bj[(size_t)r * D] = x[r];
-            if (j < ns - 1) {
-                const float* bs = Bsm + (j % kScanRing) * kScanRows * D + k;
+            if (more) {
+                const float* bs = Bsm + (t % kScanRing) * kScanRows * D + k;
 #pragma unroll
                 for (int r = 0; r < 4; ++r) acc[r] = bs[r * D];
             }
         }
-        if (j == ns - 1) break;
-        const float* P = Ps + (j % kScanRing) * D * D + k;
+        if (!more) break;
+        const float* P = Ps + (t % kScanRing) * D * D + k;
         float acc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
         for (int m = 32 * mg; m < 32 * mg + 32; m += 2) {
@@ -1326,15 +1342,15 @@ __global__ void __launch_bounds__(kScanThreads) chunk_seg_scan_kernel(TcParams p
 #pragma unroll
         for (int r = 0; r < 4; ++r) acc[r] += acc2[r];
         if (mg > 0) red[mg - 1][k] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        __syncthreads();  // partials written; every read of the old start state, P_j and B_j is done
+        __syncthreads();  // partials written; every read of the old start state, P and B is done
         if (mg == 0) {
 #pragma unroll
             for (int g2 = 0; g2 < kScanGroups - 1; ++g2) {
-                const float4 t = red[g2][k];
-                acc[0] += t.x;
-                acc[1] += t.y;
-                acc[2] += t.z;
-                acc[3] += t.w;
+                const float4 tt = red[g2][k];
+                acc[0] += tt.x;
+                acc[1] += tt.y;
+                acc[2] += tt.z;
+                acc[3] += tt.w;
             }
             Xs[k] = make_float4(acc[0], acc[1], acc[2], acc[3]);
 #pragma unroll
@@ -1344,8 +1360,9 @@ __global__ void __launch_bounds__(kScanThreads) chunk_seg_scan_kernel(TcParams p
     // no copy may still be writing shared memory when the CTA exits (they are
     // all waited for above unless a wait gave up): the last use of each slot
     if (tid == 0) {
-        for (int j = (ns - 1 > kScanRing ? ns - 1 - kScanRing : 0); j < ns - 1; ++j)
-            tc::mbar_wait_copies(tc::smem_u32(&full[j % kScanRing]), (j / kScanRing) & 1);
+        const int last_t = ns - 3;  // last step with copies
+        for (int t = (last_t - kScanRing + 1 > 0 ? last_t - kScanRing + 1 : 0); t <= last_t; ++t)
+            tc::mbar_wait_copies(tc::smem_u32(&full[t % kScanRing]), (t / kScanRing) & 1);
     }
 }
 

@@ -35,10 +35,12 @@ def test_long_few_heads_full_size():
 
 
 SCAN_CASES = [
-    # (lens, Hk, Hv, gate, g_range, h0)
-    ([4096], 1, 1, "g", (-0.5, 0.0), True),                 # 8 segments of 8 chunks
-    ([1536], 1, 1, "g", (-0.05, 0.0), False),               # 3 segments, the last ends on its boundary
-    ([1500, 65, 3000, 1], 1, 2, "g", (-0.3, 0.0), True),    # partial chunks, a 1-token sequence
+    # (lens, Hk, Hv, gate, g_range, h0); the library picks the segment length
+    # (4 to 7 chunks at these sizes): 2 to 13 segments per sequence
+    ([4096], 1, 1, "g", (-0.5, 0.0), True),                 # 13 segments
+    ([512], 1, 1, "g", (-0.3, 0.0), True),                  # 2 segments: the scan forms no product
+    ([1536], 1, 1, "g", (-0.05, 0.0), False),               # the last segment ends on its boundary
+    ([1500, 65, 3000, 1], 1, 2, "g", (-0.3, 0.0), True),    # partial chunks, one-segment sequences
     ([1030, 2], 2, 4, "g", (-2.0, 0.0), True),              # GVA, adversarial decay
     ([2100, 700], 1, 2, "gk", (-0.3, 0.0), False),          # per-channel gates
     ([1100], 2, 4, "gk", (-0.05, 0.0), True),               # per-channel gates, GVA, h0
