@@ -253,6 +253,15 @@ __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict_
     __syncthreads();  // Tm complete before any thread reads it
 }
 
+// The 8 per-channel values of one 16-byte operand chunk (channels 8 ch ..
+// 8 ch + 7 of a row of fp32 gates) as two 16-byte shared loads: scalar loads
+// at this 32-byte lane stride would hit each bank eight times over.
+__device__ __forceinline__ void ld8(const float* p, float (&f)[8]) {
+    const float4 a = *reinterpret_cast<const float4*>(p), b = *reinterpret_cast<const float4*>(p + 4);
+    f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+    f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
 // Stage 64 token rows [64][128] bf16 (rows >= L zero-filled) into rows
 // [row0, row0 + 64) of a k128 smem tile of `rows` rows, with cp.async (all
 // 16-byte pieces in flight at once).
@@ -421,7 +430,6 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
         tc::fence_after();
         GDR_TRACE_PREP(1);
         const uint32_t sX = tc::smem_u32(sm + S::kX), sV = tc::smem_u32(sm + S::kV);
-        auto gm = [&](int i, int c) -> float { return kKDA ? gam[i * D + c] : gam[i]; };
         const float* gl = kKDA ? gam + (L - 1) * D : gam + (L - 1);
 
         // ---- [K K^T ; Q K^T] on the tensor cores (scalar gate), one M = 128 group ------
@@ -444,11 +452,13 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
                 const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(C + i, ch, 2 * C));
                 const __nv_bfloat16* qv = reinterpret_cast<const __nv_bfloat16*>(&raw);
                 uint32_t w4[4];
+                float gq[8];
+                if (kKDA) ld8(gam + i * D + ch * 8, gq);
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int c = ch * 8 + 2 * u;
-                    w4[u] = tc::pack_bf16(__bfloat162float(qv[2 * u]) * __expf(gm(i, c)),
-                                          __bfloat162float(qv[2 * u + 1]) * __expf(gm(i, c + 1)));
+                    const float g0 = kKDA ? gq[2 * u] : gam[i], g1 = kKDA ? gq[2 * u + 1] : gam[i];
+                    w4[u] = tc::pack_bf16(__bfloat162float(qv[2 * u]) * __expf(g0),
+                                          __bfloat162float(qv[2 * u + 1]) * __expf(g1));
                 }
                 *reinterpret_cast<uint4*>(Qdst + tc::chunk_k128(C + i, ch, 2 * C)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
@@ -467,11 +477,13 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
                     const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(i, ch, 2 * C));
                     const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&raw);
                     uint32_t hw[4], lw[4];
+                    float gL[8], gI[8];
+                    ld8(gl + ch * 8, gL);
+                    ld8(gam + i * D + ch * 8, gI);
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        const int c = ch * 8 + 2 * u;
-                        const float x0 = i < L ? __bfloat162float(kv[2 * u]) * __expf(gl[c] - gam[i * D + c]) : 0.f;
-                        const float x1 = i < L ? __bfloat162float(kv[2 * u + 1]) * __expf(gl[c + 1] - gam[i * D + c + 1]) : 0.f;
+                        const float x0 = i < L ? __bfloat162float(kv[2 * u]) * __expf(gL[2 * u] - gI[2 * u]) : 0.f;
+                        const float x1 = i < L ? __bfloat162float(kv[2 * u + 1]) * __expf(gL[2 * u + 1] - gI[2 * u + 1]) : 0.f;
                         tc::split2(x0, x1, hw[u], lw[u]);
                     }
                     const uint32_t off = tc::chunk_k128(i, ch, C);
@@ -708,12 +720,12 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
                 const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(i, ch, 2 * C));
                 const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&raw);
                 uint32_t hw[4], lw[4];
+                float gI[8];
+                ld8(gam + i * D + ch * 8, gI);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int c = ch * 8 + 2 * u;
-                    tc::split2(__bfloat162float(kv[2 * u]) * __expf(gam[i * D + c]),
-                               __bfloat162float(kv[2 * u + 1]) * __expf(gam[i * D + c + 1]), hw[u], lw[u]);
-                }
+                for (int u = 0; u < 4; ++u)
+                    tc::split2(__bfloat162float(kv[2 * u]) * __expf(gI[2 * u]),
+                               __bfloat162float(kv[2 * u + 1]) * __expf(gI[2 * u + 1]), hw[u], lw[u]);
                 const uint32_t off = tc::chunk_k128(i, ch, C);
                 *reinterpret_cast<uint4*>(sm + S::kKgh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                 *reinterpret_cast<uint4*>(sm + S::kKgl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
