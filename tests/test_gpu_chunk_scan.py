@@ -146,3 +146,25 @@ def test_scan_with_qk_l2norm():
     check_out(o.cpu(), ro, "o")
     check_state(sf.cpu(), rs, "final state")
 
+
+
+@pytest.mark.parametrize("trial", range(6))
+def test_random_configurations(trial):
+    """Seeded random shapes through the tensor-core path, with and without the
+    scan: 1-6 sequences of 1-1500 tokens, GVA 1 or 2, scalar or per-channel
+    gates, with or without h0."""
+    rng = np.random.default_rng(900 + trial)
+    n = int(rng.integers(1, 7))
+    lens = [int(x) for x in rng.integers(1, 1501, n)]
+    Hk = int(rng.integers(1, 3))
+    Hv = Hk * int(rng.integers(1, 3))
+    gate = "g" if rng.random() < 0.6 else "gk"
+    lo = float(rng.choice([-2.0, -0.5, -0.05]))
+    h0 = trial % 3 != 0
+    flags = SCAN if trial % 2 == 0 else 0
+    case = workloads.chunk_case(910 + trial, lens, Hk, Hv, 128, 128, dtype=torch.bfloat16, gate=gate,
+                                g_range=(lo, 0.0), h0_std=0.1 if h0 else None)
+    o, sf = run_gpu(case, flags=flags)
+    ro, rs = oracle_ref(case)
+    check_out(o.cpu(), ro, f"o (trial {trial}: lens {lens}, Hk {Hk}, Hv {Hv}, {gate}, flags {flags})")
+    check_state(sf.cpu(), rs, f"final state (trial {trial})")
