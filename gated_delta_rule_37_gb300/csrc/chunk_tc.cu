@@ -1,8 +1,8 @@
 // Chunked prefill on the Blackwell tensor cores (bf16 inputs, K = V = 128).
 //
-// Two kernels after the chunk metadata:
+// Two kernels after the chunk metadata (three with the chunk-parallel scan):
 //
-//  prep  (one CTA per chunk x value-head, fully parallel)
+//  prep  (persistent CTAs walking the (chunk, value-head) items, fully parallel)
 //        gam = in-chunk cumsum of the gate; G = K K^T and Q K^T on tcgen05
 //        (exact bf16 products, fp32 accumulation); A_ij = beta_i e^{gam_i-gam_j}
 //        G_ij (j < i); Tm = (I + A)^{-1} by a blocked forward substitution in
@@ -12,9 +12,12 @@
 //        e^{gam_i} q_i and the decay factors.  Results are written as
 //        pre-swizzled operand images ("blobs") so the chain kernel stages them
 //        with single 1-D bulk copies.
-//        Per-key-channel gates (KDA) take the same route with A and P formed
-//        per channel on the CUDA cores, W = Tm diag(beta) (K o e^{Gam}) with a
-//        3-term split, and the decayed keys Kd = K o e^{gam_L - Gam} as hi/lo.
+//        Per-key-channel gates (KDA) take the same route on 16 warps: A and P
+//        from pivoted products (pairs across the halves of 2h-token blocks on
+//        tcgen05 with the decays folded into both operands around the pivot,
+//        each factor <= 1; pairs inside 4-token blocks on the CUDA cores),
+//        W = Tm diag(beta) (K o e^{Gam}) with a 3-term split, and the decayed
+//        keys Kd = K o e^{gam_L - Gam} as hi/lo.
 //
 //  chain (one CTA per value-head x 32-column block of V x sequence, serial
 //        over the sequence's chunks; attention-gym PR #344's inter-chunk state
@@ -31,6 +34,12 @@
 //        one MMA per 60 cycles, so the work is split three ways); warps 14 and
 //        15 drain the output accumulator (double-buffered in TMEM) to bf16
 //        rows of o.
+//        With the chunk-parallel scan the chain runs per segment of G chunks:
+//        a summary pass (the first segment of each sequence from h0 with its
+//        output; the other segments from zero, their offsets B, and the middle
+//        ones from the identity with U = 0, their transitions P), then
+//        chunk_seg_scan_kernel composes the start states, then an output pass
+//        runs every later segment from its start state.
 //
 // Every exponential is of gam_i - gam_j with i >= j or of gam_i, all <= 0:
 // any finite gate <= 0 keeps every operand finite (cuLA PR #113 review).
@@ -126,9 +135,11 @@ struct TcParams {
     int N, Hk, Hv;
     float scale;
     // chunk-parallel scan: mode 0 = one chain CTA runs a whole sequence;
-    // 1 = segment summaries (transition Mt from the identity with U = 0, offset
-    // Bs from zero), no output; 2 = segments from the scanned start states in Bs,
-    // with output
+    // 1 = segment summaries: the first segment of a sequence from h0 with its
+    // output (end state into Bs, or the final state), the others from zero
+    // without output (offset into Bs) and, for the middle ones, from the
+    // identity with U = 0 (transition into Mt); 2 = every later segment from
+    // its scanned start state in Bs, with output
     int mode;
     const int4* segs;    // (sequence, first chunk in sequence, chunks, last?)
     const int* segoff;   // [N + 1] first segment of each sequence
