@@ -117,15 +117,16 @@ GDR_API int gdr_chunk_workspace_size(int N, int64_t T_total, int Hk, int Hv, int
  * GDR_CHUNK_SCAN (bf16, K = V = 128; ignored otherwise, with the same
  * results): the serial chain over a sequence's chunks is cut into segments.
  * The state map of a segment is affine in its start state,
- * S_end = S_start P + B, with P [K, K] and B [V, K]; the segments' P and B
- * are formed in parallel, a scan composes them into every segment's start
- * state, and the segments then run in parallel again to write o.  It pays
- * for long sequences with few value heads: the plain chain runs
- * Hv * K / 32 CTAs per sequence, 64 tokens per step, and the scan costs
- * about three chain passes of work instead of one, so it wins while
- * 12 * Hv * N is well under the GPU's SM count (measured on GB300 with one
- * 32768-token sequence: 5x at Hv = 1, 2.3x at Hv = 4, 1.3x at Hv = 8, a loss
- * at Hv = 16).  The caller decides; the flag always takes the scan where it
+ * S_end = S_start P + B, with P [K, K] and B [V, K]; in one parallel pass
+ * the first segment of each sequence runs from the initial state (writing
+ * its part of o) while the others form their B (and P, but for the last),
+ * a scan composes them into every segment's start state, and the later
+ * segments then run in parallel again to write o.  It pays for long
+ * sequences with few value heads: the plain chain runs Hv * K / 32 CTAs per
+ * sequence, 64 tokens per step, and the scan costs about three chain passes
+ * of work instead of one, so it wins while 12 * Hv * N is well under the
+ * GPU's SM count (measured on GB300 with one 32768-token sequence: 5x at
+ * Hv = 1, 2.5x at Hv = 4, 1.5x at Hv = 8, a loss at Hv = 16).  The caller decides; the flag always takes the scan where it
  * applies.  The workspace grows by about
  * 2 * (ceil(T_total / 64 / G) + N + 1) * Hv * K * K * 4 bytes, G the segment
  * length in chunks (at least 4 where sequences allow) that the library derives
