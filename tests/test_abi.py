@@ -114,6 +114,15 @@ def test_chunk_fwd_rejects_before_launch(lib, kw, code):
     assert lib.gdr_last_error().decode()
 
 
+def test_chunk_scan_rejects_segment_capacity_above_grid_limit(lib):
+    """GDR_CHUNK_SCAN launches one CTA row per segment of capacity; more than
+    65535 of them is rejected before anything runs."""
+    N = 65535
+    rc = _chunk_call(lib, N=N, T=64 * N, Hk=1, Hv=1, flags=gdr.GDR_CHUNK_SCAN)
+    assert rc == 2
+    assert "segment capacity" in lib.gdr_last_error().decode()
+
+
 def test_chunk_fwd_empty_is_ok_without_device(lib):
     assert _chunk_call(lib, N=0, T=0) == 0
 
