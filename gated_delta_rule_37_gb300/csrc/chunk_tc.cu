@@ -165,13 +165,9 @@ __device__ __forceinline__ void raise_error(const TcParams& p, unsigned code) {
 // to every thread on return.  Z holds 1024 floats of scratch.  Threads from 256
 // on only take part in the barriers.
 // ---------------------------------------------------------------------------
-template <int NT, int kBarId = 0>
+template <int NT>
 __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict__ Tm, float* __restrict__ Z,
                                  int tid) {
-    auto sync = [] {
-        if (kBarId == 0) __syncthreads();
-        else tc::bar_sync(kBarId, NT);
-    };
     static_assert(NT == 256 || NT == 512, "solve_unit_lower runs on 256 of 256 or 512 threads");
     const bool act = NT == 256 || tid < 256;
     if (tid < 64) {
@@ -195,7 +191,7 @@ __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict_
             Tm[(16 * bi + r) * LDA + 16 * bj + c] = 0.f;
         }
     }
-    sync();
+    __syncthreads();
     GDR_TRACE_PREP(21);
     // step 2: pair p = tid / 128; thread: row i, columns j0, j0 + 1 of a 16 x 16 block
     {
@@ -212,7 +208,7 @@ __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict_
             Z[p * 256 + i * 16 + j0] = y0;
             Z[p * 256 + i * 16 + j0 + 1] = y1;
         }
-        sync();
+        __syncthreads();
         if (act) {
             float t0 = 0.f, t1 = 0.f;
 #pragma unroll
@@ -225,7 +221,7 @@ __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict_
             Tm[(r1 + i) * LDA + r0 + j0 + 1] = -t1;
         }
     }
-    sync();
+    __syncthreads();
     GDR_TRACE_PREP(22);
     // step 3: 2 x 2 tile per thread, rows 2 ti, 2 ti + 1 and columns 2 tj, 2 tj + 1
     {
@@ -246,7 +242,7 @@ __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict_
             Z[(i0 + 1) * 32 + j0] = y10;
             Z[(i0 + 1) * 32 + j0 + 1] = y11;
         }
-        sync();
+        __syncthreads();
         GDR_TRACE_PREP(23);
         if (act) {
             float t00 = 0.f, t01 = 0.f, t10 = 0.f, t11 = 0.f;
@@ -265,7 +261,7 @@ __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict_
             Tm[(33 + i0) * LDA + j0 + 1] = -t11;
         }
     }
-    sync();  // Tm complete before any thread reads it
+    __syncthreads();  // Tm complete before any thread reads it
 }
 
 // The 8 per-channel values of one 16-byte operand chunk (channels 8 ch ..
@@ -332,542 +328,27 @@ struct PrepSmem {
     static_assert(!kKDA || kRl + 32 * 256 <= kGam, "pivot operands overlap the gate cumsum");
 };
 
-// One prep item (chunk, value head): stage, form A / P, solve, W / U and
-// write the operand images.  kBarId 0 synchronises the whole CTA; otherwise
-// the item's NT threads synchronise on named barrier kBarId (two items run
-// side by side in one CTA).  next_item >= 0 is warmed in L2 meanwhile.  With
-// ready != nullptr the item's flag is released once its images are in global
-// memory.
-template <bool kKDA, int kBarId>
-__device__ __forceinline__ void prep_sync() {
-    if (kBarId == 0) __syncthreads();
-    else tc::bar_sync(kBarId, prep_threads<kKDA>());
-}
-
-template <bool kKDA, int kBarId>
-__device__ __forceinline__ void prep_item(const TcParams& p, const int item, const int next_item, unsigned char* sm,
-                                          const uint32_t tmem, const uint32_t bar0, const uint32_t bar1, uint32_t& ph0,
-                                          uint32_t& ph1, volatile int* abort_flag, const int tid, int* ready) {
+template <bool kKDA>
+__global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep_kernel(TcParams p) {
     using S = PrepSmem<kKDA>;
     constexpr int NT = prep_threads<kKDA>();
-    const int warp = tid >> 5, lane = tid & 31;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // Persistent: CTA x takes items x, x + gridDim.x, ... (item = chunk * Hv + h)
+    // and warms L2 with the next item's rows while it computes the current one.
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int q = warp & 3, hf = warp >> 2;  // TMEM lane quadrant, column half
     const int grp = p.Hv / p.Hk;
     const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(p.q);
     const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(p.k);
     const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(p.v);
     const __nv_bfloat16* bp = static_cast<const __nv_bfloat16*>(p.beta);
+
     float* As = reinterpret_cast<float*>(sm + S::kA);
     float* Tm = reinterpret_cast<float*>(sm + S::kTm);
     float* Z = reinterpret_cast<float*>(sm + S::kZ);
     float* gam = reinterpret_cast<float*>(sm + S::kGam);
     float* bet = reinterpret_cast<float*>(sm + S::kBeta);
-    const int chunk = item / p.Hv, h = item - chunk * p.Hv;
-    const int4 info = p.table[chunk];
-    const int start = info.y, L = info.z;
-    const int kh = h / grp;
-
-    GDR_TRACE_PREP(0);
-    GDR_TRACE_ITEM(item, 0);
-    // ---- stage K, Q (as X) and V rows (cp.async), gates, beta -------------------
-    stage_rows_async<NT>(sm + S::kX, 2 * C, 0, kp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
-    stage_rows_async<NT>(sm + S::kX, 2 * C, C, qp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
-    stage_rows_async<NT>(sm + S::kV, C, 0, vp + ((size_t)start * p.Hv + h) * D, (size_t)p.Hv * D, L, tid);
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    {
-        const int nxt = next_item;
-        if (nxt >= 0) {
-            const int nc = nxt / p.Hv, nh = nxt - nc * p.Hv;
-            const int4 ni = p.table[nc];
-            const int r = tid & 63, which = tid >> 6;
-            const size_t tok = (size_t)ni.y + r;
-            if (r < ni.z) {
-                if (which == 0) tc::prefetch_l2(kp + (tok * p.Hk + nh / grp) * D, D * 2);
-                else if (which == 1) tc::prefetch_l2(qp + (tok * p.Hk + nh / grp) * D, D * 2);
-                else if (which == 2) tc::prefetch_l2(vp + (tok * p.Hv + nh) * D, D * 2);
-                else if (kKDA && which == 3) tc::prefetch_l2(p.gk + (tok * p.Hv + nh) * D, D * 4);
-            }
-            if (!kKDA && tid == 255) tc::prefetch_l2_span(p.g + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 4);
-            if (tid == 254) tc::prefetch_l2_span(bp + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 2);
-        }
-    }
-    if (tid < C) bet[tid] = tid < L ? to_f(bp[((size_t)start + tid) * p.Hv + h]) : 0.f;
-    if (kKDA) {
-        // per-channel inclusive cumsum in token order: thread (channel c, quarter
-        // qt) scans tokens 16 qt .. 16 qt + 15 (all 16 loads issued before the
-        // dependent adds), then adds the totals of the earlier quarters
-        static_assert(!kKDA || NT == 4 * D, "one thread per channel and quarter of the chunk");
-        const int c = tid & (D - 1), qt = tid >> 7;
-        const float* __restrict__ gk = p.gk + ((size_t)start * p.Hv + h) * D + c;
-        float x[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int i = 16 * qt + u;
-            x[u] = i < L ? __ldg(gk + (size_t)i * p.Hv * D) : 0.f;
-        }
-#pragma unroll
-        for (int u = 1; u < 16; ++u) x[u] += x[u - 1];
-        Z[qt * D + c] = x[15];  // Z is free until the solve
-        prep_sync<kKDA, kBarId>();
-        float off = 0.f;
-        for (int u = 0; u < qt; ++u) off += Z[u * D + c];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) gam[(16 * qt + u) * D + c] = x[u] + off;
-    } else if (warp < 2) {
-        // scalar gate: inclusive scan over 64 tokens with two warps
-        float x = tid < L ? __ldg(p.g + ((size_t)start + tid) * p.Hv + h) : 0.f;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, x, off);
-            if (lane >= off) x += y;
-        }
-        gam[tid] = x;
-    }
-    prep_sync<kKDA, kBarId>();
-    if (!kKDA && warp == 1) gam[tid] += gam[31];
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
-    tc::fence_proxy_async();
-    tc::fence_before();
-    prep_sync<kKDA, kBarId>();
-    tc::fence_after();
-    GDR_TRACE_PREP(1);
-    const uint32_t sX = tc::smem_u32(sm + S::kX), sV = tc::smem_u32(sm + S::kV);
-    const float* gl = kKDA ? gam + (L - 1) * D : gam + (L - 1);
-
-    // ---- [K K^T ; Q K^T] on the tensor cores (scalar gate), one M = 128 group ------
-    if (!kKDA && tid == 0) {
-        constexpr uint32_t id = tc::idesc_bf16(128, 64, false, false);
-        for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = (ks >> 2) * kXcb + (ks & 3) * 32;
-            tc::mma_bf16(tmem, tc::smem_desc(sX + off, 16, 1024, tc::kSwizzle128),
-                         tc::smem_desc(sX + off, 16, 1024, tc::kSwizzle128), id, ks > 0);
-        }
-        tc::mma_commit(bar0);
-    }
-    __syncwarp();
-
-    // ---- while that runs: Qd blob, K / Kd blob, decay record ------------------------
-    {
-        unsigned char* Qdst = p.Xw + ((size_t)chunk * p.Hv + h) * kXwBytes;  // rows 64..127
-        for (int e = tid; e < C * 16; e += NT) {
-            const int i = e >> 4, ch = e & 15;
-            const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(C + i, ch, 2 * C));
-            const __nv_bfloat16* qv = reinterpret_cast<const __nv_bfloat16*>(&raw);
-            uint32_t w4[4];
-            float gq[8];
-            if (kKDA) ld8(gam + i * D + ch * 8, gq);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float g0 = kKDA ? gq[2 * u] : gam[i], g1 = kKDA ? gq[2 * u + 1] : gam[i];
-                w4[u] = tc::pack_bf16(__bfloat162float(qv[2 * u]) * __expf(g0),
-                                      __bfloat162float(qv[2 * u + 1]) * __expf(g1));
-            }
-            *reinterpret_cast<uint4*>(Qdst + tc::chunk_k128(C + i, ch, 2 * C)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-        }
-        if (!kKDA) {
-            if (h % grp == 0) {  // K rows of X, both column blocks -> a [64][128] k128 image
-                unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hk + kh) * kTile64x128;
-                for (int e = tid; e < (int)(kTile64x128 / 16); e += NT) {
-                    const int cb = e >> 9, r = e & 511;
-                    reinterpret_cast<uint4*>(Kdst)[e] = reinterpret_cast<const uint4*>(sm + S::kX + cb * kXcb)[r];
-                }
-            }
-        } else {
-            unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hv + h) * 2 * kTile64x128;
-            for (int e = tid; e < C * 16; e += NT) {
-                const int i = e >> 4, ch = e & 15;
-                const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(i, ch, 2 * C));
-                const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&raw);
-                uint32_t hw[4], lw[4];
-                float gL[8], gI[8];
-                ld8(gl + ch * 8, gL);
-                ld8(gam + i * D + ch * 8, gI);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float x0 = i < L ? __bfloat162float(kv[2 * u]) * __expf(gL[2 * u] - gI[2 * u]) : 0.f;
-                    const float x1 = i < L ? __bfloat162float(kv[2 * u + 1]) * __expf(gL[2 * u + 1] - gI[2 * u + 1]) : 0.f;
-                    tc::split2(x0, x1, hw[u], lw[u]);
-                }
-                const uint32_t off = tc::chunk_k128(i, ch, C);
-                *reinterpret_cast<uint4*>(Kdst + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4*>(Kdst + kTile64x128 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            }
-        }
-        float* rec = reinterpret_cast<float*>(p.Rb + ((size_t)chunk * p.Hv + h) * kRec);
-        if (tid < C) rec[tid] = tid < L ? (kKDA ? 1.f : __expf(gl[0] - gam[tid])) : 0.f;
-        if (tid < D) rec[64 + tid] = __expf(kKDA ? gl[tid] : gl[0]);
-        if (tid == 0) reinterpret_cast<int*>(rec)[192] = L;
-    }
-    GDR_TRACE_PREP(2);
-
-    // ---- A (strictly lower) and P (lower incl. diagonal) -------------------------
-    unsigned char* Pdst = p.Yw + ((size_t)chunk * p.Hv + h) * kYwBytes;  // rows 64..127 of column block 0
-    if (!kKDA) {
-        if (!tc::mbar_wait(bar0, ph0, abort_flag)) raise_error(p, 1u);
-        ph0 ^= 1u;
-        tc::fence_after();
-        GDR_TRACE_PREP(24);
-        GDR_TRACE_WARP(0);
-        // thread: accumulator row r = 32 q + lane (rows < 64: K K^T, >= 64: Q K^T),
-        // columns [32 hf, 32 hf + 32)
-        const int r = 32 * q + lane, i = r & 63;
-        // all shared-memory reads first (gam, beta), then the arithmetic, then
-        // the stores: As may alias gam as far as the compiler knows, and an
-        // interleaved load / store order would serialise the 32 elements
-        float gj[32];
-#pragma unroll
-        for (int jj = 0; jj < 32; jj += 4) {
-            const float4 g4 = *reinterpret_cast<const float4*>(gam + 32 * hf + jj);
-            gj[jj] = g4.x; gj[jj + 1] = g4.y; gj[jj + 2] = g4.z; gj[jj + 3] = g4.w;
-        }
-        const float gi = gam[i], bi = bet[i];
-        float gv[32];
-        GDR_TRACE_WARP(3);
-        tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * hf, gv);
-        GDR_TRACE_WARP(4);
-        if (r < C) {
-            const float sc = i < L ? bi : 0.f;
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const int j = 32 * hf + jj;
-                gv[jj] = j < i ? sc * __expf(gi - gj[jj]) * gv[jj] : 0.f;
-            }
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) As[i * LDA + 32 * hf + jj] = gv[jj];
-        } else {
-            uint32_t pk[16];
-            const float sc = i < L ? 1.f : 0.f;
-#pragma unroll
-            for (int jj = 0; jj < 32; jj += 2) {
-                const int j = 32 * hf + jj;
-                const float p0 = j <= i ? sc * __expf(gi - gj[jj]) * gv[jj] : 0.f;
-                const float p1 = j + 1 <= i ? sc * __expf(gi - gj[jj + 1]) * gv[jj + 1] : 0.f;
-                pk[jj >> 1] = tc::pack_bf16(p0, p1);
-            }
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-                *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(C + i, 4 * hf + cc, 2 * C)) =
-                    make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-        }
-        GDR_TRACE_WARP(1);
-    } else {
-        // Per-channel decays: A_ij = beta_i sum_c k_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}
-        // and P_ij = sum_c q_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}.  Pairs in different
-        // halves of a block of 2h tokens (h = 32, 16, 8, 4) go through the tensor
-        // cores with the pivot p = first token of the upper half (j < p <= i):
-        // e^{gam_i - gam_j} = e^{gam_i - gam_p} e^{gam_p - gam_j}, both factors
-        // <= 1, folded into the left (k_i, q_i) and right (k_j) operands, each
-        // split into bf16 hi + lo (3 products).  Pairs inside a 4-token block are
-        // formed directly.  Every exponent is <= 0 for any finite gate.
-        float* Pf = reinterpret_cast<float*>(sm + S::kPf);
-        for (int e = tid; e < C * LDA; e += NT) {
-            As[e] = 0.f;
-            Pf[e] = 0.f;
-        }
-        constexpr uint32_t idL = tc::idesc_bf16(64, 32, false, false);
-        for (int lev = 0; lev < 4; ++lev) {
-            const int sh = 5 - lev, hh = 1 << sh;  // half-block size 32, 16, 8, 4
-            // operand rows: 32 left tokens (K rows 0..31 and Q rows 32..63 of the
-            // 64-row tile) and 32 right tokens, each in 16 chunks of 8 channels
-            for (int e = tid; e < 64 * 16; e += NT) {
-                const int tr = e >> 4, ch = e & 15;
-                const bool left = tr < 32;
-                const int idx = tr & 31, B = idx >> sh, t = idx & (hh - 1);
-                const int piv = 2 * hh * B + hh;
-                const int tok = left ? piv + t : piv - hh + t;
-                const float4* gt = reinterpret_cast<const float4*>(gam + tok * D + ch * 8);
-                const float4* gp = reinterpret_cast<const float4*>(gam + piv * D + ch * 8);
-                float f[8];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const float4 a4 = gt[u], b4 = gp[u];
-                    const float d0 = a4.x - b4.x, d1 = a4.y - b4.y, d2 = a4.z - b4.z, d3 = a4.w - b4.w;
-                    f[4 * u + 0] = __expf(left ? d0 : -d0);
-                    f[4 * u + 1] = __expf(left ? d1 : -d1);
-                    f[4 * u + 2] = __expf(left ? d2 : -d2);
-                    f[4 * u + 3] = __expf(left ? d3 : -d3);
-                }
-                const uint4 kr = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(tok, ch, 2 * C));
-                const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&kr);
-                uint32_t hw[4], lw[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    tc::split2(__bfloat162float(kv[2 * u]) * f[2 * u], __bfloat162float(kv[2 * u + 1]) * f[2 * u + 1],
-                               hw[u], lw[u]);
-                if (left) {
-                    const uint32_t off = tc::chunk_k128(idx, ch, C);
-                    *reinterpret_cast<uint4*>(sm + S::kLh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4*>(sm + S::kLl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                    const uint4 qr = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(C + tok, ch, 2 * C));
-                    const __nv_bfloat16* qv = reinterpret_cast<const __nv_bfloat16*>(&qr);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        tc::split2(__bfloat162float(qv[2 * u]) * f[2 * u], __bfloat162float(qv[2 * u + 1]) * f[2 * u + 1],
-                                   hw[u], lw[u]);
-                    const uint32_t offq = tc::chunk_k128(32 + idx, ch, C);
-                    *reinterpret_cast<uint4*>(sm + S::kLh + offq) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4*>(sm + S::kLl + offq) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                } else {
-                    const uint32_t off = tc::chunk_k128(idx, ch, 32);
-                    *reinterpret_cast<uint4*>(sm + S::kRh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4*>(sm + S::kRl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                }
-            }
-            tc::fence_proxy_async();
-            tc::fence_before();
-            prep_sync<kKDA, kBarId>();
-            tc::fence_after();
-            GDR_TRACE_PREP(9 + 3 * lev);
-            // three issuers, one split product each, into accumulator columns 32 w
-            if (warp < 3 && lane == 0) {
-                const uint32_t la = tc::smem_u32(sm + (warp == 2 ? S::kLl : S::kLh));
-                const uint32_t rb = tc::smem_u32(sm + (warp == 1 ? S::kRl : S::kRh));
-                for (int ks = 0; ks < 8; ++ks)
-                    tc::mma_bf16(tmem + 32 * warp,
-                                 tc::smem_desc(la + (ks >> 2) * (C * 128) + (ks & 3) * 32, 16, 1024, tc::kSwizzle128),
-                                 tc::smem_desc(rb + (ks >> 2) * (32 * 128) + (ks & 3) * 32, 16, 1024, tc::kSwizzle128),
-                                 idL, ks > 0);
-                tc::mma_commit(bar1);
-            }
-            __syncwarp();
-            if (!tc::mbar_wait(bar1, ph1, abort_flag)) raise_error(p, 1u);
-            ph1 ^= 1u;
-            tc::fence_after();
-            GDR_TRACE_PREP(10 + 3 * lev);
-            if (warp < 4) {
-                // M = 64 accumulator: row r = 16 warp + lane (lane < 16); rows 0..31
-                // are A rows, 32..63 P rows; column n pairs with row r when both
-                // fall in the same block of 2h tokens
-                float d[32], e2[32];
-                const uint32_t lrow = tmem + ((uint32_t)(32 * warp) << 16);
-                tc::tmem_ld32(lrow, d);
-                tc::tmem_ld32(lrow + 32, e2);
-#pragma unroll
-                for (int n = 0; n < 32; ++n) d[n] += e2[n];
-                tc::tmem_ld32(lrow + 64, e2);
-#pragma unroll
-                for (int n = 0; n < 32; ++n) d[n] += e2[n];
-                const int r = 16 * warp + lane, idx = r & 31, B = idx >> sh;
-                const int i = 2 * hh * B + hh + (idx & (hh - 1));
-                if (lane < 16 && i < L) {
-                    float* dst = (warp < 2 ? As : Pf) + i * LDA;
-                    const float sc = warp < 2 ? bet[i] : 1.f;
-#pragma unroll
-                    for (int n = 0; n < 32; ++n)
-                        if ((n >> sh) == B) dst[2 * hh * B + (n & (hh - 1))] = sc * d[n];
-                }
-            }
-            tc::fence_before();
-            GDR_TRACE_PREP(11 + 3 * lev);
-        }
-        {
-            // pairs inside a 4-token block: warp w takes the block of tokens
-            // 4w..4w+3 (its 10 pairs j <= i), lane l channels 4l..4l+3; the 10
-            // A sums and the 10 P sums are reduced across the warp together
-            static_assert(!kKDA || NT / 32 == C / 4, "one warp per 4-token block");
-            const int t0 = 4 * warp;
-            float gv[4][4], kf[4][4], qf[4][4];
-#pragma unroll
-            for (int tk = 0; tk < 4; ++tk) {
-                const int tok = t0 + tk;
-                const float4 g4 = *reinterpret_cast<const float4*>(gam + tok * D + 4 * lane);
-                gv[tk][0] = g4.x; gv[tk][1] = g4.y; gv[tk][2] = g4.z; gv[tk][3] = g4.w;
-                const uint2 kr = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(tok, 4 * lane, 2 * C));
-                const uint2 qr = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(C + tok, 4 * lane, 2 * C));
-                const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&kr);
-                const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(&qr);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    kf[tk][c] = __bfloat162float(kb[c]);
-                    qf[tk][c] = __bfloat162float(qb[c]);
-                }
-            }
-            float xs[32];  // [0, 10): A pairs, [10, 20): P pairs
-#pragma unroll
-            for (int pp = 0; pp < 32; ++pp) xs[pp] = 0.f;
-#pragma unroll
-            for (int pr = 0; pr < 10; ++pr) {
-                const int di = (pr >= 1) + (pr >= 3) + (pr >= 6), dj = pr - di * (di + 1) / 2;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float kd = kf[dj][c] * __expf(gv[di][c] - gv[dj][c]);
-                    xs[pr] = fmaf(kf[di][c], kd, xs[pr]);
-                    xs[10 + pr] = fmaf(qf[di][c], kd, xs[10 + pr]);
-                }
-            }
-            const float rs = reduce32_to_lane(xs, lane);
-            if (lane < 20) {
-                const int pr = lane % 10, di = (pr >= 1) + (pr >= 3) + (pr >= 6), dj = pr - di * (di + 1) / 2;
-                const int i = t0 + di, j = t0 + dj;
-                if (i < L) {
-                    if (lane < 10) {
-                        if (j < i) As[i * LDA + j] = bet[i] * rs;
-                    } else {
-                        Pf[i * LDA + j] = rs;
-                    }
-                }
-            }
-        }
-        prep_sync<kKDA, kBarId>();
-        for (int e = tid; e < C * 8; e += NT) {
-            const int i = e >> 3, ch = e & 7;
-            uint32_t w4[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) w4[u] = tc::pack_bf16(Pf[i * LDA + ch * 8 + 2 * u], Pf[i * LDA + ch * 8 + 2 * u + 1]);
-            *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(C + i, ch, 2 * C)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-        }
-        // K o e^{Gam} as hi / lo for W
-        for (int e = tid; e < C * 16; e += NT) {
-            const int i = e >> 4, ch = e & 15;
-            const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(i, ch, 2 * C));
-            const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&raw);
-            uint32_t hw[4], lw[4];
-            float gI[8];
-            ld8(gam + i * D + ch * 8, gI);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                tc::split2(__bfloat162float(kv[2 * u]) * __expf(gI[2 * u]),
-                           __bfloat162float(kv[2 * u + 1]) * __expf(gI[2 * u + 1]), hw[u], lw[u]);
-            const uint32_t off = tc::chunk_k128(i, ch, C);
-            *reinterpret_cast<uint4*>(sm + S::kKgh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(sm + S::kKgl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        }
-    }
-    tc::fence_before();
-    prep_sync<kKDA, kBarId>();
-    GDR_TRACE_PREP(3);
-    GDR_TRACE_WARP(2);
-
-    // ---- Tm = (I + A)^{-1} -----------------------------------------------------------
-    solve_unit_lower<NT, kBarId>(As, Tm, Z, tid);
-    GDR_TRACE_PREP(4);
-
-    // ---- split operands: T' = Tm diag(beta e^{gam}) (scalar gate) or Tm diag(beta);
-    //      T'' = Tm diag(beta).  Written over the dead Q rows of X and the A matrix.
-    for (int e = tid; e < C * 8; e += NT) {
-        const int i = e >> 3, ch = e & 7;
-        uint32_t h1[4], l1[4], h2[4], l2[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int j = ch * 8 + 2 * u;
-            const float t0 = Tm[i * LDA + j] * bet[j], t1 = Tm[i * LDA + j + 1] * bet[j + 1];
-            tc::split2(kKDA ? t0 : t0 * __expf(gam[j]), kKDA ? t1 : t1 * __expf(gam[j + 1]), h1[u], l1[u]);
-            tc::split2(t0, t1, h2[u], l2[u]);
-        }
-        const uint32_t off = tc::chunk_k128(i, ch, C);
-        *reinterpret_cast<uint4*>(sm + S::kT1h + off) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
-        *reinterpret_cast<uint4*>(sm + S::kT1l + off) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
-        *reinterpret_cast<uint4*>(sm + S::kT2h + off) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
-        *reinterpret_cast<uint4*>(sm + S::kT2l + off) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
-    }
-    tc::fence_proxy_async();
-    prep_sync<kKDA, kBarId>();
-    GDR_TRACE_PREP(5);
-
-    // ---- W = T' K (or T'' (K o e^Gam)), U = T'' V ----------------------------------------
-    if (tid == 0) {
-        tc::fence_after();
-        constexpr uint32_t id = tc::idesc_bf16(64, 128, false, true);
-        const uint32_t t1h = tc::smem_u32(sm + S::kT1h), t1l = tc::smem_u32(sm + S::kT1l);
-        const uint32_t t2h = tc::smem_u32(sm + S::kT2h), t2l = tc::smem_u32(sm + S::kT2l);
-        // B operands read MN-major: K rows of X (atom stride kXcb), V / Kg (atom stride 8 KB)
-        auto mm = [&](uint32_t dcol, uint32_t a, uint32_t b, uint32_t atom, bool first) {
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_bf16(tmem + dcol, tc::smem_desc(a + ks * 32, 16, 1024, tc::kSwizzle128),
-                             tc::smem_desc(b + ks * 2048, atom, 1024, tc::kSwizzle128), id, (first && ks == 0) ? 0u : 1u);
-        };
-        if (!kKDA) {
-            mm(0, t1h, sX, kXcb, true);
-            mm(0, t1l, sX, kXcb, false);
-        } else {
-            const uint32_t kgh = tc::smem_u32(sm + S::kKgh), kgl = tc::smem_u32(sm + S::kKgl);
-            mm(0, t2h, kgh, C * 128, true);
-            mm(0, t2h, kgl, C * 128, false);
-            mm(0, t2l, kgh, C * 128, false);
-        }
-        mm(128, t2h, sV, C * 128, true);
-        mm(128, t2l, sV, C * 128, false);
-        tc::mma_commit(bar0);
-    }
-    __syncwarp();
-    GDR_TRACE_PREP(6);
-
-    // ---- W, U out of TMEM into their blobs: row i = 16 q + lane (lane < 16);
-    //      8 warps: columns [64 hf, 64 hf + 64) of W and of U, 16 warps: columns
-    //      [32 hf, 32 hf + 32).  The images are staged in
-    //      shared memory left dead by the finished MMAs (W hi / lo as 64-row k128
-    //      tiles over X, U value-major over V and A) and written with bulk copies,
-    //      so every global write is a contiguous run. ---------------------------------
-    // the item's last completion of bar0 (the scalar gate's K K^T / Q K^T group was the first)
-    if (!tc::mbar_wait(bar0, ph0, abort_flag)) raise_error(p, 1u);
-    ph0 ^= 1u;
-    tc::fence_after();
-    {
-        const int i = 16 * q + (lane & 15);
-        const uint32_t lrow = tmem + ((uint32_t)(32 * q) << 16);
-        unsigned char* sWh = sm + S::kX;            // [64][128] k128, column-block stride 8 KB
-        unsigned char* sWl = sm + S::kX + kTile64x128;
-        float* sU = reinterpret_cast<float*>(sm + S::kV);  // 4 x [32 v][64 i]
-        constexpr int kBlocks = 512 / NT;  // 32-column blocks per warp: 2 (8 warps) or 1 (16 warps)
-        for (int q2 = 0; q2 < kBlocks; ++q2) {
-            const int cb = kBlocks * hf + q2;  // 32-column block of W and of U
-            float wv[32], uv[32];
-            tc::tmem_ld32(lrow + 32 * cb, wv);
-            tc::tmem_ld32(lrow + 128 + 32 * cb, uv);
-            if (lane < 16) {
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t hw[4], lw[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) tc::split2(wv[8 * cc + 2 * u], wv[8 * cc + 2 * u + 1], hw[u], lw[u]);
-                    const uint32_t off = tc::chunk_k128(i, 4 * cb + cc, C);
-                    *reinterpret_cast<uint4*>(sWh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4*>(sWl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                }
-                // U block cb value-major [32 v][64 i]: the chain's thread for row i
-                // then reads a conflict-free column of shared memory
-                float* ublk = sU + cb * (C * BV) + i;
-#pragma unroll
-                for (int v = 0; v < BV; ++v) ublk[v * C] = uv[v];
-            }
-        }
-        tc::fence_proxy_async();
-        prep_sync<kKDA, kBarId>();
-        if (tid == 0) {
-            unsigned char* Xd = p.Xw + ((size_t)chunk * p.Hv + h) * kXwBytes;  // rows 0..63 of each column block
-            unsigned char* Yd = p.Yw + ((size_t)chunk * p.Hv + h) * kYwBytes;
-            const uint32_t half = kTile64x128 / 2;  // one 64-row column block
-            tc::bulk_s2g(Xd, tc::smem_u32(sWh), half);
-            tc::bulk_s2g(Xd + 2 * half, tc::smem_u32(sWh) + half, half);
-            tc::bulk_s2g(Yd, tc::smem_u32(sWl), half);
-            tc::bulk_s2g(Yd + 2 * half, tc::smem_u32(sWl) + half, half);
-            tc::bulk_s2g(p.Ub + ((size_t)chunk * p.Hv + h) * NVB * kUBlock, tc::smem_u32(sU), NVB * kUBlock);
-            tc::bulk_commit();
-            if (ready) tc::bulk_wait_all();  // published below: the images must have landed
-            else tc::bulk_wait_read();       // the staging area is reused by the next item
-        }
-    }
-    if (ready) __threadfence();  // this thread's image stores, before the flag
-    GDR_TRACE_PREP(7);
-    tc::fence_before();
-    prep_sync<kKDA, kBarId>();
-    tc::fence_after();
-    GDR_TRACE_PREP(8);
-    GDR_TRACE_ITEM(item, 1);
-    if (ready && tid == 0) {  // every image of this (chunk, head) item is in global memory
-        tc::fence_proxy_async_global();
-        tc::st_release_gpu(ready + item, 1);
-    }
-}
-
-template <bool kKDA>
-__global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep_kernel(TcParams p) {
-    using S = PrepSmem<kKDA>;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    // Persistent: CTA x takes items x, x + gridDim.x, ... (item = chunk * Hv + h)
-    // and warms L2 with the next item's rows while it computes the current one.
-    const int tid = threadIdx.x, warp = tid >> 5;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::kBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::kBar + 16);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::kBar + 24);
@@ -890,9 +371,497 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
     const int nitems = p.meta[0] * p.Hv;
 
     for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
-        const int nxt = item + (int)gridDim.x;
-        prep_item<kKDA, 0>(p, item, nxt < nitems ? nxt : -1, sm, tmem, bar0, bar1, ph0, ph1, abort_flag, tid, nullptr);
-    }
+        const int chunk = item / p.Hv, h = item - chunk * p.Hv;
+        const int4 info = p.table[chunk];
+        const int start = info.y, L = info.z;
+        const int kh = h / grp;
+
+        GDR_TRACE_PREP(0);
+        GDR_TRACE_ITEM(item, 0);
+        // ---- stage K, Q (as X) and V rows (cp.async), gates, beta -------------------
+        stage_rows_async<NT>(sm + S::kX, 2 * C, 0, kp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
+        stage_rows_async<NT>(sm + S::kX, 2 * C, C, qp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
+        stage_rows_async<NT>(sm + S::kV, C, 0, vp + ((size_t)start * p.Hv + h) * D, (size_t)p.Hv * D, L, tid);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        {
+            const int nxt = item + (int)gridDim.x;
+            if (nxt < nitems) {
+                const int nc = nxt / p.Hv, nh = nxt - nc * p.Hv;
+                const int4 ni = p.table[nc];
+                const int r = tid & 63, which = tid >> 6;
+                const size_t tok = (size_t)ni.y + r;
+                if (r < ni.z) {
+                    if (which == 0) tc::prefetch_l2(kp + (tok * p.Hk + nh / grp) * D, D * 2);
+                    else if (which == 1) tc::prefetch_l2(qp + (tok * p.Hk + nh / grp) * D, D * 2);
+                    else if (which == 2) tc::prefetch_l2(vp + (tok * p.Hv + nh) * D, D * 2);
+                    else if (kKDA && which == 3) tc::prefetch_l2(p.gk + (tok * p.Hv + nh) * D, D * 4);
+                }
+                if (!kKDA && tid == 255) tc::prefetch_l2_span(p.g + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 4);
+                if (tid == 254) tc::prefetch_l2_span(bp + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 2);
+            }
+        }
+        if (tid < C) bet[tid] = tid < L ? to_f(bp[((size_t)start + tid) * p.Hv + h]) : 0.f;
+        if (kKDA) {
+            // per-channel inclusive cumsum in token order: thread (channel c, quarter
+            // qt) scans tokens 16 qt .. 16 qt + 15 (all 16 loads issued before the
+            // dependent adds), then adds the totals of the earlier quarters
+            static_assert(!kKDA || NT == 4 * D, "one thread per channel and quarter of the chunk");
+            const int c = tid & (D - 1), qt = tid >> 7;
+            const float* __restrict__ gk = p.gk + ((size_t)start * p.Hv + h) * D + c;
+            float x[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int i = 16 * qt + u;
+                x[u] = i < L ? __ldg(gk + (size_t)i * p.Hv * D) : 0.f;
+            }
+#pragma unroll
+            for (int u = 1; u < 16; ++u) x[u] += x[u - 1];
+            Z[qt * D + c] = x[15];  // Z is free until the solve
+            __syncthreads();
+            float off = 0.f;
+            for (int u = 0; u < qt; ++u) off += Z[u * D + c];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) gam[(16 * qt + u) * D + c] = x[u] + off;
+        } else if (warp < 2) {
+            // scalar gate: inclusive scan over 64 tokens with two warps
+            float x = tid < L ? __ldg(p.g + ((size_t)start + tid) * p.Hv + h) : 0.f;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, off);
+                if (lane >= off) x += y;
+            }
+            gam[tid] = x;
+        }
+        __syncthreads();
+        if (!kKDA && warp == 1) gam[tid] += gam[31];
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        tc::fence_proxy_async();
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+        GDR_TRACE_PREP(1);
+        const uint32_t sX = tc::smem_u32(sm + S::kX), sV = tc::smem_u32(sm + S::kV);
+        const float* gl = kKDA ? gam + (L - 1) * D : gam + (L - 1);
+
+        // ---- [K K^T ; Q K^T] on the tensor cores (scalar gate), one M = 128 group ------
+        if (!kKDA && tid == 0) {
+            constexpr uint32_t id = tc::idesc_bf16(128, 64, false, false);
+            for (int ks = 0; ks < 8; ++ks) {
+                const uint32_t off = (ks >> 2) * kXcb + (ks & 3) * 32;
+                tc::mma_bf16(tmem, tc::smem_desc(sX + off, 16, 1024, tc::kSwizzle128),
+                             tc::smem_desc(sX + off, 16, 1024, tc::kSwizzle128), id, ks > 0);
+            }
+            tc::mma_commit(bar0);
+        }
+        __syncwarp();
+
+        // ---- while that runs: Qd blob, K / Kd blob, decay record ------------------------
+        {
+            unsigned char* Qdst = p.Xw + ((size_t)chunk * p.Hv + h) * kXwBytes;  // rows 64..127
+            for (int e = tid; e < C * 16; e += NT) {
+                const int i = e >> 4, ch = e & 15;
+                const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(C + i, ch, 2 * C));
+                const __nv_bfloat16* qv = reinterpret_cast<const __nv_bfloat16*>(&raw);
+                uint32_t w4[4];
+                float gq[8];
+                if (kKDA) ld8(gam + i * D + ch * 8, gq);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float g0 = kKDA ? gq[2 * u] : gam[i], g1 = kKDA ? gq[2 * u + 1] : gam[i];
+                    w4[u] = tc::pack_bf16(__bfloat162float(qv[2 * u]) * __expf(g0),
+                                          __bfloat162float(qv[2 * u + 1]) * __expf(g1));
+                }
+                *reinterpret_cast<uint4*>(Qdst + tc::chunk_k128(C + i, ch, 2 * C)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+            if (!kKDA) {
+                if (h % grp == 0) {  // K rows of X, both column blocks -> a [64][128] k128 image
+                    unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hk + kh) * kTile64x128;
+                    for (int e = tid; e < (int)(kTile64x128 / 16); e += NT) {
+                        const int cb = e >> 9, r = e & 511;
+                        reinterpret_cast<uint4*>(Kdst)[e] = reinterpret_cast<const uint4*>(sm + S::kX + cb * kXcb)[r];
+                    }
+                }
+            } else {
+                unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hv + h) * 2 * kTile64x128;
+                for (int e = tid; e < C * 16; e += NT) {
+                    const int i = e >> 4, ch = e & 15;
+                    const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(i, ch, 2 * C));
+                    const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&raw);
+                    uint32_t hw[4], lw[4];
+                    float gL[8], gI[8];
+                    ld8(gl + ch * 8, gL);
+                    ld8(gam + i * D + ch * 8, gI);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float x0 = i < L ? __bfloat162float(kv[2 * u]) * __expf(gL[2 * u] - gI[2 * u]) : 0.f;
+                        const float x1 = i < L ? __bfloat162float(kv[2 * u + 1]) * __expf(gL[2 * u + 1] - gI[2 * u + 1]) : 0.f;
+                        tc::split2(x0, x1, hw[u], lw[u]);
+                    }
+                    const uint32_t off = tc::chunk_k128(i, ch, C);
+                    *reinterpret_cast<uint4*>(Kdst + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4*>(Kdst + kTile64x128 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
+            }
+            float* rec = reinterpret_cast<float*>(p.Rb + ((size_t)chunk * p.Hv + h) * kRec);
+            if (tid < C) rec[tid] = tid < L ? (kKDA ? 1.f : __expf(gl[0] - gam[tid])) : 0.f;
+            if (tid < D) rec[64 + tid] = __expf(kKDA ? gl[tid] : gl[0]);
+            if (tid == 0) reinterpret_cast<int*>(rec)[192] = L;
+        }
+        GDR_TRACE_PREP(2);
+
+        // ---- A (strictly lower) and P (lower incl. diagonal) -------------------------
+        unsigned char* Pdst = p.Yw + ((size_t)chunk * p.Hv + h) * kYwBytes;  // rows 64..127 of column block 0
+        if (!kKDA) {
+            if (!tc::mbar_wait(bar0, ph0, abort_flag)) raise_error(p, 1u);
+            ph0 ^= 1u;
+            tc::fence_after();
+            GDR_TRACE_PREP(24);
+            GDR_TRACE_WARP(0);
+            // thread: accumulator row r = 32 q + lane (rows < 64: K K^T, >= 64: Q K^T),
+            // columns [32 hf, 32 hf + 32)
+            const int r = 32 * q + lane, i = r & 63;
+            // all shared-memory reads first (gam, beta), then the arithmetic, then
+            // the stores: As may alias gam as far as the compiler knows, and an
+            // interleaved load / store order would serialise the 32 elements
+            float gj[32];
+#pragma unroll
+            for (int jj = 0; jj < 32; jj += 4) {
+                const float4 g4 = *reinterpret_cast<const float4*>(gam + 32 * hf + jj);
+                gj[jj] = g4.x; gj[jj + 1] = g4.y; gj[jj + 2] = g4.z; gj[jj + 3] = g4.w;
+            }
+            const float gi = gam[i], bi = bet[i];
+            float gv[32];
+            GDR_TRACE_WARP(3);
+            tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * hf, gv);
+            GDR_TRACE_WARP(4);
+            if (r < C) {
+                const float sc = i < L ? bi : 0.f;
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = 32 * hf + jj;
+                    gv[jj] = j < i ? sc * __expf(gi - gj[jj]) * gv[jj] : 0.f;
+                }
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) As[i * LDA + 32 * hf + jj] = gv[jj];
+            } else {
+                uint32_t pk[16];
+                const float sc = i < L ? 1.f : 0.f;
+#pragma unroll
+                for (int jj = 0; jj < 32; jj += 2) {
+                    const int j = 32 * hf + jj;
+                    const float p0 = j <= i ? sc * __expf(gi - gj[jj]) * gv[jj] : 0.f;
+                    const float p1 = j + 1 <= i ? sc * __expf(gi - gj[jj + 1]) * gv[jj + 1] : 0.f;
+                    pk[jj >> 1] = tc::pack_bf16(p0, p1);
+                }
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc)
+                    *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(C + i, 4 * hf + cc, 2 * C)) =
+                        make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+            }
+            GDR_TRACE_WARP(1);
+        } else {
+            // Per-channel decays: A_ij = beta_i sum_c k_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}
+            // and P_ij = sum_c q_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}.  Pairs in different
+            // halves of a block of 2h tokens (h = 32, 16, 8, 4) go through the tensor
+            // cores with the pivot p = first token of the upper half (j < p <= i):
+            // e^{gam_i - gam_j} = e^{gam_i - gam_p} e^{gam_p - gam_j}, both factors
+            // <= 1, folded into the left (k_i, q_i) and right (k_j) operands, each
+            // split into bf16 hi + lo (3 products).  Pairs inside a 4-token block are
+            // formed directly.  Every exponent is <= 0 for any finite gate.
+            float* Pf = reinterpret_cast<float*>(sm + S::kPf);
+            for (int e = tid; e < C * LDA; e += NT) {
+                As[e] = 0.f;
+                Pf[e] = 0.f;
+            }
+            constexpr uint32_t idL = tc::idesc_bf16(64, 32, false, false);
+            for (int lev = 0; lev < 4; ++lev) {
+                const int sh = 5 - lev, hh = 1 << sh;  // half-block size 32, 16, 8, 4
+                // operand rows: 32 left tokens (K rows 0..31 and Q rows 32..63 of the
+                // 64-row tile) and 32 right tokens, each in 16 chunks of 8 channels
+                for (int e = tid; e < 64 * 16; e += NT) {
+                    const int tr = e >> 4, ch = e & 15;
+                    const bool left = tr < 32;
+                    const int idx = tr & 31, B = idx >> sh, t = idx & (hh - 1);
+                    const int piv = 2 * hh * B + hh;
+                    const int tok = left ? piv + t : piv - hh + t;
+                    const float4* gt = reinterpret_cast<const float4*>(gam + tok * D + ch * 8);
+                    const float4* gp = reinterpret_cast<const float4*>(gam + piv * D + ch * 8);
+                    float f[8];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const float4 a4 = gt[u], b4 = gp[u];
+                        const float d0 = a4.x - b4.x, d1 = a4.y - b4.y, d2 = a4.z - b4.z, d3 = a4.w - b4.w;
+                        f[4 * u + 0] = __expf(left ? d0 : -d0);
+                        f[4 * u + 1] = __expf(left ? d1 : -d1);
+                        f[4 * u + 2] = __expf(left ? d2 : -d2);
+                        f[4 * u + 3] = __expf(left ? d3 : -d3);
+                    }
+                    const uint4 kr = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(tok, ch, 2 * C));
+                    const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&kr);
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        tc::split2(__bfloat162float(kv[2 * u]) * f[2 * u], __bfloat162float(kv[2 * u + 1]) * f[2 * u + 1],
+                                   hw[u], lw[u]);
+                    if (left) {
+                        const uint32_t off = tc::chunk_k128(idx, ch, C);
+                        *reinterpret_cast<uint4*>(sm + S::kLh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4*>(sm + S::kLl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                        const uint4 qr = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(C + tok, ch, 2 * C));
+                        const __nv_bfloat16* qv = reinterpret_cast<const __nv_bfloat16*>(&qr);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            tc::split2(__bfloat162float(qv[2 * u]) * f[2 * u], __bfloat162float(qv[2 * u + 1]) * f[2 * u + 1],
+                                       hw[u], lw[u]);
+                        const uint32_t offq = tc::chunk_k128(32 + idx, ch, C);
+                        *reinterpret_cast<uint4*>(sm + S::kLh + offq) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4*>(sm + S::kLl + offq) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    } else {
+                        const uint32_t off = tc::chunk_k128(idx, ch, 32);
+                        *reinterpret_cast<uint4*>(sm + S::kRh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4*>(sm + S::kRl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    }
+                }
+                tc::fence_proxy_async();
+                tc::fence_before();
+                __syncthreads();
+                tc::fence_after();
+                GDR_TRACE_PREP(9 + 3 * lev);
+                // three issuers, one split product each, into accumulator columns 32 w
+                if (warp < 3 && lane == 0) {
+                    const uint32_t la = tc::smem_u32(sm + (warp == 2 ? S::kLl : S::kLh));
+                    const uint32_t rb = tc::smem_u32(sm + (warp == 1 ? S::kRl : S::kRh));
+                    for (int ks = 0; ks < 8; ++ks)
+                        tc::mma_bf16(tmem + 32 * warp,
+                                     tc::smem_desc(la + (ks >> 2) * (C * 128) + (ks & 3) * 32, 16, 1024, tc::kSwizzle128),
+                                     tc::smem_desc(rb + (ks >> 2) * (32 * 128) + (ks & 3) * 32, 16, 1024, tc::kSwizzle128),
+                                     idL, ks > 0);
+                    tc::mma_commit(bar1);
+                }
+                __syncwarp();
+                if (!tc::mbar_wait(bar1, ph1, abort_flag)) raise_error(p, 1u);
+                ph1 ^= 1u;
+                tc::fence_after();
+                GDR_TRACE_PREP(10 + 3 * lev);
+                if (warp < 4) {
+                    // M = 64 accumulator: row r = 16 warp + lane (lane < 16); rows 0..31
+                    // are A rows, 32..63 P rows; column n pairs with row r when both
+                    // fall in the same block of 2h tokens
+                    float d[32], e2[32];
+                    const uint32_t lrow = tmem + ((uint32_t)(32 * warp) << 16);
+                    tc::tmem_ld32(lrow, d);
+                    tc::tmem_ld32(lrow + 32, e2);
+#pragma unroll
+                    for (int n = 0; n < 32; ++n) d[n] += e2[n];
+                    tc::tmem_ld32(lrow + 64, e2);
+#pragma unroll
+                    for (int n = 0; n < 32; ++n) d[n] += e2[n];
+                    const int r = 16 * warp + lane, idx = r & 31, B = idx >> sh;
+                    const int i = 2 * hh * B + hh + (idx & (hh - 1));
+                    if (lane < 16 && i < L) {
+                        float* dst = (warp < 2 ? As : Pf) + i * LDA;
+                        const float sc = warp < 2 ? bet[i] : 1.f;
+#pragma unroll
+                        for (int n = 0; n < 32; ++n)
+                            if ((n >> sh) == B) dst[2 * hh * B + (n & (hh - 1))] = sc * d[n];
+                    }
+                }
+                tc::fence_before();
+                GDR_TRACE_PREP(11 + 3 * lev);
+            }
+            {
+                // pairs inside a 4-token block: warp w takes the block of tokens
+                // 4w..4w+3 (its 10 pairs j <= i), lane l channels 4l..4l+3; the 10
+                // A sums and the 10 P sums are reduced across the warp together
+                static_assert(!kKDA || NT / 32 == C / 4, "one warp per 4-token block");
+                const int t0 = 4 * warp;
+                float gv[4][4], kf[4][4], qf[4][4];
+#pragma unroll
+                for (int tk = 0; tk < 4; ++tk) {
+                    const int tok = t0 + tk;
+                    const float4 g4 = *reinterpret_cast<const float4*>(gam + tok * D + 4 * lane);
+                    gv[tk][0] = g4.x; gv[tk][1] = g4.y; gv[tk][2] = g4.z; gv[tk][3] = g4.w;
+                    const uint2 kr = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(tok, 4 * lane, 2 * C));
+                    const uint2 qr = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(C + tok, 4 * lane, 2 * C));
+                    const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&kr);
+                    const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(&qr);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        kf[tk][c] = __bfloat162float(kb[c]);
+                        qf[tk][c] = __bfloat162float(qb[c]);
+                    }
+                }
+                float xs[32];  // [0, 10): A pairs, [10, 20): P pairs
+#pragma unroll
+                for (int pp = 0; pp < 32; ++pp) xs[pp] = 0.f;
+#pragma unroll
+                for (int pr = 0; pr < 10; ++pr) {
+                    const int di = (pr >= 1) + (pr >= 3) + (pr >= 6), dj = pr - di * (di + 1) / 2;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const float kd = kf[dj][c] * __expf(gv[di][c] - gv[dj][c]);
+                        xs[pr] = fmaf(kf[di][c], kd, xs[pr]);
+                        xs[10 + pr] = fmaf(qf[di][c], kd, xs[10 + pr]);
+                    }
+                }
+                const float rs = reduce32_to_lane(xs, lane);
+                if (lane < 20) {
+                    const int pr = lane % 10, di = (pr >= 1) + (pr >= 3) + (pr >= 6), dj = pr - di * (di + 1) / 2;
+                    const int i = t0 + di, j = t0 + dj;
+                    if (i < L) {
+                        if (lane < 10) {
+                            if (j < i) As[i * LDA + j] = bet[i] * rs;
+                        } else {
+                            Pf[i * LDA + j] = rs;
+                        }
+                    }
+                }
+            }
+            __syncthreads();
+            for (int e = tid; e < C * 8; e += NT) {
+                const int i = e >> 3, ch = e & 7;
+                uint32_t w4[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) w4[u] = tc::pack_bf16(Pf[i * LDA + ch * 8 + 2 * u], Pf[i * LDA + ch * 8 + 2 * u + 1]);
+                *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(C + i, ch, 2 * C)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+            // K o e^{Gam} as hi / lo for W
+            for (int e = tid; e < C * 16; e += NT) {
+                const int i = e >> 4, ch = e & 15;
+                const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(i, ch, 2 * C));
+                const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&raw);
+                uint32_t hw[4], lw[4];
+                float gI[8];
+                ld8(gam + i * D + ch * 8, gI);
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    tc::split2(__bfloat162float(kv[2 * u]) * __expf(gI[2 * u]),
+                               __bfloat162float(kv[2 * u + 1]) * __expf(gI[2 * u + 1]), hw[u], lw[u]);
+                const uint32_t off = tc::chunk_k128(i, ch, C);
+                *reinterpret_cast<uint4*>(sm + S::kKgh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(sm + S::kKgl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+        }
+        tc::fence_before();
+        __syncthreads();
+        GDR_TRACE_PREP(3);
+        GDR_TRACE_WARP(2);
+
+        // ---- Tm = (I + A)^{-1} -----------------------------------------------------------
+        solve_unit_lower<NT>(As, Tm, Z, tid);
+        GDR_TRACE_PREP(4);
+
+        // ---- split operands: T' = Tm diag(beta e^{gam}) (scalar gate) or Tm diag(beta);
+        //      T'' = Tm diag(beta).  Written over the dead Q rows of X and the A matrix.
+        for (int e = tid; e < C * 8; e += NT) {
+            const int i = e >> 3, ch = e & 7;
+            uint32_t h1[4], l1[4], h2[4], l2[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = ch * 8 + 2 * u;
+                const float t0 = Tm[i * LDA + j] * bet[j], t1 = Tm[i * LDA + j + 1] * bet[j + 1];
+                tc::split2(kKDA ? t0 : t0 * __expf(gam[j]), kKDA ? t1 : t1 * __expf(gam[j + 1]), h1[u], l1[u]);
+                tc::split2(t0, t1, h2[u], l2[u]);
+            }
+            const uint32_t off = tc::chunk_k128(i, ch, C);
+            *reinterpret_cast<uint4*>(sm + S::kT1h + off) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
+            *reinterpret_cast<uint4*>(sm + S::kT1l + off) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
+            *reinterpret_cast<uint4*>(sm + S::kT2h + off) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+            *reinterpret_cast<uint4*>(sm + S::kT2l + off) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
+        }
+        tc::fence_proxy_async();
+        __syncthreads();
+        GDR_TRACE_PREP(5);
+
+        // ---- W = T' K (or T'' (K o e^Gam)), U = T'' V ----------------------------------------
+        if (tid == 0) {
+            tc::fence_after();
+            constexpr uint32_t id = tc::idesc_bf16(64, 128, false, true);
+            const uint32_t t1h = tc::smem_u32(sm + S::kT1h), t1l = tc::smem_u32(sm + S::kT1l);
+            const uint32_t t2h = tc::smem_u32(sm + S::kT2h), t2l = tc::smem_u32(sm + S::kT2l);
+            // B operands read MN-major: K rows of X (atom stride kXcb), V / Kg (atom stride 8 KB)
+            auto mm = [&](uint32_t dcol, uint32_t a, uint32_t b, uint32_t atom, bool first) {
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16(tmem + dcol, tc::smem_desc(a + ks * 32, 16, 1024, tc::kSwizzle128),
+                                 tc::smem_desc(b + ks * 2048, atom, 1024, tc::kSwizzle128), id, (first && ks == 0) ? 0u : 1u);
+            };
+            if (!kKDA) {
+                mm(0, t1h, sX, kXcb, true);
+                mm(0, t1l, sX, kXcb, false);
+            } else {
+                const uint32_t kgh = tc::smem_u32(sm + S::kKgh), kgl = tc::smem_u32(sm + S::kKgl);
+                mm(0, t2h, kgh, C * 128, true);
+                mm(0, t2h, kgl, C * 128, false);
+                mm(0, t2l, kgh, C * 128, false);
+            }
+            mm(128, t2h, sV, C * 128, true);
+            mm(128, t2l, sV, C * 128, false);
+            tc::mma_commit(bar0);
+        }
+        __syncwarp();
+        GDR_TRACE_PREP(6);
+
+        // ---- W, U out of TMEM into their blobs: row i = 16 q + lane (lane < 16);
+        //      8 warps: columns [64 hf, 64 hf + 64) of W and of U, 16 warps: columns
+        //      [32 hf, 32 hf + 32).  The images are staged in
+        //      shared memory left dead by the finished MMAs (W hi / lo as 64-row k128
+        //      tiles over X, U value-major over V and A) and written with bulk copies,
+        //      so every global write is a contiguous run. ---------------------------------
+        // the item's last completion of bar0 (the scalar gate's K K^T / Q K^T group was the first)
+        if (!tc::mbar_wait(bar0, ph0, abort_flag)) raise_error(p, 1u);
+        ph0 ^= 1u;
+        tc::fence_after();
+        {
+            const int i = 16 * q + (lane & 15);
+            const uint32_t lrow = tmem + ((uint32_t)(32 * q) << 16);
+            unsigned char* sWh = sm + S::kX;            // [64][128] k128, column-block stride 8 KB
+            unsigned char* sWl = sm + S::kX + kTile64x128;
+            float* sU = reinterpret_cast<float*>(sm + S::kV);  // 4 x [32 v][64 i]
+            constexpr int kBlocks = 512 / NT;  // 32-column blocks per warp: 2 (8 warps) or 1 (16 warps)
+            for (int q2 = 0; q2 < kBlocks; ++q2) {
+                const int cb = kBlocks * hf + q2;  // 32-column block of W and of U
+                float wv[32], uv[32];
+                tc::tmem_ld32(lrow + 32 * cb, wv);
+                tc::tmem_ld32(lrow + 128 + 32 * cb, uv);
+                if (lane < 16) {
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t hw[4], lw[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) tc::split2(wv[8 * cc + 2 * u], wv[8 * cc + 2 * u + 1], hw[u], lw[u]);
+                        const uint32_t off = tc::chunk_k128(i, 4 * cb + cc, C);
+                        *reinterpret_cast<uint4*>(sWh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4*>(sWl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    }
+                    // U block cb value-major [32 v][64 i]: the chain's thread for row i
+                    // then reads a conflict-free column of shared memory
+                    float* ublk = sU + cb * (C * BV) + i;
+#pragma unroll
+                    for (int v = 0; v < BV; ++v) ublk[v * C] = uv[v];
+                }
+            }
+            tc::fence_proxy_async();
+            __syncthreads();
+            if (tid == 0) {
+                unsigned char* Xd = p.Xw + ((size_t)chunk * p.Hv + h) * kXwBytes;  // rows 0..63 of each column block
+                unsigned char* Yd = p.Yw + ((size_t)chunk * p.Hv + h) * kYwBytes;
+                const uint32_t half = kTile64x128 / 2;  // one 64-row column block
+                tc::bulk_s2g(Xd, tc::smem_u32(sWh), half);
+                tc::bulk_s2g(Xd + 2 * half, tc::smem_u32(sWh) + half, half);
+                tc::bulk_s2g(Yd, tc::smem_u32(sWl), half);
+                tc::bulk_s2g(Yd + 2 * half, tc::smem_u32(sWl) + half, half);
+                tc::bulk_s2g(p.Ub + ((size_t)chunk * p.Hv + h) * NVB * kUBlock, tc::smem_u32(sU), NVB * kUBlock);
+                tc::bulk_commit();
+                tc::bulk_wait_read();  // the staging area is reused by the next item
+            }
+        }
+        GDR_TRACE_PREP(7);
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+        GDR_TRACE_PREP(8);
+        GDR_TRACE_ITEM(item, 1);
+    }  // item loop
     if (tid == 0) tc::bulk_wait_all();
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
 }
@@ -935,21 +904,68 @@ __device__ __forceinline__ uint32_t chain_bar_count(int i) {
     return i == kD1Full ? 2u : (i == kEmpty0 || i == kEmpty1) ? 3u : 1u;
 }
 
-// The chain over one work unit (value head h, value block vb, nc chunks from
-// global chunk c0 of sequence b; segment fields as in TcParams::mode).  The
-// caller has allocated TMEM (256 columns at tmem) and initialised the
-// barriers in the stage layout at sm.  With ready != nullptr each chunk's
-// copies wait for the flags of the prep items that wrote its images.
 template <bool kKDA>
-__device__ __forceinline__ void chain_body(const TcParams& p, unsigned char* sm, const uint32_t tmem, uint64_t* bars,
-                                           volatile int* abort_flag, const int tid, const int b, const int h,
-                                           const int vb, const int nc, const int c0, const int cs0, const int sg,
-                                           const bool last, const bool transition, const bool first,
-                                           const bool outputs, const int* ready) {
+__global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
     using S = ChainSmem<kKDA>;
-    const int warp = tid >> 5, lane = tid & 31;
-    const int v0 = vb * BV;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::kBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::kBar + 8 * kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::kBar + 8 * kNumBars + 8);
     auto bar = [&](int i) { return tc::smem_u32(&bars[i]); };
+
+    // prologue (touches no memory the earlier kernels write), then wait for them
+    if (warp == 2) tc::tmem_alloc(tc::smem_u32(tmem_slot), 256);
+    if (tid == 0) {
+        for (int i = 0; i < kNumBars; ++i) tc::mbar_init(bar(i), chain_bar_count(i));
+        *abort_flag = 0;
+        tc::mbar_fence_init();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+    tc::grid_dep_wait();
+    if (!p.meta[1]) {  // malformed cu_seqlens
+        tc::fence_before();
+        __syncthreads();
+        if (warp == 2) tc::tmem_dealloc(tmem, 256);
+        return;
+    }
+    // Work unit: a whole sequence (mode 0) or one segment of G chunks of it
+    // (modes 1 and 2; the summary pass runs two CTA sets, the transition from
+    // the identity with U = 0 and the offset from zero).
+    const int hx = blockIdx.x % (p.Hv * NVB);
+    const bool transition = p.mode == 1 && blockIdx.x >= p.Hv * NVB;
+    const int h = hx / NVB, vb = hx % NVB, v0 = vb * BV;
+    int b, nc, c0, cs0 = 0, sg = 0;
+    bool last = true;
+    if (p.mode == 0) {
+        b = p.order[blockIdx.y];
+        nc = (p.cu[b + 1] - p.cu[b] + C - 1) / C;
+        c0 = p.offsets[b];
+    } else {
+        sg = blockIdx.y;
+        bool idle = sg >= p.meta[2];  // beyond this call's segment count
+        if (!idle) {
+            const int4 e = p.segs[sg];
+            b = e.x; cs0 = e.y; nc = e.z; last = e.w != 0;
+            c0 = p.offsets[b] + cs0;
+            // the first segment of a sequence runs from h0 in the summary pass
+            // (the true chain: output and end state); no transition is formed for
+            // it or for the last one, and the output pass skips it
+            idle = p.mode == 1 ? (transition && (cs0 == 0 || last)) : cs0 == 0;
+        }
+        if (idle) {
+            tc::fence_before();
+            __syncthreads();
+            if (warp == 2) tc::tmem_dealloc(tmem, 256);
+            return;
+        }
+    }
+    const bool first = cs0 == 0;
+    const bool outputs = p.mode != 1 || first;  // transitions are never first
     const int bos = p.cu[b] + cs0 * C, eos = p.cu[b + 1];
     const int kh = h / (p.Hv / p.Hk);
     // Accumulators (fp32 TMEM columns).  The hi and lo split terms of the state
@@ -974,17 +990,6 @@ __device__ __forceinline__ void chain_body(const TcParams& p, unsigned char* sm,
                 if (c >= 2 && !tc::mbar_wait(bar(kEmpty0 + s), ((c >> 1) - 1) & 1, abort_flag)) { fail(); break; }
                 GDR_TRACE_POINT(0, c);
                 const size_t gc = (size_t)c0 + c;
-                if (ready) {  // the chunk's operand images are released by the prep items that wrote them
-                    const int* f0 = ready + gc * p.Hv + h;
-                    const int* f1 = ready + gc * p.Hv + kh * (p.Hv / p.Hk);  // the K image's writer
-                    const uint64_t t0 = tc::globaltimer_ns();
-                    bool ok = true;
-                    while (!(tc::ld_acquire_gpu(f0) && tc::ld_acquire_gpu(f1))) {
-                        if (*abort_flag || tc::globaltimer_ns() - t0 > tc::kWaitLimitNs) { ok = false; break; }
-                    }
-                    if (!ok) { fail(); break; }
-                    tc::fence_proxy_async_global();
-                }
                 const uint32_t st = base + s * S::kStage;
                 const uint32_t fb = bar(kFull0 + s);
                 tc::mbar_arrive_tx(fb, S::kStageTx);
@@ -994,8 +999,7 @@ __device__ __forceinline__ void chain_body(const TcParams& p, unsigned char* sm,
                 if (kKDA) tc::bulk_g2s(st + S::kKt, p.Kb + (gc * p.Hv + h) * 2 * kTile64x128, 2 * kTile64x128, fb);
                 else tc::bulk_g2s(st + S::kKt, p.Kb + (gc * p.Hk + kh) * kTile64x128, kTile64x128, fb);
                 tc::bulk_g2s(st + S::kRec_, p.Rb + (gc * p.Hv + h) * kRec, kRec, fb);
-                if (c + 2 < nc && (!ready || tc::ld_acquire_gpu(ready + (gc + 2) * p.Hv + h))) {
-                    // warm L2 with the blobs of chunk c + 2
+                if (c + 2 < nc) {  // warm L2 with the blobs of chunk c + 2
                     const size_t g2 = gc + 2;
                     tc::prefetch_l2(p.Xw + (g2 * p.Hv + h) * kXwBytes, kXwBytes);
                     tc::prefetch_l2(p.Yw + (g2 * p.Hv + h) * kYwBytes, kYwBytes);
@@ -1241,72 +1245,6 @@ __device__ __forceinline__ void chain_body(const TcParams& p, unsigned char* sm,
             }
         }
     }
-}
-
-template <bool kKDA>
-__global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
-    using S = ChainSmem<kKDA>;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int tid = threadIdx.x, warp = tid >> 5;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::kBar);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::kBar + 8 * kNumBars);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::kBar + 8 * kNumBars + 8);
-    auto bar = [&](int i) { return tc::smem_u32(&bars[i]); };
-
-    // prologue (touches no memory the earlier kernels write), then wait for them
-    if (warp == 2) tc::tmem_alloc(tc::smem_u32(tmem_slot), 256);
-    if (tid == 0) {
-        for (int i = 0; i < kNumBars; ++i) tc::mbar_init(bar(i), chain_bar_count(i));
-        *abort_flag = 0;
-        tc::mbar_fence_init();
-    }
-    tc::fence_before();
-    __syncthreads();
-    tc::fence_after();
-    const uint32_t tmem = *tmem_slot;
-    tc::grid_dep_wait();
-    if (!p.meta[1]) {  // malformed cu_seqlens
-        tc::fence_before();
-        __syncthreads();
-        if (warp == 2) tc::tmem_dealloc(tmem, 256);
-        return;
-    }
-    // Work unit: a whole sequence (mode 0) or one segment of G chunks of it
-    // (modes 1 and 2; the summary pass runs two CTA sets, the transition from
-    // the identity with U = 0 and the offset from zero).
-    const int hx = blockIdx.x % (p.Hv * NVB);
-    const bool transition = p.mode == 1 && blockIdx.x >= p.Hv * NVB;
-    const int h = hx / NVB, vb = hx % NVB;
-    int b, nc, c0, cs0 = 0, sg = 0;
-    bool last = true;
-    if (p.mode == 0) {
-        b = p.order[blockIdx.y];
-        nc = (p.cu[b + 1] - p.cu[b] + C - 1) / C;
-        c0 = p.offsets[b];
-    } else {
-        sg = blockIdx.y;
-        bool idle = sg >= p.meta[2];  // beyond this call's segment count
-        if (!idle) {
-            const int4 e = p.segs[sg];
-            b = e.x; cs0 = e.y; nc = e.z; last = e.w != 0;
-            c0 = p.offsets[b] + cs0;
-            // the first segment of a sequence runs from h0 in the summary pass
-            // (the true chain: output and end state); no transition is formed for
-            // it or for the last one, and the output pass skips it
-            idle = p.mode == 1 ? (transition && (cs0 == 0 || last)) : cs0 == 0;
-        }
-        if (idle) {
-            tc::fence_before();
-            __syncthreads();
-            if (warp == 2) tc::tmem_dealloc(tmem, 256);
-            return;
-        }
-    }
-    const bool first = cs0 == 0;
-    const bool outputs = p.mode != 1 || first;  // transitions are never first
-    chain_body<kKDA>(p, sm, tmem, bars, abort_flag, tid, b, h, vb, nc, c0, cs0, sg, last, transition, first, outputs,
-                     nullptr);
     tc::fence_before();
     __syncthreads();
     if (warp == 2) tc::tmem_dealloc(tmem, 256);
