@@ -418,6 +418,7 @@ def cpu_baseline_prefill(case, budget_s=12.0):
         if time.perf_counter() - t0 > budget_s:
             break
     dt = (time.perf_counter() - t0) / reps
+    used = min(cores, oracle.num_threads())  # threads of the run above (the one-core run below changes it)
     # one core: 2 of the heads, scaled to all heads (the oracle's work is
     # independent per (sequence, head))
     Hv, Hk = case.v.shape[1], case.q.shape[1]
@@ -430,7 +431,7 @@ def cpu_baseline_prefill(case, budget_s=12.0):
     t1 = time.perf_counter()
     oracle.tokenwise(**one, nthreads=1)
     d1 = (time.perf_counter() - t1) * Hv / len(hs)
-    return {"value": round(ntok / dt, 2), "unit": "tokens/s", "cores": min(cores, oracle.num_threads()),
+    return {"value": round(ntok / dt, 2), "unit": "tokens/s", "cores": used,
             "kind": "oracle",
             "sample": f"1 sequence of {ntok} tokens x all {Hv} heads of the varlen workload, "
                       f"{reps} repetitions ({dt * reps:.1f} s)",
