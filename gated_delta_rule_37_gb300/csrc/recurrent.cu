@@ -93,7 +93,7 @@ recurrent_kernel(RecParams p) {
     const InT* __restrict__ gap = static_cast<const InT*>(p.ga);
     const InT* __restrict__ gbp = static_cast<const InT*>(p.gb);
     const float negA = raw ? -expf(p.A_log[h]) : 0.f, dtb = raw ? p.dt_bias[h] : 0.f;
-    float kn[KPT], qn[KPT], gcn[KPT], gn = 0.f, bn = 0.f, vn = 0.f, zn = 0.f;
+    float kn[KPT], qn[KPT], gcn[KPT], gn = 0.f, bn = 0.f, vn = 0.f, zn = 0.f, an = 0.f, bbn = 0.f;
     const InT* __restrict__ nzp = static_cast<const InT*>(p.nz);
     const float nwv = kNorm ? p.nw[v0 + (lane & 15)] : 0.f;
     int par = 0;
@@ -103,23 +103,24 @@ recurrent_kernel(RecParams p) {
         if (chan) Vec<float, KPT>::load(p.g + ((size_t)t * p.Hv + h) * K + lane * KPT, gcn);
         else if (!raw) gn = p.g[(size_t)t * p.Hv + h];
         if (!raw) bn = to_f(bp[(size_t)t * p.Hv + h]);
+        if (raw) {  // raw projections of the gates
+            an = to_f(gap[(size_t)t * p.Hv + h]);
+            bbn = to_f(gbp[(size_t)t * p.Hv + h]);
+        }
         vn = to_f(vp[((size_t)t * p.Hv + h) * V + v0 + (lane & 15)]);
         if (kNorm) zn = to_f(nzp[((size_t)t * p.Hv + h) * V + v0 + (lane & 15)]);
     };
-    // raw projections: lane j forms the decay and beta of token base + j for the
-    // next 32 tokens at once, off the per-token dependency chain; each token
-    // then takes its pair with one shuffle
+    // raw projections: the decay and beta of the next token are formed at the
+    // end of the current one, once its loads have landed, off the next token's
+    // dependency chain (every lane forms them; no exchange)
     float ra = 1.f, rb = 0.f;
-    auto form_gates = [&](int base) {
-        const int t = base + lane;
-        if (t < eos) {
-            const float x = to_f(gap[(size_t)t * p.Hv + h]) + dtb;  // softplus, threshold 20, as gdr_gating_fwd
-            ra = __expf(negA * (x > 20.f ? x : log1pf(expf(x))));
-            rb = p.beta_mul / (1.f + expf(-to_f(gbp[(size_t)t * p.Hv + h])));
-        }
+    auto form_gates = [&]() {
+        const float x = an + dtb;  // softplus, threshold 20, as gdr_gating_fwd
+        ra = __expf(negA * (x > 20.f ? x : log1pf(expf(x))));
+        rb = p.beta_mul / (1.f + expf(-bbn));
     };
-    if (bos < eos) load_token(bos);  // first, so its loads overlap those of the gates
-    if (raw && bos < eos) form_gates(bos);
+    if (bos < eos) load_token(bos);
+    if (raw && bos < eos) form_gates();
 #pragma unroll 1
     for (int t = bos; t < eos; ++t) {
         float kk[KPT], qq[KPT], ac[KPT];
@@ -127,9 +128,8 @@ recurrent_kernel(RecParams p) {
         for (int c = 0; c < KPT; ++c) { kk[c] = kn[c]; qq[c] = qn[c]; ac[c] = chan ? __expf(gcn[c]) : 1.f; }
         float a, bt;
         if (raw) {
-            if (t > bos && ((t - bos) & 31) == 0) form_gates(t);
-            a = __shfl_sync(0xffffffffu, ra, (t - bos) & 31);
-            bt = __shfl_sync(0xffffffffu, rb, (t - bos) & 31);
+            a = ra;
+            bt = rb;
         } else {
             a = chan ? 1.f : __expf(gn);
             bt = bn;
@@ -201,6 +201,7 @@ recurrent_kernel(RecParams p) {
 #pragma unroll
             for (int r = 0; r < kRowsPerWarp; ++r) Vec<PoolT, KPT>::store(irow + (size_t)r * K, s[r]);
         }
+        if (raw && t + 1 < eos) form_gates();  // token t + 1's raw values were loaded at the top
     }
     if (p.flags & 4) {  // GDR_COMMIT
 #pragma unroll
