@@ -21,6 +21,8 @@ namespace gdr {
 namespace {
 
 constexpr int kRowsPerWarp = 16;
+constexpr int kLptMax = 1024;  // sequences ranked in shared memory
+
 
 struct RecParams {
     const void* q;
@@ -34,6 +36,7 @@ struct RecParams {
     void* o;
     void* ibuf;
     int Hk, Hv, steps, flags, num_slots;
+    int lpt;  // multi-token batch of at most kLptMax sequences: longest first
     int64_t T;
     float scale;
     const void* ga;  // raw gate projections (kGate == 2)
@@ -45,6 +48,64 @@ struct RecParams {
     const void* nz;
     float neps;
 };
+
+// The sequence of rank r in longest-first order (ties by index; padding and
+// out-of-range slots last, as zero-length), for the CTA's NT threads.  Every
+// CTA of a multi-token call ranks the (at most kLptMax) sequences itself: the
+// lengths are bucketed (0..63, longer ones share bucket 63), the bucket of
+// rank r found from the bucket counts, then its sequence by a block-wide
+// count in index order.  Costs one coalesced pass over cu_seqlens and the
+// slot indices.
+template <int NT>
+__device__ int lpt_sequence(const RecParams& p, int N, int r) {
+    __shared__ int hist[64];
+    __shared__ unsigned char key[kLptMax];
+    __shared__ int wsum[NT / 32];
+    __shared__ int sel_bucket, sel_off, sel;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < 64; i += NT) hist[i] = 0;
+    if (tid == 0) sel = -1;
+    __syncthreads();
+    for (int j = tid; j < N; j += NT) {
+        const int slot = p.idx[j];
+        const int64_t lo = max(p.cu[j], 0), hi = min((int64_t)p.cu[j + 1], p.T);
+        const int len = (slot < 0 || slot >= p.num_slots || hi <= lo) ? 0 : (int)min(hi - lo, (int64_t)63);
+        key[j] = (unsigned char)len;
+        atomicAdd(&hist[len], 1);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int acc = 0, bk = 0, off = 0;
+        for (int k = 63; k >= 0; --k) {
+            if (r < acc + hist[k]) { bk = k; off = r - acc; break; }
+            acc += hist[k];
+        }
+        sel_bucket = bk;
+        sel_off = off;
+    }
+    __syncthreads();
+    const int bk = sel_bucket;
+    int off = sel_off;
+    for (int base = 0; base < N; base += NT) {
+        const int j = base + tid;
+        const bool f = j < N && key[j] == bk;
+        const unsigned m = __ballot_sync(0xffffffffu, f);
+        if (lane == 0) wsum[warp] = __popc(m);
+        __syncthreads();
+        int pre = 0, tot = 0;
+#pragma unroll
+        for (int w = 0; w < NT / 32; ++w) {
+            pre += w < warp ? wsum[w] : 0;
+            tot += wsum[w];
+        }
+        pre += __popc(m & ((1u << lane) - 1u));
+        if (f && pre == off) sel = j;
+        off -= tot;
+        __syncthreads();
+        if (sel >= 0) break;  // uniform: read after the barrier
+    }
+    return sel;
+}
 
 // kMode & 3: 0 scalar log-decay g [T, Hv]; 1 per-key-channel g [T, Hv, K];
 // 2 gates formed from raw projections (FlashQLA in-kernel gating commit).
@@ -62,8 +123,19 @@ recurrent_kernel(RecParams p) {
     constexpr int kWarps = BV / kRowsPerWarp;
     __shared__ float ssq[2][kWarps];  // per-warp sums of squares, by token parity
     constexpr int KPT = K / 32;  // key channels per lane
-    const int b = blockIdx.x;
-    const int h = blockIdx.y;
+    // Work unit (sequence b, head h, value block zb).  Multi-token calls take
+    // the sequences longest first, sequence-major, so that the long ones do not
+    // form the tail of the grid.
+    int b = blockIdx.x, h = blockIdx.y, zb = blockIdx.z;
+    if (p.lpt) {
+        const int units = gridDim.y * gridDim.z;
+        const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+        const int r = lin / units, u = lin - r * units;
+        h = u / gridDim.z;
+        zb = u - h * gridDim.z;
+        b = lpt_sequence<BV / kRowsPerWarp * 32>(p, gridDim.x, r);
+        if (b < 0) return;
+    }
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int slot = p.idx[b];
@@ -72,7 +144,7 @@ recurrent_kernel(RecParams p) {
     const int bos = max(p.cu[b], 0), eos = (int)min((int64_t)p.cu[b + 1], p.T);
     const int kh = h / (p.Hv / p.Hk);
     const int V = gridDim.z * BV;
-    const int v0 = blockIdx.z * BV + warp * kRowsPerWarp;
+    const int v0 = zb * BV + warp * kRowsPerWarp;
 
     const InT* __restrict__ qp = static_cast<const InT*>(p.q);
     const InT* __restrict__ kp = static_cast<const InT*>(p.k);
@@ -261,6 +333,7 @@ cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t stream) {
     p.o = a.o; p.ibuf = a.ibuf;
     p.Hk = a.Hk; p.Hv = a.Hv; p.steps = a.steps; p.flags = a.flags; p.scale = a.scale;
     p.num_slots = a.num_slots;
+    p.lpt = a.T > a.N && a.N <= kLptMax;
     p.T = a.T;
     p.ga = a.ga; p.gb = a.gb; p.A_log = a.A_log; p.dt_bias = a.dt_bias; p.beta_mul = a.beta_mul;
     p.nw = a.norm_weight; p.nz = a.norm_gate; p.neps = a.norm_eps;
