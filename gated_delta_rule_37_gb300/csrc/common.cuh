@@ -58,6 +58,18 @@ template <> struct Vec<__nv_bfloat16, 4> {
         *reinterpret_cast<uint2*>(p) = t;
     }
 };
+template <> struct Vec<__nv_bfloat16, 8> {
+    static __device__ __forceinline__ void load(const __nv_bfloat16* p, float* out) {
+        uint4 t = *reinterpret_cast<const uint4*>(p);
+        const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+            out[2 * i] = f.x;
+            out[2 * i + 1] = f.y;
+        }
+    }
+};
 template <> struct Vec<__nv_bfloat16, 2> {
     static __device__ __forceinline__ void load(const __nv_bfloat16* p, float* out) {
         float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
@@ -92,6 +104,17 @@ __device__ __forceinline__ void halve(float* x, int lane) {
 
 __device__ __forceinline__ float reduce32_to_lane(float (&x)[32], int lane) {
     halve<16, 16>(x, lane);
+    halve<8, 8>(x, lane);
+    halve<4, 4>(x, lane);
+    halve<2, 2>(x, lane);
+    halve<1, 1>(x, lane);
+    return x[0];
+}
+
+// The last four steps: 16 values per lane (value i on lane l stands for value
+// i of the lane's half-warp, i.e. index 16 * (l >> 4) + i) become one, lane l
+// holding the full sum of index l.
+__device__ __forceinline__ float reduce16_to_lane(float (&x)[32], int lane) {
     halve<8, 8>(x, lane);
     halve<4, 4>(x, lane);
     halve<2, 2>(x, lane);

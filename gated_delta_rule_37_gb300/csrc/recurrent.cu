@@ -6,8 +6,18 @@
 //   * the fp32 state rows live in registers for the whole sequence: a warp
 //     owns 16 consecutive rows, lane l holds K/32 consecutive key channels of
 //     each row, so a row is one coalesced 512-byte (fp32) read;
-//   * per token the two state-vector products S k and S q are reduced for all
-//     16 rows at once with a halving butterfly (31 shuffles instead of 160);
+//   * the lane's state channels are held as fp32x2 register pairs, so the two
+//     state-vector products S k and S q and the rank-1 update run as packed
+//     FMAs (Blackwell's f32x2 pipe: half the instructions of scalar FMAs);
+//   * per token the products are reduced for all 16 rows at once with a
+//     halving butterfly (31 shuffles instead of 160); the upper half-warp
+//     takes k and q in swapped roles, so the first halving step needs no
+//     select;
+//   * multi-token calls (verify) stage each window of up to 16 tokens' inputs
+//     in shared memory with one wave of loads per CTA, and do the per-token
+//     work that does not touch the state (l2 normalisation, k . q, decays,
+//     beta) once per CTA; single-token calls (decode) read their inputs
+//     straight from global memory;
 //   * o_t = scale * S_t q_t is formed as scale * (a S_{t-1} q + n_t (k . q)),
 //     which is S_t q_t with the rank-1 term expanded;
 //   * the state stays V-major end to end (pool, intermediate states), so every
@@ -22,6 +32,24 @@ namespace {
 
 constexpr int kRowsPerWarp = 16;
 constexpr int kLptMax = 1024;  // sequences ranked in shared memory
+constexpr int kWin = 16;       // tokens whose inputs are staged in shared memory at once
+
+// Dynamic shared memory of the staged (multi-token) input path, in bytes.
+template <int K, int BV, int kMode>
+constexpr unsigned stage_bytes() {
+    return sizeof(float) * kWin * (2 * K + BV + ((kMode & 4) ? BV : 0) + ((kMode & 3) == 1 ? K : 0) + 4);
+}
+
+// N consecutive floats of shared memory (N = 2 or 4, 8- or 16-byte aligned)
+template <int N> __device__ __forceinline__ void lds(const float* p, float* out) {
+    if constexpr (N == 4) {
+        const float4 t = *reinterpret_cast<const float4*>(p);
+        out[0] = t.x; out[1] = t.y; out[2] = t.z; out[3] = t.w;
+    } else {
+        const float2 t = *reinterpret_cast<const float2*>(p);
+        out[0] = t.x; out[1] = t.y;
+    }
+}
 
 
 struct RecParams {
@@ -36,7 +64,8 @@ struct RecParams {
     void* o;
     void* ibuf;
     int Hk, Hv, steps, flags, num_slots;
-    int lpt;  // multi-token batch of at most kLptMax sequences: longest first
+    int lpt;     // multi-token batch of at most kLptMax sequences: longest first
+    int staged;  // multi-token batch: inputs staged in shared memory by window
     int64_t T;
     float scale;
     const void* ga;  // raw gate projections (kGate == 2)
@@ -154,94 +183,102 @@ recurrent_kernel(RecParams p) {
     PoolT* pool = static_cast<PoolT*>(p.pool);
 
     PoolT* srow = pool + (((size_t)slot * p.Hv + h) * V + v0) * K + lane * KPT;
-    float s[kRowsPerWarp][KPT];
+    // s2[r][i] = (S[r][2i], S[r][2i + 1]): two neighbouring channels per
+    // register pair, so the products and the update run as packed fp32x2 FMAs
+    constexpr int KP = KPT / 2;
+    float2 s2[kRowsPerWarp][KP];
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) Vec<PoolT, KPT>::load(srow + (size_t)r * K, s[r]);
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+        float t[KPT];
+        Vec<PoolT, KPT>::load(srow + (size_t)r * K, t);
+#pragma unroll
+        for (int i = 0; i < KP; ++i) s2[r][i] = make_float2(t[2 * i], t[2 * i + 1]);
+    }
+    auto row = [&](int r, float* t) {
+#pragma unroll
+        for (int i = 0; i < KP; ++i) { t[2 * i] = s2[r][i].x; t[2 * i + 1] = s2[r][i].y; }
+    };
 
-    // Per-token inputs of token t + 1 are loaded while token t is processed, so
-    // their global-load latency is hidden behind the reductions of the current token.
     constexpr bool chan = kGate == 1;  // GDR_CHANNEL_GATE: g is [T, Hv, K]
     constexpr bool raw = kGate == 2;   // g and beta from raw projections
+    constexpr int NT = kWarps * 32;
     const InT* __restrict__ gap = static_cast<const InT*>(p.ga);
     const InT* __restrict__ gbp = static_cast<const InT*>(p.gb);
-    const float negA = raw ? -expf(p.A_log[h]) : 0.f, dtb = raw ? p.dt_bias[h] : 0.f;
-    float kn[KPT], qn[KPT], gcn[KPT], gn = 0.f, bn = 0.f, vn = 0.f, zn = 0.f, an = 0.f, bbn = 0.f;
     const InT* __restrict__ nzp = static_cast<const InT*>(p.nz);
     const float nwv = kNorm ? p.nw[v0 + (lane & 15)] : 0.f;
-    int par = 0;
-    auto load_token = [&](int t) {
-        Vec<InT, KPT>::load(kp + ((size_t)t * p.Hk + kh) * K + lane * KPT, kn);
-        Vec<InT, KPT>::load(qp + ((size_t)t * p.Hk + kh) * K + lane * KPT, qn);
-        if (chan) Vec<float, KPT>::load(p.g + ((size_t)t * p.Hv + h) * K + lane * KPT, gcn);
-        else if (!raw) gn = p.g[(size_t)t * p.Hv + h];
-        if (!raw) bn = to_f(bp[(size_t)t * p.Hv + h]);
-        if (raw) {  // raw projections of the gates
-            an = to_f(gap[(size_t)t * p.Hv + h]);
-            bbn = to_f(gbp[(size_t)t * p.Hv + h]);
-        }
-        vn = to_f(vp[((size_t)t * p.Hv + h) * V + v0 + (lane & 15)]);
-        if (kNorm) zn = to_f(nzp[((size_t)t * p.Hv + h) * V + v0 + (lane & 15)]);
-    };
-    // raw projections: the decay and beta of the next token are formed at the
-    // end of the current one, once its loads have landed, off the next token's
-    // dependency chain (every lane forms them; no exchange)
-    float ra = 1.f, rb = 0.f;
-    auto form_gates = [&]() {
-        const float x = an + dtb;  // softplus, threshold 20, as gdr_gating_fwd
-        ra = __expf(negA * (x > 20.f ? x : log1pf(expf(x))));
-        rb = p.beta_mul / (1.f + expf(-bbn));
-    };
-    if (bos < eos) load_token(bos);
-    if (raw && bos < eos) form_gates();
-#pragma unroll 1
-    for (int t = bos; t < eos; ++t) {
-        float kk[KPT], qq[KPT], ac[KPT];
-#pragma unroll
-        for (int c = 0; c < KPT; ++c) { kk[c] = kn[c]; qq[c] = qn[c]; ac[c] = chan ? __expf(gcn[c]) : 1.f; }
-        float a, bt;
-        if (raw) {
-            a = ra;
-            bt = rb;
+    const int tid = threadIdx.x;
+    const bool up = lane >= 16;
+
+    // decay a (scalar gates; 1 for channel gates) and beta of token t
+    auto gates = [&](int t, float& a, float& bt) {
+        const size_t th = (size_t)t * p.Hv + h;
+        a = 1.f;
+        if (raw) {  // softplus (threshold 20) and sigmoid, as gdr_gating_fwd
+            const float x = to_f(gap[th]) + p.dt_bias[h];
+            a = __expf(-expf(p.A_log[h]) * (x > 20.f ? x : log1pf(expf(x))));
+            bt = p.beta_mul / (1.f + expf(-to_f(gbp[th])));
         } else {
-            a = chan ? 1.f : __expf(gn);
-            bt = bn;
+            if (!chan) a = __expf(p.g[th]);
+            bt = to_f(bp[th]);
         }
-        const float vv = vn, zz = zn;
-        if (t + 1 < eos) load_token(t + 1);
-        if (p.flags & 1) {  // GDR_QK_L2NORM
-            float sk = 0.f, sq = 0.f;
+    };
+    // warp-collective: l2-normalise q and k in place (GDR_QK_L2NORM), return k.q
+    auto norm_kq = [&](float* kk, float* qq) {
+        if (p.flags & 1) {
+            float s1 = 0.f, s2q = 0.f;
 #pragma unroll
-            for (int c = 0; c < KPT; ++c) { sk += kk[c] * kk[c]; sq += qq[c] * qq[c]; }
-            const float ik = rsqrtf(warp_sum(sk) + 1e-6f), iq = rsqrtf(warp_sum(sq) + 1e-6f);
+            for (int c = 0; c < KPT; ++c) { s1 += kk[c] * kk[c]; s2q += qq[c] * qq[c]; }
+            const float ik = rsqrtf(warp_sum(s1) + 1e-6f), iq = rsqrtf(warp_sum(s2q) + 1e-6f);
 #pragma unroll
             for (int c = 0; c < KPT; ++c) { kk[c] *= ik; qq[c] *= iq; }
-        }
-
-        // decayed products: scalar gate S~ = a S (a applied after the reduction);
-        // channel gate S~ = S diag(ac), i.e. S~ k = S (ac o k), S~ q = S (ac o q)
-        float ka[KPT], qa[KPT], da[KPT];
-#pragma unroll
-        for (int c = 0; c < KPT; ++c) {
-            ka[c] = chan ? kk[c] * ac[c] : kk[c];
-            qa[c] = chan ? qq[c] * ac[c] : qq[c];
-            da[c] = chan ? ac[c] : a;
-        }
-        float x[32];
-#pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r) {
-            float dk = 0.f, dq = 0.f;
-#pragma unroll
-            for (int c = 0; c < KPT; ++c) { dk += s[r][c] * ka[c]; dq += s[r][c] * qa[c]; }
-            x[r] = dk;
-            x[r + kRowsPerWarp] = dq;
         }
         float kq = 0.f;
 #pragma unroll
         for (int c = 0; c < KPT; ++c) kq += kk[c] * qq[c];
-        kq = warp_sum(kq);
+        return warp_sum(kq);
+    };
+
+    // One token on the register-resident state.  kk: the lane's k channels;
+    // uu / ww: k / q for lanes < 16 and q / k for lanes >= 16 (the upper
+    // half-warp takes them in swapped roles, so that the first halving step of
+    // the reduction pairs x[r] with the partner's x[16 + r] and needs no
+    // select); ac: exp of the channel log-decays.
+    int par = 0;
+    auto step = [&](int t, const float* kk, const float* uu, const float* ww, const float* ac, float a, float bt,
+                    float kq, float vv, float zz) {
+        // decayed products: scalar gate S~ = a S (a applied after the reduction);
+        // channel gate S~ = S diag(ac), i.e. S~ k = S (ac o k), S~ q = S (ac o q)
+        float2 u2[KP], w2[KP], da2[KP], kk2[KP];
+#pragma unroll
+        for (int i = 0; i < KP; ++i) {
+            u2[i] = make_float2(uu[2 * i], uu[2 * i + 1]);
+            w2[i] = make_float2(ww[2 * i], ww[2 * i + 1]);
+            kk2[i] = make_float2(kk[2 * i], kk[2 * i + 1]);
+            if (chan) {
+                da2[i] = make_float2(ac[2 * i], ac[2 * i + 1]);
+                u2[i] = __fmul2_rn(u2[i], da2[i]);
+                w2[i] = __fmul2_rn(w2[i], da2[i]);
+            } else {
+                da2[i] = make_float2(a, a);
+            }
+        }
+        float x[32];
+#pragma unroll
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+            float2 du = __fmul2_rn(s2[r][0], u2[0]), dw = __fmul2_rn(s2[r][0], w2[0]);
+#pragma unroll
+            for (int i = 1; i < KP; ++i) {
+                du = __ffma2_rn(s2[r][i], u2[i], du);
+                dw = __ffma2_rn(s2[r][i], w2[i], dw);
+            }
+            x[r] = du.x + du.y;
+            x[16 + r] = dw.x + dw.y;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] += __shfl_xor_sync(0xffffffffu, x[i + 16], 16);
         // lane r < 16 now holds (S k)_r, lane 16 + r holds (S q)_r (before the
         // scalar decay a; channel decays are already inside)
-        const float red = reduce32_to_lane(x, lane);
+        const float red = reduce16_to_lane(x, lane);
         const float n_mine = bt * (vv - a * red);  // valid on lanes < 16
         const float n_row = __shfl_sync(0xffffffffu, n_mine, lane & 15);
         if (kNorm) {
@@ -264,20 +301,157 @@ recurrent_kernel(RecParams p) {
 #pragma unroll
         for (int r = 0; r < kRowsPerWarp; ++r) {
             const float nr = __shfl_sync(0xffffffffu, n_mine, r);
+            const float2 n2 = make_float2(nr, nr);
 #pragma unroll
-            for (int c = 0; c < KPT; ++c) s[r][c] = fmaf(da[c], s[r][c], nr * kk[c]);
+            for (int i = 0; i < KP; ++i) s2[r][i] = __ffma2_rn(da2[i], s2[r][i], __fmul2_rn(n2, kk2[i]));
         }
         if (p.ibuf && t - bos < p.steps) {
             PoolT* irow = static_cast<PoolT*>(p.ibuf) +
                           ((((size_t)b * p.steps + (t - bos)) * p.Hv + h) * V + v0) * K + lane * KPT;
 #pragma unroll
-            for (int r = 0; r < kRowsPerWarp; ++r) Vec<PoolT, KPT>::store(irow + (size_t)r * K, s[r]);
+            for (int r = 0; r < kRowsPerWarp; ++r) {
+                float t2[KPT];
+                row(r, t2);
+                Vec<PoolT, KPT>::store(irow + (size_t)r * K, t2);
+            }
         }
-        if (raw && t + 1 < eos) form_gates();  // token t + 1's raw values were loaded at the top
+    };
+
+    if (p.staged) {
+        // Multi-token calls: the inputs of up to kWin tokens are staged in
+        // shared memory, in fp32, by the whole CTA at once, so every load of a
+        // window is in flight together (with the state loads, for the first
+        // window), and the per-token work that does not depend on the state
+        // (l2 normalisation, k.q, the decays and beta) is done once per CTA
+        // rather than once per warp.  Layout (dynamic shared memory, floats):
+        // q rows [kWin][K], k rows [kWin][K], v slice [kWin][BV], norm-gate
+        // slice [kWin][BV] (kNorm), exp'd channel decays [kWin][K] (chan),
+        // per token {decay, beta, k.q, -} [kWin][4].
+        extern __shared__ __align__(16) float dsm[];
+        float* sq = dsm;
+        float* sk = sq + kWin * K;
+        float* sv = sk + kWin * K;
+        float* sz = sv + kWin * BV;
+        float* sg = sz + (kNorm ? kWin * BV : 0);
+        float* stok = sg + (chan ? kWin * K : 0);
+        const float* ub = up ? sq : sk;
+        const float* wb = up ? sk : sq;
+#pragma unroll 1
+        for (int t0 = bos; t0 < eos; t0 += kWin) {
+            const int n = min(kWin, eos - t0);
+            if (t0 > bos) __syncthreads();  // the previous window has been read
+            constexpr int E = 16 / sizeof(InT);  // elements per 16-byte piece
+            constexpr int PR = K / E, PV = BV / E;
+#pragma unroll
+            for (int it = 0; it < (kWin * PR + NT - 1) / NT; ++it) {
+                const int i = it * NT + tid, j = i / PR, c = (i - j * PR) * E;
+                if (j < n) {
+                    const size_t off = ((size_t)(t0 + j) * p.Hk + kh) * K + c;
+                    float a[E], bq[E];
+                    Vec<InT, E>::load(kp + off, a);
+                    Vec<InT, E>::load(qp + off, bq);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        sk[j * K + c + e] = a[e];
+                        sq[j * K + c + e] = bq[e];
+                    }
+                }
+            }
+#pragma unroll
+            for (int it = 0; it < (kWin * PV + NT - 1) / NT; ++it) {
+                const int i = it * NT + tid, j = i / PV, c = (i - j * PV) * E;
+                if (j < n) {
+                    const size_t off = ((size_t)(t0 + j) * p.Hv + h) * V + zb * BV + c;
+                    float a[E], z[E];
+                    Vec<InT, E>::load(vp + off, a);
+                    if (kNorm) Vec<InT, E>::load(nzp + off, z);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) {
+                        sv[j * BV + c + e] = a[e];
+                        if (kNorm) sz[j * BV + c + e] = z[e];
+                    }
+                }
+            }
+            if (chan) {
+#pragma unroll
+                for (int it = 0; it < (kWin * K / 4 + NT - 1) / NT; ++it) {
+                    const int i = it * NT + tid, j = i / (K / 4), c = (i - j * (K / 4)) * 4;
+                    if (j < n) {
+                        float gc[4];
+                        Vec<float, 4>::load(p.g + ((size_t)(t0 + j) * p.Hv + h) * K + c, gc);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) sg[j * K + c + e] = __expf(gc[e]);
+                    }
+                }
+            }
+            if (tid < n) {
+                float a, bt;
+                gates(t0 + tid, a, bt);
+                stok[4 * tid] = a;
+                stok[4 * tid + 1] = bt;
+            }
+            __syncthreads();
+            for (int j = warp; j < n; j += kWarps) {  // one warp per token
+                float kk[KPT], qq[KPT];
+                lds<KPT>(sk + j * K + lane * KPT, kk);
+                lds<KPT>(sq + j * K + lane * KPT, qq);
+                const float kq = norm_kq(kk, qq);
+                if (p.flags & 1) {
+#pragma unroll
+                    for (int c = 0; c < KPT; ++c) {
+                        sk[j * K + lane * KPT + c] = kk[c];
+                        sq[j * K + lane * KPT + c] = qq[c];
+                    }
+                }
+                if (lane == 0) stok[4 * j + 2] = kq;
+            }
+            __syncthreads();
+#pragma unroll 1
+            for (int j = 0; j < n; ++j) {
+                float kk[KPT], uu[KPT], ww[KPT], ac[KPT];
+                lds<KPT>(sk + j * K + lane * KPT, kk);
+                lds<KPT>(ub + j * K + lane * KPT, uu);
+                lds<KPT>(wb + j * K + lane * KPT, ww);
+                if (chan) lds<KPT>(sg + j * K + lane * KPT, ac);
+                const float4 tk = *reinterpret_cast<const float4*>(stok + 4 * j);
+                const int vr = warp * kRowsPerWarp + (lane & 15);
+                step(t0 + j, kk, uu, ww, ac, tk.x, tk.y, tk.z, sv[j * BV + vr], kNorm ? sz[j * BV + vr] : 0.f);
+            }
+        }
+    } else {
+        // Single-token calls (decode): every warp reads its token's inputs
+        // straight from global memory, with no shared-memory round trip.
+#pragma unroll 1
+        for (int t = bos; t < eos; ++t) {
+            float kk[KPT], qq[KPT], uu[KPT], ww[KPT], ac[KPT];
+            Vec<InT, KPT>::load(kp + ((size_t)t * p.Hk + kh) * K + lane * KPT, kk);
+            Vec<InT, KPT>::load(qp + ((size_t)t * p.Hk + kh) * K + lane * KPT, qq);
+            if (chan) {
+                Vec<float, KPT>::load(p.g + ((size_t)t * p.Hv + h) * K + lane * KPT, ac);
+#pragma unroll
+                for (int c = 0; c < KPT; ++c) ac[c] = __expf(ac[c]);
+            }
+            const size_t vo = ((size_t)t * p.Hv + h) * V + v0 + (lane & 15);
+            const float vv = to_f(vp[vo]);
+            const float zz = kNorm ? to_f(nzp[vo]) : 0.f;
+            float a, bt;
+            gates(t, a, bt);
+            const float kq = norm_kq(kk, qq);
+#pragma unroll
+            for (int c = 0; c < KPT; ++c) {
+                uu[c] = up ? qq[c] : kk[c];
+                ww[c] = up ? kk[c] : qq[c];
+            }
+            step(t, kk, uu, ww, ac, a, bt, kq, vv, zz);
+        }
     }
     if (p.flags & 4) {  // GDR_COMMIT
 #pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r) Vec<PoolT, KPT>::store(srow + (size_t)r * K, s[r]);
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+            float t2[KPT];
+            row(r, t2);
+            Vec<PoolT, KPT>::store(srow + (size_t)r * K, t2);
+        }
     }
 }
 
@@ -285,7 +459,8 @@ template <typename InT, typename PoolT, int K, int kGate>
 cudaError_t launch_k(const RecParams& p, int N, int V, cudaStream_t stream) {
     if (kGate != 2 && p.nw) {  // gated-norm epilogue: one CTA per (sequence, head), BV = V = K
         KernelTimer kt("recurrent", stream);
-        recurrent_kernel<InT, PoolT, K, K, kGate | 4><<<dim3(N, p.Hv, 1), K / kRowsPerWarp * 32, 0, stream>>>(p);
+        const unsigned smem = p.staged ? stage_bytes<K, K, kGate | 4>() : 0;
+        recurrent_kernel<InT, PoolT, K, K, kGate | 4><<<dim3(N, p.Hv, 1), K / kRowsPerWarp * 32, smem, stream>>>(p);
         return cudaGetLastError();
     }
     // V-column split: 64-row blocks (128 threads) measured best on GB300 for
@@ -301,13 +476,15 @@ cudaError_t launch_k(const RecParams& p, int N, int V, cudaStream_t stream) {
     KernelTimer kt("recurrent", stream);
     switch (bv) {
         case 128:
-            recurrent_kernel<InT, PoolT, K, 128, kGate><<<grid, 256, 0, stream>>>(p);
+            recurrent_kernel<InT, PoolT, K, 128, kGate>
+                <<<grid, 256, p.staged ? stage_bytes<K, 128, kGate>() : 0, stream>>>(p);
             break;
         case 64:
-            recurrent_kernel<InT, PoolT, K, 64, kGate><<<grid, 128, 0, stream>>>(p);
+            recurrent_kernel<InT, PoolT, K, 64, kGate>
+                <<<grid, 128, p.staged ? stage_bytes<K, 64, kGate>() : 0, stream>>>(p);
             break;
         default:
-            recurrent_kernel<InT, PoolT, K, 32, kGate><<<grid, 64, 0, stream>>>(p);
+            recurrent_kernel<InT, PoolT, K, 32, kGate><<<grid, 64, p.staged ? stage_bytes<K, 32, kGate>() : 0, stream>>>(p);
             break;
     }
     return cudaGetLastError();
@@ -334,6 +511,7 @@ cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t stream) {
     p.Hk = a.Hk; p.Hv = a.Hv; p.steps = a.steps; p.flags = a.flags; p.scale = a.scale;
     p.num_slots = a.num_slots;
     p.lpt = a.T > a.N && a.N <= kLptMax;
+    p.staged = a.T > a.N;
     p.T = a.T;
     p.ga = a.ga; p.gb = a.gb; p.A_log = a.A_log; p.dt_bias = a.dt_bias; p.beta_mul = a.beta_mul;
     p.nw = a.norm_weight; p.nz = a.norm_gate; p.neps = a.norm_eps;

@@ -306,3 +306,54 @@ def test_cuda_graph_replay_equals_eager():
     graph.replay()
     torch.cuda.synchronize()
     assert bits_equal(o, o_e) and bits_equal(ib, ib_e)
+
+
+# Multi-token calls stage each window of up to 16 tokens' inputs in shared
+# memory; sequences of 17, 33 and 40 tokens cross one to two window edges.
+LONG_LENS = [1, 17, 40, 0, 33, 16]
+
+
+@pytest.mark.parametrize("mode", ["scalar", "channel", "gated", "norm", "norm_channel"])
+@pytest.mark.parametrize("K", [64, 128])
+def test_multi_window_sequences(mode, K):
+    dtype = torch.float32 if K == 64 else torch.bfloat16
+    pool_dtype = torch.bfloat16 if mode.startswith("norm") else torch.float32
+    case = workloads.pool_case(71 + K, LONG_LENS, 2, 4, K, K, 8, dtype=dtype, pool_dtype=pool_dtype, pad_count=1,
+                               commit=True, steps=40, ibuf_rows=6, g_range=(-0.5, 0.0),
+                               channel_gate=mode in ("channel", "norm_channel"))
+    if mode.startswith("norm"):
+        case.norm = workloads.output_norm(72, case.T, 4, K, dtype=dtype, eps=1e-4)
+    if mode == "gated":
+        case.raw = workloads.raw_gates(73, case.T, 4, dtype=dtype)
+    pool, o, ib, o_init = run_case(case, flags=gdr.GDR_COMMIT, with_ibuf=True, gated=mode == "gated")
+    check_case(_with_oracle_gates(case) if mode == "gated" else case, pool, o, ib, o_init, commit=True)
+
+
+def test_multi_window_qk_l2norm():
+    """GDR_QK_L2NORM on the staged path: q and k normalised once per window."""
+    case = workloads.pool_case(74, LONG_LENS, 2, 4, 128, 128, 8, dtype=torch.float32, pool_dtype=torch.float32,
+                               commit=True)
+    gen = torch.Generator().manual_seed(6)
+    case.q = torch.randn(case.q.shape, generator=gen) * 3.0
+    case.k = torch.randn(case.k.shape, generator=gen) * 0.5
+    pool, o, _, _ = run_case(case, flags=gdr.GDR_COMMIT | gdr.GDR_QK_L2NORM, with_ibuf=False)
+    qn = torch.from_numpy(oracle.l2norm(case.q, 1e-6))
+    kn = torch.from_numpy(oracle.l2norm(case.k, 1e-6))
+    ro, rpool, _ = oracle.pool(qn, kn, case.v, case.g, case.beta, case.pool, case.state_indices,
+                               case.cu_seqlens, scale=case.scale, commit=True)
+    check_out(o.view.cpu(), ro, "o")
+    used = sorted(int(s) for s in case.state_indices if s >= 0)
+    check_state(pool.view.cpu()[used], rpool[used], "pool")
+
+
+@pytest.mark.parametrize("mode", ["scalar", "channel", "norm"])
+def test_direct_path_multi_token_sequence(mode):
+    """A call with as many tokens as sequences reads its inputs straight from
+    global memory; a 3-token sequence beside two empty ones still runs every
+    token in order."""
+    case = workloads.pool_case(75, [3, 0, 0, 1], 2, 4, 128, 128, 5, pool_dtype=torch.float32, commit=True,
+                               steps=3, ibuf_rows=4, channel_gate=mode == "channel")
+    if mode == "norm":
+        case.norm = workloads.output_norm(76, case.T, 4, 128, eps=1e-4)
+    pool, o, ib, o_init = run_case(case, flags=gdr.GDR_COMMIT, with_ibuf=True)
+    check_case(case, pool, o, ib, o_init, commit=True)
