@@ -103,14 +103,28 @@ __device__ int lpt_sequence(const RecParams& p, int N, int r) {
         atomicAdd(&hist[len], 1);
     }
     __syncthreads();
-    if (tid == 0) {
-        int acc = 0, bk = 0, off = 0;
-        for (int k = 63; k >= 0; --k) {
-            if (r < acc + hist[k]) { bk = k; off = r - acc; break; }
-            acc += hist[k];
+    if (warp == 0) {
+        // lane l covers buckets 63 - 2l and 62 - 2l: a prefix sum over the lanes
+        // counts the sequences in longer buckets, and the one lane whose span
+        // holds rank r names the bucket and the offset in it
+        const int h0 = hist[63 - 2 * lane], h1 = hist[62 - 2 * lane];
+        int incl = h0 + h1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
         }
-        sel_bucket = bk;
-        sel_off = off;
+        const int before = incl - h0 - h1;
+        const bool hit = r >= before && r < incl;
+        if (hit) {
+            const bool first = r < before + h0;
+            sel_bucket = first ? 63 - 2 * lane : 62 - 2 * lane;
+            sel_off = first ? r - before : r - before - h0;
+        }
+        if (__ballot_sync(0xffffffffu, hit) == 0u && lane == 0) {  // r beyond the count: none
+            sel_bucket = 0;
+            sel_off = 0;
+        }
     }
     __syncthreads();
     const int bk = sel_bucket;
