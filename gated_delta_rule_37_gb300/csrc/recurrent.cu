@@ -477,12 +477,19 @@ cudaError_t launch_k(const RecParams& p, int N, int V, cudaStream_t stream) {
         recurrent_kernel<InT, PoolT, K, K, kGate | 4><<<dim3(N, p.Hv, 1), K / kRowsPerWarp * 32, smem, stream>>>(p);
         return cudaGetLastError();
     }
-    // V-column split: 64-row blocks (128 threads) measured best on GB300 for
-    // both single-token decode (6.50 vs 6.42 TB/s at 128 rows) and 12-token
-    // verify (4.42 vs 4.10 TB/s); 32-row blocks when there are few sequences.
+    // V-column split.  Single-token decode: 64-row blocks (128 threads)
+    // measured best on GB300 (6.50 vs 6.42 TB/s at 128 rows).  Multi-token
+    // calls: 128-row blocks (256 threads), since one CTA then stages a window's
+    // q, k rows and per-token scalars for twice the rows (verify 0.098 vs
+    // 0.103 ms), as long as the units fill every SM with two such CTAs.
+    // 32-row blocks when there are few sequences.
     const long units = (long)N * p.Hv;
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 0;
     int bv = 64;
     if (V < 64 || units < 256) bv = 32;
+    else if (p.staged && V % 128 == 0 && sms > 0 && units >= 2L * sms) bv = 128;
 #ifdef GDR_REC_BV
     if (GDR_REC_BV <= V) bv = GDR_REC_BV;  // fixed split for tuning builds
 #endif

@@ -357,3 +357,18 @@ def test_direct_path_multi_token_sequence(mode):
         case.norm = workloads.output_norm(76, case.T, 4, 128, eps=1e-4)
     pool, o, ib, o_init = run_case(case, flags=gdr.GDR_COMMIT, with_ibuf=True)
     check_case(case, pool, o, ib, o_init, commit=True)
+
+
+@pytest.mark.parametrize("mode", ["scalar", "channel", "gated"])
+def test_multi_token_wide_blocks(mode):
+    """Enough (sequence, head) units for the 128-row blocks of multi-token
+    calls (80 x 4 = 320, two per SM): ragged 1..40-token sequences, so windows
+    of every fill, and padding rows; the pool is committed (the per-token
+    states of these block sizes are covered by the full-size verify tests)."""
+    lens = torch.randint(1, 41, (80,), generator=torch.Generator().manual_seed(77)).tolist()
+    case = workloads.pool_case(78, lens, 2, 4, 128, 128, 90, pool_dtype=torch.bfloat16, pad_count=3, commit=True,
+                               g_range=(-0.5, 0.0), channel_gate=mode == "channel")
+    if mode == "gated":
+        case.raw = workloads.raw_gates(79, case.T, 4)
+    pool, o, ib, o_init = run_case(case, flags=gdr.GDR_COMMIT, with_ibuf=False, gated=mode == "gated")
+    check_case(_with_oracle_gates(case) if mode == "gated" else case, pool, o, ib, o_init, commit=True)
