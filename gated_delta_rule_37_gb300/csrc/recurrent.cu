@@ -26,6 +26,7 @@
 // No tensor cores: every step is a matrix-vector product (M = 1).
 #include "common.cuh"
 #include "launch.h"
+#include "tc.cuh"
 
 namespace gdr {
 namespace {
@@ -65,6 +66,7 @@ struct RecParams {
     void* ibuf;
     int Hk, Hv, steps, flags, num_slots;
     int lpt;     // multi-token batch of at most kLptMax sequences: longest first
+    int pf_stride;  // with lpt: CTAs resident at once (L2 warming of the next unit), 0 = off
     int staged;  // multi-token batch: inputs staged in shared memory by window
     int64_t T;
     float scale;
@@ -78,22 +80,24 @@ struct RecParams {
     float neps;
 };
 
-// The sequence of rank r in longest-first order (ties by index; padding and
-// out-of-range slots last, as zero-length), for the CTA's NT threads.  Every
-// CTA of a multi-token call ranks the (at most kLptMax) sequences itself: the
-// lengths are bucketed (0..63, longer ones share bucket 63), the bucket of
-// rank r found from the bucket counts, then its sequence by a block-wide
-// count in index order.  Costs one coalesced pass over cu_seqlens and the
-// slot indices.
+// The sequences of ranks r and r2 in longest-first order (ties by index;
+// padding and out-of-range slots last, as zero-length), for the CTA's NT
+// threads; r2 < 0 asks for none (-1 returned).  Every CTA of a multi-token
+// call ranks the (at most kLptMax) sequences itself: the lengths are bucketed
+// (0..63, longer ones share bucket 63), the bucket of each rank is found from
+// the bucket counts (one warp per rank, two buckets per lane, a prefix sum
+// over the lanes), then its sequence by a block-wide count in index order.
+// Costs one coalesced pass over cu_seqlens and the slot indices.
 template <int NT>
-__device__ int lpt_sequence(const RecParams& p, int N, int r) {
+__device__ int2 lpt_sequences(const RecParams& p, int N, int r, int r2) {
+    static_assert(NT >= 64, "two warps search the two ranks");
     __shared__ int hist[64];
     __shared__ unsigned char key[kLptMax];
-    __shared__ int wsum[NT / 32];
-    __shared__ int sel_bucket, sel_off, sel;
+    __shared__ int wsum[2][NT / 32];
+    __shared__ int sel_bucket[2], sel_off[2], sel[2];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int i = tid; i < 64; i += NT) hist[i] = 0;
-    if (tid == 0) sel = -1;
+    if (tid < 2) sel[tid] = -1;
     __syncthreads();
     for (int j = tid; j < N; j += NT) {
         const int slot = p.idx[j];
@@ -103,10 +107,11 @@ __device__ int lpt_sequence(const RecParams& p, int N, int r) {
         atomicAdd(&hist[len], 1);
     }
     __syncthreads();
-    if (warp == 0) {
+    if (warp < 2) {
         // lane l covers buckets 63 - 2l and 62 - 2l: a prefix sum over the lanes
         // counts the sequences in longer buckets, and the one lane whose span
-        // holds rank r names the bucket and the offset in it
+        // holds the rank names the bucket and the offset in it
+        const int rr = warp ? r2 : r;
         const int h0 = hist[63 - 2 * lane], h1 = hist[62 - 2 * lane];
         int incl = h0 + h1;
 #pragma unroll
@@ -115,39 +120,46 @@ __device__ int lpt_sequence(const RecParams& p, int N, int r) {
             if (lane >= o) incl += y;
         }
         const int before = incl - h0 - h1;
-        const bool hit = r >= before && r < incl;
+        const bool hit = rr >= before && rr < incl;
         if (hit) {
-            const bool first = r < before + h0;
-            sel_bucket = first ? 63 - 2 * lane : 62 - 2 * lane;
-            sel_off = first ? r - before : r - before - h0;
+            const bool first = rr < before + h0;
+            sel_bucket[warp] = first ? 63 - 2 * lane : 62 - 2 * lane;
+            sel_off[warp] = first ? rr - before : rr - before - h0;
         }
-        if (__ballot_sync(0xffffffffu, hit) == 0u && lane == 0) {  // r beyond the count: none
-            sel_bucket = 0;
-            sel_off = 0;
+        if (__ballot_sync(0xffffffffu, hit) == 0u && lane == 0) {  // no such rank (r2 < 0)
+            sel_bucket[warp] = -1;
+            sel_off[warp] = 0;
         }
     }
     __syncthreads();
-    const int bk = sel_bucket;
-    int off = sel_off;
+    const int bk0 = sel_bucket[0], bk1 = sel_bucket[1];
+    int off0 = sel_off[0], off1 = sel_off[1];
     for (int base = 0; base < N; base += NT) {
         const int j = base + tid;
-        const bool f = j < N && key[j] == bk;
-        const unsigned m = __ballot_sync(0xffffffffu, f);
-        if (lane == 0) wsum[warp] = __popc(m);
+        const bool f0 = j < N && key[j] == bk0, f1 = j < N && key[j] == bk1;
+        const unsigned m0 = __ballot_sync(0xffffffffu, f0), m1 = __ballot_sync(0xffffffffu, f1);
+        if (lane == 0) {
+            wsum[0][warp] = __popc(m0);
+            wsum[1][warp] = __popc(m1);
+        }
         __syncthreads();
-        int pre = 0, tot = 0;
+        int pre0 = 0, tot0 = 0, pre1 = 0, tot1 = 0;
 #pragma unroll
         for (int w = 0; w < NT / 32; ++w) {
-            pre += w < warp ? wsum[w] : 0;
-            tot += wsum[w];
+            pre0 += w < warp ? wsum[0][w] : 0;
+            tot0 += wsum[0][w];
+            pre1 += w < warp ? wsum[1][w] : 0;
+            tot1 += wsum[1][w];
         }
-        pre += __popc(m & ((1u << lane) - 1u));
-        if (f && pre == off) sel = j;
-        off -= tot;
+        const unsigned below = (1u << lane) - 1u;
+        if (f0 && pre0 + __popc(m0 & below) == off0) sel[0] = j;
+        if (f1 && pre1 + __popc(m1 & below) == off1) sel[1] = j;
+        off0 -= tot0;
+        off1 -= tot1;
         __syncthreads();
-        if (sel >= 0) break;  // uniform: read after the barrier
+        if (sel[0] >= 0 && (bk1 < 0 || sel[1] >= 0)) break;  // uniform: read after the barrier
     }
-    return sel;
+    return make_int2(sel[0], sel[1]);
 }
 
 // kMode & 3: 0 scalar log-decay g [T, Hv]; 1 per-key-channel g [T, Hv, K];
@@ -169,14 +181,28 @@ recurrent_kernel(RecParams p) {
     // Work unit (sequence b, head h, value block zb).  Multi-token calls take
     // the sequences longest first, sequence-major, so that the long ones do not
     // form the tail of the grid.
+    // With pf_stride (the CTAs resident at once), the CTA also names the unit
+    // that its slot of the GPU will most likely run next, lin + pf_stride, and
+    // warms L2 with that unit's state slab and first input rows.
     int b = blockIdx.x, h = blockIdx.y, zb = blockIdx.z;
+    int pb = -1, ph = 0, pzb = 0;  // the next unit on this slot (pb < 0: none)
     if (p.lpt) {
         const int units = gridDim.y * gridDim.z;
         const int lin = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
         const int r = lin / units, u = lin - r * units;
         h = u / gridDim.z;
         zb = u - h * gridDim.z;
-        b = lpt_sequence<BV / kRowsPerWarp * 32>(p, gridDim.x, r);
+        const int lin2 = lin + p.pf_stride;
+        const bool pf = p.pf_stride > 0 && lin2 < (int)gridDim.x * units;
+        const int r2 = pf ? lin2 / units : -1;
+        const int2 bb = lpt_sequences<BV / kRowsPerWarp * 32>(p, gridDim.x, r, r2);
+        b = bb.x;
+        if (pf && bb.y >= 0) {
+            const int u2 = lin2 - r2 * units;
+            pb = bb.y;
+            ph = u2 / gridDim.z;
+            pzb = u2 - ph * gridDim.z;
+        }
         if (b < 0) return;
     }
     const int lane = threadIdx.x & 31;
@@ -420,6 +446,25 @@ recurrent_kernel(RecParams p) {
                 if (lane == 0) stok[4 * j + 2] = kq;
             }
             __syncthreads();
+            if (t0 == bos && pb >= 0 && warp == kWarps - 1) {
+                // warm L2 for the next unit on this slot of the GPU: its state
+                // slab, and the k, q rows and v slice of its first window
+                const int s2 = p.idx[pb];
+                if (s2 >= 0 && s2 < p.num_slots) {
+                    const int bos2 = max(p.cu[pb], 0), eos2 = (int)min((int64_t)p.cu[pb + 1], p.T);
+                    const int n2 = min(kWin, eos2 - bos2), kh2 = ph / (p.Hv / p.Hk);
+                    if (lane == 0)
+                        tc::prefetch_l2(pool + (((size_t)s2 * p.Hv + ph) * V + pzb * BV) * K,
+                                        (uint32_t)(BV * K * sizeof(PoolT)));
+                    for (int e = lane - 1; e >= 0 && e < 3 * n2; e += 31) {
+                        const int i = e / 3, w = e - 3 * i;
+                        const size_t t2 = (size_t)(bos2 + i);
+                        if (w == 0) tc::prefetch_l2(kp + (t2 * p.Hk + kh2) * K, (uint32_t)(K * sizeof(InT)));
+                        else if (w == 1) tc::prefetch_l2(qp + (t2 * p.Hk + kh2) * K, (uint32_t)(K * sizeof(InT)));
+                        else tc::prefetch_l2(vp + (t2 * p.Hv + ph) * V + pzb * BV, (uint32_t)(BV * sizeof(InT)));
+                    }
+                }
+            }
 #pragma unroll 1
             for (int j = 0; j < n; ++j) {
                 float kk[KPT], uu[KPT], ww[KPT], ac[KPT];
@@ -469,14 +514,36 @@ recurrent_kernel(RecParams p) {
     }
 }
 
+// One instantiation on `grid`.  Multi-token calls in longest-first order also
+// get the number of CTAs resident at once (occupancy x SMs), which names the
+// unit each CTA warms L2 for.
+template <typename InT, typename PoolT, int K, int BV, int kMode>
+cudaError_t launch_one(RecParams p, dim3 grid, int sms, cudaStream_t stream) {
+    constexpr int threads = BV / kRowsPerWarp * 32;
+    const unsigned smem = p.staged ? stage_bytes<K, BV, kMode>() : 0;
+    p.pf_stride = 0;
+    if (p.lpt && sms > 0) {
+        static const int per_sm = [] {
+            int n = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, recurrent_kernel<InT, PoolT, K, BV, kMode>, threads,
+                                                              stage_bytes<K, BV, kMode>()) != cudaSuccess)
+                n = 0;
+            return n;
+        }();
+        p.pf_stride = per_sm * sms;
+    }
+    recurrent_kernel<InT, PoolT, K, BV, kMode><<<grid, threads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
 template <typename InT, typename PoolT, int K, int kGate>
 cudaError_t launch_k(const RecParams& p, int N, int V, cudaStream_t stream) {
-    if (kGate != 2 && p.nw) {  // gated-norm epilogue: one CTA per (sequence, head), BV = V = K
-        KernelTimer kt("recurrent", stream);
-        const unsigned smem = p.staged ? stage_bytes<K, K, kGate | 4>() : 0;
-        recurrent_kernel<InT, PoolT, K, K, kGate | 4><<<dim3(N, p.Hv, 1), K / kRowsPerWarp * 32, smem, stream>>>(p);
-        return cudaGetLastError();
-    }
+    int sms = 0, dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 0;
+    KernelTimer kt("recurrent", stream);
+    if (kGate != 2 && p.nw)  // gated-norm epilogue: one CTA per (sequence, head), BV = V = K
+        return launch_one<InT, PoolT, K, K, kGate | 4>(p, dim3(N, p.Hv, 1), sms, stream);
     // V-column split.  Single-token decode: 64-row blocks (128 threads)
     // measured best on GB300 (6.50 vs 6.42 TB/s at 128 rows).  Multi-token
     // calls: 128-row blocks (256 threads), since one CTA then stages a window's
@@ -484,31 +551,18 @@ cudaError_t launch_k(const RecParams& p, int N, int V, cudaStream_t stream) {
     // 0.103 ms), as long as the units fill every SM with two such CTAs.
     // 32-row blocks when there are few sequences.
     const long units = (long)N * p.Hv;
-    int sms = 0, dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        sms = 0;
     int bv = 64;
     if (V < 64 || units < 256) bv = 32;
     else if (p.staged && V % 128 == 0 && sms > 0 && units >= 2L * sms) bv = 128;
 #ifdef GDR_REC_BV
     if (GDR_REC_BV <= V) bv = GDR_REC_BV;  // fixed split for tuning builds
 #endif
-    dim3 grid(N, p.Hv, V / bv);
-    KernelTimer kt("recurrent", stream);
+    const dim3 grid(N, p.Hv, V / bv);
     switch (bv) {
-        case 128:
-            recurrent_kernel<InT, PoolT, K, 128, kGate>
-                <<<grid, 256, p.staged ? stage_bytes<K, 128, kGate>() : 0, stream>>>(p);
-            break;
-        case 64:
-            recurrent_kernel<InT, PoolT, K, 64, kGate>
-                <<<grid, 128, p.staged ? stage_bytes<K, 64, kGate>() : 0, stream>>>(p);
-            break;
-        default:
-            recurrent_kernel<InT, PoolT, K, 32, kGate><<<grid, 64, p.staged ? stage_bytes<K, 32, kGate>() : 0, stream>>>(p);
-            break;
+        case 128: return launch_one<InT, PoolT, K, 128, kGate>(p, grid, sms, stream);
+        case 64: return launch_one<InT, PoolT, K, 64, kGate>(p, grid, sms, stream);
+        default: return launch_one<InT, PoolT, K, 32, kGate>(p, grid, sms, stream);
     }
-    return cudaGetLastError();
 }
 
 template <typename InT, typename PoolT>
@@ -533,6 +587,7 @@ cudaError_t launch_recurrent(const RecurrentArgs& a, cudaStream_t stream) {
     p.num_slots = a.num_slots;
     p.lpt = a.T > a.N && a.N <= kLptMax;
     p.staged = a.T > a.N;
+    p.pf_stride = 0;
     p.T = a.T;
     p.ga = a.ga; p.gb = a.gb; p.A_log = a.A_log; p.dt_bias = a.dt_bias; p.beta_mul = a.beta_mul;
     p.nw = a.norm_weight; p.nz = a.norm_gate; p.neps = a.norm_eps;
