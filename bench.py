@@ -1,17 +1,20 @@
 """Benchmark of the GB300 gated delta rule forward library.
 
 One step = one chunked-prefill call (gdr_chunk_fwd: chunk metadata, intra-chunk
-cumsum / A / solve / WY, inter-chunk state recurrence, output) over the varlen
-bf16 workload: 4 sequences {65, 1000, 2048, 3000} (6113 tokens), 16 heads,
-K = V = 128, g ~ U[-2, 0], fp32 initial state.  `value` is prefill tokens/s with
-inputs resident in HBM; the L2 (129 MB) is flushed before every timed step by
-writing a 256 MB buffer outside the step's events.  The same line carries the
-recurrent decode (256 sequences, fp32 pool, commit), the multi-step verify
-(64 sequences, 1..12 tokens, bf16 pool + per-token states), the same verify
-with the gates formed in the kernel from raw projections, the decode with
-per-key-channel gates, the decode with the gated RMSNorm output epilogue and
-the long KDA prefill (T = 32768, Hv = 32,
-per-channel gate) as extra objects, each with its own roofline.
+cumsum / A / solve / WY, inter-chunk state recurrence, output) over the long
+KDA-style workload: one sequence of 32768 tokens, Hk = 16, Hv = 32 (two value
+heads per key head), K = V = 128, bf16, per-key-channel decays gk ~ U[-0.1, 0]
+of shape [T, 32, 128]; the largest prefill configuration that fits one GPU.
+`value` is prefill tokens/s with inputs resident in HBM; the step's inputs
+(1.1 GB) are larger than L2 (129 MB), and L2 is flushed before every timed step
+as well by writing a 256 MB buffer outside the step's events.  The same line
+carries the varlen prefill (4 sequences {65, 1000, 2048, 3000}, 16 heads,
+g ~ U[-2, 0], fp32 initial state), the recurrent decode (256 sequences, fp32
+pool, commit), the multi-step verify (64 sequences, 1..12 tokens, bf16 pool +
+per-token states), the same verify with the gates formed in the kernel from
+raw projections, the decode with per-key-channel gates, the decode with the
+gated RMSNorm output epilogue and the long few-head prefill with the
+chunk-parallel scan as extra objects, each with its own roofline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -26,6 +29,7 @@ import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -168,12 +172,12 @@ class ClockSampler:
     def __init__(self, device_index):
         self.idx = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = None
 
     def start(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
+            fd, self.path = tempfile.mkstemp(prefix="gdr_clocks_", suffix=".csv")
+            self.f = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
@@ -188,7 +192,10 @@ class ClockSampler:
         self.f.close()
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        with open(self.path) as f:
+            rows = f.read().splitlines()
+        os.unlink(self.path)
+        for line in rows:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -395,19 +402,51 @@ def measure(runner, K, W, flush, stream, work_fn, bound_of, peaks, units_per_ste
     return ms, prof, roofline(prof, K, work_fn, peaks, bound_of, runner.case.name), units_per_step / (ms / 1e3)
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu), for the CPU-baseline record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine() or "unknown"
+
+
+ORACLE_SAMPLE_TOKENS = 1024
+
+
+def oracle_sample(case):
+    """A bounded sample of a prefill workload for the oracle: the first
+    ORACLE_SAMPLE_TOKENS tokens of its longest sequence (with that sequence's
+    initial state), all heads.  Returns (keyword arguments of oracle.tokenwise,
+    tokens, description)."""
+    cu = case.cu_seqlens.tolist()
+    b = max(range(case.N), key=lambda i: cu[i + 1] - cu[i])
+    ntok = min(ORACLE_SAMPLE_TOKENS, cu[b + 1] - cu[b])
+    sl = slice(cu[b], cu[b] + ntok)
+    h0 = case.initial_state[b:b + 1] if case.initial_state is not None else None
+    kw = dict(q=case.q[sl], k=case.k[sl], v=case.v[sl], beta=case.beta[sl],
+              g=case.g[sl] if case.g is not None else None, gk=case.gk[sl] if case.gk is not None else None,
+              initial_state=h0, cu_seqlens=[0, ntok], scale=case.scale)
+    Hv = case.v.shape[1]
+    return kw, ntok, f"the first {ntok} tokens of the longest sequence x all {Hv} heads of {case.name}"
+
+
 def cpu_baseline_prefill(case, budget_s=12.0):
     """The oracle as it stands (fp64 tokenwise, OpenMP over sequence x head) on a
-    bounded sample of the varlen workload: the 1000-token sequence, all heads,
-    repeated until about `budget_s` seconds of wall time have passed."""
+    bounded sample of the workload (oracle_sample), repeated until about
+    `budget_s` seconds of wall time have passed."""
     import oracle
-    cu = case.cu_seqlens.tolist()
-    b = 1
-    sl = slice(cu[b], cu[b + 1])
-    ntok = cu[b + 1] - cu[b]
-    h0 = case.initial_state[b:b + 1] if case.initial_state is not None else None
-    args = dict(q=case.q[sl], k=case.k[sl], v=case.v[sl], beta=case.beta[sl],
-                g=case.g[sl] if case.g is not None else None, gk=case.gk[sl] if case.gk is not None else None,
-                initial_state=h0, cu_seqlens=[0, ntok], scale=case.scale)
+    args, ntok, what = oracle_sample(case)
     cores = len(os.sched_getaffinity(0))
     oracle.tokenwise(**args, nthreads=cores)      # load + warm
     t0 = time.perf_counter()
@@ -423,27 +462,26 @@ def cpu_baseline_prefill(case, budget_s=12.0):
     # independent per (sequence, head))
     Hv, Hk = case.v.shape[1], case.q.shape[1]
     hs = [0, 1]
-    kh = [h // (Hv // Hk) for h in hs]
+    kh = sorted({h // (Hv // Hk) for h in hs})
     one = dict(args, q=args["q"][:, kh], k=args["k"][:, kh], v=args["v"][:, hs], beta=args["beta"][:, hs],
                g=args["g"][:, hs] if args["g"] is not None else None,
                gk=args["gk"][:, hs] if args["gk"] is not None else None,
-               initial_state=h0[:, hs] if h0 is not None else None)
+               initial_state=args["initial_state"][:, hs] if args["initial_state"] is not None else None)
     t1 = time.perf_counter()
     oracle.tokenwise(**one, nthreads=1)
     d1 = (time.perf_counter() - t1) * Hv / len(hs)
-    return {"value": round(ntok / dt, 2), "unit": "tokens/s", "cores": used,
-            "kind": "oracle",
-            "sample": f"1 sequence of {ntok} tokens x all {Hv} heads of the varlen workload, "
-                      f"{reps} repetitions ({dt * reps:.1f} s)",
+    return {"value": round(ntok / dt, 2), "unit": "tokens/s", "cores": used, "cpu_model": cpu_model(),
+            "kind": "oracle", "sample": f"{what}, {reps} repetitions ({dt * reps:.1f} s)",
             "value_1core": round(ntok / d1, 2),
-            "sample_1core": f"the same sequence, {len(hs)} of the {Hv} heads on 1 thread, scaled to all heads"}
+            "sample_1core": f"the same tokens, {len(hs)} of the {Hv} heads on 1 thread, scaled to all heads"}
 
 
 def config_of(case):
     d = case.dims
     return {"workload": case.name, "global_batch": case.N, "seq_len": case.T, "heads_k": d["Hk"],
-            "heads_v": d["Hv"], "head_dim": d["K"], "chunk": 64, "parallelism": "replicas",
-            "l2": "flushed (256 MB write) before every timed step"}
+            "heads_v": d["Hv"], "head_dim": d["K"], "chunk": 64,
+            "gate": "per-key-channel gk [T, Hv, K]" if case.gk is not None else "scalar g [T, Hv]",
+            "parallelism": "replicas", "l2": "flushed (256 MB write) before every timed step"}
 
 
 def reference_arm(args):
@@ -453,13 +491,8 @@ def reference_arm(args):
     if rank != 0:
         return
     import oracle
-    case = workloads.varlen_bf16_prefill()
-    cu = case.cu_seqlens.tolist()
-    b = 1
-    sl = slice(cu[b], cu[b + 1])
-    ntok = cu[b + 1] - cu[b]
-    kw = dict(q=case.q[sl], k=case.k[sl], v=case.v[sl], beta=case.beta[sl], g=case.g[sl],
-              initial_state=case.initial_state[b:b + 1], cu_seqlens=[0, ntok], scale=case.scale)
+    case = workloads.kda_long_prefill(args.kda_T)
+    kw, ntok, what = oracle_sample(case)
     cores = len(os.sched_getaffinity(0))
     for _ in range(args.warmup):
         oracle.tokenwise(**kw, nthreads=cores)
@@ -473,23 +506,36 @@ def reference_arm(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_of(case),
             "cpu_baseline": {"value": round(val, 2), "unit": "tokens/s", "cores": min(cores, oracle.num_threads()),
-                             "kind": "oracle",
-                             "sample": f"1 sequence of {ntok} tokens x all 16 heads of the varlen workload per step"},
+                             "cpu_model": cpu_model(), "kind": "oracle", "sample": f"{what} per step"},
             "e2e": {"value": round(val, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+PREFILL_TARGET_FRAC_BF16 = 0.5  # the chunked prefill's target share of the bf16 tensor peak
+
+
+def prefill_whole_call(case, ms, peaks):
+    """The whole prefill call against both peaks (algorithmic flop and bytes)."""
+    d = case.dims
+    fl = prefill_flops(case.T, d["Hv"], d["K"], d["V"])
+    by = prefill_bytes(case)
+    return {"tflops": round(fl / (ms / 1e3) / 1e12, 3), "frac_bf16": round(fl / (ms / 1e3) / 1e12 / peaks["bf16"], 5),
+            "gbs": round(by / (ms / 1e3) / 1e9, 2), "frac_hbm": round(by / (ms / 1e3) / 1e9 / peaks["hbm"], 5),
+            "algorithmic_flop_per_step": fl, "algorithmic_bytes_per_step": by}
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", default="", help="comma list of sections: prefill,decode,verify,kda,kda_decode,"
-                                               "verify_gated,decode_norm,long_scan")
+    ap.add_argument("--only", default="", help="comma list of extra sections: varlen,decode,verify,kda_decode,"
+                                               "verify_gated,decode_norm,long_scan (the headline always runs)")
     ap.add_argument("--kda-T", type=int, default=32768,
-                    help="tokens of the long KDA prefill section (32768 is the workload; smaller for profiling)")
+                    help="tokens of the long KDA prefill (32768 is the workload; smaller for profiling)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end run (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -510,7 +556,7 @@ def main():
     stream = torch.cuda.Stream()
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush = lambda: flush_buf.fill_(1)
-    only = set(filter(None, args.only.split(","))) or {"prefill", "decode", "verify", "kda", "kda_decode",
+    only = set(filter(None, args.only.split(","))) or {"varlen", "decode", "verify", "kda_decode",
                                                         "verify_gated", "decode_norm", "long_scan"}
 
     dist_ = Dist(world, dev)
@@ -521,10 +567,12 @@ def main():
 
     max_over_ranks = dist_.max
 
-    pre_case = workloads.varlen_bf16_prefill()
-    pre = Prefill(pre_case, dev)
+    head_case = workloads.kda_long_prefill(args.kda_T)
+    head = Prefill(head_case, dev)
     extra = {}
-    dec = ver = kda = kdec = vg = dn = None
+    var = dec = ver = kdec = vg = dn = None
+    if "varlen" in only:
+        var = Prefill(workloads.varlen_bf16_prefill(), dev)
     if "decode" in only:
         dec = PoolRun(workloads.decode_fp32_pool(), dev)
     if "kda_decode" in only:
@@ -535,88 +583,51 @@ def main():
         dn = PoolRun(workloads.decode_fp32_pool_norm(), dev)
     if "verify" in only:
         ver = PoolRun(workloads.verify_bf16_pool(), dev)
-    if "kda" in only:
-        kda = Prefill(workloads.kda_long_prefill(args.kda_T), dev)
     lsc = lpl = None
     if "long_scan" in only:
         long_case = workloads.long_few_heads_prefill()
         lsc = Prefill(long_case, dev, flags=gdr.GDR_CHUNK_SCAN)
         lpl = Prefill(long_case, dev)
     for _ in range(args.warmup):
-        pre.step(stream)
+        head.step(stream)
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
     barrier()
-    times, prof = timed_steps(lambda: pre.step(stream), args.steps, flush, stream)
+    times, prof = timed_steps(lambda: head.step(stream), args.steps, flush, stream)
     barrier()
     ms = max_over_ranks(float(np.mean(times)))
     launches = sum(v[1] for v in prof.values())
-    roof = roofline(prof, args.steps, prefill_work_fn(pre_case), peaks, lambda n: "tensor", pre_case.name)
-    tokens = pre_case.T
-    value = whole_job_throughput(tokens, ms, world)
-    whole_flops = prefill_flops(pre_case.T, 16, 128, 128)
-    whole_bytes = prefill_bytes(pre_case)
-    whole = {"tflops": round(whole_flops / (ms / 1e3) / 1e12, 3),
-             "frac_bf16": round(whole_flops / (ms / 1e3) / 1e12 / peaks["bf16"], 5),
-             "gbs": round(whole_bytes / (ms / 1e3) / 1e9, 2),
-             "frac_hbm": round(whole_bytes / (ms / 1e3) / 1e9 / peaks["hbm"], 5),
-             "algorithmic_flop_per_step": whole_flops, "algorithmic_bytes_per_step": whole_bytes}
+    roof = roofline(prof, args.steps, prefill_work_fn(head_case), peaks, lambda n: "tensor", head_case.name)
+    value = whole_job_throughput(head_case.T, ms, world)
+    whole = prefill_whole_call(head_case, ms, peaks)
+    target = {"prefill_frac_bf16_target": PREFILL_TARGET_FRAC_BF16,
+              "dominant_kernel_frac_bf16": roof["frac"], "whole_call_frac_bf16": whole["frac_bf16"],
+              "met": roof["frac"] >= PREFILL_TARGET_FRAC_BF16,
+              "gap_x": round(PREFILL_TARGET_FRAC_BF16 / max(roof["frac"], 1e-9), 1)}
 
-    if dec is not None:
-        nbytes, toks = pool_bytes(dec.case)
-        d_ms, d_prof, d_roof, _ = measure(dec, max(args.steps, 20), args.warmup, flush, stream,
-                                          lambda n: nbytes, lambda n: "hbm", peaks, toks)
-        launches += sum(v[1] for v in d_prof.values())
-        d_ms = max_over_ranks(d_ms)
-        extra["decode"] = {"workload": dec.case.name, "tokens_per_s": round(world * toks / (d_ms / 1e3), 1),
-                           "ms_per_step": round(d_ms, 4), "valid_tokens": toks, "roofline": d_roof}
-    if ver is not None:
-        nbytes, toks = pool_bytes(ver.case)
-        v_ms, v_prof, v_roof, _ = measure(ver, max(args.steps, 20), args.warmup, flush, stream,
-                                          lambda n: nbytes, lambda n: "hbm", peaks, toks)
+    if var is not None:
+        v_ms, v_prof, v_roof, _ = measure(var, args.steps, args.warmup, flush, stream, prefill_work_fn(var.case),
+                                          lambda n: "tensor", peaks, var.case.T)
         launches += sum(v[1] for v in v_prof.values())
         v_ms = max_over_ranks(v_ms)
-        extra["verify"] = {"workload": ver.case.name, "tokens_per_s": round(world * toks / (v_ms / 1e3), 1),
-                           "ms_per_step": round(v_ms, 4), "valid_tokens": toks, "roofline": v_roof}
-    if kdec is not None:
-        nbytes, toks = pool_bytes(kdec.case)
-        kd_ms, kd_prof, kd_roof, _ = measure(kdec, max(args.steps, 20), args.warmup, flush, stream,
-                                             lambda n: nbytes, lambda n: "hbm", peaks, toks)
-        launches += sum(v[1] for v in kd_prof.values())
-        kd_ms = max_over_ranks(kd_ms)
-        extra["kda_decode"] = {"workload": kdec.case.name, "tokens_per_s": round(world * toks / (kd_ms / 1e3), 1),
-                               "ms_per_step": round(kd_ms, 4), "valid_tokens": toks, "roofline": kd_roof}
-    if vg is not None:
-        nbytes, toks = pool_bytes(vg.case)
-        vg_ms, vg_prof, vg_roof, _ = measure(vg, max(args.steps, 20), args.warmup, flush, stream,
-                                             lambda n: nbytes, lambda n: "hbm", peaks, toks)
-        launches += sum(v[1] for v in vg_prof.values())
-        vg_ms = max_over_ranks(vg_ms)
-        extra["verify_gated"] = {"workload": vg.case.name, "tokens_per_s": round(world * toks / (vg_ms / 1e3), 1),
-                                 "ms_per_step": round(vg_ms, 4), "valid_tokens": toks, "roofline": vg_roof}
-    if dn is not None:
-        nbytes, toks = pool_bytes(dn.case)
-        dn_ms, dn_prof, dn_roof, _ = measure(dn, max(args.steps, 20), args.warmup, flush, stream,
-                                             lambda n: nbytes, lambda n: "hbm", peaks, toks)
-        launches += sum(v[1] for v in dn_prof.values())
-        dn_ms = max_over_ranks(dn_ms)
-        extra["decode_norm"] = {"workload": dn.case.name, "tokens_per_s": round(world * toks / (dn_ms / 1e3), 1),
-                                "ms_per_step": round(dn_ms, 4), "valid_tokens": toks, "roofline": dn_roof}
-    if kda is not None:
-        k_ms, k_prof, k_roof, _ = measure(kda, max(3, args.steps // 10), args.warmup, flush, stream,
-                                          prefill_work_fn(kda.case), lambda n: "tensor", peaks, kda.case.T)
-        launches += sum(v[1] for v in k_prof.values())
-        k_ms = max_over_ranks(k_ms)
-        kf = prefill_flops(kda.case.T, 32, 128, 128)
-        kb = prefill_bytes(kda.case)
-        extra["kda_long"] = {"workload": kda.case.name, "tokens_per_s": round(world * kda.case.T / (k_ms / 1e3), 1),
-                             "ms_per_step": round(k_ms, 4), "roofline": k_roof,
-                             "whole_call": {"tflops": round(kf / (k_ms / 1e3) / 1e12, 3),
-                                            "gbs": round(kb / (k_ms / 1e3) / 1e9, 2),
-                                            "frac_hbm": round(kb / (k_ms / 1e3) / 1e9 / peaks["hbm"], 5)}}
+        extra["varlen_prefill"] = {"workload": var.case.name,
+                                   "tokens_per_s": round(world * var.case.T / (v_ms / 1e3), 1),
+                                   "ms_per_step": round(v_ms, 5), "roofline": v_roof,
+                                   "whole_call": prefill_whole_call(var.case, v_ms, peaks)}
+    for key, run in (("decode", dec), ("verify", ver), ("kda_decode", kdec), ("verify_gated", vg),
+                     ("decode_norm", dn)):
+        if run is None:
+            continue
+        nbytes, toks = pool_bytes(run.case)
+        p_ms, p_prof, p_roof, _ = measure(run, max(args.steps, 20), args.warmup, flush, stream,
+                                          lambda n, nb=nbytes: nb, lambda n: "hbm", peaks, toks)
+        launches += sum(v[1] for v in p_prof.values())
+        p_ms = max_over_ranks(p_ms)
+        extra[key] = {"workload": run.case.name, "tokens_per_s": round(world * toks / (p_ms / 1e3), 1),
+                      "ms_per_step": round(p_ms, 4), "valid_tokens": toks, "roofline": p_roof}
     if lsc is not None:
         # the long few-head sequence with the chunk-parallel scan, and the
         # one-pass chain on the same inputs for comparison
@@ -627,8 +638,6 @@ def main():
                                        lambda n: "tensor", peaks, lpl.case.T)
         launches += sum(v[1] for v in ls_prof.values()) + sum(v[1] for v in lp_prof.values())
         ls_ms, lp_ms = max_over_ranks(ls_ms), max_over_ranks(lp_ms)
-        d = lsc.case.dims
-        lf = prefill_flops(lsc.case.T, d["Hv"], d["K"], d["V"])
         extra["long_scan"] = {
             "workload": lsc.case.name, "flags": "GDR_CHUNK_SCAN",
             "tokens_per_s": round(world * lsc.case.T / (ls_ms / 1e3), 1), "ms_per_step": round(ls_ms, 4),
@@ -638,25 +647,26 @@ def main():
                                               for k, v in lp_prof.items()}},
             "speedup_vs_one_pass": round(lp_ms / ls_ms, 3),
             "kernel_ms": {k: round(v[0] / v[1], 4) for k, v in ls_prof.items()},
-            "whole_call": {"tflops": round(lf / (ls_ms / 1e3) / 1e12, 3),
-                           "frac_bf16": round(lf / (ls_ms / 1e3) / 1e12 / peaks["bf16"], 5)},
+            "whole_call": prefill_whole_call(lsc.case, ls_ms, peaks),
             "roofline": ls_roof}
     clocks = sampler.stop()
 
     # end to end through the public API from pinned host buffers
-    e2e_ms, h2d, d2h = pre.e2e(max(5, args.steps // 5), stream)
-    e2e_ms = max_over_ranks(e2e_ms)
+    e2e = None
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = head.e2e(max(5, args.steps // 4), stream)
+        e2e_ms = max_over_ranks(e2e_ms)
+        e2e = {"value": round(world * head_case.T / (e2e_ms / 1e3), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)}
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = cpu_baseline_prefill(pre_case)
+        cpu = cpu_baseline_prefill(head_case)
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-                "data": "synthetic", "config": config_of(pre_case),
-                "roofline": roof, "whole_call": whole,
-                "e2e": {"value": round(world * tokens / (e2e_ms / 1e3), 1), "unit": "tokens/s",
-                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+                "data": "synthetic", "config": config_of(head_case),
+                "roofline": roof, "whole_call": whole, "target": target, "e2e": e2e,
                 "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu, **extra}
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -47,53 +47,6 @@
 #include "launch.h"
 #include "tc.cuh"
 
-// Optional timeline trace of one chain CTA (built only with -DGDR_TRACE):
-// %globaltimer stamps per role and chunk, read back with gdr_trace_dump.
-#ifdef GDR_TRACE
-__device__ unsigned long long g_trace[24][64];
-#define GDR_TRACE_POINT(slot, c)                                                      \
-    do {                                                                              \
-        if (blockIdx.x == 0 && blockIdx.y == 0 && (c) < 64) g_trace[slot][c] = clock64(); \
-    } while (0)
-#define GDR_TRACE_PREP(phase)                                                                      \
-    do {                                                                                           \
-        if (blockIdx.x == 7 && blockIdx.y == 0 && threadIdx.x == 0) g_trace[23][phase] = clock64(); \
-    } while (0)
-#define GDR_TRACE_WARP(slot)                                                                                   \
-    do {                                                                                                       \
-        if (blockIdx.x == 7 && blockIdx.y == 0 && (threadIdx.x & 31) == 0) g_trace[22][(slot) * 8 + (threadIdx.x >> 5)] = clock64(); \
-    } while (0)
-__device__ unsigned long long g_items[4096][3];  // prep item: start, end (%globaltimer), SM id
-extern "C" __attribute__((visibility("default"))) int gdr_trace_dump(unsigned long long* host) {
-    return (int)cudaMemcpyFromSymbol(host, g_trace, sizeof(g_trace));
-}
-extern "C" __attribute__((visibility("default"))) int gdr_trace_items(unsigned long long* host) {
-    return (int)cudaMemcpyFromSymbol(host, g_items, sizeof(g_items));
-}
-#define GDR_TRACE_ITEM(item, which)                                                                  \
-    do {                                                                                             \
-        if (threadIdx.x == 0 && (item) < 4096) {                                                     \
-            unsigned long long t;                                                                    \
-            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));                                    \
-            g_items[item][which] = t;                                                                \
-            if (which == 0) { unsigned sm; asm("mov.u32 %0, %%smid;" : "=r"(sm)); g_items[item][2] = sm; } \
-        }                                                                                            \
-    } while (0)
-#else
-#define GDR_TRACE_POINT(slot, c) \
-    do {                         \
-    } while (0)
-#define GDR_TRACE_PREP(phase) \
-    do {                      \
-    } while (0)
-#define GDR_TRACE_ITEM(item, which) \
-    do {                            \
-    } while (0)
-#define GDR_TRACE_WARP(slot) \
-    do {                     \
-    } while (0)
-#endif
-
 namespace gdr {
 namespace {
 
@@ -192,7 +145,6 @@ __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict_
         }
     }
     __syncthreads();
-    GDR_TRACE_PREP(21);
     // step 2: pair p = tid / 128; thread: row i, columns j0, j0 + 1 of a 16 x 16 block
     {
         const int p = (tid >> 7) & 1, e = tid & 127, i = e >> 3, j0 = 2 * (e & 7);
@@ -222,7 +174,6 @@ __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict_
         }
     }
     __syncthreads();
-    GDR_TRACE_PREP(22);
     // step 3: 2 x 2 tile per thread, rows 2 ti, 2 ti + 1 and columns 2 tj, 2 tj + 1
     {
         const int ti = (tid >> 4) & 15, tj = tid & 15, i0 = 2 * ti, j0 = 2 * tj;
@@ -243,7 +194,6 @@ __device__ void solve_unit_lower(const float* __restrict__ A, float* __restrict_
             Z[(i0 + 1) * 32 + j0 + 1] = y11;
         }
         __syncthreads();
-        GDR_TRACE_PREP(23);
         if (act) {
             float t00 = 0.f, t01 = 0.f, t10 = 0.f, t11 = 0.f;
 #pragma unroll 8
@@ -376,8 +326,6 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
         const int start = info.y, L = info.z;
         const int kh = h / grp;
 
-        GDR_TRACE_PREP(0);
-        GDR_TRACE_ITEM(item, 0);
         // ---- stage K, Q (as X) and V rows (cp.async), gates, beta -------------------
         stage_rows_async<NT>(sm + S::kX, 2 * C, 0, kp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
         stage_rows_async<NT>(sm + S::kX, 2 * C, C, qp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
@@ -439,7 +387,6 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
         tc::fence_before();
         __syncthreads();
         tc::fence_after();
-        GDR_TRACE_PREP(1);
         const uint32_t sX = tc::smem_u32(sm + S::kX), sV = tc::smem_u32(sm + S::kV);
         const float* gl = kKDA ? gam + (L - 1) * D : gam + (L - 1);
 
@@ -507,7 +454,6 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
             if (tid < D) rec[64 + tid] = __expf(kKDA ? gl[tid] : gl[0]);
             if (tid == 0) reinterpret_cast<int*>(rec)[192] = L;
         }
-        GDR_TRACE_PREP(2);
 
         // ---- A (strictly lower) and P (lower incl. diagonal) -------------------------
         unsigned char* Pdst = p.Yw + ((size_t)chunk * p.Hv + h) * kYwBytes;  // rows 64..127 of column block 0
@@ -515,8 +461,6 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
             if (!tc::mbar_wait(bar0, ph0, abort_flag)) raise_error(p, 1u);
             ph0 ^= 1u;
             tc::fence_after();
-            GDR_TRACE_PREP(24);
-            GDR_TRACE_WARP(0);
             // thread: accumulator row r = 32 q + lane (rows < 64: K K^T, >= 64: Q K^T),
             // columns [32 hf, 32 hf + 32)
             const int r = 32 * q + lane, i = r & 63;
@@ -531,9 +475,7 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
             }
             const float gi = gam[i], bi = bet[i];
             float gv[32];
-            GDR_TRACE_WARP(3);
             tc::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + 32 * hf, gv);
-            GDR_TRACE_WARP(4);
             if (r < C) {
                 const float sc = i < L ? bi : 0.f;
 #pragma unroll
@@ -558,7 +500,6 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
                     *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(C + i, 4 * hf + cc, 2 * C)) =
                         make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
             }
-            GDR_TRACE_WARP(1);
         } else {
             // Per-channel decays: A_ij = beta_i sum_c k_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}
             // and P_ij = sum_c q_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}.  Pairs in different
@@ -626,7 +567,6 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
                 tc::fence_before();
                 __syncthreads();
                 tc::fence_after();
-                GDR_TRACE_PREP(9 + 3 * lev);
                 // three issuers, one split product each, into accumulator columns 32 w
                 if (warp < 3 && lane == 0) {
                     const uint32_t la = tc::smem_u32(sm + (warp == 2 ? S::kLl : S::kLh));
@@ -642,7 +582,6 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
                 if (!tc::mbar_wait(bar1, ph1, abort_flag)) raise_error(p, 1u);
                 ph1 ^= 1u;
                 tc::fence_after();
-                GDR_TRACE_PREP(10 + 3 * lev);
                 if (warp < 4) {
                     // M = 64 accumulator: row r = 16 warp + lane (lane < 16); rows 0..31
                     // are A rows, 32..63 P rows; column n pairs with row r when both
@@ -667,7 +606,6 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
                     }
                 }
                 tc::fence_before();
-                GDR_TRACE_PREP(11 + 3 * lev);
             }
             {
                 // pairs inside a 4-token block: warp w takes the block of tokens
@@ -744,12 +682,9 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
         }
         tc::fence_before();
         __syncthreads();
-        GDR_TRACE_PREP(3);
-        GDR_TRACE_WARP(2);
 
         // ---- Tm = (I + A)^{-1} -----------------------------------------------------------
         solve_unit_lower<NT>(As, Tm, Z, tid);
-        GDR_TRACE_PREP(4);
 
         // ---- split operands: T' = Tm diag(beta e^{gam}) (scalar gate) or Tm diag(beta);
         //      T'' = Tm diag(beta).  Written over the dead Q rows of X and the A matrix.
@@ -771,7 +706,6 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
         }
         tc::fence_proxy_async();
         __syncthreads();
-        GDR_TRACE_PREP(5);
 
         // ---- W = T' K (or T'' (K o e^Gam)), U = T'' V ----------------------------------------
         if (tid == 0) {
@@ -799,7 +733,6 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
             tc::mma_commit(bar0);
         }
         __syncwarp();
-        GDR_TRACE_PREP(6);
 
         // ---- W, U out of TMEM into their blobs: row i = 16 q + lane (lane < 16);
         //      8 warps: columns [64 hf, 64 hf + 64) of W and of U, 16 warps: columns
@@ -855,12 +788,9 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
                 tc::bulk_wait_read();  // the staging area is reused by the next item
             }
         }
-        GDR_TRACE_PREP(7);
         tc::fence_before();
         __syncthreads();
         tc::fence_after();
-        GDR_TRACE_PREP(8);
-        GDR_TRACE_ITEM(item, 1);
     }  // item loop
     if (tid == 0) tc::bulk_wait_all();
     if (warp == 0) tc::tmem_dealloc(tmem, 256);
@@ -988,7 +918,6 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             for (int c = 0; c < nc && !*abort_flag; ++c) {
                 const int s = c & 1;
                 if (c >= 2 && !tc::mbar_wait(bar(kEmpty0 + s), ((c >> 1) - 1) & 1, abort_flag)) { fail(); break; }
-                GDR_TRACE_POINT(0, c);
                 const size_t gc = (size_t)c0 + c;
                 const uint32_t st = base + s * S::kStage;
                 const uint32_t fb = bar(kFull0 + s);
@@ -1008,7 +937,6 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                     else tc::prefetch_l2(p.Kb + (g2 * p.Hk + kh) * kTile64x128, kTile64x128);
                     tc::prefetch_l2(p.Rb + (g2 * p.Hv + h) * kRec, kRec);
                 }
-                GDR_TRACE_POINT(1, c);
             }
             // drain: wait for the copies of the last (up to) two stages to land
             for (int c = (nc > 2 ? nc - 2 : 0); c < nc; ++c)
@@ -1071,7 +999,6 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             const unsigned char* stg = sm + s * S::kStage;
             const uint32_t st = base + s * S::kStage;
             if (!tc::mbar_wait(bar(kFull0 + s), (c >> 1) & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
-            if (lead) GDR_TRACE_POINT(21, c);
             // S^T rows (hi, lo) into the MMA operand tiles.  Their readers (the N
             // products of chunk c - 1) finished before the last state update.
 #pragma unroll
@@ -1083,11 +1010,9 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                 *reinterpret_cast<uint4*>(sSh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                 *reinterpret_cast<uint4*>(sSl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
-            if (lead) GDR_TRACE_POINT(19, c);
             tc::fence_proxy_async();
             tc::fence_before();
             tc::bar_sync(1, 256);
-            if (lead) GDR_TRACE_POINT(8, c);
             if (isA) {
                 // the output rows of D1[ob] were drained (chunk c - 2) before reuse
                 if (c >= 2 && !tc::mbar_wait(bar(kOFree0 + ob), ((c >> 1) - 1) & 1, abort_flag)) fail();
@@ -1095,7 +1020,6 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                 tc::mma_ksteps<8>(tD1 + 64 * ob, dk128(st + S::kXW), a128, dmn64(base + S::kSh, D * BV * 2), 64, idA, true);
                 tc::mma_commit(bar(kD1Full));
                 issued = true;
-                GDR_TRACE_POINT(4, c);
             } else if (isB) {
                 // rows 64..127 of the second column block are not part of the blob;
                 // the accumulator rows they reach are not read
@@ -1117,7 +1041,6 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             }
             // N = U - W S^T  ->  N' = rowf * N (hi, lo), N (bf16, masked)
             if (!tc::mbar_wait(bar(kD1Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
-            if (lead) GDR_TRACE_POINT(9, c);
             tc::fence_after();
             float ws[16];  // (W S^T) for this thread's row and 16 columns
             if (nrow) {  // quadrants 0 and 1 (warp-uniform)
@@ -1127,7 +1050,6 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
 #pragma unroll
                 for (int v = 0; v < 16; ++v) ws[v] = dv[v] + dv[16 + v] + dv[32 + v];
             }
-            if (lead) GDR_TRACE_POINT(15, c);
             // the N tile was last read by the output product of chunk c - kNBuf
             if (S::kNBuf == 2) {
                 if (c >= 2 && !tc::mbar_wait(bar(kOFull0 + ob), ((c - 2) >> 1) & 1, abort_flag)) fail();
@@ -1135,7 +1057,6 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                 if (c >= 1 && !tc::mbar_wait(bar(kOFull0 + ((c - 1) & 1)), ((c - 1) >> 1) & 1, abort_flag)) fail();
             }
             const uint32_t nbuf = (uint32_t)(ob % S::kNBuf) * (C * BV * 2);
-            if (lead) GDR_TRACE_POINT(16, c);
             if (nrow) {
                 const float keep = i < Lc ? 1.f : 0.f;  // rows past the chunk end
 #pragma unroll
@@ -1155,11 +1076,9 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                     *reinterpret_cast<uint4*>(sm + S::kN + nbuf + off) = make_uint4(nw[0], nw[1], nw[2], nw[3]);
                 }
             }
-            if (lead) GDR_TRACE_POINT(17, c);
             tc::fence_proxy_async();
             tc::fence_before();
             tc::bar_sync(1, 256);
-            if (lead) GDR_TRACE_POINT(10, c);
             if (isA) {
                 tc::fence_after();
                 tc::mma_ksteps<4>(tD2, dmn128(st + S::kKt), amn, dmn64(base + S::kNh, C * BV * 2), 64, id2w, true);
@@ -1167,7 +1086,6 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                     tc::mma_ksteps<4>(tD2, dmn128(st + S::kKt + kTile64x128), amn, dmn64(base + S::kNh, 512), 64, id2n, false);
                 tc::mma_commit(bar(kD2Full));
                 tc::mma_commit(bar(kEmpty0 + s));
-                GDR_TRACE_POINT(6, c);
             } else if (isC) {
                 if (!outputs) {  // segment summary: no output, so no P N product
                     tc::mbar_arrive(bar(kOFull0 + ob));
@@ -1183,7 +1101,6 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             }
             // S^T <- colf * S^T + dS^T  (hi and lo halves of the accumulator summed)
             if (!tc::mbar_wait(bar(kD2Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
-            if (lead) GDR_TRACE_POINT(11, c);
             tc::fence_after();
             {
                 float dv[48];
@@ -1191,7 +1108,6 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
 #pragma unroll
                 for (int v = 0; v < 16; ++v) Sreg[v] = fmaf(colf, Sreg[v], dv[v] + dv[16 + v]);
             }
-            if (lead) GDR_TRACE_POINT(12, c);
             tc::fence_before();
         }
         if (issued) {  // every MMA this thread issued finished before the CTA leaves
@@ -1219,7 +1135,6 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
         for (int c = 0; c < nc; ++c) {
             const int ob = c & 1;
             if (!tc::mbar_wait(bar(kOFull0 + ob), (c >> 1) & 1, abort_flag)) fail();
-            if (tid == 384) GDR_TRACE_POINT(13, c);
             tc::fence_after();
             if (drain && outputs) {
                 float ov[BV], ld[2 * BV];
@@ -1240,7 +1155,6 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             tc::fence_before();
             tc::bar_sync(2, 128);
             if (tid == 384) {
-                GDR_TRACE_POINT(14, c);
                 tc::mbar_arrive(bar(kOFree0 + ob));
             }
         }

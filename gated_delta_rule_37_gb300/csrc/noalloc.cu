@@ -12,10 +12,13 @@
 // The scratch array is a file-scope __device__ array of kStaticWorkspaceBytes.
 // Every GPU that loads this library holds it until the process exits.  In host
 // code its name is only a host-side stand-in, so its device address is looked
-// up with cudaGetSymbolAddress once per device (with that device current) the
-// first time the entry point runs on that device, and cached.
+// up with cudaGetSymbolAddress on every call, in the context current on the
+// calling thread.  The address belongs to that context, not to the device
+// index: after cudaDeviceReset, or with another context current on the same
+// device, the array lives at a new address, and a cached pointer would send
+// the kernels to memory that is no longer mapped.  The lookup is a host-side
+// table read once the library's device code is loaded in the context.
 #include <cstdio>
-#include <mutex>
 
 #include "gdr.h"
 #include "launch.h"
@@ -24,31 +27,17 @@ namespace gdr {
 namespace {
 
 constexpr size_t kStaticWorkspaceBytes = (size_t)GDR_NOALLOC_WORKSPACE_BYTES;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_static_workspace[kStaticWorkspaceBytes];
 
-std::mutex g_ws_mu;
-void* g_ws_addr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (set-up on the
-// first call per device).
+// Device address of the scratch array in the current context.
 int static_workspace(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return set_last_error(GDR_ERR_LAUNCH, "cudaGetDevice: %s", cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxDevices)
-        return set_last_error(GDR_ERR_UNSUPPORTED, "device index %d above %d", dev, kMaxDevices - 1);
-    std::lock_guard<std::mutex> lk(g_ws_mu);
-    if (!g_ws_addr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_static_workspace);
-        if (e != cudaSuccess || p == nullptr)
-            return set_last_error(GDR_ERR_LAUNCH, "cudaGetSymbolAddress of the static workspace failed: %s",
-                                  cudaGetErrorString(e));
-        g_ws_addr[dev] = p;
-    }
-    *out = g_ws_addr[dev];
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_workspace);
+    if (e != cudaSuccess || p == nullptr)
+        return set_last_error(GDR_ERR_LAUNCH, "cudaGetSymbolAddress of the static workspace failed: %s",
+                              cudaGetErrorString(e));
+    *out = p;
     return GDR_OK;
 }
 

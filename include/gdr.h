@@ -73,7 +73,11 @@ typedef enum gdr_gate_kind {
 #define GDR_QK_L2NORM  0x1 /* normalise q and k rows in-library: x * rsqrt(sum x^2 + 1e-6) */
 #define GDR_NEG_EIGVAL 0x2 /* gdr_gating_fwd: beta = 2 * sigmoid(b)                         */
 #define GDR_COMMIT     0x4 /* gdr_recurrent_fwd: write the final state back to the pool     */
-#define GDR_VALIDATE   0x8 /* check input contents on the device first (synchronises)       */
+#define GDR_VALIDATE   0x8 /* check input contents on the device first (synchronises).
+                              * The findings land in one library-wide device word:
+                              * validated calls from different host threads must be
+                              * serialised by the caller, or one call's reset of the
+                              * word can hide the other's findings.                  */
 #define GDR_CHANNEL_GATE 0x10 /* gdr_recurrent_fwd: g is per key channel, [T_total, Hv, K]  */
 #define GDR_CHUNK_SCAN 0x20   /* gdr_chunk_fwd: chunk-parallel state scan (long sequences)     */
 
@@ -150,9 +154,11 @@ GDR_API int gdr_chunk_fwd(const void* q, const void* k, const void* v, const flo
  *   the library; every GPU that loads the library holds it until exit.  A
  *   problem whose gdr_chunk_workspace_size exceeds it is rejected with
  *   GDR_ERR_WORKSPACE before anything runs.
- *   The first call on each device looks up the array's device address (with
- *   that device current) and caches it: make that first call before any
- *   stream capture.
+ *   Every call looks up the array's device address in the context current on
+ *   the calling thread (the address belongs to the context, so it stays right
+ *   after cudaDeviceReset or with another context current on the device).
+ *   The first call in a context may load the library's device code there:
+ *   make it before any stream capture.
  *   Nothing is allocated or freed, by the library or any routine it calls.
  *   All calls share the one array and it keeps the previous call's contents
  *   (nothing in it has to start at zero): calls whose work overlaps on the

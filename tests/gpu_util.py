@@ -39,10 +39,16 @@ def check_out(got: torch.Tensor, ref, what: str):
 
 
 def check_state(got: torch.Tensor, ref, what: str):
+    """fp32 states: rel-L2 <= 1e-4.  bf16 states (pools, per-token states):
+    rel-L2 <= 5e-3 and max-abs <= 3e-2, the bounds of every bf16 result."""
     g = got.detach().float().cpu().numpy()
     e = rel_l2(g, ref)
-    bound = F32_REL if got.dtype == torch.float32 else BF16_REL
-    assert e <= bound, f"{what}: rel-L2 {e:.3e} > {bound}"
+    assert np.isfinite(g).all(), f"{what}: non-finite values"
+    if got.dtype == torch.float32:
+        assert e <= F32_REL, f"{what}: rel-L2 {e:.3e} > {F32_REL}"
+    else:
+        m = max_abs(g, ref)
+        assert e <= BF16_REL and m <= BF16_ABS, f"{what}: rel-L2 {e:.3e} max-abs {m:.3e}"
     return e
 
 

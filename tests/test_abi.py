@@ -207,3 +207,30 @@ def test_noalloc_rejects_oversized_problem_before_touching_the_device(lib):
                                    16, 32, 128, 128, 0.1, 0, 0, P(112), None, None)
     assert rc == 3
     assert "static scratch" in lib.gdr_last_error().decode()
+
+
+def test_noalloc_limit_matches_header_and_rejects_exactly_above_it(lib):
+    """The binding's NOALLOC_WORKSPACE_BYTES is the header's
+    GDR_NOALLOC_WORKSPACE_BYTES, and the size check rejects a problem exactly
+    when its workspace exceeds it (host-side: the call that fits goes on and
+    fails later only for want of a device here)."""
+    src = open(os.path.join(ROOT, "include", "gdr.h")).read()
+    m = re.search(r"#define\s+GDR_NOALLOC_WORKSPACE_BYTES\s+\((\d+)ull\s*<<\s*(\d+)\)", src)
+    assert m, "GDR_NOALLOC_WORKSPACE_BYTES not found in gdr.h"
+    assert int(m.group(1)) << int(m.group(2)) == gdr.NOALLOC_WORKSPACE_BYTES
+
+    def need(T):
+        return gdr.chunk_workspace_size(1, T, 4, 4, 128, 128, gate_kind=0, dtype=0)
+    T = 64
+    while need(T + 64) <= gdr.NOALLOC_WORKSPACE_BYTES:
+        T += 64
+    P = ctypes.c_void_p
+
+    def call(T):
+        return lib.gdr_chunk_fwd_noalloc(P(16), P(32), P(48), P(64), None, P(80), None, P(96), 1, T,
+                                         4, 4, 128, 128, 0.1, 0, 0, P(112), None, None)
+    assert need(T) <= gdr.NOALLOC_WORKSPACE_BYTES < need(T + 64)
+    assert call(T + 64) == 3 and "static scratch" in lib.gdr_last_error().decode()
+    import torch
+    if not torch.cuda.is_available():
+        assert call(T) != 3

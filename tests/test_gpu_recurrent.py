@@ -198,6 +198,60 @@ def test_gated_small_cases(neg_eigval, dtype, pool_dtype):
     check_case(_with_oracle_gates(case, neg_eigval), pool, o, ib, o_init, commit=True)
 
 
+def _unnormalised(case, seed):
+    """The case with each q / k row rescaled by a random factor in [0.25, 4]
+    (rounded to the input dtype): inputs for the in-kernel normalisation."""
+    gen = torch.Generator().manual_seed(seed)
+    out = []
+    for x in (case.q, case.k):
+        f = torch.exp(torch.empty(x.shape[:2] + (1,)).uniform_(-1.386, 1.386, generator=gen))
+        out.append((x.float() * f).to(x.dtype))
+    return out
+
+
+def _with_oracle_l2norm(case):
+    """The case with q and k normalised by the oracle (x / sqrt(sum x^2 + 1e-6), fp64)."""
+    import dataclasses
+    return dataclasses.replace(case, q=torch.from_numpy(oracle.l2norm(case.q, 1e-6)),
+                               k=torch.from_numpy(oracle.l2norm(case.k, 1e-6)))
+
+
+@pytest.mark.parametrize("pool_dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_gated_with_qk_l2norm_ragged(dtype, pool_dtype):
+    """The in-kernel gating and the in-kernel q / k normalisation in one verify
+    launch (FlashQLA's in-kernel gating commit forms both inside the kernel):
+    ragged 1..40-token sequences (windows of every fill, one empty sequence),
+    padding rows, per-token states, the pool committed."""
+    lens = torch.randint(1, 41, (9,), generator=torch.Generator().manual_seed(91)).tolist() + [0]
+    case = workloads.pool_case(92, lens, 2, 4, 128, 128, 12, dtype=dtype, pool_dtype=pool_dtype, pad_count=2,
+                               commit=True, steps=40, ibuf_rows=10)
+    case.raw = workloads.raw_gates(93, case.T, 4, dtype=dtype)
+    case.q, case.k = _unnormalised(case, 94)
+    pool, o, ib, o_init = run_case(case, flags=gdr.GDR_COMMIT | gdr.GDR_QK_L2NORM, with_ibuf=True, gated=True)
+    check_case(_with_oracle_l2norm(_with_oracle_gates(case)), pool, o, ib, o_init, commit=True)
+
+
+def test_gated_with_qk_l2norm_decode():
+    """Gating and normalisation in the kernel on single-token calls (inputs
+    read straight from global memory), fp32 pool committed, padding rows."""
+    case = workloads.pool_case(95, [1] * 24, 2, 4, 128, 128, 30, pool_dtype=torch.float32, pad_count=3,
+                               commit=True)
+    case.raw = workloads.raw_gates(96, case.T, 4)
+    case.q, case.k = _unnormalised(case, 97)
+    pool, o, ib, o_init = run_case(case, flags=gdr.GDR_COMMIT | gdr.GDR_QK_L2NORM, with_ibuf=False, gated=True)
+    check_case(_with_oracle_l2norm(_with_oracle_gates(case)), pool, o, ib, o_init, commit=True)
+
+
+def test_gated_with_qk_l2norm_verify_full_size():
+    """The raw-gate verify workload (64 sequences of 1..12 tokens, bf16 pool,
+    per-token states) with un-normalised q / k normalised in the kernel."""
+    case = workloads.verify_bf16_pool_raw_gates()
+    case.q, case.k = _unnormalised(case, 98)
+    pool, o, ib, o_init = run_case(case, flags=gdr.GDR_QK_L2NORM, with_ibuf=True, gated=True)
+    check_case(_with_oracle_l2norm(_with_oracle_gates(case)), pool, o, ib, o_init, commit=False)
+
+
 @pytest.mark.parametrize("Hk,Hv", [(4, 4), (2, 8), (1, 4)])       # MHA, GVA 4, MQA
 @pytest.mark.parametrize("K", [64, 128])
 @pytest.mark.parametrize("dtype,pool_dtype", [(torch.bfloat16, torch.float32), (torch.float32, torch.float32),
