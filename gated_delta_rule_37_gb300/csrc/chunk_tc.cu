@@ -797,6 +797,573 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
 }
 
 // ---------------------------------------------------------------------------
+// prep kernel with per-key-channel gates (KDA): 256 threads, two CTAs per SM
+// ---------------------------------------------------------------------------
+// The same outputs as the scalar-gate prep (W_hi / Qd, W_lo / P, U, the decayed
+// keys Kd as hi / lo, the decay record), for gates gk [T, Hv, K].
+//   * The in-chunk cumsum is kept in log2 units, Gam2 = log2(e) Gam, so every
+//     decay factor is one ex2 of a difference that is <= 0.
+//   * Thread (t0 = tid / 8, g = tid % 8) owns tokens t0 and t0 + 32 and, of
+//     each, the 16-byte operand chunks g and g + 8 (channels 8g .. 8g + 7 and
+//     64 + 8g .. 64 + 8g + 7).  It holds their Gam2 in registers for the whole
+//     item; only the rows of the pivots (tokens 4, 8, ..., 60) and of the last
+//     token stay in shared memory.
+//   * A_ij = beta_i sum_c k_i[c] k_j[c] e^{Gam_i[c] - Gam_j[c]} (j < i) and
+//     P_ij = sum_c q_i[c] k_j[c] e^{Gam_i[c] - Gam_j[c]} (j <= i).  Pairs in
+//     different halves of a block of 2h tokens (h = 32, 16, 8, 4) go through
+//     the tensor cores around the pivot p = first token of the upper half:
+//     e^{Gam_i - Gam_j} = e^{Gam_i - Gam_p} e^{Gam_p - Gam_j}, both factors <= 1,
+//     folded into the left (k_i, q_i) and right (k_j) operands.  A takes three
+//     split products (K_l hi x R hi, K_l hi x R lo, K_l lo x R hi; fp32
+//     accuracy for the solve), P two (Q_l hi x R hi + Q_l hi x R lo: P is
+//     stored in bf16 and only feeds the output).  Each level's accumulators
+//     alternate between two TMEM column sets, so the read-out of one level
+//     runs while the next level's products are in flight.  Pairs inside a
+//     4-token block are formed on the CUDA cores, one warp per block.
+//   * W = Tm diag(beta) (K o e^{Gam}) with a 3-term split, U = Tm diag(beta) V
+//     with a 2-term split, as for the scalar gate.
+// Shared memory stays under 113 KB, so two CTAs share an SM and one CTA's
+// waits (tensor-core round trips, barriers) are filled by the other's work.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// The two bf16 of a packed word as fp32 (element 0 in the low half).
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+// a - b on the fp32x2 pipe
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __ffma2_rn(b, make_float2(-1.f, -1.f), a); }
+// x = hi + lo with hi = bf16(x), lo = bf16(x - hi), two values at once
+__device__ __forceinline__ void split2x(float2 x, uint32_t& hi, uint32_t& lo) {
+    hi = tc::pack_bf16(x.x, x.y);
+    const float2 l = sub2(x, unpack_bf16x2(hi));
+    lo = tc::pack_bf16(l.x, l.y);
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kKdaThreads = 256;
+
+struct KdaSmem {
+    static constexpr uint32_t kX = 0;                         // [K ; Q] 128 x 128 bf16 (32 KB)
+    static constexpr uint32_t kOps = 2 * kTile64x128;         // 40 KB work region
+    static constexpr uint32_t kLh = kOps;                     // [K_l hi ; Q_l hi] 64 x 128 (16 KB)
+    static constexpr uint32_t kLl = kLh + kTile64x128;        // K_l lo 32 x 128 (8 KB)
+    static constexpr uint32_t kRh = kLl + kTile64x128 / 2;    // R hi 32 x 128
+    static constexpr uint32_t kRl = kRh + kTile64x128 / 2;    // R lo 32 x 128
+    static constexpr uint32_t kOpsEnd = kRl + kTile64x128 / 2;
+    static constexpr uint32_t kGt = kOps;                     // fp32 [64][128] Gam2 scratch (cumsum, 4-token pairs)
+    static constexpr uint32_t kTm = kOps;                     // fp32 [64][65] after the A / P products
+    static constexpr uint32_t kZ = kTm + C * LDA * 4;         // fp32 [1024]
+    static constexpr uint32_t kV = kOps + 24576;              // V 64 x 128 (16 KB), loaded after the products
+    static constexpr uint32_t kA = kOpsEnd;                   // fp32 [64][65]
+    static constexpr uint32_t kT2h = kA, kT2l = kA + kTile64x64;  // T'' hi / lo over A after the solve
+    static constexpr uint32_t kP = (kA + C * LDA * 4 + 1023) & ~1023u;  // P bf16 64 x 64 (8 KB)
+    static constexpr uint32_t kPiv = kP + kTile64x64;         // fp32 [16][128]: Gam2 of tokens 4, 8, .., 60 and L - 1
+    static constexpr uint32_t kBeta = kPiv + 16 * D * 4;
+    static constexpr uint32_t kBar = kBeta + C * 4;
+    static constexpr uint32_t kTotal = kBar + 64 + 1024;      // + alignment slack
+    static_assert(kGt + C * D * 4 <= kOpsEnd, "Gam2 scratch beyond the work region");
+    static_assert(kZ + 4096 <= kV, "Z overlaps V");
+    static_assert(kV + kTile64x128 == kOpsEnd, "V at the end of the work region");
+    static_assert(kT2l + kTile64x64 <= kA + C * LDA * 4, "T'' beyond A");
+    static_assert(kTotal <= 113 * 1024, "two CTAs per SM");
+};
+
+__global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams p) {
+    using S = KdaSmem;
+    constexpr int NT = kKdaThreads;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = tid >> 3, g = tid & 7;  // tokens t0, t0 + 32; operand chunks g, g + 8
+    const int grp = p.Hv / p.Hk;
+    const __nv_bfloat16* qp = static_cast<const __nv_bfloat16*>(p.q);
+    const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(p.k);
+    const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(p.v);
+    const __nv_bfloat16* bp = static_cast<const __nv_bfloat16*>(p.beta);
+
+    float* As = reinterpret_cast<float*>(sm + S::kA);
+    float* Tm = reinterpret_cast<float*>(sm + S::kTm);
+    float* Z = reinterpret_cast<float*>(sm + S::kZ);
+    float* gt = reinterpret_cast<float*>(sm + S::kGt);
+    float* piv = reinterpret_cast<float*>(sm + S::kPiv);
+    float* bet = reinterpret_cast<float*>(sm + S::kBeta);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::kBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::kBar + 24);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::kBar + 32);
+    const uint32_t barL[2] = {tc::smem_u32(&bars[0]), tc::smem_u32(&bars[1])};
+    const uint32_t barW = tc::smem_u32(&bars[2]);
+
+    if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), 256);
+    if (tid == 0) {
+        tc::mbar_init(barL[0], 3);
+        tc::mbar_init(barL[1], 3);
+        tc::mbar_init(barW, 1);
+        *abort_flag = 0;
+        tc::mbar_fence_init();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = *tmem_slot;
+    uint32_t phW = 0;
+    tc::grid_dep_wait();    // the chunk table comes from the metadata kernel
+    tc::grid_dep_launch();  // the chain kernel may start its prologue on free SMs
+    const int nitems = p.meta[0] * p.Hv;
+    const uint32_t sX = tc::smem_u32(sm + S::kX);
+
+    for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+        const int chunk = item / p.Hv, h = item - chunk * p.Hv;
+        const int4 info = p.table[chunk];
+        const int start = info.y, L = info.z;
+        const int kh = h / grp;
+
+        // ---- stage K, Q rows and the gate rows (cp.async); zero A and P; beta; warm L2
+        //      for the next item ----------------------------------------------------------
+        stage_rows_async<NT>(sm + S::kX, 2 * C, 0, kp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
+        stage_rows_async<NT>(sm + S::kX, 2 * C, C, qp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
+        {
+            // gk rows [64][128] fp32 into the scratch (rows >= L zero-filled)
+            const float* src = p.gk + ((size_t)start * p.Hv + h) * D;
+            for (int e = tid; e < C * (D / 4); e += NT) {
+                const int row = e >> 5, pc = e & 31;
+                const float* gsrc = src + (size_t)(row < L ? row : 0) * p.Hv * D + 4 * pc;
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
+                             :: "r"(tc::smem_u32(gt + row * D + 4 * pc)), "l"(gsrc), "r"(row < L ? 16 : 0) : "memory");
+            }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        {
+            const int nxt = item + (int)gridDim.x;
+            if (nxt < nitems) {
+                const int nc = nxt / p.Hv, nh = nxt - nc * p.Hv;
+                const int4 ni = p.table[nc];
+                const int r = tid & 63, which = tid >> 6;
+                const size_t tok = (size_t)ni.y + r;
+                if (r < ni.z) {
+                    if (which == 0) tc::prefetch_l2(kp + (tok * p.Hk + nh / grp) * D, D * 2);
+                    else if (which == 1) tc::prefetch_l2(qp + (tok * p.Hk + nh / grp) * D, D * 2);
+                    else if (which == 2) tc::prefetch_l2(vp + (tok * p.Hv + nh) * D, D * 2);
+                    else tc::prefetch_l2(p.gk + (tok * p.Hv + nh) * D, D * 4);
+                }
+                if (tid == 0) tc::prefetch_l2_span(bp + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 2);
+            }
+        }
+        for (int e = tid; e < (int)(C * LDA); e += NT) As[e] = 0.f;
+        for (int e = tid; e < (int)(kTile64x64 / 16); e += NT)
+            reinterpret_cast<uint4*>(sm + S::kP)[e] = make_uint4(0u, 0u, 0u, 0u);
+        if (tid < C) bet[tid] = tid < L ? to_f(bp[((size_t)start + tid) * p.Hv + h]) : 0.f;
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        __syncthreads();
+
+        // ---- per-channel cumsum in place, log2 units: thread (channel c, half hf) scans
+        //      32 tokens ----------------------------------------------------------------
+        {
+            const int c = tid & (D - 1), hf = tid >> 7;
+            float x[32];
+#pragma unroll
+            for (int u = 0; u < 32; ++u) x[u] = gt[(32 * hf + u) * D + c];
+#pragma unroll
+            for (int u = 1; u < 32; ++u) x[u] += x[u - 1];
+            if (hf == 0) piv[c] = x[31];  // the first half's total, read by the second half
+            __syncthreads();
+            const float off = hf ? piv[c] : 0.f;
+#pragma unroll
+            for (int u = 0; u < 32; ++u) gt[(32 * hf + u) * D + c] = (x[u] + off) * kLog2e;
+        }
+        __syncthreads();
+        // pivot rows (tokens 4, 8, .., 60) and the last token's row; this thread's Gam2
+        for (int e = tid; e < 16 * D; e += NT) {
+            const int r = e >> 7, tok = r < 15 ? 4 * (r + 1) : L - 1;
+            piv[e] = gt[tok * D + (e & (D - 1))];
+        }
+        float G[2][16];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const float* src = gt + (t0 + 32 * u) * D + 8 * (g + 8 * cc);
+                const float4 a = *reinterpret_cast<const float4*>(src), b = *reinterpret_cast<const float4*>(src + 4);
+                G[u][8 * cc + 0] = a.x; G[u][8 * cc + 1] = a.y; G[u][8 * cc + 2] = a.z; G[u][8 * cc + 3] = a.w;
+                G[u][8 * cc + 4] = b.x; G[u][8 * cc + 5] = b.y; G[u][8 * cc + 6] = b.z; G[u][8 * cc + 7] = b.w;
+            }
+        __syncthreads();
+
+        // ---- Qd = Q o e^{Gam} and Kd = K o e^{Gam_L - Gam} (hi / lo) straight to their blobs ----
+        {
+            unsigned char* Qdst = p.Xw + ((size_t)chunk * p.Hv + h) * kXwBytes;
+            unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hv + h) * 2 * kTile64x128;
+            const float* gL = piv + 15 * D;
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int t = t0 + 32 * u, ch = g + 8 * cc;
+                    const uint4 qr = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(C + t, ch, 2 * C));
+                    const uint4 kr = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(t, ch, 2 * C));
+                    const __nv_bfloat16* qv = reinterpret_cast<const __nv_bfloat16*>(&qr);
+                    const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&kr);
+                    float l8[8];
+                    ld8(gL + 8 * ch, l8);
+                    uint32_t qw[4], hw[4], lw[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float* gg = &G[u][8 * cc + 2 * e];
+                        qw[e] = tc::pack_bf16(__bfloat162float(qv[2 * e]) * ex2(gg[0]),
+                                              __bfloat162float(qv[2 * e + 1]) * ex2(gg[1]));
+                        tc::split2(__bfloat162float(kv[2 * e]) * ex2(l8[2 * e] - gg[0]),
+                                   __bfloat162float(kv[2 * e + 1]) * ex2(l8[2 * e + 1] - gg[1]), hw[e], lw[e]);
+                    }
+                    *reinterpret_cast<uint4*>(Qdst + tc::chunk_k128(C + t, ch, 2 * C)) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+                    const uint32_t off = tc::chunk_k128(t, ch, C);
+                    *reinterpret_cast<uint4*>(Kdst + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4*>(Kdst + kTile64x128 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                }
+            float* rec = reinterpret_cast<float*>(p.Rb + ((size_t)chunk * p.Hv + h) * kRec);
+            if (tid < C) rec[tid] = tid < L ? 1.f : 0.f;
+            if (tid < D) rec[64 + tid] = ex2(gL[tid]);
+            if (tid == 0) reinterpret_cast<int*>(rec)[192] = L;
+        }
+
+        // ---- A and P across the halves of 2h-token blocks (h = 32, 16, 8, 4) on tcgen05 ----
+        constexpr uint32_t idL = tc::idesc_bf16(64, 32, false, false);
+        // build level lev's operands: this thread's tokens are left (upper half) or
+        // right (lower half) of their block; the 4 tokens of a warp always agree
+        auto build = [&](int lev) {
+            const int sh = 5 - lev, hh = 1 << sh;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int t = t0 + 32 * u;
+                const int B = t >> (sh + 1), up = (t >> sh) & 1, pv = (2 * B + 1) << sh;
+                const int idx = (B << sh) + (t & (hh - 1));
+                const float* gp = piv + ((pv >> 2) - 1) * D;
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int ch = g + 8 * cc;
+                    float p8[8];
+                    ld8(gp + 8 * ch, p8);
+                    float2 f[4];
+                    if (up) {  // e^{Gam_t - Gam_p}, t >= p
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 d = sub2(make_float2(G[u][8 * cc + 2 * e], G[u][8 * cc + 2 * e + 1]),
+                                                  make_float2(p8[2 * e], p8[2 * e + 1]));
+                            f[e] = make_float2(ex2(d.x), ex2(d.y));
+                        }
+                    } else {  // e^{Gam_p - Gam_t}, t < p
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 d = sub2(make_float2(p8[2 * e], p8[2 * e + 1]),
+                                                  make_float2(G[u][8 * cc + 2 * e], G[u][8 * cc + 2 * e + 1]));
+                            f[e] = make_float2(ex2(d.x), ex2(d.y));
+                        }
+                    }
+                    const uint4 kr = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(t, ch, 2 * C));
+                    const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w};
+                    uint32_t hw[4], lw[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) split2x(__fmul2_rn(unpack_bf16x2(kw[e]), f[e]), hw[e], lw[e]);
+                    if (up) {
+                        *reinterpret_cast<uint4*>(sm + S::kLh + tc::chunk_k128(idx, ch, C)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4*>(sm + S::kLl + tc::chunk_k128(idx, ch, 32)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                        const uint4 qr = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(C + t, ch, 2 * C));
+                        const uint32_t qw4[4] = {qr.x, qr.y, qr.z, qr.w};
+                        uint32_t qw[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 x = __fmul2_rn(unpack_bf16x2(qw4[e]), f[e]);
+                            qw[e] = tc::pack_bf16(x.x, x.y);
+                        }
+                        *reinterpret_cast<uint4*>(sm + S::kLh + tc::chunk_k128(32 + idx, ch, C)) = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+                    } else {
+                        const uint32_t off = tc::chunk_k128(idx, ch, 32);
+                        *reinterpret_cast<uint4*>(sm + S::kRh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4*>(sm + S::kRl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    }
+                }
+            }
+            tc::fence_proxy_async();
+            tc::fence_before();
+            __syncthreads();
+            tc::fence_after();
+        };
+        // three issuers, one split product each, into columns 96 (lev % 2) + 32 w.
+        // K_l lo is a 32-row tile: the M = 64 product also reads the 32 rows after
+        // it (real memory), which land in accumulator rows that are not read.
+        auto issue = [&](int lev) {
+            if (warp < 3 && lane == 0) {
+                const uint32_t la = tc::smem_u32(sm + (warp == 2 ? S::kLl : S::kLh));
+                const uint32_t astr = warp == 2 ? 32 * 128 : C * 128;
+                const uint32_t rb = tc::smem_u32(sm + (warp == 1 ? S::kRl : S::kRh));
+                const uint32_t d = tmem + 96 * (lev & 1) + 32 * warp;
+                for (int ks = 0; ks < 8; ++ks)
+                    tc::mma_bf16(d, tc::smem_desc(la + (ks >> 2) * astr + (ks & 3) * 32, 16, 1024, tc::kSwizzle128),
+                                 tc::smem_desc(rb + (ks >> 2) * (32 * 128) + (ks & 3) * 32, 16, 1024, tc::kSwizzle128),
+                                 idL, ks > 0);
+                tc::mma_commit(barL[lev & 1]);
+            }
+            __syncwarp();
+        };
+        // level lev's accumulator: row r = 16 (w % 4) + lane (lane < 16), rows 0..31 A
+        // (left token keys), 32..63 P (left token queries); warps w and w + 4 take
+        // the right columns n < 16 and n >= 16.  Column n pairs with row r when both
+        // fall in the same block of 2h tokens.
+        auto wait_level = [&](int lev) {
+            if (!tc::mbar_wait(barL[lev & 1], (lev >> 1) & 1, abort_flag)) raise_error(p, 1u);
+            tc::fence_after();
+        };
+        auto readout = [&](int lev) {
+            const int sh = 5 - lev, hh = 1 << sh;
+            const int q = warp & 3, nh = warp >> 2;
+            // below h = 32 a warp's rows (one half of the left tokens) pair only
+            // with the right columns of one half: the other warp of the quadrant
+            // has nothing to read
+            if (hh < 32 && (q & 1) != nh) return;
+            const uint32_t a = tmem + ((uint32_t)(32 * q) << 16) + 96 * (lev & 1) + 16 * nh;
+            float d[48];
+            tc::tmem_ld16x3(a, a + 32, a + 64, d);
+            const int r = 16 * q + lane, idx = r & 31, B = idx >> sh;
+            const int i = (2 * B + 1) * hh + (idx & (hh - 1));
+            if (lane < 16) {
+                if (q < 2) {
+                    const float bi = bet[i];
+#pragma unroll
+                    for (int n2 = 0; n2 < 16; ++n2) {
+                        const int n = 16 * nh + n2;
+                        if ((n >> sh) == B) As[i * LDA + 2 * hh * B + (n & (hh - 1))] = bi * (d[n2] + d[16 + n2] + d[32 + n2]);
+                    }
+                } else {
+#pragma unroll
+                    for (int n2 = 0; n2 < 16; ++n2) {
+                        const int n = 16 * nh + n2;
+                        if ((n >> sh) == B)
+                            *reinterpret_cast<__nv_bfloat16*>(sm + S::kP + tc::off_k128(i, 2 * hh * B + (n & (hh - 1)), C)) =
+                                __float2bfloat16_rn(d[n2] + d[16 + n2]);
+                    }
+                }
+            }
+        };
+        build(0);
+        issue(0);
+        wait_level(0);
+        build(1);
+        issue(1);
+        readout(0);
+        wait_level(1);
+        build(2);
+        issue(2);
+        readout(1);
+        wait_level(2);
+        build(3);
+        issue(3);
+        readout(2);
+        wait_level(3);
+        readout(3);
+
+        // ---- pairs inside a 4-token block: warp w has the blocks at tokens 4w and
+        //      4w + 32.  Lane (u, o): block u, channels 8o .. 8o + 7; it forms the 6
+        //      pairs i > j (A and P) and the 4 diagonal P entries over its 8 channels,
+        //      and the 16 partial sums are reduced over the 16 lanes of the block
+        //      (transposed, so lane o ends with sum o). --------------------------------
+        {
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    float* dst = gt + (t0 + 32 * u) * D + 8 * (g + 8 * cc);
+                    *reinterpret_cast<float4*>(dst) = make_float4(G[u][8 * cc], G[u][8 * cc + 1], G[u][8 * cc + 2], G[u][8 * cc + 3]);
+                    *reinterpret_cast<float4*>(dst + 4) = make_float4(G[u][8 * cc + 4], G[u][8 * cc + 5], G[u][8 * cc + 6], G[u][8 * cc + 7]);
+                }
+            __syncwarp();
+            const int o = lane & 15, tb = 4 * warp + 32 * (lane >> 4);
+            float v[16];
+            {
+                uint4 kr[4], qr[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    kr[a] = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(tb + a, o, 2 * C));
+                    qr[a] = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(C + tb + a, o, 2 * C));
+                }
+                // diagonal: P_aa = q_a . k_a
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&kr[a]);
+                    const __nv_bfloat16* qv = reinterpret_cast<const __nv_bfloat16*>(&qr[a]);
+                    float acc = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc = fmaf(__bfloat162float(qv[e]), __bfloat162float(kv[e]), acc);
+                    v[12 + a] = acc;
+                }
+                // pairs (1,0) (2,0) (3,0) (2,1) (3,1) (3,2): A in v[0..5], P in v[6..11]
+#pragma unroll
+                for (int m = 0; m < 6; ++m) {
+                    const int i = m < 3 ? m + 1 : (m < 5 ? m - 1 : 3), j = m < 3 ? 0 : (m < 5 ? 1 : 2);
+                    float gi[8], gj[8];
+                    ld8(gt + (tb + i) * D + 8 * o, gi);
+                    ld8(gt + (tb + j) * D + 8 * o, gj);
+                    const __nv_bfloat16* ki = reinterpret_cast<const __nv_bfloat16*>(&kr[i]);
+                    const __nv_bfloat16* qi = reinterpret_cast<const __nv_bfloat16*>(&qr[i]);
+                    const __nv_bfloat16* kj = reinterpret_cast<const __nv_bfloat16*>(&kr[j]);
+                    float sa = 0.f, sp = 0.f;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float kd = __bfloat162float(kj[e]) * ex2(gi[e] - gj[e]);
+                        sa = fmaf(__bfloat162float(ki[e]), kd, sa);
+                        sp = fmaf(__bfloat162float(qi[e]), kd, sp);
+                    }
+                    v[m] = sa;
+                    v[6 + m] = sp;
+                }
+            }
+            // transposed reduction over the 16 lanes of the block: lane o ends with sum o
+#pragma unroll
+            for (int k = 8; k >= 1; k >>= 1) {
+                const bool upper = (lane & k) != 0;
+#pragma unroll
+                for (int e = 0; e < k; ++e) {
+                    const float send = upper ? v[e] : v[e + k];
+                    const float keep = upper ? v[e + k] : v[e];
+                    v[e] = keep + __shfl_xor_sync(0xffffffffu, send, k);
+                }
+            }
+            {
+                const int m = o < 6 ? o : (o < 12 ? o - 6 : 0);
+                const int i = tb + (o >= 12 ? o - 12 : (m < 3 ? m + 1 : (m < 5 ? m - 1 : 3)));
+                const int j = o >= 12 ? i : tb + (m < 3 ? 0 : (m < 5 ? 1 : 2));
+                if (o < 6) As[i * LDA + j] = bet[i] * v[0];
+                else *reinterpret_cast<__nv_bfloat16*>(sm + S::kP + tc::off_k128(i, j, C)) = __float2bfloat16_rn(v[0]);
+            }
+        }
+        tc::fence_proxy_async();  // P is read by a bulk copy
+        __syncthreads();
+
+        // ---- P to its blob; K o e^{Gam} as hi / lo over X (hi over the dead Q rows, lo
+        //      in place), the gates read back from the scratch ------------------------------
+        if (tid == 0) {
+            unsigned char* Pd = p.Yw + ((size_t)chunk * p.Hv + h) * kYwBytes + kTile64x64;  // rows 64..127 of column block 0
+            tc::bulk_s2g(Pd, tc::smem_u32(sm + S::kP), kTile64x64);
+            tc::bulk_commit();
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int t = t0 + 32 * u, ch = g + 8 * cc;
+                const uint32_t off = tc::chunk_k128(t, ch, 2 * C);
+                const uint4 kr = *reinterpret_cast<const uint4*>(sm + S::kX + off);
+                const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&kr);
+                float g8[8];
+                ld8(gt + t * D + 8 * ch, g8);
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    tc::split2(__bfloat162float(kv[2 * e]) * ex2(g8[2 * e]), __bfloat162float(kv[2 * e + 1]) * ex2(g8[2 * e + 1]),
+                               hw[e], lw[e]);
+                *reinterpret_cast<uint4*>(sm + S::kX + tc::chunk_k128(C + t, ch, 2 * C)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(sm + S::kX + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+        __syncthreads();
+        // V rows (cp.async) over the dead scratch, waited for after the solve
+        stage_rows_async<NT>(sm + S::kV, C, 0, vp + ((size_t)start * p.Hv + h) * D, (size_t)p.Hv * D, L, tid);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+
+        // ---- Tm = (I + A)^{-1}; T'' = Tm diag(beta) as hi / lo over A ---------------
+        solve_unit_lower<NT>(As, Tm, Z, tid);
+        for (int e = tid; e < C * 8; e += NT) {
+            const int i = e >> 3, ch = e & 7;
+            uint32_t h2[4], l2[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = ch * 8 + 2 * u;
+                tc::split2(Tm[i * LDA + j] * bet[j], Tm[i * LDA + j + 1] * bet[j + 1], h2[u], l2[u]);
+            }
+            const uint32_t off = tc::chunk_k128(i, ch, C);
+            *reinterpret_cast<uint4*>(sm + S::kT2h + off) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+            *reinterpret_cast<uint4*>(sm + S::kT2l + off) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
+        }
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+        tc::fence_proxy_async();
+        __syncthreads();
+
+        // ---- W = T'' (K o e^Gam) (3 terms), U = T'' V (2 terms) ------------------------
+        if (tid == 0) {
+            tc::fence_after();
+            constexpr uint32_t id = tc::idesc_bf16(64, 128, false, true);
+            const uint32_t t2h = tc::smem_u32(sm + S::kT2h), t2l = tc::smem_u32(sm + S::kT2l);
+            const uint32_t kgh = sX + C * 128, kgl = sX, sV = tc::smem_u32(sm + S::kV);
+            auto mm = [&](uint32_t dcol, uint32_t a, uint32_t b, uint32_t atom, bool first) {
+                for (int ks = 0; ks < 4; ++ks)
+                    tc::mma_bf16(tmem + dcol, tc::smem_desc(a + ks * 32, 16, 1024, tc::kSwizzle128),
+                                 tc::smem_desc(b + ks * 2048, atom, 1024, tc::kSwizzle128), id, (first && ks == 0) ? 0u : 1u);
+            };
+            mm(0, t2h, kgh, kXcb, true);
+            mm(0, t2h, kgl, kXcb, false);
+            mm(0, t2l, kgh, kXcb, false);
+            mm(128, t2h, sV, C * 128, true);
+            mm(128, t2l, sV, C * 128, false);
+            tc::mma_commit(barW);
+        }
+        __syncwarp();
+        if (!tc::mbar_wait(barW, phW, abort_flag)) raise_error(p, 1u);
+        phW ^= 1u;
+        tc::fence_after();
+        // ---- W, U out of TMEM (row i = 16 q + lane, lane < 16; warp: two 32-column
+        //      blocks of W and of U), staged as blob images (W hi / lo over X, U over
+        //      the work region) and written with bulk copies ----------------------------
+        {
+            const int q = warp & 3, hf = warp >> 2;
+            const int i = 16 * q + (lane & 15);
+            const uint32_t lrow = tmem + ((uint32_t)(32 * q) << 16);
+            unsigned char* sWh = sm + S::kX;
+            unsigned char* sWl = sm + S::kX + kTile64x128;
+            float* sU = reinterpret_cast<float*>(sm + S::kOps);
+            for (int q2 = 0; q2 < 2; ++q2) {
+                const int cb = 2 * hf + q2;
+                float wv[32], uv[32];
+                tc::tmem_ld32(lrow + 32 * cb, wv);
+                tc::tmem_ld32(lrow + 128 + 32 * cb, uv);
+                if (lane < 16) {
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t hw[4], lw[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) tc::split2(wv[8 * cc + 2 * u], wv[8 * cc + 2 * u + 1], hw[u], lw[u]);
+                        const uint32_t off = tc::chunk_k128(i, 4 * cb + cc, C);
+                        *reinterpret_cast<uint4*>(sWh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                        *reinterpret_cast<uint4*>(sWl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                    }
+                    float* ublk = sU + cb * (C * BV) + i;
+#pragma unroll
+                    for (int v = 0; v < BV; ++v) ublk[v * C] = uv[v];
+                }
+            }
+            tc::fence_proxy_async();
+            __syncthreads();
+            if (tid == 0) {
+                unsigned char* Xd = p.Xw + ((size_t)chunk * p.Hv + h) * kXwBytes;
+                unsigned char* Yd = p.Yw + ((size_t)chunk * p.Hv + h) * kYwBytes;
+                const uint32_t half = kTile64x128 / 2;
+                tc::bulk_s2g(Xd, tc::smem_u32(sWh), half);
+                tc::bulk_s2g(Xd + 2 * half, tc::smem_u32(sWh) + half, half);
+                tc::bulk_s2g(Yd, tc::smem_u32(sWl), half);
+                tc::bulk_s2g(Yd + 2 * half, tc::smem_u32(sWl) + half, half);
+                tc::bulk_s2g(p.Ub + ((size_t)chunk * p.Hv + h) * NVB * kUBlock, tc::smem_u32(sU), NVB * kUBlock);
+                tc::bulk_commit();
+                tc::bulk_wait_read();  // the staging areas (and P) are reused by the next item
+            }
+        }
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+    }  // item loop
+    if (tid == 0) tc::bulk_wait_all();
+    if (warp == 0) tc::tmem_dealloc(tmem, 256);
+}
+
+// ---------------------------------------------------------------------------
 // chain kernel
 // ---------------------------------------------------------------------------
 template <bool kKDA>
@@ -1385,8 +1952,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* w
         KernelTimer kt("chunk_chain", stream);
         return launch_dependent(chain_kernel, dim3(a.Hv * NVB, segs), dim3(512), (size_t)smc, stream, p);
     };
-    const cudaError_t e = kda ? run(chunk_prep_kernel<true>, chunk_chain_kernel<true>, PrepSmem<true>::kTotal,
-                                    ChainSmem<true>::kTotal, 1, prep_threads<true>())
+    const cudaError_t e = kda ? run(chunk_prep_kda_kernel, chunk_chain_kernel<true>, (int)KdaSmem::kTotal,
+                                    ChainSmem<true>::kTotal, 2, kKdaThreads)
                               : run(chunk_prep_kernel<false>, chunk_chain_kernel<false>, PrepSmem<false>::kTotal,
                                     ChainSmem<false>::kTotal, 2, prep_threads<false>());
     if (e != cudaSuccess) return e;
