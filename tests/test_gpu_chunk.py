@@ -126,6 +126,21 @@ def test_gate_minus_two_everywhere(gate):
     check_state(sf.cpu(), rs, "final state")
 
 
+@pytest.mark.parametrize("g_range", [(-0.3, 0.0), (-4.0, 0.0)])
+def test_channel_gate_every_chunk_length(g_range):
+    """Per-key-channel gates on sequences of every length 1..64 (so a chunk of
+    every fill, each pivot of the in-chunk pairs falling inside and beyond the
+    chunk end), behind 65- and 128-token sequences, GVA 2, with an initial
+    state; decays up to -4 per token and channel."""
+    lens = [65] + list(range(1, 65)) + [128]
+    case = workloads.chunk_case(63 + int(-g_range[0]), lens, 1, 2, 128, 128, gate="gk", g_range=g_range, h0_std=0.1)
+    o, sf = run_gpu(case)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(sf).all()
+    ro, rs = oracle_ref(case)
+    check_out(o.cpu(), ro, "o")
+    check_state(sf.cpu(), rs, "final state")
+
+
 def test_gate_zero_and_beta_endpoints():
     case = workloads.chunk_case(62, [70, 64], 2, 2, 128, 128, h0_std=0.1)
     case.g[:40] = 0.0
