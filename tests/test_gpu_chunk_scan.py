@@ -8,6 +8,7 @@ import pytest
 import torch
 
 import gated_delta_rule_37_gb300 as gdr
+import oracle
 from gated_delta_rule_37_gb300 import workloads
 from tests.gpu_util import bits_equal, check_out, check_state, rel_l2
 from tests.test_gpu_chunk import oracle_ref, run_gpu
@@ -67,6 +68,11 @@ def test_scan_agrees_with_one_pass_chain():
     o2, s2 = run_gpu(case, flags=SCAN)
     assert rel_l2(s2.cpu().numpy(), s1.cpu().numpy()) <= 1e-4
     assert rel_l2(o2.float().cpu().numpy(), o1.float().cpu().numpy()) <= 5e-3
+    ro, rs = oracle.tokenwise(case.q, case.k, case.v, case.beta, case.cu_seqlens, g=case.g,
+                              initial_state=case.initial_state, scale=case.scale)
+    for o, sf, what in ((o1, s1, "one pass"), (o2, s2, "scan")):
+        check_out(o.cpu(), ro, f"o ({what}) vs oracle")
+        check_state(sf.cpu(), rs, f"final state ({what}) vs oracle")
 
 
 def test_scan_deterministic_and_graph_safe():

@@ -51,6 +51,11 @@ def run_case(case, *, flags, with_ibuf, gated=False):
     return pool, o, ib, o_init
 
 
+def _o_init(case):
+    """The sentinel run_case fills o with."""
+    return sentinel_like((case.T, case.v.shape[1], case.v.shape[2]), case.q.dtype)
+
+
 def check_case(case, pool, o, ib, o_init, *, commit):
     ro, rpool, rib = oracle.pool(case.q, case.k, case.v, case.g, case.beta, case.pool, case.state_indices,
                                  case.cu_seqlens, scale=case.scale, commit=commit, steps=case.steps,
@@ -146,6 +151,9 @@ def test_channel_gate_constant_matches_scalar_gate():
     for b in range(case.N):
         L = cu[b + 1] - cu[b]
         check_state(ib_b.view[b, :L].cpu(), ib_a.view[b, :L].cpu().double().numpy(), f"ibuf row {b}")
+    # and both against the oracle, the per-channel one on its own per-channel gates
+    check_case(case, pool_a, o_a, ib_a, _o_init(case), commit=True)
+    check_case(chan, pool_b, o_b, ib_b, _o_init(chan), commit=True)
 
 
 def test_output_norm_decode_full_size():
@@ -305,6 +313,13 @@ def test_decode_equals_chunk_path_at_one_token():
     torch.cuda.synchronize()
     check_state(pool.view.cpu(), sc.cpu().double().numpy(), "decode vs chunk state")
     check_out(o.view.cpu(), oc.float().cpu().double().numpy(), "decode vs chunk o")
+    # and both against the oracle's tokenwise recurrence from the same states
+    ro, rs = oracle.tokenwise(case.q, case.k, case.v, case.beta, case.cu_seqlens, g=case.g,
+                              initial_state=case.pool[:4], scale=case.scale)
+    check_state(sc.cpu(), rs, "chunk path final state vs oracle")
+    check_state(pool.view.cpu(), rs, "decode pool vs oracle")
+    check_out(oc.cpu(), ro, "chunk path o vs oracle")
+    check_out(o.view.cpu(), ro, "decode o vs oracle")
 
 
 def test_deterministic_repeat():
