@@ -12,8 +12,9 @@
 //        e^{gam_i} q_i and the decay factors.  Results are written as
 //        pre-swizzled operand images ("blobs") so the chain kernel stages them
 //        with single 1-D bulk copies.
-//        Per-key-channel gates (KDA) take the same route on 16 warps: A and P
-//        from pivoted products (pairs across the halves of 2h-token blocks on
+//        Per-key-channel gates (KDA) have a prep kernel of their own
+//        (chunk_prep_kda_kernel, two 256-thread CTAs per SM): A and P from
+//        pivoted products (pairs across the halves of 2h-token blocks on
 //        tcgen05 with the decays folded into both operands around the pivot,
 //        each factor <= 1; pairs inside 4-token blocks on the CUDA cores),
 //        W = Tm diag(beta) (K o e^{Gam}) with a 3-term split, and the decayed
@@ -245,15 +246,10 @@ __device__ __forceinline__ void stage_rows_async(unsigned char* tile, int rows, 
 // operand, so K K^T and Q K^T come from one group of MMAs.  Dead regions are
 // reused: the Q rows of X hold T' hi / lo and the fp32 A matrix holds T'' hi /
 // lo once the solve has finished.
-// 256 threads (two CTAs per SM) with a scalar gate; 512 threads (one CTA per
-// SM, its shared memory does not fit twice) with per-channel gates, so that
-// the long elementwise phases of that path run on 16 warps.  The 64 x 64
-// solve always runs on the first 256.
-template <bool kKDA>
-constexpr int prep_threads() { return kKDA ? 512 : 256; }
+// 256 threads, two CTAs per SM.
+constexpr int kPrepThreads = 256;
 constexpr uint32_t kXcb = 2 * C * 128;  // column-block stride of X (128 rows x 128 B)
 
-template <bool kKDA>
 struct PrepSmem {
     static constexpr uint32_t kX = 0;                         // [K; Q] 128 x 128 bf16 (32 KB)
     static constexpr uint32_t kV = kX + 2 * kTile64x128;      // V tile 64 x 128 (16 KB)
@@ -264,24 +260,16 @@ struct PrepSmem {
     static constexpr uint32_t kT2l = kA + kTile64x64;
     static constexpr uint32_t kTm = (kA + C * LDA * 4 + 1023) & ~1023u;  // fp32 [64][65]
     static constexpr uint32_t kZ = kTm + C * LDA * 4;                   // fp32 [1024]
-    static constexpr uint32_t kKgh = (kZ + 4 * 256 * 4 + 1023) & ~1023u;  // K o e^Gam hi (channel gate)
-    static constexpr uint32_t kKgl = kKgh + (kKDA ? kTile64x128 : 0);
-    static constexpr uint32_t kGam = kKgl + (kKDA ? kTile64x128 : 0);    // fp32 [64][128] or [64]
-    static constexpr uint32_t kPf = kGam + (kKDA ? C * D * 4 : C * 4);   // fp32 [64][65] P staging (channel gate)
-    static constexpr uint32_t kBeta = kPf + (kKDA ? C * LDA * 4 : 0);
-    // channel gate, while A and P are formed: pivoted operands over the dead
-    // Tm / Z / Kg region (64-row left and 32-row right tiles, hi and lo)
-    static constexpr uint32_t kLh = kTm, kLl = kLh + C * 256, kRh = kLl + C * 256, kRl = kRh + 32 * 256;
+    static constexpr uint32_t kGam = (kZ + 4 * 256 * 4 + 1023) & ~1023u;  // fp32 [64] gate cumsum
+    static constexpr uint32_t kBeta = kGam + C * 4;
     static constexpr uint32_t kBar = kBeta + C * 4;
     static constexpr uint32_t kTotal = kBar + 64 + 1024;  // + alignment slack
     static_assert(kT2l + kTile64x64 <= kTm, "T'' tiles overlap Tm");
-    static_assert(!kKDA || kRl + 32 * 256 <= kGam, "pivot operands overlap the gate cumsum");
 };
 
-template <bool kKDA>
-__global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep_kernel(TcParams p) {
-    using S = PrepSmem<kKDA>;
-    constexpr int NT = prep_threads<kKDA>();
+__global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p) {
+    using S = PrepSmem;
+    constexpr int NT = kPrepThreads;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     // Persistent: CTA x takes items x, x + gridDim.x, ... (item = chunk * Hv + h)
@@ -302,12 +290,11 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::kBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::kBar + 16);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::kBar + 24);
-    const uint32_t bar0 = tc::smem_u32(&bars[0]), bar1 = tc::smem_u32(&bars[1]);
+    const uint32_t bar0 = tc::smem_u32(&bars[0]);
 
     if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), 256);
     if (tid == 0) {
         tc::mbar_init(bar0, 1);
-        tc::mbar_init(bar1, 3);
         *abort_flag = 0;
         tc::mbar_fence_init();
     }
@@ -315,7 +302,7 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
-    uint32_t ph0 = 0, ph1 = 0;  // parity of the next completion of bar0 / bar1
+    uint32_t ph0 = 0;  // parity of the next completion of bar0
     tc::grid_dep_wait();    // the chunk table comes from the metadata kernel
     tc::grid_dep_launch();  // the chain kernel may start its prologue on free SMs
     const int nitems = p.meta[0] * p.Hv;
@@ -342,35 +329,13 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
                     if (which == 0) tc::prefetch_l2(kp + (tok * p.Hk + nh / grp) * D, D * 2);
                     else if (which == 1) tc::prefetch_l2(qp + (tok * p.Hk + nh / grp) * D, D * 2);
                     else if (which == 2) tc::prefetch_l2(vp + (tok * p.Hv + nh) * D, D * 2);
-                    else if (kKDA && which == 3) tc::prefetch_l2(p.gk + (tok * p.Hv + nh) * D, D * 4);
                 }
-                if (!kKDA && tid == 255) tc::prefetch_l2_span(p.g + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 4);
+                if (tid == 255) tc::prefetch_l2_span(p.g + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 4);
                 if (tid == 254) tc::prefetch_l2_span(bp + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 2);
             }
         }
         if (tid < C) bet[tid] = tid < L ? to_f(bp[((size_t)start + tid) * p.Hv + h]) : 0.f;
-        if (kKDA) {
-            // per-channel inclusive cumsum in token order: thread (channel c, quarter
-            // qt) scans tokens 16 qt .. 16 qt + 15 (all 16 loads issued before the
-            // dependent adds), then adds the totals of the earlier quarters
-            static_assert(!kKDA || NT == 4 * D, "one thread per channel and quarter of the chunk");
-            const int c = tid & (D - 1), qt = tid >> 7;
-            const float* __restrict__ gk = p.gk + ((size_t)start * p.Hv + h) * D + c;
-            float x[16];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                const int i = 16 * qt + u;
-                x[u] = i < L ? __ldg(gk + (size_t)i * p.Hv * D) : 0.f;
-            }
-#pragma unroll
-            for (int u = 1; u < 16; ++u) x[u] += x[u - 1];
-            Z[qt * D + c] = x[15];  // Z is free until the solve
-            __syncthreads();
-            float off = 0.f;
-            for (int u = 0; u < qt; ++u) off += Z[u * D + c];
-#pragma unroll
-            for (int u = 0; u < 16; ++u) gam[(16 * qt + u) * D + c] = x[u] + off;
-        } else if (warp < 2) {
+        if (warp < 2) {
             // scalar gate: inclusive scan over 64 tokens with two warps
             float x = tid < L ? __ldg(p.g + ((size_t)start + tid) * p.Hv + h) : 0.f;
 #pragma unroll
@@ -381,17 +346,17 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
             gam[tid] = x;
         }
         __syncthreads();
-        if (!kKDA && warp == 1) gam[tid] += gam[31];
+        if (warp == 1) gam[tid] += gam[31];
         asm volatile("cp.async.wait_group 0;" ::: "memory");
         tc::fence_proxy_async();
         tc::fence_before();
         __syncthreads();
         tc::fence_after();
         const uint32_t sX = tc::smem_u32(sm + S::kX), sV = tc::smem_u32(sm + S::kV);
-        const float* gl = kKDA ? gam + (L - 1) * D : gam + (L - 1);
+        const float* gl = gam + (L - 1);
 
         // ---- [K K^T ; Q K^T] on the tensor cores (scalar gate), one M = 128 group ------
-        if (!kKDA && tid == 0) {
+        if (tid == 0) {
             constexpr uint32_t id = tc::idesc_bf16(128, 64, false, false);
             for (int ks = 0; ks < 8; ++ks) {
                 const uint32_t off = (ks >> 2) * kXcb + (ks & 3) * 32;
@@ -410,54 +375,28 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
                 const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(C + i, ch, 2 * C));
                 const __nv_bfloat16* qv = reinterpret_cast<const __nv_bfloat16*>(&raw);
                 uint32_t w4[4];
-                float gq[8];
-                if (kKDA) ld8(gam + i * D + ch * 8, gq);
+                const float eg = __expf(gam[i]);
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float g0 = kKDA ? gq[2 * u] : gam[i], g1 = kKDA ? gq[2 * u + 1] : gam[i];
-                    w4[u] = tc::pack_bf16(__bfloat162float(qv[2 * u]) * __expf(g0),
-                                          __bfloat162float(qv[2 * u + 1]) * __expf(g1));
-                }
+                for (int u = 0; u < 4; ++u)
+                    w4[u] = tc::pack_bf16(__bfloat162float(qv[2 * u]) * eg, __bfloat162float(qv[2 * u + 1]) * eg);
                 *reinterpret_cast<uint4*>(Qdst + tc::chunk_k128(C + i, ch, 2 * C)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
-            if (!kKDA) {
-                if (h % grp == 0) {  // K rows of X, both column blocks -> a [64][128] k128 image
-                    unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hk + kh) * kTile64x128;
-                    for (int e = tid; e < (int)(kTile64x128 / 16); e += NT) {
-                        const int cb = e >> 9, r = e & 511;
-                        reinterpret_cast<uint4*>(Kdst)[e] = reinterpret_cast<const uint4*>(sm + S::kX + cb * kXcb)[r];
-                    }
-                }
-            } else {
-                unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hv + h) * 2 * kTile64x128;
-                for (int e = tid; e < C * 16; e += NT) {
-                    const int i = e >> 4, ch = e & 15;
-                    const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(i, ch, 2 * C));
-                    const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&raw);
-                    uint32_t hw[4], lw[4];
-                    float gL[8], gI[8];
-                    ld8(gl + ch * 8, gL);
-                    ld8(gam + i * D + ch * 8, gI);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float x0 = i < L ? __bfloat162float(kv[2 * u]) * __expf(gL[2 * u] - gI[2 * u]) : 0.f;
-                        const float x1 = i < L ? __bfloat162float(kv[2 * u + 1]) * __expf(gL[2 * u + 1] - gI[2 * u + 1]) : 0.f;
-                        tc::split2(x0, x1, hw[u], lw[u]);
-                    }
-                    const uint32_t off = tc::chunk_k128(i, ch, C);
-                    *reinterpret_cast<uint4*>(Kdst + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                    *reinterpret_cast<uint4*>(Kdst + kTile64x128 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            if (h % grp == 0) {  // K rows of X, both column blocks -> a [64][128] k128 image
+                unsigned char* Kdst = p.Kb + ((size_t)chunk * p.Hk + kh) * kTile64x128;
+                for (int e = tid; e < (int)(kTile64x128 / 16); e += NT) {
+                    const int cb = e >> 9, r = e & 511;
+                    reinterpret_cast<uint4*>(Kdst)[e] = reinterpret_cast<const uint4*>(sm + S::kX + cb * kXcb)[r];
                 }
             }
             float* rec = reinterpret_cast<float*>(p.Rb + ((size_t)chunk * p.Hv + h) * kRec);
-            if (tid < C) rec[tid] = tid < L ? (kKDA ? 1.f : __expf(gl[0] - gam[tid])) : 0.f;
-            if (tid < D) rec[64 + tid] = __expf(kKDA ? gl[tid] : gl[0]);
+            if (tid < C) rec[tid] = tid < L ? __expf(gl[0] - gam[tid]) : 0.f;
+            if (tid < D) rec[64 + tid] = __expf(gl[0]);
             if (tid == 0) reinterpret_cast<int*>(rec)[192] = L;
         }
 
         // ---- A (strictly lower) and P (lower incl. diagonal) -------------------------
         unsigned char* Pdst = p.Yw + ((size_t)chunk * p.Hv + h) * kYwBytes;  // rows 64..127 of column block 0
-        if (!kKDA) {
+        {
             if (!tc::mbar_wait(bar0, ph0, abort_flag)) raise_error(p, 1u);
             ph0 ^= 1u;
             tc::fence_after();
@@ -500,185 +439,6 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
                     *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(C + i, 4 * hf + cc, 2 * C)) =
                         make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
             }
-        } else {
-            // Per-channel decays: A_ij = beta_i sum_c k_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}
-            // and P_ij = sum_c q_i[c] k_j[c] e^{gam_i[c]-gam_j[c]}.  Pairs in different
-            // halves of a block of 2h tokens (h = 32, 16, 8, 4) go through the tensor
-            // cores with the pivot p = first token of the upper half (j < p <= i):
-            // e^{gam_i - gam_j} = e^{gam_i - gam_p} e^{gam_p - gam_j}, both factors
-            // <= 1, folded into the left (k_i, q_i) and right (k_j) operands, each
-            // split into bf16 hi + lo (3 products).  Pairs inside a 4-token block are
-            // formed directly.  Every exponent is <= 0 for any finite gate.
-            float* Pf = reinterpret_cast<float*>(sm + S::kPf);
-            for (int e = tid; e < C * LDA; e += NT) {
-                As[e] = 0.f;
-                Pf[e] = 0.f;
-            }
-            constexpr uint32_t idL = tc::idesc_bf16(64, 32, false, false);
-            for (int lev = 0; lev < 4; ++lev) {
-                const int sh = 5 - lev, hh = 1 << sh;  // half-block size 32, 16, 8, 4
-                // operand rows: 32 left tokens (K rows 0..31 and Q rows 32..63 of the
-                // 64-row tile) and 32 right tokens, each in 16 chunks of 8 channels
-                for (int e = tid; e < 64 * 16; e += NT) {
-                    const int tr = e >> 4, ch = e & 15;
-                    const bool left = tr < 32;
-                    const int idx = tr & 31, B = idx >> sh, t = idx & (hh - 1);
-                    const int piv = 2 * hh * B + hh;
-                    const int tok = left ? piv + t : piv - hh + t;
-                    const float4* gt = reinterpret_cast<const float4*>(gam + tok * D + ch * 8);
-                    const float4* gp = reinterpret_cast<const float4*>(gam + piv * D + ch * 8);
-                    float f[8];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const float4 a4 = gt[u], b4 = gp[u];
-                        const float d0 = a4.x - b4.x, d1 = a4.y - b4.y, d2 = a4.z - b4.z, d3 = a4.w - b4.w;
-                        f[4 * u + 0] = __expf(left ? d0 : -d0);
-                        f[4 * u + 1] = __expf(left ? d1 : -d1);
-                        f[4 * u + 2] = __expf(left ? d2 : -d2);
-                        f[4 * u + 3] = __expf(left ? d3 : -d3);
-                    }
-                    const uint4 kr = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(tok, ch, 2 * C));
-                    const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&kr);
-                    uint32_t hw[4], lw[4];
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        tc::split2(__bfloat162float(kv[2 * u]) * f[2 * u], __bfloat162float(kv[2 * u + 1]) * f[2 * u + 1],
-                                   hw[u], lw[u]);
-                    if (left) {
-                        const uint32_t off = tc::chunk_k128(idx, ch, C);
-                        *reinterpret_cast<uint4*>(sm + S::kLh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                        *reinterpret_cast<uint4*>(sm + S::kLl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                        const uint4 qr = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(C + tok, ch, 2 * C));
-                        const __nv_bfloat16* qv = reinterpret_cast<const __nv_bfloat16*>(&qr);
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            tc::split2(__bfloat162float(qv[2 * u]) * f[2 * u], __bfloat162float(qv[2 * u + 1]) * f[2 * u + 1],
-                                       hw[u], lw[u]);
-                        const uint32_t offq = tc::chunk_k128(32 + idx, ch, C);
-                        *reinterpret_cast<uint4*>(sm + S::kLh + offq) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                        *reinterpret_cast<uint4*>(sm + S::kLl + offq) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                    } else {
-                        const uint32_t off = tc::chunk_k128(idx, ch, 32);
-                        *reinterpret_cast<uint4*>(sm + S::kRh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                        *reinterpret_cast<uint4*>(sm + S::kRl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                    }
-                }
-                tc::fence_proxy_async();
-                tc::fence_before();
-                __syncthreads();
-                tc::fence_after();
-                // three issuers, one split product each, into accumulator columns 32 w
-                if (warp < 3 && lane == 0) {
-                    const uint32_t la = tc::smem_u32(sm + (warp == 2 ? S::kLl : S::kLh));
-                    const uint32_t rb = tc::smem_u32(sm + (warp == 1 ? S::kRl : S::kRh));
-                    for (int ks = 0; ks < 8; ++ks)
-                        tc::mma_bf16(tmem + 32 * warp,
-                                     tc::smem_desc(la + (ks >> 2) * (C * 128) + (ks & 3) * 32, 16, 1024, tc::kSwizzle128),
-                                     tc::smem_desc(rb + (ks >> 2) * (32 * 128) + (ks & 3) * 32, 16, 1024, tc::kSwizzle128),
-                                     idL, ks > 0);
-                    tc::mma_commit(bar1);
-                }
-                __syncwarp();
-                if (!tc::mbar_wait(bar1, ph1, abort_flag)) raise_error(p, 1u);
-                ph1 ^= 1u;
-                tc::fence_after();
-                if (warp < 4) {
-                    // M = 64 accumulator: row r = 16 warp + lane (lane < 16); rows 0..31
-                    // are A rows, 32..63 P rows; column n pairs with row r when both
-                    // fall in the same block of 2h tokens
-                    float d[32], e2[32];
-                    const uint32_t lrow = tmem + ((uint32_t)(32 * warp) << 16);
-                    tc::tmem_ld32(lrow, d);
-                    tc::tmem_ld32(lrow + 32, e2);
-#pragma unroll
-                    for (int n = 0; n < 32; ++n) d[n] += e2[n];
-                    tc::tmem_ld32(lrow + 64, e2);
-#pragma unroll
-                    for (int n = 0; n < 32; ++n) d[n] += e2[n];
-                    const int r = 16 * warp + lane, idx = r & 31, B = idx >> sh;
-                    const int i = 2 * hh * B + hh + (idx & (hh - 1));
-                    if (lane < 16 && i < L) {
-                        float* dst = (warp < 2 ? As : Pf) + i * LDA;
-                        const float sc = warp < 2 ? bet[i] : 1.f;
-#pragma unroll
-                        for (int n = 0; n < 32; ++n)
-                            if ((n >> sh) == B) dst[2 * hh * B + (n & (hh - 1))] = sc * d[n];
-                    }
-                }
-                tc::fence_before();
-            }
-            {
-                // pairs inside a 4-token block: warp w takes the block of tokens
-                // 4w..4w+3 (its 10 pairs j <= i), lane l channels 4l..4l+3; the 10
-                // A sums and the 10 P sums are reduced across the warp together
-                static_assert(!kKDA || NT / 32 == C / 4, "one warp per 4-token block");
-                const int t0 = 4 * warp;
-                float gv[4][4], kf[4][4], qf[4][4];
-#pragma unroll
-                for (int tk = 0; tk < 4; ++tk) {
-                    const int tok = t0 + tk;
-                    const float4 g4 = *reinterpret_cast<const float4*>(gam + tok * D + 4 * lane);
-                    gv[tk][0] = g4.x; gv[tk][1] = g4.y; gv[tk][2] = g4.z; gv[tk][3] = g4.w;
-                    const uint2 kr = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(tok, 4 * lane, 2 * C));
-                    const uint2 qr = *reinterpret_cast<const uint2*>(sm + S::kX + tc::off_k128(C + tok, 4 * lane, 2 * C));
-                    const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(&kr);
-                    const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(&qr);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        kf[tk][c] = __bfloat162float(kb[c]);
-                        qf[tk][c] = __bfloat162float(qb[c]);
-                    }
-                }
-                float xs[32];  // [0, 10): A pairs, [10, 20): P pairs
-#pragma unroll
-                for (int pp = 0; pp < 32; ++pp) xs[pp] = 0.f;
-#pragma unroll
-                for (int pr = 0; pr < 10; ++pr) {
-                    const int di = (pr >= 1) + (pr >= 3) + (pr >= 6), dj = pr - di * (di + 1) / 2;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const float kd = kf[dj][c] * __expf(gv[di][c] - gv[dj][c]);
-                        xs[pr] = fmaf(kf[di][c], kd, xs[pr]);
-                        xs[10 + pr] = fmaf(qf[di][c], kd, xs[10 + pr]);
-                    }
-                }
-                const float rs = reduce32_to_lane(xs, lane);
-                if (lane < 20) {
-                    const int pr = lane % 10, di = (pr >= 1) + (pr >= 3) + (pr >= 6), dj = pr - di * (di + 1) / 2;
-                    const int i = t0 + di, j = t0 + dj;
-                    if (i < L) {
-                        if (lane < 10) {
-                            if (j < i) As[i * LDA + j] = bet[i] * rs;
-                        } else {
-                            Pf[i * LDA + j] = rs;
-                        }
-                    }
-                }
-            }
-            __syncthreads();
-            for (int e = tid; e < C * 8; e += NT) {
-                const int i = e >> 3, ch = e & 7;
-                uint32_t w4[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) w4[u] = tc::pack_bf16(Pf[i * LDA + ch * 8 + 2 * u], Pf[i * LDA + ch * 8 + 2 * u + 1]);
-                *reinterpret_cast<uint4*>(Pdst + tc::chunk_k128(C + i, ch, 2 * C)) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-            }
-            // K o e^{Gam} as hi / lo for W
-            for (int e = tid; e < C * 16; e += NT) {
-                const int i = e >> 4, ch = e & 15;
-                const uint4 raw = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(i, ch, 2 * C));
-                const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&raw);
-                uint32_t hw[4], lw[4];
-                float gI[8];
-                ld8(gam + i * D + ch * 8, gI);
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    tc::split2(__bfloat162float(kv[2 * u]) * __expf(gI[2 * u]),
-                               __bfloat162float(kv[2 * u + 1]) * __expf(gI[2 * u + 1]), hw[u], lw[u]);
-                const uint32_t off = tc::chunk_k128(i, ch, C);
-                *reinterpret_cast<uint4*>(sm + S::kKgh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4*>(sm + S::kKgl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            }
         }
         tc::fence_before();
         __syncthreads();
@@ -695,7 +455,7 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
             for (int u = 0; u < 4; ++u) {
                 const int j = ch * 8 + 2 * u;
                 const float t0 = Tm[i * LDA + j] * bet[j], t1 = Tm[i * LDA + j + 1] * bet[j + 1];
-                tc::split2(kKDA ? t0 : t0 * __expf(gam[j]), kKDA ? t1 : t1 * __expf(gam[j + 1]), h1[u], l1[u]);
+                tc::split2(t0 * __expf(gam[j]), t1 * __expf(gam[j + 1]), h1[u], l1[u]);
                 tc::split2(t0, t1, h2[u], l2[u]);
             }
             const uint32_t off = tc::chunk_k128(i, ch, C);
@@ -719,15 +479,8 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
                     tc::mma_bf16(tmem + dcol, tc::smem_desc(a + ks * 32, 16, 1024, tc::kSwizzle128),
                                  tc::smem_desc(b + ks * 2048, atom, 1024, tc::kSwizzle128), id, (first && ks == 0) ? 0u : 1u);
             };
-            if (!kKDA) {
-                mm(0, t1h, sX, kXcb, true);
-                mm(0, t1l, sX, kXcb, false);
-            } else {
-                const uint32_t kgh = tc::smem_u32(sm + S::kKgh), kgl = tc::smem_u32(sm + S::kKgl);
-                mm(0, t2h, kgh, C * 128, true);
-                mm(0, t2h, kgl, C * 128, false);
-                mm(0, t2l, kgh, C * 128, false);
-            }
+            mm(0, t1h, sX, kXcb, true);
+            mm(0, t1l, sX, kXcb, false);
             mm(128, t2h, sV, C * 128, true);
             mm(128, t2l, sV, C * 128, false);
             tc::mma_commit(bar0);
@@ -735,8 +488,7 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
         __syncwarp();
 
         // ---- W, U out of TMEM into their blobs: row i = 16 q + lane (lane < 16);
-        //      8 warps: columns [64 hf, 64 hf + 64) of W and of U, 16 warps: columns
-        //      [32 hf, 32 hf + 32).  The images are staged in
+        //      warp: columns [64 hf, 64 hf + 64) of W and of U.  The images are staged in
         //      shared memory left dead by the finished MMAs (W hi / lo as 64-row k128
         //      tiles over X, U value-major over V and A) and written with bulk copies,
         //      so every global write is a contiguous run. ---------------------------------
@@ -750,7 +502,7 @@ __global__ void __launch_bounds__(prep_threads<kKDA>(), kKDA ? 1 : 2) chunk_prep
             unsigned char* sWh = sm + S::kX;            // [64][128] k128, column-block stride 8 KB
             unsigned char* sWl = sm + S::kX + kTile64x128;
             float* sU = reinterpret_cast<float*>(sm + S::kV);  // 4 x [32 v][64 i]
-            constexpr int kBlocks = 512 / NT;  // 32-column blocks per warp: 2 (8 warps) or 1 (16 warps)
+            constexpr int kBlocks = 2;  // 32-column blocks of W and of U per warp
             for (int q2 = 0; q2 < kBlocks; ++q2) {
                 const int cb = kBlocks * hf + q2;  // 32-column block of W and of U
                 float wv[32], uv[32];
@@ -1527,7 +1279,6 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
         // to the start-address field (tiles sit below 256 KB, so no carry).
         const int q = warp & 3, hf = (warp - 4) >> 2;
         const int t = 32 * q + lane;            // TMEM lane = row k of S^T
-        const bool lead = warp == 4 && lane == 0;
         const bool isA = warp == 4 && lane == 0, isB = warp == 5 && lane == 0, isC = warp == 6 && lane == 0;
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         const bool nrow = q < 2;                // owns row i = t of the N accumulator
@@ -1954,8 +1705,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* w
     };
     const cudaError_t e = kda ? run(chunk_prep_kda_kernel, chunk_chain_kernel<true>, (int)KdaSmem::kTotal,
                                     ChainSmem<true>::kTotal, 2, kKdaThreads)
-                              : run(chunk_prep_kernel<false>, chunk_chain_kernel<false>, PrepSmem<false>::kTotal,
-                                    ChainSmem<false>::kTotal, 2, prep_threads<false>());
+                              : run(chunk_prep_kernel, chunk_chain_kernel<false>, (int)PrepSmem::kTotal,
+                                    ChainSmem<false>::kTotal, 2, kPrepThreads);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
