@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
         // ---- A (strictly lower) and P (lower incl. diagonal) -------------------------
         unsigned char* Pdst = p.Yw + ((size_t)chunk * p.Hv + h) * kYwBytes;  // rows 64..127 of column block 0
         {
-            if (!tc::mbar_wait(bar0, ph0, abort_flag)) raise_error(p, 1u);
+            if (!tc::mbar_wait(bar0, ph0, abort_flag)) { *abort_flag = 1; raise_error(p, 1u); }
             ph0 ^= 1u;
             tc::fence_after();
             // thread: accumulator row r = 32 q + lane (rows < 64: K K^T, >= 64: Q K^T),
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
         //      tiles over X, U value-major over V and A) and written with bulk copies,
         //      so every global write is a contiguous run. ---------------------------------
         // the item's last completion of bar0 (the scalar gate's K K^T / Q K^T group was the first)
-        if (!tc::mbar_wait(bar0, ph0, abort_flag)) raise_error(p, 1u);
+        if (!tc::mbar_wait(bar0, ph0, abort_flag)) { *abort_flag = 1; raise_error(p, 1u); }
         ph0 ^= 1u;
         tc::fence_after();
         {
@@ -571,7 +571,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
 //     stored in bf16 and only feeds the output).  Each level's accumulators
 //     alternate between two TMEM column sets, so the read-out of one level
 //     runs while the next level's products are in flight.  Pairs inside a
-//     4-token block are formed on the CUDA cores, one warp per block.
+//     4-token block are formed on the CUDA cores (a warp takes two blocks, a
+//     lane one block and 8 channels).
 //   * W = Tm diag(beta) (K o e^{Gam}) with a 3-term split, U = Tm diag(beta) V
 //     with a 2-term split, as for the scalar gate.
 // Shared memory stays under 113 KB, so two CTAs share an SM and one CTA's
@@ -864,7 +865,7 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
         // the right columns n < 16 and n >= 16.  Column n pairs with row r when both
         // fall in the same block of 2h tokens.
         auto wait_level = [&](int lev) {
-            if (!tc::mbar_wait(barL[lev & 1], (lev >> 1) & 1, abort_flag)) raise_error(p, 1u);
+            if (!tc::mbar_wait(barL[lev & 1], (lev >> 1) & 1, abort_flag)) { *abort_flag = 1; raise_error(p, 1u); }
             tc::fence_after();
         };
         auto readout = [&](int lev) {
@@ -1059,7 +1060,7 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
             tc::mma_commit(barW);
         }
         __syncwarp();
-        if (!tc::mbar_wait(barW, phW, abort_flag)) raise_error(p, 1u);
+        if (!tc::mbar_wait(barW, phW, abort_flag)) { *abort_flag = 1; raise_error(p, 1u); }
         phW ^= 1u;
         tc::fence_after();
         // ---- W, U out of TMEM (row i = 16 q + lane, lane < 16; warp: two 32-column
