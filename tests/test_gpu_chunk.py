@@ -249,3 +249,30 @@ def test_gating_kernel():
         rg, rb = oracle.gating(a, dt, A_log, b, neg_eigval=neg)
         np.testing.assert_allclose(g.cpu().double().numpy(), rg, rtol=1e-5, atol=1e-6)
         np.testing.assert_allclose(beta.cpu().double().numpy(), rb, rtol=1e-5, atol=1e-6)
+
+
+def test_most_sequences_per_call():
+    """65535 sequences in one call, the most the tensor-core path accepts (one
+    grid row per sequence): mostly one token, some spanning one, two and four
+    chunks, in a shuffled order.  A sample of the sequences (every long one and
+    a random set of short ones) is checked against the oracle, computed on each
+    sequence alone; every output row must be finite."""
+    gen = torch.Generator().manual_seed(64)
+    lens = [1] * 65400 + [64] * 100 + [65] * 20 + [200] * 15
+    lens = [lens[i] for i in torch.randperm(len(lens), generator=gen).tolist()]
+    case = workloads.chunk_case(64, lens, 1, 1, 128, 128, gate="g", g_range=(-1.0, 0.0))
+    dev = DEV
+    q, k, v, beta, g = (t.to(dev) for t in (case.q, case.k, case.v, case.beta, case.g))
+    o, sf = gdr.chunk_fwd(q, k, v, beta, case.cu_seqlens.to(dev), g=g, scale=case.scale)
+    torch.cuda.synchronize()
+    assert gdr.device_status() == 0
+    assert torch.isfinite(o.float()).all()
+    cu = case.cu_seqlens.tolist()
+    longs = [b for b in range(case.N) if cu[b + 1] - cu[b] > 1]
+    shorts = torch.randperm(case.N, generator=gen)[:64].tolist()
+    for b in longs + shorts:
+        sl = slice(cu[b], cu[b + 1])
+        ro, rs = oracle.tokenwise(case.q[sl], case.k[sl], case.v[sl], case.beta[sl], [0, cu[b + 1] - cu[b]],
+                                  g=case.g[sl], scale=case.scale)
+        check_out(o[sl].cpu(), ro, f"o of sequence {b}")
+        check_state(sf[b:b + 1].cpu(), rs, f"final state of sequence {b}")

@@ -441,3 +441,14 @@ def test_multi_token_wide_blocks(mode):
         case.raw = workloads.raw_gates(79, case.T, 4)
     pool, o, ib, o_init = run_case(case, flags=gdr.GDR_COMMIT, with_ibuf=False, gated=mode == "gated")
     check_case(_with_oracle_gates(case) if mode == "gated" else case, pool, o, ib, o_init, commit=True)
+
+
+def test_multi_token_beyond_longest_first_limit():
+    """1500 multi-token sequences (more than the 1024 a call ranks longest
+    first, so the CTAs take them in index order): 1..4 tokens each, padding
+    rows, bf16 pool committed, per-token states."""
+    lens = torch.randint(1, 5, (1500,), generator=torch.Generator().manual_seed(81)).tolist()
+    case = workloads.pool_case(82, lens, 1, 2, 128, 128, 1600, pool_dtype=torch.bfloat16, pad_count=40, commit=True,
+                               steps=4, ibuf_rows=1500, g_range=(-0.5, 0.0))
+    pool, o, ib, o_init = run_case(case, flags=gdr.GDR_COMMIT, with_ibuf=True)
+    check_case(case, pool, o, ib, o_init, commit=True)
