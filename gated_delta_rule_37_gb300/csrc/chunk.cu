@@ -26,6 +26,8 @@
 #include "common.cuh"
 #include "launch.h"
 
+#include <type_traits>
+
 namespace gdr {
 
 static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -74,11 +76,14 @@ ChunkWorkspace chunk_workspace_layout(int N, int64_t T, int Hk, int Hv, int K, i
     w.off_qn = take(l2 ? esz * (size_t)T * Hk * K : 0);
     w.off_kn = take(l2 ? esz * (size_t)T * Hk * K : 0);
     w.off_order = take(sizeof(int) * (size_t)(N + 1));
-    w.tc = dtype == 0 && K == 128 && V == 128;
+    // bf16 inputs take the tensor-core path (a 64-channel head runs on its
+    // 128-channel tiles with the upper half zero); fp32 inputs the CUDA cores
+    w.tc = dtype == 0 && K == V && (K == 128 || K == 64);
     if (w.tc) {
         // tensor-core path: pre-swizzled per-chunk operand images only
         w.off_blobs = take(chunk_tc_blob_bytes(w.max_chunks, Hk, Hv, gate_kind == 1));
-        w.seg_chunks = (flags & 0x20) ? chunk_scan_segment(N, T, Hv) : 0;  // GDR_CHUNK_SCAN (>= 1)
+        // GDR_CHUNK_SCAN (>= 1): 128-channel heads only (the flag is ignored otherwise)
+        w.seg_chunks = ((flags & 0x20) && K == 128) ? chunk_scan_segment(N, T, Hv) : 0;
         if (w.seg_chunks > 0) {
             w.max_segs = (w.max_chunks + w.seg_chunks - 1) / w.seg_chunks + N;
             w.off_segs = take(16 * (size_t)w.max_segs);
@@ -523,29 +528,32 @@ cudaError_t launch_chunk_t(const ChunkArgs& a, cudaStream_t stream) {
         p.q = qn;
         p.k = kn;
     }
-    if (w.tc) return launch_chunk_tc(a, w, ws, p.q, p.k, stream);
-    const size_t sm_intra = sizeof(float) * (4 * C * LD + 2 * C * (C + 1) + C);
-    cudaFuncSetAttribute(chunk_intra_kernel<InT, K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_intra);
-    {
-        KernelTimer kt("chunk_intra", stream);
-        chunk_intra_kernel<InT, K><<<dim3((unsigned)w.max_chunks, a.Hv), 256, sm_intra, stream>>>(p);
-    }
+    if constexpr (std::is_same<InT, __nv_bfloat16>::value) {
+        return launch_chunk_tc(a, w, ws, p.q, p.k, stream);  // every bf16 shape is a tensor-core shape
+    } else {
+        const size_t sm_intra = sizeof(float) * (4 * C * LD + 2 * C * (C + 1) + C);
+        cudaFuncSetAttribute(chunk_intra_kernel<InT, K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_intra);
+        {
+            KernelTimer kt("chunk_intra", stream);
+            chunk_intra_kernel<InT, K><<<dim3((unsigned)w.max_chunks, a.Hv), 256, sm_intra, stream>>>(p);
+        }
 
-    constexpr int BV = 32;
-    const size_t sm_state = sizeof(float) * (BV * LD + 2 * C * LD + C * (BV + 1) + K);
-    cudaFuncSetAttribute(chunk_state_kernel<K, BV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_state);
-    {
-        KernelTimer kt("chunk_state", stream);
-        chunk_state_kernel<K, BV><<<dim3(a.N, a.Hv, a.V / BV), 256, sm_state, stream>>>(p);
-    }
+        constexpr int BV = 32;
+        const size_t sm_state = sizeof(float) * (BV * LD + 2 * C * LD + C * (BV + 1) + K);
+        cudaFuncSetAttribute(chunk_state_kernel<K, BV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_state);
+        {
+            KernelTimer kt("chunk_state", stream);
+            chunk_state_kernel<K, BV><<<dim3(a.N, a.Hv, a.V / BV), 256, sm_state, stream>>>(p);
+        }
 
-    const size_t sm_out = sizeof(float) * ((2 * C + K) * LD + C * (C + 1));
-    cudaFuncSetAttribute(chunk_out_kernel<InT, K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_out);
-    {
-        KernelTimer kt("chunk_out", stream);
-        chunk_out_kernel<InT, K><<<dim3((unsigned)w.max_chunks, a.Hv), 256, sm_out, stream>>>(p);
+        const size_t sm_out = sizeof(float) * ((2 * C + K) * LD + C * (C + 1));
+        cudaFuncSetAttribute(chunk_out_kernel<InT, K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm_out);
+        {
+            KernelTimer kt("chunk_out", stream);
+            chunk_out_kernel<InT, K><<<dim3((unsigned)w.max_chunks, a.Hv), 256, sm_out, stream>>>(p);
+        }
+        return cudaGetLastError();
     }
-    return cudaGetLastError();
 }
 
 }  // namespace

@@ -87,6 +87,11 @@ struct TcParams {
     unsigned char* Rb;   // [chunk][Hv][1 KB]
     unsigned int* err;
     int N, Hk, Hv;
+    // channels of K and V in global memory (64 or 128).  The kernels always
+    // work on 128-channel tiles; with 64 channels the upper half of every
+    // staged row is zero, so every product, image and state entry beyond
+    // channel 64 is zero, and the chain runs only the value blocks below 64.
+    int dk;
     float scale;
     // chunk-parallel scan: mode 0 = one chain CTA runs a whole sequence;
     // 1 = segment summaries: the first segment of a sequence from h0 with its
@@ -224,17 +229,19 @@ __device__ __forceinline__ void ld8(const float* p, float (&f)[8]) {
     f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
 }
 
-// Stage 64 token rows [64][128] bf16 (rows >= L zero-filled) into rows
-// [row0, row0 + 64) of a k128 smem tile of `rows` rows, with cp.async (all
-// 16-byte pieces in flight at once).
+// Stage 64 token rows [64][128] bf16 into rows [row0, row0 + 64) of a k128
+// smem tile of `rows` rows, with cp.async (all 16-byte pieces in flight at
+// once).  Rows >= L and the 16-byte pieces of a row beyond the first nch
+// (channels >= 8 nch: a 64-channel head) are zero-filled.
 template <int NT>
 __device__ __forceinline__ void stage_rows_async(unsigned char* tile, int rows, int row0, const __nv_bfloat16* src,
-                                                 size_t row_stride, int L, int tid) {
+                                                 size_t row_stride, int L, int nch, int tid) {
     for (int e = tid; e < C * 16; e += NT) {
         const int row = e >> 4, ch = e & 15;
-        const __nv_bfloat16* g = src + (size_t)(row < L ? row : 0) * row_stride + ch * 8;
+        const bool ok = row < L && ch < nch;
+        const __nv_bfloat16* g = src + (size_t)(row < L ? row : 0) * row_stride + (ch < nch ? ch : 0) * 8;
         const uint32_t dst = tc::smem_u32(tile + tc::chunk_k128(row0 + row, ch, rows));
-        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(g), "r"(row < L ? 16 : 0)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" :: "r"(dst), "l"(g), "r"(ok ? 16 : 0)
                      : "memory");
     }
 }
@@ -314,9 +321,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
         const int kh = h / grp;
 
         // ---- stage K, Q (as X) and V rows (cp.async), gates, beta -------------------
-        stage_rows_async<NT>(sm + S::kX, 2 * C, 0, kp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
-        stage_rows_async<NT>(sm + S::kX, 2 * C, C, qp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
-        stage_rows_async<NT>(sm + S::kV, C, 0, vp + ((size_t)start * p.Hv + h) * D, (size_t)p.Hv * D, L, tid);
+        stage_rows_async<NT>(sm + S::kX, 2 * C, 0, kp + ((size_t)start * p.Hk + kh) * p.dk, (size_t)p.Hk * p.dk, L,
+                             p.dk / 8, tid);
+        stage_rows_async<NT>(sm + S::kX, 2 * C, C, qp + ((size_t)start * p.Hk + kh) * p.dk, (size_t)p.Hk * p.dk, L,
+                             p.dk / 8, tid);
+        stage_rows_async<NT>(sm + S::kV, C, 0, vp + ((size_t)start * p.Hv + h) * p.dk, (size_t)p.Hv * p.dk, L,
+                             p.dk / 8, tid);
         asm volatile("cp.async.commit_group;" ::: "memory");
         {
             const int nxt = item + (int)gridDim.x;
@@ -326,9 +336,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
                 const int r = tid & 63, which = tid >> 6;
                 const size_t tok = (size_t)ni.y + r;
                 if (r < ni.z) {
-                    if (which == 0) tc::prefetch_l2(kp + (tok * p.Hk + nh / grp) * D, D * 2);
-                    else if (which == 1) tc::prefetch_l2(qp + (tok * p.Hk + nh / grp) * D, D * 2);
-                    else if (which == 2) tc::prefetch_l2(vp + (tok * p.Hv + nh) * D, D * 2);
+                    if (which == 0) tc::prefetch_l2(kp + (tok * p.Hk + nh / grp) * p.dk, p.dk * 2);
+                    else if (which == 1) tc::prefetch_l2(qp + (tok * p.Hk + nh / grp) * p.dk, p.dk * 2);
+                    else if (which == 2) tc::prefetch_l2(vp + (tok * p.Hv + nh) * p.dk, p.dk * 2);
                 }
                 if (tid == 255) tc::prefetch_l2_span(p.g + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 4);
                 if (tid == 254) tc::prefetch_l2_span(bp + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 2);
@@ -676,16 +686,20 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
 
         // ---- stage K, Q rows and the gate rows (cp.async); zero A and P; beta; warm L2
         //      for the next item ----------------------------------------------------------
-        stage_rows_async<NT>(sm + S::kX, 2 * C, 0, kp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
-        stage_rows_async<NT>(sm + S::kX, 2 * C, C, qp + ((size_t)start * p.Hk + kh) * D, (size_t)p.Hk * D, L, tid);
+        stage_rows_async<NT>(sm + S::kX, 2 * C, 0, kp + ((size_t)start * p.Hk + kh) * p.dk, (size_t)p.Hk * p.dk, L,
+                             p.dk / 8, tid);
+        stage_rows_async<NT>(sm + S::kX, 2 * C, C, qp + ((size_t)start * p.Hk + kh) * p.dk, (size_t)p.Hk * p.dk, L,
+                             p.dk / 8, tid);
         {
-            // gk rows [64][128] fp32 into the scratch (rows >= L zero-filled)
-            const float* src = p.gk + ((size_t)start * p.Hv + h) * D;
+            // gk rows [64][128] fp32 into the scratch (rows >= L and channels
+            // >= dk zero-filled: a zero log-decay on a zero channel)
+            const float* src = p.gk + ((size_t)start * p.Hv + h) * p.dk;
             for (int e = tid; e < C * (D / 4); e += NT) {
                 const int row = e >> 5, pc = e & 31;
-                const float* gsrc = src + (size_t)(row < L ? row : 0) * p.Hv * D + 4 * pc;
+                const bool ok = row < L && 4 * pc < p.dk;
+                const float* gsrc = src + (size_t)(row < L ? row : 0) * p.Hv * p.dk + (4 * pc < p.dk ? 4 * pc : 0);
                 asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
-                             :: "r"(tc::smem_u32(gt + row * D + 4 * pc)), "l"(gsrc), "r"(row < L ? 16 : 0) : "memory");
+                             :: "r"(tc::smem_u32(gt + row * D + 4 * pc)), "l"(gsrc), "r"(ok ? 16 : 0) : "memory");
             }
         }
         asm volatile("cp.async.commit_group;" ::: "memory");
@@ -697,10 +711,10 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
                 const int r = tid & 63, which = tid >> 6;
                 const size_t tok = (size_t)ni.y + r;
                 if (r < ni.z) {
-                    if (which == 0) tc::prefetch_l2(kp + (tok * p.Hk + nh / grp) * D, D * 2);
-                    else if (which == 1) tc::prefetch_l2(qp + (tok * p.Hk + nh / grp) * D, D * 2);
-                    else if (which == 2) tc::prefetch_l2(vp + (tok * p.Hv + nh) * D, D * 2);
-                    else tc::prefetch_l2(p.gk + (tok * p.Hv + nh) * D, D * 4);
+                    if (which == 0) tc::prefetch_l2(kp + (tok * p.Hk + nh / grp) * p.dk, p.dk * 2);
+                    else if (which == 1) tc::prefetch_l2(qp + (tok * p.Hk + nh / grp) * p.dk, p.dk * 2);
+                    else if (which == 2) tc::prefetch_l2(vp + (tok * p.Hv + nh) * p.dk, p.dk * 2);
+                    else tc::prefetch_l2(p.gk + (tok * p.Hv + nh) * p.dk, p.dk * 4);
                 }
                 if (tid == 0) tc::prefetch_l2_span(bp + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 2);
             }
@@ -1020,7 +1034,8 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
             }
         __syncthreads();
         // V rows (cp.async) over the dead scratch, waited for after the solve
-        stage_rows_async<NT>(sm + S::kV, C, 0, vp + ((size_t)start * p.Hv + h) * D, (size_t)p.Hv * D, L, tid);
+        stage_rows_async<NT>(sm + S::kV, C, 0, vp + ((size_t)start * p.Hv + h) * p.dk, (size_t)p.Hv * p.dk, L,
+                             p.dk / 8, tid);
         asm volatile("cp.async.commit_group;" ::: "memory");
 
         // ---- Tm = (I + A)^{-1}; T'' = Tm diag(beta) as hi / lo over A ---------------
@@ -1186,9 +1201,12 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
     // Work unit: a whole sequence (mode 0) or one segment of G chunks of it
     // (modes 1 and 2; the summary pass runs two CTA sets, the transition from
     // the identity with U = 0 and the offset from zero).
-    const int hx = blockIdx.x % (p.Hv * NVB);
-    const bool transition = p.mode == 1 && blockIdx.x >= p.Hv * NVB;
-    const int h = hx / NVB, vb = hx % NVB, v0 = vb * BV;
+    // value blocks of the head that carry data: 4, or 2 for a 64-channel head
+    // (the operand images keep 4 U blocks per (chunk, head) either way)
+    const int nvb = p.dk / BV;
+    const int hx = blockIdx.x % (p.Hv * nvb);
+    const bool transition = p.mode == 1 && blockIdx.x >= p.Hv * nvb;
+    const int h = hx / nvb, vb = hx % nvb, v0 = vb * BV;
     int b, nc, c0, cs0 = 0, sg = 0;
     bool last = true;
     if (p.mode == 0) {
@@ -1305,7 +1323,8 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             for (int v = 0; v < 16; ++v) Sreg[v] = (v0 + vh + v == t) ? 1.f : 0.f;
         } else if (p.h0 && first) {
 #pragma unroll
-            for (int v = 0; v < 16; ++v) Sreg[v] = p.h0[(((size_t)b * p.Hv + h) * D + v0 + vh + v) * D + t];
+            for (int v = 0; v < 16; ++v)
+                Sreg[v] = t < p.dk ? p.h0[(((size_t)b * p.Hv + h) * p.dk + v0 + vh + v) * p.dk + t] : 0.f;
         } else {
 #pragma unroll
             for (int v = 0; v < 16; ++v) Sreg[v] = 0.f;
@@ -1439,8 +1458,10 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
 #pragma unroll
             for (int v = 0; v < 16; ++v) dst[(size_t)v * D] = Sreg[v];
         } else if (p.hT && last && !*abort_flag) {
+            if (t < p.dk) {
 #pragma unroll
-            for (int v = 0; v < 16; ++v) p.hT[(((size_t)b * p.Hv + h) * D + v0 + vh + v) * D + t] = Sreg[v];
+                for (int v = 0; v < 16; ++v) p.hT[(((size_t)b * p.Hv + h) * p.dk + v0 + vh + v) * p.dk + t] = Sreg[v];
+            }
         }
     } else if (warp >= 12) {
         // ------------------------------ output warps ------------------------------
@@ -1462,7 +1483,7 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                 for (int v = 0; v < BV; ++v) ov[v] = ld[v] + ld[BV + v];
                 const int cs = bos + c * C;
                 if (cs + i < eos) {
-                    uint4* dst = reinterpret_cast<uint4*>(op + ((size_t)(cs + i) * p.Hv + h) * D + v0);
+                    uint4* dst = reinterpret_cast<uint4*>(op + ((size_t)(cs + i) * p.Hv + h) * p.dk + v0);
 #pragma unroll
                     for (int u = 0; u < BV / 8; ++u)
                         dst[u] = make_uint4(tc::pack_bf16(p.scale * ov[8 * u], p.scale * ov[8 * u + 1]),
@@ -1664,6 +1685,8 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* w
     p.Rb = blob;
     p.err = device_error_word();
     p.N = a.N; p.Hk = a.Hk; p.Hv = a.Hv; p.scale = a.scale;
+    p.dk = a.K;
+    const unsigned nvb = (unsigned)(a.K / BV);  // value blocks per head in the chain
 
     if (w.seg_chunks > 0) {
         p.segs = reinterpret_cast<const int4*>(ws + w.off_segs);
@@ -1683,13 +1706,13 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* w
         if (w.seg_chunks == 0) {
             p.mode = 0;
             KernelTimer kt("chunk_chain", stream);
-            return launch_dependent(chain_kernel, dim3(a.Hv * NVB, a.N), dim3(512), (size_t)smc, stream, p);
+            return launch_dependent(chain_kernel, dim3(a.Hv * nvb, a.N), dim3(512), (size_t)smc, stream, p);
         }
         const unsigned segs = (unsigned)w.max_segs;
         {
             p.mode = 1;  // segment transitions and offsets
             KernelTimer kt("chunk_chain_summary", stream);
-            const cudaError_t e = launch_dependent(chain_kernel, dim3(2 * a.Hv * NVB, segs), dim3(512), (size_t)smc,
+            const cudaError_t e = launch_dependent(chain_kernel, dim3(2 * a.Hv * nvb, segs), dim3(512), (size_t)smc,
                                                    stream, p);
             if (e != cudaSuccess) return e;
         }
@@ -1702,7 +1725,7 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* w
         }
         p.mode = 2;  // segments from their start states, with the output
         KernelTimer kt("chunk_chain", stream);
-        return launch_dependent(chain_kernel, dim3(a.Hv * NVB, segs), dim3(512), (size_t)smc, stream, p);
+        return launch_dependent(chain_kernel, dim3(a.Hv * nvb, segs), dim3(512), (size_t)smc, stream, p);
     };
     const cudaError_t e = kda ? run(chunk_prep_kda_kernel, chunk_chain_kernel<true>, (int)KdaSmem::kTotal,
                                     ChainSmem<true>::kTotal, 2, kKdaThreads)

@@ -114,7 +114,9 @@ GDR_API int gdr_chunk_workspace_size(int N, int64_t T_total, int Hk, int Hv, int
  *   final_state    [N, Hv, V, K] fp32 (written), or NULL
  *   workspace      device scratch of at least gdr_chunk_workspace_size bytes,
  *                  256-byte aligned; contents need no initialisation
- * Supported: Hv % Hk == 0, K == V, K in {64, 128}.  Any finite g <= 0 is
+ * Supported: Hv % Hk == 0, K == V, K in {64, 128}.  bf16 inputs run on the
+ * tensor cores at both sizes (a 64-channel head as a 128-channel tile whose
+ * upper channels are zero), fp32 inputs on the CUDA cores.  Any finite g <= 0 is
  * accepted: every exponential formed is of an in-chunk difference
  * exp(gam_i - gam_j), i >= j (cuLA PR #113 review on exp(-prefix) overflow).
  *
@@ -130,8 +132,9 @@ GDR_API int gdr_chunk_workspace_size(int N, int64_t T_total, int Hk, int Hv, int
  * sequence, 64 tokens per step, and the scan costs about three chain passes
  * of work instead of one, so it wins while 12 * Hv * N is well under the
  * GPU's SM count (measured on GB300 with one 32768-token sequence: 5x at
- * Hv = 1, 2.5x at Hv = 4, 1.5x at Hv = 8, a loss at Hv = 16).  The caller decides; the flag always takes the scan where it
- * applies.  The workspace grows by about
+ * Hv = 1, 2.5x at Hv = 4, 1.5x at Hv = 8, a loss at Hv = 16).  The caller
+ * decides; the flag always takes the scan where it applies.  The workspace
+ * grows by about
  * 2 * (ceil(T_total / 64 / G) + N + 1) * Hv * K * K * 4 bytes, G the segment
  * length in chunks (at least 4 where sequences allow) that the library derives
  * from N, T_total and Hv.

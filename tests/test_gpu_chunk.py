@@ -96,6 +96,8 @@ CASES = [
     ([65, 1, 129, 63], 1, 4, "gk", (-0.3, 0.0), True, torch.bfloat16, 128),  # KDA GVA 4
     ([200, 7], 2, 4, "gk", (-2.0, 0.0), False, torch.bfloat16, 128),         # KDA adversarial
     ([100, 28], 2, 2, "g", (-1.0, 0.0), True, torch.float32, 64),
+    ([65, 1, 130, 64], 2, 4, "g", (-2.0, 0.0), True, torch.bfloat16, 64),   # bf16, 64 channels: tensor cores
+    ([130, 7, 64], 1, 2, "gk", (-0.5, 0.0), True, torch.bfloat16, 64),      # KDA, 64 channels
     ([130, 3], 1, 2, "gk", (-0.5, 0.0), True, torch.float32, 128),
 ]
 
@@ -276,3 +278,36 @@ def test_most_sequences_per_call():
                                   g=case.g[sl], scale=case.scale)
         check_out(o[sl].cpu(), ro, f"o of sequence {b}")
         check_state(sf[b:b + 1].cpu(), rs, f"final state of sequence {b}")
+
+
+def test_bf16_64_channels_run_on_the_tensor_cores():
+    """bf16 heads of 64 channels take the tensor-core kernels (128-channel
+    tiles, upper half zero), not the CUDA-core ones; GDR_CHUNK_SCAN is ignored
+    for them (bit-identical results); the in-library q/k normalisation too."""
+    case = workloads.chunk_case(65, [300, 40, 129], 2, 4, 64, 64, gate="g", g_range=(-1.0, 0.0), h0_std=0.1)
+    gdr.profile_read()
+    gdr.profile_enable(True)
+    o, sf = run_gpu(case)
+    o, sf = o.clone(), sf.clone()
+    o2, s2 = run_gpu(case, flags=gdr.GDR_CHUNK_SCAN)
+    torch.cuda.synchronize()
+    gdr.profile_enable(False)
+    names = set(gdr.profile_read())
+    assert {"chunk_prep", "chunk_chain"} <= names, names
+    assert not names & {"chunk_intra", "chunk_state", "chunk_out", "chunk_seg_scan"}, names
+    ro, rs = oracle_ref(case)
+    check_out(o.cpu(), ro, "o")
+    check_state(sf.cpu(), rs, "final state")
+    assert bits_equal(o, o2) and bits_equal(sf, s2)
+
+    gen = torch.Generator().manual_seed(66)
+    case.q = (torch.randn(case.q.shape, generator=gen) * 2.0).to(torch.bfloat16)
+    case.k = (torch.randn(case.k.shape, generator=gen) * 0.7).to(torch.bfloat16)
+    o3, s3 = run_gpu(case, flags=gdr.GDR_QK_L2NORM)
+    # the library stores the normalised rows in the input type: the oracle runs on them rounded to bf16
+    qn = torch.from_numpy(oracle.l2norm(case.q, 1e-6)).to(torch.bfloat16)
+    kn = torch.from_numpy(oracle.l2norm(case.k, 1e-6)).to(torch.bfloat16)
+    ro3, rs3 = oracle.tokenwise(qn, kn, case.v, case.beta, case.cu_seqlens, g=case.g,
+                                initial_state=case.initial_state, scale=case.scale)
+    check_out(o3.cpu(), ro3, "o (in-library q/k normalisation)")
+    check_state(s3.cpu(), rs3, "final state (in-library q/k normalisation)")
