@@ -1,4 +1,4 @@
-// Chunked prefill on the Blackwell tensor cores (bf16 inputs, K = V = 128).
+// Chunked prefill on the Blackwell tensor cores (bf16 inputs, K = V = 128, or 64 as zero-padded 128-channel tiles).
 //
 // Two kernels after the chunk metadata (three with the chunk-parallel scan):
 //
@@ -87,11 +87,6 @@ struct TcParams {
     unsigned char* Rb;   // [chunk][Hv][1 KB]
     unsigned int* err;
     int N, Hk, Hv;
-    // channels of K and V in global memory (64 or 128).  The kernels always
-    // work on 128-channel tiles; with 64 channels the upper half of every
-    // staged row is zero, so every product, image and state entry beyond
-    // channel 64 is zero, and the chain runs only the value blocks below 64.
-    int dk;
     float scale;
     // chunk-parallel scan: mode 0 = one chain CTA runs a whole sequence;
     // 1 = segment summaries: the first segment of a sequence from h0 with its
@@ -274,7 +269,14 @@ struct PrepSmem {
     static_assert(kT2l + kTile64x64 <= kTm, "T'' tiles overlap Tm");
 };
 
+// Every kernel here takes the channel count of K and V in global memory as
+// kDk (128, or 64).  The kernels always work on 128-channel tiles; with 64
+// channels the upper half of every staged row is zero, so every product,
+// image and state entry beyond channel 64 is zero, and the chain runs only
+// the value blocks below 64.
+template <int kDk>
 __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p) {
+    static_assert(kDk == 128 || kDk == 64, "K = V = 128 or 64");
     using S = PrepSmem;
     constexpr int NT = kPrepThreads;
     extern __shared__ unsigned char smem_raw[];
@@ -321,12 +323,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
         const int kh = h / grp;
 
         // ---- stage K, Q (as X) and V rows (cp.async), gates, beta -------------------
-        stage_rows_async<NT>(sm + S::kX, 2 * C, 0, kp + ((size_t)start * p.Hk + kh) * p.dk, (size_t)p.Hk * p.dk, L,
-                             p.dk / 8, tid);
-        stage_rows_async<NT>(sm + S::kX, 2 * C, C, qp + ((size_t)start * p.Hk + kh) * p.dk, (size_t)p.Hk * p.dk, L,
-                             p.dk / 8, tid);
-        stage_rows_async<NT>(sm + S::kV, C, 0, vp + ((size_t)start * p.Hv + h) * p.dk, (size_t)p.Hv * p.dk, L,
-                             p.dk / 8, tid);
+        stage_rows_async<NT>(sm + S::kX, 2 * C, 0, kp + ((size_t)start * p.Hk + kh) * kDk, (size_t)p.Hk * kDk, L,
+                             kDk / 8, tid);
+        stage_rows_async<NT>(sm + S::kX, 2 * C, C, qp + ((size_t)start * p.Hk + kh) * kDk, (size_t)p.Hk * kDk, L,
+                             kDk / 8, tid);
+        stage_rows_async<NT>(sm + S::kV, C, 0, vp + ((size_t)start * p.Hv + h) * kDk, (size_t)p.Hv * kDk, L,
+                             kDk / 8, tid);
         asm volatile("cp.async.commit_group;" ::: "memory");
         {
             const int nxt = item + (int)gridDim.x;
@@ -336,9 +338,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
                 const int r = tid & 63, which = tid >> 6;
                 const size_t tok = (size_t)ni.y + r;
                 if (r < ni.z) {
-                    if (which == 0) tc::prefetch_l2(kp + (tok * p.Hk + nh / grp) * p.dk, p.dk * 2);
-                    else if (which == 1) tc::prefetch_l2(qp + (tok * p.Hk + nh / grp) * p.dk, p.dk * 2);
-                    else if (which == 2) tc::prefetch_l2(vp + (tok * p.Hv + nh) * p.dk, p.dk * 2);
+                    if (which == 0) tc::prefetch_l2(kp + (tok * p.Hk + nh / grp) * kDk, kDk * 2);
+                    else if (which == 1) tc::prefetch_l2(qp + (tok * p.Hk + nh / grp) * kDk, kDk * 2);
+                    else if (which == 2) tc::prefetch_l2(vp + (tok * p.Hv + nh) * kDk, kDk * 2);
                 }
                 if (tid == 255) tc::prefetch_l2_span(p.g + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 4);
                 if (tid == 254) tc::prefetch_l2_span(bp + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 2);
@@ -635,7 +637,9 @@ struct KdaSmem {
     static_assert(kTotal <= 113 * 1024, "two CTAs per SM");
 };
 
+template <int kDk>
 __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams p) {
+    static_assert(kDk == 128 || kDk == 64, "K = V = 128 or 64");
     using S = KdaSmem;
     constexpr int NT = kKdaThreads;
     extern __shared__ unsigned char smem_raw[];
@@ -686,18 +690,18 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
 
         // ---- stage K, Q rows and the gate rows (cp.async); zero A and P; beta; warm L2
         //      for the next item ----------------------------------------------------------
-        stage_rows_async<NT>(sm + S::kX, 2 * C, 0, kp + ((size_t)start * p.Hk + kh) * p.dk, (size_t)p.Hk * p.dk, L,
-                             p.dk / 8, tid);
-        stage_rows_async<NT>(sm + S::kX, 2 * C, C, qp + ((size_t)start * p.Hk + kh) * p.dk, (size_t)p.Hk * p.dk, L,
-                             p.dk / 8, tid);
+        stage_rows_async<NT>(sm + S::kX, 2 * C, 0, kp + ((size_t)start * p.Hk + kh) * kDk, (size_t)p.Hk * kDk, L,
+                             kDk / 8, tid);
+        stage_rows_async<NT>(sm + S::kX, 2 * C, C, qp + ((size_t)start * p.Hk + kh) * kDk, (size_t)p.Hk * kDk, L,
+                             kDk / 8, tid);
         {
             // gk rows [64][128] fp32 into the scratch (rows >= L and channels
             // >= dk zero-filled: a zero log-decay on a zero channel)
-            const float* src = p.gk + ((size_t)start * p.Hv + h) * p.dk;
+            const float* src = p.gk + ((size_t)start * p.Hv + h) * kDk;
             for (int e = tid; e < C * (D / 4); e += NT) {
                 const int row = e >> 5, pc = e & 31;
-                const bool ok = row < L && 4 * pc < p.dk;
-                const float* gsrc = src + (size_t)(row < L ? row : 0) * p.Hv * p.dk + (4 * pc < p.dk ? 4 * pc : 0);
+                const bool ok = row < L && 4 * pc < kDk;
+                const float* gsrc = src + (size_t)(row < L ? row : 0) * p.Hv * kDk + (4 * pc < kDk ? 4 * pc : 0);
                 asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;"
                              :: "r"(tc::smem_u32(gt + row * D + 4 * pc)), "l"(gsrc), "r"(ok ? 16 : 0) : "memory");
             }
@@ -711,10 +715,10 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
                 const int r = tid & 63, which = tid >> 6;
                 const size_t tok = (size_t)ni.y + r;
                 if (r < ni.z) {
-                    if (which == 0) tc::prefetch_l2(kp + (tok * p.Hk + nh / grp) * p.dk, p.dk * 2);
-                    else if (which == 1) tc::prefetch_l2(qp + (tok * p.Hk + nh / grp) * p.dk, p.dk * 2);
-                    else if (which == 2) tc::prefetch_l2(vp + (tok * p.Hv + nh) * p.dk, p.dk * 2);
-                    else tc::prefetch_l2(p.gk + (tok * p.Hv + nh) * p.dk, p.dk * 4);
+                    if (which == 0) tc::prefetch_l2(kp + (tok * p.Hk + nh / grp) * kDk, kDk * 2);
+                    else if (which == 1) tc::prefetch_l2(qp + (tok * p.Hk + nh / grp) * kDk, kDk * 2);
+                    else if (which == 2) tc::prefetch_l2(vp + (tok * p.Hv + nh) * kDk, kDk * 2);
+                    else tc::prefetch_l2(p.gk + (tok * p.Hv + nh) * kDk, kDk * 4);
                 }
                 if (tid == 0) tc::prefetch_l2_span(bp + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 2);
             }
@@ -1034,8 +1038,8 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
             }
         __syncthreads();
         // V rows (cp.async) over the dead scratch, waited for after the solve
-        stage_rows_async<NT>(sm + S::kV, C, 0, vp + ((size_t)start * p.Hv + h) * p.dk, (size_t)p.Hv * p.dk, L,
-                             p.dk / 8, tid);
+        stage_rows_async<NT>(sm + S::kV, C, 0, vp + ((size_t)start * p.Hv + h) * kDk, (size_t)p.Hv * kDk, L,
+                             kDk / 8, tid);
         asm volatile("cp.async.commit_group;" ::: "memory");
 
         // ---- Tm = (I + A)^{-1}; T'' = Tm diag(beta) as hi / lo over A ---------------
@@ -1169,8 +1173,9 @@ __device__ __forceinline__ uint32_t chain_bar_count(int i) {
     return i == kD1Full ? 2u : (i == kEmpty0 || i == kEmpty1) ? 3u : 1u;
 }
 
-template <bool kKDA>
+template <bool kKDA, int kDk>
 __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
+    static_assert(kDk == 128 || kDk == 64, "K = V = 128 or 64");
     using S = ChainSmem<kKDA>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1203,7 +1208,7 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
     // the identity with U = 0 and the offset from zero).
     // value blocks of the head that carry data: 4, or 2 for a 64-channel head
     // (the operand images keep 4 U blocks per (chunk, head) either way)
-    const int nvb = p.dk / BV;
+    constexpr int nvb = kDk / BV;
     const int hx = blockIdx.x % (p.Hv * nvb);
     const bool transition = p.mode == 1 && blockIdx.x >= p.Hv * nvb;
     const int h = hx / nvb, vb = hx % nvb, v0 = vb * BV;
@@ -1324,7 +1329,7 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
         } else if (p.h0 && first) {
 #pragma unroll
             for (int v = 0; v < 16; ++v)
-                Sreg[v] = t < p.dk ? p.h0[(((size_t)b * p.Hv + h) * p.dk + v0 + vh + v) * p.dk + t] : 0.f;
+                Sreg[v] = t < kDk ? p.h0[(((size_t)b * p.Hv + h) * kDk + v0 + vh + v) * kDk + t] : 0.f;
         } else {
 #pragma unroll
             for (int v = 0; v < 16; ++v) Sreg[v] = 0.f;
@@ -1458,9 +1463,9 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
 #pragma unroll
             for (int v = 0; v < 16; ++v) dst[(size_t)v * D] = Sreg[v];
         } else if (p.hT && last && !*abort_flag) {
-            if (t < p.dk) {
+            if (t < kDk) {
 #pragma unroll
-                for (int v = 0; v < 16; ++v) p.hT[(((size_t)b * p.Hv + h) * p.dk + v0 + vh + v) * p.dk + t] = Sreg[v];
+                for (int v = 0; v < 16; ++v) p.hT[(((size_t)b * p.Hv + h) * kDk + v0 + vh + v) * kDk + t] = Sreg[v];
             }
         }
     } else if (warp >= 12) {
@@ -1483,7 +1488,7 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                 for (int v = 0; v < BV; ++v) ov[v] = ld[v] + ld[BV + v];
                 const int cs = bos + c * C;
                 if (cs + i < eos) {
-                    uint4* dst = reinterpret_cast<uint4*>(op + ((size_t)(cs + i) * p.Hv + h) * p.dk + v0);
+                    uint4* dst = reinterpret_cast<uint4*>(op + ((size_t)(cs + i) * p.Hv + h) * kDk + v0);
 #pragma unroll
                     for (int u = 0; u < BV / 8; ++u)
                         dst[u] = make_uint4(tc::pack_bf16(p.scale * ov[8 * u], p.scale * ov[8 * u + 1]),
@@ -1685,7 +1690,6 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* w
     p.Rb = blob;
     p.err = device_error_word();
     p.N = a.N; p.Hk = a.Hk; p.Hv = a.Hv; p.scale = a.scale;
-    p.dk = a.K;
     const unsigned nvb = (unsigned)(a.K / BV);  // value blocks per head in the chain
 
     if (w.seg_chunks > 0) {
@@ -1727,10 +1731,14 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* w
         KernelTimer kt("chunk_chain", stream);
         return launch_dependent(chain_kernel, dim3(a.Hv * nvb, segs), dim3(512), (size_t)smc, stream, p);
     };
-    const cudaError_t e = kda ? run(chunk_prep_kda_kernel, chunk_chain_kernel<true>, (int)KdaSmem::kTotal,
-                                    ChainSmem<true>::kTotal, 2, kKdaThreads)
-                              : run(chunk_prep_kernel, chunk_chain_kernel<false>, (int)PrepSmem::kTotal,
-                                    ChainSmem<false>::kTotal, 2, kPrepThreads);
+    const bool half = a.K == 64;
+    const cudaError_t e =
+        kda ? run(half ? chunk_prep_kda_kernel<64> : chunk_prep_kda_kernel<128>,
+                  half ? chunk_chain_kernel<true, 64> : chunk_chain_kernel<true, 128>, (int)KdaSmem::kTotal,
+                  ChainSmem<true>::kTotal, 2, kKdaThreads)
+            : run(half ? chunk_prep_kernel<64> : chunk_prep_kernel<128>,
+                  half ? chunk_chain_kernel<false, 64> : chunk_chain_kernel<false, 128>, (int)PrepSmem::kTotal,
+                  ChainSmem<false>::kTotal, 2, kPrepThreads);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

@@ -311,3 +311,18 @@ def test_bf16_64_channels_run_on_the_tensor_cores():
                                 initial_state=case.initial_state, scale=case.scale)
     check_out(o3.cpu(), ro3, "o (in-library q/k normalisation)")
     check_state(s3.cpu(), rs3, "final state (in-library q/k normalisation)")
+
+
+def test_state_error_matches_the_split_model():
+    """The kernels' final-state error against the oracle is the one the CPU
+    model of their bf16 hi / lo split products predicts (within 3x): no
+    rounding beyond the modelled split terms, on weak and strong decays."""
+    from tests.test_split_terms import ALL_TERMS, _cases, model_final_states, rel_l2
+    for name, case in _cases().items():
+        _, sf = run_gpu(case)
+        _, rs = oracle_ref(case)
+        rs = np.asarray(rs)
+        e_gpu = rel_l2(sf.cpu().double().numpy(), rs)
+        e_model = rel_l2(model_final_states(case, ALL_TERMS), rs)
+        print(f"{name}: GPU {e_gpu:.2e}, model {e_model:.2e}")
+        assert e_gpu <= 3 * e_model, f"{name}: GPU {e_gpu:.2e} against the model's {e_model:.2e}"

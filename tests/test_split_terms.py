@@ -1,0 +1,218 @@
+"""Which bf16 hi / lo split products the fp32 state bound needs.
+
+The tensor-core prefill carries the fp32 state through bf16 products: every
+fp32 operand x that meets a contraction is written as x_hi + x_lo (x_hi the
+bf16 rounding of x, x_lo that of the remainder), the products accumulate in
+fp32, and the cross term lo x lo is never formed.  Per 64-token chunk the
+kernels form
+
+  prep   Tm = (I + A)^{-1} in fp32;  W = (Tm diag(beta e^gam)) K  and
+         U = (Tm diag(beta)) V with the fp32 factor split (2 terms, K and V
+         exact bf16); for per-channel gates W = (Tm diag(beta)) (K o e^Gam) with
+         both factors split (3 terms);
+  chain  N = U - W S^T  (3 terms: W_hi S_hi, W_hi S_lo, W_lo S_hi);
+         S <- e^{gam_L} S + K^T (f o N)  (2 terms: N'_hi, N'_lo; K exact), or,
+         per-channel, S <- S diag(e^{Gam_L}) + Kd^T N with Kd = K o e^{Gam_L - Gam}
+         (3 terms: Kd_hi N_hi, Kd_hi N_lo, Kd_lo N_hi).
+
+This file models that rounding on the CPU (numpy, bf16 round-to-nearest-even,
+fp32 results) and measures the final state against the oracle.  The model is
+test infrastructure, like the oracle, and shares no code with the CUDA path.
+What it shows (the final-state bound is rel-L2 <= 1e-4):
+
+- with every term the state stays near 5e-6 (20x under the bound), with
+  strong decays (g ~ U[-2, 0]) and weak ones (g ~ U[-0.01, 0]) alike;
+- dropping any one term (a cross term of N, the lo half of N in the update,
+  Kd_lo, the lo half of Tm, the lo half of K o e^Gam) breaks the bound when
+  the decay is weak: the state then remembers many chunks, and N = U - W S^T
+  is a small difference of large terms;
+- with strong decay the cross terms of N and the lo half of Tm could go (the
+  state forgets within a chunk or two), but a kernel cannot choose terms by
+  gates it has not read yet, so all of them stay.
+"""
+import numpy as np
+import pytest
+import scipy.linalg as sla
+import torch
+
+import oracle
+from gated_delta_rule_37_gb300 import workloads
+
+ALL_TERMS = ("ws_hl", "ws_lh", "upd_lo", "kd_lo", "t_lo", "kg_lo")
+STATE_BOUND = 1e-4
+
+
+def bf16(x):
+    """Round to bf16 (round to nearest, ties to even), returned as float64."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000).astype(np.uint32)
+    return r.view(np.float32).astype(np.float64)
+
+
+def f32(x):
+    return np.asarray(x, dtype=np.float32).astype(np.float64)
+
+
+def split(x):
+    x = f32(x)
+    hi = bf16(x)
+    return hi, bf16(x - hi)
+
+
+def model_state(q, k, v, beta, g, gk, S0, terms, rounding=True):
+    """Final state [V, K] of one (sequence, value-head) through the chunked WY
+    form, with the kernels' bf16 split products when `rounding` (and exact
+    float64 arithmetic otherwise).  `terms` names the split products kept."""
+    T = q.shape[0]
+    keep = set(terms)
+    S = f32(S0) if rounding else np.array(S0, dtype=np.float64)
+    for c0 in range(0, T, 64):
+        c1 = min(c0 + 64, T)
+        L = c1 - c0
+        K_, V_, b = k[c0:c1], v[c0:c1], beta[c0:c1]
+        cdt = np.float32 if rounding else np.float64  # the kernels' cumsum runs in fp32
+        if gk is None:
+            gam = np.cumsum(g[c0:c1].astype(cdt), dtype=cdt).astype(np.float64)
+            A = np.tril(b[:, None] * np.exp(gam[:, None] - gam[None, :]) * (K_ @ K_.T), -1)
+            Kg = K_ * np.exp(gam)[:, None]
+            decay_L = np.full(K_.shape[1], np.exp(gam[-1]))
+            f = np.exp(gam[-1] - gam)
+        else:
+            Gam = np.cumsum(gk[c0:c1].astype(cdt), axis=0, dtype=cdt).astype(np.float64)
+            A = np.zeros((L, L))
+            for i in range(1, L):
+                A[i, :i] = b[i] * (K_[i] * K_[:i] * np.exp(Gam[i] - Gam[:i])).sum(1)
+            Kg = K_ * np.exp(Gam)
+            decay_L = np.exp(Gam[-1])
+            Kd = K_ * np.exp(Gam[-1] - Gam)
+        eye = np.eye(L)
+        if not rounding:
+            Tm = np.linalg.solve(eye + A, eye)
+            W = Tm @ (b[:, None] * Kg)
+            U = Tm @ (b[:, None] * V_)
+            N = U - W @ S.T
+            if gk is None:
+                S = decay_L[0] * S + (f[:, None] * N).T @ K_
+            else:
+                S = S * decay_L[None, :] + N.T @ Kd
+            continue
+        Tm = sla.solve_triangular((eye + f32(A)).astype(np.float32), np.eye(L, dtype=np.float32),
+                                  lower=True).astype(np.float64)
+        Tb_hi, Tb_lo = split(Tm * b[None, :])
+        t_lo = Tb_lo if "t_lo" in keep else np.zeros_like(Tb_lo)
+        if gk is None:
+            Tw_hi, Tw_lo = split(f32(Tm) * (b * np.exp(gam))[None, :])
+            W = f32(Tw_hi @ K_ + (Tw_lo @ K_ if "t_lo" in keep else 0.0))
+        else:
+            Kg_hi, Kg_lo = split(Kg)
+            W = f32(Tb_hi @ Kg_hi + (Tb_hi @ Kg_lo if "kg_lo" in keep else 0.0) + t_lo @ Kg_hi)
+        U = f32(Tb_hi @ V_ + t_lo @ V_)
+        W_hi, W_lo = split(W)
+        S_hi, S_lo = split(S)
+        WS = W_hi @ S_hi.T
+        if "ws_hl" in keep:
+            WS = WS + W_hi @ S_lo.T
+        if "ws_lh" in keep:
+            WS = WS + W_lo @ S_hi.T
+        N = f32(U - f32(WS))
+        if gk is None:
+            n_hi, n_lo = split(f[:, None] * N)
+            upd = (n_hi + (n_lo if "upd_lo" in keep else 0.0)).T @ K_
+            S = f32(f32(decay_L[0] * S) + f32(upd))
+        else:
+            Kd_hi, Kd_lo = split(Kd)
+            n_hi, n_lo = split(N)
+            upd = (n_hi + (n_lo if "upd_lo" in keep else 0.0)).T @ Kd_hi
+            if "kd_lo" in keep:
+                upd = upd + n_hi.T @ Kd_lo
+            S = f32(f32(S * f32(decay_L)[None, :]) + f32(upd))
+    return S
+
+
+def model_final_states(case, terms, rounding=True):
+    """[N, Hv, V, K] final states of a ChunkCase through the model."""
+    q, k, v = (t.double().numpy() for t in (case.q, case.k, case.v))
+    beta = case.beta.double().numpy()
+    g = None if case.g is None else case.g.double().numpy()
+    gk = None if case.gk is None else case.gk.double().numpy()
+    cu = case.cu_seqlens.tolist()
+    Hk, Hv, K, V = q.shape[1], v.shape[1], q.shape[2], v.shape[2]
+    out = np.zeros((case.N, Hv, V, K))
+    for n in range(case.N):
+        s0, s1 = cu[n], cu[n + 1]
+        for h in range(Hv):
+            kh = h // (Hv // Hk)
+            S0 = np.zeros((V, K)) if case.initial_state is None else case.initial_state[n, h].double().numpy()
+            out[n, h] = model_state(q[s0:s1, kh], k[s0:s1, kh], v[s0:s1, h], beta[s0:s1, h],
+                                    None if g is None else g[s0:s1, h], None if gk is None else gk[s0:s1, h],
+                                    S0, terms, rounding)
+    return out
+
+
+def rel_l2(a, b):
+    return float(np.linalg.norm((a - b).ravel()) / np.linalg.norm(np.asarray(b).ravel()))
+
+
+def _cases():
+    return {
+        # weak decays: the state remembers tens of chunks
+        "scalar gate, g ~ U[-0.01, 0]": workloads.chunk_case(5, [2048], 1, 1, 128, 128, gate="g",
+                                                              g_range=(-0.01, 0.0), h0_std=0.1),
+        "channel gate, gk ~ U[-0.01, 0]": workloads.chunk_case(7, [2048], 1, 1, 128, 128, gate="gk",
+                                                                g_range=(-0.01, 0.0), h0_std=0.1),
+        # strong decays, ragged sequences
+        "scalar gate, g ~ U[-2, 0], ragged": workloads.chunk_case(9, [65, 700, 130], 1, 1, 128, 128, gate="g",
+                                                                   g_range=(-2.0, 0.0), h0_std=0.1),
+    }
+
+
+@pytest.fixture(scope="module")
+def cases():
+    out = {}
+    for name, case in _cases().items():
+        _, rs = oracle.tokenwise(case.q, case.k, case.v, case.beta, case.cu_seqlens, g=case.g, gk=case.gk,
+                                 initial_state=case.initial_state, scale=case.scale)
+        out[name] = (case, np.asarray(rs))
+    return out
+
+
+def test_bf16_rounding_matches_torch():
+    """The model's bf16 rounding is torch's (round to nearest, ties to even),
+    over a wide range of magnitudes and on exact ties."""
+    gen = torch.Generator().manual_seed(11)
+    x = torch.randn(100000, generator=gen) * torch.exp(torch.randn(100000, generator=gen) * 8)
+    ties = torch.tensor([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8), 2.0 ** -100 * (1 + 2.0 ** -8)])
+    x = torch.cat([x, ties])
+    want = x.to(torch.bfloat16).double().numpy()
+    assert np.array_equal(bf16(x.numpy()), want)
+    hi, lo = split(x.numpy())
+    assert np.array_equal(hi, want)
+    assert np.all(np.abs(hi + lo - x.double().numpy()) <= np.abs(x.double().numpy()) * 2.0 ** -16)
+
+
+def test_model_algebra_is_the_recurrence(cases):
+    """Without rounding the model's chunked form is the token-by-token
+    recurrence (the oracle) to float64 precision."""
+    for name, (case, rs) in cases.items():
+        S = model_final_states(case, ALL_TERMS, rounding=False)
+        assert rel_l2(S, rs) < 1e-12, name
+
+
+def test_kept_terms_meet_the_state_bound(cases):
+    for name, (case, rs) in cases.items():
+        e = rel_l2(model_final_states(case, ALL_TERMS), rs)
+        assert e < STATE_BOUND / 10, f"{name}: {e:.2e}"
+
+
+@pytest.mark.parametrize("dropped", ALL_TERMS)
+def test_every_split_term_is_needed(cases, dropped):
+    """Without any one of the kept split products some workload's final state
+    leaves the 1e-4 bound (the weak-decay ones, by a factor of 4 or more)."""
+    terms = [t for t in ALL_TERMS if t != dropped]
+    errs = {}
+    for name, (case, rs) in cases.items():
+        if dropped in ("kd_lo", "kg_lo") and case.gk is None:
+            continue
+        errs[name] = rel_l2(model_final_states(case, terms), rs)
+    assert max(errs.values()) > 4 * STATE_BOUND, errs
