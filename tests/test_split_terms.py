@@ -9,7 +9,8 @@ kernels form
   prep   Tm = (I + A)^{-1} in fp32;  W = (Tm diag(beta e^gam)) K  and
          U = (Tm diag(beta)) V with the fp32 factor split (2 terms, K and V
          exact bf16); for per-channel gates W = (Tm diag(beta)) (K o e^Gam) with
-         both factors split (3 terms);
+         both factors split (3 terms), and A from pivoted products of decayed
+         keys, both split (3 terms, see pivoted_A);
   chain  N = U - W S^T  (3 terms: W_hi S_hi, W_hi S_lo, W_lo S_hi);
          S <- e^{gam_L} S + K^T (f o N)  (2 terms: N'_hi, N'_lo; K exact), or,
          per-channel, S <- S diag(e^{Gam_L}) + Kd^T N with Kd = K o e^{Gam_L - Gam}
@@ -23,7 +24,8 @@ What it shows (the final-state bound is rel-L2 <= 1e-4):
 - with every term the state stays near 5e-6 (20x under the bound), with
   strong decays (g ~ U[-2, 0]) and weak ones (g ~ U[-0.01, 0]) alike;
 - dropping any one term (a cross term of N, the lo half of N in the update,
-  Kd_lo, the lo half of Tm, the lo half of K o e^Gam) breaks the bound when
+  Kd_lo, the lo half of Tm, the lo half of K o e^Gam, the lo half of the
+  pivoted left operand of A) breaks the bound when
   the decay is weak: the state then remembers many chunks, and N = U - W S^T
   is a small difference of large terms;
 - with strong decay the cross terms of N and the lo half of Tm could go (the
@@ -38,7 +40,7 @@ import torch
 import oracle
 from gated_delta_rule_37_gb300 import workloads
 
-ALL_TERMS = ("ws_hl", "ws_lh", "upd_lo", "kd_lo", "t_lo", "kg_lo")
+ALL_TERMS = ("ws_hl", "ws_lh", "upd_lo", "kd_lo", "t_lo", "kg_lo", "a_lo")
 STATE_BOUND = 1e-4
 
 
@@ -58,6 +60,33 @@ def split(x):
     x = f32(x)
     hi = bf16(x)
     return hi, bf16(x - hi)
+
+
+def pivoted_A(K_, Gam, b, keep):
+    """A_ij = b_i sum_c k_i[c] k_j[c] e^{Gam_i[c] - Gam_j[c]} (j < i) the way the
+    per-channel prep forms it: the pairs across the halves of each 2h-token
+    block (h = 32, 16, 8, 4) from operands decayed around the pivot p = first
+    token of the upper half, left k_i e^{Gam_i - Gam_p} and right
+    k_j e^{Gam_p - Gam_j} (both rounded to fp32, split hi / lo, products
+    L_hi R_hi + L_hi R_lo + L_lo R_hi); the pairs inside a 4-token block summed
+    in fp32."""
+    L = K_.shape[0]
+    A = np.zeros((L, L))
+    for h in (32, 16, 8, 4):
+        for p in range(h, L, 2 * h):
+            i0, i1, j0 = p, min(p + h, L), p - h
+            left = f32(K_[i0:i1] * np.exp(Gam[i0:i1] - Gam[p]))
+            right = f32(K_[j0:p] * np.exp(Gam[p] - Gam[j0:p]))
+            l_hi, l_lo = split(left)
+            r_hi, r_lo = split(right)
+            blk = l_hi @ r_hi.T + l_hi @ r_lo.T
+            if "a_lo" in keep:
+                blk = blk + l_lo @ r_hi.T
+            A[i0:i1, j0:p] = f32(blk)
+    for i in range(L):
+        for j in range(i - i % 4, i):
+            A[i, j] = f32((K_[i] * K_[j] * np.exp(Gam[i] - Gam[j])).sum())
+    return f32(b[:, None] * A)
 
 
 def model_state(q, k, v, beta, g, gk, S0, terms, rounding=True):
@@ -80,9 +109,12 @@ def model_state(q, k, v, beta, g, gk, S0, terms, rounding=True):
             f = np.exp(gam[-1] - gam)
         else:
             Gam = np.cumsum(gk[c0:c1].astype(cdt), axis=0, dtype=cdt).astype(np.float64)
-            A = np.zeros((L, L))
-            for i in range(1, L):
-                A[i, :i] = b[i] * (K_[i] * K_[:i] * np.exp(Gam[i] - Gam[:i])).sum(1)
+            if rounding:
+                A = pivoted_A(K_, Gam, b, keep)
+            else:
+                A = np.zeros((L, L))
+                for i in range(1, L):
+                    A[i, :i] = b[i] * (K_[i] * K_[:i] * np.exp(Gam[i] - Gam[:i])).sum(1)
             Kg = K_ * np.exp(Gam)
             decay_L = np.exp(Gam[-1])
             Kd = K_ * np.exp(Gam[-1] - Gam)
@@ -212,7 +244,7 @@ def test_every_split_term_is_needed(cases, dropped):
     terms = [t for t in ALL_TERMS if t != dropped]
     errs = {}
     for name, (case, rs) in cases.items():
-        if dropped in ("kd_lo", "kg_lo") and case.gk is None:
+        if dropped in ("kd_lo", "kg_lo", "a_lo") and case.gk is None:
             continue
         errs[name] = rel_l2(model_final_states(case, terms), rs)
     assert max(errs.values()) > 4 * STATE_BOUND, errs
