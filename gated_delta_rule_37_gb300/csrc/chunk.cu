@@ -84,6 +84,7 @@ ChunkWorkspace chunk_workspace_layout(int N, int64_t T, int Hk, int Hv, int K, i
         w.off_blobs = take(chunk_tc_blob_bytes(w.max_chunks, Hk, Hv, gate_kind == 1));
         // GDR_CHUNK_SCAN (>= 1): 128-channel heads only (the flag is ignored otherwise)
         w.seg_chunks = ((flags & 0x20) && K == 128) ? chunk_scan_segment(N, T, Hv) : 0;
+        w.local_meta = w.seg_chunks == 0 && N <= kLocalMetaSeqs;
         if (w.seg_chunks > 0) {
             w.max_segs = (w.max_chunks + w.seg_chunks - 1) / w.seg_chunks + N;
             w.off_segs = take(16 * (size_t)w.max_segs);
@@ -113,6 +114,10 @@ namespace {
 // ---------------------------------------------------------------------------
 // A malformed cu_seqlens (cu[0] != 0, a decreasing entry, cu[N] != T) makes
 // the chunk count 0 and meta[1] = 0, so the later kernels touch no memory.
+// Below kMetaSmemSeqs sequences the offsets also go to shared memory and the
+// chunk table is written with one thread per chunk (its sequence found by
+// binary search over the offsets), so one long sequence does not leave its
+// table to a single thread; beyond, one thread per sequence writes its chunks.
 // Also writes order[]: sequence indices by decreasing length (ties by index),
 // the longest-first launch order of the per-sequence kernels (N <= 4096;
 // identity beyond).
@@ -120,6 +125,7 @@ namespace {
 // of G chunks (the last one shorter): segs[] = (sequence, first chunk within
 // the sequence, chunk count, 1 if it is the sequence's last segment),
 // segoff[b] = first segment of sequence b, meta[2] = the segment count.
+constexpr int kMetaSmemSeqs = 4096;
 __global__ void __launch_bounds__(1024) chunk_meta_kernel(const int32_t* __restrict__ cu, int N,
                                                           int64_t T, int* __restrict__ meta,
                                                           int* __restrict__ offsets,
@@ -128,6 +134,7 @@ __global__ void __launch_bounds__(1024) chunk_meta_kernel(const int32_t* __restr
                                                           int* __restrict__ segoff) {
     __shared__ int warp_sum[32];
     __shared__ int seg_sum[32];
+    __shared__ int s_off[kMetaSmemSeqs + 1];
     __shared__ int bad;
     // the next kernel, if launched as a dependent, may start its prologue now
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -170,11 +177,34 @@ __global__ void __launch_bounds__(1024) chunk_meta_kernel(const int32_t* __restr
         meta[1] = 1;
         offsets[N] = warp_sum[31];
     }
-    for (int b = b0; b < b1; ++b) {
-        offsets[b] = c;
-        const int bos = cu[b], len = cu[b + 1] - bos;
-        for (int s = 0; s < len; s += kChunk, ++c)
-            table[c] = make_int4(b, bos + s, min(kChunk, len - s), 0);
+    if (N < kMetaSmemSeqs) {
+        // offsets into shared memory, then the chunk table with one thread per
+        // chunk (its sequence by binary search over the offsets)
+        for (int b = b0; b < b1; ++b) {
+            offsets[b] = c;
+            s_off[b] = c;
+            c += (cu[b + 1] - cu[b] + kChunk - 1) / kChunk;
+        }
+        if (tid == 0) s_off[N] = warp_sum[31];
+        __syncthreads();
+        const int total = warp_sum[31];
+        for (int ci = tid; ci < total; ci += blockDim.x) {
+            int lo = 0, hi = N - 1;  // the last sequence whose first chunk is <= ci
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_off[mid] <= ci) lo = mid;
+                else hi = mid - 1;
+            }
+            const int bos = cu[lo], len = cu[lo + 1] - bos, s = (ci - s_off[lo]) * kChunk;
+            table[ci] = make_int4(lo, bos + s, min(kChunk, len - s), 0);
+        }
+    } else {
+        for (int b = b0; b < b1; ++b) {
+            offsets[b] = c;
+            const int bos = cu[b], len = cu[b + 1] - bos;
+            for (int s = 0; s < len; s += kChunk, ++c)
+                table[c] = make_int4(b, bos + s, min(kChunk, len - s), 0);
+        }
     }
     if (G > 0) {
         // the same block-wide exclusive scan over the per-thread segment counts
@@ -508,7 +538,7 @@ cudaError_t launch_chunk_t(const ChunkArgs& a, cudaStream_t stream) {
     p.Vn = reinterpret_cast<float*>(ws + w.off_vn);
     p.Hk = a.Hk; p.Hv = a.Hv; p.scale = a.scale;
 
-    {
+    if (!w.local_meta) {
         KernelTimer kt("chunk_meta", stream);
         chunk_meta_kernel<<<1, 1024, 0, stream>>>(a.cu_seqlens, a.N, a.T, reinterpret_cast<int*>(ws + w.off_meta),
                                                   reinterpret_cast<int*>(ws + w.off_offsets),

@@ -76,10 +76,17 @@ struct TcParams {
     void* o;
     float* hT;
     const int32_t* cu;
-    const int* meta;
-    const int* offsets;
+    // chunk metadata: [0] chunk count, [1] 1 if cu_seqlens is well formed,
+    // [2] segment count; per-sequence first chunk; chunk table; sequences by
+    // decreasing length.  Written by the metadata kernel, or, with local_meta,
+    // by CTA 0 of the prep kernel (which then forms its own item map and
+    // leaves the table unwritten).
+    int* meta;
+    int* offsets;
     const int4* table;
-    const int* order;
+    int* order;
+    int local_meta;
+    int64_t T;
     unsigned char* Xw;   // [chunk][Hv][32 KB]: k128 128 rows = [W_hi ; Qd]
     unsigned char* Ub;   // [chunk][Hv][NVB][8 KB]
     unsigned char* Yw;   // [chunk][Hv][24 KB]: k128 128 rows = [W_lo ; P] (column block 1: W_lo only)
@@ -103,6 +110,78 @@ struct TcParams {
 
 __device__ __forceinline__ void raise_error(const TcParams& p, unsigned code) {
     atomicOr(p.err, code);
+}
+
+// ---------------------------------------------------------------------------
+// Chunk metadata of a call with at most kLocalMetaSeqs sequences, formed by
+// each prep CTA in shared memory instead of by the metadata kernel (one launch
+// fewer ahead of the prep): cu_seqlens and the first chunk of every sequence.
+// A malformed cu_seqlens (cu[0] != 0, a decreasing entry, cu[N] != T) gives
+// no chunks.  CTA 0 also writes what the chain kernel reads: the chunk count
+// and validity, the per-sequence first chunks and the longest-first order
+// (ties by index).
+// ---------------------------------------------------------------------------
+struct LocalMeta {
+    int total;  // chunks of the call (0: malformed cu_seqlens)
+    int valid;  // cu_seqlens well formed
+    int pad[2];
+    int cu[kLocalMetaSeqs + 1];
+    int off[kLocalMetaSeqs + 1];
+};
+
+template <int NT>
+__device__ void local_meta_build(const TcParams& p, LocalMeta& m, int tid) {
+    static_assert(NT > kLocalMetaSeqs, "one thread per cu_seqlens entry");
+    if (tid <= p.N) m.cu[tid] = p.cu[tid];
+    __syncthreads();
+    if (tid == 0) {
+        bool bad = m.cu[0] != 0 || (int64_t)m.cu[p.N] != p.T;
+        int c = 0;
+        for (int b = 0; b < p.N; ++b) {
+            const int len = m.cu[b + 1] - m.cu[b];
+            bad = bad || len < 0;
+            m.off[b] = c;
+            c += len > 0 ? (len + C - 1) / C : 0;
+        }
+        m.off[p.N] = c;
+        m.total = bad ? 0 : c;
+        m.valid = bad ? 0 : 1;
+        if (blockIdx.x == 0) {
+            p.meta[0] = m.total;
+            p.meta[1] = bad ? 0 : 1;
+            p.meta[2] = 0;
+        }
+    }
+    __syncthreads();
+    if (blockIdx.x == 0 && m.valid) {
+        if (tid <= p.N) p.offsets[tid] = m.off[tid];
+        if (tid < p.N) {
+            const int lb = m.cu[tid + 1] - m.cu[tid];
+            int rank = 0;
+            for (int j = 0; j < p.N; ++j) {
+                const int lj = m.cu[j + 1] - m.cu[j];
+                rank += (lj > lb) || (lj == lb && j < tid);
+            }
+            p.order[rank] = tid;
+        }
+    }
+}
+
+// (first token, length) of chunk ci: from the chunk table, or with local
+// metadata from the sequence found by binary search over the first chunks.
+__device__ __forceinline__ int2 chunk_rows(const TcParams& p, const LocalMeta& m, int ci) {
+    if (!p.local_meta) {
+        const int4 e = p.table[ci];
+        return make_int2(e.y, e.z);
+    }
+    int lo = 0, hi = p.N - 1;  // the last sequence whose first chunk is <= ci
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (m.off[mid] <= ci) lo = mid;
+        else hi = mid - 1;
+    }
+    const int start = m.cu[lo] + (ci - m.off[lo]) * C;
+    return make_int2(start, min(C, m.cu[lo + 1] - start));
 }
 
 // ---------------------------------------------------------------------------
@@ -265,7 +344,8 @@ struct PrepSmem {
     static constexpr uint32_t kGam = (kZ + 4 * 256 * 4 + 1023) & ~1023u;  // fp32 [64] gate cumsum
     static constexpr uint32_t kBeta = kGam + C * 4;
     static constexpr uint32_t kBar = kBeta + C * 4;
-    static constexpr uint32_t kTotal = kBar + 64 + 1024;  // + alignment slack
+    static constexpr uint32_t kMeta = kBar + 64;          // LocalMeta
+    static constexpr uint32_t kTotal = kMeta + sizeof(LocalMeta) + 1024;  // + alignment slack
     static_assert(kT2l + kTile64x64 <= kTm, "T'' tiles overlap Tm");
 };
 
@@ -314,12 +394,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
     uint32_t ph0 = 0;  // parity of the next completion of bar0
     tc::grid_dep_wait();    // the chunk table comes from the metadata kernel
     tc::grid_dep_launch();  // the chain kernel may start its prologue on free SMs
-    const int nitems = p.meta[0] * p.Hv;
+    LocalMeta& lm = *reinterpret_cast<LocalMeta*>(sm + S::kMeta);
+    if (p.local_meta) local_meta_build<NT>(p, lm, tid);
+    const int nitems = (p.local_meta ? lm.total : p.meta[0]) * p.Hv;
 
     for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
         const int chunk = item / p.Hv, h = item - chunk * p.Hv;
-        const int4 info = p.table[chunk];
-        const int start = info.y, L = info.z;
+        const int2 info = chunk_rows(p, lm, chunk);
+        const int start = info.x, L = info.y;
         const int kh = h / grp;
 
         // ---- stage K, Q (as X) and V rows (cp.async), gates, beta -------------------
@@ -334,16 +416,16 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
             const int nxt = item + (int)gridDim.x;
             if (nxt < nitems) {
                 const int nc = nxt / p.Hv, nh = nxt - nc * p.Hv;
-                const int4 ni = p.table[nc];
+                const int2 ni = chunk_rows(p, lm, nc);
                 const int r = tid & 63, which = tid >> 6;
-                const size_t tok = (size_t)ni.y + r;
-                if (r < ni.z) {
+                const size_t tok = (size_t)ni.x + r;
+                if (r < ni.y) {
                     if (which == 0) tc::prefetch_l2(kp + (tok * p.Hk + nh / grp) * kDk, kDk * 2);
                     else if (which == 1) tc::prefetch_l2(qp + (tok * p.Hk + nh / grp) * kDk, kDk * 2);
                     else if (which == 2) tc::prefetch_l2(vp + (tok * p.Hv + nh) * kDk, kDk * 2);
                 }
-                if (tid == 255) tc::prefetch_l2_span(p.g + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 4);
-                if (tid == 254) tc::prefetch_l2_span(bp + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 2);
+                if (tid == 255) tc::prefetch_l2_span(p.g + (size_t)ni.x * p.Hv, (size_t)ni.y * p.Hv * 4);
+                if (tid == 254) tc::prefetch_l2_span(bp + (size_t)ni.x * p.Hv, (size_t)ni.y * p.Hv * 2);
             }
         }
         if (tid < C) bet[tid] = tid < L ? to_f(bp[((size_t)start + tid) * p.Hv + h]) : 0.f;
@@ -629,7 +711,8 @@ struct KdaSmem {
     static constexpr uint32_t kPiv = kP + kTile64x64;         // fp32 [16][128]: Gam2 of tokens 4, 8, .., 60 and L - 1
     static constexpr uint32_t kBeta = kPiv + 16 * D * 4;
     static constexpr uint32_t kBar = kBeta + C * 4;
-    static constexpr uint32_t kTotal = kBar + 64 + 1024;      // + alignment slack
+    static constexpr uint32_t kMeta = kBar + 64;              // LocalMeta
+    static constexpr uint32_t kTotal = kMeta + sizeof(LocalMeta) + 1024;  // + alignment slack
     static_assert(kGt + C * D * 4 <= kOpsEnd, "Gam2 scratch beyond the work region");
     static_assert(kZ + 4096 <= kV, "Z overlaps V");
     static_assert(kV + kTile64x128 == kOpsEnd, "V at the end of the work region");
@@ -679,13 +762,15 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
     uint32_t phW = 0;
     tc::grid_dep_wait();    // the chunk table comes from the metadata kernel
     tc::grid_dep_launch();  // the chain kernel may start its prologue on free SMs
-    const int nitems = p.meta[0] * p.Hv;
+    LocalMeta& lm = *reinterpret_cast<LocalMeta*>(sm + S::kMeta);
+    if (p.local_meta) local_meta_build<NT>(p, lm, tid);
+    const int nitems = (p.local_meta ? lm.total : p.meta[0]) * p.Hv;
     const uint32_t sX = tc::smem_u32(sm + S::kX);
 
     for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
         const int chunk = item / p.Hv, h = item - chunk * p.Hv;
-        const int4 info = p.table[chunk];
-        const int start = info.y, L = info.z;
+        const int2 info = chunk_rows(p, lm, chunk);
+        const int start = info.x, L = info.y;
         const int kh = h / grp;
 
         // ---- stage K, Q rows and the gate rows (cp.async); zero A and P; beta; warm L2
@@ -711,16 +796,16 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
             const int nxt = item + (int)gridDim.x;
             if (nxt < nitems) {
                 const int nc = nxt / p.Hv, nh = nxt - nc * p.Hv;
-                const int4 ni = p.table[nc];
+                const int2 ni = chunk_rows(p, lm, nc);
                 const int r = tid & 63, which = tid >> 6;
-                const size_t tok = (size_t)ni.y + r;
-                if (r < ni.z) {
+                const size_t tok = (size_t)ni.x + r;
+                if (r < ni.y) {
                     if (which == 0) tc::prefetch_l2(kp + (tok * p.Hk + nh / grp) * kDk, kDk * 2);
                     else if (which == 1) tc::prefetch_l2(qp + (tok * p.Hk + nh / grp) * kDk, kDk * 2);
                     else if (which == 2) tc::prefetch_l2(vp + (tok * p.Hv + nh) * kDk, kDk * 2);
                     else tc::prefetch_l2(p.gk + (tok * p.Hv + nh) * kDk, kDk * 4);
                 }
-                if (tid == 0) tc::prefetch_l2_span(bp + (size_t)ni.y * p.Hv, (size_t)ni.z * p.Hv * 2);
+                if (tid == 0) tc::prefetch_l2_span(bp + (size_t)ni.x * p.Hv, (size_t)ni.y * p.Hv * 2);
             }
         }
         for (int e = tid; e < (int)(C * LDA); e += NT) As[e] = 0.f;
@@ -1677,10 +1762,12 @@ cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* w
     TcParams p{};
     p.q = q; p.k = k; p.v = a.v; p.g = a.g; p.gk = a.gk; p.beta = a.beta;
     p.h0 = a.initial_state; p.o = a.o; p.hT = a.final_state; p.cu = a.cu_seqlens;
-    p.meta = reinterpret_cast<const int*>(ws + w.off_meta);
-    p.offsets = reinterpret_cast<const int*>(ws + w.off_offsets);
+    p.meta = reinterpret_cast<int*>(ws + w.off_meta);
+    p.offsets = reinterpret_cast<int*>(ws + w.off_offsets);
     p.table = reinterpret_cast<const int4*>(ws + w.off_table);
-    p.order = reinterpret_cast<const int*>(ws + w.off_order);
+    p.order = reinterpret_cast<int*>(ws + w.off_order);
+    p.local_meta = w.local_meta ? 1 : 0;
+    p.T = a.T;
     const size_t mc = (size_t)w.max_chunks;
     unsigned char* blob = reinterpret_cast<unsigned char*>(ws + w.off_blobs);
     p.Xw = blob; blob += mc * a.Hv * kXwBytes;

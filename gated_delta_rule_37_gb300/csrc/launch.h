@@ -74,7 +74,10 @@ struct ChunkWorkspace {
     size_t off_vn;        // fp32 [T, Hv, V]
     size_t off_order;     // int [N]: sequences by decreasing length
     size_t off_blobs;     // tensor-core path operand images
-    bool tc;              // tensor-core path (bf16, K = V = 128)
+    bool tc;              // tensor-core path (bf16, K = V = 128 or 64)
+    // tensor-core path, at most kLocalMetaSeqs sequences and no scan: the
+    // metadata kernel is not launched; the prep kernel forms the metadata
+    bool local_meta;
     // chunk-parallel scan (GDR_CHUNK_SCAN on the tensor-core path)
     int seg_chunks;       // segment length G in chunks; 0 = scan off
     int64_t max_segs;     // segment capacity: ceil(max_chunks / G) + N
@@ -94,7 +97,11 @@ ChunkWorkspace chunk_workspace_layout(int N, int64_t T, int Hk, int Hv, int K, i
 
 cudaError_t launch_chunk(const ChunkArgs& a, cudaStream_t stream);
 
-// Tensor-core chunked prefill (bf16, K = V = 128): blob bytes and launcher.
+// Calls with at most this many sequences (and no chunk-parallel scan) have
+// their chunk metadata formed inside the tensor-core prep kernel.
+constexpr int kLocalMetaSeqs = 64;
+
+// Tensor-core chunked prefill (bf16, K = V = 128 or 64): blob bytes and launcher.
 size_t chunk_tc_blob_bytes(int64_t max_chunks, int Hk, int Hv, bool channel_gate);
 cudaError_t launch_chunk_tc(const ChunkArgs& a, const ChunkWorkspace& w, char* ws, const void* q, const void* k,
                             cudaStream_t stream);

@@ -108,7 +108,10 @@ GDR_API int gdr_chunk_workspace_size(int N, int64_t T_total, int Hk, int Hv, int
  *   beta           [T_total, Hv]      dtype, in [0, 1] (or [0, 2])
  *   initial_state  [N, Hv, V, K] fp32, or NULL for zeros
  *   cu_seqlens     [N+1] int32 device, cu[0] = 0, non-decreasing,
- *                  cu[N] = T_total; every sequence non-empty
+ *                  cu[N] = T_total; every sequence non-empty.  A cu_seqlens
+ *                  that breaks the first three rules is found on the device
+ *                  and nothing is written (the call still returns GDR_OK;
+ *                  GDR_VALIDATE turns it into GDR_ERR_VALIDATION)
  *   scale          read scale (usually 1/sqrt(K))
  *   o              [T_total, Hv, V]   dtype (written)
  *   final_state    [N, Hv, V, K] fp32 (written), or NULL

@@ -8,7 +8,7 @@ import torch
 import gated_delta_rule_37_gb300 as gdr
 import oracle
 from gated_delta_rule_37_gb300 import workloads
-from tests.gpu_util import Guarded, bits_equal, check_out, check_state
+from tests.gpu_util import Guarded, bits_equal, check_out, check_state, sentinel_like
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -210,6 +210,33 @@ def test_validate_flag():
     with pytest.raises(gdr.GdrError):
         gdr.chunk_fwd(case.q.to(dev), case.k.to(dev), case.v.to(dev), case.beta.to(dev), bad_cu,
                       g=case.g.to(dev), flags=gdr.GDR_VALIDATE)
+
+
+@pytest.mark.parametrize("n_seqs", [3, 70])
+@pytest.mark.parametrize("defect", ["decreasing", "last_not_T", "first_not_zero"])
+def test_malformed_cu_seqlens_writes_nothing(n_seqs, defect):
+    """Without GDR_VALIDATE a malformed cu_seqlens is found on the device and
+    no output is written (3 sequences: the prep forms the chunk metadata
+    itself; 70: the metadata kernel does)."""
+    case = workloads.chunk_case(67, [40] * n_seqs, 1, 2, 128, 128, gate="g", h0_std=0.1)
+    cu = case.cu_seqlens.clone()
+    if defect == "decreasing":
+        cu[1], cu[2] = cu[2].item(), cu[1].item()
+    elif defect == "last_not_T":
+        cu[-1] -= 5
+    else:
+        cu[0] = 1
+    dev = DEV
+    o = Guarded(tuple(case.v.shape), case.q.dtype, dev, fill_bytes=sentinel_like(case.v.shape, case.q.dtype))
+    sf_shape = (case.N, 2, 128, 128)
+    sf = Guarded(sf_shape, torch.float32, dev, fill_bytes=sentinel_like(sf_shape, torch.float32))
+    gdr.chunk_fwd(case.q.to(dev), case.k.to(dev), case.v.to(dev), case.beta.to(dev), cu.to(dev), g=case.g.to(dev),
+                  initial_state=case.initial_state.to(dev), scale=case.scale, o=o.view, final_state=sf.view)
+    torch.cuda.synchronize()
+    assert gdr.device_status() == 0
+    assert o.guards_intact() and sf.guards_intact()
+    assert bits_equal(o.view, sentinel_like(case.v.shape, case.q.dtype))
+    assert bits_equal(sf.view, sentinel_like(sf_shape, torch.float32))
 
 
 def test_cuda_graph_replay_equals_eager():
