@@ -950,11 +950,13 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
         // K_l lo is a 32-row tile: the M = 64 product also reads the 32 rows after
         // it (real memory), which land in accumulator rows that are not read.
         auto issue = [&](int lev) {
-            if (warp < 3 && lane == 0) {
-                const uint32_t la = tc::smem_u32(sm + (warp == 2 ? S::kLl : S::kLh));
-                const uint32_t astr = warp == 2 ? 32 * 128 : C * 128;
-                const uint32_t rb = tc::smem_u32(sm + (warp == 1 ? S::kRl : S::kRh));
-                const uint32_t d = tmem + 96 * (lev & 1) + 32 * warp;
+            // issuers: warps 3, 1 and 4, which skip the read-outs of levels 1..3
+            const int role = warp == 3 ? 0 : warp == 1 ? 1 : warp == 4 ? 2 : -1;
+            if (role >= 0 && lane == 0) {
+                const uint32_t la = tc::smem_u32(sm + (role == 2 ? S::kLl : S::kLh));
+                const uint32_t astr = role == 2 ? 32 * 128 : C * 128;
+                const uint32_t rb = tc::smem_u32(sm + (role == 1 ? S::kRl : S::kRh));
+                const uint32_t d = tmem + 96 * (lev & 1) + 32 * role;
                 for (int ks = 0; ks < 8; ++ks)
                     tc::mma_bf16(d, tc::smem_desc(la + (ks >> 2) * astr + (ks & 3) * 32, 16, 1024, tc::kSwizzle128),
                                  tc::smem_desc(rb + (ks >> 2) * (32 * 128) + (ks & 3) * 32, 16, 1024, tc::kSwizzle128),
