@@ -380,10 +380,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::kBar + 16);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + S::kBar + 24);
     const uint32_t bar0 = tc::smem_u32(&bars[0]);
+    const uint32_t barWU = tc::smem_u32(&bars[1]);  // W and U products: two issuers
 
     if (warp == 0) tc::tmem_alloc(tc::smem_u32(tmem_slot), 256);
     if (tid == 0) {
         tc::mbar_init(bar0, 1);
+        tc::mbar_init(barWU, 2);
         *abort_flag = 0;
         tc::mbar_fence_init();
     }
@@ -392,6 +394,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
     uint32_t ph0 = 0;  // parity of the next completion of bar0
+    uint32_t phWU = 0;
     tc::grid_dep_wait();    // the chunk table comes from the metadata kernel
     tc::grid_dep_launch();  // the chain kernel may start its prologue on free SMs
     LocalMeta& lm = *reinterpret_cast<LocalMeta*>(sm + S::kMeta);
@@ -561,8 +564,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
         tc::fence_proxy_async();
         __syncthreads();
 
-        // ---- W = T' K (or T'' (K o e^Gam)), U = T'' V ----------------------------------------
-        if (tid == 0) {
+        // ---- W = T' K (lane 0 of warp 0), U = T'' V (lane 0 of warp 1) ----------------------
+        if (warp < 2 && lane == 0) {
             tc::fence_after();
             constexpr uint32_t id = tc::idesc_bf16(64, 128, false, true);
             const uint32_t t1h = tc::smem_u32(sm + S::kT1h), t1l = tc::smem_u32(sm + S::kT1l);
@@ -573,11 +576,14 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
                     tc::mma_bf16(tmem + dcol, tc::smem_desc(a + ks * 32, 16, 1024, tc::kSwizzle128),
                                  tc::smem_desc(b + ks * 2048, atom, 1024, tc::kSwizzle128), id, (first && ks == 0) ? 0u : 1u);
             };
-            mm(0, t1h, sX, kXcb, true);
-            mm(0, t1l, sX, kXcb, false);
-            mm(128, t2h, sV, C * 128, true);
-            mm(128, t2l, sV, C * 128, false);
-            tc::mma_commit(bar0);
+            if (warp == 0) {
+                mm(0, t1h, sX, kXcb, true);
+                mm(0, t1l, sX, kXcb, false);
+            } else {
+                mm(128, t2h, sV, C * 128, true);
+                mm(128, t2l, sV, C * 128, false);
+            }
+            tc::mma_commit(barWU);
         }
         __syncwarp();
 
@@ -586,9 +592,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
         //      shared memory left dead by the finished MMAs (W hi / lo as 64-row k128
         //      tiles over X, U value-major over V and A) and written with bulk copies,
         //      so every global write is a contiguous run. ---------------------------------
-        // the item's last completion of bar0 (the scalar gate's K K^T / Q K^T group was the first)
-        if (!tc::mbar_wait(bar0, ph0, abort_flag)) { *abort_flag = 1; raise_error(p, 1u); }
-        ph0 ^= 1u;
+        if (!tc::mbar_wait(barWU, phWU, abort_flag)) { *abort_flag = 1; raise_error(p, 1u); }
+        phWU ^= 1u;
         tc::fence_after();
         {
             const int i = 16 * q + (lane & 15);
@@ -751,7 +756,7 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
     if (tid == 0) {
         tc::mbar_init(barL[0], 3);
         tc::mbar_init(barL[1], 3);
-        tc::mbar_init(barW, 1);
+        tc::mbar_init(barW, 2);
         *abort_flag = 0;
         tc::mbar_fence_init();
     }
@@ -1147,8 +1152,9 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
         tc::fence_proxy_async();
         __syncthreads();
 
-        // ---- W = T'' (K o e^Gam) (3 terms), U = T'' V (2 terms) ------------------------
-        if (tid == 0) {
+        // ---- W = T'' (K o e^Gam) (3 terms, lane 0 of warp 0), U = T'' V (2 terms, lane 0
+        //      of warp 1) ------------------------------------------------------------------
+        if (warp < 2 && lane == 0) {
             tc::fence_after();
             constexpr uint32_t id = tc::idesc_bf16(64, 128, false, true);
             const uint32_t t2h = tc::smem_u32(sm + S::kT2h), t2l = tc::smem_u32(sm + S::kT2l);
@@ -1158,11 +1164,14 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
                     tc::mma_bf16(tmem + dcol, tc::smem_desc(a + ks * 32, 16, 1024, tc::kSwizzle128),
                                  tc::smem_desc(b + ks * 2048, atom, 1024, tc::kSwizzle128), id, (first && ks == 0) ? 0u : 1u);
             };
-            mm(0, t2h, kgh, kXcb, true);
-            mm(0, t2h, kgl, kXcb, false);
-            mm(0, t2l, kgh, kXcb, false);
-            mm(128, t2h, sV, C * 128, true);
-            mm(128, t2l, sV, C * 128, false);
+            if (warp == 0) {
+                mm(0, t2h, kgh, kXcb, true);
+                mm(0, t2h, kgl, kXcb, false);
+                mm(0, t2l, kgh, kXcb, false);
+            } else {
+                mm(128, t2h, sV, C * 128, true);
+                mm(128, t2l, sV, C * 128, false);
+            }
             tc::mma_commit(barW);
         }
         __syncwarp();
