@@ -14,11 +14,12 @@
 //        with single 1-D bulk copies.
 //        Per-key-channel gates (KDA) have a prep kernel of their own
 //        (chunk_prep_kda_kernel, two 256-thread CTAs per SM): A and P from
-//        pivoted products (pairs across the halves of 2h-token blocks on
-//        tcgen05 with the decays folded into both operands around the pivot,
-//        each factor <= 1; pairs inside 4-token blocks on the CUDA cores),
-//        W = Tm diag(beta) (K o e^{Gam}) with a 3-term split, and the decayed
-//        keys Kd = K o e^{gam_L - Gam} as hi/lo.
+//        products with the decays folded into both operands around a pivot on
+//        tcgen05 (one pivot at the chunk's first token while no channel decays
+//        by more than 2^64 over the chunk; otherwise pairs across the halves
+//        of 2h-token blocks, each factor <= 1, and pairs inside 4-token blocks
+//        on the CUDA cores), W = Tm diag(beta) (K o e^{Gam}) with a 3-term
+//        split, and the decayed keys Kd = K o e^{gam_L - Gam} as hi/lo.
 //
 //  chain (one CTA per value-head x 32-column block of V x sequence, serial
 //        over the sequence's chunks; attention-gym PR #344's inter-chunk state
@@ -657,11 +658,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
 //   * Thread (t0 = tid / 8, g = tid % 8) owns tokens t0 and t0 + 32 and, of
 //     each, the 16-byte operand chunks g and g + 8 (channels 8g .. 8g + 7 and
 //     64 + 8g .. 64 + 8g + 7).  It holds their Gam2 in registers for the whole
-//     item; only the rows of the pivots (tokens 4, 8, ..., 60) and of the last
-//     token stay in shared memory.
+//     item; only the rows of the pivots (tokens 4, 8, ..., 60), of the first
+//     and of the last token stay in shared memory.
 //   * A_ij = beta_i sum_c k_i[c] k_j[c] e^{Gam_i[c] - Gam_j[c]} (j < i) and
-//     P_ij = sum_c q_i[c] k_j[c] e^{Gam_i[c] - Gam_j[c]} (j <= i).  Pairs in
-//     different halves of a block of 2h tokens (h = 32, 16, 8, 4) go through
+//     P_ij = sum_c q_i[c] k_j[c] e^{Gam_i[c] - Gam_j[c]} (j <= i).  While no
+//     channel decays by more than 2^64 over the chunk (every chunk of slowly
+//     decaying gates), one pivot at the first token serves every pair:
+//     e^{Gam_i - Gam_j} = e^{Gam_i - Gam_0} e^{Gam_0 - Gam_j}, the left factor
+//     <= 1 and the right one >= 1, both inside [2^-64, 2^64], so each stays in
+//     the normal range and its hi / lo split keeps its relative accuracy.
+//     One stacked product [K L hi ; Q L hi] [K R hi | K R lo] (N = 128) and
+//     one K L lo x K R hi (N = 64) then give all of A and P.  Otherwise, pairs
+//     in different halves of a block of 2h tokens (h = 32, 16, 8, 4) go through
 //     the tensor cores around the pivot p = first token of the upper half:
 //     e^{Gam_i - Gam_j} = e^{Gam_i - Gam_p} e^{Gam_p - Gam_j}, both factors <= 1,
 //     folded into the left (k_i, q_i) and right (k_j) operands.  A takes three
@@ -697,6 +705,7 @@ __device__ __forceinline__ void split2x(float2 x, uint32_t& hi, uint32_t& lo) {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kKdaThreads = 256;
+constexpr float kSinglePivotSpan2 = 64.f;  // log2 units: factors within [2^-64, 2^64]
 
 struct KdaSmem {
     static constexpr uint32_t kX = 0;                         // [K ; Q] 128 x 128 bf16 (32 KB)
@@ -717,7 +726,20 @@ struct KdaSmem {
     static constexpr uint32_t kBeta = kPiv + 16 * D * 4;
     static constexpr uint32_t kBar = kBeta + C * 4;
     static constexpr uint32_t kMeta = kBar + 64;              // LocalMeta
-    static constexpr uint32_t kTotal = kMeta + sizeof(LocalMeta) + 1024;  // + alignment slack
+    static constexpr uint32_t kG0 = (kMeta + sizeof(LocalMeta) + 15) & ~15u;  // fp32 [128]: Gam2 of token 0
+    static constexpr uint32_t kTotal = kG0 + D * 4 + 1024;    // + alignment slack
+    // single-pivot operands: [K L hi ; Q L hi] over A (column block 0) and P + pivot rows
+    // (column block 1), [K R hi ; K R lo] over the work region, K L lo over the work
+    // region's tail (column block 0) and the query rows of X (column block 1)
+    static constexpr uint32_t kSgA1 = kP;
+    static constexpr uint32_t kSgB = kOps;
+    static constexpr uint32_t kSgLl0 = kOps + 2 * kTile64x128;
+    static constexpr uint32_t kSgLl1 = kX + C * 128;
+    static_assert(kTile64x128 <= C * LDA * 4, "A column block 0 (128 rows x 128 B) in the A region");
+    static_assert(kSgA1 + kTile64x128 == kBeta, "A column block 1 over P and the pivot rows");
+    static_assert(kSgB + 2 * kTile64x128 == kSgLl0, "B column blocks ahead of K L lo");
+    static_assert(kSgLl0 + kTile64x128 / 2 == kOpsEnd, "K L lo column block 0 at the work region's tail");
+    static_assert((kA | kSgA1 | kSgB | kSgLl0 | kSgLl1) % 1024 == 0, "128-byte swizzled tiles on 1 KB boundaries");
     static_assert(kGt + C * D * 4 <= kOpsEnd, "Gam2 scratch beyond the work region");
     static_assert(kZ + 4096 <= kV, "Z overlaps V");
     static_assert(kV + kTile64x128 == kOpsEnd, "V at the end of the work region");
@@ -745,6 +767,7 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
     float* Z = reinterpret_cast<float*>(sm + S::kZ);
     float* gt = reinterpret_cast<float*>(sm + S::kGt);
     float* piv = reinterpret_cast<float*>(sm + S::kPiv);
+    float* g0 = reinterpret_cast<float*>(sm + S::kG0);
     float* bet = reinterpret_cast<float*>(sm + S::kBeta);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::kBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + S::kBar + 24);
@@ -813,9 +836,8 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
                 if (tid == 0) tc::prefetch_l2_span(bp + (size_t)ni.x * p.Hv, (size_t)ni.y * p.Hv * 2);
             }
         }
-        for (int e = tid; e < (int)(C * LDA); e += NT) As[e] = 0.f;
-        for (int e = tid; e < (int)(kTile64x64 / 16); e += NT)
-            reinterpret_cast<uint4*>(sm + S::kP)[e] = make_uint4(0u, 0u, 0u, 0u);
+        // (A needs no clearing: the solve reads its strict lower triangle, all of
+        // which the products write)
         if (tid < C) bet[tid] = tid < L ? to_f(bp[((size_t)start + tid) * p.Hv + h]) : 0.f;
         asm volatile("cp.async.wait_group 0;" ::: "memory");
         __syncthreads();
@@ -836,11 +858,18 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
             for (int u = 0; u < 32; ++u) gt[(32 * hf + u) * D + c] = (x[u] + off) * kLog2e;
         }
         __syncthreads();
-        // pivot rows (tokens 4, 8, .., 60) and the last token's row; this thread's Gam2
-        for (int e = tid; e < 16 * D; e += NT) {
+        // One pivot at the chunk's first token serves every pair while no channel
+        // decays by more than 2^kSinglePivotSpan2 over the chunk: the factors
+        // e^{Gam_i - Gam_0} <= 1 and e^{Gam_0 - Gam_j} >= 1 then stay well inside the
+        // normal range, and each is split hi / lo relative to its own size.
+        const bool single = __syncthreads_and(tid >= D || gt[tid] - gt[(L - 1) * D + tid] <= kSinglePivotSpan2) != 0;
+        // pivot rows (tokens 4, 8, .., 60; the pivot levels only) and the last token's
+        // row; token 0's row; this thread's Gam2
+        for (int e = single ? 15 * D + tid : tid; e < 16 * D; e += NT) {
             const int r = e >> 7, tok = r < 15 ? 4 * (r + 1) : L - 1;
             piv[e] = gt[tok * D + (e & (D - 1))];
         }
+        if (tid < D) g0[tid] = gt[tid];
         float G[2][16];
 #pragma unroll
         for (int u = 0; u < 2; ++u)
@@ -1009,95 +1038,196 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
                 }
             }
         };
-        build(0);
-        issue(0);
-        wait_level(0);
-        build(1);
-        issue(1);
-        readout(0);
-        wait_level(1);
-        build(2);
-        issue(2);
-        readout(1);
-        wait_level(2);
-        build(3);
-        issue(3);
-        readout(2);
-        wait_level(3);
-        readout(3);
+        if (!single) {
+            // P entries above the diagonal are never written on this path
+            for (int e = tid; e < (int)(kTile64x64 / 16); e += NT)
+                reinterpret_cast<uint4*>(sm + S::kP)[e] = make_uint4(0u, 0u, 0u, 0u);
+            build(0);
+            issue(0);
+            wait_level(0);
+            build(1);
+            issue(1);
+            readout(0);
+            wait_level(1);
+            build(2);
+            issue(2);
+            readout(1);
+            wait_level(2);
+            build(3);
+            issue(3);
+            readout(2);
+            wait_level(3);
+            readout(3);
 
-        // ---- pairs inside a 4-token block: warp w has the blocks at tokens 4w and
-        //      4w + 32.  Lane (u, o): block u, channels 8o .. 8o + 7; it forms the 6
-        //      pairs i > j (A and P) and the 4 diagonal P entries over its 8 channels,
-        //      and the 16 partial sums are reduced over the 16 lanes of the block
-        //      (transposed, so lane o ends with sum o). --------------------------------
-        {
+            // ---- pairs inside a 4-token block: warp w has the blocks at tokens 4w and
+            //      4w + 32.  Lane (u, o): block u, channels 8o .. 8o + 7; it forms the 6
+            //      pairs i > j (A and P) and the 4 diagonal P entries over its 8 channels,
+            //      and the 16 partial sums are reduced over the 16 lanes of the block
+            //      (transposed, so lane o ends with sum o). --------------------------------
+            {
+    #pragma unroll
+                for (int u = 0; u < 2; ++u)
+    #pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        float* dst = gt + (t0 + 32 * u) * D + 8 * (g + 8 * cc);
+                        *reinterpret_cast<float4*>(dst) = make_float4(G[u][8 * cc], G[u][8 * cc + 1], G[u][8 * cc + 2], G[u][8 * cc + 3]);
+                        *reinterpret_cast<float4*>(dst + 4) = make_float4(G[u][8 * cc + 4], G[u][8 * cc + 5], G[u][8 * cc + 6], G[u][8 * cc + 7]);
+                    }
+                __syncwarp();
+                const int o = lane & 15, tb = 4 * warp + 32 * (lane >> 4);
+                float v[16];
+                {
+                    uint4 kr[4], qr[4];
+    #pragma unroll
+                    for (int a = 0; a < 4; ++a) {
+                        kr[a] = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(tb + a, o, 2 * C));
+                        qr[a] = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(C + tb + a, o, 2 * C));
+                    }
+                    // diagonal: P_aa = q_a . k_a
+    #pragma unroll
+                    for (int a = 0; a < 4; ++a) {
+                        const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&kr[a]);
+                        const __nv_bfloat16* qv = reinterpret_cast<const __nv_bfloat16*>(&qr[a]);
+                        float acc = 0.f;
+    #pragma unroll
+                        for (int e = 0; e < 8; ++e) acc = fmaf(__bfloat162float(qv[e]), __bfloat162float(kv[e]), acc);
+                        v[12 + a] = acc;
+                    }
+                    // pairs (1,0) (2,0) (3,0) (2,1) (3,1) (3,2): A in v[0..5], P in v[6..11]
+    #pragma unroll
+                    for (int m = 0; m < 6; ++m) {
+                        const int i = m < 3 ? m + 1 : (m < 5 ? m - 1 : 3), j = m < 3 ? 0 : (m < 5 ? 1 : 2);
+                        float gi[8], gj[8];
+                        ld8(gt + (tb + i) * D + 8 * o, gi);
+                        ld8(gt + (tb + j) * D + 8 * o, gj);
+                        const __nv_bfloat16* ki = reinterpret_cast<const __nv_bfloat16*>(&kr[i]);
+                        const __nv_bfloat16* qi = reinterpret_cast<const __nv_bfloat16*>(&qr[i]);
+                        const __nv_bfloat16* kj = reinterpret_cast<const __nv_bfloat16*>(&kr[j]);
+                        float sa = 0.f, sp = 0.f;
+    #pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float kd = __bfloat162float(kj[e]) * ex2(gi[e] - gj[e]);
+                            sa = fmaf(__bfloat162float(ki[e]), kd, sa);
+                            sp = fmaf(__bfloat162float(qi[e]), kd, sp);
+                        }
+                        v[m] = sa;
+                        v[6 + m] = sp;
+                    }
+                }
+                // transposed reduction over the 16 lanes of the block: lane o ends with sum o
+    #pragma unroll
+                for (int k = 8; k >= 1; k >>= 1) {
+                    const bool upper = (lane & k) != 0;
+    #pragma unroll
+                    for (int e = 0; e < k; ++e) {
+                        const float send = upper ? v[e] : v[e + k];
+                        const float keep = upper ? v[e + k] : v[e];
+                        v[e] = keep + __shfl_xor_sync(0xffffffffu, send, k);
+                    }
+                }
+                {
+                    const int m = o < 6 ? o : (o < 12 ? o - 6 : 0);
+                    const int i = tb + (o >= 12 ? o - 12 : (m < 3 ? m + 1 : (m < 5 ? m - 1 : 3)));
+                    const int j = o >= 12 ? i : tb + (m < 3 ? 0 : (m < 5 ? 1 : 2));
+                    if (o < 6) As[i * LDA + j] = bet[i] * v[0];
+                    else *reinterpret_cast<__nv_bfloat16*>(sm + S::kP + tc::off_k128(i, j, C)) = __float2bfloat16_rn(v[0]);
+                }
+            }
+        } else {
+            // ---- one pivot at the chunk's first token: every pair from one stacked product.
+            //      Left L_i = e^{Gam_i - Gam_0} <= 1: [K L hi ; Q L hi] (128 rows) and K L lo;
+            //      right R_j = e^{Gam_0 - Gam_j} >= 1: [K R hi ; K R lo] (128 rows).
+            //      A_ij = beta_i (KL_hi KR_hi + KL_hi KR_lo + KL_lo KR_hi)_ij for j < i and
+            //      P_ij = (QL_hi KR_hi + QL_hi KR_lo)_ij for j <= i. ----------------------------
+            __syncthreads();  // the key images have read the pivot rows, which the operands overwrite
 #pragma unroll
-            for (int u = 0; u < 2; ++u)
+            for (int u = 0; u < 2; ++u) {
+                const int t = t0 + 32 * u;
+                // cc = 0 first: its query chunk is where cc = 1 puts K L lo (same thread, same address)
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
-                    float* dst = gt + (t0 + 32 * u) * D + 8 * (g + 8 * cc);
-                    *reinterpret_cast<float4*>(dst) = make_float4(G[u][8 * cc], G[u][8 * cc + 1], G[u][8 * cc + 2], G[u][8 * cc + 3]);
-                    *reinterpret_cast<float4*>(dst + 4) = make_float4(G[u][8 * cc + 4], G[u][8 * cc + 5], G[u][8 * cc + 6], G[u][8 * cc + 7]);
-                }
-            __syncwarp();
-            const int o = lane & 15, tb = 4 * warp + 32 * (lane >> 4);
-            float v[16];
-            {
-                uint4 kr[4], qr[4];
+                    const int ch = g + 8 * cc, c8 = ch & 7;
+                    float z8[8];
+                    ld8(g0 + 8 * ch, z8);
+                    const uint4 kr = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(t, ch, 2 * C));
+                    const uint4 qr = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(C + t, ch, 2 * C));
+                    const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w}, qw4[4] = {qr.x, qr.y, qr.z, qr.w};
+                    uint32_t lh[4], ll[4], rh[4], rl[4], qh[4];
 #pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    kr[a] = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(tb + a, o, 2 * C));
-                    qr[a] = *reinterpret_cast<const uint4*>(sm + S::kX + tc::chunk_k128(C + tb + a, o, 2 * C));
-                }
-                // diagonal: P_aa = q_a . k_a
-#pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&kr[a]);
-                    const __nv_bfloat16* qv = reinterpret_cast<const __nv_bfloat16*>(&qr[a]);
-                    float acc = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc = fmaf(__bfloat162float(qv[e]), __bfloat162float(kv[e]), acc);
-                    v[12 + a] = acc;
-                }
-                // pairs (1,0) (2,0) (3,0) (2,1) (3,1) (3,2): A in v[0..5], P in v[6..11]
-#pragma unroll
-                for (int m = 0; m < 6; ++m) {
-                    const int i = m < 3 ? m + 1 : (m < 5 ? m - 1 : 3), j = m < 3 ? 0 : (m < 5 ? 1 : 2);
-                    float gi[8], gj[8];
-                    ld8(gt + (tb + i) * D + 8 * o, gi);
-                    ld8(gt + (tb + j) * D + 8 * o, gj);
-                    const __nv_bfloat16* ki = reinterpret_cast<const __nv_bfloat16*>(&kr[i]);
-                    const __nv_bfloat16* qi = reinterpret_cast<const __nv_bfloat16*>(&qr[i]);
-                    const __nv_bfloat16* kj = reinterpret_cast<const __nv_bfloat16*>(&kr[j]);
-                    float sa = 0.f, sp = 0.f;
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float kd = __bfloat162float(kj[e]) * ex2(gi[e] - gj[e]);
-                        sa = fmaf(__bfloat162float(ki[e]), kd, sa);
-                        sp = fmaf(__bfloat162float(qi[e]), kd, sp);
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 d = sub2(make_float2(G[u][8 * cc + 2 * e], G[u][8 * cc + 2 * e + 1]),
+                                              make_float2(z8[2 * e], z8[2 * e + 1]));  // Gam_t - Gam_0 <= 0
+                        const float2 fl = make_float2(ex2(d.x), ex2(d.y));
+                        const float2 fr = make_float2(ex2(-d.x), ex2(-d.y));
+                        const float2 kf = unpack_bf16x2(kw[e]);
+                        split2x(__fmul2_rn(kf, fl), lh[e], ll[e]);
+                        split2x(__fmul2_rn(kf, fr), rh[e], rl[e]);
+                        const float2 x = __fmul2_rn(unpack_bf16x2(qw4[e]), fl);
+                        qh[e] = tc::pack_bf16(x.x, x.y);
                     }
-                    v[m] = sa;
-                    v[6 + m] = sp;
+                    unsigned char* a_blk = sm + (cc ? S::kSgA1 : S::kA);
+                    unsigned char* b_blk = sm + S::kSgB + cc * kTile64x128;
+                    unsigned char* l_blk = sm + (cc ? S::kSgLl1 : S::kSgLl0);
+                    *reinterpret_cast<uint4*>(a_blk + tc::chunk_k128(t, c8, 2 * C)) = make_uint4(lh[0], lh[1], lh[2], lh[3]);
+                    *reinterpret_cast<uint4*>(a_blk + tc::chunk_k128(C + t, c8, 2 * C)) = make_uint4(qh[0], qh[1], qh[2], qh[3]);
+                    *reinterpret_cast<uint4*>(b_blk + tc::chunk_k128(t, c8, 2 * C)) = make_uint4(rh[0], rh[1], rh[2], rh[3]);
+                    *reinterpret_cast<uint4*>(b_blk + tc::chunk_k128(C + t, c8, 2 * C)) = make_uint4(rl[0], rl[1], rl[2], rl[3]);
+                    *reinterpret_cast<uint4*>(l_blk + tc::chunk_k128(t, c8, C)) = make_uint4(ll[0], ll[1], ll[2], ll[3]);
                 }
             }
-            // transposed reduction over the 16 lanes of the block: lane o ends with sum o
-#pragma unroll
-            for (int k = 8; k >= 1; k >>= 1) {
-                const bool upper = (lane & k) != 0;
-#pragma unroll
-                for (int e = 0; e < k; ++e) {
-                    const float send = upper ? v[e] : v[e + k];
-                    const float keep = upper ? v[e + k] : v[e];
-                    v[e] = keep + __shfl_xor_sync(0xffffffffu, send, k);
+            tc::fence_proxy_async();
+            tc::fence_before();
+            __syncthreads();
+            tc::fence_after();
+            // [K L hi ; Q L hi] [K R hi | K R lo] (N = 128) into columns 0..127 (lane 0 of
+            // warp 3); [K L lo ; -] K R hi (N = 64) into columns 128..191 (lane 0 of warp 1).
+            // The K L lo operand reads 128 rows: rows 64..127 are the tiles after it (real
+            // memory) and land in accumulator rows that are not read.
+            if (lane == 0 && (warp == 3 || warp == 1)) {
+                const bool lo = warp == 1;
+                const uint32_t idS = lo ? tc::idesc_bf16(128, 64, false, false) : tc::idesc_bf16(128, 128, false, false);
+                const uint32_t d = tmem + (lo ? 128 : 0);
+                const uint32_t a0 = tc::smem_u32(sm + (lo ? S::kSgLl0 : S::kA));
+                const uint32_t a1 = tc::smem_u32(sm + (lo ? S::kSgLl1 : S::kSgA1));
+                const uint32_t b0 = tc::smem_u32(sm + S::kSgB);
+                for (int ks = 0; ks < 8; ++ks) {
+                    const uint32_t kin = (ks & 3) * 32;
+                    tc::mma_bf16(d, tc::smem_desc(((ks >> 2) ? a1 : a0) + kin, 16, 1024, tc::kSwizzle128),
+                                 tc::smem_desc(b0 + (ks >> 2) * kTile64x128 + kin, 16, 1024, tc::kSwizzle128), idS,
+                                 ks > 0);
                 }
+                tc::mma_commit(barW);
             }
+            __syncwarp();
+            if (!tc::mbar_wait(barW, phW, abort_flag)) { *abort_flag = 1; raise_error(p, 1u); }
+            phW ^= 1u;
+            tc::fence_after();
+            // read-out: TMEM lane r = accumulator row r (rows 0..63 A, 64..127 P); warps w and
+            // w + 4 take the columns j < 32 and j >= 32
             {
-                const int m = o < 6 ? o : (o < 12 ? o - 6 : 0);
-                const int i = tb + (o >= 12 ? o - 12 : (m < 3 ? m + 1 : (m < 5 ? m - 1 : 3)));
-                const int j = o >= 12 ? i : tb + (m < 3 ? 0 : (m < 5 ? 1 : 2));
-                if (o < 6) As[i * LDA + j] = bet[i] * v[0];
-                else *reinterpret_cast<__nv_bfloat16*>(sm + S::kP + tc::off_k128(i, j, C)) = __float2bfloat16_rn(v[0]);
+                const int q = warp & 3, nh = warp >> 2;
+                const int i = 32 * (q & 1) + lane;
+                const float bi = bet[i];
+#pragma unroll
+                for (int hh2 = 0; hh2 < 2; ++hh2) {
+                    const int j0 = 32 * nh + 16 * hh2;
+                    const uint32_t a = tmem + ((uint32_t)(32 * q) << 16) + j0;
+                    float d[48];
+                    tc::tmem_ld16x3(a, a + 64, a + 128, d);
+                    if (q < 2) {
+#pragma unroll
+                        for (int n2 = 0; n2 < 16; ++n2)
+                            if (j0 + n2 < i) As[i * LDA + j0 + n2] = bi * (d[n2] + d[16 + n2] + d[32 + n2]);
+                    } else {
+#pragma unroll
+                        for (int n2 = 0; n2 < 16; n2 += 2) {
+                            const int j = j0 + n2;
+                            const float p0 = j <= i ? d[n2] + d[16 + n2] : 0.f;
+                            const float p1 = j + 1 <= i ? d[n2 + 1] + d[17 + n2] : 0.f;
+                            *reinterpret_cast<uint32_t*>(sm + S::kP + tc::off_k128(i, j, C)) = tc::pack_bf16(p0, p1);
+                        }
+                    }
+                }
             }
         }
         tc::fence_proxy_async();  // P is read by a bulk copy
@@ -1119,7 +1249,12 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
                 const uint4 kr = *reinterpret_cast<const uint4*>(sm + S::kX + off);
                 const __nv_bfloat16* kv = reinterpret_cast<const __nv_bfloat16*>(&kr);
                 float g8[8];
-                ld8(gt + t * D + 8 * ch, g8);
+                if (single) {  // the scratch holds the right operand now; this thread's Gam2 is in G
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) g8[e] = G[u][8 * cc + e];
+                } else {
+                    ld8(gt + t * D + 8 * ch, g8);
+                }
                 uint32_t hw[4], lw[4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e)

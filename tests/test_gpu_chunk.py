@@ -353,3 +353,25 @@ def test_state_error_matches_the_split_model():
         e_model = rel_l2(model_final_states(case, ALL_TERMS), rs)
         print(f"{name}: GPU {e_gpu:.2e}, model {e_model:.2e}")
         assert e_gpu <= 3 * e_model, f"{name}: GPU {e_gpu:.2e} against the model's {e_model:.2e}"
+
+
+def test_channel_gate_single_and_level_pivot_chunks():
+    """Per-channel gates whose chunks fall on both sides of the single-pivot
+    limit (a decay span of 2^64 over a chunk on some channel): chunks of
+    small decays, of large decays (-2 per token), and chunks with spans just
+    below and just above the limit, in one call with GVA, ragged lengths and
+    an initial state."""
+    lens = [130, 257, 64, 70, 5]
+    case = workloads.chunk_case(71, lens, 1, 2, 128, 128, gate="gk", g_range=(-0.05, 0.0), h0_std=0.1)
+    gk = case.gk
+    ln2 = float(np.log(2.0))
+    # a chunk's span is the decay after its first token: 63 tokens of a 64-token chunk
+    gk[130:200] *= 40.0                        # up to -2 per token: spans far above the limit
+    gk[387:451] = -60.0 * ln2 / 64.0           # the 64-token sequence: 2^59 on half the channels,
+    gk[387:451, :, 64:] = -66.0 * ln2 / 64.0   # 2^65 on the others (just above the limit)
+    gk[451:515] = -64.5 * ln2 / 64.0           # a whole chunk at 2^63.5 (just below)
+    o, sf = run_gpu(case)
+    assert torch.isfinite(o.float()).all() and torch.isfinite(sf).all()
+    ro, rs = oracle_ref(case)
+    check_out(o.cpu(), ro, "o")
+    check_state(sf.cpu(), rs, "final state")

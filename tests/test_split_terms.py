@@ -9,8 +9,8 @@ kernels form
   prep   Tm = (I + A)^{-1} in fp32;  W = (Tm diag(beta e^gam)) K  and
          U = (Tm diag(beta)) V with the fp32 factor split (2 terms, K and V
          exact bf16); for per-channel gates W = (Tm diag(beta)) (K o e^Gam) with
-         both factors split (3 terms), and A from pivoted products of decayed
-         keys, both split (3 terms, see pivoted_A);
+         both factors split (3 terms), and A from products of keys decayed
+         around a pivot, both split (3 terms, see pivoted_A);
   chain  N = U - W S^T  (3 terms: W_hi S_hi, W_hi S_lo, W_lo S_hi);
          S <- e^{gam_L} S + K^T (f o N)  (2 terms: N'_hi, N'_lo; K exact), or,
          per-channel, S <- S diag(e^{Gam_L}) + Kd^T N with Kd = K o e^{Gam_L - Gam}
@@ -62,27 +62,36 @@ def split(x):
     return hi, bf16(x - hi)
 
 
+SINGLE_PIVOT_SPAN2 = 64.0  # log2 units: the largest per-channel decay over a chunk for one pivot
+
+
 def pivoted_A(K_, Gam, b, keep):
     """A_ij = b_i sum_c k_i[c] k_j[c] e^{Gam_i[c] - Gam_j[c]} (j < i) the way the
-    per-channel prep forms it: the pairs across the halves of each 2h-token
-    block (h = 32, 16, 8, 4) from operands decayed around the pivot p = first
-    token of the upper half, left k_i e^{Gam_i - Gam_p} and right
-    k_j e^{Gam_p - Gam_j} (both rounded to fp32, split hi / lo, products
-    L_hi R_hi + L_hi R_lo + L_lo R_hi); the pairs inside a 4-token block summed
-    in fp32."""
+    per-channel prep forms it.  While no channel decays by more than
+    2^SINGLE_PIVOT_SPAN2 over the chunk, one pivot at the first token serves every
+    pair: left k_i e^{Gam_i - Gam_0} (<= 1), right k_j e^{Gam_0 - Gam_j} (>= 1).
+    Otherwise the pairs across the halves of each 2h-token block (h = 32, 16,
+    8, 4) come from operands decayed around the pivot p = first token of the
+    upper half, left k_i e^{Gam_i - Gam_p} and right k_j e^{Gam_p - Gam_j}, and
+    the pairs inside a 4-token block are summed in fp32.  Operands are rounded
+    to fp32, split hi / lo, and multiplied L_hi R_hi + L_hi R_lo + L_lo R_hi."""
     L = K_.shape[0]
+
+    def product(left, right):
+        l_hi, l_lo = split(left)
+        r_hi, r_lo = split(right)
+        out = l_hi @ r_hi.T + l_hi @ r_lo.T
+        return out + l_lo @ r_hi.T if "a_lo" in keep else out
+
+    if (Gam[0] - Gam[L - 1]).max() / np.log(2.0) <= SINGLE_PIVOT_SPAN2:
+        A = np.tril(product(f32(K_ * np.exp(Gam - Gam[0])), f32(K_ * np.exp(Gam[0] - Gam))), -1)
+        return f32(b[:, None] * f32(A))
     A = np.zeros((L, L))
     for h in (32, 16, 8, 4):
         for p in range(h, L, 2 * h):
             i0, i1, j0 = p, min(p + h, L), p - h
-            left = f32(K_[i0:i1] * np.exp(Gam[i0:i1] - Gam[p]))
-            right = f32(K_[j0:p] * np.exp(Gam[p] - Gam[j0:p]))
-            l_hi, l_lo = split(left)
-            r_hi, r_lo = split(right)
-            blk = l_hi @ r_hi.T + l_hi @ r_lo.T
-            if "a_lo" in keep:
-                blk = blk + l_lo @ r_hi.T
-            A[i0:i1, j0:p] = f32(blk)
+            A[i0:i1, j0:p] = f32(product(f32(K_[i0:i1] * np.exp(Gam[i0:i1] - Gam[p])),
+                                         f32(K_[j0:p] * np.exp(Gam[p] - Gam[j0:p]))))
     for i in range(L):
         for j in range(i - i % 4, i):
             A[i, j] = f32((K_[i] * K_[j] * np.exp(Gam[i] - Gam[j])).sum())
