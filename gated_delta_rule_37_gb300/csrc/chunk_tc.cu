@@ -807,6 +807,9 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
                              kDk / 8, tid);
         stage_rows_async<NT>(sm + S::kX, 2 * C, C, qp + ((size_t)start * p.Hk + kh) * kDk, (size_t)p.Hk * kDk, L,
                              kDk / 8, tid);
+        // the previous item's U image (bulk group before its W image) sits in the scratch
+        if (tid == 0) tc::bulk_wait_read_1();
+        __syncthreads();
         {
             // gk rows [64][128] fp32 into the scratch (rows >= L and channels
             // >= dk zero-filled: a zero log-decay on a zero channel)
@@ -840,6 +843,7 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
         // which the products write)
         if (tid < C) bet[tid] = tid < L ? to_f(bp[((size_t)start + tid) * p.Hv + h]) : 0.f;
         asm volatile("cp.async.wait_group 0;" ::: "memory");
+        if (tid == 0) tc::bulk_wait_read();  // the previous item's W image (over A, P and the pivot rows)
         __syncthreads();
 
         // ---- per-channel cumsum in place, log2 units: thread (channel c, half hf) scans
@@ -1284,6 +1288,7 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
             *reinterpret_cast<uint4*>(sm + S::kT2l + off) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
         }
         asm volatile("cp.async.wait_group 0;" ::: "memory");
+        if (tid == 0) tc::bulk_wait_read();  // the P image, whose tile the W image staging reuses
         tc::fence_proxy_async();
         __syncthreads();
 
@@ -1314,14 +1319,17 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
         phW ^= 1u;
         tc::fence_after();
         // ---- W, U out of TMEM (row i = 16 q + lane, lane < 16; warp: two 32-column
-        //      blocks of W and of U), staged as blob images (W hi / lo over X, U over
-        //      the work region) and written with bulk copies ----------------------------
+        //      blocks of W and of U), staged as blob images (W hi over A, W lo over P
+        //      and the pivot rows, U over the work region) and written with bulk
+        //      copies: U's first, then W's.  The next item waits for U's to have read
+        //      the work region before its gate rows land there, and for W's before
+        //      its cumsum; its K and Q rows go into X at once. -----------------------
         {
             const int q = warp & 3, hf = warp >> 2;
             const int i = 16 * q + (lane & 15);
             const uint32_t lrow = tmem + ((uint32_t)(32 * q) << 16);
-            unsigned char* sWh = sm + S::kX;
-            unsigned char* sWl = sm + S::kX + kTile64x128;
+            unsigned char* sWh = sm + S::kA;
+            unsigned char* sWl = sm + S::kP;
             float* sU = reinterpret_cast<float*>(sm + S::kOps);
             for (int q2 = 0; q2 < 2; ++q2) {
                 const int cb = 2 * hf + q2;
@@ -1349,13 +1357,13 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
                 unsigned char* Xd = p.Xw + ((size_t)chunk * p.Hv + h) * kXwBytes;
                 unsigned char* Yd = p.Yw + ((size_t)chunk * p.Hv + h) * kYwBytes;
                 const uint32_t half = kTile64x128 / 2;
+                tc::bulk_s2g(p.Ub + ((size_t)chunk * p.Hv + h) * NVB * kUBlock, tc::smem_u32(sU), NVB * kUBlock);
+                tc::bulk_commit();
                 tc::bulk_s2g(Xd, tc::smem_u32(sWh), half);
                 tc::bulk_s2g(Xd + 2 * half, tc::smem_u32(sWh) + half, half);
                 tc::bulk_s2g(Yd, tc::smem_u32(sWl), half);
                 tc::bulk_s2g(Yd + 2 * half, tc::smem_u32(sWl) + half, half);
-                tc::bulk_s2g(p.Ub + ((size_t)chunk * p.Hv + h) * NVB * kUBlock, tc::smem_u32(sU), NVB * kUBlock);
                 tc::bulk_commit();
-                tc::bulk_wait_read();  // the staging areas (and P) are reused by the next item
             }
         }
         tc::fence_before();
