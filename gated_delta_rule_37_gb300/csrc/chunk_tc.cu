@@ -346,8 +346,13 @@ struct PrepSmem {
     static constexpr uint32_t kBeta = kGam + C * 4;
     static constexpr uint32_t kBar = kBeta + C * 4;
     static constexpr uint32_t kMeta = kBar + 64;          // LocalMeta
-    static constexpr uint32_t kTotal = kMeta + sizeof(LocalMeta) + 1024;  // + alignment slack
+    // W lo image staging (W hi is staged over Tm), so that the next item's K, Q
+    // rows need not wait for the bulk copies of this item's images
+    static constexpr uint32_t kWl = (kMeta + sizeof(LocalMeta) + 1023) & ~1023u;
+    static constexpr uint32_t kTotal = kWl + kTile64x128 + 1024;  // + alignment slack
     static_assert(kT2l + kTile64x64 <= kTm, "T'' tiles overlap Tm");
+    static_assert(kTile64x128 <= C * LDA * 4 && kTm % 1024 == 0, "W hi image over Tm");
+    static_assert(kTotal <= 113 * 1024, "two CTAs per SM");
 };
 
 // Every kernel here takes the channel count of K and V in global memory as
@@ -413,6 +418,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
                              kDk / 8, tid);
         stage_rows_async<NT>(sm + S::kX, 2 * C, C, qp + ((size_t)start * p.Hk + kh) * kDk, (size_t)p.Hk * kDk, L,
                              kDk / 8, tid);
+        // the previous item's U image (over V and A; bulk group before its W image)
+        if (tid == 0) tc::bulk_wait_read_1();
+        __syncthreads();
         stage_rows_async<NT>(sm + S::kV, C, 0, vp + ((size_t)start * p.Hv + h) * kDk, (size_t)p.Hv * kDk, L,
                              kDk / 8, tid);
         asm volatile("cp.async.commit_group;" ::: "memory");
@@ -538,6 +546,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
                         make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
             }
         }
+        if (tid == 0) tc::bulk_wait_read();  // the previous item's W images (over Tm and kWl)
         tc::fence_before();
         __syncthreads();
 
@@ -591,16 +600,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
         // ---- W, U out of TMEM into their blobs: row i = 16 q + lane (lane < 16);
         //      warp: columns [64 hf, 64 hf + 64) of W and of U.  The images are staged in
         //      shared memory left dead by the finished MMAs (W hi / lo as 64-row k128
-        //      tiles over X, U value-major over V and A) and written with bulk copies,
-        //      so every global write is a contiguous run. ---------------------------------
+        //      tiles over Tm and in their own region, U value-major over V and A) and
+        //      written with bulk copies, so every global write is a contiguous run: U's
+        //      first, then W's.  The next item stages its K and Q rows at once, waits
+        //      for U's copy before its V rows and for W's before its solve. ------------
         if (!tc::mbar_wait(barWU, phWU, abort_flag)) { *abort_flag = 1; raise_error(p, 1u); }
         phWU ^= 1u;
         tc::fence_after();
         {
             const int i = 16 * q + (lane & 15);
             const uint32_t lrow = tmem + ((uint32_t)(32 * q) << 16);
-            unsigned char* sWh = sm + S::kX;            // [64][128] k128, column-block stride 8 KB
-            unsigned char* sWl = sm + S::kX + kTile64x128;
+            unsigned char* sWh = sm + S::kTm;           // [64][128] k128, column-block stride 8 KB
+            unsigned char* sWl = sm + S::kWl;
             float* sU = reinterpret_cast<float*>(sm + S::kV);  // 4 x [32 v][64 i]
             constexpr int kBlocks = 2;  // 32-column blocks of W and of U per warp
             for (int q2 = 0; q2 < kBlocks; ++q2) {
@@ -631,13 +642,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
                 unsigned char* Xd = p.Xw + ((size_t)chunk * p.Hv + h) * kXwBytes;  // rows 0..63 of each column block
                 unsigned char* Yd = p.Yw + ((size_t)chunk * p.Hv + h) * kYwBytes;
                 const uint32_t half = kTile64x128 / 2;  // one 64-row column block
+                tc::bulk_s2g(p.Ub + ((size_t)chunk * p.Hv + h) * NVB * kUBlock, tc::smem_u32(sU), NVB * kUBlock);
+                tc::bulk_commit();
                 tc::bulk_s2g(Xd, tc::smem_u32(sWh), half);
                 tc::bulk_s2g(Xd + 2 * half, tc::smem_u32(sWh) + half, half);
                 tc::bulk_s2g(Yd, tc::smem_u32(sWl), half);
                 tc::bulk_s2g(Yd + 2 * half, tc::smem_u32(sWl) + half, half);
-                tc::bulk_s2g(p.Ub + ((size_t)chunk * p.Hv + h) * NVB * kUBlock, tc::smem_u32(sU), NVB * kUBlock);
                 tc::bulk_commit();
-                tc::bulk_wait_read();  // the staging area is reused by the next item
             }
         }
         tc::fence_before();
