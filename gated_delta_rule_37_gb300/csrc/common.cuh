@@ -31,6 +31,10 @@ template <> struct Vec<float, 4> {
     static __device__ __forceinline__ void store(float* p, const float* in) {
         *reinterpret_cast<float4*>(p) = make_float4(in[0], in[1], in[2], in[3]);
     }
+    // streaming store (evict-first): data this kernel never reads back
+    static __device__ __forceinline__ void store_cs(float* p, const float* in) {
+        __stcs(reinterpret_cast<float4*>(p), make_float4(in[0], in[1], in[2], in[3]));
+    }
 };
 template <> struct Vec<float, 2> {
     static __device__ __forceinline__ void load(const float* p, float* out) {
@@ -39,6 +43,9 @@ template <> struct Vec<float, 2> {
     }
     static __device__ __forceinline__ void store(float* p, const float* in) {
         *reinterpret_cast<float2*>(p) = make_float2(in[0], in[1]);
+    }
+    static __device__ __forceinline__ void store_cs(float* p, const float* in) {
+        __stcs(reinterpret_cast<float2*>(p), make_float2(in[0], in[1]));
     }
 };
 template <> struct Vec<__nv_bfloat16, 4> {
@@ -56,6 +63,15 @@ template <> struct Vec<__nv_bfloat16, 4> {
         t.x = *reinterpret_cast<uint32_t*>(&a);
         t.y = *reinterpret_cast<uint32_t*>(&b);
         *reinterpret_cast<uint2*>(p) = t;
+    }
+    // streaming store (evict-first): data this kernel never reads back
+    static __device__ __forceinline__ void store_cs(__nv_bfloat16* p, const float* in) {
+        __nv_bfloat162 a = __floats2bfloat162_rn(in[0], in[1]);
+        __nv_bfloat162 b = __floats2bfloat162_rn(in[2], in[3]);
+        uint2 t;
+        t.x = *reinterpret_cast<uint32_t*>(&a);
+        t.y = *reinterpret_cast<uint32_t*>(&b);
+        __stcs(reinterpret_cast<uint2*>(p), t);
     }
 };
 template <> struct Vec<__nv_bfloat16, 8> {
@@ -77,6 +93,10 @@ template <> struct Vec<__nv_bfloat16, 2> {
     }
     static __device__ __forceinline__ void store(__nv_bfloat16* p, const float* in) {
         *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(in[0], in[1]);
+    }
+    static __device__ __forceinline__ void store_cs(__nv_bfloat16* p, const float* in) {
+        __nv_bfloat162 a = __floats2bfloat162_rn(in[0], in[1]);
+        __stcs(reinterpret_cast<unsigned int*>(p), *reinterpret_cast<unsigned int*>(&a));
     }
 };
 

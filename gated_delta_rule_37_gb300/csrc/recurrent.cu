@@ -352,7 +352,7 @@ recurrent_kernel(RecParams p) {
             for (int r = 0; r < kRowsPerWarp; ++r) {
                 float t2[KPT];
                 row(r, t2);
-                Vec<PoolT, KPT>::store(irow + (size_t)r * K, t2);
+                Vec<PoolT, KPT>::store_cs(irow + (size_t)r * K, t2);  // never read back here
             }
         }
     };
