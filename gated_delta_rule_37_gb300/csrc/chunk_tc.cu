@@ -24,9 +24,11 @@
 //  chain (one CTA per value-head x 32-column block of V x sequence, serial
 //        over the sequence's chunks; attention-gym PR #344's inter-chunk state
 //        recurrence with the output fused in):
-//          N  = U - W S0^T            M=64, 3-term split (W hi/lo x S hi/lo)
-//          O  = Qd S0^T + P N         M=64 (output, 2 + 1 MMA groups)
-//          S  = e^{gam_L} S0 + K^T (f o N)     M=128, 2-term split
+//          N  = U - W S0^T            3-term split (W hi/lo x S hi/lo)
+//          O  = Qd S0^T + P N         (output)
+//          S  = e^{gam_L} S0 + K^T (f o N)     2-term split
+//        All M = 128: W_hi and Qd are stacked into one A operand (so is W_lo
+//        with P), so the product that forms N forms the output's Qd S0^T too.
 //        Warp roles (512 threads): warp 0 stages chunk blobs with
 //        cp.async.bulk into a two-deep ring; warp 2 owns the TMEM allocation;
 //        warps 4-11 hold the fp32 state S^T (row k in TMEM lane k, 16 of the 32
