@@ -1417,7 +1417,7 @@ struct ChainSmem {
 
 enum ChainBar {
     kFull0 = 0, kFull1, kEmpty0, kEmpty1, kSReady, kD1Full, kNReady, kD2Full, kOFull0, kOFull1, kOFree0, kOFree1,
-    kDrainA, kDrainB, kDrainC, kSPub0, kSPub1, kNumBars
+    kDrainA, kDrainB, kDrainC, kSPub0, kSPub1, kNPub0, kNPub1, kNumBars
 };
 // Arrival counts: the N accumulator is committed by issuers A and B, a stage is
 // released by all three issuers, everything else by one arrival.
@@ -1675,6 +1675,7 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             tc::fence_proxy_async();
             tc::fence_before();
             tc::bar_sync(1, 256);
+            if (kKDA && tid == 128) tc::mbar_arrive(bar(kNPub0 + s));  // N published: the output warps may drain chunk c - 1
             if (isA) {
                 tc::fence_after();
                 tc::mma_ksteps<4>(tD2, dmn128(st + S::kKt), amn, dmn64(base + S::kNh, C * BV * 2), 64, id2w, true);
@@ -1733,13 +1734,16 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
         for (int c = 0; c < nc; ++c) {
             const int ob = c & 1;
             if (!tc::mbar_wait(bar(kOFull0 + ob), (c >> 1) & 1, abort_flag)) fail();
-            // scalar gate: drain while the next chunk's N product runs (the state
-            // warps then wait for it) rather than beside their state update and S
-            // store (varlen prefill chain 90 -> 87 us; with per-channel gates it
-            // measured slower, 0.847 -> 0.881 ms, and drains at once).  Two barriers
-            // by chunk parity: the state group cannot publish chunk c + 3 before
-            // this chunk is drained (its N product waits for kOFree).
+            // Drain when the state warps idle rather than beside their state update
+            // and S store: with a scalar gate once the next chunk's S is published
+            // (the N product runs; varlen prefill chain 90 -> 87 us), with
+            // per-channel gates once its N is published (the update product runs;
+            // 0.846 -> 0.838 ms; the N-product window measured slower there).  Two
+            // barriers by chunk parity: the state group cannot publish chunk c + 3
+            // before this chunk is drained (its N product waits for kOFree).
             if (!kKDA && c + 1 < nc && !tc::mbar_wait(bar(kSPub0 + ((c + 1) & 1)), ((c + 1) >> 1) & 1, abort_flag))
+                fail();
+            if (kKDA && c + 1 < nc && !tc::mbar_wait(bar(kNPub0 + ((c + 1) & 1)), ((c + 1) >> 1) & 1, abort_flag))
                 fail();
             tc::fence_after();
             if (drain && outputs) {
