@@ -154,6 +154,21 @@ def test_gate_zero_and_beta_endpoints():
     check_state(sf.cpu(), rs, "final state")
 
 
+def test_channel_gate_zero_and_beta_endpoints():
+    """Per-channel gates with no decay at all: tokens on which no channel
+    decays (chunks of decay span 0) and channels that never decay, with beta
+    at 0 and at 1, GVA 2 and an initial state."""
+    case = workloads.chunk_case(65, [70, 64, 130], 1, 2, 128, 128, gate="gk", g_range=(-0.5, 0.0), h0_std=0.1)
+    case.gk[:40] = 0.0
+    case.gk[:, :, :16] = 0.0
+    case.beta[:20] = 0.0
+    case.beta[20:60] = 1.0
+    o, sf = run_gpu(case)
+    ro, rs = oracle_ref(case)
+    check_out(o.cpu(), ro, "o")
+    check_state(sf.cpu(), rs, "final state")
+
+
 def test_qk_l2norm_flag():
     case = workloads.chunk_case(63, [90, 40], 2, 4, 128, 128, dtype=torch.float32, h0_std=0.1)
     gen = torch.Generator().manual_seed(3)
