@@ -1600,7 +1600,7 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             for (int cc = 0; cc < 2; ++cc) {
                 uint32_t hw[4], lw[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) tc::split2(Sreg[8 * cc + 2 * u], Sreg[8 * cc + 2 * u + 1], hw[u], lw[u]);
+                for (int u = 0; u < 4; ++u) split2x(make_float2(Sreg[8 * cc + 2 * u], Sreg[8 * cc + 2 * u + 1]), hw[u], lw[u]);
                 const uint32_t off = tc::chunk_mn64(t, 2 * hf + cc);
                 *reinterpret_cast<uint4*>(sSh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                 *reinterpret_cast<uint4*>(sSl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
@@ -1644,7 +1644,12 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                 tc::tmem_ld16x3(tD1 + 64 * ob + lane_base + vh, tD1 + 64 * ob + lane_base + BV + vh,
                                 tD1b + lane_base + vh, dv);
 #pragma unroll
-                for (int v = 0; v < 16; ++v) ws[v] = dv[v] + dv[16 + v] + dv[32 + v];
+                for (int v = 0; v < 16; v += 2) {  // on the fp32x2 pipe
+                    const float2 w2 = __fadd2_rn(__fadd2_rn(make_float2(dv[v], dv[v + 1]), make_float2(dv[16 + v], dv[17 + v])),
+                                                 make_float2(dv[32 + v], dv[33 + v]));
+                    ws[v] = w2.x;
+                    ws[v + 1] = w2.y;
+                }
             }
             // the N tile was last read by the output product of chunk c - kNBuf
             if (S::kNBuf == 2) {
@@ -1661,9 +1666,10 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int v = 8 * cc + 2 * u;
-                        const float n0 = (uv[v] - ws[v]) * keep;
-                        const float n1 = (uv[v + 1] - ws[v + 1]) * keep;
-                        tc::split2(n0 * rowf, n1 * rowf, hw[u], lw[u]);
+                        const float2 nn = __fmul2_rn(sub2(make_float2(uv[v], uv[v + 1]), make_float2(ws[v], ws[v + 1])),
+                                                     make_float2(keep, keep));
+                        const float n0 = nn.x, n1 = nn.y;
+                        split2x(__fmul2_rn(make_float2(n0, n1), make_float2(rowf, rowf)), hw[u], lw[u]);
                         nw[u] = tc::pack_bf16(n0, n1);
                     }
                     const uint32_t off = tc::chunk_mn64(i, 2 * hf + cc);
@@ -1700,10 +1706,15 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             if (!tc::mbar_wait(bar(kD2Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
             tc::fence_after();
             {
-                float dv[48];
-                tc::tmem_ld16x3(tD2 + lane_base + vh, tD2 + lane_base + BV + vh, tD2 + lane_base + vh, dv);
+                float dv[32];
+                tc::tmem_ld16x2(tD2 + lane_base + vh, tD2 + lane_base + BV + vh, dv);
 #pragma unroll
-                for (int v = 0; v < 16; ++v) Sreg[v] = fmaf(colf, Sreg[v], dv[v] + dv[16 + v]);
+                for (int v = 0; v < 16; v += 2) {  // on the fp32x2 pipe
+                    const float2 s2 = __ffma2_rn(make_float2(colf, colf), make_float2(Sreg[v], Sreg[v + 1]),
+                                                 __fadd2_rn(make_float2(dv[v], dv[v + 1]), make_float2(dv[16 + v], dv[17 + v])));
+                    Sreg[v] = s2.x;
+                    Sreg[v + 1] = s2.y;
+                }
             }
             tc::fence_before();
         }

@@ -271,6 +271,25 @@ __device__ __forceinline__ void tmem_ld16x3(uint32_t a0, uint32_t a1, uint32_t a
     for (int j = 0; j < 48; ++j) v[j] = __uint_as_float(r[j]);
 }
 
+// 16 consecutive fp32 columns of this thread's lane from each of two
+// addresses, one wait.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t a0, uint32_t a1, float* v) {
+    uint32_t r[32];
+#define GDR_LD16(base, addr)                                                                                \
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];" \
+                 : "=r"(r[base + 0]), "=r"(r[base + 1]), "=r"(r[base + 2]), "=r"(r[base + 3]), "=r"(r[base + 4]), \
+                   "=r"(r[base + 5]), "=r"(r[base + 6]), "=r"(r[base + 7]), "=r"(r[base + 8]), "=r"(r[base + 9]), \
+                   "=r"(r[base + 10]), "=r"(r[base + 11]), "=r"(r[base + 12]), "=r"(r[base + 13]),              \
+                   "=r"(r[base + 14]), "=r"(r[base + 15])                                                       \
+                 : "r"(addr))
+    GDR_LD16(0, a0);
+    GDR_LD16(16, a1);
+#undef GDR_LD16
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+}
+
 // ---- bf16 packing -------------------------------------------------------------
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 t = __floats2bfloat162_rn(a, b);
