@@ -64,7 +64,7 @@ constexpr int LDA = C + 1;  // padded fp32 row stride for the 64 x 64 solve
 constexpr uint32_t kTile64x128 = C * D * 2;       // 16 KB bf16 [64][128]
 constexpr uint32_t kTile64x64 = C * C * 2;        // 8 KB bf16 [64][64]
 constexpr uint32_t kUBlock = C * BV * 4;          // 8 KB fp32 [64][32]
-constexpr uint32_t kRec = 1024;                   // rowf[64], colf[128], L
+constexpr uint32_t kRec = 1024;                   // rowf[64], colf[128]
 constexpr uint32_t kXwBytes = 2 * kTile64x128;    // 32 KB stacked [W_hi ; Qd]
 constexpr uint32_t kYwBytes = 3 * C * 128;        // 24 KB stacked [W_lo ; P] without its last 8 KB
 
@@ -499,7 +499,6 @@ __global__ void __launch_bounds__(kPrepThreads, 2) chunk_prep_kernel(TcParams p)
             float* rec = reinterpret_cast<float*>(p.Rb + ((size_t)chunk * p.Hv + h) * kRec);
             if (tid < C) rec[tid] = tid < L ? __expf(gl[0] - gam[tid]) : 0.f;
             if (tid < D) rec[64 + tid] = __expf(gl[0]);
-            if (tid == 0) reinterpret_cast<int*>(rec)[192] = L;
         }
 
         // ---- A (strictly lower) and P (lower incl. diagonal) -------------------------
@@ -932,7 +931,6 @@ __global__ void __launch_bounds__(kKdaThreads, 2) chunk_prep_kda_kernel(TcParams
             float* rec = reinterpret_cast<float*>(p.Rb + ((size_t)chunk * p.Hv + h) * kRec);
             if (tid < C) rec[tid] = tid < L ? 1.f : 0.f;
             if (tid < D) rec[64 + tid] = ex2(gL[tid]);
-            if (tid == 0) reinterpret_cast<int*>(rec)[192] = L;
         }
 
         // ---- A and P across the halves of 2h-token blocks (h = 32, 16, 8, 4) on tcgen05 ----
@@ -1628,14 +1626,15 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             const float* rec = reinterpret_cast<const float*>(stg + S::kRec_);
             const float colf = rec[64 + t];
             const float rowf = nrow ? rec[i] : 0.f;
-            const int Lc = reinterpret_cast<const int*>(rec)[192];
             float uv[16];
             if (nrow) {
                 const float* ucol = reinterpret_cast<const float*>(stg + S::kU) + (size_t)vh * C + i;
 #pragma unroll
                 for (int v = 0; v < 16; ++v) uv[v] = transition ? 0.f : ucol[(size_t)v * C];  // transition: U = 0
             }
-            // N = U - W S^T  ->  N' = rowf * N (hi, lo), N (bf16, masked)
+            // N = U - W S^T  ->  N' = rowf * N (hi, lo), N (bf16).  Rows past the chunk
+            // end come out exactly zero: the prep's U and W rows there are zero (beta
+            // is zero there, so are those rows of (I + A)^{-1} diag(beta)).
             if (!tc::mbar_wait(bar(kD1Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
             tc::fence_after();
             float ws[16];  // (W S^T) for this thread's row and 16 columns
@@ -1659,15 +1658,13 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             }
             const uint32_t nbuf = (uint32_t)(ob % S::kNBuf) * (C * BV * 2);
             if (nrow) {
-                const float keep = i < Lc ? 1.f : 0.f;  // rows past the chunk end
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     uint32_t hw[4], lw[4], nw[4];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int v = 8 * cc + 2 * u;
-                        const float2 nn = __fmul2_rn(sub2(make_float2(uv[v], uv[v + 1]), make_float2(ws[v], ws[v + 1])),
-                                                     make_float2(keep, keep));
+                        const float2 nn = sub2(make_float2(uv[v], uv[v + 1]), make_float2(ws[v], ws[v + 1]));
                         const float n0 = nn.x, n1 = nn.y;
                         split2x(__fmul2_rn(make_float2(n0, n1), make_float2(rowf, rowf)), hw[u], lw[u]);
                         nw[u] = tc::pack_bf16(n0, n1);
