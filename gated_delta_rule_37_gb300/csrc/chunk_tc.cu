@@ -1587,11 +1587,12 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
         unsigned char* sSh = sm + S::kSh;
         unsigned char* sSl = sm + S::kSl;
         bool issued = false;
+        bool staged = false;  // this chunk's stage was seen landed during the last update product
         for (int c = 0; c < nc; ++c) {
             const int s = c & 1, ob = c & 1;
             const unsigned char* stg = sm + s * S::kStage;
             const uint32_t st = base + s * S::kStage;
-            if (!tc::mbar_wait(bar(kFull0 + s), (c >> 1) & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
+            if (!staged && !tc::mbar_wait(bar(kFull0 + s), (c >> 1) & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
             // S^T rows (hi, lo) into the MMA operand tiles.  Their readers (the N
             // products of chunk c - 1) finished before the last state update.
 #pragma unroll
@@ -1632,6 +1633,13 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
 #pragma unroll
                 for (int v = 0; v < 16; ++v) uv[v] = transition ? 0.f : ucol[(size_t)v * C];  // transition: U = 0
             }
+            // the N tile was last read by the output product of chunk c - kNBuf (waited
+            // for here, while the N product runs)
+            if (S::kNBuf == 2) {
+                if (c >= 2 && !tc::mbar_wait(bar(kOFull0 + ob), ((c - 2) >> 1) & 1, abort_flag)) fail();
+            } else {
+                if (c >= 1 && !tc::mbar_wait(bar(kOFull0 + ((c - 1) & 1)), ((c - 1) >> 1) & 1, abort_flag)) fail();
+            }
             // N = U - W S^T  ->  N' = rowf * N (hi, lo), N (bf16).  Rows past the chunk
             // end come out exactly zero: the prep's U and W rows there are zero (beta
             // is zero there, so are those rows of (I + A)^{-1} diag(beta)).
@@ -1649,12 +1657,6 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                     ws[v] = w2.x;
                     ws[v + 1] = w2.y;
                 }
-            }
-            // the N tile was last read by the output product of chunk c - kNBuf
-            if (S::kNBuf == 2) {
-                if (c >= 2 && !tc::mbar_wait(bar(kOFull0 + ob), ((c - 2) >> 1) & 1, abort_flag)) fail();
-            } else {
-                if (c >= 1 && !tc::mbar_wait(bar(kOFull0 + ((c - 1) & 1)), ((c - 1) >> 1) & 1, abort_flag)) fail();
             }
             const uint32_t nbuf = (uint32_t)(ob % S::kNBuf) * (C * BV * 2);
             if (nrow) {
@@ -1699,6 +1701,8 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                     issued = true;
                 }
             }
+            // while the update product runs: has the next chunk's stage landed?
+            staged = c + 1 < nc && tc::mbar_test(bar(kFull0 + (s ^ 1)), ((c + 1) >> 1) & 1);
             // S^T <- colf * S^T + dS^T  (hi and lo halves of the accumulator summed)
             if (!tc::mbar_wait(bar(kD2Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
             tc::fence_after();
