@@ -1588,6 +1588,7 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
         unsigned char* sSl = sm + S::kSl;
         bool issued = false;
         bool staged = false;  // this chunk's stage was seen landed during the last update product
+        bool drained = false;  // (issuer A) this chunk's output buffer was seen drained then too
         for (int c = 0; c < nc; ++c) {
             const int s = c & 1, ob = c & 1;
             const unsigned char* stg = sm + s * S::kStage;
@@ -1610,7 +1611,7 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
             if (!kKDA && tid == 128) tc::mbar_arrive(bar(kSPub0 + s));  // S published: the output warps may drain chunk c - 1
             if (isA) {
                 // the output rows of D1[ob] were drained (chunk c - 2) before reuse
-                if (c >= 2 && !tc::mbar_wait(bar(kOFree0 + ob), ((c >> 1) - 1) & 1, abort_flag)) fail();
+                if (c >= 2 && !drained && !tc::mbar_wait(bar(kOFree0 + ob), ((c >> 1) - 1) & 1, abort_flag)) fail();
                 tc::fence_after();
                 tc::mma_ksteps<8>(tD1 + 64 * ob, dk128(st + S::kXW), a128, dmn64(base + S::kSh, D * BV * 2), 64, idA, true);
                 tc::mma_commit(bar(kD1Full));
@@ -1701,8 +1702,10 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                     issued = true;
                 }
             }
-            // while the update product runs: has the next chunk's stage landed?
+            // while the update product runs: has the next chunk's stage landed (and,
+            // for issuer A, its output buffer been drained)?
             staged = c + 1 < nc && tc::mbar_test(bar(kFull0 + (s ^ 1)), ((c + 1) >> 1) & 1);
+            drained = isA && c >= 1 && c + 1 < nc && tc::mbar_test(bar(kOFree0 + (ob ^ 1)), (((c + 1) >> 1) - 1) & 1);
             // S^T <- colf * S^T + dS^T  (hi and lo halves of the accumulator summed)
             if (!tc::mbar_wait(bar(kD2Full), c & 1, abort_flag)) fail();  // keep going: every named barrier is reached by all threads
             tc::fence_after();
