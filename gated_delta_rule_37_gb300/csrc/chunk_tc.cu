@@ -1720,7 +1720,8 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                     Sreg[v + 1] = s2.y;
                 }
             }
-            tc::fence_before();
+            // (the next thread synchronisation, the barrier that publishes S, is
+            // preceded by its own tcgen05 fence)
         }
         if (issued) {  // every MMA this thread issued finished before the CTA leaves
             const int dr = isA ? kDrainA : isB ? kDrainB : kDrainC;
