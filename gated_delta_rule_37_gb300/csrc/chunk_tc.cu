@@ -1414,9 +1414,14 @@ struct ChainSmem {
 };
 
 enum ChainBar {
-    kFull0 = 0, kFull1, kEmpty0, kEmpty1, kSReady, kD1Full, kNReady, kD2Full, kOFull0, kOFull1, kOFree0, kOFree1,
+    kFull0 = 0, kFull1, kEmpty0, kEmpty1, kD1Full, kD2Full, kOFull0, kOFull1, kOFree0, kOFree1,
     kDrainA, kDrainB, kDrainC, kSPub0, kSPub1, kNPub0, kNPub1, kNumBars
 };
+// pairs indexed by chunk (or stage) parity: the second of each is the first + 1
+static_assert(kFull1 == kFull0 + 1 && kEmpty1 == kEmpty0 + 1 && kOFull1 == kOFull0 + 1 && kOFree1 == kOFree0 + 1 &&
+                  kSPub1 == kSPub0 + 1 && kNPub1 == kNPub0 + 1,
+              "barrier pairs indexed by parity must be adjacent");
+static_assert(8 * kNumBars + 16 <= 256, "barriers, TMEM slot and abort flag fit the 256-byte barrier area");
 // Arrival counts: the N accumulator is committed by issuers A and B, a stage is
 // released by all three issuers, everything else by one arrival.
 __device__ __forceinline__ uint32_t chain_bar_count(int i) {
