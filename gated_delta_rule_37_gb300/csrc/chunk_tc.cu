@@ -1404,9 +1404,9 @@ struct ChainSmem {
     static constexpr uint32_t kSl = kSh + D * BV * 2;        // S^T lo (the next atom: [S_hi | S_lo])
     static constexpr uint32_t kNh = kSl + D * BV * 2;        // N' hi [64][32] mn64
     static constexpr uint32_t kNl = kNh + C * BV * 2;        // N' lo
-    // N (bf16) for the output: two buffers by chunk parity (one with per-channel
-    // gates, whose stages carry the second K tile and leave no room)
-    static constexpr int kNBuf = kKDA ? 1 : 2;
+    // N (bf16) for the output: two buffers by chunk parity with a scalar gate;
+    // with per-channel gates the row factor is 1, so the output reads N'_hi
+    static constexpr int kNBuf = kKDA ? 0 : 2;
     static constexpr uint32_t kN = kNl + C * BV * 2;
     static constexpr uint32_t kBar = kN + kNBuf * C * BV * 2;
     static constexpr uint32_t kTotal = kBar + 256 + 1024;
@@ -1639,8 +1639,9 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
 #pragma unroll
                 for (int v = 0; v < 16; ++v) uv[v] = transition ? 0.f : ucol[(size_t)v * C];  // transition: U = 0
             }
-            // the N tile was last read by the output product of chunk c - kNBuf (waited
-            // for here, while the N product runs)
+            // the output's N tile was last read by the output product of chunk c - 2
+            // (scalar gate) or c - 1 (per-channel gates: N'_hi) (waited for here, while
+            // the N product runs)
             if (S::kNBuf == 2) {
                 if (c >= 2 && !tc::mbar_wait(bar(kOFull0 + ob), ((c - 2) >> 1) & 1, abort_flag)) fail();
             } else {
@@ -1664,7 +1665,7 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                     ws[v + 1] = w2.y;
                 }
             }
-            const uint32_t nbuf = (uint32_t)(ob % S::kNBuf) * (C * BV * 2);
+            const uint32_t nbuf = (uint32_t)ob * (C * BV * 2);  // scalar gate: the output's N buffer
             if (nrow) {
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
@@ -1673,14 +1674,19 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                     for (int u = 0; u < 4; ++u) {
                         const int v = 8 * cc + 2 * u;
                         const float2 nn = sub2(make_float2(uv[v], uv[v + 1]), make_float2(ws[v], ws[v + 1]));
-                        const float n0 = nn.x, n1 = nn.y;
-                        split2x(__fmul2_rn(make_float2(n0, n1), make_float2(rowf, rowf)), hw[u], lw[u]);
-                        nw[u] = tc::pack_bf16(n0, n1);
+                        if (kKDA) {
+                            // the row factor is 1 on the chunk's rows (and the rows past
+                            // its end are zero), so N' = N and N'_hi is the output's N
+                            split2x(nn, hw[u], lw[u]);
+                        } else {
+                            split2x(__fmul2_rn(nn, make_float2(rowf, rowf)), hw[u], lw[u]);
+                            nw[u] = tc::pack_bf16(nn.x, nn.y);
+                        }
                     }
                     const uint32_t off = tc::chunk_mn64(i, 2 * hf + cc);
                     *reinterpret_cast<uint4*>(sm + S::kNh + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
                     *reinterpret_cast<uint4*>(sm + S::kNl + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                    *reinterpret_cast<uint4*>(sm + S::kN + nbuf + off) = make_uint4(nw[0], nw[1], nw[2], nw[3]);
+                    if (!kKDA) *reinterpret_cast<uint4*>(sm + S::kN + nbuf + off) = make_uint4(nw[0], nw[1], nw[2], nw[3]);
                 }
             }
             tc::fence_proxy_async();
@@ -1700,8 +1706,8 @@ __global__ void __launch_bounds__(512, 1) chunk_chain_kernel(TcParams p) {
                     tc::mbar_arrive(bar(kEmpty0 + s));
                 } else {
                     tc::fence_after();
-                    tc::mma_ksteps<4>(tD1 + 64 * ob, dk128(st + S::kYW), a64, dmn64(base + S::kN + nbuf, 512), 64,
-                                      idB, false);
+                    tc::mma_ksteps<4>(tD1 + 64 * ob, dk128(st + S::kYW), a64,
+                                      dmn64(base + (kKDA ? S::kNh : S::kN + nbuf), 512), 64, idB, false);
                     tc::mma_commit(bar(kOFull0 + ob));
                     tc::mma_commit(bar(kEmpty0 + s));
                     issued = true;
